@@ -1,0 +1,318 @@
+"""fp64 CPU oracle of the Ulysses attention path.
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, ``__graft_entry__.smoke()`` and
+the CPU-baseline / reference leg of ``bench.py`` may import this package.  The
+CUDA library and its Python binding never import it, and it imports nothing
+from them.
+
+The arithmetic lives in ``ulysses_oracle.c`` (plain loops, double precision);
+this module only builds that file with gcc, marshals numpy buffers and strings
+the steps together in the order the pages give them:
+
+  [SP2] "Sequence Parallelism II: DeepSpeed Ulysses and All-to-All Attention",
+        §2 "Forward Pass in Slow Motion" (split by sequence, project, All-to-All
+        Q/K/V, local attention, All-to-All the output back) and §6 "Backward
+        Pass Intuition" (the same layout changes, reversed);
+  [CMP] "Comparing Ulysses and Megatron Sequence Parallelism", "A simple
+        attention skeleton" (rope before the transpose) and "DeepSpeed
+        Attention" (per-rank shapes [B,S/P,heads,D] <-> [B,S,heads/P,D]).
+
+Every virtual rank holds its own numpy array; the All-to-All is the C double
+loop over (destination, source) that also counts the bytes crossing ranks.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import math
+import os
+import subprocess
+from typing import List, Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ulysses_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (portable flags: the file must give the
+    same results on x86-64 and aarch64, so no -march and no FMA contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+                               "-shared", "-pthread", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+class _Shape(ctypes.Structure):
+    _fields_ = [("P", ctypes.c_int), ("B", ctypes.c_int), ("S", ctypes.c_int),
+                ("n_head", ctypes.c_int), ("n_kv_head", ctypes.c_int), ("D", ctypes.c_int),
+                ("causal", ctypes.c_int), ("scale", ctypes.c_double)]
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _lib = load_library(build())
+    return _lib
+
+
+def load_library(path: str):
+    """Load a compiled oracle (the tests also load deliberately broken
+    builds of the same source, to check that the pins catch them)."""
+    L = ctypes.CDLL(path)
+    pp = ctypes.POINTER(ctypes.c_void_p)
+    ll = ctypes.POINTER(ctypes.c_longlong)
+    L.oracle_a2a_seq_to_head.argtypes = [ctypes.c_int] * 6 + [pp, pp, ll, ll, ctypes.c_int, ctypes.c_int]
+    L.oracle_a2a_head_to_seq.argtypes = [ctypes.c_int] * 6 + [pp, pp, ll, ll, ctypes.c_int, ctypes.c_int]
+    L.oracle_rope_seq.argtypes = [ctypes.c_int] * 5 + [ctypes.c_double, ctypes.c_int, pp]
+    L.oracle_rope_seq.restype = None
+    ip = ctypes.POINTER(ctypes.c_int)
+    L.oracle_attention_fwd.argtypes = [ctypes.POINTER(_Shape), pp, pp, pp, pp, pp, ip,
+                                       ctypes.c_long, ctypes.c_int]
+    L.oracle_attention_unsharded.argtypes = [ctypes.POINTER(_Shape)] + [ctypes.c_void_p] * 5 + [ctypes.c_int]
+    L.oracle_attention_bwd_group.argtypes = [ctypes.POINTER(_Shape), ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, pp, pp, pp, pp, pp, pp, pp, ip,
+                                             ctypes.c_long, ip, ctypes.c_long, ctypes.c_int]
+    return L
+
+
+@dataclasses.dataclass
+class Problem:
+    """The pages' problem statement ([CMP] skeleton and "Megatron Attention
+    costs" constants): batch B, sequence S, n_head, n_kv_head, head_dim D,
+    group size P; plus the causal flag and the rope base."""
+    B: int
+    S: int
+    n_head: int
+    n_kv_head: int
+    D: int
+    P: int
+    causal: bool = True
+    use_rope: bool = True
+    rope_base: float = 10000.0
+    scale: Optional[float] = None
+
+    @property
+    def Sl(self) -> int:
+        return self.S // self.P
+
+    @property
+    def softmax_scale(self) -> float:
+        return self.scale if self.scale is not None else 1.0 / math.sqrt(self.D)
+
+    def shape(self) -> _Shape:
+        return _Shape(self.P, self.B, self.S, self.n_head, self.n_kv_head, self.D,
+                      1 if self.causal else 0, self.softmax_scale)
+
+
+def _nthreads(n: Optional[int]) -> int:
+    return n if n else (os.cpu_count() or 1)
+
+
+def _ptrs(arrays: Sequence[np.ndarray]):
+    for a in arrays:
+        assert a.dtype == np.float64 and a.flags.c_contiguous
+    return (ctypes.c_void_p * len(arrays))(*[a.ctypes.data for a in arrays])
+
+
+def shard_sequence(x: np.ndarray, P: int) -> List[np.ndarray]:
+    """[SP2] §2 first step: split [B, S, ...] by sequence into P contiguous
+    chunks; rank r gets tokens [r*S/P, (r+1)*S/P)."""
+    S = x.shape[1]
+    assert S % P == 0
+    Sl = S // P
+    return [np.ascontiguousarray(x[:, r * Sl:(r + 1) * Sl], dtype=np.float64) for r in range(P)]
+
+
+def unshard_sequence(xs: Sequence[np.ndarray]) -> np.ndarray:
+    return np.concatenate(list(xs), axis=1)
+
+
+def a2a_seq_to_head(x_ranks: Sequence[np.ndarray], heads: int, elem_bytes: int = 2,
+                    skip: Optional[tuple] = None, fill: float = 0.0):
+    """Loop All-to-All, [B,Sl,heads,D] per rank -> [B,S,heads/P,D] per rank.
+    Returns (y_ranks, sent_bytes[P], recv_bytes[P])."""
+    P = len(x_ranks)
+    B, Sl, h, D = x_ranks[0].shape
+    assert h == heads
+    y = [np.full((B, Sl * P, heads // P, D), fill, dtype=np.float64) for _ in range(P)]
+    sent = (ctypes.c_longlong * P)()
+    recv = (ctypes.c_longlong * P)()
+    ss, sd = skip if skip else (-1, -1)
+    rc = lib().oracle_a2a_seq_to_head(P, B, Sl, heads, D, elem_bytes, _ptrs(x_ranks), _ptrs(y),
+                                      sent, recv, ss, sd)
+    if rc != 0:
+        raise ValueError("heads must be a multiple of P")
+    return y, list(sent), list(recv)
+
+
+def a2a_head_to_seq(y_ranks: Sequence[np.ndarray], heads: int, elem_bytes: int = 2,
+                    skip: Optional[tuple] = None, fill: float = 0.0):
+    """Inverse loop All-to-All, [B,S,heads/P,D] per rank -> [B,Sl,heads,D]."""
+    P = len(y_ranks)
+    B, S, hp, D = y_ranks[0].shape
+    assert hp * P == heads and S % P == 0
+    Sl = S // P
+    x = [np.full((B, Sl, heads, D), fill, dtype=np.float64) for _ in range(P)]
+    sent = (ctypes.c_longlong * P)()
+    recv = (ctypes.c_longlong * P)()
+    ss, sd = skip if skip else (-1, -1)
+    rc = lib().oracle_a2a_head_to_seq(P, B, Sl, heads, D, elem_bytes, _ptrs(y_ranks), _ptrs(x),
+                                      sent, recv, ss, sd)
+    if rc != 0:
+        raise ValueError("heads must be a multiple of P")
+    return x, list(sent), list(recv)
+
+
+def rope_seq(x_ranks: Sequence[np.ndarray], base: float, direction: int = 1) -> List[np.ndarray]:
+    """Rotate copies of the per-rank [B,Sl,heads,D] buffers by global position
+    (direction=-1: inverse rotation)."""
+    out = [np.array(a, dtype=np.float64, copy=True) for a in x_ranks]
+    P = len(out)
+    B, Sl, h, D = out[0].shape
+    lib().oracle_rope_seq(P, B, Sl, h, D, float(base), int(direction), _ptrs(out))
+    return out
+
+
+def attention_fwd(prob: Problem, q_head, k_head, v_head, rows=None, nthreads=None):
+    """Per-rank attention over the full sequence for the rank's heads.
+    Returns (o_head ranks [B,S,hp,D], lse ranks [B,hp,S]); rows not in `rows`
+    stay NaN."""
+    P, B, S, hp, D = prob.P, prob.B, prob.S, prob.n_head // prob.P, prob.D
+    o = [np.full((B, S, hp, D), np.nan) for _ in range(P)]
+    lse = [np.full((B, hp, S), np.nan) for _ in range(P)]
+    sh = prob.shape()
+    if rows is not None:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int32)
+        rp, nr = rows_arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), len(rows_arr)
+    else:
+        rows_arr, rp, nr = None, None, 0
+    rc = lib().oracle_attention_fwd(ctypes.byref(sh), _ptrs(q_head), _ptrs(k_head), _ptrs(v_head),
+                                    _ptrs(o), _ptrs(lse), rp, nr, _nthreads(nthreads))
+    if rc != 0:
+        raise ValueError("head counts do not divide")
+    return o, lse
+
+
+def attention_unsharded(prob: Problem, q, k, v, nthreads=None):
+    """Plain attention on global [B,S,heads,D] tensors (no ranks at all)."""
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    k = np.ascontiguousarray(k, dtype=np.float64)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    o = np.zeros_like(q)
+    lse = np.zeros((prob.B, prob.n_head, prob.S))
+    sh = prob.shape()
+    rc = lib().oracle_attention_unsharded(ctypes.byref(sh), q.ctypes.data, k.ctypes.data,
+                                          v.ctypes.data, o.ctypes.data, lse.ctypes.data,
+                                          _nthreads(nthreads))
+    if rc != 0:
+        raise ValueError("head counts do not divide")
+    return o, lse
+
+
+def attention_bwd(prob: Problem, q_head, k_head, v_head, do_head, groups=None,
+                  q_rows=None, kv_rows=None, nthreads=None):
+    """Backward on head-sharded buffers for the listed (rank, batch, local
+    kv-head) groups (default: all).  Returns (dq, dk, dv) head-layout ranks;
+    entries not computed stay NaN."""
+    P, B, S, D = prob.P, prob.B, prob.S, prob.D
+    hp, kvp = prob.n_head // P, prob.n_kv_head // P
+    dq = [np.full((B, S, hp, D), np.nan) for _ in range(P)]
+    dk = [np.full((B, S, kvp, D), np.nan) for _ in range(P)]
+    dv = [np.full((B, S, kvp, D), np.nan) for _ in range(P)]
+    if groups is None:
+        groups = [(r, b, kl) for r in range(P) for b in range(B) for kl in range(kvp)]
+    qa = np.ascontiguousarray(q_rows, dtype=np.int32) if q_rows is not None else None
+    ka = np.ascontiguousarray(kv_rows, dtype=np.int32) if kv_rows is not None else None
+    ip = ctypes.POINTER(ctypes.c_int)
+    sh = prob.shape()
+    ptrs = [_ptrs(x) for x in (q_head, k_head, v_head, do_head, dq, dk, dv)]
+    for (r, b, kl) in groups:
+        rc = lib().oracle_attention_bwd_group(
+            ctypes.byref(sh), r, b, kl, *ptrs,
+            qa.ctypes.data_as(ip) if qa is not None else None, len(qa) if qa is not None else 0,
+            ka.ctypes.data_as(ip) if ka is not None else None, len(ka) if ka is not None else 0,
+            _nthreads(nthreads))
+        if rc != 0:
+            raise ValueError(f"oracle backward failed ({rc})")
+    return dq, dk, dv
+
+
+# --------------------------------------------------------------------------
+# The whole path, in the pages' order.
+# --------------------------------------------------------------------------
+
+def forward(prob: Problem, Q, K, V, rows=None, elem_bytes=2, nthreads=None):
+    """[SP2] §2: split by sequence; rope q, k at global positions ([CMP]
+    skeleton); All-to-All Q, K, V (seq -> head); local attention; All-to-All
+    the output back (head -> seq).  Q: [B,S,n_head,D], K/V: [B,S,n_kv,D]
+    global arrays of the already-rounded input values.  Returns a dict with
+    every intermediate, the output o_seq ranks [B,Sl,n_head,D] and the bytes
+    each A2A moved."""
+    P = prob.P
+    q_seq, k_seq, v_seq = (shard_sequence(np.asarray(t, dtype=np.float64), P) for t in (Q, K, V))
+    if prob.use_rope:
+        q_seq = rope_seq(q_seq, prob.rope_base, +1)
+        k_seq = rope_seq(k_seq, prob.rope_base, +1)
+    q_head, sq, _ = a2a_seq_to_head(q_seq, prob.n_head, elem_bytes)
+    k_head, sk, _ = a2a_seq_to_head(k_seq, prob.n_kv_head, elem_bytes)
+    v_head, sv, _ = a2a_seq_to_head(v_seq, prob.n_kv_head, elem_bytes)
+    o_head, lse = attention_fwd(prob, q_head, k_head, v_head, rows=rows, nthreads=nthreads)
+    if rows is None:
+        o_seq, so, _ = a2a_head_to_seq(o_head, prob.n_head, elem_bytes)
+    else:
+        o_seq, so = None, None
+    return dict(q_seq_roped=q_seq, k_seq_roped=k_seq, q_head=q_head, k_head=k_head, v_head=v_head,
+                o_head=o_head, lse=lse, o_seq=o_seq,
+                sent=dict(q=sq, k=sk, v=sv, o=so))
+
+
+def backward(prob: Problem, Q, K, V, dO, groups=None, q_rows=None, kv_rows=None,
+             elem_bytes=2, nthreads=None):
+    """[SP2] §6: the output gradient dO ([B,S,H] global, H = n_head*D) is
+    split by sequence and All-to-All'd into head layout; per-head attention
+    backward; dQ, dK, dV are All-to-All'd back to sequence layout; the rope
+    rotation is undone on dQ and dK (gradients w.r.t. the pre-rope q, k).
+    Returns dict with dq_seq/dk_seq/dv_seq ranks and the head-layout
+    gradients."""
+    P, B, S, D = prob.P, prob.B, prob.S, prob.D
+    fw = forward(prob, Q, K, V, rows=[0], elem_bytes=elem_bytes, nthreads=nthreads)
+    do_glob = np.asarray(dO, dtype=np.float64).reshape(B, S, prob.n_head, D)
+    do_seq = shard_sequence(do_glob, P)
+    do_head, sdo, _ = a2a_seq_to_head(do_seq, prob.n_head, elem_bytes)
+    dq_h, dk_h, dv_h = attention_bwd(prob, fw["q_head"], fw["k_head"], fw["v_head"], do_head,
+                                     groups=groups, q_rows=q_rows, kv_rows=kv_rows,
+                                     nthreads=nthreads)
+    dq_seq, sdq, _ = a2a_head_to_seq(dq_h, prob.n_head, elem_bytes, fill=np.nan)
+    dk_seq, sdk, _ = a2a_head_to_seq(dk_h, prob.n_kv_head, elem_bytes, fill=np.nan)
+    dv_seq, sdv, _ = a2a_head_to_seq(dv_h, prob.n_kv_head, elem_bytes, fill=np.nan)
+    if prob.use_rope:
+        dq_seq = rope_seq(dq_seq, prob.rope_base, -1)
+        dk_seq = rope_seq(dk_seq, prob.rope_base, -1)
+    return dict(dq_seq=dq_seq, dk_seq=dk_seq, dv_seq=dv_seq, dq_head=dq_h, dk_head=dk_h,
+                dv_head=dv_h, do_head=do_head, q_head=fw["q_head"], k_head=fw["k_head"],
+                v_head=fw["v_head"], sent=dict(do=sdo, dq=sdq, dk=sdk, dv=sdv))
+
+
+def unsharded(prob: Problem, Q, K, V, nthreads=None):
+    """The same attention with no ranks: rope on global positions (one rank
+    holding everything), then plain attention on [B,S,heads,D]."""
+    q = np.asarray(Q, dtype=np.float64)
+    k = np.asarray(K, dtype=np.float64)
+    if prob.use_rope:
+        q = rope_seq([q], prob.rope_base, +1)[0]
+        k = rope_seq([k], prob.rope_base, +1)[0]
+    return attention_unsharded(prob, q, k, np.asarray(V, dtype=np.float64), nthreads=nthreads)
+
+
+def a2a_bytes_formula(N_bytes: int, P: int) -> float:
+    """[CMP] "DeepSpeed Attention costs": an All-to-All of an N-byte global
+    tensor over P ranks sends and receives N*(P-1)/P^2 bytes per rank."""
+    return N_bytes * (P - 1) / (P * P)
