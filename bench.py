@@ -1,0 +1,388 @@
+"""Benchmark of the Ulysses attention path on GB300 (one JSON line on stdout).
+
+A step is one pass of the whole path over one batch of seeded synthetic input
+in HBM: seq->head pack with RoPE, tensor-core attention forward, head->seq
+unpack and, for workloads with a backward, the backward with its reverse
+All-to-Alls.  Default workload: the pages' sizing (P=8 virtual ranks, B=1,
+S=32768, 32 heads, D=128, bf16, causal, RoPE).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload C4] [--impl ulysses|reference]
+
+N > 1 runs N independent replicas (one per GPU, launched by torchrun): the
+path has no data exchange between GPUs once its P virtual ranks share one
+HBM, so the job is weak-scaled and the only cross-GPU traffic is the timing
+reduction.  `--impl reference` times the fp64 CPU oracle on the host cores on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from ulysses_sequence_attention_seq_gb300.synthetic import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "tokens/s + attn TFLOP/s (S=32K, 32 heads, P=8 virtual); seq↔head permute GB/s"
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def attn_fwd_flops(w):
+    """Algorithmic FLOPs of the attention forward: two matmuls (QK^T and PV),
+    2*D flops per (query, key) pair each; causal counts S(S+1)/2 pairs."""
+    pairs = w.S * (w.S + 1) / 2 if w.causal else float(w.S) * w.S
+    return 4.0 * w.B * w.n_head * w.head_dim * pairs
+
+
+def permute_bytes(w, es):
+    """Bytes read + written by the seq->head pack of Q, K, V (2 x tensor bytes)."""
+    return 2.0 * w.B * w.S * (w.n_head + 2 * w.n_kv_head) * w.head_dim * es
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ our CUDA path
+
+def run_ulysses(args, w, rank, world):
+    from ulysses_sequence_attention_seq_gb300 import binding as U
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    prob = U.Problem.from_workload(w)
+    backward = w.backward and not args.fwd_only
+    ins = make_inputs(w, with_grad=backward)
+    buf = U.Buffers(prob, device=dev, backward=backward)
+    host = {"q": U.seq_layout(ins["q"], w.P).pin_memory(), "k": U.seq_layout(ins["k"], w.P).pin_memory(),
+            "v": U.seq_layout(ins["v"], w.P).pin_memory()}
+    if backward:
+        host["do"] = U.seq_layout(ins["do"], w.P).pin_memory()
+    buf.q_seq.copy_(host["q"])
+    buf.k_seq.copy_(host["k"])
+    buf.v_seq.copy_(host["v"])
+    if backward:
+        buf.do_seq.copy_(host["do"])
+    stream = torch.cuda.current_stream()
+    U.ulysses_workspace_init(prob, buf.ws)
+    torch.cuda.synchronize()
+
+    names = ["pack_qkv", "attn_fwd", "unpack_out"] + (["attn_bwd"] if backward else [])
+    launches_per_step = 3 + (3 if backward else 0)
+
+    def step(evs=None):
+        def mark(i):
+            if evs is not None:
+                evs[i].record(stream)
+        mark(0)
+        U.ulysses_pack_qkv(prob, buf.q_seq, buf.k_seq, buf.v_seq, buf.q_head, buf.k_head, buf.v_head, buf.ws)
+        mark(1)
+        U.ulysses_attn_fwd(prob, buf.q_head, buf.k_head, buf.v_head, buf.o_head, buf.lse, buf.ws)
+        mark(2)
+        U.ulysses_unpack_out(prob, buf.o_head, buf.o_seq)
+        mark(3)
+        if backward:
+            buf.backward()
+            mark(4)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if U.ulysses_read_status(buf.ws) != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    # ---- device-resident timing: K steps, per-kernel events on the stream
+    nev = len(names) + 1
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    total_ms = t0.elapsed_time(t1)
+    per = {n: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)] for i, n in enumerate(names)}
+
+    # ---- end to end through the public API with host buffers
+    o_host = torch.empty(buf.o_seq.shape, dtype=buf.o_seq.dtype, pin_memory=True)
+    grads_host = None
+    if backward:
+        grads_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (buf.dq_seq, buf.dk_seq, buf.dv_seq)]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = o_host.numel() * o_host.element_size() + (sum(t.numel() * t.element_size() for t in grads_host) if grads_host else 0)
+
+    def e2e_step():
+        buf.q_seq.copy_(host["q"], non_blocking=True)
+        buf.k_seq.copy_(host["k"], non_blocking=True)
+        buf.v_seq.copy_(host["v"], non_blocking=True)
+        if backward:
+            buf.do_seq.copy_(host["do"], non_blocking=True)
+        step()
+        o_host.copy_(buf.o_seq, non_blocking=True)
+        if backward:
+            for h, d in zip(grads_host, (buf.dq_seq, buf.dk_seq, buf.dv_seq)):
+                h.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    status = U.ulysses_read_status(buf.ws)
+    return dict(total_ms=total_ms, per=per, clocks=clk, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
+                launches=launches_per_step * args.steps, status=status, backward=backward)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------- the CPU oracle
+
+class OracleBench:
+    """Times the fp64 oracle, as it stands, on a bounded sample of a workload.
+
+    One sampled step runs the oracle's steps in the path's order: split by
+    sequence, RoPE and the three loop All-to-Alls of Q, K, V in full;
+    attention for `n_rows` query rows of every head; the inverse All-to-All in
+    full.  The full step's time is estimated as layout time + attention time x
+    (query-key pairs of the full workload / pairs sampled)."""
+
+    def __init__(self, w, nthreads=None):
+        sys.path.insert(0, os.path.join(ROOT, "tests"))
+        import oracle
+        self.oracle = oracle
+        self.w = w
+        self.nthreads = nthreads or (os.cpu_count() or 1)
+        ins = make_inputs(w, with_grad=False)
+        self.x = {k: v.to(torch.float64).numpy() for k, v in ins.items()}
+        del ins
+        self.op = oracle.Problem(B=w.B, S=w.S, n_head=w.n_head, n_kv_head=w.n_kv_head, D=w.head_dim,
+                                 P=w.P, causal=w.causal, use_rope=w.use_rope,
+                                 rope_base=float(np.float32(w.rope_base)))
+        self.rng = np.random.default_rng(0)
+
+    def step(self, n_rows):
+        o, w, x = self.oracle, self.w, self.x
+        t0 = time.perf_counter()
+        q, k, v = (o.shard_sequence(x[n], w.P) for n in ("q", "k", "v"))
+        if w.use_rope:
+            q, k = o.rope_seq(q, self.op.rope_base), o.rope_seq(k, self.op.rope_base)
+        qh, _, _ = o.a2a_seq_to_head(q, w.n_head)
+        kh, _, _ = o.a2a_seq_to_head(k, w.n_kv_head)
+        vh, _, _ = o.a2a_seq_to_head(v, w.n_kv_head)
+        t1 = time.perf_counter()
+        rows = sorted(set(int(r) for r in self.rng.integers(0, w.S, n_rows)))
+        oh, _ = o.attention_fwd(self.op, qh, kh, vh, rows=rows, nthreads=self.nthreads)
+        t2 = time.perf_counter()
+        o.a2a_head_to_seq(oh, w.n_head)
+        t3 = time.perf_counter()
+        pairs = sum((r + 1) if w.causal else w.S for r in rows)
+        full = w.S * (w.S + 1) / 2 if w.causal else float(w.S) * w.S
+        t_full = (t1 - t0) + (t3 - t2) + (t2 - t1) * full / pairs
+        return t_full, len(rows), pairs, t3 - t0
+
+    def calibrate(self, attn_budget_s):
+        """Row count whose attention takes about `attn_budget_s` seconds."""
+        n = 16
+        while True:
+            _, nr, pairs, wall = self.step(n)
+            if wall > attn_budget_s or n >= self.w.S:
+                return n
+            n = min(self.w.S, n * 4)
+
+    def describe(self, n_rows):
+        w = self.w
+        return (f"{w.name} (P={w.P}, S={w.S}, {w.n_head} heads, D={w.head_dim}): split, RoPE and the 4 loop "
+                f"all-to-alls in full; attention for {n_rows} random query rows of all {w.n_head} heads, "
+                f"scaled to the full causal triangle by query-key pairs")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="C4", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ulysses", choices=["ulysses", "reference"])
+    ap.add_argument("--fwd-only", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    w = WORKLOADS[args.workload]
+    hbm, tf_burst, tf_sust, peak_src = load_peaks()
+    tokens = w.B * w.S
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        ob = OracleBench(w)
+        per_step_budget = max(2.0, 150.0 / max(args.steps + args.warmup, 1))
+        n_rows = ob.calibrate(per_step_budget / 2)
+        times = [ob.step(n_rows)[0] for _ in range(args.steps)]
+        t = statistics.median(times)
+        value = tokens / t
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": w.name, "P": w.P, "B": w.B, "S": w.S, "n_head": w.n_head,
+                           "n_kv_head": w.n_kv_head, "head_dim": w.head_dim, "passes": "fwd"},
+                "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": ob.nthreads, "kind": "oracle",
+                                 "sample": ob.describe(n_rows)},
+                "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    r = run_ulysses(args, w, rank, world)
+    ms = max_over_ranks(r["total_ms"], world) / args.steps
+    e2e_ms = max_over_ranks(r["e2e_ms"], world) / args.steps
+    per = {k: statistics.mean(v) for k, v in r["per"].items()}
+    fl = attn_fwd_flops(w)
+    es = 2 if w.dtype == "bf16" else 4
+    attn_ms = per["attn_fwd"]
+    attn_tflops = fl / (attn_ms * 1e-3) / 1e12
+    pack_gbs = permute_bytes(w, es) / (per["pack_qkv"] * 1e-3) / 1e9
+    unpack_gbs = 2.0 * w.B * w.S * w.n_head * w.head_dim * es / (per["unpack_out"] * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": tokens * world / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded normal inputs of the workload's shape)",
+        "config": {"workload": w.name, "P": w.P, "B": w.B, "S": w.S, "n_head": w.n_head,
+                   "n_kv_head": w.n_kv_head, "head_dim": w.head_dim, "causal": w.causal, "rope": w.use_rope,
+                   "passes": "fwd+bwd" if r["backward"] else "fwd",
+                   "l2": "inputs larger than L2 (Q/K/V/O each >= 128 MiB); no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU, P virtual ranks"},
+        "attn_fwd_tflops": attn_tflops, "attn_fwd_ms": attn_ms,
+        "pack_gbs": pack_gbs, "unpack_gbs": unpack_gbs,
+        "kernel_ms": per,
+        "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": tf_sust, "unit": "TFLOP/s",
+                     "frac": attn_tflops / tf_sust, "traffic": None,
+                     "peak_source": f"{peak_src} bf16 sustained",
+                     "kernel": "attn_fwd_tc_kernel<128>"},
+        "secondary_rooflines": {"pack_qkv": {"bound": "hbm", "achieved": pack_gbs, "peak": hbm, "unit": "GB/s",
+                                             "frac": pack_gbs / hbm},
+                                "unpack_out": {"bound": "hbm", "achieved": unpack_gbs, "peak": hbm, "unit": "GB/s",
+                                               "frac": unpack_gbs / hbm}},
+        "clocks": r["clocks"],
+        "e2e": {"value": tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": r["launches"],
+        "device_status": r["status"],
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        ob = OracleBench(w)
+        n_rows = ob.calibrate(8.0)
+        t_full = ob.step(n_rows)[0]
+        line["cpu_baseline"] = {"value": tokens / t_full, "unit": "tokens/s", "cores": ob.nthreads,
+                                "kind": "oracle", "sample": ob.describe(n_rows)}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,178 @@
+/*
+ * ulysses.h -- C ABI of the single-GPU Ulysses attention path (sm_103a).
+ *
+ * The method ("Sequence Parallelism II: DeepSpeed Ulysses and All-to-All
+ * Attention", §1-§3 and §6; "Comparing Ulysses and Megatron Sequence
+ * Parallelism", "DeepSpeed Attention"): activations are sharded by sequence
+ * over P ranks; an All-to-All turns "all heads for my tokens" into "all tokens
+ * for my heads"; every rank runs ordinary attention over the full sequence
+ * for its n_head/P heads; a second All-to-All turns the output back.  Here
+ * the P ranks are virtual: all of their buffers live in one GPU's memory, the
+ * All-to-All is an on-device permutation kernel and attention runs on the
+ * tensor cores.
+ *
+ * Notation: hp = n_head/P, kvp = n_kv_head/P, Sl = S/P, D = head_dim,
+ * H = n_head*D.  Every multi-rank tensor is ONE allocation, rank-major,
+ * row-major, innermost index last:
+ *   sequence-sharded   X[P][B][Sl][heads][D]   (rank r holds tokens [r*Sl,(r+1)*Sl))
+ *   head-sharded       Y[P][B][S][hp or kvp][D] (rank r holds q-heads [r*hp,(r+1)*hp)
+ *                                                and kv-heads [r*kvp,(r+1)*kvp))
+ *   log-sum-exp        LSE[P][B][hp][S]  float, natural log
+ * Element type is bf16 (dtype 0) or fp32 (dtype 1), the same for every
+ * activation tensor of a call.  Query head g reads kv-head g/(n_head/n_kv_head).
+ *
+ * Ownership and execution.  The caller allocates and frees every buffer,
+ * including the workspace; the library allocates no device memory and keeps no
+ * state between calls.  Every entry point that takes a stream only enqueues
+ * work on it (no host synchronisation) and returns once the launches are
+ * queued; the outputs are valid when the stream reaches that point.  A NULL
+ * stream is the legacy default stream.  Inputs are never written.  Input and
+ * output byte ranges of one call must not overlap (ULYSSES_ERR_ALIAS).  Every
+ * device pointer must be 16-byte aligned (ULYSSES_ERR_ALIGN).
+ *
+ * Errors.  Entry points return ULYSSES_OK (0) or a negative code; on an error
+ * nothing has been enqueued, except ULYSSES_ERR_CUDA (a launch failed; the
+ * CUDA error is also left in cudaGetLastError).  Faults found while kernels
+ * run (a bounded wait that timed out, a workspace whose RoPE table does not
+ * match the problem) set bits in the workspace's status word, which
+ * ulysses_read_status() returns; kernels never trap.
+ */
+#ifndef ULYSSES_H
+#define ULYSSES_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *ulysses_stream_t; /* the same type as cudaStream_t */
+
+enum ulysses_dtype { ULYSSES_BF16 = 0, ULYSSES_FP32 = 1 };
+
+enum ulysses_status_code {
+  ULYSSES_OK = 0,
+  ULYSSES_ERR_ARG = -1,          /* NULL pointer, or a size <= 0 */
+  ULYSSES_ERR_DIVISIBILITY = -2, /* S%P, n_head%P, n_kv_head%P or n_head%n_kv_head != 0:
+                                    the head-count bound of plain Ulysses */
+  ULYSSES_ERR_HIDDEN = -3,       /* hidden != n_head * head_dim */
+  ULYSSES_ERR_UNSUPPORTED = -4,  /* head_dim / dtype / pass with no kernel */
+  ULYSSES_ERR_ALIGN = -5,        /* a pointer is not 16-byte aligned */
+  ULYSSES_ERR_ALIAS = -6,        /* an output overlaps an input or another output */
+  ULYSSES_ERR_WORKSPACE = -7,    /* workspace NULL or smaller than ulysses_workspace_bytes() */
+  ULYSSES_ERR_CUDA = -8          /* a CUDA launch or query failed */
+};
+
+/* Bits of the device status word (ulysses_read_status). */
+enum ulysses_device_status {
+  ULYSSES_STATUS_FWD_TIMEOUT = 1u << 0,  /* attention forward: a pipeline wait gave up */
+  ULYSSES_STATUS_BWD_TIMEOUT = 1u << 1,  /* attention backward: a pipeline wait gave up */
+  ULYSSES_STATUS_ROPE_TABLE = 1u << 2    /* RoPE table missing or built for another problem */
+};
+
+/*
+ * The problem statement of "Comparing Ulysses and Megatron Sequence
+ * Parallelism" ("A simple attention skeleton" and the constants of "Megatron
+ * Attention costs"): batch B, sequence length S, hidden size, n_head,
+ * n_kv_head, head_dim and the sequence-parallel group size P; plus the causal
+ * flag, the element type, RoPE on/off with its base, and the softmax scale
+ * (0 selects 1/sqrt(head_dim)).
+ */
+typedef struct ulysses_problem {
+  int B, S, hidden, n_head, n_kv_head, head_dim, P;
+  int causal;   /* 1: key k attends for query i iff k <= i (global positions) */
+  int dtype;    /* enum ulysses_dtype */
+  int use_rope; /* 1: rotate q and k by their global position inside the pack */
+  float rope_base;
+  float softmax_scale;
+} ulysses_problem;
+
+/* Checks the problem statement alone.  Returns ULYSSES_OK or the first failing
+ * code among ERR_ARG, ERR_DIVISIBILITY, ERR_HIDDEN, ERR_UNSUPPORTED.
+ * Host only; needs no GPU. */
+int ulysses_validate(const ulysses_problem *prob);
+
+/* Workspace bytes for a phase: 0 = forward (pack + attention + unpack),
+ * 1 = backward (also valid for the forward).  Returns 0 for an invalid
+ * problem.  Host only; needs no GPU. */
+size_t ulysses_workspace_bytes(const ulysses_problem *prob, int phase);
+
+/* Prepares a workspace for `prob`: clears the status word and, when use_rope
+ * is set, fills the RoPE table (cos and sin of p*base^(-2i/D), p < S,
+ * i < D/2, computed in double precision and rounded to float).  Call once per
+ * (workspace, problem) before any call that takes `ws`; calls with a
+ * workspace prepared for another problem flag ULYSSES_STATUS_ROPE_TABLE and
+ * leave their outputs unwritten. */
+int ulysses_workspace_init(const ulysses_problem *prob, void *ws, size_t ws_bytes,
+                           ulysses_stream_t stream);
+
+/* Copies the workspace status word to *status (synchronises `stream`). */
+int ulysses_read_status(const void *ws, uint32_t *status, ulysses_stream_t stream);
+
+/*
+ * Seq -> head All-to-All of Q, K and V, RoPE fused ("Sequence Parallelism II",
+ * §1 ownership example and §3; "Comparing Ulysses and Megatron Sequence
+ * Parallelism", skeleton: rope, then transpose):
+ *   q_head[d][b][s*Sl+t][j][:] = rope(q_seq[s][b][t][d*hp+j][:], s*Sl+t)
+ *   k_head likewise with kvp, v_head without rope.
+ * q_seq [P][B][Sl][n_head][D], k_seq/v_seq [P][B][Sl][n_kv_head][D];
+ * q_head [P][B][S][hp][D], k_head/v_head [P][B][S][kvp][D].
+ * RoPE: rotate-half, x'_i = x_i cos - x_{i+D/2} sin, x'_{i+D/2} = x_{i+D/2} cos
+ * + x_i sin, angle p*base^(-2i/D); float arithmetic on the input values, one
+ * rounding to the element type.  Without RoPE the result is a bit-exact copy.
+ * `ws` (phase 0) must have been prepared by ulysses_workspace_init.
+ */
+int ulysses_pack_qkv(const ulysses_problem *prob, const void *q_seq, const void *k_seq,
+                     const void *v_seq, void *q_head, void *k_head, void *v_head, void *ws,
+                     size_t ws_bytes, ulysses_stream_t stream);
+
+/*
+ * Per-rank attention over the full sequence for the rank's heads
+ * ("Sequence Parallelism II", §2 fourth step): for rank r, batch b, local
+ * head j (global g = r*hp+j, kv-head g/(n_head/n_kv_head)):
+ *   o[i] = sum_k softmax_k(scale * q_i.k_k [+ causal mask]) v_k,
+ *   lse[i] = log sum_k exp(scale * q_i.k_k).
+ * bf16: tensor-core kernel, head_dim 64 or 128, fp32 accumulation and softmax.
+ * fp32: CUDA-core kernel, head_dim 32, 64 or 128.
+ * o_head [P][B][S][hp][D] (element type), lse [P][B][hp][S] float.
+ */
+int ulysses_attn_fwd(const ulysses_problem *prob, const void *q_head, const void *k_head,
+                     const void *v_head, void *o_head, float *lse, void *ws, size_t ws_bytes,
+                     ulysses_stream_t stream);
+
+/*
+ * Head -> seq All-to-All of the attention output ("Sequence Parallelism II",
+ * §2 fifth step; "Comparing Ulysses and Megatron Sequence Parallelism",
+ * "DeepSpeed Attention": [B,S,heads/P,D] back to [B,S/P,heads,D] = [B,S/P,H]):
+ *   o_seq[d][b][t][(s*hp+j)*D+e] = o_head[s][b][d*Sl+t][j][e]   (bit-exact copy)
+ * o_head [P][B][S][hp][D] -> o_seq [P][B][Sl][H].
+ */
+int ulysses_unpack_out(const ulysses_problem *prob, const void *o_head, void *o_seq,
+                       ulysses_stream_t stream);
+
+/*
+ * Backward of the whole path ("Sequence Parallelism II", §6; "Comparing
+ * Ulysses and Megatron Sequence Parallelism", "DeepSpeed Attention costs":
+ * the inverse All-to-All for each tensor): dO_seq [P][B][Sl][H] goes seq ->
+ * head, per-head attention backward, dQ/dK/dV go head -> seq with the RoPE
+ * rotation undone on dQ and dK (gradients w.r.t. the pre-rope q, k; dK and dV
+ * summed over the q-heads that share a kv-head).
+ * Inputs: the head-layout q/k/v written by ulysses_pack_qkv, o_head and lse
+ * written by ulysses_attn_fwd, do_seq.  Outputs: dq_seq [P][B][Sl][n_head][D],
+ * dk_seq/dv_seq [P][B][Sl][n_kv_head][D].  bf16, head_dim 64 or 128.
+ * `ws` must be sized for phase 1 and prepared by ulysses_workspace_init.
+ */
+int ulysses_attn_bwd(const ulysses_problem *prob, const void *q_head, const void *k_head,
+                     const void *v_head, const void *o_head, const float *lse,
+                     const void *do_seq, void *dq_seq, void *dk_seq, void *dv_seq, void *ws,
+                     size_t ws_bytes, ulysses_stream_t stream);
+
+/* A static English description of a return code. */
+const char *ulysses_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ULYSSES_H */

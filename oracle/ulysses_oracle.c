@@ -175,22 +175,29 @@ int oracle_a2a_head_to_seq(int P, int B, int Sl, int heads, int D, int elem_byte
 void oracle_rope_seq(int P, int B, int Sl, int heads, int D, double base, int direction,
                      double *const *x_seq) {
   const int half = D / 2;
+  double *c = (double *)malloc(sizeof(double) * (size_t)(half > 0 ? half : 1));
+  double *s = (double *)malloc(sizeof(double) * (size_t)(half > 0 ? half : 1));
   for (int r = 0; r < P; ++r)
-    for (int b = 0; b < B; ++b)
-      for (int t = 0; t < Sl; ++t) {
-        const double p = (double)r * Sl + t;
+    for (int t = 0; t < Sl; ++t) {
+      const double p = (double)r * Sl + t;
+      for (int i = 0; i < half; ++i) {
+        double theta = pow(base, -2.0 * i / D);
+        double a = direction * p * theta;
+        c[i] = cos(a);
+        s[i] = sin(a);
+      }
+      for (int b = 0; b < B; ++b)
         for (int h = 0; h < heads; ++h) {
           double *v = x_seq[r] + (((long)b * Sl + t) * heads + h) * D;
           for (int i = 0; i < half; ++i) {
-            double theta = pow(base, -2.0 * i / D);
-            double a = direction * p * theta;
-            double c = cos(a), s = sin(a);
             double x1 = v[i], x2 = v[i + half];
-            v[i] = x1 * c - x2 * s;
-            v[i + half] = x2 * c + x1 * s;
+            v[i] = x1 * c[i] - x2 * s[i];
+            v[i + half] = x2 * c[i] + x1 * s[i];
           }
         }
-      }
+    }
+  free(c);
+  free(s);
 }
 
 /* ------------------------------------------------------------------------ */

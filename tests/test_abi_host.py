@@ -1,0 +1,108 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point that
+include/ulysses.h declares, and its host-side validation returns the
+documented codes.  Every call here fails validation before any launch (the
+pointers are fake addresses that are never dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from ulysses_sequence_attention_seq_gb300 import binding as U
+from ulysses_sequence_attention_seq_gb300 import build as B
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "ulysses.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(U.LIB_PATH):
+        B.build()
+    return U.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(ulysses_\w+)\s*\(", text, re.M)))
+
+
+def test_exports_every_declared_entry_point(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(U.EXPORTS) <= set(names)
+
+
+def prob(**kw):
+    base = dict(B=1, S=4096, hidden=4096, n_head=32, n_kv_head=8, head_dim=128, P=8, causal=True,
+                dtype=U.BF16, use_rope=True, rope_base=10000.0)
+    base.update(kw)
+    return U.Problem(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    ({}, 0),
+    (dict(B=0), -1), (dict(S=-4), -1), (dict(P=0), -1), (dict(rope_base=0.0), -1),
+    (dict(rope_base=0.0, use_rope=False), 0), (dict(softmax_scale=-1.0), -1),
+    (dict(S=4100), -2),                        # S % P
+    (dict(n_head=36, hidden=36 * 128), -2),    # n_head % P
+    (dict(n_kv_head=4), -2),                   # n_kv_head % P: P > n_kv_head
+    (dict(P=64, S=4096 * 64), -2),             # P > n_head: the head-count bound
+    (dict(n_kv_head=24), -2),                  # n_head % n_kv_head
+    (dict(hidden=1024), -3),
+    (dict(head_dim=96, hidden=32 * 96), -4), (dict(dtype=7), -4),
+    (dict(dtype=U.FP32, head_dim=32, hidden=1024), 0),
+])
+def test_validate_codes(lib, kw, code):
+    assert U.ulysses_validate(prob(**kw)) == code
+
+
+def test_workspace_sizes(lib):
+    p = prob()
+    f, b = U.ulysses_workspace_bytes(p, 0), U.ulysses_workspace_bytes(p, 1)
+    assert f >= 256 + p.S * p.head_dim * 4 and f % 256 == 0
+    # backward adds delta [B][n_head][S] fp32 and dO in head layout
+    assert b >= f + p.B * p.n_head * p.S * 4 + p.B * p.S * p.n_head * p.head_dim * 2
+    assert U.ulysses_workspace_bytes(prob(use_rope=False), 0) == 256
+    assert U.ulysses_workspace_bytes(prob(B=0), 0) == 0
+
+
+def test_status_strings(lib):
+    for code in range(0, -9, -1):
+        s = lib.ulysses_status_string(code)
+        assert s and b"unknown" not in s
+    assert b"unknown" in lib.ulysses_status_string(-99)
+
+
+def _call_pack(lib, p, q, k, v, qh, kh, vh, ws, nws):
+    vp = ctypes.c_void_p
+    return lib.ulysses_pack_qkv(ctypes.byref(p.c()), vp(q), vp(k), vp(v), vp(qh), vp(kh), vp(vh),
+                                vp(ws), nws, vp(0))
+
+
+def test_pointer_checks_fail_before_launch(lib):
+    p = prob(S=1024)
+    nq = p.B * p.S * p.n_head * p.head_dim * 2
+    nk = p.B * p.S * p.n_kv_head * p.head_dim * 2
+    nws = U.ulysses_workspace_bytes(p, 0)
+    base = 1 << 40
+    q, k, v = base, base + nq, base + nq + nk
+    qh, kh, vh = base + 4 * nq, base + 5 * nq, base + 6 * nq
+    ws = base + 8 * nq
+    assert _call_pack(lib, p, 0, k, v, qh, kh, vh, ws, nws) == -1          # NULL input
+    assert _call_pack(lib, p, q + 8, k, v, qh, kh, vh, ws, nws) == -5      # misaligned
+    assert _call_pack(lib, p, q, k, v, q + 16, kh, vh, ws, nws) == -6      # output overlaps input
+    assert _call_pack(lib, p, q, k, v, qh, qh + 16, vh, ws, nws) == -6     # outputs overlap
+    assert _call_pack(lib, p, q, k, v, qh, kh, vh, ws, nws - 1) == -7      # workspace too small
+    assert _call_pack(lib, p, q, k, v, qh, kh, vh, 0, nws) == -7           # no workspace
+    bad = prob(S=1024, n_kv_head=3)
+    assert _call_pack(lib, bad, q, k, v, qh, kh, vh, ws, nws) == -2
+    vp = ctypes.c_void_p
+    # the tensor-core forward has no kernel for head_dim 32 in bf16
+    p32 = prob(head_dim=32, hidden=32 * 32, S=1024)
+    assert lib.ulysses_attn_fwd(ctypes.byref(p32.c()), vp(q), vp(k), vp(v), vp(qh), vp(kh), vp(ws), nws,
+                                vp(0)) == -4
+    # the backward has no fp32 kernel
+    pf = prob(dtype=U.FP32, S=1024)
+    assert lib.ulysses_attn_bwd(ctypes.byref(pf.c()), *[vp(base + i * nq) for i in range(10)], nws, vp(0)) == -4

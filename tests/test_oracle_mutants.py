@@ -26,7 +26,7 @@ MUTANTS = [
      "double *to = x + (((long)b * Sl + t) * heads + ((long)j * P + src)) * D;"),
     ("self piece counted as traffic", "      if (src != dst) {\n        long long piece",
      "      {\n        long long piece"),
-    ("rope sign flipped", "v[i] = x1 * c - x2 * s;", "v[i] = x1 * c + x2 * s;"),
+    ("rope sign flipped", "v[i] = x1 * c[i] - x2 * s[i];", "v[i] = x1 * c[i] + x2 * s[i];"),
     ("rope uses local position", "const double p = (double)r * Sl + t;", "const double p = (double)t;"),
     ("rope frequency schedule", "pow(base, -2.0 * i / D)", "pow(base, -1.0 * i / D)"),
     ("softmax scale dropped", "w[k] = scale * dot;", "w[k] = dot;"),

@@ -1,0 +1,61 @@
+// internal.h -- declarations shared by the translation units of libulysses.
+// Host-side launch helpers; no public API (that is include/ulysses.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ulysses.h"
+
+namespace ulysses {
+
+// Workspace layout (byte offsets, 256-aligned).  The first 256 bytes hold the
+// device status word (uint32 at 0) and the RoPE table key (uint32 at 4).
+struct WorkspaceLayout {
+  size_t status = 0;
+  size_t rope = 0, rope_bytes = 0;    // float cos[S][D/2], then float sin[S][D/2]
+  size_t delta = 0, delta_bytes = 0;  // float [P][B][hp][S]          (backward)
+  size_t dohead = 0, dohead_bytes = 0;  // dO in head layout [P][B][S][hp][D] (backward)
+  size_t total_fwd = 0, total_bwd = 0;
+};
+WorkspaceLayout workspace_layout(const ulysses_problem &p);
+
+// A 32-bit key of (S, D, base) written next to the RoPE table by the init;
+// kernels that read the table compare it with the key of their own problem.
+uint32_t rope_key(const ulysses_problem &p);
+
+inline size_t elem_size(const ulysses_problem &p) { return p.dtype == ULYSSES_BF16 ? 2 : 4; }
+
+// ---- permutation kernels (permute.cu) ----
+cudaError_t launch_rope_table(const ulysses_problem &p, void *ws, cudaStream_t st);
+cudaError_t launch_pack_qkv(const ulysses_problem &p, const void *q, const void *k, const void *v,
+                            void *qh, void *kh, void *vh, void *ws, cudaStream_t st);
+cudaError_t launch_unpack(const ulysses_problem &p, const void *o_head, void *o_seq,
+                          cudaStream_t st);
+// dO seq -> head and delta[i] = sum_e dO[i][e] * O[i][e] per (rank, b, head, row).
+cudaError_t launch_pack_do_delta(const ulysses_problem &p, const void *do_seq, const void *o_head,
+                                 void *do_head, float *delta, cudaStream_t st);
+
+// ---- attention kernels ----
+struct TmaEncoder {
+  // cuTensorMapEncodeTiled, fetched from the driver at run time.
+  CUresult (*encode)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                     const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                     CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                     CUtensorMapFloatOOBfill) = nullptr;
+};
+bool get_tma_encoder(TmaEncoder *enc);
+
+cudaError_t launch_attn_fwd_simt(const ulysses_problem &p, const float *q, const float *k,
+                                 const float *v, float *o, float *lse, cudaStream_t st);
+cudaError_t launch_attn_fwd_tc(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
+                               const void *k, const void *v, void *o, float *lse,
+                               uint32_t *status, cudaStream_t st);
+cudaError_t launch_attn_bwd_tc(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
+                               const void *k, const void *v, const void *do_head,
+                               const float *lse, const float *delta, const void *ws,
+                               void *dq_seq, void *dk_seq, void *dv_seq, uint32_t *status,
+                               cudaStream_t st);
+
+}  // namespace ulysses

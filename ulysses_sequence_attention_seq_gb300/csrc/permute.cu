@@ -1,0 +1,316 @@
+// permute.cu -- the All-to-All of the Ulysses method as on-device permutations.
+//
+// "Sequence Parallelism II: DeepSpeed Ulysses and All-to-All Attention", §3:
+// every rank splits its local tensor into P pieces, keeps the one addressed to
+// itself and sends the rest; afterwards every rank holds one piece from every
+// rank.  With all P virtual ranks in one HBM this is a gather/scatter copy:
+// the piece rank s sends to rank d is s's head slice [d*hp, (d+1)*hp) of every
+// local token, and rank d stores it at sequence block s (§1: rank 0 goes from
+// S0H0,S0H1,S0H2,S0H3 to S0H0,S1H0,S2H0,S3H0).
+//
+// One kernel serves both directions.  It walks the sequence-sharded index
+// space (token row (s, b, t), destination rank d, local head j, 16-byte chunk
+// c) and computes the head-sharded address of the same element; `to_head`
+// selects which side is read.  For each (row, d) the hp*D elements of the
+// piece are contiguous on both sides, so a warp moves contiguous 512-byte
+// spans with 16-byte vector loads and stores.  RoPE ("Comparing Ulysses and
+// Megatron Sequence Parallelism", skeleton: rope before the transpose) is
+// fused: a thread owning chunk c of the first half also owns chunk c of the
+// second half, so each rotation pair (i, i + D/2) is in one thread.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace ulysses {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+struct PermJob {
+  const void *src;  // read side
+  void *dst;        // write side
+  int heads;        // heads of this tensor
+  int rope;         // 0: copy; +1: rotate by +angle; -1: rotate by -angle
+};
+
+struct PermParams {
+  PermJob job[3];
+  int njobs;
+  int P, B, Sl, D;
+  int to_head;  // 1: src is sequence-sharded (pack); 0: src is head-sharded (unpack)
+  const float *rope_cos, *rope_sin;  // [S][D/2] each
+  const uint32_t *rope_key_ptr;
+  uint32_t rope_key;
+  uint32_t *status;
+};
+
+__device__ __forceinline__ void rotate(float &x, float &y, float c, float s, int dir) {
+  // x' = x cos(a) - y sin(a), y' = y cos(a) + x sin(a), a = dir * angle.
+  const float sn = dir > 0 ? s : -s;
+  const float nx = x * c - y * sn;
+  const float ny = y * c + x * sn;
+  x = nx;
+  y = ny;
+}
+
+template <typename T>
+struct Chunk;
+
+template <>
+struct Chunk<__nv_bfloat16> {
+  static constexpr int kVec = 8;
+  static __device__ __forceinline__ void rope(uint4 &a, uint4 &b, const float *cs, const float *sn,
+                                              int dir) {
+    uint32_t *pa = reinterpret_cast<uint32_t *>(&a);
+    uint32_t *pb = reinterpret_cast<uint32_t *>(&b);
+    const float4 c0 = *reinterpret_cast<const float4 *>(cs);
+    const float4 c1 = *reinterpret_cast<const float4 *>(cs + 4);
+    const float4 s0 = *reinterpret_cast<const float4 *>(sn);
+    const float4 s1 = *reinterpret_cast<const float4 *>(sn + 4);
+    const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      __nv_bfloat162 xa = *reinterpret_cast<__nv_bfloat162 *>(&pa[w]);
+      __nv_bfloat162 xb = *reinterpret_cast<__nv_bfloat162 *>(&pb[w]);
+      float2 fa = __bfloat1622float2(xa), fb = __bfloat1622float2(xb);
+      rotate(fa.x, fb.x, cc[2 * w], ss[2 * w], dir);
+      rotate(fa.y, fb.y, cc[2 * w + 1], ss[2 * w + 1], dir);
+      __nv_bfloat162 ra = __float22bfloat162_rn(fa), rb = __float22bfloat162_rn(fb);
+      pa[w] = *reinterpret_cast<uint32_t *>(&ra);
+      pb[w] = *reinterpret_cast<uint32_t *>(&rb);
+    }
+  }
+};
+
+template <>
+struct Chunk<float> {
+  static constexpr int kVec = 4;
+  static __device__ __forceinline__ void rope(uint4 &a, uint4 &b, const float *cs, const float *sn,
+                                              int dir) {
+    float *fa = reinterpret_cast<float *>(&a);
+    float *fb = reinterpret_cast<float *>(&b);
+    const float4 c0 = *reinterpret_cast<const float4 *>(cs);
+    const float4 s0 = *reinterpret_cast<const float4 *>(sn);
+    const float cc[4] = {c0.x, c0.y, c0.z, c0.w};
+    const float ss[4] = {s0.x, s0.y, s0.z, s0.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) rotate(fa[w], fb[w], cc[w], ss[w], dir);
+  }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) permute_kernel(const PermParams p) {
+  constexpr int V = Chunk<T>::kVec;
+  const int S = p.P * p.Sl;
+  const long long rows = (long long)p.P * p.B * p.Sl;
+  bool any_rope = false;
+#pragma unroll
+  for (int q = 0; q < 3; ++q) any_rope |= (q < p.njobs && p.job[q].rope != 0);
+  if (any_rope && *p.rope_key_ptr != p.rope_key) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.status, (uint32_t)ULYSSES_STATUS_ROPE_TABLE);
+    return;
+  }
+  for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
+    // row = (s*B + b)*Sl + t : token t of sequence shard s, batch b
+    const int t = (int)(row % p.Sl);
+    const long long sb = row / p.Sl;
+    const int b = (int)(sb % p.B);
+    const int s = (int)(sb / p.B);
+    const int pos = s * p.Sl + t;  // global token position
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      if (q >= p.njobs) break;
+      const PermJob J = p.job[q];
+      const int hp = J.heads / p.P;
+      const int cph = J.rope ? p.D / (2 * V) : p.D / V;  // chunks per head handled per unit
+      const int run = hp * cph;                           // units per destination piece
+      const int units = J.heads * cph;
+      const long long seq_row = row * (long long)J.heads * p.D;
+      for (int u = threadIdx.x; u < units; u += kThreads) {
+        const int d = u / run;  // the rank on the head side of this piece
+        const int w = u - d * run;
+        const int j = w / cph, c = w - j * cph;
+        const long long head_off =
+            (((long long)(d * p.B + b) * S + pos) * hp + j) * p.D + (long long)c * V;
+        const long long seq_off = seq_row + (long long)(d * hp + j) * p.D + (long long)c * V;
+        const long long src_off = p.to_head ? seq_off : head_off;
+        const long long dst_off = p.to_head ? head_off : seq_off;
+        const T *src = static_cast<const T *>(J.src);
+        T *dst = static_cast<T *>(J.dst);
+        if (J.rope == 0) {
+          const uint4 x = __ldg(reinterpret_cast<const uint4 *>(src + src_off));
+          *reinterpret_cast<uint4 *>(dst + dst_off) = x;
+        } else {
+          const int half = p.D / 2;
+          uint4 x = __ldg(reinterpret_cast<const uint4 *>(src + src_off));
+          uint4 y = __ldg(reinterpret_cast<const uint4 *>(src + src_off + half));
+          const long long toff = (long long)pos * half + (long long)c * V;
+          Chunk<T>::rope(x, y, p.rope_cos + toff, p.rope_sin + toff, J.rope);
+          *reinterpret_cast<uint4 *>(dst + dst_off) = x;
+          *reinterpret_cast<uint4 *>(dst + dst_off + half) = y;
+        }
+      }
+    }
+  }
+}
+
+// cos/sin(p * base^(-2i/D)) in double precision, rounded to float.
+__global__ void rope_table_kernel(float *cs, float *sn, int S, int D, double base, uint32_t *hdr,
+                                  uint32_t key) {
+  const int half = D / 2;
+  const long long n = (long long)S * half;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int pos = (int)(idx / half), i = (int)(idx % half);
+    const double theta = pow(base, -2.0 * i / D);
+    double sv, cv;
+    sincos((double)pos * theta, &sv, &cv);
+    cs[idx] = (float)cv;
+    sn[idx] = (float)sv;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    hdr[0] = 0u;   // status word
+    hdr[1] = key;  // table key
+  }
+}
+
+// dO: seq -> head, plus delta[d][b][j][pos] = sum_e dO * O (O read in head layout).
+// A group of D/8 lanes owns one (token, head); bf16 only.
+__global__ void __launch_bounds__(kThreads)
+    pack_do_delta_kernel(const __nv_bfloat16 *__restrict__ dout, const __nv_bfloat16 *__restrict__ o,
+                         __nv_bfloat16 *__restrict__ do_head, float *__restrict__ delta, int P, int B,
+                         int Sl, int H, int D) {
+  const int S = P * Sl, hp = H / P;
+  const int lanes = D / 8;  // 8 or 16: divides 32
+  const long long groups = (long long)P * B * Sl * H;
+  const int lane = threadIdx.x & 31;
+  const int c = lane % lanes;
+  // The loop bound is uniform across the warp so that the shuffles below see
+  // every lane: a warp always covers 32/lanes consecutive groups.
+  const long long warp_first = ((blockIdx.x * (long long)kThreads + threadIdx.x) & ~31ll) / lanes;
+  const long long gstride = (long long)gridDim.x * kThreads / lanes;
+  for (long long wg = warp_first; wg < groups; wg += gstride) {
+    const long long gid = wg + lane / lanes;
+    const bool live = gid < groups;
+    float acc = 0.f;
+    long long head_row = 0;
+    int d = 0, b = 0, j = 0, pos = 0;
+    if (live) {
+      const int g = (int)(gid % H);
+      const long long row = gid / H;
+      const int t = (int)(row % Sl);
+      const long long sb = row / Sl;
+      b = (int)(sb % B);
+      const int s = (int)(sb / B);
+      pos = s * Sl + t;
+      d = g / hp;
+      j = g - d * hp;
+      head_row = (((long long)(d * B + b) * S + pos) * hp + j) * D;
+      const uint4 x = __ldg(reinterpret_cast<const uint4 *>(dout + gid * D + c * 8));
+      const uint4 y = __ldg(reinterpret_cast<const uint4 *>(o + head_row + c * 8));
+      *reinterpret_cast<uint4 *>(do_head + head_row + c * 8) = x;
+      const __nv_bfloat162 *px = reinterpret_cast<const __nv_bfloat162 *>(&x);
+      const __nv_bfloat162 *py = reinterpret_cast<const __nv_bfloat162 *>(&y);
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        float2 a = __bfloat1622float2(px[w]), bb = __bfloat1622float2(py[w]);
+        acc = fmaf(a.x, bb.x, acc);
+        acc = fmaf(a.y, bb.y, acc);
+      }
+    }
+    for (int off = lanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (live && c == 0) delta[((long long)(d * B + b) * hp + j) * S + pos] = acc;
+  }
+}
+
+int grid_for(long long rows) {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long g = (long long)sms * 8;
+  if (rows < g) g = rows;
+  return (int)(g > 0 ? g : 1);
+}
+
+}  // namespace
+
+cudaError_t launch_rope_table(const ulysses_problem &p, void *ws, cudaStream_t st) {
+  WorkspaceLayout L = workspace_layout(p);
+  uint8_t *base = static_cast<uint8_t *>(ws);
+  uint32_t *hdr = reinterpret_cast<uint32_t *>(base + L.status);
+  if (!p.use_rope) {
+    // clear the status word and write the key anyway
+    const uint32_t h[2] = {0u, rope_key(p)};
+    return cudaMemcpyAsync(hdr, h, sizeof h, cudaMemcpyHostToDevice, st);
+  }
+  float *cs = reinterpret_cast<float *>(base + L.rope);
+  float *sn = cs + (size_t)p.S * (p.head_dim / 2);
+  long long n = (long long)p.S * (p.head_dim / 2);
+  int grid = (int)((n + 255) / 256);
+  if (grid > 4096) grid = 4096;
+  rope_table_kernel<<<grid, 256, 0, st>>>(cs, sn, p.S, p.head_dim, (double)p.rope_base, hdr, rope_key(p));
+  return cudaGetLastError();
+}
+
+static PermParams base_params(const ulysses_problem &p, const void *ws, int to_head) {
+  PermParams pp{};
+  pp.P = p.P;
+  pp.B = p.B;
+  pp.Sl = p.S / p.P;
+  pp.D = p.head_dim;
+  pp.to_head = to_head;
+  if (ws) {
+    WorkspaceLayout L = workspace_layout(p);
+    const uint8_t *base = static_cast<const uint8_t *>(ws);
+    pp.status = reinterpret_cast<uint32_t *>(const_cast<uint8_t *>(base + L.status));
+    pp.rope_key_ptr = pp.status + 1;
+    pp.rope_key = rope_key(p);
+    pp.rope_cos = reinterpret_cast<const float *>(base + L.rope);
+    pp.rope_sin = pp.rope_cos + (size_t)p.S * (p.head_dim / 2);
+  }
+  return pp;
+}
+
+static cudaError_t launch_perm(const ulysses_problem &p, const PermParams &pp, cudaStream_t st) {
+  const int grid = grid_for((long long)p.B * p.S);
+  if (p.dtype == ULYSSES_BF16)
+    permute_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(pp);
+  else
+    permute_kernel<float><<<grid, kThreads, 0, st>>>(pp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_qkv(const ulysses_problem &p, const void *q, const void *k, const void *v,
+                            void *qh, void *kh, void *vh, void *ws, cudaStream_t st) {
+  PermParams pp = base_params(p, ws, 1);
+  const int r = p.use_rope ? 1 : 0;
+  pp.job[0] = {q, qh, p.n_head, r};
+  pp.job[1] = {k, kh, p.n_kv_head, r};
+  pp.job[2] = {v, vh, p.n_kv_head, 0};
+  pp.njobs = 3;
+  return launch_perm(p, pp, st);
+}
+
+cudaError_t launch_unpack(const ulysses_problem &p, const void *o_head, void *o_seq,
+                          cudaStream_t st) {
+  PermParams pp = base_params(p, nullptr, 0);
+  pp.job[0] = {o_head, o_seq, p.n_head, 0};
+  pp.njobs = 1;
+  return launch_perm(p, pp, st);
+}
+
+cudaError_t launch_pack_do_delta(const ulysses_problem &p, const void *do_seq, const void *o_head,
+                                 void *do_head, float *delta, cudaStream_t st) {
+  const long long groups = (long long)p.B * p.S * p.n_head;
+  const int lanes = p.head_dim / 8;
+  long long blocks = (groups * lanes + kThreads - 1) / kThreads;
+  int grid = grid_for(blocks);
+  pack_do_delta_kernel<<<grid, kThreads, 0, st>>>(
+      static_cast<const __nv_bfloat16 *>(do_seq), static_cast<const __nv_bfloat16 *>(o_head),
+      static_cast<__nv_bfloat16 *>(do_head), delta, p.P, p.B, p.S / p.P, p.n_head, p.head_dim);
+  return cudaGetLastError();
+}
+
+}  // namespace ulysses

@@ -1,0 +1,261 @@
+// ulysses_abi.cu -- the extern "C" entry points of include/ulysses.h.
+//
+// Host side only: argument validation (the head-count bound of plain Ulysses,
+// "Sequence Parallelism II: DeepSpeed Ulysses and All-to-All Attention", §4,
+// and the shape contract of "Comparing Ulysses and Megatron Sequence
+// Parallelism", "DeepSpeed Attention"), workspace layout, and kernel launches.
+// Nothing here computes on the host and nothing allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "internal.h"
+
+namespace ulysses {
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+WorkspaceLayout workspace_layout(const ulysses_problem &p) {
+  WorkspaceLayout L;
+  const size_t es = elem_size(p);
+  L.status = 0;
+  L.rope = 256;
+  L.rope_bytes = p.use_rope ? (size_t)p.S * p.head_dim * 4 : 0;
+  L.total_fwd = align256(L.rope + L.rope_bytes);
+  L.delta = L.total_fwd;
+  L.delta_bytes = (size_t)p.B * p.n_head * p.S * 4;
+  L.dohead = align256(L.delta + L.delta_bytes);
+  L.dohead_bytes = (size_t)p.B * p.S * p.n_head * p.head_dim * es;
+  L.total_bwd = align256(L.dohead + L.dohead_bytes);
+  return L;
+}
+
+uint32_t rope_key(const ulysses_problem &p) {
+  uint32_t bits = 0;
+  const float base = p.use_rope ? p.rope_base : 0.f;
+  memcpy(&bits, &base, 4);
+  uint32_t h = 2166136261u;
+  const uint32_t words[4] = {(uint32_t)p.S, (uint32_t)p.head_dim, bits, (uint32_t)p.use_rope};
+  for (uint32_t w : words) {
+    h ^= w;
+    h *= 16777619u;
+  }
+  return h | 1u;  // never 0, so a zeroed workspace never matches
+}
+
+bool get_tma_encoder(TmaEncoder *enc) {
+  static const TmaEncoder cached = [] {
+    TmaEncoder e;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess && fn)
+      e.encode = reinterpret_cast<decltype(e.encode)>(fn);
+    else
+      cudaGetLastError();
+    return e;
+  }();
+  *enc = cached;
+  return cached.encode != nullptr;
+}
+
+}  // namespace ulysses
+
+using namespace ulysses;
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Span {
+  const void *p;
+  size_t n;
+};
+
+bool overlaps(Span a, Span b) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+  return a.n && b.n && a0 < b0 + b.n && b0 < a0 + a.n;
+}
+
+// Every output must be disjoint from every input and from every other output.
+int check_spans(const Span *in, int nin, const Span *out, int nout) {
+  for (int i = 0; i < nin; ++i)
+    if (!in[i].p) return ULYSSES_ERR_ARG;
+  for (int i = 0; i < nout; ++i)
+    if (!out[i].p) return ULYSSES_ERR_ARG;
+  for (int i = 0; i < nin; ++i)
+    if (!aligned16(in[i].p)) return ULYSSES_ERR_ALIGN;
+  for (int i = 0; i < nout; ++i)
+    if (!aligned16(out[i].p)) return ULYSSES_ERR_ALIGN;
+  for (int o = 0; o < nout; ++o) {
+    for (int i = 0; i < nin; ++i)
+      if (overlaps(out[o], in[i])) return ULYSSES_ERR_ALIAS;
+    for (int o2 = o + 1; o2 < nout; ++o2)
+      if (overlaps(out[o], out[o2])) return ULYSSES_ERR_ALIAS;
+  }
+  return ULYSSES_OK;
+}
+
+int check_ws(const ulysses_problem &p, const void *ws, size_t ws_bytes, int phase) {
+  if (!ws) return ULYSSES_ERR_WORKSPACE;
+  if (!aligned16(ws)) return ULYSSES_ERR_ALIGN;
+  const WorkspaceLayout L = workspace_layout(p);
+  if (ws_bytes < (phase ? L.total_bwd : L.total_fwd)) return ULYSSES_ERR_WORKSPACE;
+  return ULYSSES_OK;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA; }
+
+size_t act_bytes(const ulysses_problem &p, int heads) {
+  return (size_t)p.B * p.S * heads * p.head_dim * elem_size(p);
+}
+
+}  // namespace
+
+extern "C" {
+
+int ulysses_validate(const ulysses_problem *prob) {
+  if (!prob) return ULYSSES_ERR_ARG;
+  const ulysses_problem &p = *prob;
+  if (p.B <= 0 || p.S <= 0 || p.hidden <= 0 || p.n_head <= 0 || p.n_kv_head <= 0 ||
+      p.head_dim <= 0 || p.P <= 0)
+    return ULYSSES_ERR_ARG;
+  if ((p.causal != 0 && p.causal != 1) || (p.use_rope != 0 && p.use_rope != 1))
+    return ULYSSES_ERR_ARG;
+  if (!(p.softmax_scale >= 0.f) || isinf(p.softmax_scale)) return ULYSSES_ERR_ARG;
+  if (p.use_rope && (!(p.rope_base > 0.f) || isinf(p.rope_base))) return ULYSSES_ERR_ARG;
+  if (p.S % p.P || p.n_head % p.P || p.n_kv_head % p.P || p.n_head % p.n_kv_head)
+    return ULYSSES_ERR_DIVISIBILITY;
+  if ((long long)p.n_head * p.head_dim != p.hidden) return ULYSSES_ERR_HIDDEN;
+  if (p.dtype != ULYSSES_BF16 && p.dtype != ULYSSES_FP32) return ULYSSES_ERR_UNSUPPORTED;
+  if (p.head_dim != 32 && p.head_dim != 64 && p.head_dim != 128) return ULYSSES_ERR_UNSUPPORTED;
+  // Index arithmetic inside the kernels keeps per-tensor element counts in
+  // 64 bits and per-row quantities in 32 bits.
+  if ((long long)p.B * p.P > (1ll << 30) || (long long)p.S * p.n_head > (1ll << 31))
+    return ULYSSES_ERR_UNSUPPORTED;
+  return ULYSSES_OK;
+}
+
+size_t ulysses_workspace_bytes(const ulysses_problem *prob, int phase) {
+  if (ulysses_validate(prob) != ULYSSES_OK) return 0;
+  const WorkspaceLayout L = workspace_layout(*prob);
+  return phase ? L.total_bwd : L.total_fwd;
+}
+
+int ulysses_workspace_init(const ulysses_problem *prob, void *ws, size_t ws_bytes,
+                           ulysses_stream_t stream) {
+  int rc = ulysses_validate(prob);
+  if (rc) return rc;
+  if ((rc = check_ws(*prob, ws, ws_bytes, 0))) return rc;
+  return cuda_rc(launch_rope_table(*prob, ws, (cudaStream_t)stream));
+}
+
+int ulysses_read_status(const void *ws, uint32_t *status, ulysses_stream_t stream) {
+  if (!ws || !status) return ULYSSES_ERR_ARG;
+  cudaError_t e = cudaMemcpyAsync(status, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost,
+                                  (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  return cuda_rc(e);
+}
+
+int ulysses_pack_qkv(const ulysses_problem *prob, const void *q_seq, const void *k_seq,
+                     const void *v_seq, void *q_head, void *k_head, void *v_head, void *ws,
+                     size_t ws_bytes, ulysses_stream_t stream) {
+  int rc = ulysses_validate(prob);
+  if (rc) return rc;
+  const ulysses_problem &p = *prob;
+  const size_t nq = act_bytes(p, p.n_head), nk = act_bytes(p, p.n_kv_head);
+  const Span in[4] = {{q_seq, nq}, {k_seq, nk}, {v_seq, nk}, {ws, ws_bytes}};
+  const Span out[3] = {{q_head, nq}, {k_head, nk}, {v_head, nk}};
+  if ((rc = check_ws(p, ws, ws_bytes, 0))) return rc;
+  if ((rc = check_spans(in, 4, out, 3))) return rc;
+  return cuda_rc(launch_pack_qkv(p, q_seq, k_seq, v_seq, q_head, k_head, v_head, ws,
+                                 (cudaStream_t)stream));
+}
+
+int ulysses_attn_fwd(const ulysses_problem *prob, const void *q_head, const void *k_head,
+                     const void *v_head, void *o_head, float *lse, void *ws, size_t ws_bytes,
+                     ulysses_stream_t stream) {
+  int rc = ulysses_validate(prob);
+  if (rc) return rc;
+  const ulysses_problem &p = *prob;
+  if (p.dtype == ULYSSES_BF16 && p.head_dim != 64 && p.head_dim != 128) return ULYSSES_ERR_UNSUPPORTED;
+  const size_t nq = act_bytes(p, p.n_head), nk = act_bytes(p, p.n_kv_head);
+  const size_t nl = (size_t)p.B * p.n_head * p.S * sizeof(float);
+  const Span in[3] = {{q_head, nq}, {k_head, nk}, {v_head, nk}};
+  const Span out[3] = {{o_head, nq}, {lse, nl}, {ws, ws_bytes}};
+  if ((rc = check_ws(p, ws, ws_bytes, 0))) return rc;
+  if ((rc = check_spans(in, 3, out, 3))) return rc;
+  uint32_t *status = static_cast<uint32_t *>(ws);
+  if (p.dtype == ULYSSES_FP32)
+    return cuda_rc(launch_attn_fwd_simt(p, static_cast<const float *>(q_head),
+                                        static_cast<const float *>(k_head),
+                                        static_cast<const float *>(v_head),
+                                        static_cast<float *>(o_head), lse, (cudaStream_t)stream));
+  TmaEncoder enc;
+  if (!get_tma_encoder(&enc)) return ULYSSES_ERR_CUDA;
+  return cuda_rc(launch_attn_fwd_tc(p, enc, q_head, k_head, v_head, o_head, lse, status,
+                                    (cudaStream_t)stream));
+}
+
+int ulysses_unpack_out(const ulysses_problem *prob, const void *o_head, void *o_seq,
+                       ulysses_stream_t stream) {
+  int rc = ulysses_validate(prob);
+  if (rc) return rc;
+  const ulysses_problem &p = *prob;
+  const size_t n = act_bytes(p, p.n_head);
+  const Span in[1] = {{o_head, n}};
+  const Span out[1] = {{o_seq, n}};
+  if ((rc = check_spans(in, 1, out, 1))) return rc;
+  return cuda_rc(launch_unpack(p, o_head, o_seq, (cudaStream_t)stream));
+}
+
+int ulysses_attn_bwd(const ulysses_problem *prob, const void *q_head, const void *k_head,
+                     const void *v_head, const void *o_head, const float *lse,
+                     const void *do_seq, void *dq_seq, void *dk_seq, void *dv_seq, void *ws,
+                     size_t ws_bytes, ulysses_stream_t stream) {
+  int rc = ulysses_validate(prob);
+  if (rc) return rc;
+  const ulysses_problem &p = *prob;
+  if (p.dtype != ULYSSES_BF16 || (p.head_dim != 64 && p.head_dim != 128))
+    return ULYSSES_ERR_UNSUPPORTED;
+  const size_t nq = act_bytes(p, p.n_head), nk = act_bytes(p, p.n_kv_head);
+  const size_t nl = (size_t)p.B * p.n_head * p.S * sizeof(float);
+  const Span in[6] = {{q_head, nq}, {k_head, nk}, {v_head, nk}, {o_head, nq}, {lse, nl}, {do_seq, nq}};
+  const Span out[4] = {{dq_seq, nq}, {dk_seq, nk}, {dv_seq, nk}, {ws, ws_bytes}};
+  if ((rc = check_ws(p, ws, ws_bytes, 1))) return rc;
+  if ((rc = check_spans(in, 6, out, 4))) return rc;
+  TmaEncoder enc;
+  if (!get_tma_encoder(&enc)) return ULYSSES_ERR_CUDA;
+  const WorkspaceLayout L = workspace_layout(p);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  float *delta = reinterpret_cast<float *>(w + L.delta);
+  void *do_head = w + L.dohead;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = launch_pack_do_delta(p, do_seq, o_head, do_head, delta, st);
+  if (e == cudaSuccess)
+    e = launch_attn_bwd_tc(p, enc, q_head, k_head, v_head, do_head, lse, delta, ws, dq_seq, dk_seq,
+                           dv_seq, reinterpret_cast<uint32_t *>(w + L.status), st);
+  return cuda_rc(e);
+}
+
+const char *ulysses_status_string(int code) {
+  switch (code) {
+    case ULYSSES_OK: return "ok";
+    case ULYSSES_ERR_ARG: return "invalid argument (NULL pointer or non-positive size)";
+    case ULYSSES_ERR_DIVISIBILITY:
+      return "divisibility: S, n_head and n_kv_head must be multiples of P and n_head a multiple of n_kv_head";
+    case ULYSSES_ERR_HIDDEN: return "hidden must equal n_head * head_dim";
+    case ULYSSES_ERR_UNSUPPORTED: return "unsupported head_dim / dtype / pass combination";
+    case ULYSSES_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case ULYSSES_ERR_ALIAS: return "an output buffer overlaps an input or another output";
+    case ULYSSES_ERR_WORKSPACE: return "workspace missing or too small";
+    case ULYSSES_ERR_CUDA: return "a CUDA call failed";
+    default: return "unknown status code";
+  }
+}
+
+}  // extern "C"
