@@ -342,6 +342,8 @@ def main():
     fl = attn_fwd_flops(w)
     es = 2 if w.dtype == "bf16" else 4
     attn_ms = per["attn_fwd"]
+    bwd_ms = per.get("attn_bwd")
+    bwd_tflops = 2.0 * fl / (bwd_ms * 1e-3) / 1e12 if bwd_ms else None
     attn_tflops = fl / (attn_ms * 1e-3) / 1e12
     pack_gbs = permute_bytes(w, es) / (per["pack_qkv"] * 1e-3) / 1e9
     unpack_gbs = 2.0 * w.B * w.S * w.n_head * w.head_dim * es / (per["unpack_out"] * 1e-3) / 1e9
@@ -356,6 +358,8 @@ def main():
                    "l2": "inputs larger than L2 (Q/K/V/O each >= 128 MiB); no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU, P virtual ranks"},
         "attn_fwd_tflops": attn_tflops, "attn_fwd_ms": attn_ms,
+        "attn_bwd_tflops": bwd_tflops, "attn_bwd_ms": bwd_ms,
+        "attn_bwd_flops_note": "backward algorithmic FLOPs = 2x forward (dV, dP, dQ, dK); the QK^T recompute is not counted",
         "pack_gbs": pack_gbs, "unpack_gbs": unpack_gbs,
         "kernel_ms": per,
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": tf_sust, "unit": "TFLOP/s",

@@ -1,13 +1,657 @@
-// attn_bwd_tc.cu -- bf16 attention backward on the tensor cores (in progress).
+// attn_bwd_tc.cu -- bf16 attention backward on the 5th-generation tensor cores,
+// with the reverse All-to-All of the gradients fused into the epilogues.
+//
+// "Sequence Parallelism II: DeepSpeed Ulysses and All-to-All Attention", §6:
+// the output gradient is All-to-All'd into head layout (done before these
+// kernels, together with delta = rowsum(dO * O)); the Q, K, V gradients are
+// produced per head and All-to-All'd back to sequence layout.  The gradient
+// formulas of softmax(scale q k^T) v, with P = exp(scale q.k - lse):
+//   dV = P^T dO          dP = dO V^T          dS = P * (dP - delta)
+//   dQ = scale dS K      dK = scale dS^T Q    (dK, dV summed over the q-heads
+//                                              that share a kv-head)
+// Two kernels, each deterministic (no atomics):
+//   dkdv: one CTA per 128-key tile of one kv-head.  K and V stay in shared
+//         memory; the loop runs over the q-heads of the group and the 64-row
+//         query tiles at or after the key tile (causal).  Per step:
+//         S^T = K Q^T and dP^T = V dO^T into double-buffered TMEM, the softmax
+//         warps form P^T and dS^T (bf16, shared memory), then dV += P^T dO and
+//         dK += dS^T Q accumulate in TMEM across the whole loop.
+//   dq:   one CTA per 128-row query tile of one head.  Q and dO stay in shared
+//         memory; the loop runs over 64-row key tiles at or before the query
+//         tile.  Per step: S = Q K^T and dP = dO V^T into double-buffered TMEM,
+//         dS (bf16) to shared memory, dQ += dS K in TMEM.
+// Epilogues: the thread that owns a row of the accumulator writes it straight
+// to its place in the sequence-sharded output (the inverse All-to-All as
+// addressing) after undoing the RoPE rotation on dQ and dK (both elements of
+// every rotation pair are in the same thread's row).
+// Warp roles: warps 0-7 softmax / epilogue (two warpgroups, each owns half of
+// the tile's columns; warp w reads TMEM lanes 32*(w%4)...), warp 8 TMA
+// producer, warp 9 MMA issuer.  All waits are bounded.
+#include <cuda_bf16.h>
+#include <math.h>
+#include <stdint.h>
+
 #include "internal.h"
+#include "sm100.cuh"
+#include "tmap.h"
 
 namespace ulysses {
+namespace {
 
-cudaError_t launch_attn_bwd_tc(const ulysses_problem &, const TmaEncoder &, const void *,
-                               const void *, const void *, const void *, const float *,
-                               const float *, const void *, void *, void *, void *, uint32_t *,
-                               cudaStream_t) {
-  return cudaErrorNotSupported;
+using namespace sm100;
+using dev::warp_wait;
+
+constexpr int kThreads = 320;
+constexpr int kTmaWarp = 8, kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct BwdParams {
+  int B, S, P, Sl, hp, kvp, group, causal;
+  int n_head, n_kv;                    // global head counts (row widths of the seq layout)
+  float scale, scale_log2;
+  const float *lse, *delta;            // [P][B][hp][S]
+  const float *rope_cos, *rope_sin;    // [S][D/2], or null without RoPE
+  __nv_bfloat16 *dq, *dk, *dv;         // sequence-sharded outputs
+  uint32_t *status;                    // status word; the RoPE table key follows it
+  uint32_t rope_key;
+};
+
+// True (and the status bit set) when the workspace's RoPE table was built for
+// another problem: the kernel then writes nothing.
+__device__ __forceinline__ bool stale_rope_table(const BwdParams &p) {
+  if (p.rope_cos && p.status[1] != p.rope_key) {
+    if (threadIdx.x == 0) atomicOr(p.status, (uint32_t)ULYSSES_STATUS_ROPE_TABLE);
+    return true;
+  }
+  return false;
+}
+
+// Barrier block shared by both kernels (byte offsets).
+enum : uint32_t {
+  kBarIn = 0,       // resident operands loaded
+  kBarFull = 8,     // [2] streamed operands loaded
+  kBarEmpty = 24,   // [2] streamed operands consumed
+  kBarSFull = 40,   // [2] score / dP MMAs done
+  kBarTFree = 56,   // [2] TMEM score buffers read (256 arrivals)
+  kBarPFull = 72,   // [2] P / dS written to shared memory (256 arrivals)
+  kBarPFree = 88,   // [2] accumulating MMAs that read P / dS done
+  kBarAcc = 104,    // all accumulation done
+  kBarDrain = 112,
+  kTmemSlot = 120,
+  kAbortSlot = 124
+};
+
+__device__ __forceinline__ void init_barriers(uint32_t bar) {
+  mbar_init(bar + kBarIn, 1);
+  for (int i = 0; i < 2; ++i) {
+    mbar_init(bar + kBarFull + 8 * i, 1);
+    mbar_init(bar + kBarEmpty + 8 * i, 1);
+    mbar_init(bar + kBarSFull + 8 * i, 1);
+    mbar_init(bar + kBarTFree + 8 * i, 256);
+    mbar_init(bar + kBarPFull + 8 * i, 256);
+    mbar_init(bar + kBarPFree + 8 * i, 1);
+  }
+  mbar_init(bar + kBarAcc, 1);
+  mbar_init(bar + kBarDrain, 1);
+}
+
+// 32 bf16 values of one row chunk into shared memory, 128-byte-swizzled
+// K-major layout: row `r` of a tile whose rows are 128 bytes, 16-byte units
+// u0..u0+3 (32 columns of a 64-column tile).
+__device__ __forceinline__ void st_row_units(uint32_t tile, int r, int u0, const uint32_t (&w)[16]) {
+#pragma unroll
+  for (int v = 0; v < 4; ++v)
+    st_shared_v4(tile + r * 128 + (((u0 + v) ^ (r & 7)) << 4), w[4 * v], w[4 * v + 1], w[4 * v + 2],
+                 w[4 * v + 3]);
+}
+
+// 32 fp32 accumulator columns -> scaled bf16 in global memory.
+__device__ __forceinline__ void store_plain(__nv_bfloat16 *dst, const uint32_t (&x)[32], float scale) {
+  uint32_t w[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e)
+    w[e] = pack_bf16x2(__uint_as_float(x[2 * e]) * scale, __uint_as_float(x[2 * e + 1]) * scale);
+  uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) d[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+}
+
+// Columns [i0, i0+32) (x) and [i0+D/2, i0+D/2+32) (y) of a gradient row:
+// scale, undo the rotation by the position's angle (x' = x cos + y sin,
+// y' = y cos - x sin), round to bf16 and store.
+__device__ __forceinline__ void store_unrotated(__nv_bfloat16 *dx, __nv_bfloat16 *dy, uint32_t (&x)[32],
+                                                uint32_t (&y)[32], float scale, const float *cs,
+                                                const float *sn) {
+  if (cs) {
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+      const float4 c4 = *reinterpret_cast<const float4 *>(cs + e);
+      const float4 s4 = *reinterpret_cast<const float4 *>(sn + e);
+      const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, ss[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float a = __uint_as_float(x[e + q]), b = __uint_as_float(y[e + q]);
+        x[e + q] = __float_as_uint(a * cc[q] + b * ss[q]);
+        y[e + q] = __float_as_uint(b * cc[q] - a * ss[q]);
+      }
+    }
+  }
+  store_plain(dx, x, scale);
+  store_plain(dy, y, scale);
+}
+
+// ============================================================= dK / dV kernel
+template <int D>
+struct KVLayout {
+  static constexpr uint32_t kKV = 128u * D * 2;  // K or V tile: 128 rows
+  static constexpr uint32_t kQ = 64u * D * 2;    // Q or dO tile: 64 rows
+  static constexpr uint32_t kPS = 128u * 128;    // P^T or dS^T: 128 key rows x 64 queries
+  static constexpr uint32_t oK = 0, oV = oK + kKV, oQ = oV + kKV, odO = oQ + 2 * kQ,
+                            oP = odO + 2 * kQ, odS = oP + 2 * kPS, oL = odS + 2 * kPS,
+                            oDl = oL + 2 * 256, oBar = oDl + 2 * 256;
+  static constexpr uint32_t kAlloc = oBar + 256 + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    dkdv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                const __grid_constant__ CUtensorMap tmL, const __grid_constant__ CUtensorMap tmDl,
+                const BwdParams p) {
+  using L = KVLayout<D>;
+  constexpr int kCh = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  uint8_t *smem = smem_raw + pad;
+  const uint32_t sb = raw + pad;
+  const uint32_t sK = sb + L::oK, sV = sb + L::oV, sQ = sb + L::oQ, sdO = sb + L::odO, sP = sb + L::oP,
+                 sdS = sb + L::odS, sL = sb + L::oL, sDl = sb + L::oDl, bar = sb + L::oBar;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::oBar + kAbortSlot);
+  const volatile uint32_t *gst = p.status;
+  if ((*gst & 3u) || stale_rope_table(p)) return;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int heads_total = p.P * p.B * p.kvp;
+  const int n = (int)(blockIdx.x / heads_total);  // key tile; low tiles have the most work
+  const int hid = (int)(blockIdx.x % heads_total);
+  const int kl = hid % p.kvp, rb = hid / p.kvp;
+  const int n_qt = (p.S + 63) / 64;
+  const int m0 = p.causal ? 2 * n : 0;
+  const int n_m = n_qt - m0;
+  const int n_iter = p.group * n_m;
+
+  if (threadIdx.x == 0) {
+    init_barriers(bar);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tmem_alloc(bar + kTmemSlot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::oBar + kTmemSlot);
+  const uint32_t tdV = tmem + 256, tdK = tmem + 256 + D;
+
+  if (warp == kTmaWarp) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmQ);
+      mbar_arrive_expect_tx(bar + kBarIn, 2 * L::kKV);
+      for (int c = 0; c < kCh; ++c) {
+        tma_load_4d(sK + c * 16384, &tmK, bar + kBarIn, c * 64, kl, n * 128, rb);
+        tma_load_4d(sV + c * 16384, &tmV, bar + kBarIn, c * 64, kl, n * 128, rb);
+      }
+      int issued = -1;
+      for (int i = 0; i < n_iter; ++i) {
+        const int b = i & 1;
+        const uint32_t ph = (i >> 1) & 1;
+        if (!mbar_wait_bounded(bar + kBarEmpty + 8 * b, ph ^ 1, abort_flag, gst)) break;
+        const int gi = i / n_m, m = m0 + i % n_m, j = kl * p.group + gi;
+        mbar_arrive_expect_tx(bar + kBarFull + 8 * b, 2 * L::kQ + 2 * 256);
+        for (int c = 0; c < kCh; ++c) {
+          tma_load_4d(sQ + b * L::kQ + c * 8192, &tmQ, bar + kBarFull + 8 * b, c * 64, j, m * 64, rb);
+          tma_load_4d(sdO + b * L::kQ + c * 8192, &tmdO, bar + kBarFull + 8 * b, c * 64, j, m * 64, rb);
+        }
+        dev::tma_load_2d(sL + b * 256, &tmL, bar + kBarFull + 8 * b, m * 64, rb * p.hp + j);
+        dev::tma_load_2d(sDl + b * 256, &tmDl, bar + kBarFull + 8 * b, m * 64, rb * p.hp + j);
+        issued = i;
+      }
+      if (*abort_flag) {
+        volatile int never = 0;
+        mbar_wait_bounded(bar + kBarIn, 0, &never, nullptr, 500000000ull);
+        for (int i = issued - 1; i <= issued; ++i)
+          if (i >= 0) mbar_wait_bounded(bar + kBarFull + 8 * (i & 1), (i >> 1) & 1, &never, nullptr, 500000000ull);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, 64, 0, 0);  // S^T, dP^T: both operands K-major
+      constexpr uint32_t idA = idesc_bf16_f32(128, D, 0, 1);   // dV, dK: B (dO, Q) MN-major
+      auto issue_acc = [&](int i) -> bool {
+        const int b = i & 1;
+        if (!mbar_wait_bounded(bar + kBarPFull + 8 * b, (i >> 1) & 1, abort_flag, gst)) return false;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t a = smem_desc_sw128(sP + b * L::kPS + kk * 32, 16, 1024);
+          const uint64_t bb = smem_desc_sw128(sdO + b * L::kQ + kk * 2048, 8192, 1024);
+          mma_bf16_ss(tdV, a, bb, idA, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t a = smem_desc_sw128(sdS + b * L::kPS + kk * 32, 16, 1024);
+          const uint64_t bb = smem_desc_sw128(sQ + b * L::kQ + kk * 2048, 8192, 1024);
+          mma_bf16_ss(tdK, a, bb, idA, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar + kBarPFree + 8 * b);
+        mma_commit(bar + kBarEmpty + 8 * b);
+        return true;
+      };
+      bool ok = mbar_wait_bounded(bar + kBarIn, 0, abort_flag, gst);
+      for (int i = 0; ok && i < n_iter; ++i) {
+        const int b = i & 1;
+        const uint32_t ph = (i >> 1) & 1;
+        if (!mbar_wait_bounded(bar + kBarFull + 8 * b, ph, abort_flag, gst)) { ok = false; break; }
+        if (i >= 2 && !mbar_wait_bounded(bar + kBarTFree + 8 * b, ((i - 2) >> 1) & 1, abort_flag, gst)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t oa = (kk >> 2) * 16384 + (kk & 3) * 32, ob = (kk >> 2) * 8192 + (kk & 3) * 32;
+          mma_bf16_ss(tmem + b * 64, smem_desc_sw128(sK + oa, 16, 1024),
+                      smem_desc_sw128(sQ + b * L::kQ + ob, 16, 1024), idS, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t oa = (kk >> 2) * 16384 + (kk & 3) * 32, ob = (kk >> 2) * 8192 + (kk & 3) * 32;
+          mma_bf16_ss(tmem + 128 + b * 64, smem_desc_sw128(sV + oa, 16, 1024),
+                      smem_desc_sw128(sdO + b * L::kQ + ob, 16, 1024), idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar + kBarSFull + 8 * b);
+        if (i > 0) ok = issue_acc(i - 1);
+      }
+      if (ok && n_iter > 0) issue_acc(n_iter - 1);
+      mma_commit(bar + kBarAcc);
+      mma_commit(bar + kBarDrain);
+      volatile int never = 0;
+      mbar_wait_bounded(bar + kBarDrain, 0, &never, nullptr);
+    }
+  } else {
+    // ---------------------------------------------- softmax warps (0..7)
+    const int g = warp >> 2, w4 = warp & 3;
+    const int r = w4 * 32 + lane;  // key row within the tile == TMEM lane
+    const uint32_t lane_base = (uint32_t)(w4 * 32) << 16;
+    const int kvr = n * 128 + r;
+    bool ok = true;
+    for (int i = 0; i < n_iter; ++i) {
+      const int b = i & 1;
+      const uint32_t ph = (i >> 1) & 1;
+      if (!warp_wait(bar + kBarSFull + 8 * b, ph, abort_flag, gst)) { ok = false; break; }
+      tc_fence_after_sync();
+      uint32_t sr[32], dr[32];
+      tmem_ld32(tmem + lane_base + b * 64 + g * 32, sr);
+      tmem_ld32(tmem + lane_base + 128 + b * 64 + g * 32, dr);
+      tmem_wait_ld();
+      tc_fence_before_sync();
+      mbar_arrive(bar + kBarTFree + 8 * b);
+      if (!warp_wait(bar + kBarFull + 8 * b, ph, abort_flag, gst)) { ok = false; break; }
+      const int q0 = (m0 + i % n_m) * 64 + g * 32;
+      const float *lse = reinterpret_cast<const float *>(smem + L::oL + b * 256) + g * 32;
+      const float *dlt = reinterpret_cast<const float *>(smem + L::oDl + b * 256) + g * 32;
+      uint32_t wp[16], wd[16];
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        float pe[2], ds[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int qi = q0 + c + h;
+          const bool valid = qi < p.S && (!p.causal || qi >= kvr);
+          const float x = fmaf(__uint_as_float(sr[c + h]), p.scale_log2, -lse[c + h] * kLog2e);
+          pe[h] = valid ? ex2(x) : 0.f;
+          ds[h] = pe[h] * (__uint_as_float(dr[c + h]) - dlt[c + h]);
+        }
+        wp[c >> 1] = pack_bf16x2(pe[0], pe[1]);
+        wd[c >> 1] = pack_bf16x2(ds[0], ds[1]);
+      }
+      if (i >= 2 && !warp_wait(bar + kBarPFree + 8 * b, ((i - 2) >> 1) & 1, abort_flag, gst)) {
+        ok = false;
+        break;
+      }
+      st_row_units(sP + b * L::kPS, r, g * 4, wp);
+      st_row_units(sdS + b * L::kPS, r, g * 4, wd);
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      mbar_arrive(bar + kBarPFull + 8 * b);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok) ok = warp_wait(bar + kBarAcc, 0, abort_flag, gst);
+    if (ok) {
+      tc_fence_after_sync();
+      const bool live = kvr < p.S;
+      const int s_rank = kvr / p.Sl, t = kvr - s_rank * p.Sl;
+      const int rr = rb / p.B, bb = rb - rr * p.B;
+      const size_t row = (((size_t)(s_rank * p.B + bb) * p.Sl + t) * p.n_kv + (rr * p.kvp + kl)) * D;
+      // dV: warpgroup g owns columns [g*D/2, (g+1)*D/2)
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t x[32];
+        const int col = g * (D / 2) + c * 32;
+        tmem_ld32(tdV + lane_base + col, x);
+        tmem_wait_ld();
+        if (live) store_plain(p.dv + row + col, x, 1.0f);
+      }
+      // dK: rotation pairs (i, i + D/2); warpgroup g owns i in [g*32, g*32+32)
+      // for D = 128, warpgroup 0 owns all 32 pairs for D = 64.
+      if (D == 128 || g == 0) {
+        const int i0 = g * 32;
+        uint32_t x[32], y[32];
+        tmem_ld32(tdK + lane_base + i0, x);
+        tmem_ld32(tdK + lane_base + D / 2 + i0, y);
+        tmem_wait_ld();
+        if (live) {
+          const float *cs = p.rope_cos ? p.rope_cos + (size_t)kvr * (D / 2) + i0 : nullptr;
+          const float *sn = p.rope_sin ? p.rope_sin + (size_t)kvr * (D / 2) + i0 : nullptr;
+          store_unrotated(p.dk + row + i0, p.dk + row + D / 2 + i0, x, y, p.scale, cs, sn);
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(p.status, (uint32_t)ULYSSES_STATUS_BWD_TIMEOUT);
+}
+
+// ================================================================== dQ kernel
+template <int D>
+struct QLayout {
+  static constexpr uint32_t kQ = 128u * D * 2;   // Q or dO: 128 rows
+  static constexpr uint32_t kKV = 64u * D * 2;   // K or V tile: 64 rows
+  static constexpr uint32_t kS = 128u * 128;     // dS: 128 queries x 64 keys
+  static constexpr uint32_t oQ = 0, odO = oQ + kQ, oK = odO + kQ, oV = oK + 2 * kKV,
+                            odS = oV + 2 * kKV, oBar = odS + 2 * kS;
+  static constexpr uint32_t kAlloc = oBar + 256 + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+              const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+              const BwdParams p) {
+  using L = QLayout<D>;
+  constexpr int kCh = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  uint8_t *smem = smem_raw + pad;
+  const uint32_t sb = raw + pad;
+  const uint32_t sQ = sb + L::oQ, sdO = sb + L::odO, sK = sb + L::oK, sV = sb + L::oV,
+                 sdS = sb + L::odS, bar = sb + L::oBar;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::oBar + kAbortSlot);
+  const volatile uint32_t *gst = p.status;
+  if ((*gst & 3u) || stale_rope_table(p)) return;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int heads_total = p.P * p.B * p.hp;
+  const int n_qt = (p.S + 127) / 128;
+  const int m = n_qt - 1 - (int)(blockIdx.x / heads_total);  // longest tiles first
+  const int hid = (int)(blockIdx.x % heads_total);
+  const int j = hid % p.hp, rb = hid / p.hp;
+  const int kl = j / p.group;
+  const int n_kt = (p.S + 63) / 64;
+  const int n_kv = p.causal ? min(n_kt, 2 * m + 2) : n_kt;
+
+  if (threadIdx.x == 0) {
+    init_barriers(bar);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tmem_alloc(bar + kTmemSlot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::oBar + kTmemSlot);
+  const uint32_t tdQ = tmem + 256;
+
+  if (warp == kTmaWarp) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      mbar_arrive_expect_tx(bar + kBarIn, 2 * L::kQ);
+      for (int c = 0; c < kCh; ++c) {
+        tma_load_4d(sQ + c * 16384, &tmQ, bar + kBarIn, c * 64, j, m * 128, rb);
+        tma_load_4d(sdO + c * 16384, &tmdO, bar + kBarIn, c * 64, j, m * 128, rb);
+      }
+      int issued = -1;
+      for (int i = 0; i < n_kv; ++i) {
+        const int b = i & 1;
+        const uint32_t ph = (i >> 1) & 1;
+        if (!mbar_wait_bounded(bar + kBarEmpty + 8 * b, ph ^ 1, abort_flag, gst)) break;
+        mbar_arrive_expect_tx(bar + kBarFull + 8 * b, 2 * L::kKV);
+        for (int c = 0; c < kCh; ++c) {
+          tma_load_4d(sK + b * L::kKV + c * 8192, &tmK, bar + kBarFull + 8 * b, c * 64, kl, i * 64, rb);
+          tma_load_4d(sV + b * L::kKV + c * 8192, &tmV, bar + kBarFull + 8 * b, c * 64, kl, i * 64, rb);
+        }
+        issued = i;
+      }
+      if (*abort_flag) {
+        volatile int never = 0;
+        mbar_wait_bounded(bar + kBarIn, 0, &never, nullptr, 500000000ull);
+        for (int i = issued - 1; i <= issued; ++i)
+          if (i >= 0) mbar_wait_bounded(bar + kBarFull + 8 * (i & 1), (i >> 1) & 1, &never, nullptr, 500000000ull);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, 64, 0, 0);  // S, dP: both operands K-major
+      constexpr uint32_t idQ = idesc_bf16_f32(128, D, 0, 1);   // dQ: B (K tile) MN-major
+      auto issue_dq = [&](int i) -> bool {
+        const int b = i & 1;
+        if (!mbar_wait_bounded(bar + kBarPFull + 8 * b, (i >> 1) & 1, abort_flag, gst)) return false;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t a = smem_desc_sw128(sdS + b * L::kS + kk * 32, 16, 1024);
+          const uint64_t bb = smem_desc_sw128(sK + b * L::kKV + kk * 2048, 8192, 1024);
+          mma_bf16_ss(tdQ, a, bb, idQ, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar + kBarPFree + 8 * b);
+        mma_commit(bar + kBarEmpty + 8 * b);
+        return true;
+      };
+      bool ok = mbar_wait_bounded(bar + kBarIn, 0, abort_flag, gst);
+      for (int i = 0; ok && i < n_kv; ++i) {
+        const int b = i & 1;
+        const uint32_t ph = (i >> 1) & 1;
+        if (!mbar_wait_bounded(bar + kBarFull + 8 * b, ph, abort_flag, gst)) { ok = false; break; }
+        if (i >= 2 && !mbar_wait_bounded(bar + kBarTFree + 8 * b, ((i - 2) >> 1) & 1, abort_flag, gst)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t oa = (kk >> 2) * 16384 + (kk & 3) * 32, ob = (kk >> 2) * 8192 + (kk & 3) * 32;
+          mma_bf16_ss(tmem + b * 64, smem_desc_sw128(sQ + oa, 16, 1024),
+                      smem_desc_sw128(sK + b * L::kKV + ob, 16, 1024), idS, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t oa = (kk >> 2) * 16384 + (kk & 3) * 32, ob = (kk >> 2) * 8192 + (kk & 3) * 32;
+          mma_bf16_ss(tmem + 128 + b * 64, smem_desc_sw128(sdO + oa, 16, 1024),
+                      smem_desc_sw128(sV + b * L::kKV + ob, 16, 1024), idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar + kBarSFull + 8 * b);
+        if (i > 0) ok = issue_dq(i - 1);
+      }
+      if (ok && n_kv > 0) issue_dq(n_kv - 1);
+      mma_commit(bar + kBarAcc);
+      mma_commit(bar + kBarDrain);
+      volatile int never = 0;
+      mbar_wait_bounded(bar + kBarDrain, 0, &never, nullptr);
+    }
+  } else {
+    const int g = warp >> 2, w4 = warp & 3;
+    const int r = w4 * 32 + lane;  // query row within the tile == TMEM lane
+    const uint32_t lane_base = (uint32_t)(w4 * 32) << 16;
+    const int qi = m * 128 + r;
+    const bool live = qi < p.S;
+    const size_t lrow = ((size_t)rb * p.hp + j) * p.S + (live ? qi : 0);
+    const float nl2 = live ? -p.lse[lrow] * kLog2e : 0.f;
+    const float dlt = live ? p.delta[lrow] : 0.f;
+    bool ok = true;
+    for (int i = 0; i < n_kv; ++i) {
+      const int b = i & 1;
+      const uint32_t ph = (i >> 1) & 1;
+      if (!warp_wait(bar + kBarSFull + 8 * b, ph, abort_flag, gst)) { ok = false; break; }
+      tc_fence_after_sync();
+      uint32_t sr[32], dr[32];
+      tmem_ld32(tmem + lane_base + b * 64 + g * 32, sr);
+      tmem_ld32(tmem + lane_base + 128 + b * 64 + g * 32, dr);
+      tmem_wait_ld();
+      tc_fence_before_sync();
+      mbar_arrive(bar + kBarTFree + 8 * b);
+      const int k0 = i * 64 + g * 32;
+      uint32_t wd[16];
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        float ds[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int kv = k0 + c + h;
+          const bool valid = kv < p.S && (!p.causal || kv <= qi);
+          const float pe = valid ? ex2(fmaf(__uint_as_float(sr[c + h]), p.scale_log2, nl2)) : 0.f;
+          ds[h] = pe * (__uint_as_float(dr[c + h]) - dlt);
+        }
+        wd[c >> 1] = pack_bf16x2(ds[0], ds[1]);
+      }
+      if (i >= 2 && !warp_wait(bar + kBarPFree + 8 * b, ((i - 2) >> 1) & 1, abort_flag, gst)) {
+        ok = false;
+        break;
+      }
+      st_row_units(sdS + b * L::kS, r, g * 4, wd);
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      mbar_arrive(bar + kBarPFull + 8 * b);
+    }
+    if (ok) ok = warp_wait(bar + kBarAcc, 0, abort_flag, gst);
+    if (ok && (D == 128 || g == 0)) {
+      tc_fence_after_sync();
+      const int s_rank = qi / p.Sl, t = qi - s_rank * p.Sl;
+      const int rr = rb / p.B, bb = rb - rr * p.B;
+      const size_t row = (((size_t)(s_rank * p.B + bb) * p.Sl + t) * p.n_head + (rr * p.hp + j)) * D;
+      const int i0 = g * 32;
+      uint32_t x[32], y[32];
+      tmem_ld32(tdQ + lane_base + i0, x);
+      tmem_ld32(tdQ + lane_base + D / 2 + i0, y);
+      tmem_wait_ld();
+      if (live) {
+        const float *cs = p.rope_cos ? p.rope_cos + (size_t)qi * (D / 2) + i0 : nullptr;
+        const float *sn = p.rope_sin ? p.rope_sin + (size_t)qi * (D / 2) + i0 : nullptr;
+        store_unrotated(p.dq + row + i0, p.dq + row + D / 2 + i0, x, y, p.scale, cs, sn);
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(p.status, (uint32_t)ULYSSES_STATUS_BWD_TIMEOUT);
+}
+
+template <int D>
+cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void *q, const void *k,
+                     const void *v, const void *do_head, const float *lse, const float *delta,
+                     const void *ws, void *dq, void *dk, void *dv, uint32_t *status, cudaStream_t st) {
+  const int hp = p.n_head / p.P, kvp = p.n_kv_head / p.P, PB = p.P * p.B;
+  CUtensorMap mK128, mV128, mQ64, mdO64, mL, mDl, mQ128, mdO128, mK64, mV64;
+  bool ok = make_act_map(enc, &mK128, k, D, kvp, p.S, PB, 128) &&
+            make_act_map(enc, &mV128, v, D, kvp, p.S, PB, 128) &&
+            make_act_map(enc, &mQ64, q, D, hp, p.S, PB, 64) &&
+            make_act_map(enc, &mdO64, do_head, D, hp, p.S, PB, 64) &&
+            make_row_map(enc, &mL, lse, p.S, PB * hp, 64) &&
+            make_row_map(enc, &mDl, delta, p.S, PB * hp, 64) &&
+            make_act_map(enc, &mQ128, q, D, hp, p.S, PB, 128) &&
+            make_act_map(enc, &mdO128, do_head, D, hp, p.S, PB, 128) &&
+            make_act_map(enc, &mK64, k, D, kvp, p.S, PB, 64) &&
+            make_act_map(enc, &mV64, v, D, kvp, p.S, PB, 64);
+  if (!ok) return cudaErrorInvalidValue;
+  BwdParams bp;
+  bp.B = p.B;
+  bp.S = p.S;
+  bp.P = p.P;
+  bp.Sl = p.S / p.P;
+  bp.hp = hp;
+  bp.kvp = kvp;
+  bp.group = hp / kvp;
+  bp.causal = p.causal;
+  bp.n_head = p.n_head;
+  bp.n_kv = p.n_kv_head;
+  bp.scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)D);
+  bp.scale_log2 = bp.scale * kLog2e;
+  bp.lse = lse;
+  bp.delta = delta;
+  if (p.use_rope) {
+    const WorkspaceLayout W = workspace_layout(p);
+    bp.rope_cos = reinterpret_cast<const float *>(static_cast<const uint8_t *>(ws) + W.rope);
+    bp.rope_sin = bp.rope_cos + (size_t)p.S * (D / 2);
+  } else {
+    bp.rope_cos = bp.rope_sin = nullptr;
+  }
+  bp.dq = static_cast<__nv_bfloat16 *>(dq);
+  bp.dk = static_cast<__nv_bfloat16 *>(dk);
+  bp.dv = static_cast<__nv_bfloat16 *>(dv);
+  bp.status = status;
+  bp.rope_key = rope_key(p);
+
+  const long long kv_blocks = (long long)((p.S + 127) / 128) * PB * kvp;
+  const long long q_blocks = (long long)((p.S + 127) / 128) * PB * hp;
+  if (kv_blocks > 0x7fffffffll || q_blocks > 0x7fffffffll) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)KVLayout<D>::kAlloc);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QLayout<D>::kAlloc);
+  if (e != cudaSuccess) return e;
+  dkdv_kernel<D><<<(unsigned)kv_blocks, kThreads, KVLayout<D>::kAlloc, st>>>(mK128, mV128, mQ64, mdO64, mL,
+                                                                            mDl, bp);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dq_kernel<D><<<(unsigned)q_blocks, kThreads, QLayout<D>::kAlloc, st>>>(mQ128, mdO128, mK64, mV64, bp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd_tc(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
+                               const void *k, const void *v, const void *do_head, const float *lse,
+                               const float *delta, const void *ws, void *dq_seq, void *dk_seq,
+                               void *dv_seq, uint32_t *status, cudaStream_t st) {
+  if (p.head_dim == 128)
+    return launch_d<128>(p, enc, q, k, v, do_head, lse, delta, ws, dq_seq, dk_seq, dv_seq, status, st);
+  if (p.head_dim == 64)
+    return launch_d<64>(p, enc, q, k, v, do_head, lse, delta, ws, dq_seq, dk_seq, dv_seq, status, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace ulysses
