@@ -226,11 +226,18 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """The slowest rank's time: every replica processed its units within it."""
     if world == 1:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(units_per_rank, seconds_max, world):
+    """Whole-job rate: the units all replicas processed over the max-over-ranks time."""
+    return units_per_rank * world / seconds_max
 
 
 # ---------------------------------------------------------- the CPU oracle
@@ -348,7 +355,7 @@ def main():
     pack_gbs = permute_bytes(w, es) / (per["pack_qkv"] * 1e-3) / 1e9
     unpack_gbs = 2.0 * w.B * w.S * w.n_head * w.head_dim * es / (per["unpack_out"] * 1e-3) / 1e9
     line = {
-        "metric": METRIC, "value": tokens * world / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": job_throughput(tokens, ms * 1e-3, world), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic (seeded normal inputs of the workload's shape)",
@@ -371,7 +378,7 @@ def main():
                                 "unpack_out": {"bound": "hbm", "achieved": unpack_gbs, "peak": hbm, "unit": "GB/s",
                                                "frac": unpack_gbs / hbm}},
         "clocks": r["clocks"],
-        "e2e": {"value": tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": job_throughput(tokens, e2e_ms * 1e-3, world), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": r["launches"],
         "device_status": r["status"],
