@@ -168,6 +168,35 @@ int ulysses_attn_bwd(const ulysses_problem *prob, const void *q_head, const void
                      const void *do_seq, void *dq_seq, void *dk_seq, void *dv_seq, void *ws,
                      size_t ws_bytes, ulysses_stream_t stream);
 
+/*
+ * The backward for callers that cannot allocate device memory.
+ *
+ * The paper has no counterpart to this entry point (the pages describe no
+ * allocation policy).  It exists for callers that cannot hand the library a
+ * workspace: code running under an allocator it does not own (a host framework
+ * that owns every device allocation), paths that must not call cudaMalloc or
+ * cudaFree because those can synchronise the device, or embedders with a memory
+ * budget fixed up front.
+ *
+ * Same arguments, layouts and results as ulysses_attn_bwd, without `ws`.  The
+ * scratch (RoPE table, delta, dO in head layout, status word) comes from a
+ * 32 MiB array in the library's own device memory, which every GPU that loads
+ * the library holds until the process exits.  A problem whose phase-1
+ * workspace (ulysses_workspace_bytes(prob, 1)) exceeds 32 MiB is rejected with
+ * ULYSSES_ERR_WORKSPACE before anything is enqueued.  No device memory is
+ * allocated by this call.
+ * The first call on each device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  Every call
+ * rebuilds the RoPE table and clears the status word in the array before the
+ * backward kernels run.  All calls share the one array: calls whose kernels
+ * overlap on the GPU (other streams, other host threads) race on it and must
+ * be ordered by the caller.
+ */
+int ulysses_attn_bwd_noalloc(const ulysses_problem *prob, const void *q_head, const void *k_head,
+                             const void *v_head, const void *o_head, const float *lse,
+                             const void *do_seq, void *dq_seq, void *dk_seq, void *dv_seq,
+                             ulysses_stream_t stream);
+
 /* A static English description of a return code. */
 const char *ulysses_status_string(int code);
 

@@ -107,6 +107,7 @@ def lib():
         L.ulysses_attn_fwd.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_unpack_out.argtypes = [P, vp, vp, vp]
         L.ulysses_attn_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.ulysses_attn_bwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.ulysses_status_string.argtypes = [ctypes.c_int]
         L.ulysses_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -174,6 +175,15 @@ def ulysses_attn_bwd(prob, q_head, k_head, v_head, o_head, lse, do_seq, dq_seq, 
         ctypes.byref(prob.c()), _ptr(q_head), _ptr(k_head), _ptr(v_head), _ptr(o_head), _ptr(lse),
         _ptr(do_seq), _ptr(dq_seq), _ptr(dk_seq), _ptr(dv_seq), _ptr(ws), ws.numel() * ws.element_size(),
         _stream(stream)))
+
+
+def ulysses_attn_bwd_noalloc(prob, q_head, k_head, v_head, o_head, lse, do_seq, dq_seq, dk_seq,
+                             dv_seq, stream=None):
+    """The backward without a workspace (for callers that cannot allocate):
+    scratch comes from the library's fixed 32 MiB device array."""
+    _check("ulysses_attn_bwd_noalloc", lib().ulysses_attn_bwd_noalloc(
+        ctypes.byref(prob.c()), _ptr(q_head), _ptr(k_head), _ptr(v_head), _ptr(o_head), _ptr(lse),
+        _ptr(do_seq), _ptr(dq_seq), _ptr(dk_seq), _ptr(dv_seq), _stream(stream)))
 
 
 # ---------------------------------------------------------------- buffers
