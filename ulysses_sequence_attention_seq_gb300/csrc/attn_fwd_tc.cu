@@ -7,88 +7,95 @@
 // the full sequence, plus the row log-sum-exp.  Query head g = r*hp + j reads
 // kv-head g / (n_head / n_kv_head), i.e. local kv index j / (hp / kvp).
 //
-// How (one CTA per 128-query tile of one head, 6 warps):
-//   warp 4      TMA producer: Q tile once, then K_t and V_t tiles into a
-//               2-stage ring (128 rows x D, 128-byte swizzle, 4-D tensor maps
-//               over [P*B][S][heads][D] so tiles never cross a sequence end).
-//   warp 5      MMA issuer (one thread): S_t = Q K_t^T into one of two TMEM
-//               score buffers, then O += P_{t-1} V_{t-1} into the TMEM output
-//               accumulator, so the score MMA of tile t runs while the softmax
-//               warps work on tile t-1.  Completion is signalled with
-//               tcgen05.commit on mbarriers.
-//   warps 0-3   softmax: thread i owns query row i = TMEM lane i.  It reads its
-//               score row from TMEM, applies scale and mask, keeps a running
-//               max in the base-2 domain and rescales the TMEM accumulator only
-//               when the max grows by more than 2^8 (otherwise the stale max is
-//               kept: every exponent stays <= 2^8, exact in fp32 and bf16), and
-//               writes P (bf16) into one of two shared-memory buffers in the
-//               swizzled K-major layout the next MMA reads.  At the end it
-//               divides by the row sum and stores O (bf16) and the LSE.
-// Causal tiles beyond the diagonal are skipped entirely; only the diagonal
-// tile is masked.  CTAs are ordered longest-first (highest query tile first)
-// so the triangular work balances across the 152 SMs.
-// Every wait is bounded (a few seconds); a timeout sets a status bit, the CTA
-// drains its outstanding tensor-core work, frees TMEM and exits.
+// How: one CTA per pair of 128-query tiles (A = rows [256i, 256i+128),
+// B = the next 128) of one head, 12 warps (warps 10-11 only complete the
+// third warpgroup, which the per-warpgroup register split needs).
+//   warp 8      TMA producer: both Q tiles once, then K_0, V_0, K_1, V_1, ...
+//               through a 3-slot ring (128 rows x D, 128-byte swizzle, 4-D
+//               tensor maps over [P*B][S][heads][D] so a tile never crosses a
+//               sequence end).  Every K/V tile serves 256 query rows.
+//   warp 9      MMA issuer (one thread), in the order
+//                 S_A(0) S_B(0) | PV_A(0) S_A(1) PV_B(0) S_B(1) | PV_A(1) ...
+//               so the tensor core alternates between the two tiles while the
+//               other tile's softmax runs.  Because S_X(j+1) is issued after
+//               PV_X(j), the commit that reports S_X(j+1) also reports that
+//               PV_X(j) has finished: the softmax can then overwrite P_X and
+//               rescale O_X without any further barrier.
+//   warps 0-3   softmax of tile A, warps 4-7 of tile B: thread i of a
+//               warpgroup owns query row i = TMEM lane i.  It reads its score
+//               row from TMEM, keeps a running max in the base-2 domain and
+//               rescales its TMEM accumulator row only when the max grows by
+//               more than 2^8 (otherwise the stale max stays: every exponent is
+//               <= 2^8, exact in fp32 and bf16), writes P (bf16) into its
+//               tile's shared-memory buffer in the swizzled K-major layout the
+//               PV MMA reads, and at the end divides by the row sum and stores
+//               O (bf16) and the LSE.
+// TMEM: S_A, S_B (128 columns each), O_A, O_B (D columns each).
+// Causal tiles past the diagonal are skipped; only the diagonal tile and the
+// ragged tail are masked.  CTAs are ordered longest-first.  Every wait is
+// bounded (2 s); a timeout sets a status bit, the CTA drains its tensor-core
+// work and copies in flight, frees TMEM and exits, and the other CTAs stop.
 #include <cuda_bf16.h>
 #include <math.h>
 #include <stdint.h>
 
 #include "internal.h"
 #include "sm100.cuh"
+#include "tmap.h"
 
 namespace ulysses {
 namespace {
 
 using namespace sm100;
+using dev::warp_wait;
 
-constexpr int BM = 128;  // query rows per CTA
-constexpr int BN = 128;  // keys per tile
-constexpr int kThreads = 192;
-constexpr int kTmaWarp = 4, kMmaWarp = 5;
+constexpr int BM = 128;        // query rows per tile (two tiles per CTA)
+constexpr int BN = 128;        // keys per tile
+constexpr int kThreads = 384;  // warpgroups 0-1 softmax, warpgroup 2: TMA, MMA, 2 idle warps
+constexpr int kTmaWarp = 8, kMmaWarp = 9;
+// Register split (launch: 384 threads x 168): warpgroup 2 drops to 56, the
+// softmax warpgroups rise to 224: 128*56 + 256*224 = 64512 = 384*168.
+constexpr uint32_t kRegsProducer = 56, kRegsSoftmax = 224;
+static_assert(128 * kRegsProducer + 256 * kRegsSoftmax <= 384 * 168, "register split over budget");
+constexpr int kSlots = 3;  // K/V ring
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;  // S buffers at columns 0 and 128, O at 256
-constexpr uint32_t kChunkBytes = 128 * 128;  // 128 rows x 128 bytes (64 bf16)
+constexpr uint32_t kChunkBytes = 128 * 128;    // 128 rows x 128 bytes (64 bf16)
+constexpr uint32_t kPBytes = 2 * kChunkBytes;  // one 128x128 bf16 P tile
 
 template <int D>
 struct Layout {
-  static constexpr uint32_t kTile = 128u * D * 2;  // one 128-row tile of Q, K or V
-  static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kQ + kTile;          // 2 stages
-  static constexpr uint32_t kV = kK + 2 * kTile;      // 2 stages
-  static constexpr uint32_t kP = kV + 2 * kTile;      // 2 buffers of 128x128 bf16
-  static constexpr uint32_t kBar = kP + 2 * 2 * kChunkBytes;
-  static constexpr uint32_t kBytes = kBar + 256;
-  static constexpr uint32_t kAlloc = kBytes + 1024;   // room to align the base to 1024
+  static constexpr uint32_t kTile = 128u * D * 2;       // one 128-row tile of Q, K or V
+  static constexpr uint32_t kQ = 0;                      // Q_A, Q_B
+  static constexpr uint32_t kKV = kQ + 2 * kTile;        // ring of kSlots tiles
+  static constexpr uint32_t kP = kKV + kSlots * kTile;   // P_A, P_B
+  static constexpr uint32_t kBar = kP + 2 * kPBytes;
+  static constexpr uint32_t kAlloc = kBar + 256 + 1024;  // room to align the base to 1024
 };
 
 // Barrier slots (byte offsets inside the barrier block).
 enum : uint32_t {
   kBarQFull = 0,
-  kBarKFull = 8,     // [2]
-  kBarKEmpty = 24,   // [2]
-  kBarVFull = 40,    // [2]
-  kBarVEmpty = 56,   // [2]
-  kBarSFull = 72,    // [2]
-  kBarPFull = 88,    // [2]
-  kBarPVDone = 104,  // [2]
-  kBarDrain = 120,
-  kTmemSlot = 128,
-  kAbortSlot = 132
+  kBarKVFull = 8,    // [3]
+  kBarKVEmpty = 32,  // [3]
+  kBarSFull = 56,    // [2] A, B
+  kBarPFull = 72,    // [2] A, B (128 arrivals)
+  kBarODone = 88,    // [2] A, B
+  kBarDrain = 104,
+  kTmemSlot = 112,
+  kAbortSlot = 116
 };
 
 struct FwdParams {
-  int B, S, P, hp, kvp, group, causal, n_qt;
+  int B, S, P, hp, kvp, group, causal, n_pairs;
   float scale_log2;
   __nv_bfloat16 *o;  // [P][B][S][hp][D]
   float *lse;        // [P][B][hp][S]
   uint32_t *status;
 };
 
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          const volatile uint32_t *gst) {
-  const bool ok = mbar_wait_bounded(bar, parity, abort_flag, gst);
-  return __all_sync(0xffffffffu, ok);
-}
+// Position in the K/V ring of the n-th tile streamed (K_j is n = 2j, V_j is 2j+1).
+__device__ __forceinline__ uint32_t ring_slot(int n) { return (uint32_t)(n % kSlots); }
+__device__ __forceinline__ uint32_t ring_parity(int n) { return (uint32_t)((n / kSlots) & 1); }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -102,33 +109,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
   uint8_t *smem = smem_raw + pad;
   const uint32_t sb = raw + pad;
-  const uint32_t sQ = sb + L::kQ, sK = sb + L::kK, sV = sb + L::kV, sP = sb + L::kP;
+  const uint32_t sQ = sb + L::kQ, sKV = sb + L::kKV, sP = sb + L::kP;
   const uint32_t bar = sb + L::kBar;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kBar + kAbortSlot);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const volatile uint32_t *gst = p.status;
   // A CTA of this grid (or an earlier launch on this workspace) gave up on a
   // wait: do not start more work.
   if (*gst & (ULYSSES_STATUS_FWD_TIMEOUT | ULYSSES_STATUS_BWD_TIMEOUT)) return;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int heads_total = p.P * p.B * p.hp;
-  const int qt = p.n_qt - 1 - (int)(blockIdx.x / heads_total);  // longest tiles first
+  const int qp = p.n_pairs - 1 - (int)(blockIdx.x / heads_total);  // longest pairs first
   const int hid = (int)(blockIdx.x % heads_total);
   const int j = hid % p.hp;
   const int rb = hid / p.hp;  // r*B + b
   const int kl = j / p.group;
-  const int n_kv = p.causal ? qt + 1 : (p.S + BN - 1) / BN;
+  const int n_kt = (p.S + BN - 1) / BN;
+  const int nA = p.causal ? min(2 * qp + 1, n_kt) : n_kt;  // key tiles of query tile A
+  const int nB = p.causal ? min(2 * qp + 2, n_kt) : n_kt;  // ... of query tile B (>= nA)
 
   if (threadIdx.x == 0) {
     mbar_init(bar + kBarQFull, 1);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(bar + kBarKVFull + 8 * i, 1);
+      mbar_init(bar + kBarKVEmpty + 8 * i, 1);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar + kBarKFull + 8 * i, 1);
-      mbar_init(bar + kBarKEmpty + 8 * i, 1);
-      mbar_init(bar + kBarVFull + 8 * i, 1);
-      mbar_init(bar + kBarVEmpty + 8 * i, 1);
       mbar_init(bar + kBarSFull + 8 * i, 1);
       mbar_init(bar + kBarPFull + 8 * i, 128);
-      mbar_init(bar + kBarPVDone + 8 * i, 1);
+      mbar_init(bar + kBarODone + 8 * i, 1);
     }
     mbar_init(bar + kBarDrain, 1);
     *abort_flag = 0;
@@ -144,178 +153,194 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kBar + kTmemSlot);
 
-  if (warp == kTmaWarp) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ producer
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(bar + kBarQFull, L::kTile);
-      for (int c = 0; c < kChunks; ++c)
-        tma_load_4d(sQ + c * kChunkBytes, &tmQ, bar + kBarQFull, c * 64, j, qt * BM, rb);
-      int issued_k = -1, issued_v = -1;
-      for (int t = 0; t < n_kv; ++t) {
-        const int st = t & 1;
-        const uint32_t ph = (t >> 1) & 1;
-        if (!mbar_wait_bounded(bar + kBarKEmpty + 8 * st, ph ^ 1, abort_flag, gst)) break;
-        mbar_arrive_expect_tx(bar + kBarKFull + 8 * st, L::kTile);
-        for (int c = 0; c < kChunks; ++c)
-          tma_load_4d(sK + st * L::kTile + c * kChunkBytes, &tmK, bar + kBarKFull + 8 * st, c * 64,
-                      kl, t * BN, rb);
-        issued_k = t;
-        if (!mbar_wait_bounded(bar + kBarVEmpty + 8 * st, ph ^ 1, abort_flag, gst)) break;
-        mbar_arrive_expect_tx(bar + kBarVFull + 8 * st, L::kTile);
-        for (int c = 0; c < kChunks; ++c)
-          tma_load_4d(sV + st * L::kTile + c * kChunkBytes, &tmV, bar + kBarVFull + 8 * st, c * 64,
-                      kl, t * BN, rb);
-        issued_v = t;
+  if (warp >= 8) {
+    regs_dec<kRegsProducer>();
+    if (warp == kTmaWarp) {
+      if (lane == 0) {
+        // ---------------------------------------------------------- producer
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        mbar_arrive_expect_tx(bar + kBarQFull, 2 * L::kTile);
+        for (int x = 0; x < 2; ++x)
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_4d(sQ + x * L::kTile + c * kChunkBytes, &tmQ, bar + kBarQFull, c * 64, j,
+                        qp * 2 * BM + x * BM, rb);
+        int issued = -1;
+        for (int n = 0; n < 2 * nB; ++n) {
+          const uint32_t slot = ring_slot(n);
+          if (!mbar_wait_bounded(bar + kBarKVEmpty + 8 * slot, ring_parity(n) ^ 1, abort_flag, gst))
+            break;
+          mbar_arrive_expect_tx(bar + kBarKVFull + 8 * slot, L::kTile);
+          const CUtensorMap *m = (n & 1) ? &tmV : &tmK;
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_4d(sKV + slot * L::kTile + c * kChunkBytes, m, bar + kBarKVFull + 8 * slot,
+                        c * 64, kl, (n >> 1) * BN, rb);
+          issued = n;
+        }
+        if (*abort_flag) {
+          // Let the copies already in flight land before the CTA goes away.
+          volatile int never = 0;
+          mbar_wait_bounded(bar + kBarQFull, 0, &never, nullptr, 500000000ull);
+          for (int n = issued - (kSlots - 1); n <= issued; ++n)
+            if (n >= 0)
+              mbar_wait_bounded(bar + kBarKVFull + 8 * ring_slot(n), ring_parity(n), &never, nullptr,
+                                500000000ull);
+        }
       }
-      if (*abort_flag) {
-        // Let the copies already in flight land before the CTA goes away.
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) {
+        // -------------------------------------------------------------- MMA
+        constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);  // Q, K both K-major
+        constexpr uint32_t idPV = idesc_bf16_f32(BM, D, 0, 1);  // P K-major, V MN-major
+        auto issue_s = [&](int x, int t) -> bool {
+          const int n = 2 * t;
+          if (!mbar_wait_bounded(bar + kBarKVFull + 8 * ring_slot(n), ring_parity(n), abort_flag, gst))
+            return false;
+          tc_fence_after_sync();
+          const uint32_t kt = sKV + ring_slot(n) * L::kTile;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+            mma_bf16_ss(tmem + x * BN, smem_desc_sw128(sQ + x * L::kTile + koff, 16, 1024),
+                        smem_desc_sw128(kt + koff, 16, 1024), idS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar + kBarSFull + 8 * x);
+          return true;
+        };
+        auto issue_pv = [&](int x, int t) -> bool {
+          const int n = 2 * t + 1;
+          if (!mbar_wait_bounded(bar + kBarPFull + 8 * x, t & 1, abort_flag, gst)) return false;
+          if (!mbar_wait_bounded(bar + kBarKVFull + 8 * ring_slot(n), ring_parity(n), abort_flag, gst))
+            return false;
+          tc_fence_after_sync();
+          const uint32_t vt = sKV + ring_slot(n) * L::kTile;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t a =
+                smem_desc_sw128(sP + x * kPBytes + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024);
+            const uint64_t b = smem_desc_sw128(vt + kk * 16 * 128, kChunkBytes, 1024);
+            mma_bf16_ss(tmem + 2 * BN + x * D, a, b, idPV, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          return true;
+        };
+        bool ok = mbar_wait_bounded(bar + kBarQFull, 0, abort_flag, gst);
+        if (ok && nA > 0) ok = issue_s(0, 0);
+        if (ok) ok = issue_s(1, 0);
+        if (ok) mma_commit(bar + kBarKVEmpty + 8 * ring_slot(0));
+        for (int t = 0; ok && t < nB; ++t) {
+          if (t < nA) {
+            if (!(ok = issue_pv(0, t))) break;
+            if (t == nA - 1)
+              mma_commit(bar + kBarODone);
+            else if (!(ok = issue_s(0, t + 1)))
+              break;
+          }
+          if (!(ok = issue_pv(1, t))) break;
+          mma_commit(bar + kBarKVEmpty + 8 * ring_slot(2 * t + 1));
+          if (t == nB - 1) {
+            mma_commit(bar + kBarODone + 8);
+          } else {
+            if (!(ok = issue_s(1, t + 1))) break;
+            mma_commit(bar + kBarKVEmpty + 8 * ring_slot(2 * t + 2));
+          }
+        }
+        // All tensor-core work of this CTA is complete once this commit lands.
+        mma_commit(bar + kBarDrain);
         volatile int never = 0;
-        mbar_wait_bounded(bar + kBarQFull, 0, &never, nullptr, 500000000ull);
-        for (int t = issued_k - 1; t <= issued_k; ++t)
-          if (t >= 0) mbar_wait_bounded(bar + kBarKFull + 8 * (t & 1), (t >> 1) & 1, &never, nullptr, 500000000ull);
-        for (int t = issued_v - 1; t <= issued_v; ++t)
-          if (t >= 0) mbar_wait_bounded(bar + kBarVFull + 8 * (t & 1), (t >> 1) & 1, &never, nullptr, 500000000ull);
+        mbar_wait_bounded(bar + kBarDrain, 0, &never, nullptr);
       }
-    }
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) {
-      // ---------------------------------------------------------------- MMA
-      constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);  // Q, K both K-major
-      constexpr uint32_t idPV = idesc_bf16_f32(BM, D, 0, 1);  // P K-major, V MN-major
-      auto issue_pv = [&](int i) -> bool {
-        const int st = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
-        if (!mbar_wait_bounded(bar + kBarPFull + 8 * st, ph, abort_flag, gst)) return false;
-        if (!mbar_wait_bounded(bar + kBarVFull + 8 * st, ph, abort_flag, gst)) return false;
-        tc_fence_after_sync();
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t a = smem_desc_sw128(
-              sP + st * 2 * kChunkBytes + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = smem_desc_sw128(sV + st * L::kTile + kk * 16 * 128, kChunkBytes, 1024);
-          mma_bf16_ss(tmem + kColO, a, b, idPV, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar + kBarPVDone + 8 * st);
-        mma_commit(bar + kBarVEmpty + 8 * st);
-        return true;
-      };
-      bool ok = mbar_wait_bounded(bar + kBarQFull, 0, abort_flag, gst);
-      for (int t = 0; ok && t < n_kv; ++t) {
-        const int st = t & 1;
-        const uint32_t ph = (t >> 1) & 1;
-        if (!mbar_wait_bounded(bar + kBarKFull + 8 * st, ph, abort_flag, gst)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          const uint64_t a = smem_desc_sw128(sQ + koff, 16, 1024);
-          const uint64_t b = smem_desc_sw128(sK + st * L::kTile + koff, 16, 1024);
-          mma_bf16_ss(tmem + st * BN, a, b, idS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar + kBarSFull + 8 * st);
-        mma_commit(bar + kBarKEmpty + 8 * st);
-        if (t > 0) ok = issue_pv(t - 1);
-      }
-      if (ok) issue_pv(n_kv - 1);
-      // All tensor-core work of this CTA is complete once this commit lands.
-      mma_commit(bar + kBarDrain);
-      volatile int never = 0;
-      mbar_wait_bounded(bar + kBarDrain, 0, &never, nullptr);
     }
   } else {
-    // ---------------------------------------------------------- softmax warps
-    const int row = threadIdx.x;  // 0..127 == TMEM lane
-    const int qpos = qt * BM + row;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    float m_used = -INFINITY, l = 0.f;
+    regs_inc<kRegsSoftmax>();
+    // ------------------------------------------------ softmax warpgroups A, B
+    const int x = warp >> 2;                 // 0: tile A, 1: tile B
+    const int row = (warp & 3) * 32 + lane;  // query row in the tile == TMEM lane
+    const int qpos = qp * 2 * BM + x * BM + row;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + x * BN;
+    const uint32_t tO = tmem + lane_base + 2 * BN + x * D;
+    const int n_mine = x ? nB : nA;
+    const int diag = p.causal ? 2 * qp + x : -1;  // the key tile holding this tile's diagonal
+    const uint32_t prow = sP + x * kPBytes + row * 128;
+    const float sl2 = p.scale_log2;
+    float m_used = -INFINITY, l = 0.f;  // running max (scaled, base 2) and row sum
     bool ok = true;
-    for (int t = 0; t < n_kv; ++t) {
-      const int st = t & 1;
-      if (!warp_wait(bar + kBarSFull + 8 * st, (t >> 1) & 1, abort_flag, gst)) {
+    for (int t = 0; t < n_mine; ++t) {
+      if (!warp_wait(bar + kBarSFull + 8 * x, t & 1, abort_flag, gst)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      uint32_t sr[BN / 32][32];
+      uint32_t s[4][32];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) tmem_ld32(tmem + lane_base + st * BN + c * 32, sr[c]);
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
       tmem_wait_ld();
-      float s[BN];
       const int kv0 = t * BN;
-      const bool need_mask = (p.causal && t == qt) || (kv0 + BN > p.S);
-      float mx = -INFINITY;
+      if (t == diag || kv0 + BN > p.S) {
+        // keys past this query row (causal) or past the sequence end
+        const int lim = min(p.causal ? qpos - kv0 : BN - 1, p.S - 1 - kv0);
 #pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        float x = __uint_as_float(sr[c >> 5][c & 31]) * p.scale_log2;
-        if (need_mask) {
-          const int kv = kv0 + c;
-          if (kv >= p.S || (p.causal && kv > qpos)) x = -INFINITY;
-        }
-        s[c] = x;
-        mx = fmaxf(mx, x);
+        for (int c = 0; c < BN; ++c)
+          if (c > lim) s[c >> 5][c & 31] = __float_as_uint(-INFINITY);
       }
-      // P buffer `st` is free once the PV MMA of tile t-2 has completed.
-      if (t >= 2 && !warp_wait(bar + kBarPVDone + 8 * st, ((t - 2) >> 1) & 1, abort_flag, gst)) {
-        ok = false;
-        break;
-      }
-      const bool need = mx > m_used + 8.0f;  // first tile: m_used = -inf
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(s[i >> 1][(i & 1) * 16]);
+#pragma unroll
+      for (int c = 0; c < BN; ++c)
+        if ((c & 15) != 0) mx[c >> 4] = fmaxf(mx[c >> 4], __uint_as_float(s[c >> 5][c & 31]));
+      const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float ms = mraw * sl2;
+      const bool need = ms > m_used + 8.0f;  // first tile: m_used = -inf
       if (__any_sync(0xffffffffu, need)) {
-        const float alpha = need ? ex2(m_used - mx) : 1.0f;
-        if (t >= 1) {
-          // Rescale the accumulator row once the PV MMA of tile t-1 is done.
-          if (!warp_wait(bar + kBarPVDone + 8 * ((t - 1) & 1), ((t - 1) >> 1) & 1, abort_flag, gst)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
+        // The S_X(t) commit we waited on also covers PV_X(t-1): O_X is final
+        // for tiles < t and no MMA touches it until P_X(t) is published.
+        const float alpha = need ? ex2(m_used - ms) : 1.0f;
+        if (t > 0) {
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t r[32];
-            tmem_ld32(tmem + lane_base + kColO + c * 32, r);
+            tmem_ld32(tO + c * 32, r);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            tmem_st32(tmem + lane_base + kColO + c * 32, r);
+            tmem_st32(tO + c * 32, r);
           }
           tmem_wait_st();
         }
         if (need) {
           l *= alpha;
-          m_used = mx;
+          m_used = ms;
         }
       }
-      uint32_t pk[BN / 2];
-      float rs = 0.f;
+      const float nb = -m_used;
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < BN / 2; ++c) {
-        const float p0 = ex2(s[2 * c] - m_used), p1 = ex2(s[2 * c + 1] - m_used);
-        rs += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
-      }
-      l += rs;
-      // Row `row` of P into buffer st: two 64-key chunks, 8 swizzled 16-byte units each.
-      const uint32_t prow = sP + st * 2 * kChunkBytes + row * 128;
+      for (int c = 0; c < 4; ++c) {
+        uint32_t w[16];
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch)
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int w = ch * 32 + u * 4;
-          st_shared_v4(prow + ch * kChunkBytes + ((u ^ (row & 7)) << 4), pk[w], pk[w + 1], pk[w + 2],
-                       pk[w + 3]);
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ex2(fmaf(__uint_as_float(s[c][2 * e]), sl2, nb));
+          const float p1 = ex2(fmaf(__uint_as_float(s[c][2 * e + 1]), sl2, nb));
+          rs[e & 3] += p0 + p1;
+          w[e] = pack_bf16x2(p0, p1);
         }
+        // columns [32c, 32c+32): 64-key chunk c/2, 16-byte units (c&1)*4 .. +3
+        const uint32_t base = prow + (c >> 1) * kChunkBytes;
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          st_shared_v4(base + ((((c & 1) * 4 + v) ^ (row & 7)) << 4), w[4 * v], w[4 * v + 1],
+                       w[4 * v + 2], w[4 * v + 3]);
+      }
+      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
       fence_proxy_async_smem();
       tc_fence_before_sync();
-      mbar_arrive(bar + kBarPFull + 8 * st);
+      mbar_arrive(bar + kBarPFull + 8 * x);
     }
     // --------------------------------------------------------------- epilogue
-    if (ok) ok = warp_wait(bar + kBarPVDone + 8 * ((n_kv - 1) & 1), ((n_kv - 1) >> 1) & 1, abort_flag, gst);
+    if (ok) ok = warp_wait(bar + kBarODone + 8 * x, 0, abort_flag, gst);
     if (ok) {
       tc_fence_after_sync();
       const float inv = 1.0f / l;
@@ -323,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_base + kColO + c * 32, r);
+        tmem_ld32(tO + c * 32, r);
         tmem_wait_ld();
         if (qpos < p.S) {
           uint32_t w[16];
@@ -351,26 +376,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && *abort_flag) atomicOr(p.status, (uint32_t)ULYSSES_STATUS_FWD_TIMEOUT);
 }
 
-bool make_map(const TmaEncoder &enc, CUtensorMap *m, const void *base, int D, int heads, int S,
-              int PB) {
-  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)S, (cuuint64_t)PB};
-  const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2,
-                                 (cuuint64_t)S * heads * D * 2};
-  const cuuint32_t box[4] = {64, 1, 128, 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  return enc.encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
-}
-
 template <int D>
 cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void *q, const void *k,
                      const void *v, void *o, float *lse, uint32_t *status, cudaStream_t st) {
-  const int hp = p.n_head / p.P, kvp = p.n_kv_head / p.P;
+  const int hp = p.n_head / p.P, kvp = p.n_kv_head / p.P, PB = p.P * p.B;
   CUtensorMap mq, mk, mv;
-  if (!make_map(enc, &mq, q, D, hp, p.S, p.P * p.B) || !make_map(enc, &mk, k, D, kvp, p.S, p.P * p.B) ||
-      !make_map(enc, &mv, v, D, kvp, p.S, p.P * p.B))
+  if (!make_act_map(enc, &mq, q, D, hp, p.S, PB, 128) || !make_act_map(enc, &mk, k, D, kvp, p.S, PB, 128) ||
+      !make_act_map(enc, &mv, v, D, kvp, p.S, PB, 128))
     return cudaErrorInvalidValue;
   FwdParams fp;
   fp.B = p.B;
@@ -380,13 +392,13 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   fp.kvp = kvp;
   fp.group = hp / kvp;
   fp.causal = p.causal;
-  fp.n_qt = (p.S + BM - 1) / BM;
+  fp.n_pairs = (p.S + 2 * BM - 1) / (2 * BM);
   const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)D);
   fp.scale_log2 = scale * 1.4426950408889634f;
   fp.o = static_cast<__nv_bfloat16 *>(o);
   fp.lse = lse;
   fp.status = status;
-  const long long blocks = (long long)fp.n_qt * p.P * p.B * hp;
+  const long long blocks = (long long)fp.n_pairs * PB * hp;
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)Layout<D>::kAlloc);

@@ -198,6 +198,20 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ------------------------------------------------------- register budgets
+// Per-warpgroup register limits (all four warps of a warpgroup execute the
+// same one).  The limits of all warpgroups must add up to no more than the
+// registers the block was launched with.  ptxas applies a limit to the code
+// the instruction dominates, so it belongs inside the branch of its role.
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // --------------------------------------------------------------- arithmetic
 // Hardware base-2 exponential (MUFU), flush-to-zero; exp2(-inf) = 0.
 __device__ __forceinline__ float ex2(float x) {
