@@ -70,23 +70,31 @@ __device__ __forceinline__ bool stale_rope_table(const BwdParams &p) {
 // Barrier block shared by both kernels (byte offsets).
 enum : uint32_t {
   kBarIn = 0,       // resident operands loaded
-  kBarFull = 8,     // [2] streamed operands loaded
-  kBarEmpty = 24,   // [2] streamed operands consumed
-  kBarSFull = 40,   // [2] score / dP MMAs done
-  kBarTFree = 56,   // [2] TMEM score buffers read (256 arrivals)
-  kBarPFull = 72,   // [2] P / dS written to shared memory (256 arrivals)
-  kBarPFree = 88,   // [2] accumulating MMAs that read P / dS done
-  kBarAcc = 104,    // all accumulation done
-  kBarDrain = 112,
-  kTmemSlot = 120,
-  kAbortSlot = 124
+  kBarFull = 8,     // [kMaxStages] streamed operands loaded
+  kBarEmpty = 40,   // [kMaxStages] streamed operands consumed
+  kBarSFull = 72,   // [2] score / dP MMAs done
+  kBarTFree = 88,   // [2] TMEM score buffers read (256 arrivals)
+  kBarPFull = 104,  // [2] P / dS written to shared memory (256 arrivals)
+  kBarPFree = 120,  // [2] accumulating MMAs that read P / dS done
+  kBarAcc = 136,    // all accumulation done
+  kBarDrain = 144,
+  kTmemSlot = 152,
+  kAbortSlot = 156
 };
+constexpr int kMaxStages = 4;
+// Depth of the streamed-operand ring: a stage is refilled only after the
+// accumulating MMAs of the iteration that used it have finished, so the ring
+// must cover the load latency plus one softmax step.
+constexpr int kStagesKV = 3;  // dkdv: Q, dO, LSE, delta per 64-query step
+constexpr int kStagesQ = 4;   // dq: K, V per 64-key step
 
 __device__ __forceinline__ void init_barriers(uint32_t bar) {
   mbar_init(bar + kBarIn, 1);
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < kMaxStages; ++i) {
     mbar_init(bar + kBarFull + 8 * i, 1);
     mbar_init(bar + kBarEmpty + 8 * i, 1);
+  }
+  for (int i = 0; i < 2; ++i) {
     mbar_init(bar + kBarSFull + 8 * i, 1);
     mbar_init(bar + kBarTFree + 8 * i, 256);
     mbar_init(bar + kBarPFull + 8 * i, 256);
@@ -147,9 +155,9 @@ struct KVLayout {
   static constexpr uint32_t kKV = 128u * D * 2;  // K or V tile: 128 rows
   static constexpr uint32_t kQ = 64u * D * 2;    // Q or dO tile: 64 rows
   static constexpr uint32_t kPS = 128u * 128;    // P^T or dS^T: 128 key rows x 64 queries
-  static constexpr uint32_t oK = 0, oV = oK + kKV, oQ = oV + kKV, odO = oQ + 2 * kQ,
-                            oP = odO + 2 * kQ, odS = oP + 2 * kPS, oL = odS + 2 * kPS,
-                            oDl = oL + 2 * 256, oBar = oDl + 2 * 256;
+  static constexpr uint32_t oK = 0, oV = oK + kKV, oQ = oV + kKV, odO = oQ + kStagesKV * kQ,
+                            oP = odO + kStagesKV * kQ, odS = oP + 2 * kPS, oL = odS + 2 * kPS,
+                            oDl = oL + kStagesKV * 256, oBar = oDl + kStagesKV * 256;
   static constexpr uint32_t kAlloc = oBar + 256 + 1024;
 };
 
@@ -209,24 +217,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int issued = -1;
       for (int i = 0; i < n_iter; ++i) {
-        const int b = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
-        if (!mbar_wait_bounded(bar + kBarEmpty + 8 * b, ph ^ 1, abort_flag, gst)) break;
+        const int st = i % kStagesKV;
+        const uint32_t ph = (i / kStagesKV) & 1;
+        if (!mbar_wait_bounded(bar + kBarEmpty + 8 * st, ph ^ 1, abort_flag, gst)) break;
         const int gi = i / n_m, m = m0 + i % n_m, j = kl * p.group + gi;
-        mbar_arrive_expect_tx(bar + kBarFull + 8 * b, 2 * L::kQ + 2 * 256);
+        mbar_arrive_expect_tx(bar + kBarFull + 8 * st, 2 * L::kQ + 2 * 256);
         for (int c = 0; c < kCh; ++c) {
-          tma_load_4d(sQ + b * L::kQ + c * 8192, &tmQ, bar + kBarFull + 8 * b, c * 64, j, m * 64, rb);
-          tma_load_4d(sdO + b * L::kQ + c * 8192, &tmdO, bar + kBarFull + 8 * b, c * 64, j, m * 64, rb);
+          tma_load_4d(sQ + st * L::kQ + c * 8192, &tmQ, bar + kBarFull + 8 * st, c * 64, j, m * 64, rb);
+          tma_load_4d(sdO + st * L::kQ + c * 8192, &tmdO, bar + kBarFull + 8 * st, c * 64, j, m * 64, rb);
         }
-        dev::tma_load_2d(sL + b * 256, &tmL, bar + kBarFull + 8 * b, m * 64, rb * p.hp + j);
-        dev::tma_load_2d(sDl + b * 256, &tmDl, bar + kBarFull + 8 * b, m * 64, rb * p.hp + j);
+        dev::tma_load_2d(sL + st * 256, &tmL, bar + kBarFull + 8 * st, m * 64, rb * p.hp + j);
+        dev::tma_load_2d(sDl + st * 256, &tmDl, bar + kBarFull + 8 * st, m * 64, rb * p.hp + j);
         issued = i;
       }
       if (*abort_flag) {
         volatile int never = 0;
         mbar_wait_bounded(bar + kBarIn, 0, &never, nullptr, 500000000ull);
-        for (int i = issued - 1; i <= issued; ++i)
-          if (i >= 0) mbar_wait_bounded(bar + kBarFull + 8 * (i & 1), (i >> 1) & 1, &never, nullptr, 500000000ull);
+        for (int i = issued - (kStagesKV - 1); i <= issued; ++i)
+          if (i >= 0)
+            mbar_wait_bounded(bar + kBarFull + 8 * (i % kStagesKV), (i / kStagesKV) & 1, &never, nullptr,
+                              500000000ull);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -234,30 +244,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idS = idesc_bf16_f32(128, 64, 0, 0);  // S^T, dP^T: both operands K-major
       constexpr uint32_t idA = idesc_bf16_f32(128, D, 0, 1);   // dV, dK: B (dO, Q) MN-major
       auto issue_acc = [&](int i) -> bool {
-        const int b = i & 1;
+        const int b = i & 1, st = i % kStagesKV;
         if (!mbar_wait_bounded(bar + kBarPFull + 8 * b, (i >> 1) & 1, abort_flag, gst)) return false;
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t a = smem_desc_sw128(sP + b * L::kPS + kk * 32, 16, 1024);
-          const uint64_t bb = smem_desc_sw128(sdO + b * L::kQ + kk * 2048, 8192, 1024);
+          const uint64_t bb = smem_desc_sw128(sdO + st * L::kQ + kk * 2048, 8192, 1024);
           mma_bf16_ss(tdV, a, bb, idA, (i > 0 || kk > 0) ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t a = smem_desc_sw128(sdS + b * L::kPS + kk * 32, 16, 1024);
-          const uint64_t bb = smem_desc_sw128(sQ + b * L::kQ + kk * 2048, 8192, 1024);
+          const uint64_t bb = smem_desc_sw128(sQ + st * L::kQ + kk * 2048, 8192, 1024);
           mma_bf16_ss(tdK, a, bb, idA, (i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(bar + kBarPFree + 8 * b);
-        mma_commit(bar + kBarEmpty + 8 * b);
+        mma_commit(bar + kBarEmpty + 8 * st);
         return true;
       };
       bool ok = mbar_wait_bounded(bar + kBarIn, 0, abort_flag, gst);
       for (int i = 0; ok && i < n_iter; ++i) {
-        const int b = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
-        if (!mbar_wait_bounded(bar + kBarFull + 8 * b, ph, abort_flag, gst)) { ok = false; break; }
+        const int b = i & 1, st = i % kStagesKV;
+        if (!mbar_wait_bounded(bar + kBarFull + 8 * st, (i / kStagesKV) & 1, abort_flag, gst)) {
+          ok = false;
+          break;
+        }
         if (i >= 2 && !mbar_wait_bounded(bar + kBarTFree + 8 * b, ((i - 2) >> 1) & 1, abort_flag, gst)) {
           ok = false;
           break;
@@ -267,13 +279,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * 16384 + (kk & 3) * 32, ob = (kk >> 2) * 8192 + (kk & 3) * 32;
           mma_bf16_ss(tmem + b * 64, smem_desc_sw128(sK + oa, 16, 1024),
-                      smem_desc_sw128(sQ + b * L::kQ + ob, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                      smem_desc_sw128(sQ + st * L::kQ + ob, 16, 1024), idS, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * 16384 + (kk & 3) * 32, ob = (kk >> 2) * 8192 + (kk & 3) * 32;
           mma_bf16_ss(tmem + 128 + b * 64, smem_desc_sw128(sV + oa, 16, 1024),
-                      smem_desc_sw128(sdO + b * L::kQ + ob, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                      smem_desc_sw128(sdO + st * L::kQ + ob, 16, 1024), idS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar + kBarSFull + 8 * b);
         if (i > 0) ok = issue_acc(i - 1);
@@ -302,10 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       tc_fence_before_sync();
       mbar_arrive(bar + kBarTFree + 8 * b);
-      if (!warp_wait(bar + kBarFull + 8 * b, ph, abort_flag, gst)) { ok = false; break; }
+      const int st = i % kStagesKV;
+      if (!warp_wait(bar + kBarFull + 8 * st, (i / kStagesKV) & 1, abort_flag, gst)) { ok = false; break; }
       const int q0 = (m0 + i % n_m) * 64 + g * 32;
-      const float *lse = reinterpret_cast<const float *>(smem + L::oL + b * 256) + g * 32;
-      const float *dlt = reinterpret_cast<const float *>(smem + L::oDl + b * 256) + g * 32;
+      const float *lse = reinterpret_cast<const float *>(smem + L::oL + st * 256) + g * 32;
+      const float *dlt = reinterpret_cast<const float *>(smem + L::oDl + st * 256) + g * 32;
       uint32_t wp[16], wd[16];
 #pragma unroll
       for (int c = 0; c < 32; c += 2) {
@@ -381,8 +394,8 @@ struct QLayout {
   static constexpr uint32_t kQ = 128u * D * 2;   // Q or dO: 128 rows
   static constexpr uint32_t kKV = 64u * D * 2;   // K or V tile: 64 rows
   static constexpr uint32_t kS = 128u * 128;     // dS: 128 queries x 64 keys
-  static constexpr uint32_t oQ = 0, odO = oQ + kQ, oK = odO + kQ, oV = oK + 2 * kKV,
-                            odS = oV + 2 * kKV, oBar = odS + 2 * kS;
+  static constexpr uint32_t oQ = 0, odO = oQ + kQ, oK = odO + kQ, oV = oK + kStagesQ * kKV,
+                            odS = oV + kStagesQ * kKV, oBar = odS + 2 * kS;
   static constexpr uint32_t kAlloc = oBar + 256 + 1024;
 };
 
@@ -441,21 +454,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int issued = -1;
       for (int i = 0; i < n_kv; ++i) {
-        const int b = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
-        if (!mbar_wait_bounded(bar + kBarEmpty + 8 * b, ph ^ 1, abort_flag, gst)) break;
-        mbar_arrive_expect_tx(bar + kBarFull + 8 * b, 2 * L::kKV);
+        const int st = i % kStagesQ;
+        const uint32_t ph = (i / kStagesQ) & 1;
+        if (!mbar_wait_bounded(bar + kBarEmpty + 8 * st, ph ^ 1, abort_flag, gst)) break;
+        mbar_arrive_expect_tx(bar + kBarFull + 8 * st, 2 * L::kKV);
         for (int c = 0; c < kCh; ++c) {
-          tma_load_4d(sK + b * L::kKV + c * 8192, &tmK, bar + kBarFull + 8 * b, c * 64, kl, i * 64, rb);
-          tma_load_4d(sV + b * L::kKV + c * 8192, &tmV, bar + kBarFull + 8 * b, c * 64, kl, i * 64, rb);
+          tma_load_4d(sK + st * L::kKV + c * 8192, &tmK, bar + kBarFull + 8 * st, c * 64, kl, i * 64, rb);
+          tma_load_4d(sV + st * L::kKV + c * 8192, &tmV, bar + kBarFull + 8 * st, c * 64, kl, i * 64, rb);
         }
         issued = i;
       }
       if (*abort_flag) {
         volatile int never = 0;
         mbar_wait_bounded(bar + kBarIn, 0, &never, nullptr, 500000000ull);
-        for (int i = issued - 1; i <= issued; ++i)
-          if (i >= 0) mbar_wait_bounded(bar + kBarFull + 8 * (i & 1), (i >> 1) & 1, &never, nullptr, 500000000ull);
+        for (int i = issued - (kStagesQ - 1); i <= issued; ++i)
+          if (i >= 0)
+            mbar_wait_bounded(bar + kBarFull + 8 * (i % kStagesQ), (i / kStagesQ) & 1, &never, nullptr,
+                              500000000ull);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -463,24 +478,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idS = idesc_bf16_f32(128, 64, 0, 0);  // S, dP: both operands K-major
       constexpr uint32_t idQ = idesc_bf16_f32(128, D, 0, 1);   // dQ: B (K tile) MN-major
       auto issue_dq = [&](int i) -> bool {
-        const int b = i & 1;
+        const int b = i & 1, st = i % kStagesQ;
         if (!mbar_wait_bounded(bar + kBarPFull + 8 * b, (i >> 1) & 1, abort_flag, gst)) return false;
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t a = smem_desc_sw128(sdS + b * L::kS + kk * 32, 16, 1024);
-          const uint64_t bb = smem_desc_sw128(sK + b * L::kKV + kk * 2048, 8192, 1024);
+          const uint64_t bb = smem_desc_sw128(sK + st * L::kKV + kk * 2048, 8192, 1024);
           mma_bf16_ss(tdQ, a, bb, idQ, (i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(bar + kBarPFree + 8 * b);
-        mma_commit(bar + kBarEmpty + 8 * b);
+        mma_commit(bar + kBarEmpty + 8 * st);
         return true;
       };
       bool ok = mbar_wait_bounded(bar + kBarIn, 0, abort_flag, gst);
       for (int i = 0; ok && i < n_kv; ++i) {
-        const int b = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
-        if (!mbar_wait_bounded(bar + kBarFull + 8 * b, ph, abort_flag, gst)) { ok = false; break; }
+        const int b = i & 1, st = i % kStagesQ;
+        if (!mbar_wait_bounded(bar + kBarFull + 8 * st, (i / kStagesQ) & 1, abort_flag, gst)) {
+          ok = false;
+          break;
+        }
         if (i >= 2 && !mbar_wait_bounded(bar + kBarTFree + 8 * b, ((i - 2) >> 1) & 1, abort_flag, gst)) {
           ok = false;
           break;
@@ -490,13 +507,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * 16384 + (kk & 3) * 32, ob = (kk >> 2) * 8192 + (kk & 3) * 32;
           mma_bf16_ss(tmem + b * 64, smem_desc_sw128(sQ + oa, 16, 1024),
-                      smem_desc_sw128(sK + b * L::kKV + ob, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                      smem_desc_sw128(sK + st * L::kKV + ob, 16, 1024), idS, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * 16384 + (kk & 3) * 32, ob = (kk >> 2) * 8192 + (kk & 3) * 32;
           mma_bf16_ss(tmem + 128 + b * 64, smem_desc_sw128(sdO + oa, 16, 1024),
-                      smem_desc_sw128(sV + b * L::kKV + ob, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                      smem_desc_sw128(sV + st * L::kKV + ob, 16, 1024), idS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar + kBarSFull + 8 * b);
         if (i > 0) ok = issue_dq(i - 1);
