@@ -50,7 +50,7 @@ struct BwdParams {
   int B, S, P, Sl, hp, kvp, group, causal;
   int n_head, n_kv;                    // global head counts (row widths of the seq layout)
   float scale, scale_log2;
-  const float *lse, *delta;            // [P][B][hp][S]
+  const float *nlse, *delta;           // [P][B][hp][S]; nlse = -lse * log2(e)
   const float *rope_cos, *rope_sin;    // [S][D/2], or null without RoPE
   __nv_bfloat16 *dq, *dk, *dv;         // sequence-sharded outputs
   uint32_t *status;                    // status word; the RoPE table key follows it
@@ -317,22 +317,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = i % kStagesKV;
       if (!warp_wait(bar + kBarFull + 8 * st, (i / kStagesKV) & 1, abort_flag, gst)) { ok = false; break; }
       const int q0 = (m0 + i % n_m) * 64 + g * 32;
-      const float *lse = reinterpret_cast<const float *>(smem + L::oL + st * 256) + g * 32;
-      const float *dlt = reinterpret_cast<const float *>(smem + L::oDl + st * 256) + g * 32;
+      const float4 *nl4 = reinterpret_cast<const float4 *>(smem + L::oL + st * 256) + g * 8;
+      const float4 *dl4 = reinterpret_cast<const float4 *>(smem + L::oDl + st * 256) + g * 8;
+      // Query q0 + c sees key kvr iff q0 + c >= kvr (causal) and q0 + c < S:
+      // columns [lo, hi) of this thread's 32 are valid.
+      const int lo = p.causal ? kvr - q0 : 0, hi = p.S - q0;
+      const bool full = __all_sync(0xffffffffu, lo <= 0 && hi >= 32);
       uint32_t wp[16], wd[16];
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        float pe[2], ds[2];
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 nl = nl4[c4], dl = dl4[c4];
+        const float nls[4] = {nl.x, nl.y, nl.z, nl.w}, dls[4] = {dl.x, dl.y, dl.z, dl.w};
+        float pe[4], ds[4];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int qi = q0 + c + h;
-          const bool valid = qi < p.S && (!p.causal || qi >= kvr);
-          const float x = fmaf(__uint_as_float(sr[c + h]), p.scale_log2, -lse[c + h] * kLog2e);
-          pe[h] = valid ? ex2(x) : 0.f;
-          ds[h] = pe[h] * (__uint_as_float(dr[c + h]) - dlt[c + h]);
+        for (int e = 0; e < 4; ++e) {
+          const int c = 4 * c4 + e;
+          pe[e] = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, nls[e]));
+          if (!full && (c < lo || c >= hi)) pe[e] = 0.f;
+          ds[e] = pe[e] * (__uint_as_float(dr[c]) - dls[e]);
         }
-        wp[c >> 1] = pack_bf16x2(pe[0], pe[1]);
-        wd[c >> 1] = pack_bf16x2(ds[0], ds[1]);
+        wp[2 * c4] = pack_bf16x2(pe[0], pe[1]);
+        wp[2 * c4 + 1] = pack_bf16x2(pe[2], pe[3]);
+        wd[2 * c4] = pack_bf16x2(ds[0], ds[1]);
+        wd[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
       }
       if (i >= 2 && !warp_wait(bar + kBarPFree + 8 * b, ((i - 2) >> 1) & 1, abort_flag, gst)) {
         ok = false;
@@ -531,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qi = m * 128 + r;
     const bool live = qi < p.S;
     const size_t lrow = ((size_t)rb * p.hp + j) * p.S + (live ? qi : 0);
-    const float nl2 = live ? -p.lse[lrow] * kLog2e : 0.f;
+    const float nl2 = live ? p.nlse[lrow] : 0.f;
     const float dlt = live ? p.delta[lrow] : 0.f;
     bool ok = true;
     for (int i = 0; i < n_kv; ++i) {
@@ -546,15 +553,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before_sync();
       mbar_arrive(bar + kBarTFree + 8 * b);
       const int k0 = i * 64 + g * 32;
+      // Key k0 + c is seen by query qi iff k0 + c <= qi (causal) and k0 + c < S:
+      // columns [0, hi) of this thread's 32 are valid.
+      const int hi = min(p.causal ? qi - k0 + 1 : 32, p.S - k0);
+      const bool full = __all_sync(0xffffffffu, hi >= 32);
       uint32_t wd[16];
 #pragma unroll
       for (int c = 0; c < 32; c += 2) {
         float ds[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int kv = k0 + c + h;
-          const bool valid = kv < p.S && (!p.causal || kv <= qi);
-          const float pe = valid ? ex2(fmaf(__uint_as_float(sr[c + h]), p.scale_log2, nl2)) : 0.f;
+          float pe = ex2(fmaf(__uint_as_float(sr[c + h]), p.scale_log2, nl2));
+          if (!full && c + h >= hi) pe = 0.f;
           ds[h] = pe * (__uint_as_float(dr[c + h]) - dlt);
         }
         wd[c >> 1] = pack_bf16x2(ds[0], ds[1]);
@@ -599,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void *q, const void *k,
-                     const void *v, const void *do_head, const float *lse, const float *delta,
+                     const void *v, const void *do_head, const float *nlse, const float *delta,
                      const void *ws, void *dq, void *dk, void *dv, uint32_t *status, cudaStream_t st) {
   const int hp = p.n_head / p.P, kvp = p.n_kv_head / p.P, PB = p.P * p.B;
   CUtensorMap mK128, mV128, mQ64, mdO64, mL, mDl, mQ128, mdO128, mK64, mV64;
@@ -607,7 +617,7 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
             make_act_map(enc, &mV128, v, D, kvp, p.S, PB, 128) &&
             make_act_map(enc, &mQ64, q, D, hp, p.S, PB, 64) &&
             make_act_map(enc, &mdO64, do_head, D, hp, p.S, PB, 64) &&
-            make_row_map(enc, &mL, lse, p.S, PB * hp, 64) &&
+            make_row_map(enc, &mL, nlse, p.S, PB * hp, 64) &&
             make_row_map(enc, &mDl, delta, p.S, PB * hp, 64) &&
             make_act_map(enc, &mQ128, q, D, hp, p.S, PB, 128) &&
             make_act_map(enc, &mdO128, do_head, D, hp, p.S, PB, 128) &&
@@ -627,7 +637,7 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   bp.n_kv = p.n_kv_head;
   bp.scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)D);
   bp.scale_log2 = bp.scale * kLog2e;
-  bp.lse = lse;
+  bp.nlse = nlse;
   bp.delta = delta;
   if (p.use_rope) {
     const WorkspaceLayout W = workspace_layout(p);
@@ -661,13 +671,13 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
 }  // namespace
 
 cudaError_t launch_attn_bwd_tc(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
-                               const void *k, const void *v, const void *do_head, const float *lse,
+                               const void *k, const void *v, const void *do_head, const float *nlse,
                                const float *delta, const void *ws, void *dq_seq, void *dk_seq,
                                void *dv_seq, uint32_t *status, cudaStream_t st) {
   if (p.head_dim == 128)
-    return launch_d<128>(p, enc, q, k, v, do_head, lse, delta, ws, dq_seq, dk_seq, dv_seq, status, st);
+    return launch_d<128>(p, enc, q, k, v, do_head, nlse, delta, ws, dq_seq, dk_seq, dv_seq, status, st);
   if (p.head_dim == 64)
-    return launch_d<64>(p, enc, q, k, v, do_head, lse, delta, ws, dq_seq, dk_seq, dv_seq, status, st);
+    return launch_d<64>(p, enc, q, k, v, do_head, nlse, delta, ws, dq_seq, dk_seq, dv_seq, status, st);
   return cudaErrorInvalidValue;
 }
 

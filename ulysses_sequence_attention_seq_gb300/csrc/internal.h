@@ -16,6 +16,7 @@ struct WorkspaceLayout {
   size_t status = 0;
   size_t rope = 0, rope_bytes = 0;    // float cos[S][D/2], then float sin[S][D/2]
   size_t delta = 0, delta_bytes = 0;  // float [P][B][hp][S]          (backward)
+  size_t nlse = 0, nlse_bytes = 0;    // float [P][B][hp][S], -lse*log2(e) (backward)
   size_t dohead = 0, dohead_bytes = 0;  // dO in head layout [P][B][S][hp][D] (backward)
   size_t total_fwd = 0, total_bwd = 0;
 };
@@ -33,9 +34,11 @@ cudaError_t launch_pack_qkv(const ulysses_problem &p, const void *q, const void 
                             void *qh, void *kh, void *vh, void *ws, cudaStream_t st);
 cudaError_t launch_unpack(const ulysses_problem &p, const void *o_head, void *o_seq,
                           cudaStream_t st);
-// dO seq -> head and delta[i] = sum_e dO[i][e] * O[i][e] per (rank, b, head, row).
+// dO seq -> head, delta[i] = sum_e dO[i][e] * O[i][e] and nlse[i] = -lse[i] * log2(e)
+// per (rank, b, head, row).
 cudaError_t launch_pack_do_delta(const ulysses_problem &p, const void *do_seq, const void *o_head,
-                                 void *do_head, float *delta, cudaStream_t st);
+                                 const float *lse, void *do_head, float *delta, float *nlse,
+                                 cudaStream_t st);
 
 // ---- attention kernels ----
 struct TmaEncoder {
@@ -54,7 +57,7 @@ cudaError_t launch_attn_fwd_tc(const ulysses_problem &p, const TmaEncoder &enc, 
                                uint32_t *status, cudaStream_t st);
 cudaError_t launch_attn_bwd_tc(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
                                const void *k, const void *v, const void *do_head,
-                               const float *lse, const float *delta, const void *ws,
+                               const float *nlse, const float *delta, const void *ws,
                                void *dq_seq, void *dk_seq, void *dv_seq, uint32_t *status,
                                cudaStream_t st);
 

@@ -177,11 +177,14 @@ __global__ void rope_table_kernel(float *cs, float *sn, int S, int D, double bas
   }
 }
 
-// dO: seq -> head, plus delta[d][b][j][pos] = sum_e dO * O (O read in head layout).
+// dO: seq -> head, plus delta[d][b][j][pos] = sum_e dO * O (O read in head layout)
+// and nlse = -lse * log2(e) at the same index (the exponent offset the backward
+// kernels add to scale * s * log2(e)).
 // A group of D/8 lanes owns one (token, head); bf16 only.
 __global__ void __launch_bounds__(kThreads)
     pack_do_delta_kernel(const __nv_bfloat16 *__restrict__ dout, const __nv_bfloat16 *__restrict__ o,
-                         __nv_bfloat16 *__restrict__ do_head, float *__restrict__ delta, int P, int B,
+                         const float *__restrict__ lse, __nv_bfloat16 *__restrict__ do_head,
+                         float *__restrict__ delta, float *__restrict__ nlse, int P, int B,
                          int Sl, int H, int D) {
   const int S = P * Sl, hp = H / P;
   const int lanes = D / 8;  // 8 or 16: divides 32
@@ -222,7 +225,11 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
     for (int off = lanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (live && c == 0) delta[((long long)(d * B + b) * hp + j) * S + pos] = acc;
+    if (live && c == 0) {
+      const long long idx = ((long long)(d * B + b) * hp + j) * S + pos;
+      delta[idx] = acc;
+      nlse[idx] = -lse[idx] * 1.4426950408889634f;
+    }
   }
 }
 
@@ -302,14 +309,16 @@ cudaError_t launch_unpack(const ulysses_problem &p, const void *o_head, void *o_
 }
 
 cudaError_t launch_pack_do_delta(const ulysses_problem &p, const void *do_seq, const void *o_head,
-                                 void *do_head, float *delta, cudaStream_t st) {
+                                 const float *lse, void *do_head, float *delta, float *nlse,
+                                 cudaStream_t st) {
   const long long groups = (long long)p.B * p.S * p.n_head;
   const int lanes = p.head_dim / 8;
   long long blocks = (groups * lanes + kThreads - 1) / kThreads;
   int grid = grid_for(blocks);
   pack_do_delta_kernel<<<grid, kThreads, 0, st>>>(
       static_cast<const __nv_bfloat16 *>(do_seq), static_cast<const __nv_bfloat16 *>(o_head),
-      static_cast<__nv_bfloat16 *>(do_head), delta, p.P, p.B, p.S / p.P, p.n_head, p.head_dim);
+      lse, static_cast<__nv_bfloat16 *>(do_head), delta, nlse, p.P, p.B, p.S / p.P, p.n_head,
+      p.head_dim);
   return cudaGetLastError();
 }
 

@@ -26,7 +26,9 @@ WorkspaceLayout workspace_layout(const ulysses_problem &p) {
   L.total_fwd = align256(L.rope + L.rope_bytes);
   L.delta = L.total_fwd;
   L.delta_bytes = (size_t)p.B * p.n_head * p.S * 4;
-  L.dohead = align256(L.delta + L.delta_bytes);
+  L.nlse = align256(L.delta + L.delta_bytes);
+  L.nlse_bytes = L.delta_bytes;
+  L.dohead = align256(L.nlse + L.nlse_bytes);
   L.dohead_bytes = (size_t)p.B * p.S * p.n_head * p.head_dim * es;
   L.total_bwd = align256(L.dohead + L.dohead_bytes);
   return L;
@@ -233,11 +235,12 @@ int ulysses_attn_bwd(const ulysses_problem *prob, const void *q_head, const void
   const WorkspaceLayout L = workspace_layout(p);
   uint8_t *w = static_cast<uint8_t *>(ws);
   float *delta = reinterpret_cast<float *>(w + L.delta);
+  float *nlse = reinterpret_cast<float *>(w + L.nlse);
   void *do_head = w + L.dohead;
   cudaStream_t st = (cudaStream_t)stream;
-  cudaError_t e = launch_pack_do_delta(p, do_seq, o_head, do_head, delta, st);
+  cudaError_t e = launch_pack_do_delta(p, do_seq, o_head, lse, do_head, delta, nlse, st);
   if (e == cudaSuccess)
-    e = launch_attn_bwd_tc(p, enc, q_head, k_head, v_head, do_head, lse, delta, ws, dq_seq, dk_seq,
+    e = launch_attn_bwd_tc(p, enc, q_head, k_head, v_head, do_head, nlse, delta, ws, dq_seq, dk_seq,
                            dv_seq, reinterpret_cast<uint32_t *>(w + L.status), st);
   return cuda_rc(e);
 }
