@@ -73,8 +73,8 @@ enum : uint32_t {
   kBarFull = 8,     // [kMaxStages] streamed operands loaded
   kBarEmpty = 40,   // [kMaxStages] streamed operands consumed
   kBarSFull = 72,   // [2] score / dP MMAs done
-  kBarTFree = 88,   // [2] TMEM score buffers read (256 arrivals)
-  kBarPFull = 104,  // [2] P / dS written to shared memory (256 arrivals)
+  kBarTFree = 88,   // [2] TMEM score buffers read (128 arrivals: one warpgroup)
+  kBarPFull = 104,  // [2] P / dS written to shared memory (128 arrivals)
   kBarPFree = 120,  // [2] accumulating MMAs that read P / dS done
   kBarAcc = 136,    // all accumulation done
   kBarDrain = 144,
@@ -96,8 +96,8 @@ __device__ __forceinline__ void init_barriers(uint32_t bar) {
   }
   for (int i = 0; i < 2; ++i) {
     mbar_init(bar + kBarSFull + 8 * i, 1);
-    mbar_init(bar + kBarTFree + 8 * i, 256);
-    mbar_init(bar + kBarPFull + 8 * i, 256);
+    mbar_init(bar + kBarTFree + 8 * i, 128);
+    mbar_init(bar + kBarPFull + 8 * i, 128);
     mbar_init(bar + kBarPFree + 8 * i, 1);
   }
   mbar_init(bar + kBarAcc, 1);
@@ -298,57 +298,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------- softmax warps (0..7)
+    // Warpgroup g takes the steps i with i % 2 == g (TMEM and P/dS buffer g),
+    // all 64 query columns, in two halves: the two warpgroups' chains of TMEM
+    // load -> exponentials -> shared-memory store -> barrier overlap.
     const int g = warp >> 2, w4 = warp & 3;
     const int r = w4 * 32 + lane;  // key row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)(w4 * 32) << 16;
     const int kvr = n * 128 + r;
     bool ok = true;
-    for (int i = 0; i < n_iter; ++i) {
-      const int b = i & 1;
+    for (int i = g; i < n_iter; i += 2) {
+      const int b = g;
       const uint32_t ph = (i >> 1) & 1;
       if (!warp_wait(bar + kBarSFull + 8 * b, ph, abort_flag, gst)) { ok = false; break; }
       tc_fence_after_sync();
-      uint32_t sr[32], dr[32];
-      tmem_ld32(tmem + lane_base + b * 64 + g * 32, sr);
-      tmem_ld32(tmem + lane_base + 128 + b * 64 + g * 32, dr);
-      tmem_wait_ld();
-      tc_fence_before_sync();
-      mbar_arrive(bar + kBarTFree + 8 * b);
       const int st = i % kStagesKV;
       if (!warp_wait(bar + kBarFull + 8 * st, (i / kStagesKV) & 1, abort_flag, gst)) { ok = false; break; }
-      const int q0 = (m0 + i % n_m) * 64 + g * 32;
-      const float4 *nl4 = reinterpret_cast<const float4 *>(smem + L::oL + st * 256) + g * 8;
-      const float4 *dl4 = reinterpret_cast<const float4 *>(smem + L::oDl + st * 256) + g * 8;
-      // Query q0 + c sees key kvr iff q0 + c >= kvr (causal) and q0 + c < S:
-      // columns [lo, hi) of this thread's 32 are valid.
-      const int lo = p.causal ? kvr - q0 : 0, hi = p.S - q0;
-      const bool full = __all_sync(0xffffffffu, lo <= 0 && hi >= 32);
-      uint32_t wp[16], wd[16];
-#pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 nl = nl4[c4], dl = dl4[c4];
-        const float nls[4] = {nl.x, nl.y, nl.z, nl.w}, dls[4] = {dl.x, dl.y, dl.z, dl.w};
-        float pe[4], ds[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = 4 * c4 + e;
-          pe[e] = ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, nls[e]));
-          if (!full && (c < lo || c >= hi)) pe[e] = 0.f;
-          ds[e] = pe[e] * (__uint_as_float(dr[c]) - dls[e]);
-        }
-        wp[2 * c4] = pack_bf16x2(pe[0], pe[1]);
-        wp[2 * c4 + 1] = pack_bf16x2(pe[2], pe[3]);
-        wd[2 * c4] = pack_bf16x2(ds[0], ds[1]);
-        wd[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
-      }
+      // The S^T/dP^T commit of step i also covers the dV/dK MMAs of step i-2,
+      // so P/dS buffer b is free; the wait below is then immediate.
       if (i >= 2 && !warp_wait(bar + kBarPFree + 8 * b, ((i - 2) >> 1) & 1, abort_flag, gst)) {
         ok = false;
         break;
       }
-      st_row_units(sP + b * L::kPS, r, g * 4, wp);
-      st_row_units(sdS + b * L::kPS, r, g * 4, wd);
+      const int q0 = (m0 + i % n_m) * 64;
+      // Query q0 + c sees key kvr iff q0 + c >= kvr (causal) and q0 + c < S:
+      // columns [lo, hi) of the 64 are valid.
+      const int lo = p.causal ? kvr - q0 : 0, hi = p.S - q0;
+      const bool full = __all_sync(0xffffffffu, lo <= 0 && hi >= 64);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tmem + lane_base + b * 64 + h * 32, sr);
+        tmem_ld32(tmem + lane_base + 128 + b * 64 + h * 32, dr);
+        tmem_wait_ld();
+        const float4 *nl4 = reinterpret_cast<const float4 *>(smem + L::oL + st * 256) + h * 8;
+        const float4 *dl4 = reinterpret_cast<const float4 *>(smem + L::oDl + st * 256) + h * 8;
+        uint32_t wp[16], wd[16];
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 nl = nl4[c4], dl = dl4[c4];
+          const float nls[4] = {nl.x, nl.y, nl.z, nl.w}, dls[4] = {dl.x, dl.y, dl.z, dl.w};
+          float pe[4], ds[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = h * 32 + 4 * c4 + e;
+            pe[e] = ex2(fmaf(__uint_as_float(sr[4 * c4 + e]), p.scale_log2, nls[e]));
+            if (!full && (c < lo || c >= hi)) pe[e] = 0.f;
+            ds[e] = pe[e] * (__uint_as_float(dr[4 * c4 + e]) - dls[e]);
+          }
+          wp[2 * c4] = pack_bf16x2(pe[0], pe[1]);
+          wp[2 * c4 + 1] = pack_bf16x2(pe[2], pe[3]);
+          wd[2 * c4] = pack_bf16x2(ds[0], ds[1]);
+          wd[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
+        }
+        st_row_units(sP + b * L::kPS, r, h * 4, wp);
+        st_row_units(sdS + b * L::kPS, r, h * 4, wd);
+      }
       fence_proxy_async_smem();
       tc_fence_before_sync();
+      mbar_arrive(bar + kBarTFree + 8 * b);
       mbar_arrive(bar + kBarPFull + 8 * b);
     }
     // ------------------------------------------------------------ epilogue
@@ -541,41 +548,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float nl2 = live ? p.nlse[lrow] : 0.f;
     const float dlt = live ? p.delta[lrow] : 0.f;
     bool ok = true;
-    for (int i = 0; i < n_kv; ++i) {
-      const int b = i & 1;
+    // Warpgroup g takes the key tiles i with i % 2 == g (TMEM and dS buffer g),
+    // all 64 key columns, in two halves, so the two warpgroups' chains overlap.
+    for (int i = g; i < n_kv; i += 2) {
+      const int b = g;
       const uint32_t ph = (i >> 1) & 1;
       if (!warp_wait(bar + kBarSFull + 8 * b, ph, abort_flag, gst)) { ok = false; break; }
       tc_fence_after_sync();
-      uint32_t sr[32], dr[32];
-      tmem_ld32(tmem + lane_base + b * 64 + g * 32, sr);
-      tmem_ld32(tmem + lane_base + 128 + b * 64 + g * 32, dr);
-      tmem_wait_ld();
-      tc_fence_before_sync();
-      mbar_arrive(bar + kBarTFree + 8 * b);
-      const int k0 = i * 64 + g * 32;
-      // Key k0 + c is seen by query qi iff k0 + c <= qi (causal) and k0 + c < S:
-      // columns [0, hi) of this thread's 32 are valid.
-      const int hi = min(p.causal ? qi - k0 + 1 : 32, p.S - k0);
-      const bool full = __all_sync(0xffffffffu, hi >= 32);
-      uint32_t wd[16];
-#pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        float ds[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float pe = ex2(fmaf(__uint_as_float(sr[c + h]), p.scale_log2, nl2));
-          if (!full && c + h >= hi) pe = 0.f;
-          ds[h] = pe * (__uint_as_float(dr[c + h]) - dlt);
-        }
-        wd[c >> 1] = pack_bf16x2(ds[0], ds[1]);
-      }
+      // The S/dP commit of tile i also covers the dQ MMA of tile i-2, so dS
+      // buffer b is free; the wait below is then immediate.
       if (i >= 2 && !warp_wait(bar + kBarPFree + 8 * b, ((i - 2) >> 1) & 1, abort_flag, gst)) {
         ok = false;
         break;
       }
-      st_row_units(sdS + b * L::kS, r, g * 4, wd);
+      const int k0 = i * 64;
+      // Key k0 + c is seen by query qi iff k0 + c <= qi (causal) and k0 + c < S:
+      // columns [0, hi) of the 64 are valid.
+      const int hi = min(p.causal ? qi - k0 + 1 : 64, p.S - k0);
+      const bool full = __all_sync(0xffffffffu, hi >= 64);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tmem + lane_base + b * 64 + h * 32, sr);
+        tmem_ld32(tmem + lane_base + 128 + b * 64 + h * 32, dr);
+        tmem_wait_ld();
+        uint32_t wd[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float ds[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float pe = ex2(fmaf(__uint_as_float(sr[c + e]), p.scale_log2, nl2));
+            if (!full && h * 32 + c + e >= hi) pe = 0.f;
+            ds[e] = pe * (__uint_as_float(dr[c + e]) - dlt);
+          }
+          wd[c >> 1] = pack_bf16x2(ds[0], ds[1]);
+        }
+        st_row_units(sdS + b * L::kS, r, h * 4, wd);
+      }
       fence_proxy_async_smem();
       tc_fence_before_sync();
+      mbar_arrive(bar + kBarTFree + 8 * b);
       mbar_arrive(bar + kBarPFull + 8 * b);
     }
     if (ok) ok = warp_wait(bar + kBarAcc, 0, abort_flag, gst);
