@@ -42,6 +42,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep in hardware until the phase
+// completes or about `hint_ns` nanoseconds pass, instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -59,19 +73,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   const volatile uint32_t *gstatus = nullptr,
                                                   uint64_t limit_ns = 2000000000ull) {
   if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (gstatus && (*gstatus & 3u) != 0u) {  // a timeout bit of the status word
-        *abort_flag = 1;
-        return false;
-      }
-      if (globaltimer_ns() - t0 > limit_ns) {
-        *abort_flag = 1;
-        return false;
-      }
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    // Sleeps until the phase completes (or ~1 us), so waiting warps do not
+    // take issue slots from the warps doing the work.
+    if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
+    if (*abort_flag) return false;
+    if (gstatus && (*gstatus & 3u) != 0u) {  // a timeout bit of the status word
+      *abort_flag = 1;
+      return false;
+    }
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      return false;
     }
   }
 }
