@@ -215,9 +215,37 @@ def run_ulysses(args, w, rank, world):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
+    # ---- folded forward (pack + attention + unpack in one kernel) vs the three
+    # calls, same shapes with RoPE off (the folded path needs pre-rotated q, k)
+    folded = None
+    if w.dtype == "bf16" and w.Sl % 128 == 0:
+        import dataclasses
+        pf = dataclasses.replace(prob, use_rope=False)
+
+        def three():
+            U.ulysses_pack_qkv(pf, buf.q_seq, buf.k_seq, buf.v_seq, buf.q_head, buf.k_head, buf.v_head, buf.ws)
+            U.ulysses_attn_fwd(pf, buf.q_head, buf.k_head, buf.v_head, buf.o_head, buf.lse, buf.ws)
+            U.ulysses_unpack_out(pf, buf.o_head, buf.o_seq)
+
+        def fold():
+            U.ulysses_attn_fwd_folded(pf, buf.q_seq, buf.k_seq, buf.v_seq, buf.o_seq, buf.lse, buf.ws)
+
+        times = {}
+        for name, fn in (("unfolded_ms", three), ("ms", fold)):
+            for _ in range(2):
+                fn()
+            a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(args.steps):
+                fn()
+            b2.record(stream)
+            torch.cuda.synchronize()
+            times[name] = a.elapsed_time(b2) / args.steps
+        folded = dict(times, workload=f"{w.name} shapes, RoPE off (q and k rotated by their producer)")
     status = U.ulysses_read_status(buf.ws)
     return dict(total_ms=total_ms, per=per, clocks=clk, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
-                launches=launches_per_step * args.steps, status=status, backward=backward)
+                launches=launches_per_step * args.steps, status=status, backward=backward,
+                folded=folded)
 
 
 def barrier(world):
@@ -381,6 +409,7 @@ def main():
         "e2e": {"value": job_throughput(tokens, e2e_ms * 1e-3, world), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": r["launches"],
+        "folded_fwd": r["folded"],
         "device_status": r["status"],
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -142,6 +142,24 @@ int ulysses_attn_fwd(const ulysses_problem *prob, const void *q_head, const void
                      ulysses_stream_t stream);
 
 /*
+ * Folded forward: pack, attention and unpack in one kernel, with both
+ * All-to-Alls turned into addressing ("Sequence Parallelism II", §1: the
+ * All-to-All is a distributed transpose of ownership).  The tensor-core kernel
+ * reads the 128-row tiles of rank r's heads straight out of the
+ * sequence-sharded buffers (the tile at global position p comes from rank
+ * p/Sl, row p%Sl) and writes O straight into sequence layout.  Results are
+ * identical to ulysses_pack_qkv + ulysses_attn_fwd + ulysses_unpack_out.
+ * q_seq [P][B][Sl][n_head][D], k_seq/v_seq [P][B][Sl][n_kv_head][D] ->
+ * o_seq [P][B][Sl][H], lse [P][B][hp][S] float.
+ * Requires bf16, head_dim 64 or 128, use_rope == 0 (q and k must already be
+ * rotated by their producer) and S/P a multiple of 128, else
+ * ULYSSES_ERR_UNSUPPORTED.  `ws` (phase 0) carries the status word.
+ */
+int ulysses_attn_fwd_folded(const ulysses_problem *prob, const void *q_seq, const void *k_seq,
+                            const void *v_seq, void *o_seq, float *lse, void *ws, size_t ws_bytes,
+                            ulysses_stream_t stream);
+
+/*
  * Head -> seq All-to-All of the attention output ("Sequence Parallelism II",
  * §2 fifth step; "Comparing Ulysses and Megatron Sequence Parallelism",
  * "DeepSpeed Attention": [B,S,heads/P,D] back to [B,S/P,heads,D] = [B,S/P,H]):

@@ -1,0 +1,73 @@
+"""Folded forward (ulysses_attn_fwd_folded): the attention kernel reads the
+sequence-sharded Q/K/V directly and writes O in sequence layout, so both
+All-to-Alls become addressing.  It must reproduce pack -> attention -> unpack
+bit for bit, and the fp64 oracle within the bf16 tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from pathcheck import GpuRun, LSE_BF16_MAX_ABS, assert_close, oracle_inputs, oracle_problem, to64
+from test_gpu_forward import wl
+from ulysses_sequence_attention_seq_gb300 import binding as U
+from ulysses_sequence_attention_seq_gb300.synthetic import WORKLOADS
+
+pytestmark = pytest.mark.gpu
+
+CASES = [wl(2, 1, 512, 4, 2, 128, rope=False),          # Sl = 256, GQA
+         wl(4, 2, 1024, 8, 8, 64, rope=False),          # D = 64, B = 2
+         wl(8, 1, 2048, 32, 8, 128, rope=False),        # the GQA workload's head layout
+         wl(2, 1, 256, 4, 4, 128, causal=False, rope=False),   # Sl = 128, non-causal
+         wl(4, 1, 1536, 4, 4, 128, rope=False)]         # odd number of 128-row tiles
+
+
+def _folded(run):
+    b = run.buf
+    o = torch.full_like(b.o_seq, float("nan"))
+    lse = torch.full_like(b.lse, float("nan"))
+    U.ulysses_attn_fwd_folded(run.prob, b.q_seq, b.k_seq, b.v_seq, o, lse, b.ws)
+    torch.cuda.synchronize()
+    assert U.ulysses_read_status(b.ws) == 0
+    return o, lse
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: f"P{w.P}B{w.B}S{w.S}h{w.n_head}kv{w.n_kv_head}D{w.head_dim}{'c' if w.causal else 'n'}")
+def test_folded_equals_pack_attend_unpack_bit_exact(w):
+    run = GpuRun(w)
+    run.forward()
+    o, lse = _folded(run)
+    assert torch.equal(o, run.buf.o_seq)
+    assert torch.equal(lse, run.buf.lse)
+
+
+def test_folded_matches_oracle():
+    w = CASES[0]
+    run = GpuRun(w)
+    o, lse = _folded(run)
+    x = oracle_inputs(run.inputs)
+    want = oracle.forward(oracle_problem(w), x["q"], x["k"], x["v"])
+    assert_close(to64(o), np.stack([a.reshape(w.B, w.Sl, -1) for a in want["o_seq"]]), w, "folded o_seq")
+    assert np.abs(to64(lse) - np.stack(want["lse"])).max() <= LSE_BF16_MAX_ABS
+
+
+def test_folded_full_size_pages_sizing_without_rope():
+    """The pages' sizing (P=8, S=32768, 32 heads, D=128) with pre-rotated q/k."""
+    w = WORKLOADS["C4"].with_(use_rope=False)
+    run = GpuRun(w)
+    run.forward()
+    o, lse = _folded(run)
+    assert torch.equal(o, run.buf.o_seq)
+    assert torch.equal(lse, run.buf.lse)
+
+
+def test_folded_refuses_what_it_cannot_fold():
+    run = GpuRun(wl(2, 1, 512, 4, 2, 128, rope=True))
+    b = run.buf
+    with pytest.raises(U.UlyssesError) as e:      # RoPE must be applied by the producer
+        U.ulysses_attn_fwd_folded(run.prob, b.q_seq, b.k_seq, b.v_seq, b.o_seq, b.lse, b.ws)
+    assert e.value.code == -4
+    run = GpuRun(wl(2, 1, 200, 4, 2, 128, rope=False))   # Sl = 100: tiles would straddle ranks
+    b = run.buf
+    with pytest.raises(U.UlyssesError) as e:
+        U.ulysses_attn_fwd_folded(run.prob, b.q_seq, b.k_seq, b.v_seq, b.o_seq, b.lse, b.ws)
+    assert e.value.code == -4

@@ -25,7 +25,7 @@ STATUS_FWD_TIMEOUT, STATUS_BWD_TIMEOUT, STATUS_ROPE_TABLE = 1, 2, 4
 
 EXPORTS = ("ulysses_validate", "ulysses_workspace_bytes", "ulysses_workspace_init",
            "ulysses_read_status", "ulysses_pack_qkv", "ulysses_attn_fwd", "ulysses_unpack_out",
-           "ulysses_attn_bwd", "ulysses_status_string")
+           "ulysses_attn_bwd", "ulysses_attn_fwd_folded", "ulysses_status_string")
 
 
 class UlyssesError(RuntimeError):
@@ -106,6 +106,7 @@ def lib():
         L.ulysses_pack_qkv.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_attn_fwd.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_unpack_out.argtypes = [P, vp, vp, vp]
+        L.ulysses_attn_fwd_folded.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_attn_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_attn_bwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.ulysses_status_string.argtypes = [ctypes.c_int]
@@ -161,6 +162,12 @@ def ulysses_pack_qkv(prob, q_seq, k_seq, v_seq, q_head, k_head, v_head, ws, stre
 def ulysses_attn_fwd(prob, q_head, k_head, v_head, o_head, lse, ws, stream=None):
     _check("ulysses_attn_fwd", lib().ulysses_attn_fwd(
         ctypes.byref(prob.c()), _ptr(q_head), _ptr(k_head), _ptr(v_head), _ptr(o_head), _ptr(lse),
+        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def ulysses_attn_fwd_folded(prob, q_seq, k_seq, v_seq, o_seq, lse, ws, stream=None):
+    _check("ulysses_attn_fwd_folded", lib().ulysses_attn_fwd_folded(
+        ctypes.byref(prob.c()), _ptr(q_seq), _ptr(k_seq), _ptr(v_seq), _ptr(o_seq), _ptr(lse),
         _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 

@@ -87,11 +87,28 @@ enum : uint32_t {
 
 struct FwdParams {
   int B, S, P, hp, kvp, group, causal, n_pairs;
+  // Folded addressing: the tensor maps cover the sequence-sharded buffers
+  // [P][B][Sl][heads][D] and O is written in sequence layout [P][B][Sl][H]
+  // (the two All-to-Alls become addressing).  Needs Sl % 128 == 0 so a tile
+  // never straddles two ranks' shards.
+  int folded, Sl, n_head, n_kv_head;
   float scale_log2;
-  __nv_bfloat16 *o;  // [P][B][S][hp][D]
+  __nv_bfloat16 *o;  // [P][B][S][hp][D], or [P][B][Sl][H] when folded
   float *lse;        // [P][B][hp][S]
   uint32_t *status;
 };
+
+// TMA coordinates (head, row, rank*B+batch) of the 128-row tile starting at
+// global position `pos` of local head `lh` on rank `r` (rb = r*B + b).
+struct TileCoord {
+  int head, row, outer;
+};
+__device__ __forceinline__ TileCoord tile_coord(const FwdParams &p, int rb, int lh, int heads_local,
+                                                int pos) {
+  if (!p.folded) return {lh, pos, rb};
+  const int r = rb / p.B, b = rb - r * p.B, src = pos / p.Sl;
+  return {r * heads_local + lh, pos - src * p.Sl, src * p.B + b};
+}
 
 // Position in the K/V ring of the n-th tile streamed (K_j is n = 2j, V_j is 2j+1).
 __device__ __forceinline__ uint32_t ring_slot(int n) { return (uint32_t)(n % kSlots); }
@@ -162,10 +179,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         mbar_arrive_expect_tx(bar + kBarQFull, 2 * L::kTile);
-        for (int x = 0; x < 2; ++x)
+        for (int x = 0; x < 2; ++x) {
+          const TileCoord tq = tile_coord(p, rb, j, p.hp, qp * 2 * BM + x * BM);
           for (int c = 0; c < kChunks; ++c)
-            tma_load_4d(sQ + x * L::kTile + c * kChunkBytes, &tmQ, bar + kBarQFull, c * 64, j,
-                        qp * 2 * BM + x * BM, rb);
+            tma_load_4d(sQ + x * L::kTile + c * kChunkBytes, &tmQ, bar + kBarQFull, c * 64, tq.head,
+                        tq.row, tq.outer);
+        }
         int issued = -1;
         for (int n = 0; n < 2 * nB; ++n) {
           const uint32_t slot = ring_slot(n);
@@ -173,9 +192,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           mbar_arrive_expect_tx(bar + kBarKVFull + 8 * slot, L::kTile);
           const CUtensorMap *m = (n & 1) ? &tmV : &tmK;
+          const TileCoord tk = tile_coord(p, rb, kl, p.kvp, (n >> 1) * BN);
           for (int c = 0; c < kChunks; ++c)
             tma_load_4d(sKV + slot * L::kTile + c * kChunkBytes, m, bar + kBarKVFull + 8 * slot,
-                        c * 64, kl, (n >> 1) * BN, rb);
+                        c * 64, tk.head, tk.row, tk.outer);
           issued = n;
         }
         if (*abort_flag) {
@@ -344,7 +364,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after_sync();
       const float inv = 1.0f / l;
-      __nv_bfloat16 *orow = p.o + (((size_t)rb * p.S + qpos) * p.hp + j) * D;
+      __nv_bfloat16 *orow;
+      if (!p.folded) {
+        orow = p.o + (((size_t)rb * p.S + qpos) * p.hp + j) * D;
+      } else {  // token qpos of rank qpos/Sl, global head r*hp + j
+        const int r = rb / p.B, b = rb - r * p.B, dst = qpos / p.Sl;
+        orow = p.o + (((size_t)(dst * p.B + b) * p.Sl + (qpos - dst * p.Sl)) * p.n_head + r * p.hp + j) * D;
+      }
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
@@ -378,11 +404,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void *q, const void *k,
-                     const void *v, void *o, float *lse, uint32_t *status, cudaStream_t st) {
-  const int hp = p.n_head / p.P, kvp = p.n_kv_head / p.P, PB = p.P * p.B;
+                     const void *v, void *o, float *lse, uint32_t *status, bool folded, cudaStream_t st) {
+  const int hp = p.n_head / p.P, kvp = p.n_kv_head / p.P, PB = p.P * p.B, Sl = p.S / p.P;
   CUtensorMap mq, mk, mv;
-  if (!make_act_map(enc, &mq, q, D, hp, p.S, PB, 128) || !make_act_map(enc, &mk, k, D, kvp, p.S, PB, 128) ||
-      !make_act_map(enc, &mv, v, D, kvp, p.S, PB, 128))
+  // head-sharded maps: [P*B][S][hp|kvp][D]; folded maps: [P*B][Sl][n_head|n_kv_head][D]
+  const int rows = folded ? Sl : p.S;
+  if (!make_act_map(enc, &mq, q, D, folded ? p.n_head : hp, rows, PB, 128) ||
+      !make_act_map(enc, &mk, k, D, folded ? p.n_kv_head : kvp, rows, PB, 128) ||
+      !make_act_map(enc, &mv, v, D, folded ? p.n_kv_head : kvp, rows, PB, 128))
     return cudaErrorInvalidValue;
   FwdParams fp;
   fp.B = p.B;
@@ -393,6 +422,10 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   fp.group = hp / kvp;
   fp.causal = p.causal;
   fp.n_pairs = (p.S + 2 * BM - 1) / (2 * BM);
+  fp.folded = folded ? 1 : 0;
+  fp.Sl = Sl;
+  fp.n_head = p.n_head;
+  fp.n_kv_head = p.n_kv_head;
   const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)D);
   fp.scale_log2 = scale * 1.4426950408889634f;
   fp.o = static_cast<__nv_bfloat16 *>(o);
@@ -411,9 +444,9 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
 
 cudaError_t launch_attn_fwd_tc(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
                                const void *k, const void *v, void *o, float *lse, uint32_t *status,
-                               cudaStream_t st) {
-  if (p.head_dim == 128) return launch_d<128>(p, enc, q, k, v, o, lse, status, st);
-  if (p.head_dim == 64) return launch_d<64>(p, enc, q, k, v, o, lse, status, st);
+                               bool folded, cudaStream_t st) {
+  if (p.head_dim == 128) return launch_d<128>(p, enc, q, k, v, o, lse, status, folded, st);
+  if (p.head_dim == 64) return launch_d<64>(p, enc, q, k, v, o, lse, status, folded, st);
   return cudaErrorInvalidValue;
 }
 

@@ -52,9 +52,11 @@ bool get_tma_encoder(TmaEncoder *enc);
 
 cudaError_t launch_attn_fwd_simt(const ulysses_problem &p, const float *q, const float *k,
                                  const float *v, float *o, float *lse, cudaStream_t st);
+// folded: q/k/v are the sequence-sharded buffers and o is written in sequence
+// layout (requires S/P % 128 == 0).
 cudaError_t launch_attn_fwd_tc(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
                                const void *k, const void *v, void *o, float *lse,
-                               uint32_t *status, cudaStream_t st);
+                               uint32_t *status, bool folded, cudaStream_t st);
 cudaError_t launch_attn_bwd_tc(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
                                const void *k, const void *v, const void *do_head,
                                const float *nlse, const float *delta, const void *ws,

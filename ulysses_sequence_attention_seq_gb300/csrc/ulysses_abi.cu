@@ -199,8 +199,29 @@ int ulysses_attn_fwd(const ulysses_problem *prob, const void *q_head, const void
                                         static_cast<float *>(o_head), lse, (cudaStream_t)stream));
   TmaEncoder enc;
   if (!get_tma_encoder(&enc)) return ULYSSES_ERR_CUDA;
-  return cuda_rc(launch_attn_fwd_tc(p, enc, q_head, k_head, v_head, o_head, lse, status,
+  return cuda_rc(launch_attn_fwd_tc(p, enc, q_head, k_head, v_head, o_head, lse, status, false,
                                     (cudaStream_t)stream));
+}
+
+int ulysses_attn_fwd_folded(const ulysses_problem *prob, const void *q_seq, const void *k_seq,
+                            const void *v_seq, void *o_seq, float *lse, void *ws, size_t ws_bytes,
+                            ulysses_stream_t stream) {
+  int rc = ulysses_validate(prob);
+  if (rc) return rc;
+  const ulysses_problem &p = *prob;
+  if (p.dtype != ULYSSES_BF16 || (p.head_dim != 64 && p.head_dim != 128) || p.use_rope ||
+      (p.S / p.P) % 128 != 0)
+    return ULYSSES_ERR_UNSUPPORTED;
+  const size_t nq = act_bytes(p, p.n_head), nk = act_bytes(p, p.n_kv_head);
+  const size_t nl = (size_t)p.B * p.n_head * p.S * sizeof(float);
+  const Span in[3] = {{q_seq, nq}, {k_seq, nk}, {v_seq, nk}};
+  const Span out[3] = {{o_seq, nq}, {lse, nl}, {ws, ws_bytes}};
+  if ((rc = check_ws(p, ws, ws_bytes, 0))) return rc;
+  if ((rc = check_spans(in, 3, out, 3))) return rc;
+  TmaEncoder enc;
+  if (!get_tma_encoder(&enc)) return ULYSSES_ERR_CUDA;
+  return cuda_rc(launch_attn_fwd_tc(p, enc, q_seq, k_seq, v_seq, o_seq, lse, static_cast<uint32_t *>(ws),
+                                    true, (cudaStream_t)stream));
 }
 
 int ulysses_unpack_out(const ulysses_problem *prob, const void *o_head, void *o_seq,
