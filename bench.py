@@ -329,6 +329,53 @@ class OracleBench:
                 f"scaled to the full causal triangle by query-key pairs")
 
 
+def run_sweep(args):
+    """Permutation alone at the head-count bound (P=32, one head per virtual
+    rank, 32 heads, D=128, bf16), S = 4K..128K, RoPE on and off: median time
+    of the seq->head pack of Q, K, V and of the head->seq unpack of O, with a
+    512 MiB L2 flush before every timed launch.  Prints one JSON line."""
+    from ulysses_sequence_attention_seq_gb300 import binding as U
+    from ulysses_sequence_attention_seq_gb300.synthetic import SWEEP_S
+    hbm = load_peaks()[0]
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1005)
+    out = []
+    for S in SWEEP_S:
+        for rope in (True, False):
+            prob = U.Problem(B=1, S=S, hidden=4096, n_head=32, n_kv_head=32, head_dim=128, P=32,
+                             use_rope=rope)
+            buf = U.Buffers(prob, device=dev)
+            for t in (buf.q_seq, buf.k_seq, buf.v_seq, buf.o_head):
+                t.copy_(torch.randn(t.shape, generator=gen, device=dev, dtype=torch.float32))
+            U.ulysses_workspace_init(prob, buf.ws)
+            res = {}
+            for name, fn in (("pack", lambda: U.ulysses_pack_qkv(prob, buf.q_seq, buf.k_seq, buf.v_seq, buf.q_head,
+                                                                 buf.k_head, buf.v_head, buf.ws)),
+                             ("unpack", lambda: U.ulysses_unpack_out(prob, buf.o_head, buf.o_seq))):
+                if name == "unpack" and not rope:
+                    continue  # the unpack has no RoPE; timed once per S
+                ts = []
+                for it in range(args.warmup + args.steps):
+                    flush.fill_(it & 255)
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    fn()
+                    b.record()
+                    torch.cuda.synchronize()
+                    if it >= args.warmup:
+                        ts.append(a.elapsed_time(b))
+                ms = statistics.median(ts)
+                nbytes = (3 if name == "pack" else 1) * 2 * S * 4096 * 2
+                res[name] = {"ms": ms, "GB/s": nbytes / (ms * 1e-3) / 1e9, "frac_of_measured_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm,
+                             "bytes": nbytes}
+            assert U.ulysses_read_status(buf.ws) == 0
+            out.append({"S": S, "rope": rope, **res})
+            del buf
+    print(json.dumps({"sweep": "permute P=32 B=1 heads=32 D=128 bf16", "hbm_peak_GBs": hbm, "results": out}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -338,10 +385,14 @@ def main():
     ap.add_argument("--impl", default="ulysses", choices=["ulysses", "reference"])
     ap.add_argument("--fwd-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="time the permutation alone over S = 4K..128K")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
 
+    if args.sweep:
+        run_sweep(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     w = WORKLOADS[args.workload]

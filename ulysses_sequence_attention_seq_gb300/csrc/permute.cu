@@ -21,6 +21,7 @@
 #include <stdint.h>
 
 #include "internal.h"
+#include "sm100.cuh"
 
 namespace ulysses {
 
@@ -125,7 +126,9 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const PermParams p) {
       if (q >= p.njobs) break;
       const PermJob J = p.job[q];
       const int hp = J.heads / p.P;
-      const int cph = J.rope ? p.D / (2 * V) : p.D / V;  // chunks per head handled per unit
+      // A unit is chunk c of both halves of a head (2 x 16 bytes), rotated or
+      // not: two loads in flight per thread either way.
+      const int cph = p.D / (2 * V);
       const int run = hp * cph;                           // units per destination piece
       const int units = J.heads * cph;
       const long long seq_row = row * (long long)J.heads * p.D;
@@ -140,21 +143,91 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const PermParams p) {
         const long long dst_off = p.to_head ? head_off : seq_off;
         const T *src = static_cast<const T *>(J.src);
         T *dst = static_cast<T *>(J.dst);
-        if (J.rope == 0) {
-          const uint4 x = __ldg(reinterpret_cast<const uint4 *>(src + src_off));
-          *reinterpret_cast<uint4 *>(dst + dst_off) = x;
-        } else {
-          const int half = p.D / 2;
-          uint4 x = __ldg(reinterpret_cast<const uint4 *>(src + src_off));
-          uint4 y = __ldg(reinterpret_cast<const uint4 *>(src + src_off + half));
+        const int half = p.D / 2;
+        uint4 x = __ldg(reinterpret_cast<const uint4 *>(src + src_off));
+        uint4 y = __ldg(reinterpret_cast<const uint4 *>(src + src_off + half));
+        if (J.rope) {
           const long long toff = (long long)pos * half + (long long)c * V;
           Chunk<T>::rope(x, y, p.rope_cos + toff, p.rope_sin + toff, J.rope);
-          *reinterpret_cast<uint4 *>(dst + dst_off) = x;
-          *reinterpret_cast<uint4 *>(dst + dst_off + half) = y;
         }
+        *reinterpret_cast<uint4 *>(dst + dst_off) = x;
+        *reinterpret_cast<uint4 *>(dst + dst_off + half) = y;
       }
     }
   }
+}
+
+// The head -> seq direction with the copy engine.  One warp per block: for
+// each token row of the sequence-sharded output it issues P bulk (TMA) loads
+// of the hp*D-element pieces (one from every rank's head-sharded buffer) into
+// a shared-memory stage and, once they have landed, one bulk store of the
+// whole row.  A ring of kBulkStages stages keeps several rows in flight per
+// block and many blocks share an SM, so the copy engine, not registers, holds
+// the bytes in flight (about 6 TB/s on the pages' sizing).
+constexpr int kBulkStages = 4;
+
+template <typename T>
+__global__ void __launch_bounds__(32) unpack_bulk_kernel(const PermParams p, uint32_t row_bytes) {
+  using namespace sm100;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + kBulkStages * row_bytes;  // one mbarrier per stage
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kBulkStages * row_bytes + 8 * kBulkStages);
+  const int lane = threadIdx.x;
+  const int S = p.P * p.Sl;
+  const long long rows = (long long)p.P * p.B * p.Sl;
+  const PermJob J = p.job[0];
+  const int hp = J.heads / p.P;
+  const uint32_t piece = row_bytes / p.P;  // hp * D elements
+  const T *src = static_cast<const T *>(J.src);
+  T *dst = static_cast<T *>(J.dst);
+  if (lane == 0) {
+    for (int i = 0; i < kBulkStages; ++i) mbar_init(bar0 + 8 * i, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncwarp();
+  const long long n_mine = rows > blockIdx.x ? (rows - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  auto load_row = [&](long long k) {
+    const long long row = blockIdx.x + k * gridDim.x;  // (d*B + b)*Sl + t of the output
+    const int t = (int)(row % p.Sl);
+    const long long db = row / p.Sl;
+    const int b = (int)(db % p.B), pos = (int)(db / p.B) * p.Sl + t;
+    const uint32_t slot = (uint32_t)(k % kBulkStages);
+    const uint32_t stage = sbase + slot * row_bytes, bar = bar0 + 8 * slot;
+    if (lane == 0) mbar_arrive_expect_tx(bar, row_bytes);
+    __syncwarp();
+    for (int r = lane; r < p.P; r += 32)  // rank r holds heads [r*hp, (r+1)*hp) at position pos
+      bulk_load(stage + r * piece, src + (((long long)(r * p.B + b) * S + pos) * hp) * p.D, piece, bar);
+  };
+  long long issued = -1, failed = n_mine;
+  for (long long k = 0; k < kBulkStages - 1 && k < n_mine; ++k) load_row(issued = k);
+  bool ok = true;
+  for (long long k = 0; k < n_mine; ++k) {
+    if (k + kBulkStages - 1 < n_mine) {
+      if (lane == 0) bulk_wait_read_all();  // row k-1's store has left its stage
+      __syncwarp();
+      load_row(issued = k + kBulkStages - 1);
+    }
+    failed = k;
+    ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar0 + 8 * (uint32_t)(k % kBulkStages),
+                                                   (uint32_t)((k / kBulkStages) & 1), abort_flag, p.status));
+    if (!ok) break;
+    failed = n_mine;
+    if (lane == 0) {
+      const long long row = blockIdx.x + k * gridDim.x;
+      bulk_store(dst + row * (long long)J.heads * p.D, sbase + (uint32_t)(k % kBulkStages) * row_bytes, row_bytes);
+      bulk_commit();
+    }
+  }
+  if (!ok) {
+    // Let the loads already in flight land before the block goes away.
+    volatile int never = 0;
+    for (long long k = failed; k <= issued; ++k)
+      mbar_wait_bounded(bar0 + 8 * (uint32_t)(k % kBulkStages), (uint32_t)((k / kBulkStages) & 1), &never,
+                        nullptr, 200000000ull);
+  }
+  if (lane == 0) bulk_wait_all();
 }
 
 // cos/sin(p * base^(-2i/D)) in double precision, rounded to float.
@@ -280,7 +353,32 @@ static PermParams base_params(const ulysses_problem &p, const void *ws, int to_h
   return pp;
 }
 
+template <typename T>
+static cudaError_t launch_unpack_bulk(const ulysses_problem &p, const PermParams &pp, uint32_t row_bytes,
+                                      cudaStream_t st) {
+  const size_t smem = (size_t)kBulkStages * row_bytes + 8 * kBulkStages + 16;
+  cudaError_t e = cudaFuncSetAttribute(unpack_bulk_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 148, per_sm = 1;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, unpack_bulk_kernel<T>, 32, smem);
+  per_sm = per_sm < 1 ? 1 : (per_sm > 32 ? 32 : per_sm);
+  long long grid = (long long)sms * per_sm;
+  const long long rows = (long long)p.B * p.S;
+  if (grid > rows) grid = rows;
+  unpack_bulk_kernel<T><<<(unsigned)grid, 32, smem, st>>>(pp, row_bytes);
+  return cudaGetLastError();
+}
+
 static cudaError_t launch_perm(const ulysses_problem &p, const PermParams &pp, cudaStream_t st) {
+  // A copy in the head -> seq direction whose output row fits a stage goes to
+  // the copy engine; everything else (the pack with RoPE) to the thread kernel.
+  const size_t row_bytes = (size_t)pp.job[0].heads * p.head_dim * elem_size(p);
+  if (!pp.to_head && pp.njobs == 1 && pp.job[0].rope == 0 && row_bytes <= 48 * 1024) {
+    if (p.dtype == ULYSSES_BF16) return launch_unpack_bulk<__nv_bfloat16>(p, pp, (uint32_t)row_bytes, st);
+    return launch_unpack_bulk<float>(p, pp, (uint32_t)row_bytes, st);
+  }
   const int grid = grid_for((long long)p.B * p.S);
   if (p.dtype == ULYSSES_BF16)
     permute_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(pp);
