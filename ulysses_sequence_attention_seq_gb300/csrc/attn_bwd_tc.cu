@@ -85,7 +85,7 @@ constexpr int kMaxStages = 4;
 // Depth of the streamed-operand ring: a stage is refilled only after the
 // accumulating MMAs of the iteration that used it have finished, so the ring
 // must cover the load latency plus one softmax step.
-constexpr int kStagesKV = 3;  // dkdv: Q, dO, LSE, delta per 64-query step
+constexpr int kStagesKV = 4;  // dkdv: Q, dO, LSE, delta per 64-query step
 constexpr int kStagesQ = 4;   // dq: K, V per 64-key step
 
 __device__ __forceinline__ void init_barriers(uint32_t bar) {
@@ -154,10 +154,9 @@ template <int D>
 struct KVLayout {
   static constexpr uint32_t kKV = 128u * D * 2;  // K or V tile: 128 rows
   static constexpr uint32_t kQ = 64u * D * 2;    // Q or dO tile: 64 rows
-  static constexpr uint32_t kPS = 128u * 128;    // P^T or dS^T: 128 key rows x 64 queries
   static constexpr uint32_t oK = 0, oV = oK + kKV, oQ = oV + kKV, odO = oQ + kStagesKV * kQ,
-                            oP = odO + kStagesKV * kQ, odS = oP + 2 * kPS, oL = odS + 2 * kPS,
-                            oDl = oL + kStagesKV * 256, oBar = oDl + kStagesKV * 256;
+                            oL = odO + kStagesKV * kQ, oDl = oL + kStagesKV * 256,
+                            oBar = oDl + kStagesKV * 256;
   static constexpr uint32_t kAlloc = oBar + 256 + 1024;
 };
 
@@ -174,8 +173,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
   uint8_t *smem = smem_raw + pad;
   const uint32_t sb = raw + pad;
-  const uint32_t sK = sb + L::oK, sV = sb + L::oV, sQ = sb + L::oQ, sdO = sb + L::odO, sP = sb + L::oP,
-                 sdS = sb + L::odS, sL = sb + L::oL, sDl = sb + L::oDl, bar = sb + L::oBar;
+  const uint32_t sK = sb + L::oK, sV = sb + L::oV, sQ = sb + L::oQ, sdO = sb + L::odO,
+                 sL = sb + L::oL, sDl = sb + L::oDl, bar = sb + L::oBar;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::oBar + kAbortSlot);
   const volatile uint32_t *gst = p.status;
   if ((*gst & 3u) || stale_rope_table(p)) return;
@@ -247,19 +246,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = i & 1, st = i % kStagesKV;
         if (!mbar_wait_bounded(bar + kBarPFull + 8 * b, (i >> 1) & 1, abort_flag, gst)) return false;
         tc_fence_after_sync();
+        // P^T and dS^T (bf16, two per column) sit in the first 32 columns of
+        // the step's S^T and dP^T buffers; 16 queries = 8 columns per MMA.
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t a = smem_desc_sw128(sP + b * L::kPS + kk * 32, 16, 1024);
           const uint64_t bb = smem_desc_sw128(sdO + st * L::kQ + kk * 2048, 8192, 1024);
-          mma_bf16_ss(tdV, a, bb, idA, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tdV, tmem + b * 64 + kk * 8, bb, idA, (i > 0 || kk > 0) ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t a = smem_desc_sw128(sdS + b * L::kPS + kk * 32, 16, 1024);
           const uint64_t bb = smem_desc_sw128(sQ + st * L::kQ + kk * 2048, 8192, 1024);
-          mma_bf16_ss(tdK, a, bb, idA, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tdK, tmem + 128 + b * 64 + kk * 8, bb, idA, (i > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(bar + kBarPFree + 8 * b);
         mma_commit(bar + kBarEmpty + 8 * st);
         return true;
       };
@@ -313,12 +311,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const int st = i % kStagesKV;
       if (!warp_wait(bar + kBarFull + 8 * st, (i / kStagesKV) & 1, abort_flag, gst)) { ok = false; break; }
-      // The S^T/dP^T commit of step i also covers the dV/dK MMAs of step i-2,
-      // so P/dS buffer b is free; the wait below is then immediate.
-      if (i >= 2 && !warp_wait(bar + kBarPFree + 8 * b, ((i - 2) >> 1) & 1, abort_flag, gst)) {
-        ok = false;
-        break;
-      }
+      // P^T and dS^T overwrite the columns of S^T and dP^T already read; the
+      // dV/dK MMAs of step i-2 read this buffer before S^T_i was written
+      // (tensor-core work of one issuer runs in order).
       const int q0 = (m0 + i % n_m) * 64;
       // Query q0 + c sees key kvr iff q0 + c >= kvr (causal) and q0 + c < S:
       // columns [lo, hi) of the 64 are valid.
@@ -350,10 +345,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           wd[2 * c4] = pack_bf16x2(ds[0], ds[1]);
           wd[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
         }
-        st_row_units(sP + b * L::kPS, r, h * 4, wp);
-        st_row_units(sdS + b * L::kPS, r, h * 4, wd);
+        tmem_st16(tmem + lane_base + b * 64 + h * 16, wp);
+        tmem_st16(tmem + lane_base + 128 + b * 64 + h * 16, wd);
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before_sync();
       mbar_arrive(bar + kBarTFree + 8 * b);
       mbar_arrive(bar + kBarPFull + 8 * b);
@@ -403,31 +398,57 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ================================================================== dQ kernel
+// 128-key tiles, every MMA 128x128x16.  TMEM: S [0,128) and dP [128,256)
+// single-buffered, dQ [256, 256+D), dS double-buffered at [384,448) and
+// [448,512) (bf16, two per column) where the dQ MMA reads it as its A operand.
+// The softmax warps load S and dP into registers and release them at once,
+// so S/dP of tile i+1 run on the tensor core while dS of tile i is formed.
+// K tiles stream through a 3-slot ring (released after the dQ MMA), V tiles
+// through a 2-slot ring (released right after the dP MMA).
+constexpr int kThreadsQ = 384;  // warpgroups 0-1 softmax, warpgroup 2: TMA, MMA, 2 idle warps
+constexpr uint32_t kRegsQProducer = 56, kRegsQSoftmax = 224;
+static_assert(128 * kRegsQProducer + 256 * kRegsQSoftmax <= 384 * 168, "register split over budget");
+constexpr int kKSlots = 3, kVSlots = 2;
+
+enum : uint32_t {
+  kQBarIn = 0,
+  kQBarKFull = 8,    // [3]
+  kQBarKEmpty = 32,  // [3]
+  kQBarVFull = 56,   // [2]
+  kQBarVEmpty = 72,  // [2]
+  kQBarSFull = 88,
+  kQBarTFree = 96,   // 256 arrivals
+  kQBarPFull = 104,  // 256 arrivals
+  kQBarPFree = 112,  // [2]
+  kQBarAcc = 128,
+  kQBarDrain = 136,
+  kQTmemSlot = 144,
+  kQAbortSlot = 148
+};
+
 template <int D>
 struct QLayout {
-  static constexpr uint32_t kQ = 128u * D * 2;   // Q or dO: 128 rows
-  static constexpr uint32_t kKV = 64u * D * 2;   // K or V tile: 64 rows
-  static constexpr uint32_t kS = 128u * 128;     // dS: 128 queries x 64 keys
-  static constexpr uint32_t oQ = 0, odO = oQ + kQ, oK = odO + kQ, oV = oK + kStagesQ * kKV,
-                            odS = oV + kStagesQ * kKV, oBar = odS + 2 * kS;
+  static constexpr uint32_t kT = 128u * D * 2;  // one 128-row tile (Q, dO, K or V)
+  static constexpr uint32_t oQ = 0, odO = kT, oK = 2 * kT, oV = oK + kKSlots * kT,
+                            oBar = oV + kVSlots * kT;
   static constexpr uint32_t kAlloc = oBar + 256 + 1024;
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsQ, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
               const BwdParams p) {
   using L = QLayout<D>;
   constexpr int kCh = D / 64;
+  constexpr uint32_t kColDQ = 256, kColDS = 384;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
   uint8_t *smem = smem_raw + pad;
   const uint32_t sb = raw + pad;
-  const uint32_t sQ = sb + L::oQ, sdO = sb + L::odO, sK = sb + L::oK, sV = sb + L::oV,
-                 sdS = sb + L::odS, bar = sb + L::oBar;
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::oBar + kAbortSlot);
+  const uint32_t sQ = sb + L::oQ, sdO = sb + L::odO, sK = sb + L::oK, sV = sb + L::oV, bar = sb + L::oBar;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::oBar + kQAbortSlot);
   const volatile uint32_t *gst = p.status;
   if ((*gst & 3u) || stale_rope_table(p)) return;
 
@@ -438,107 +459,130 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hid = (int)(blockIdx.x % heads_total);
   const int j = hid % p.hp, rb = hid / p.hp;
   const int kl = j / p.group;
-  const int n_kt = (p.S + 63) / 64;
-  const int n_kv = p.causal ? min(n_kt, 2 * m + 2) : n_kt;
+  const int n_kt = (p.S + 127) / 128;
+  const int n_kv = p.causal ? min(n_kt, m + 1) : n_kt;
 
   if (threadIdx.x == 0) {
-    init_barriers(bar);
+    mbar_init(bar + kQBarIn, 1);
+    for (int i = 0; i < kKSlots; ++i) {
+      mbar_init(bar + kQBarKFull + 8 * i, 1);
+      mbar_init(bar + kQBarKEmpty + 8 * i, 1);
+    }
+    for (int i = 0; i < kVSlots; ++i) {
+      mbar_init(bar + kQBarVFull + 8 * i, 1);
+      mbar_init(bar + kQBarVEmpty + 8 * i, 1);
+      mbar_init(bar + kQBarPFree + 8 * i, 1);
+    }
+    mbar_init(bar + kQBarSFull, 1);
+    mbar_init(bar + kQBarTFree, 256);
+    mbar_init(bar + kQBarPFull, 256);
+    mbar_init(bar + kQBarAcc, 1);
+    mbar_init(bar + kQBarDrain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
     __syncwarp();
-    tmem_alloc(bar + kTmemSlot, kTmemCols);
+    tmem_alloc(bar + kQTmemSlot, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::oBar + kTmemSlot);
-  const uint32_t tdQ = tmem + 256;
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::oBar + kQTmemSlot);
+  const uint32_t tdQ = tmem + kColDQ;
 
-  if (warp == kTmaWarp) {
-    if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      mbar_arrive_expect_tx(bar + kBarIn, 2 * L::kQ);
-      for (int c = 0; c < kCh; ++c) {
-        tma_load_4d(sQ + c * 16384, &tmQ, bar + kBarIn, c * 64, j, m * 128, rb);
-        tma_load_4d(sdO + c * 16384, &tmdO, bar + kBarIn, c * 64, j, m * 128, rb);
-      }
-      int issued = -1;
-      for (int i = 0; i < n_kv; ++i) {
-        const int st = i % kStagesQ;
-        const uint32_t ph = (i / kStagesQ) & 1;
-        if (!mbar_wait_bounded(bar + kBarEmpty + 8 * st, ph ^ 1, abort_flag, gst)) break;
-        mbar_arrive_expect_tx(bar + kBarFull + 8 * st, 2 * L::kKV);
+  if (warp >= 8) {
+    regs_dec<kRegsQProducer>();
+    if (warp == kTmaWarp) {
+      if (lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        mbar_arrive_expect_tx(bar + kQBarIn, 2 * L::kT);
         for (int c = 0; c < kCh; ++c) {
-          tma_load_4d(sK + st * L::kKV + c * 8192, &tmK, bar + kBarFull + 8 * st, c * 64, kl, i * 64, rb);
-          tma_load_4d(sV + st * L::kKV + c * 8192, &tmV, bar + kBarFull + 8 * st, c * 64, kl, i * 64, rb);
+          tma_load_4d(sQ + c * 16384, &tmQ, bar + kQBarIn, c * 64, j, m * 128, rb);
+          tma_load_4d(sdO + c * 16384, &tmdO, bar + kQBarIn, c * 64, j, m * 128, rb);
         }
-        issued = i;
+        int issued_k = -1, issued_v = -1;
+        for (int i = 0; i < n_kv; ++i) {
+          const int ks = i % kKSlots, vs = i % kVSlots;
+          if (!mbar_wait_bounded(bar + kQBarKEmpty + 8 * ks, ((i / kKSlots) & 1) ^ 1, abort_flag, gst)) break;
+          mbar_arrive_expect_tx(bar + kQBarKFull + 8 * ks, L::kT);
+          for (int c = 0; c < kCh; ++c)
+            tma_load_4d(sK + ks * L::kT + c * 16384, &tmK, bar + kQBarKFull + 8 * ks, c * 64, kl, i * 128, rb);
+          issued_k = i;
+          if (!mbar_wait_bounded(bar + kQBarVEmpty + 8 * vs, ((i / kVSlots) & 1) ^ 1, abort_flag, gst)) break;
+          mbar_arrive_expect_tx(bar + kQBarVFull + 8 * vs, L::kT);
+          for (int c = 0; c < kCh; ++c)
+            tma_load_4d(sV + vs * L::kT + c * 16384, &tmV, bar + kQBarVFull + 8 * vs, c * 64, kl, i * 128, rb);
+          issued_v = i;
+        }
+        if (*abort_flag) {
+          volatile int never = 0;
+          mbar_wait_bounded(bar + kQBarIn, 0, &never, nullptr, 500000000ull);
+          for (int i = issued_k - (kKSlots - 1); i <= issued_k; ++i)
+            if (i >= 0)
+              mbar_wait_bounded(bar + kQBarKFull + 8 * (i % kKSlots), (i / kKSlots) & 1, &never, nullptr,
+                                500000000ull);
+          for (int i = issued_v - (kVSlots - 1); i <= issued_v; ++i)
+            if (i >= 0)
+              mbar_wait_bounded(bar + kQBarVFull + 8 * (i % kVSlots), (i / kVSlots) & 1, &never, nullptr,
+                                500000000ull);
+        }
       }
-      if (*abort_flag) {
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) {
+        constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);  // S, dP: both operands K-major
+        constexpr uint32_t idQ = idesc_bf16_f32(128, D, 0, 1);    // dQ: B (K tile) MN-major
+        // S_i = Q K_i^T and dP_i = dO V_i^T into the single S/dP buffers.
+        auto issue_sdp = [&](int i) -> bool {
+          const int ks = i % kKSlots, vs = i % kVSlots;
+          if (!mbar_wait_bounded(bar + kQBarKFull + 8 * ks, (i / kKSlots) & 1, abort_flag, gst)) return false;
+          if (!mbar_wait_bounded(bar + kQBarVFull + 8 * vs, (i / kVSlots) & 1, abort_flag, gst)) return false;
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_bf16_ss(tmem, smem_desc_sw128(sQ + o, 16, 1024), smem_desc_sw128(sK + ks * L::kT + o, 16, 1024),
+                        idS, kk > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_bf16_ss(tmem + 128, smem_desc_sw128(sdO + o, 16, 1024),
+                        smem_desc_sw128(sV + vs * L::kT + o, 16, 1024), idS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar + kQBarSFull);
+          mma_commit(bar + kQBarVEmpty + 8 * vs);
+          return true;
+        };
+        bool ok = mbar_wait_bounded(bar + kQBarIn, 0, abort_flag, gst);
+        if (ok && n_kv > 0) ok = issue_sdp(0);
+        for (int i = 0; ok && i < n_kv; ++i) {
+          // the softmax has read S_i and dP_i: the next pair may overwrite them
+          if (!(ok = mbar_wait_bounded(bar + kQBarTFree, i & 1, abort_flag, gst))) break;
+          if (i + 1 < n_kv && !(ok = issue_sdp(i + 1))) break;
+          // dQ += dS_i K_i, dS_i read from TMEM (8 keys... 16 keys = 8 columns per MMA)
+          if (!(ok = mbar_wait_bounded(bar + kQBarPFull, i & 1, abort_flag, gst))) break;
+          tc_fence_after_sync();
+          const int ks = i % kKSlots, b = i & 1;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ts(tdQ, tmem + kColDS + b * 64 + kk * 8,
+                        smem_desc_sw128(sK + ks * L::kT + kk * 2048, 16384, 1024), idQ, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar + kQBarKEmpty + 8 * ks);
+          mma_commit(bar + kQBarPFree + 8 * b);
+        }
+        mma_commit(bar + kQBarAcc);
+        mma_commit(bar + kQBarDrain);
         volatile int never = 0;
-        mbar_wait_bounded(bar + kBarIn, 0, &never, nullptr, 500000000ull);
-        for (int i = issued - (kStagesQ - 1); i <= issued; ++i)
-          if (i >= 0)
-            mbar_wait_bounded(bar + kBarFull + 8 * (i % kStagesQ), (i / kStagesQ) & 1, &never, nullptr,
-                              500000000ull);
+        mbar_wait_bounded(bar + kQBarDrain, 0, &never, nullptr);
       }
-    }
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 64, 0, 0);  // S, dP: both operands K-major
-      constexpr uint32_t idQ = idesc_bf16_f32(128, D, 0, 1);   // dQ: B (K tile) MN-major
-      auto issue_dq = [&](int i) -> bool {
-        const int b = i & 1, st = i % kStagesQ;
-        if (!mbar_wait_bounded(bar + kBarPFull + 8 * b, (i >> 1) & 1, abort_flag, gst)) return false;
-        tc_fence_after_sync();
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t a = smem_desc_sw128(sdS + b * L::kS + kk * 32, 16, 1024);
-          const uint64_t bb = smem_desc_sw128(sK + st * L::kKV + kk * 2048, 8192, 1024);
-          mma_bf16_ss(tdQ, a, bb, idQ, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar + kBarPFree + 8 * b);
-        mma_commit(bar + kBarEmpty + 8 * st);
-        return true;
-      };
-      bool ok = mbar_wait_bounded(bar + kBarIn, 0, abort_flag, gst);
-      for (int i = 0; ok && i < n_kv; ++i) {
-        const int b = i & 1, st = i % kStagesQ;
-        if (!mbar_wait_bounded(bar + kBarFull + 8 * st, (i / kStagesQ) & 1, abort_flag, gst)) {
-          ok = false;
-          break;
-        }
-        if (i >= 2 && !mbar_wait_bounded(bar + kBarTFree + 8 * b, ((i - 2) >> 1) & 1, abort_flag, gst)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t oa = (kk >> 2) * 16384 + (kk & 3) * 32, ob = (kk >> 2) * 8192 + (kk & 3) * 32;
-          mma_bf16_ss(tmem + b * 64, smem_desc_sw128(sQ + oa, 16, 1024),
-                      smem_desc_sw128(sK + st * L::kKV + ob, 16, 1024), idS, kk > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t oa = (kk >> 2) * 16384 + (kk & 3) * 32, ob = (kk >> 2) * 8192 + (kk & 3) * 32;
-          mma_bf16_ss(tmem + 128 + b * 64, smem_desc_sw128(sdO + oa, 16, 1024),
-                      smem_desc_sw128(sV + st * L::kKV + ob, 16, 1024), idS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar + kBarSFull + 8 * b);
-        if (i > 0) ok = issue_dq(i - 1);
-      }
-      if (ok && n_kv > 0) issue_dq(n_kv - 1);
-      mma_commit(bar + kBarAcc);
-      mma_commit(bar + kBarDrain);
-      volatile int never = 0;
-      mbar_wait_bounded(bar + kBarDrain, 0, &never, nullptr);
     }
   } else {
+    regs_inc<kRegsQSoftmax>();
+    // ---------------------------------------- softmax warpgroups: warpgroup g
+    // owns key columns [64g, 64g+64) of every tile.
     const int g = warp >> 2, w4 = warp & 3;
     const int r = w4 * 32 + lane;  // query row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)(w4 * 32) << 16;
@@ -548,50 +592,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float nl2 = live ? p.nlse[lrow] : 0.f;
     const float dlt = live ? p.delta[lrow] : 0.f;
     bool ok = true;
-    // Warpgroup g takes the key tiles i with i % 2 == g (TMEM and dS buffer g),
-    // all 64 key columns, in two halves, so the two warpgroups' chains overlap.
-    for (int i = g; i < n_kv; i += 2) {
-      const int b = g;
-      const uint32_t ph = (i >> 1) & 1;
-      if (!warp_wait(bar + kBarSFull + 8 * b, ph, abort_flag, gst)) { ok = false; break; }
+    for (int i = 0; i < n_kv; ++i) {
+      if (!warp_wait(bar + kQBarSFull, i & 1, abort_flag, gst)) { ok = false; break; }
       tc_fence_after_sync();
-      // The S/dP commit of tile i also covers the dQ MMA of tile i-2, so dS
-      // buffer b is free; the wait below is then immediate.
-      if (i >= 2 && !warp_wait(bar + kBarPFree + 8 * b, ((i - 2) >> 1) & 1, abort_flag, gst)) {
-        ok = false;
-        break;
-      }
-      const int k0 = i * 64;
-      // Key k0 + c is seen by query qi iff k0 + c <= qi (causal) and k0 + c < S:
-      // columns [0, hi) of the 64 are valid.
-      const int hi = min(p.causal ? qi - k0 + 1 : 64, p.S - k0);
-      const bool full = __all_sync(0xffffffffu, hi >= 64);
+      uint32_t sr[2][32], dr[2][32];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tmem + lane_base + b * 64 + h * 32, sr);
-        tmem_ld32(tmem + lane_base + 128 + b * 64 + h * 32, dr);
-        tmem_wait_ld();
-        uint32_t wd[16];
+        tmem_ld32(tmem + lane_base + g * 64 + h * 32, sr[h]);
+        tmem_ld32(tmem + lane_base + 128 + g * 64 + h * 32, dr[h]);
+      }
+      tmem_wait_ld();
+      tc_fence_before_sync();
+      mbar_arrive(bar + kQBarTFree);
+      const int k0 = i * 128 + g * 64;
+      // Key k0 + c is seen by query qi iff k0 + c <= qi (causal) and k0 + c < S:
+      // columns [0, hi) of this warpgroup's 64 are valid.
+      const int hi = min(p.causal ? qi - k0 + 1 : 64, p.S - k0);
+      const bool full = __all_sync(0xffffffffu, hi >= 64);
+      uint32_t wd[2][16];
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           float ds[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            float pe = ex2(fmaf(__uint_as_float(sr[c + e]), p.scale_log2, nl2));
+            float pe = ex2(fmaf(__uint_as_float(sr[h][c + e]), p.scale_log2, nl2));
             if (!full && h * 32 + c + e >= hi) pe = 0.f;
-            ds[e] = pe * (__uint_as_float(dr[c + e]) - dlt);
+            ds[e] = pe * (__uint_as_float(dr[h][c + e]) - dlt);
           }
-          wd[c >> 1] = pack_bf16x2(ds[0], ds[1]);
+          wd[h][c >> 1] = pack_bf16x2(ds[0], ds[1]);
         }
-        st_row_units(sdS + b * L::kS, r, h * 4, wd);
+      // dS buffer i&1 is free once the dQ MMA of tile i-2 has read it.
+      if (i >= 2 && !warp_wait(bar + kQBarPFree + 8 * (i & 1), ((i - 2) >> 1) & 1, abort_flag, gst)) {
+        ok = false;
+        break;
       }
-      fence_proxy_async_smem();
+      tmem_st16(tmem + lane_base + kColDS + (i & 1) * 64 + g * 32, wd[0]);
+      tmem_st16(tmem + lane_base + kColDS + (i & 1) * 64 + g * 32 + 16, wd[1]);
+      tmem_wait_st();
       tc_fence_before_sync();
-      mbar_arrive(bar + kBarTFree + 8 * b);
-      mbar_arrive(bar + kBarPFull + 8 * b);
+      mbar_arrive(bar + kQBarPFull);
     }
-    if (ok) ok = warp_wait(bar + kBarAcc, 0, abort_flag, gst);
+    if (ok) ok = warp_wait(bar + kQBarAcc, 0, abort_flag, gst);
     if (ok && (D == 128 || g == 0)) {
       tc_fence_after_sync();
       const int s_rank = qi / p.Sl, t = qi - s_rank * p.Sl;
@@ -677,7 +720,7 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
                                                                             mDl, bp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dq_kernel<D><<<(unsigned)q_blocks, kThreads, QLayout<D>::kAlloc, st>>>(mQ128, mdO128, mK64, mV64, bp);
+  dq_kernel<D><<<(unsigned)q_blocks, kThreadsQ, QLayout<D>::kAlloc, st>>>(mQ128, mdO128, mK128, mV128, bp);
   return cudaGetLastError();
 }
 
