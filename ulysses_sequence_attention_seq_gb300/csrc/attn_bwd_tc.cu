@@ -9,24 +9,25 @@
 //   dV = P^T dO          dP = dO V^T          dS = P * (dP - delta)
 //   dQ = scale dS K      dK = scale dS^T Q    (dK, dV summed over the q-heads
 //                                              that share a kv-head)
-// Two kernels, each deterministic (no atomics):
+// Two kernels, each deterministic (no atomics), every MMA 128x128x16:
 //   dkdv: one CTA per 128-key tile of one kv-head.  K and V stay in shared
-//         memory; the loop runs over the q-heads of the group and the 64-row
-//         query tiles at or after the key tile (causal).  Per step:
-//         S^T = K Q^T and dP^T = V dO^T into double-buffered TMEM, the softmax
-//         warps form P^T and dS^T (bf16, shared memory), then dV += P^T dO and
-//         dK += dS^T Q accumulate in TMEM across the whole loop.
-//   dq:   one CTA per 128-row query tile of one head.  Q and dO stay in shared
-//         memory; the loop runs over 64-row key tiles at or before the query
-//         tile.  Per step: S = Q K^T and dP = dO V^T into double-buffered TMEM,
-//         dS (bf16) to shared memory, dQ += dS K in TMEM.
+//         memory; the loop runs over the q-heads of the group and the
+//         128-query tiles at or after the key tile (causal).  Per step:
+//         S^T = K Q^T and dP^T = V dO^T into TMEM, the softmax warps form
+//         P^T and dS^T (bf16) in TMEM, then dV += P^T dO and dK += dS^T Q
+//         (A operand read from TMEM) accumulate in TMEM across the loop.
+//   dq:   one CTA per 128-query tile of one head.  Q and dO stay in shared
+//         memory; the loop runs over 128-key tiles at or before the query
+//         tile.  Per step: S = Q K^T and dP = dO V^T into TMEM, dS (bf16) into
+//         double-buffered TMEM, dQ += dS K in TMEM.
 // Epilogues: the thread that owns a row of the accumulator writes it straight
 // to its place in the sequence-sharded output (the inverse All-to-All as
 // addressing) after undoing the RoPE rotation on dQ and dK (both elements of
 // every rotation pair are in the same thread's row).
 // Warp roles: warps 0-7 softmax / epilogue (two warpgroups, each owns half of
 // the tile's columns; warp w reads TMEM lanes 32*(w%4)...), warp 8 TMA
-// producer, warp 9 MMA issuer.  All waits are bounded.
+// producer, warp 9 MMA issuer; the dq kernel adds warps 10-11 to complete a
+// third warpgroup for its per-warpgroup register split.  All waits are bounded.
 #include <cuda_bf16.h>
 #include <math.h>
 #include <stdint.h>
@@ -41,7 +42,6 @@ namespace {
 using namespace sm100;
 using dev::warp_wait;
 
-constexpr int kThreads = 320;
 constexpr int kTmaWarp = 8, kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -65,53 +65,6 @@ __device__ __forceinline__ bool stale_rope_table(const BwdParams &p) {
     return true;
   }
   return false;
-}
-
-// Barrier block shared by both kernels (byte offsets).
-enum : uint32_t {
-  kBarIn = 0,       // resident operands loaded
-  kBarFull = 8,     // [kMaxStages] streamed operands loaded
-  kBarEmpty = 40,   // [kMaxStages] streamed operands consumed
-  kBarSFull = 72,   // [2] score / dP MMAs done
-  kBarTFree = 88,   // [2] TMEM score buffers read (128 arrivals: one warpgroup)
-  kBarPFull = 104,  // [2] P / dS written to shared memory (128 arrivals)
-  kBarPFree = 120,  // [2] accumulating MMAs that read P / dS done
-  kBarAcc = 136,    // all accumulation done
-  kBarDrain = 144,
-  kTmemSlot = 152,
-  kAbortSlot = 156
-};
-constexpr int kMaxStages = 4;
-// Depth of the streamed-operand ring: a stage is refilled only after the
-// accumulating MMAs of the iteration that used it have finished, so the ring
-// must cover the load latency plus one softmax step.
-constexpr int kStagesKV = 4;  // dkdv: Q, dO, LSE, delta per 64-query step
-constexpr int kStagesQ = 4;   // dq: K, V per 64-key step
-
-__device__ __forceinline__ void init_barriers(uint32_t bar) {
-  mbar_init(bar + kBarIn, 1);
-  for (int i = 0; i < kMaxStages; ++i) {
-    mbar_init(bar + kBarFull + 8 * i, 1);
-    mbar_init(bar + kBarEmpty + 8 * i, 1);
-  }
-  for (int i = 0; i < 2; ++i) {
-    mbar_init(bar + kBarSFull + 8 * i, 1);
-    mbar_init(bar + kBarTFree + 8 * i, 128);
-    mbar_init(bar + kBarPFull + 8 * i, 128);
-    mbar_init(bar + kBarPFree + 8 * i, 1);
-  }
-  mbar_init(bar + kBarAcc, 1);
-  mbar_init(bar + kBarDrain, 1);
-}
-
-// 32 bf16 values of one row chunk into shared memory, 128-byte-swizzled
-// K-major layout: row `r` of a tile whose rows are 128 bytes, 16-byte units
-// u0..u0+3 (32 columns of a 64-column tile).
-__device__ __forceinline__ void st_row_units(uint32_t tile, int r, int u0, const uint32_t (&w)[16]) {
-#pragma unroll
-  for (int v = 0; v < 4; ++v)
-    st_shared_v4(tile + r * 128 + (((u0 + v) ^ (r & 7)) << 4), w[4 * v], w[4 * v + 1], w[4 * v + 2],
-                 w[4 * v + 3]);
 }
 
 // 32 fp32 accumulator columns -> scaled bf16 in global memory.
@@ -150,18 +103,81 @@ __device__ __forceinline__ void store_unrotated(__nv_bfloat16 *dx, __nv_bfloat16
 }
 
 // ============================================================= dK / dV kernel
+// One CTA per 128-key tile of one kv-head; 128-query steps over the group's
+// q-heads, every MMA 128x128x16.  TMEM: S^T [0,128), dP^T [128,256),
+// dV [256, 256+D), dK [256+D, 256+2D).  Warpgroup g owns query columns
+// [64g, 64g+64) of a step: it reads its S^T columns and writes P^T (bf16, two
+// per column) over the first half of them, then reads its dP^T columns and
+// writes dS^T likewise; the dV/dK MMAs read them from there as their A
+// operand (columns [0,32) and [64,96) of each region).
+// The tensor core runs dV(i), S^T(i+1), dK(i), dP^T(i+1), ...: S^T(i+1)
+// overwrites P^T(i) only after dV(i) (one issuer's MMAs run in order) and is
+// computed while the softmax warps form dS^T(i); dP^T(i+1) likewise follows
+// dK(i) and runs while they form P^T(i+1).  So the tensor core never waits for
+// the softmax of its own step as long as each softmax phase is shorter than
+// two MMA groups.
+constexpr int kStagesKV = 2;   // Q, dO, LSE, delta per 128-query step
+constexpr int kThreadsKV = 320;  // 8 softmax warps, TMA warp, MMA warp (160 registers, no split)
+
+enum : uint32_t {
+  kKBarIn = 0,
+  kKBarFull = 8,     // [2]
+  kKBarEmpty = 24,   // [2]
+  kKBarSFull = 40,
+  kKBarDPFull = 48,
+  kKBarPFull = 56,   // 256 arrivals
+  kKBarDSFull = 64,  // 256 arrivals
+  kKBarAcc = 72,
+  kKBarDrain = 80,
+  kKTmemSlot = 88,
+  kKAbortSlot = 92
+};
+
+// P = exp2(scale*log2(e)*s - lse*log2(e)) for the 64 columns of S^T a
+// thread holds (query c's -lse*log2(e) at nl[c/2]); with kMask, columns
+// outside [lo, hi) are 0.  P is kept in fp32 for dS and packed to bf16.
+template <bool kMask>
+__device__ __forceinline__ void p_columns(const uint32_t (&s)[2][32], const float2 *nl, float sl, int lo,
+                                          int hi, float2 (&pf)[32], uint32_t (&w)[2][16]) {
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const uint32_t *sh = s[c >> 4];
+    const float2 x = fma2(make_float2(__uint_as_float(sh[2 * (c & 15)]), __uint_as_float(sh[2 * (c & 15) + 1])),
+                          make_float2(sl, sl), nl[c]);
+    float2 pe = make_float2(ex2(x.x), ex2(x.y));
+    if (kMask) {
+      if (2 * c < lo || 2 * c >= hi) pe.x = 0.f;
+      if (2 * c + 1 < lo || 2 * c + 1 >= hi) pe.y = 0.f;
+    }
+    pf[c] = pe;
+    w[c >> 4][c & 15] = pack_bf16x2(pe.x, pe.y);
+  }
+}
+
+// dS = P * (dP - delta) for the same 64 columns (query c's delta at dl[c/2]).
+__device__ __forceinline__ void ds_columns(const uint32_t (&d)[2][32], const float2 *dl, const float2 (&pf)[32],
+                                           uint32_t (&w)[2][16]) {
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const uint32_t *dh = d[c >> 4];
+    const float2 x = sub2(make_float2(__uint_as_float(dh[2 * (c & 15)]), __uint_as_float(dh[2 * (c & 15) + 1])),
+                          dl[c]);
+    const float2 ds = mul2(pf[c], x);
+    w[c >> 4][c & 15] = pack_bf16x2(ds.x, ds.y);
+  }
+}
+
 template <int D>
 struct KVLayout {
-  static constexpr uint32_t kKV = 128u * D * 2;  // K or V tile: 128 rows
-  static constexpr uint32_t kQ = 64u * D * 2;    // Q or dO tile: 64 rows
-  static constexpr uint32_t oK = 0, oV = oK + kKV, oQ = oV + kKV, odO = oQ + kStagesKV * kQ,
-                            oL = odO + kStagesKV * kQ, oDl = oL + kStagesKV * 256,
-                            oBar = oDl + kStagesKV * 256;
+  static constexpr uint32_t kT = 128u * D * 2;  // one 128-row tile
+  static constexpr uint32_t oK = 0, oV = kT, oQ = 2 * kT, odO = oQ + kStagesKV * kT,
+                            oL = odO + kStagesKV * kT, oDl = oL + kStagesKV * 512,
+                            oBar = oDl + kStagesKV * 512;
   static constexpr uint32_t kAlloc = oBar + 256 + 1024;
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsKV, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                 const __grid_constant__ CUtensorMap tmL, const __grid_constant__ CUtensorMap tmDl,
@@ -175,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sb = raw + pad;
   const uint32_t sK = sb + L::oK, sV = sb + L::oV, sQ = sb + L::oQ, sdO = sb + L::odO,
                  sL = sb + L::oL, sDl = sb + L::oDl, bar = sb + L::oBar;
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::oBar + kAbortSlot);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::oBar + kKAbortSlot);
   const volatile uint32_t *gst = p.status;
   if ((*gst & 3u) || stale_rope_table(p)) return;
 
@@ -184,177 +200,185 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = (int)(blockIdx.x / heads_total);  // key tile; low tiles have the most work
   const int hid = (int)(blockIdx.x % heads_total);
   const int kl = hid % p.kvp, rb = hid / p.kvp;
-  const int n_qt = (p.S + 63) / 64;
-  const int m0 = p.causal ? 2 * n : 0;
+  const int n_qt = (p.S + 127) / 128;
+  const int m0 = p.causal ? n : 0;
   const int n_m = n_qt - m0;
   const int n_iter = p.group * n_m;
 
   if (threadIdx.x == 0) {
-    init_barriers(bar);
+    mbar_init(bar + kKBarIn, 1);
+    for (int i = 0; i < kStagesKV; ++i) {
+      mbar_init(bar + kKBarFull + 8 * i, 1);
+      mbar_init(bar + kKBarEmpty + 8 * i, 1);
+    }
+    mbar_init(bar + kKBarSFull, 1);
+    mbar_init(bar + kKBarDPFull, 1);
+    mbar_init(bar + kKBarPFull, 256);
+    mbar_init(bar + kKBarDSFull, 256);
+    mbar_init(bar + kKBarAcc, 1);
+    mbar_init(bar + kKBarDrain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
     __syncwarp();
-    tmem_alloc(bar + kTmemSlot, kTmemCols);
+    tmem_alloc(bar + kKTmemSlot, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::oBar + kTmemSlot);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::oBar + kKTmemSlot);
   const uint32_t tdV = tmem + 256, tdK = tmem + 256 + D;
 
-  if (warp == kTmaWarp) {
-    if (lane == 0) {
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmQ);
-      mbar_arrive_expect_tx(bar + kBarIn, 2 * L::kKV);
-      for (int c = 0; c < kCh; ++c) {
-        tma_load_4d(sK + c * 16384, &tmK, bar + kBarIn, c * 64, kl, n * 128, rb);
-        tma_load_4d(sV + c * 16384, &tmV, bar + kBarIn, c * 64, kl, n * 128, rb);
-      }
-      int issued = -1;
-      for (int i = 0; i < n_iter; ++i) {
-        const int st = i % kStagesKV;
-        const uint32_t ph = (i / kStagesKV) & 1;
-        if (!mbar_wait_bounded(bar + kBarEmpty + 8 * st, ph ^ 1, abort_flag, gst)) break;
-        const int gi = i / n_m, m = m0 + i % n_m, j = kl * p.group + gi;
-        mbar_arrive_expect_tx(bar + kBarFull + 8 * st, 2 * L::kQ + 2 * 256);
+  if (warp >= 8) {
+    if (warp == kTmaWarp) {
+      if (lane == 0) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmQ);
+        mbar_arrive_expect_tx(bar + kKBarIn, 2 * L::kT);
         for (int c = 0; c < kCh; ++c) {
-          tma_load_4d(sQ + st * L::kQ + c * 8192, &tmQ, bar + kBarFull + 8 * st, c * 64, j, m * 64, rb);
-          tma_load_4d(sdO + st * L::kQ + c * 8192, &tmdO, bar + kBarFull + 8 * st, c * 64, j, m * 64, rb);
+          tma_load_4d(sK + c * 16384, &tmK, bar + kKBarIn, c * 64, kl, n * 128, rb);
+          tma_load_4d(sV + c * 16384, &tmV, bar + kKBarIn, c * 64, kl, n * 128, rb);
         }
-        dev::tma_load_2d(sL + st * 256, &tmL, bar + kBarFull + 8 * st, m * 64, rb * p.hp + j);
-        dev::tma_load_2d(sDl + st * 256, &tmDl, bar + kBarFull + 8 * st, m * 64, rb * p.hp + j);
-        issued = i;
+        int issued = -1;
+        for (int i = 0; i < n_iter; ++i) {
+          const int st = i % kStagesKV;
+          if (!mbar_wait_bounded(bar + kKBarEmpty + 8 * st, ((i / kStagesKV) & 1) ^ 1, abort_flag, gst)) break;
+          const int gi = i / n_m, m = m0 + i % n_m, j = kl * p.group + gi;
+          mbar_arrive_expect_tx(bar + kKBarFull + 8 * st, 2 * L::kT + 2 * 512);
+          for (int c = 0; c < kCh; ++c) {
+            tma_load_4d(sQ + st * L::kT + c * 16384, &tmQ, bar + kKBarFull + 8 * st, c * 64, j, m * 128, rb);
+            tma_load_4d(sdO + st * L::kT + c * 16384, &tmdO, bar + kKBarFull + 8 * st, c * 64, j, m * 128, rb);
+          }
+          dev::tma_load_2d(sL + st * 512, &tmL, bar + kKBarFull + 8 * st, m * 128, rb * p.hp + j);
+          dev::tma_load_2d(sDl + st * 512, &tmDl, bar + kKBarFull + 8 * st, m * 128, rb * p.hp + j);
+          issued = i;
+        }
+        if (*abort_flag) {
+          volatile int never = 0;
+          mbar_wait_bounded(bar + kKBarIn, 0, &never, nullptr, 500000000ull);
+          for (int i = issued - (kStagesKV - 1); i <= issued; ++i)
+            if (i >= 0)
+              mbar_wait_bounded(bar + kKBarFull + 8 * (i % kStagesKV), (i / kStagesKV) & 1, &never, nullptr,
+                                500000000ull);
+        }
       }
-      if (*abort_flag) {
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) {
+        constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);  // S^T, dP^T: both operands K-major
+        constexpr uint32_t idA = idesc_bf16_f32(128, D, 0, 1);    // dV, dK: B (dO, Q) MN-major
+        // S^T(i) = K Q_i^T, once stage i has landed.
+        auto issue_s = [&](int i) -> bool {
+          const int st = i % kStagesKV;
+          if (!mbar_wait_bounded(bar + kKBarFull + 8 * st, (i / kStagesKV) & 1, abort_flag, gst)) return false;
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_bf16_ss(tmem, smem_desc_sw128(sK + o, 16, 1024),
+                        smem_desc_sw128(sQ + st * L::kT + o, 16, 1024), idS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar + kKBarSFull);
+          return true;
+        };
+        // dP^T(i) = V dO_i^T (stage i already waited for by issue_s).
+        auto issue_dp = [&](int i) {
+          const int st = i % kStagesKV;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_bf16_ss(tmem + 128, smem_desc_sw128(sV + o, 16, 1024),
+                        smem_desc_sw128(sdO + st * L::kT + o, 16, 1024), idS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar + kKBarDPFull);
+        };
+        bool ok = mbar_wait_bounded(bar + kKBarIn, 0, abort_flag, gst);
+        if (ok && n_iter > 0 && (ok = issue_s(0))) issue_dp(0);
+        for (int i = 0; ok && i < n_iter; ++i) {
+          const int st = i % kStagesKV;
+          // P^T / dS^T: queries 16kk..16kk+15 are columns 8kk.. of warpgroup
+          // 0's half (kk < 4) or of warpgroup 1's half at +64 (kk >= 4).
+          if (!(ok = mbar_wait_bounded(bar + kKBarPFull, i & 1, abort_flag, gst))) break;
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t ac = (kk < 4 ? 0u : 64u) + (uint32_t)(kk & 3) * 8;
+            mma_bf16_ts(tdV, tmem + ac, smem_desc_sw128(sdO + st * L::kT + kk * 2048, 16384, 1024), idA,
+                        (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (i + 1 < n_iter && !(ok = issue_s(i + 1))) break;
+          if (!(ok = mbar_wait_bounded(bar + kKBarDSFull, i & 1, abort_flag, gst))) break;
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t ac = (kk < 4 ? 0u : 64u) + (uint32_t)(kk & 3) * 8;
+            mma_bf16_ts(tdK, tmem + 128 + ac, smem_desc_sw128(sQ + st * L::kT + kk * 2048, 16384, 1024), idA,
+                        (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bar + kKBarEmpty + 8 * st);
+          if (i + 1 < n_iter) issue_dp(i + 1);
+        }
+        mma_commit(bar + kKBarAcc);
+        mma_commit(bar + kKBarDrain);
         volatile int never = 0;
-        mbar_wait_bounded(bar + kBarIn, 0, &never, nullptr, 500000000ull);
-        for (int i = issued - (kStagesKV - 1); i <= issued; ++i)
-          if (i >= 0)
-            mbar_wait_bounded(bar + kBarFull + 8 * (i % kStagesKV), (i / kStagesKV) & 1, &never, nullptr,
-                              500000000ull);
+        mbar_wait_bounded(bar + kKBarDrain, 0, &never, nullptr);
       }
-    }
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 64, 0, 0);  // S^T, dP^T: both operands K-major
-      constexpr uint32_t idA = idesc_bf16_f32(128, D, 0, 1);   // dV, dK: B (dO, Q) MN-major
-      auto issue_acc = [&](int i) -> bool {
-        const int b = i & 1, st = i % kStagesKV;
-        if (!mbar_wait_bounded(bar + kBarPFull + 8 * b, (i >> 1) & 1, abort_flag, gst)) return false;
-        tc_fence_after_sync();
-        // P^T and dS^T (bf16, two per column) sit in the first 32 columns of
-        // the step's S^T and dP^T buffers; 16 queries = 8 columns per MMA.
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t bb = smem_desc_sw128(sdO + st * L::kQ + kk * 2048, 8192, 1024);
-          mma_bf16_ts(tdV, tmem + b * 64 + kk * 8, bb, idA, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t bb = smem_desc_sw128(sQ + st * L::kQ + kk * 2048, 8192, 1024);
-          mma_bf16_ts(tdK, tmem + 128 + b * 64 + kk * 8, bb, idA, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar + kBarEmpty + 8 * st);
-        return true;
-      };
-      bool ok = mbar_wait_bounded(bar + kBarIn, 0, abort_flag, gst);
-      for (int i = 0; ok && i < n_iter; ++i) {
-        const int b = i & 1, st = i % kStagesKV;
-        if (!mbar_wait_bounded(bar + kBarFull + 8 * st, (i / kStagesKV) & 1, abort_flag, gst)) {
-          ok = false;
-          break;
-        }
-        if (i >= 2 && !mbar_wait_bounded(bar + kBarTFree + 8 * b, ((i - 2) >> 1) & 1, abort_flag, gst)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t oa = (kk >> 2) * 16384 + (kk & 3) * 32, ob = (kk >> 2) * 8192 + (kk & 3) * 32;
-          mma_bf16_ss(tmem + b * 64, smem_desc_sw128(sK + oa, 16, 1024),
-                      smem_desc_sw128(sQ + st * L::kQ + ob, 16, 1024), idS, kk > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t oa = (kk >> 2) * 16384 + (kk & 3) * 32, ob = (kk >> 2) * 8192 + (kk & 3) * 32;
-          mma_bf16_ss(tmem + 128 + b * 64, smem_desc_sw128(sV + oa, 16, 1024),
-                      smem_desc_sw128(sdO + st * L::kQ + ob, 16, 1024), idS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar + kBarSFull + 8 * b);
-        if (i > 0) ok = issue_acc(i - 1);
-      }
-      if (ok && n_iter > 0) issue_acc(n_iter - 1);
-      mma_commit(bar + kBarAcc);
-      mma_commit(bar + kBarDrain);
-      volatile int never = 0;
-      mbar_wait_bounded(bar + kBarDrain, 0, &never, nullptr);
     }
   } else {
-    // ---------------------------------------------- softmax warps (0..7)
-    // Warpgroup g takes the steps i with i % 2 == g (TMEM and P/dS buffer g),
-    // all 64 query columns, in two halves: the two warpgroups' chains of TMEM
-    // load -> exponentials -> shared-memory store -> barrier overlap.
+    // ---------------------------------------------- softmax warpgroups
     const int g = warp >> 2, w4 = warp & 3;
     const int r = w4 * 32 + lane;  // key row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)(w4 * 32) << 16;
     const int kvr = n * 128 + r;
     bool ok = true;
-    for (int i = g; i < n_iter; i += 2) {
-      const int b = g;
-      const uint32_t ph = (i >> 1) & 1;
-      if (!warp_wait(bar + kBarSFull + 8 * b, ph, abort_flag, gst)) { ok = false; break; }
-      tc_fence_after_sync();
+    for (int i = 0; i < n_iter; ++i) {
       const int st = i % kStagesKV;
-      if (!warp_wait(bar + kBarFull + 8 * st, (i / kStagesKV) & 1, abort_flag, gst)) { ok = false; break; }
-      // P^T and dS^T overwrite the columns of S^T and dP^T already read; the
-      // dV/dK MMAs of step i-2 read this buffer before S^T_i was written
-      // (tensor-core work of one issuer runs in order).
-      const int q0 = (m0 + i % n_m) * 64;
+      if (!warp_wait(bar + kKBarSFull, i & 1, abort_flag, gst)) { ok = false; break; }
+      tc_fence_after_sync();
+      uint32_t sr[2][32];
+      tmem_ld32(tmem + lane_base + g * 64, sr[0]);
+      tmem_ld32(tmem + lane_base + g * 64 + 32, sr[1]);
+      // LSE and delta of this step's queries are in the stage (already landed).
+      if (!warp_wait(bar + kKBarFull + 8 * st, (i / kStagesKV) & 1, abort_flag, gst)) { ok = false; break; }
+      tmem_wait_ld();
+      reg_fence(sr[0]);
+      reg_fence(sr[1]);
+      const int q0 = (m0 + i % n_m) * 128 + g * 64;
       // Query q0 + c sees key kvr iff q0 + c >= kvr (causal) and q0 + c < S:
-      // columns [lo, hi) of the 64 are valid.
+      // columns [lo, hi) of this warpgroup's 64 are valid.
       const int lo = p.causal ? kvr - q0 : 0, hi = p.S - q0;
-      const bool full = __all_sync(0xffffffffu, lo <= 0 && hi >= 64);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tmem + lane_base + b * 64 + h * 32, sr);
-        tmem_ld32(tmem + lane_base + 128 + b * 64 + h * 32, dr);
-        tmem_wait_ld();
-        const float4 *nl4 = reinterpret_cast<const float4 *>(smem + L::oL + st * 256) + h * 8;
-        const float4 *dl4 = reinterpret_cast<const float4 *>(smem + L::oDl + st * 256) + h * 8;
-        uint32_t wp[16], wd[16];
-#pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 nl = nl4[c4], dl = dl4[c4];
-          const float nls[4] = {nl.x, nl.y, nl.z, nl.w}, dls[4] = {dl.x, dl.y, dl.z, dl.w};
-          float pe[4], ds[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = h * 32 + 4 * c4 + e;
-            pe[e] = ex2(fmaf(__uint_as_float(sr[4 * c4 + e]), p.scale_log2, nls[e]));
-            if (!full && (c < lo || c >= hi)) pe[e] = 0.f;
-            ds[e] = pe[e] * (__uint_as_float(dr[4 * c4 + e]) - dls[e]);
-          }
-          wp[2 * c4] = pack_bf16x2(pe[0], pe[1]);
-          wp[2 * c4 + 1] = pack_bf16x2(pe[2], pe[3]);
-          wd[2 * c4] = pack_bf16x2(ds[0], ds[1]);
-          wd[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
-        }
-        tmem_st16(tmem + lane_base + b * 64 + h * 16, wp);
-        tmem_st16(tmem + lane_base + 128 + b * 64 + h * 16, wd);
-      }
+      const float2 *nl2 = reinterpret_cast<const float2 *>(smem + L::oL + st * 512) + g * 32;
+      const float2 *dl2 = reinterpret_cast<const float2 *>(smem + L::oDl + st * 512) + g * 32;
+      float2 pf[32];  // P of this thread's 64 columns, kept for dS
+      uint32_t w[2][16];
+      if (__all_sync(0xffffffffu, lo <= 0 && hi >= 64))
+        p_columns<false>(sr, nl2, p.scale_log2, lo, hi, pf, w);
+      else
+        p_columns<true>(sr, nl2, p.scale_log2, lo, hi, pf, w);
+      tmem_st16(tmem + lane_base + g * 64, w[0]);
+      tmem_st16(tmem + lane_base + g * 64 + 16, w[1]);
       tmem_wait_st();
       tc_fence_before_sync();
-      mbar_arrive(bar + kBarTFree + 8 * b);
-      mbar_arrive(bar + kBarPFull + 8 * b);
+      mbar_arrive(bar + kKBarPFull);
+
+      if (!warp_wait(bar + kKBarDPFull, i & 1, abort_flag, gst)) { ok = false; break; }
+      tc_fence_after_sync();
+      uint32_t dr[2][32];
+      tmem_ld32(tmem + lane_base + 128 + g * 64, dr[0]);
+      tmem_ld32(tmem + lane_base + 128 + g * 64 + 32, dr[1]);
+      tmem_wait_ld();
+      reg_fence(dr[0]);
+      reg_fence(dr[1]);
+      ds_columns(dr, dl2, pf, w);
+      tmem_st16(tmem + lane_base + 128 + g * 64, w[0]);
+      tmem_st16(tmem + lane_base + 128 + g * 64 + 16, w[1]);
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(bar + kKBarDSFull);
     }
     // ------------------------------------------------------------ epilogue
-    if (ok) ok = warp_wait(bar + kBarAcc, 0, abort_flag, gst);
+    if (ok) ok = warp_wait(bar + kKBarAcc, 0, abort_flag, gst);
     if (ok) {
       tc_fence_after_sync();
       const bool live = kvr < p.S;
@@ -425,6 +449,29 @@ enum : uint32_t {
   kQTmemSlot = 144,
   kQAbortSlot = 148
 };
+
+// dS = P * (dP - delta), P = exp2(scale*log2(e)*s - lse*log2(e)), for the 64
+// key columns of one query row a thread holds; with kMask, columns at or past
+// hi are 0.
+template <bool kMask>
+__device__ __forceinline__ void ds_row(const uint32_t (&s)[2][32], const uint32_t (&d)[2][32], float sl, float nl,
+                                       float dlt, int hi, uint32_t (&w)[2][16]) {
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const uint32_t *sh = s[c >> 4], *dh = d[c >> 4];
+    const int e = 2 * (c & 15);
+    const float2 x = fma2(make_float2(__uint_as_float(sh[e]), __uint_as_float(sh[e + 1])), make_float2(sl, sl),
+                          make_float2(nl, nl));
+    float2 pe = make_float2(ex2(x.x), ex2(x.y));
+    if (kMask) {
+      if (2 * c >= hi) pe.x = 0.f;
+      if (2 * c + 1 >= hi) pe.y = 0.f;
+    }
+    const float2 y = sub2(make_float2(__uint_as_float(dh[e]), __uint_as_float(dh[e + 1])), make_float2(dlt, dlt));
+    const float2 ds = mul2(pe, y);
+    w[c >> 4][c & 15] = pack_bf16x2(ds.x, ds.y);
+  }
+}
 
 template <int D>
 struct QLayout {
@@ -604,25 +651,19 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       tmem_wait_ld();
       tc_fence_before_sync();
       mbar_arrive(bar + kQBarTFree);
+      reg_fence(sr[0]);
+      reg_fence(sr[1]);
+      reg_fence(dr[0]);
+      reg_fence(dr[1]);
       const int k0 = i * 128 + g * 64;
       // Key k0 + c is seen by query qi iff k0 + c <= qi (causal) and k0 + c < S:
       // columns [0, hi) of this warpgroup's 64 are valid.
       const int hi = min(p.causal ? qi - k0 + 1 : 64, p.S - k0);
-      const bool full = __all_sync(0xffffffffu, hi >= 64);
       uint32_t wd[2][16];
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float ds[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float pe = ex2(fmaf(__uint_as_float(sr[h][c + e]), p.scale_log2, nl2));
-            if (!full && h * 32 + c + e >= hi) pe = 0.f;
-            ds[e] = pe * (__uint_as_float(dr[h][c + e]) - dlt);
-          }
-          wd[h][c >> 1] = pack_bf16x2(ds[0], ds[1]);
-        }
+      if (__all_sync(0xffffffffu, hi >= 64))
+        ds_row<false>(sr, dr, p.scale_log2, nl2, dlt, hi, wd);
+      else
+        ds_row<true>(sr, dr, p.scale_log2, nl2, dlt, hi, wd);
       // dS buffer i&1 is free once the dQ MMA of tile i-2 has read it.
       if (i >= 2 && !warp_wait(bar + kQBarPFree + 8 * (i & 1), ((i - 2) >> 1) & 1, abort_flag, gst)) {
         ok = false;
@@ -668,17 +709,13 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
                      const void *v, const void *do_head, const float *nlse, const float *delta,
                      const void *ws, void *dq, void *dk, void *dv, uint32_t *status, cudaStream_t st) {
   const int hp = p.n_head / p.P, kvp = p.n_kv_head / p.P, PB = p.P * p.B;
-  CUtensorMap mK128, mV128, mQ64, mdO64, mL, mDl, mQ128, mdO128, mK64, mV64;
+  CUtensorMap mK128, mV128, mL, mDl, mQ128, mdO128;
   bool ok = make_act_map(enc, &mK128, k, D, kvp, p.S, PB, 128) &&
             make_act_map(enc, &mV128, v, D, kvp, p.S, PB, 128) &&
-            make_act_map(enc, &mQ64, q, D, hp, p.S, PB, 64) &&
-            make_act_map(enc, &mdO64, do_head, D, hp, p.S, PB, 64) &&
-            make_row_map(enc, &mL, nlse, p.S, PB * hp, 64) &&
-            make_row_map(enc, &mDl, delta, p.S, PB * hp, 64) &&
+            make_row_map(enc, &mL, nlse, p.S, PB * hp, 128) &&
+            make_row_map(enc, &mDl, delta, p.S, PB * hp, 128) &&
             make_act_map(enc, &mQ128, q, D, hp, p.S, PB, 128) &&
-            make_act_map(enc, &mdO128, do_head, D, hp, p.S, PB, 128) &&
-            make_act_map(enc, &mK64, k, D, kvp, p.S, PB, 64) &&
-            make_act_map(enc, &mV64, v, D, kvp, p.S, PB, 64);
+            make_act_map(enc, &mdO128, do_head, D, hp, p.S, PB, 128);
   if (!ok) return cudaErrorInvalidValue;
   BwdParams bp;
   bp.B = p.B;
@@ -716,8 +753,8 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QLayout<D>::kAlloc);
   if (e != cudaSuccess) return e;
-  dkdv_kernel<D><<<(unsigned)kv_blocks, kThreads, KVLayout<D>::kAlloc, st>>>(mK128, mV128, mQ64, mdO64, mL,
-                                                                            mDl, bp);
+  dkdv_kernel<D><<<(unsigned)kv_blocks, kThreadsKV, KVLayout<D>::kAlloc, st>>>(mK128, mV128, mQ128, mdO128,
+                                                                              mL, mDl, bp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   dq_kernel<D><<<(unsigned)q_blocks, kThreadsQ, QLayout<D>::kAlloc, st>>>(mQ128, mdO128, mK128, mV128, bp);
