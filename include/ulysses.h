@@ -68,7 +68,10 @@ enum ulysses_status_code {
 enum ulysses_device_status {
   ULYSSES_STATUS_FWD_TIMEOUT = 1u << 0,  /* attention forward: a pipeline wait gave up */
   ULYSSES_STATUS_BWD_TIMEOUT = 1u << 1,  /* attention backward: a pipeline wait gave up */
-  ULYSSES_STATUS_ROPE_TABLE = 1u << 2    /* RoPE table missing or built for another problem */
+  ULYSSES_STATUS_ROPE_TABLE = 1u << 2,   /* RoPE table missing or built for another problem */
+  ULYSSES_STATUS_SMEM_ALIGN = 1u << 3    /* a kernel's dynamic shared memory did not start on a
+                                            1024-byte boundary and its tiles did not fit behind
+                                            the padding: that kernel wrote nothing */
 };
 
 /*

@@ -21,7 +21,7 @@ _lib = None
 
 BF16, FP32 = 0, 1
 OK = 0
-STATUS_FWD_TIMEOUT, STATUS_BWD_TIMEOUT, STATUS_ROPE_TABLE = 1, 2, 4
+STATUS_FWD_TIMEOUT, STATUS_BWD_TIMEOUT, STATUS_ROPE_TABLE, STATUS_SMEM_ALIGN = 1, 2, 4, 8
 
 EXPORTS = ("ulysses_validate", "ulysses_workspace_bytes", "ulysses_workspace_init",
            "ulysses_read_status", "ulysses_pack_qkv", "ulysses_attn_fwd", "ulysses_unpack_out",

@@ -116,21 +116,29 @@ __device__ __forceinline__ void store_unrotated(__nv_bfloat16 *dx, __nv_bfloat16
 // dK(i) and runs while they form P^T(i+1).  So the tensor core never waits for
 // the softmax of its own step as long as each softmax phase is shorter than
 // two MMA groups.
-constexpr int kStagesKV = 2;   // Q, dO, LSE, delta per 128-query step
+// Q tiles stream through a 3-slot ring released after dK (their last reader),
+// dO tiles through a 2-slot ring released after dV; each step's delta rides in
+// its Q slot (read in the dS phase, before dK) and its LSE in its dO slot (read
+// in the P phase, before dV).  The third Q slot covers the L2 latency of a
+// tile load, which is longer than the two MMA groups between dK(i) and S^T(i+2).
+constexpr int kQSlots = 3, kOSlots = 2;
 constexpr int kThreadsKV = 320;  // 8 softmax warps, TMA warp, MMA warp (160 registers, no split)
 
 enum : uint32_t {
   kKBarIn = 0,
-  kKBarFull = 8,     // [2]
-  kKBarEmpty = 24,   // [2]
-  kKBarSFull = 40,
-  kKBarDPFull = 48,
-  kKBarPFull = 56,   // 256 arrivals
-  kKBarDSFull = 64,  // 256 arrivals
-  kKBarAcc = 72,
-  kKBarDrain = 80,
-  kKTmemSlot = 88,
-  kKAbortSlot = 92
+  kKBarQFull = 8,    // [3]
+  kKBarQEmpty = 32,  // [3]
+  kKBarOFull = 56,   // [2]
+  kKBarOEmpty = 72,  // [2]
+  kKBarSFull = 88,
+  kKBarDPFull = 96,
+  kKBarPFull = 104,  // 256 arrivals
+  kKBarDSFull = 112, // 256 arrivals
+  kKBarAcc = 120,
+  kKBarDrain = 128,
+  kKTmemSlot = 136,
+  kKAbortSlot = 140,
+  kKBarBytes = 144
 };
 
 // P = exp2(scale*log2(e)*s - lse*log2(e)) for the 64 columns of S^T a
@@ -167,13 +175,20 @@ __device__ __forceinline__ void ds_columns(const uint32_t (&d)[2][32], const flo
   }
 }
 
+constexpr uint32_t kMaxDynSmem = 232448;  // 227 KB per block
+
 template <int D>
 struct KVLayout {
   static constexpr uint32_t kT = 128u * D * 2;  // one 128-row tile
-  static constexpr uint32_t oK = 0, oV = kT, oQ = 2 * kT, odO = oQ + kStagesKV * kT,
-                            oL = odO + kStagesKV * kT, oDl = oL + kStagesKV * 512,
-                            oBar = oDl + kStagesKV * 512;
-  static constexpr uint32_t kAlloc = oBar + 256 + 1024;
+  static constexpr uint32_t oK = 0, oV = kT, oQ = 2 * kT, odO = oQ + kQSlots * kT,
+                            oDl = odO + kOSlots * kT,  // delta rows, one per Q slot
+                            oL = oDl + kQSlots * 512,  // -LSE*log2(e) rows, one per dO slot
+                            oBar = oL + kOSlots * 512;
+  static constexpr uint32_t kUsed = oBar + kKBarBytes;
+  // Room for aligning the base to 1024 bytes where it fits; at D = 128 it
+  // does not, and the kernel checks the base it was given.
+  static constexpr uint32_t kAlloc = kUsed + 1024 <= kMaxDynSmem ? kUsed + 1024 : kMaxDynSmem;
+  static_assert(kUsed <= kMaxDynSmem, "dK/dV tiles exceed shared memory");
 };
 
 template <int D>
@@ -194,6 +209,10 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::oBar + kKAbortSlot);
   const volatile uint32_t *gst = p.status;
   if ((*gst & 3u) || stale_rope_table(p)) return;
+  if (pad + L::kUsed > L::kAlloc) {  // uniform over the block: nobody has touched a barrier yet
+    if (threadIdx.x == 0) atomicOr(p.status, (uint32_t)ULYSSES_STATUS_SMEM_ALIGN);
+    return;
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int heads_total = p.P * p.B * p.kvp;
@@ -207,9 +226,13 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar + kKBarIn, 1);
-    for (int i = 0; i < kStagesKV; ++i) {
-      mbar_init(bar + kKBarFull + 8 * i, 1);
-      mbar_init(bar + kKBarEmpty + 8 * i, 1);
+    for (int i = 0; i < kQSlots; ++i) {
+      mbar_init(bar + kKBarQFull + 8 * i, 1);
+      mbar_init(bar + kKBarQEmpty + 8 * i, 1);
+    }
+    for (int i = 0; i < kOSlots; ++i) {
+      mbar_init(bar + kKBarOFull + 8 * i, 1);
+      mbar_init(bar + kKBarOEmpty + 8 * i, 1);
     }
     mbar_init(bar + kKBarSFull, 1);
     mbar_init(bar + kKBarDPFull, 1);
@@ -241,26 +264,33 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
           tma_load_4d(sK + c * 16384, &tmK, bar + kKBarIn, c * 64, kl, n * 128, rb);
           tma_load_4d(sV + c * 16384, &tmV, bar + kKBarIn, c * 64, kl, n * 128, rb);
         }
-        int issued = -1;
+        int issued_q = -1, issued_o = -1;
         for (int i = 0; i < n_iter; ++i) {
-          const int st = i % kStagesKV;
-          if (!mbar_wait_bounded(bar + kKBarEmpty + 8 * st, ((i / kStagesKV) & 1) ^ 1, abort_flag, gst)) break;
+          const int qs = i % kQSlots, os = i % kOSlots;
           const int gi = i / n_m, m = m0 + i % n_m, j = kl * p.group + gi;
-          mbar_arrive_expect_tx(bar + kKBarFull + 8 * st, 2 * L::kT + 2 * 512);
-          for (int c = 0; c < kCh; ++c) {
-            tma_load_4d(sQ + st * L::kT + c * 16384, &tmQ, bar + kKBarFull + 8 * st, c * 64, j, m * 128, rb);
-            tma_load_4d(sdO + st * L::kT + c * 16384, &tmdO, bar + kKBarFull + 8 * st, c * 64, j, m * 128, rb);
-          }
-          dev::tma_load_2d(sL + st * 512, &tmL, bar + kKBarFull + 8 * st, m * 128, rb * p.hp + j);
-          dev::tma_load_2d(sDl + st * 512, &tmDl, bar + kKBarFull + 8 * st, m * 128, rb * p.hp + j);
-          issued = i;
+          if (!mbar_wait_bounded(bar + kKBarQEmpty + 8 * qs, ((i / kQSlots) & 1) ^ 1, abort_flag, gst)) break;
+          mbar_arrive_expect_tx(bar + kKBarQFull + 8 * qs, L::kT + 512);
+          for (int c = 0; c < kCh; ++c)
+            tma_load_4d(sQ + qs * L::kT + c * 16384, &tmQ, bar + kKBarQFull + 8 * qs, c * 64, j, m * 128, rb);
+          dev::tma_load_2d(sDl + qs * 512, &tmDl, bar + kKBarQFull + 8 * qs, m * 128, rb * p.hp + j);
+          issued_q = i;
+          if (!mbar_wait_bounded(bar + kKBarOEmpty + 8 * os, ((i / kOSlots) & 1) ^ 1, abort_flag, gst)) break;
+          mbar_arrive_expect_tx(bar + kKBarOFull + 8 * os, L::kT + 512);
+          for (int c = 0; c < kCh; ++c)
+            tma_load_4d(sdO + os * L::kT + c * 16384, &tmdO, bar + kKBarOFull + 8 * os, c * 64, j, m * 128, rb);
+          dev::tma_load_2d(sL + os * 512, &tmL, bar + kKBarOFull + 8 * os, m * 128, rb * p.hp + j);
+          issued_o = i;
         }
         if (*abort_flag) {
           volatile int never = 0;
           mbar_wait_bounded(bar + kKBarIn, 0, &never, nullptr, 500000000ull);
-          for (int i = issued - (kStagesKV - 1); i <= issued; ++i)
+          for (int i = issued_q - (kQSlots - 1); i <= issued_q; ++i)
             if (i >= 0)
-              mbar_wait_bounded(bar + kKBarFull + 8 * (i % kStagesKV), (i / kStagesKV) & 1, &never, nullptr,
+              mbar_wait_bounded(bar + kKBarQFull + 8 * (i % kQSlots), (i / kQSlots) & 1, &never, nullptr,
+                                500000000ull);
+          for (int i = issued_o - (kOSlots - 1); i <= issued_o; ++i)
+            if (i >= 0)
+              mbar_wait_bounded(bar + kKBarOFull + 8 * (i % kOSlots), (i / kOSlots) & 1, &never, nullptr,
                                 500000000ull);
         }
       }
@@ -268,35 +298,38 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
       if (lane == 0) {
         constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);  // S^T, dP^T: both operands K-major
         constexpr uint32_t idA = idesc_bf16_f32(128, D, 0, 1);    // dV, dK: B (dO, Q) MN-major
-        // S^T(i) = K Q_i^T, once stage i has landed.
+        // S^T(i) = K Q_i^T, once Q tile i has landed.
         auto issue_s = [&](int i) -> bool {
-          const int st = i % kStagesKV;
-          if (!mbar_wait_bounded(bar + kKBarFull + 8 * st, (i / kStagesKV) & 1, abort_flag, gst)) return false;
+          const int qs = i % kQSlots;
+          if (!mbar_wait_bounded(bar + kKBarQFull + 8 * qs, (i / kQSlots) & 1, abort_flag, gst)) return false;
           tc_fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
             mma_bf16_ss(tmem, smem_desc_sw128(sK + o, 16, 1024),
-                        smem_desc_sw128(sQ + st * L::kT + o, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                        smem_desc_sw128(sQ + qs * L::kT + o, 16, 1024), idS, kk > 0 ? 1u : 0u);
           }
           mma_commit(bar + kKBarSFull);
           return true;
         };
-        // dP^T(i) = V dO_i^T (stage i already waited for by issue_s).
-        auto issue_dp = [&](int i) {
-          const int st = i % kStagesKV;
+        // dP^T(i) = V dO_i^T, once dO tile i has landed.
+        auto issue_dp = [&](int i) -> bool {
+          const int os = i % kOSlots;
+          if (!mbar_wait_bounded(bar + kKBarOFull + 8 * os, (i / kOSlots) & 1, abort_flag, gst)) return false;
+          tc_fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
             mma_bf16_ss(tmem + 128, smem_desc_sw128(sV + o, 16, 1024),
-                        smem_desc_sw128(sdO + st * L::kT + o, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                        smem_desc_sw128(sdO + os * L::kT + o, 16, 1024), idS, kk > 0 ? 1u : 0u);
           }
           mma_commit(bar + kKBarDPFull);
+          return true;
         };
         bool ok = mbar_wait_bounded(bar + kKBarIn, 0, abort_flag, gst);
-        if (ok && n_iter > 0 && (ok = issue_s(0))) issue_dp(0);
+        if (ok && n_iter > 0 && (ok = issue_s(0))) ok = issue_dp(0);
         for (int i = 0; ok && i < n_iter; ++i) {
-          const int st = i % kStagesKV;
+          const int qs = i % kQSlots, os = i % kOSlots;
           // P^T / dS^T: queries 16kk..16kk+15 are columns 8kk.. of warpgroup
           // 0's half (kk < 4) or of warpgroup 1's half at +64 (kk >= 4).
           if (!(ok = mbar_wait_bounded(bar + kKBarPFull, i & 1, abort_flag, gst))) break;
@@ -304,20 +337,21 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t ac = (kk < 4 ? 0u : 64u) + (uint32_t)(kk & 3) * 8;
-            mma_bf16_ts(tdV, tmem + ac, smem_desc_sw128(sdO + st * L::kT + kk * 2048, 16384, 1024), idA,
+            mma_bf16_ts(tdV, tmem + ac, smem_desc_sw128(sdO + os * L::kT + kk * 2048, 16384, 1024), idA,
                         (i > 0 || kk > 0) ? 1u : 0u);
           }
+          mma_commit(bar + kKBarOEmpty + 8 * os);
           if (i + 1 < n_iter && !(ok = issue_s(i + 1))) break;
           if (!(ok = mbar_wait_bounded(bar + kKBarDSFull, i & 1, abort_flag, gst))) break;
           tc_fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t ac = (kk < 4 ? 0u : 64u) + (uint32_t)(kk & 3) * 8;
-            mma_bf16_ts(tdK, tmem + 128 + ac, smem_desc_sw128(sQ + st * L::kT + kk * 2048, 16384, 1024), idA,
+            mma_bf16_ts(tdK, tmem + 128 + ac, smem_desc_sw128(sQ + qs * L::kT + kk * 2048, 16384, 1024), idA,
                         (i > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(bar + kKBarEmpty + 8 * st);
-          if (i + 1 < n_iter) issue_dp(i + 1);
+          mma_commit(bar + kKBarQEmpty + 8 * qs);
+          if (i + 1 < n_iter && !(ok = issue_dp(i + 1))) break;
         }
         mma_commit(bar + kKBarAcc);
         mma_commit(bar + kKBarDrain);
@@ -333,14 +367,14 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
     const int kvr = n * 128 + r;
     bool ok = true;
     for (int i = 0; i < n_iter; ++i) {
-      const int st = i % kStagesKV;
+      const int qs = i % kQSlots, os = i % kOSlots;
       if (!warp_wait(bar + kKBarSFull, i & 1, abort_flag, gst)) { ok = false; break; }
       tc_fence_after_sync();
       uint32_t sr[2][32];
       tmem_ld32(tmem + lane_base + g * 64, sr[0]);
       tmem_ld32(tmem + lane_base + g * 64 + 32, sr[1]);
-      // LSE and delta of this step's queries are in the stage (already landed).
-      if (!warp_wait(bar + kKBarFull + 8 * st, (i / kStagesKV) & 1, abort_flag, gst)) { ok = false; break; }
+      // This step's LSE rides in its dO slot (landed before dP^T(i) ran).
+      if (!warp_wait(bar + kKBarOFull + 8 * os, (i / kOSlots) & 1, abort_flag, gst)) { ok = false; break; }
       tmem_wait_ld();
       reg_fence(sr[0]);
       reg_fence(sr[1]);
@@ -348,8 +382,8 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
       // Query q0 + c sees key kvr iff q0 + c >= kvr (causal) and q0 + c < S:
       // columns [lo, hi) of this warpgroup's 64 are valid.
       const int lo = p.causal ? kvr - q0 : 0, hi = p.S - q0;
-      const float2 *nl2 = reinterpret_cast<const float2 *>(smem + L::oL + st * 512) + g * 32;
-      const float2 *dl2 = reinterpret_cast<const float2 *>(smem + L::oDl + st * 512) + g * 32;
+      const float2 *nl2 = reinterpret_cast<const float2 *>(smem + L::oL + os * 512) + g * 32;
+      const float2 *dl2 = reinterpret_cast<const float2 *>(smem + L::oDl + qs * 512) + g * 32;
       float2 pf[32];  // P of this thread's 64 columns, kept for dS
       uint32_t w[2][16];
       if (__all_sync(0xffffffffu, lo <= 0 && hi >= 64))
@@ -363,6 +397,8 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
       mbar_arrive(bar + kKBarPFull);
 
       if (!warp_wait(bar + kKBarDPFull, i & 1, abort_flag, gst)) { ok = false; break; }
+      // ... and its delta in its Q slot (landed before S^T(i) ran).
+      if (!warp_wait(bar + kKBarQFull + 8 * qs, (i / kQSlots) & 1, abort_flag, gst)) { ok = false; break; }
       tc_fence_after_sync();
       uint32_t dr[2][32];
       tmem_ld32(tmem + lane_base + 128 + g * 64, dr[0]);
