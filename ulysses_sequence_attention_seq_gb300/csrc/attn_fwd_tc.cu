@@ -11,7 +11,7 @@
 // B = the next 128) of one head, 12 warps (warps 10-11 only complete the
 // third warpgroup, which the per-warpgroup register split needs).
 //   warp 8      TMA producer: both Q tiles once, then K_0, V_0, K_1, V_1, ...
-//               through a 3-slot ring (128 rows x D, 128-byte swizzle, 4-D
+//               through a 4-slot ring (128 rows x D, 128-byte swizzle, 4-D
 //               tensor maps over [P*B][S][heads][D] so a tile never crosses a
 //               sequence end).  Every K/V tile serves 256 query rows.
 //   warp 9      MMA issuer (one thread), in the order
@@ -19,18 +19,22 @@
 //               so the tensor core alternates between the two tiles while the
 //               other tile's softmax runs.  Because S_X(j+1) is issued after
 //               PV_X(j), the commit that reports S_X(j+1) also reports that
-//               PV_X(j) has finished: the softmax can then overwrite P_X and
-//               rescale O_X without any further barrier.
+//               PV_X(j) has finished: the softmax can then rescale O_X
+//               without any further barrier.  S_X(j+1) overwrites P_X(j) only
+//               after PV_X(j) has read it (one issuer's MMAs run in order).
 //   warps 0-3   softmax of tile A, warps 4-7 of tile B: thread i of a
 //               warpgroup owns query row i = TMEM lane i.  It reads its score
 //               row from TMEM, keeps a running max in the base-2 domain and
 //               rescales its TMEM accumulator row only when the max grows by
 //               more than 2^8 (otherwise the stale max stays: every exponent is
-//               <= 2^8, exact in fp32 and bf16), writes P (bf16) into its
-//               tile's shared-memory buffer in the swizzled K-major layout the
-//               PV MMA reads, and at the end divides by the row sum and stores
-//               O (bf16) and the LSE.
-// TMEM: S_A, S_B (128 columns each), O_A, O_B (D columns each).
+//               <= 2^8, exact in fp32 and bf16), writes P (bf16, two keys per
+//               32-bit column) over the first 64 columns of its S row, where
+//               the PV MMA reads it as its A operand straight from TMEM, and at
+//               the end divides by the row sum and stores O (bf16) and the LSE.
+// TMEM: S_A, S_B (128 columns each; P_X in the first 64 of S_X), O_A, O_B (D
+// columns each).  Keeping P out of shared memory leaves the shared-memory
+// port, which a 128x128x16 MMA with both operands there saturates, to Q, K, V
+// and the TMA writes.
 // Causal tiles past the diagonal are skipped; only the diagonal tile and the
 // ragged tail are masked.  CTAs are ordered longest-first.  Every wait is
 // bounded (2 s); a timeout sets a status bit, the CTA drains its tensor-core
@@ -53,36 +57,34 @@ constexpr int BM = 128;        // query rows per tile (two tiles per CTA)
 constexpr int BN = 128;        // keys per tile
 constexpr int kThreads = 384;  // warpgroups 0-1 softmax, warpgroup 2: TMA, MMA, 2 idle warps
 constexpr int kTmaWarp = 8, kMmaWarp = 9;
-// Register split (launch: 384 threads x 168): warpgroup 2 drops to 56, the
-// softmax warpgroups rise to 224: 128*56 + 256*224 = 64512 = 384*168.
-constexpr uint32_t kRegsProducer = 56, kRegsSoftmax = 224;
+// Register split (launch: 384 threads x 168): warpgroup 2 drops to 72, the
+// softmax warpgroups rise to 216: 128*72 + 256*216 = 64512 = 384*168.
+constexpr uint32_t kRegsProducer = 72, kRegsSoftmax = 216;
 static_assert(128 * kRegsProducer + 256 * kRegsSoftmax <= 384 * 168, "register split over budget");
-constexpr int kSlots = 3;  // K/V ring
+constexpr int kSlots = 4;  // K/V ring
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kChunkBytes = 128 * 128;    // 128 rows x 128 bytes (64 bf16)
-constexpr uint32_t kPBytes = 2 * kChunkBytes;  // one 128x128 bf16 P tile
 
 template <int D>
 struct Layout {
   static constexpr uint32_t kTile = 128u * D * 2;       // one 128-row tile of Q, K or V
   static constexpr uint32_t kQ = 0;                      // Q_A, Q_B
   static constexpr uint32_t kKV = kQ + 2 * kTile;        // ring of kSlots tiles
-  static constexpr uint32_t kP = kKV + kSlots * kTile;   // P_A, P_B
-  static constexpr uint32_t kBar = kP + 2 * kPBytes;
+  static constexpr uint32_t kBar = kKV + kSlots * kTile;
   static constexpr uint32_t kAlloc = kBar + 256 + 1024;  // room to align the base to 1024
 };
 
 // Barrier slots (byte offsets inside the barrier block).
 enum : uint32_t {
   kBarQFull = 0,
-  kBarKVFull = 8,    // [3]
-  kBarKVEmpty = 32,  // [3]
-  kBarSFull = 56,    // [2] A, B
-  kBarPFull = 72,    // [2] A, B (128 arrivals)
-  kBarODone = 88,    // [2] A, B
-  kBarDrain = 104,
-  kTmemSlot = 112,
-  kAbortSlot = 116
+  kBarKVFull = 8,    // [4]
+  kBarKVEmpty = 40,  // [4]
+  kBarSFull = 72,    // [2] A, B
+  kBarPFull = 88,    // [2] A, B (128 arrivals)
+  kBarODone = 104,   // [2] A, B
+  kBarDrain = 120,
+  kTmemSlot = 128,
+  kAbortSlot = 132
 };
 
 struct FwdParams {
@@ -126,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
   uint8_t *smem = smem_raw + pad;
   const uint32_t sb = raw + pad;
-  const uint32_t sQ = sb + L::kQ, sKV = sb + L::kKV, sP = sb + L::kP;
+  const uint32_t sQ = sb + L::kQ, sKV = sb + L::kKV;
   const uint32_t bar = sb + L::kBar;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kBar + kAbortSlot);
   const volatile uint32_t *gst = p.status;
@@ -212,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         // -------------------------------------------------------------- MMA
         constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);  // Q, K both K-major
-        constexpr uint32_t idPV = idesc_bf16_f32(BM, D, 0, 1);  // P K-major, V MN-major
+        constexpr uint32_t idPV = idesc_bf16_f32(BM, D, 0, 1);  // P (TMEM), V MN-major
         auto issue_s = [&](int x, int t) -> bool {
           const int n = 2 * t;
           if (!mbar_wait_bounded(bar + kBarKVFull + 8 * ring_slot(n), ring_parity(n), abort_flag, gst))
@@ -235,12 +237,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             return false;
           tc_fence_after_sync();
           const uint32_t vt = sKV + ring_slot(n) * L::kTile;
+          // keys 16kk..16kk+15 of P_X are TMEM columns x*BN + 8kk ..
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint64_t a =
-                smem_desc_sw128(sP + x * kPBytes + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024);
             const uint64_t b = smem_desc_sw128(vt + kk * 16 * 128, kChunkBytes, 1024);
-            mma_bf16_ss(tmem + 2 * BN + x * D, a, b, idPV, (t > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16_ts(tmem + 2 * BN + x * D, tmem + x * BN + kk * 8, b, idPV, (t > 0 || kk > 0) ? 1u : 0u);
           }
           return true;
         };
@@ -282,7 +283,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + lane_base + 2 * BN + x * D;
     const int n_mine = x ? nB : nA;
     const int diag = p.causal ? 2 * qp + x : -1;  // the key tile holding this tile's diagonal
-    const uint32_t prow = sP + x * kPBytes + row * 128;
     const float sl2 = p.scale_log2;
     float m_used = -INFINITY, l = 0.f;  // running max (scaled, base 2) and row sum
     bool ok = true;
@@ -296,6 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
       tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) reg_fence(s[c]);
       const int kv0 = t * BN;
       if (t == diag || kv0 + BN > p.S) {
         // keys past this query row (causal) or past the sequence end
@@ -304,14 +306,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < BN; ++c)
           if (c > lim) s[c >> 5][c & 31] = __float_as_uint(-INFINITY);
       }
+      // eight independent chains of three-input maxima over 16 columns each
       float mx[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(s[i >> 1][(i & 1) * 16]);
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t *r = &s[i >> 1][(i & 1) * 16];
+        float m = max3(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]));
 #pragma unroll
-      for (int c = 0; c < BN; ++c)
-        if ((c & 15) != 0) mx[c >> 4] = fmaxf(mx[c >> 4], __uint_as_float(s[c >> 5][c & 31]));
-      const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        for (int e = 3; e < 15; e += 2) m = max3(m, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+        mx[i] = fmaxf(m, __uint_as_float(r[15]));
+      }
+      const float mraw = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       const float ms = mraw * sl2;
       const bool need = ms > m_used + 8.0f;  // first tile: m_used = -inf
       if (__any_sync(0xffffffffu, need)) {
@@ -325,7 +330,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(tO + c * 32, r);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            for (int e = 0; e < 32; e += 2) {
+              const float2 v = mul2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
+                                    make_float2(alpha, alpha));
+              r[e] = __float_as_uint(v.x);
+              r[e + 1] = __float_as_uint(v.y);
+            }
             tmem_st32(tO + c * 32, r);
           }
           tmem_wait_st();
@@ -335,27 +345,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_used = ms;
         }
       }
-      const float nb = -m_used;
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+      const float2 sl22 = make_float2(sl2, sl2), nb2 = make_float2(-m_used, -m_used);
+      float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
+        // keys [32c, 32c+32) -> P columns [16c, 16c+16) of this row
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2(fmaf(__uint_as_float(s[c][2 * e]), sl2, nb));
-          const float p1 = ex2(fmaf(__uint_as_float(s[c][2 * e + 1]), sl2, nb));
-          rs[e & 3] += p0 + p1;
-          w[e] = pack_bf16x2(p0, p1);
+          const float2 a =
+              fma2(make_float2(__uint_as_float(s[c][2 * e]), __uint_as_float(s[c][2 * e + 1])), sl22, nb2);
+          const float2 pe = make_float2(ex2(a.x), ex2(a.y));
+          rs[e & 1] = add2(rs[e & 1], pe);
+          w[e] = pack_bf16x2(pe.x, pe.y);
         }
-        // columns [32c, 32c+32): 64-key chunk c/2, 16-byte units (c&1)*4 .. +3
-        const uint32_t base = prow + (c >> 1) * kChunkBytes;
-#pragma unroll
-        for (int v = 0; v < 4; ++v)
-          st_shared_v4(base + ((((c & 1) * 4 + v) ^ (row & 7)) << 4), w[4 * v], w[4 * v + 1],
-                       w[4 * v + 2], w[4 * v + 3]);
+        tmem_st16(tS + c * 16, w);
       }
-      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
-      fence_proxy_async_smem();
+      l += (rs[0].x + rs[1].x) + (rs[0].y + rs[1].y);
+      tmem_wait_st();
       tc_fence_before_sync();
       mbar_arrive(bar + kBarPFull + 8 * x);
     }
