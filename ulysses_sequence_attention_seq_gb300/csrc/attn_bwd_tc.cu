@@ -16,10 +16,10 @@
 //         S^T = K Q^T and dP^T = V dO^T into TMEM, the softmax warps form
 //         P^T and dS^T (bf16) in TMEM, then dV += P^T dO and dK += dS^T Q
 //         (A operand read from TMEM) accumulate in TMEM across the loop.
-//   dq:   one CTA per 128-query tile of one head.  Q and dO stay in shared
-//         memory; the loop runs over 128-key tiles at or before the query
-//         tile.  Per step: S = Q K^T and dP = dO V^T into TMEM, dS (bf16) into
-//         double-buffered TMEM, dQ += dS K in TMEM.
+//   dq:   one CTA per 128-query tile of one head.  Q and dO stay in TMEM
+//         (the A operand of S and dP); the loop runs over 128-key tiles at or
+//         before the query tile.  Per step: S = Q K^T and dP = dO V^T into
+//         TMEM, dS (bf16) over dP, dQ += dS K in TMEM.
 // Epilogues: the thread that owns a row of the accumulator writes it straight
 // to its place in the sequence-sharded output (the inverse All-to-All as
 // addressing) after undoing the RoPE rotation on dQ and dK (both elements of
@@ -52,6 +52,7 @@ struct BwdParams {
   float scale, scale_log2;
   const float *nlse, *delta;           // [P][B][hp][S]; nlse = -lse * log2(e)
   const float *rope_cos, *rope_sin;    // [S][D/2], or null without RoPE
+  const __nv_bfloat16 *q, *dout;       // head layout [P][B][S][hp][D] (the dQ kernel's TMEM operands)
   __nv_bfloat16 *dq, *dk, *dv;         // sequence-sharded outputs
   uint32_t *status;                    // status word; the RoPE table key follows it
   uint32_t rope_key;
@@ -115,7 +116,11 @@ __device__ __forceinline__ void store_unrotated(__nv_bfloat16 *dx, __nv_bfloat16
 // computed while the softmax warps form dS^T(i); dP^T(i+1) likewise follows
 // dK(i) and runs while they form P^T(i+1).  So the tensor core never waits for
 // the softmax of its own step as long as each softmax phase is shorter than
-// two MMA groups.
+// two MMA groups.  The issuer takes every wait of a burst (dV(i) S^T(i+1), or
+// dK(i) dP^T(i+1)) before issuing any of it: a thread with MMAs in flight
+// stalls on its next shared-memory access until they have been taken by the
+// tensor core, which leaves a gap in the pipe, so there are two such points
+// per step rather than one per operand.
 // Q tiles stream through a 3-slot ring released after dK (their last reader),
 // dO tiles through a 2-slot ring released after dV; each step's delta rides in
 // its Q slot (read in the dS phase, before dK) and its LSE in its dO slot (read
@@ -298,11 +303,15 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
       if (lane == 0) {
         constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);  // S^T, dP^T: both operands K-major
         constexpr uint32_t idA = idesc_bf16_f32(128, D, 0, 1);    // dV, dK: B (dO, Q) MN-major
-        // S^T(i) = K Q_i^T, once Q tile i has landed.
-        auto issue_s = [&](int i) -> bool {
+        auto q_ready = [&](int i) -> bool {
+          return mbar_wait_bounded(bar + kKBarQFull + 8 * (i % kQSlots), (i / kQSlots) & 1, abort_flag, gst);
+        };
+        auto o_ready = [&](int i) -> bool {
+          return mbar_wait_bounded(bar + kKBarOFull + 8 * (i % kOSlots), (i / kOSlots) & 1, abort_flag, gst);
+        };
+        // S^T(i) = K Q_i^T (Q tile i has landed: the caller waited).
+        auto issue_s = [&](int i) {
           const int qs = i % kQSlots;
-          if (!mbar_wait_bounded(bar + kKBarQFull + 8 * qs, (i / kQSlots) & 1, abort_flag, gst)) return false;
-          tc_fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -310,13 +319,10 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
                         smem_desc_sw128(sQ + qs * L::kT + o, 16, 1024), idS, kk > 0 ? 1u : 0u);
           }
           mma_commit(bar + kKBarSFull);
-          return true;
         };
-        // dP^T(i) = V dO_i^T, once dO tile i has landed.
-        auto issue_dp = [&](int i) -> bool {
+        // dP^T(i) = V dO_i^T (dO tile i has landed: the caller waited).
+        auto issue_dp = [&](int i) {
           const int os = i % kOSlots;
-          if (!mbar_wait_bounded(bar + kKBarOFull + 8 * os, (i / kOSlots) & 1, abort_flag, gst)) return false;
-          tc_fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -324,15 +330,21 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
                         smem_desc_sw128(sdO + os * L::kT + o, 16, 1024), idS, kk > 0 ? 1u : 0u);
           }
           mma_commit(bar + kKBarDPFull);
-          return true;
         };
-        bool ok = mbar_wait_bounded(bar + kKBarIn, 0, abort_flag, gst);
-        if (ok && n_iter > 0 && (ok = issue_s(0))) ok = issue_dp(0);
+        bool ok = mbar_wait_bounded(bar + kKBarIn, 0, abort_flag, gst) && q_ready(0) && o_ready(0);
+        if (ok && n_iter > 0) {
+          tc_fence_after_sync();
+          issue_s(0);
+          issue_dp(0);
+        }
         for (int i = 0; ok && i < n_iter; ++i) {
           const int qs = i % kQSlots, os = i % kOSlots;
-          // P^T / dS^T: queries 16kk..16kk+15 are columns 8kk.. of warpgroup
-          // 0's half (kk < 4) or of warpgroup 1's half at +64 (kk >= 4).
-          if (!(ok = mbar_wait_bounded(bar + kKBarPFull, i & 1, abort_flag, gst))) break;
+          // burst 1: dV(i), S^T(i+1).  P^T / dS^T: queries 16kk..16kk+15 are
+          // columns 8kk.. of warpgroup 0's half (kk < 4) or of warpgroup 1's
+          // half at +64 (kk >= 4).
+          if (!(ok = mbar_wait_bounded(bar + kKBarPFull, i & 1, abort_flag, gst) &&
+                     (i + 1 == n_iter || q_ready(i + 1))))
+            break;
           tc_fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
@@ -341,8 +353,11 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
                         (i > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(bar + kKBarOEmpty + 8 * os);
-          if (i + 1 < n_iter && !(ok = issue_s(i + 1))) break;
-          if (!(ok = mbar_wait_bounded(bar + kKBarDSFull, i & 1, abort_flag, gst))) break;
+          if (i + 1 < n_iter) issue_s(i + 1);
+          // burst 2: dK(i), dP^T(i+1)
+          if (!(ok = mbar_wait_bounded(bar + kKBarDSFull, i & 1, abort_flag, gst) &&
+                     (i + 1 == n_iter || o_ready(i + 1))))
+            break;
           tc_fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
@@ -351,7 +366,7 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
                         (i > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(bar + kKBarQEmpty + 8 * qs);
-          if (i + 1 < n_iter && !(ok = issue_dp(i + 1))) break;
+          if (i + 1 < n_iter) issue_dp(i + 1);
         }
         mma_commit(bar + kKBarAcc);
         mma_commit(bar + kKBarDrain);
@@ -458,43 +473,56 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
 }
 
 // ================================================================== dQ kernel
-// 128-key tiles, every MMA 128x128x16.  TMEM: S [0,128) and dP [128,256)
-// single-buffered, dQ [256, 256+D), dS double-buffered at [384,448) and
-// [448,512) (bf16, two per column) where the dQ MMA reads it as its A operand.
-// The softmax warps load S and dP into registers and release them at once,
-// so S/dP of tile i+1 run on the tensor core while dS of tile i is formed.
+// 128-key tiles, every MMA 128x128x16.  Q and dO are the same for the whole
+// loop, so the softmax warps copy them once into TMEM (bf16, two per column),
+// where S = Q K^T and dP = dO V^T read them as their A operand: the shared
+// memory port then carries only the K and V tiles.  TMEM: S [0,128),
+// dP [128,256), dQ [256, 256+D), Q [384, 384+D/2), dO [448, 448+D/2).
+// Warpgroup g owns key columns [64g, 64g+64) of S and dP; it writes dS (bf16,
+// two per column) over the first half of its dP columns ([128+64g, 160+64g)),
+// where the dQ MMA reads it as its A operand.
+// The softmax runs in two phases per tile: it loads S_i and releases it at
+// once (P_i stays in registers), then waits for dP_i and forms dS_i.  The
+// tensor core runs S_{i+1}, dQ_i, dP_{i+1}, ...: S_{i+1} overlaps the P phase
+// of tile i+1's predecessor, dP_{i+1} overwrites dS_i only after dQ_i has read
+// it (one issuer's MMAs run in order).
 // K tiles stream through a 3-slot ring (released after the dQ MMA), V tiles
-// through a 2-slot ring (released right after the dP MMA).
+// through a 3-slot ring (released after the dP MMA).
 constexpr int kThreadsQ = 384;  // warpgroups 0-1 softmax, warpgroup 2: TMA, MMA, 2 idle warps
 constexpr uint32_t kRegsQProducer = 56, kRegsQSoftmax = 224;
 static_assert(128 * kRegsQProducer + 256 * kRegsQSoftmax <= 384 * 168, "register split over budget");
-constexpr int kKSlots = 3, kVSlots = 2;
+constexpr int kKSlots = 3, kVSlots = 3;
 
 enum : uint32_t {
-  kQBarIn = 0,
+  kQBarQReady = 0,   // 256 arrivals: Q and dO are in TMEM
   kQBarKFull = 8,    // [3]
   kQBarKEmpty = 32,  // [3]
-  kQBarVFull = 56,   // [2]
-  kQBarVEmpty = 72,  // [2]
-  kQBarSFull = 88,
-  kQBarTFree = 96,   // 256 arrivals
-  kQBarPFull = 104,  // 256 arrivals
-  kQBarPFree = 112,  // [2]
-  kQBarAcc = 128,
-  kQBarDrain = 136,
-  kQTmemSlot = 144,
-  kQAbortSlot = 148
+  kQBarVFull = 56,   // [3]
+  kQBarVEmpty = 80,  // [3]
+  kQBarSFull = 104,
+  kQBarSFree = 112,  // 256 arrivals
+  kQBarDPFull = 120,
+  kQBarDSFull = 128, // 256 arrivals
+  kQBarAcc = 136,
+  kQBarDrain = 144,
+  kQTmemSlot = 152,
+  kQAbortSlot = 156
 };
 
-// dS = P * (dP - delta), P = exp2(scale*log2(e)*s - lse*log2(e)), for the 64
-// key columns of one query row a thread holds; with kMask, columns at or past
-// hi are 0.
+template <int D>
+struct QLayout {
+  static constexpr uint32_t kT = 128u * D * 2;  // one 128-row tile of K or V
+  static constexpr uint32_t oK = 0, oV = kKSlots * kT, oBar = oV + kVSlots * kT;
+  static constexpr uint32_t kAlloc = oBar + 256 + 1024;
+};
+
+// P = exp2(scale*log2(e)*s - lse*log2(e)) for the 64 key columns of one query
+// row a thread holds; with kMask, columns at or past hi are 0.
 template <bool kMask>
-__device__ __forceinline__ void ds_row(const uint32_t (&s)[2][32], const uint32_t (&d)[2][32], float sl, float nl,
-                                       float dlt, int hi, uint32_t (&w)[2][16]) {
+__device__ __forceinline__ void p_row(const uint32_t (&s)[2][32], float sl, float nl, int hi, float2 (&pf)[32]) {
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
-    const uint32_t *sh = s[c >> 4], *dh = d[c >> 4];
+    const uint32_t *sh = s[c >> 4];
     const int e = 2 * (c & 15);
     const float2 x = fma2(make_float2(__uint_as_float(sh[e]), __uint_as_float(sh[e + 1])), make_float2(sl, sl),
                           make_float2(nl, nl));
@@ -503,34 +531,36 @@ __device__ __forceinline__ void ds_row(const uint32_t (&s)[2][32], const uint32_
       if (2 * c >= hi) pe.x = 0.f;
       if (2 * c + 1 >= hi) pe.y = 0.f;
     }
+    pf[c] = pe;
+  }
+}
+
+// dS = P * (dP - delta) for the same 64 columns, packed to bf16.
+__device__ __forceinline__ void ds_row(const uint32_t (&d)[2][32], const float2 (&pf)[32], float dlt,
+                                       uint32_t (&w)[2][16]) {
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const uint32_t *dh = d[c >> 4];
+    const int e = 2 * (c & 15);
     const float2 y = sub2(make_float2(__uint_as_float(dh[e]), __uint_as_float(dh[e + 1])), make_float2(dlt, dlt));
-    const float2 ds = mul2(pe, y);
+    const float2 ds = mul2(pf[c], y);
     w[c >> 4][c & 15] = pack_bf16x2(ds.x, ds.y);
   }
 }
 
 template <int D>
-struct QLayout {
-  static constexpr uint32_t kT = 128u * D * 2;  // one 128-row tile (Q, dO, K or V)
-  static constexpr uint32_t oQ = 0, odO = kT, oK = 2 * kT, oV = oK + kKSlots * kT,
-                            oBar = oV + kVSlots * kT;
-  static constexpr uint32_t kAlloc = oBar + 256 + 1024;
-};
-
-template <int D>
 __global__ void __launch_bounds__(kThreadsQ, 1)
-    dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
-              const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+    dq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
               const BwdParams p) {
   using L = QLayout<D>;
   constexpr int kCh = D / 64;
-  constexpr uint32_t kColDQ = 256, kColDS = 384;
+  constexpr uint32_t kColDP = 128, kColDQ = 256, kColQ = 384, kColDO = 448;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
   uint8_t *smem = smem_raw + pad;
   const uint32_t sb = raw + pad;
-  const uint32_t sQ = sb + L::oQ, sdO = sb + L::odO, sK = sb + L::oK, sV = sb + L::oV, bar = sb + L::oBar;
+  const uint32_t sK = sb + L::oK, sV = sb + L::oV, bar = sb + L::oBar;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::oBar + kQAbortSlot);
   const volatile uint32_t *gst = p.status;
   if ((*gst & 3u) || stale_rope_table(p)) return;
@@ -546,7 +576,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   const int n_kv = p.causal ? min(n_kt, m + 1) : n_kt;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar + kQBarIn, 1);
+    mbar_init(bar + kQBarQReady, 256);
     for (int i = 0; i < kKSlots; ++i) {
       mbar_init(bar + kQBarKFull + 8 * i, 1);
       mbar_init(bar + kQBarKEmpty + 8 * i, 1);
@@ -554,11 +584,11 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
     for (int i = 0; i < kVSlots; ++i) {
       mbar_init(bar + kQBarVFull + 8 * i, 1);
       mbar_init(bar + kQBarVEmpty + 8 * i, 1);
-      mbar_init(bar + kQBarPFree + 8 * i, 1);
     }
     mbar_init(bar + kQBarSFull, 1);
-    mbar_init(bar + kQBarTFree, 256);
-    mbar_init(bar + kQBarPFull, 256);
+    mbar_init(bar + kQBarSFree, 256);
+    mbar_init(bar + kQBarDPFull, 1);
+    mbar_init(bar + kQBarDSFull, 256);
     mbar_init(bar + kQBarAcc, 1);
     mbar_init(bar + kQBarDrain, 1);
     *abort_flag = 0;
@@ -579,13 +609,8 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
     regs_dec<kRegsQProducer>();
     if (warp == kTmaWarp) {
       if (lane == 0) {
-        tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
-        mbar_arrive_expect_tx(bar + kQBarIn, 2 * L::kT);
-        for (int c = 0; c < kCh; ++c) {
-          tma_load_4d(sQ + c * 16384, &tmQ, bar + kQBarIn, c * 64, j, m * 128, rb);
-          tma_load_4d(sdO + c * 16384, &tmdO, bar + kQBarIn, c * 64, j, m * 128, rb);
-        }
+        tma_prefetch_desc(&tmV);
         int issued_k = -1, issued_v = -1;
         for (int i = 0; i < n_kv; ++i) {
           const int ks = i % kKSlots, vs = i % kVSlots;
@@ -602,7 +627,6 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         }
         if (*abort_flag) {
           volatile int never = 0;
-          mbar_wait_bounded(bar + kQBarIn, 0, &never, nullptr, 500000000ull);
           for (int i = issued_k - (kKSlots - 1); i <= issued_k; ++i)
             if (i >= 0)
               mbar_wait_bounded(bar + kQBarKFull + 8 * (i % kKSlots), (i / kKSlots) & 1, &never, nullptr,
@@ -615,46 +639,68 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       }
     } else if (warp == kMmaWarp) {
       if (lane == 0) {
-        constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);  // S, dP: both operands K-major
+        constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);  // S, dP: A (TMEM) and K, V K-major
         constexpr uint32_t idQ = idesc_bf16_f32(128, D, 0, 1);    // dQ: B (K tile) MN-major
-        // S_i = Q K_i^T and dP_i = dO V_i^T into the single S/dP buffers.
-        auto issue_sdp = [&](int i) -> bool {
-          const int ks = i % kKSlots, vs = i % kVSlots;
-          if (!mbar_wait_bounded(bar + kQBarKFull + 8 * ks, (i / kKSlots) & 1, abort_flag, gst)) return false;
-          if (!mbar_wait_bounded(bar + kQBarVFull + 8 * vs, (i / kVSlots) & 1, abort_flag, gst)) return false;
-          tc_fence_after_sync();
+        auto k_ready = [&](int i) -> bool {
+          return mbar_wait_bounded(bar + kQBarKFull + 8 * (i % kKSlots), (i / kKSlots) & 1, abort_flag, gst);
+        };
+        auto v_ready = [&](int i) -> bool {
+          return mbar_wait_bounded(bar + kQBarVFull + 8 * (i % kVSlots), (i / kVSlots) & 1, abort_flag, gst);
+        };
+        // S_i = Q K_i^T (Q: D elements 16kk.. are TMEM columns kColQ + 8kk ..);
+        // K_i has landed (the caller waited).
+        auto issue_s = [&](int i) {
+          const int ks = i % kKSlots;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_bf16_ss(tmem, smem_desc_sw128(sQ + o, 16, 1024), smem_desc_sw128(sK + ks * L::kT + o, 16, 1024),
-                        idS, kk > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_bf16_ss(tmem + 128, smem_desc_sw128(sdO + o, 16, 1024),
-                        smem_desc_sw128(sV + vs * L::kT + o, 16, 1024), idS, kk > 0 ? 1u : 0u);
+            mma_bf16_ts(tmem, tmem + kColQ + kk * 8, smem_desc_sw128(sK + ks * L::kT + o, 16, 1024), idS,
+                        kk > 0 ? 1u : 0u);
           }
           mma_commit(bar + kQBarSFull);
-          mma_commit(bar + kQBarVEmpty + 8 * vs);
-          return true;
         };
-        bool ok = mbar_wait_bounded(bar + kQBarIn, 0, abort_flag, gst);
-        if (ok && n_kv > 0) ok = issue_sdp(0);
-        for (int i = 0; ok && i < n_kv; ++i) {
-          // the softmax has read S_i and dP_i: the next pair may overwrite them
-          if (!(ok = mbar_wait_bounded(bar + kQBarTFree, i & 1, abort_flag, gst))) break;
-          if (i + 1 < n_kv && !(ok = issue_sdp(i + 1))) break;
-          // dQ += dS_i K_i, dS_i read from TMEM (8 keys... 16 keys = 8 columns per MMA)
-          if (!(ok = mbar_wait_bounded(bar + kQBarPFull, i & 1, abort_flag, gst))) break;
-          tc_fence_after_sync();
-          const int ks = i % kKSlots, b = i & 1;
+        // dP_i = dO V_i^T (V_i has landed: the caller waited).
+        auto issue_dp = [&](int i) {
+          const int vs = i % kVSlots;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ts(tdQ, tmem + kColDS + b * 64 + kk * 8,
-                        smem_desc_sw128(sK + ks * L::kT + kk * 2048, 16384, 1024), idQ, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_bf16_ts(tmem + kColDP, tmem + kColDO + kk * 8, smem_desc_sw128(sV + vs * L::kT + o, 16, 1024),
+                        idS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar + kQBarDPFull);
+          mma_commit(bar + kQBarVEmpty + 8 * vs);
+        };
+        // Every wait of a burst is taken before any of its MMAs is issued (a
+        // thread with MMAs in flight stalls on its next shared-memory access).
+        bool ok = mbar_wait_bounded(bar + kQBarQReady, 0, abort_flag, gst) && (n_kv == 0 || (k_ready(0) && v_ready(0)));
+        if (ok && n_kv > 0) {
+          tc_fence_after_sync();
+          issue_s(0);
+          issue_dp(0);
+        }
+        for (int i = 0; ok && i < n_kv; ++i) {
+          // burst 1: S_{i+1}, once the softmax has loaded S_i
+          if (i + 1 < n_kv) {
+            if (!(ok = mbar_wait_bounded(bar + kQBarSFree, i & 1, abort_flag, gst) && k_ready(i + 1))) break;
+            tc_fence_after_sync();
+            issue_s(i + 1);
+          }
+          // burst 2: dQ += dS_i K_i, dP_{i+1}.  Keys 16kk.. of dS_i are columns
+          // 8kk.. of warpgroup 0's half (kk < 4) or of warpgroup 1's half at +64.
+          if (!(ok = mbar_wait_bounded(bar + kQBarDSFull, i & 1, abort_flag, gst) &&
+                     (i + 1 == n_kv || v_ready(i + 1))))
+            break;
+          tc_fence_after_sync();
+          const int ks = i % kKSlots;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t ac = kColDP + (kk < 4 ? 0u : 64u) + (uint32_t)(kk & 3) * 8;
+            mma_bf16_ts(tdQ, tmem + ac, smem_desc_sw128(sK + ks * L::kT + kk * 2048, 16384, 1024), idQ,
+                        (i > 0 || kk > 0) ? 1u : 0u);
+          }
           mma_commit(bar + kQBarKEmpty + 8 * ks);
-          mma_commit(bar + kQBarPFree + 8 * b);
+          if (i + 1 < n_kv) issue_dp(i + 1);
         }
         mma_commit(bar + kQBarAcc);
         mma_commit(bar + kQBarDrain);
@@ -671,6 +717,28 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
     const uint32_t lane_base = (uint32_t)(w4 * 32) << 16;
     const int qi = m * 128 + r;
     const bool live = qi < p.S;
+    {
+      // Warpgroup 0 copies this thread's Q row, warpgroup 1 its dO row, into
+      // TMEM (rows past S are zero).
+      const __nv_bfloat16 *src = (g == 0 ? p.q : p.dout) + (((size_t)rb * p.S + (live ? qi : 0)) * p.hp + j) * D;
+      const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t x[32];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint4 u = live ? __ldg(s4 + c * 8 + v) : make_uint4(0u, 0u, 0u, 0u);
+          x[4 * v] = u.x;
+          x[4 * v + 1] = u.y;
+          x[4 * v + 2] = u.z;
+          x[4 * v + 3] = u.w;
+        }
+        tmem_st32(tmem + lane_base + (g == 0 ? kColQ : kColDO) + c * 32, x);
+      }
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(bar + kQBarQReady);
+    }
     const size_t lrow = ((size_t)rb * p.hp + j) * p.S + (live ? qi : 0);
     const float nl2 = live ? p.nlse[lrow] : 0.f;
     const float dlt = live ? p.delta[lrow] : 0.f;
@@ -678,38 +746,39 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
     for (int i = 0; i < n_kv; ++i) {
       if (!warp_wait(bar + kQBarSFull, i & 1, abort_flag, gst)) { ok = false; break; }
       tc_fence_after_sync();
-      uint32_t sr[2][32], dr[2][32];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        tmem_ld32(tmem + lane_base + g * 64 + h * 32, sr[h]);
-        tmem_ld32(tmem + lane_base + 128 + g * 64 + h * 32, dr[h]);
-      }
+      uint32_t sr[2][32];
+      tmem_ld32(tmem + lane_base + g * 64, sr[0]);
+      tmem_ld32(tmem + lane_base + g * 64 + 32, sr[1]);
       tmem_wait_ld();
       tc_fence_before_sync();
-      mbar_arrive(bar + kQBarTFree);
+      mbar_arrive(bar + kQBarSFree);
       reg_fence(sr[0]);
       reg_fence(sr[1]);
-      reg_fence(dr[0]);
-      reg_fence(dr[1]);
       const int k0 = i * 128 + g * 64;
       // Key k0 + c is seen by query qi iff k0 + c <= qi (causal) and k0 + c < S:
       // columns [0, hi) of this warpgroup's 64 are valid.
       const int hi = min(p.causal ? qi - k0 + 1 : 64, p.S - k0);
-      uint32_t wd[2][16];
+      float2 pf[32];
       if (__all_sync(0xffffffffu, hi >= 64))
-        ds_row<false>(sr, dr, p.scale_log2, nl2, dlt, hi, wd);
+        p_row<false>(sr, p.scale_log2, nl2, hi, pf);
       else
-        ds_row<true>(sr, dr, p.scale_log2, nl2, dlt, hi, wd);
-      // dS buffer i&1 is free once the dQ MMA of tile i-2 has read it.
-      if (i >= 2 && !warp_wait(bar + kQBarPFree + 8 * (i & 1), ((i - 2) >> 1) & 1, abort_flag, gst)) {
-        ok = false;
-        break;
-      }
-      tmem_st16(tmem + lane_base + kColDS + (i & 1) * 64 + g * 32, wd[0]);
-      tmem_st16(tmem + lane_base + kColDS + (i & 1) * 64 + g * 32 + 16, wd[1]);
+        p_row<true>(sr, p.scale_log2, nl2, hi, pf);
+
+      if (!warp_wait(bar + kQBarDPFull, i & 1, abort_flag, gst)) { ok = false; break; }
+      tc_fence_after_sync();
+      uint32_t dr[2][32];
+      tmem_ld32(tmem + lane_base + kColDP + g * 64, dr[0]);
+      tmem_ld32(tmem + lane_base + kColDP + g * 64 + 32, dr[1]);
+      tmem_wait_ld();
+      reg_fence(dr[0]);
+      reg_fence(dr[1]);
+      uint32_t wd[2][16];
+      ds_row(dr, pf, dlt, wd);
+      tmem_st16(tmem + lane_base + kColDP + g * 64, wd[0]);
+      tmem_st16(tmem + lane_base + kColDP + g * 64 + 16, wd[1]);
       tmem_wait_st();
       tc_fence_before_sync();
-      mbar_arrive(bar + kQBarPFull);
+      mbar_arrive(bar + kQBarDSFull);
     }
     if (ok) ok = warp_wait(bar + kQBarAcc, 0, abort_flag, gst);
     if (ok && (D == 128 || g == 0)) {
@@ -768,6 +837,8 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   bp.scale_log2 = bp.scale * kLog2e;
   bp.nlse = nlse;
   bp.delta = delta;
+  bp.q = static_cast<const __nv_bfloat16 *>(q);
+  bp.dout = static_cast<const __nv_bfloat16 *>(do_head);
   if (p.use_rope) {
     const WorkspaceLayout W = workspace_layout(p);
     bp.rope_cos = reinterpret_cast<const float *>(static_cast<const uint8_t *>(ws) + W.rope);
@@ -793,7 +864,7 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
                                                                               mL, mDl, bp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dq_kernel<D><<<(unsigned)q_blocks, kThreadsQ, QLayout<D>::kAlloc, st>>>(mQ128, mdO128, mK128, mV128, bp);
+  dq_kernel<D><<<(unsigned)q_blocks, kThreadsQ, QLayout<D>::kAlloc, st>>>(mK128, mV128, bp);
   return cudaGetLastError();
 }
 

@@ -22,6 +22,12 @@
 //               PV_X(j) has finished: the softmax can then rescale O_X
 //               without any further barrier.  S_X(j+1) overwrites P_X(j) only
 //               after PV_X(j) has read it (one issuer's MMAs run in order).
+//               The issuer takes every wait a burst PV_X(j) S_X(j+1) needs
+//               before issuing any of it: a thread with MMAs in flight stalls
+//               on its next shared-memory access (such as a barrier wait)
+//               until they have been taken by the tensor core, and each such
+//               stall leaves a gap in the pipe, so there are two per key tile
+//               rather than one per operand.
 //   warps 0-3   softmax of tile A, warps 4-7 of tile B: thread i of a
 //               warpgroup owns query row i = TMEM lane i.  It reads its score
 //               row from TMEM, keeps a running max in the base-2 domain and
@@ -215,11 +221,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // -------------------------------------------------------------- MMA
         constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);  // Q, K both K-major
         constexpr uint32_t idPV = idesc_bf16_f32(BM, D, 0, 1);  // P (TMEM), V MN-major
-        auto issue_s = [&](int x, int t) -> bool {
+        // S_x(t) = Q_x K_t^T (K_t has landed: the caller waited for it).
+        auto issue_s = [&](int x, int t) {
           const int n = 2 * t;
-          if (!mbar_wait_bounded(bar + kBarKVFull + 8 * ring_slot(n), ring_parity(n), abort_flag, gst))
-            return false;
-          tc_fence_after_sync();
           const uint32_t kt = sKV + ring_slot(n) * L::kTile;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -228,14 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         smem_desc_sw128(kt + koff, 16, 1024), idS, kk > 0 ? 1u : 0u);
           }
           mma_commit(bar + kBarSFull + 8 * x);
-          return true;
         };
-        auto issue_pv = [&](int x, int t) -> bool {
+        // O_x += P_x(t) V_t (P_x(t) published and V_t landed: the caller waited).
+        auto issue_pv = [&](int x, int t) {
           const int n = 2 * t + 1;
-          if (!mbar_wait_bounded(bar + kBarPFull + 8 * x, t & 1, abort_flag, gst)) return false;
-          if (!mbar_wait_bounded(bar + kBarKVFull + 8 * ring_slot(n), ring_parity(n), abort_flag, gst))
-            return false;
-          tc_fence_after_sync();
           const uint32_t vt = sKV + ring_slot(n) * L::kTile;
           // keys 16kk..16kk+15 of P_X are TMEM columns x*BN + 8kk ..
 #pragma unroll
@@ -243,26 +243,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t b = smem_desc_sw128(vt + kk * 16 * 128, kChunkBytes, 1024);
             mma_bf16_ts(tmem + 2 * BN + x * D, tmem + x * BN + kk * 8, b, idPV, (t > 0 || kk > 0) ? 1u : 0u);
           }
-          return true;
         };
-        bool ok = mbar_wait_bounded(bar + kBarQFull, 0, abort_flag, gst);
-        if (ok && nA > 0) ok = issue_s(0, 0);
-        if (ok) ok = issue_s(1, 0);
+        auto kv_ready = [&](int n) -> bool {
+          return mbar_wait_bounded(bar + kBarKVFull + 8 * ring_slot(n), ring_parity(n), abort_flag, gst);
+        };
+        bool ok = mbar_wait_bounded(bar + kBarQFull, 0, abort_flag, gst) && kv_ready(0);
+        if (ok && nA > 0) issue_s(0, 0);
+        if (ok) issue_s(1, 0);
         if (ok) mma_commit(bar + kBarKVEmpty + 8 * ring_slot(0));
         for (int t = 0; ok && t < nB; ++t) {
+          // every wait of tile A's burst first: P_A(t), V_t and (when A goes on) K_{t+1}
           if (t < nA) {
-            if (!(ok = issue_pv(0, t))) break;
+            if (!(ok = mbar_wait_bounded(bar + kBarPFull, t & 1, abort_flag, gst) && kv_ready(2 * t + 1) &&
+                       (t == nA - 1 || kv_ready(2 * t + 2))))
+              break;
+            tc_fence_after_sync();
+            issue_pv(0, t);
             if (t == nA - 1)
               mma_commit(bar + kBarODone);
-            else if (!(ok = issue_s(0, t + 1)))
-              break;
+            else
+              issue_s(0, t + 1);
           }
-          if (!(ok = issue_pv(1, t))) break;
+          // then tile B's: P_B(t), V_t and K_{t+1} (again only if A skipped them)
+          if (!(ok = mbar_wait_bounded(bar + kBarPFull + 8, t & 1, abort_flag, gst) &&
+                     (t < nA || kv_ready(2 * t + 1)) && (t == nB - 1 || kv_ready(2 * t + 2))))
+            break;
+          tc_fence_after_sync();
+          issue_pv(1, t);
           mma_commit(bar + kBarKVEmpty + 8 * ring_slot(2 * t + 1));
           if (t == nB - 1) {
             mma_commit(bar + kBarODone + 8);
           } else {
-            if (!(ok = issue_s(1, t + 1))) break;
+            issue_s(1, t + 1);
             mma_commit(bar + kBarKVEmpty + 8 * ring_slot(2 * t + 2));
           }
         }
