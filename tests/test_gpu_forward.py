@@ -180,3 +180,32 @@ def test_stale_rope_table_is_flagged():
     U.ulysses_pack_qkv(run.prob, b.q_seq, b.k_seq, b.v_seq, b.q_head, b.k_head, b.v_head, b.ws)
     torch.cuda.synchronize()
     assert U.ulysses_read_status(b.ws) & U.STATUS_ROPE_TABLE
+
+
+@pytest.mark.parametrize("slope", [1.25, -1.25])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("D", [64, 128])
+def test_forward_moving_reference(slope, causal, D):
+    """Scores that rise (or fall) by about 20 in the base-2 domain per 128-key
+    tile: every query row's maximum moves far past the first tile's, so the
+    kernel's reference must move (and O, l be rescaled) on nearly every tile;
+    falling scores drive the later tiles' P to underflow.  Each head's query
+    rows are one random vector x and key s is s * slope * x / |x|^2, so
+    q.k = s * slope exactly up to the bf16 rounding both sides share."""
+    w = wl(2, 1, 768, 4, 2, D, causal=causal, rope=False)
+    g = torch.Generator().manual_seed(11)
+    x = torch.randn(w.n_kv_head, D, generator=g)
+    xq = x.repeat_interleave(w.n_head // w.n_kv_head, dim=0)          # query head j uses kv head j / group
+    q = xq.expand(w.B, w.S, w.n_head, D).clone()
+    pos = torch.arange(w.S, dtype=torch.float32).view(1, w.S, 1, 1)
+    k = pos * slope * (x / (x * x).sum(-1, keepdim=True)).view(1, 1, w.n_kv_head, D)
+    v = torch.randn(w.B, w.S, w.n_kv_head, D, generator=g)
+    inputs = {"q": q.to(torch.bfloat16), "k": k.to(torch.bfloat16), "v": v.to(torch.bfloat16)}
+    run = GpuRun(w, inputs=inputs)
+    run.forward()
+    xin = oracle_inputs(run.inputs)
+    want = oracle.forward(oracle_problem(w), xin["q"], xin["k"], xin["v"])
+    got_o = to64(run.buf.o_seq)
+    want_o = np.stack([a.reshape(w.B, w.Sl, -1) for a in want["o_seq"]])
+    assert_close(got_o, want_o, w, "o_seq")
+    assert np.abs(to64(run.buf.lse) - np.stack(want["lse"])).max() <= LSE_BF16_MAX_ABS

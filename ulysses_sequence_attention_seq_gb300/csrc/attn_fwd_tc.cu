@@ -30,10 +30,11 @@
 //               rather than one per operand.
 //   warps 0-3   softmax of tile A, warps 4-7 of tile B: thread i of a
 //               warpgroup owns query row i = TMEM lane i.  It reads its score
-//               row from TMEM, keeps a running max in the base-2 domain and
-//               rescales its TMEM accumulator row only when the max grows by
-//               more than 2^8 (otherwise the stale max stays: every exponent is
-//               <= 2^8, exact in fp32 and bf16), writes P (bf16, two keys per
+//               row from TMEM, takes the row maximum (base-2 domain) on the
+//               first key tile only and afterwards keeps that reference until
+//               a tile's row sum of P passes 2^16, when it moves the reference
+//               to the new maximum and rescales its TMEM accumulator row and
+//               the row sum (so no maximum pass on most tiles), writes P (bf16, two keys per
 //               32-bit column) over the first 64 columns of its S row, where
 //               the PV MMA reads it as its A operand straight from TMEM, and at
 //               the end divides by the row sum and stores O (bf16) and the LSE.
@@ -318,62 +319,84 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < BN; ++c)
           if (c > lim) s[c >> 5][c & 31] = __float_as_uint(-INFINITY);
       }
-      // eight independent chains of three-input maxima over 16 columns each
-      float mx[8];
+      // Row maximum of the raw scores: eight independent chains of
+      // three-input maxima over 16 columns each.
+      auto row_max = [&]() -> float {
+        float mx[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t *r = &s[i >> 1][(i & 1) * 16];
-        float m = max3(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]));
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t *r = &s[i >> 1][(i & 1) * 16];
+          float m = max3(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]));
 #pragma unroll
-        for (int e = 3; e < 15; e += 2) m = max3(m, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
-        mx[i] = fmaxf(m, __uint_as_float(r[15]));
-      }
-      const float mraw = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-      const float ms = mraw * sl2;
-      const bool need = ms > m_used + 8.0f;  // first tile: m_used = -inf
-      if (__any_sync(0xffffffffu, need)) {
-        // The S_X(t) commit we waited on also covers PV_X(t-1): O_X is final
-        // for tiles < t and no MMA touches it until P_X(t) is published.
-        const float alpha = need ? ex2(m_used - ms) : 1.0f;
-        if (t > 0) {
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tO + c * 32, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              const float2 v = mul2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
-                                    make_float2(alpha, alpha));
-              r[e] = __float_as_uint(v.x);
-              r[e + 1] = __float_as_uint(v.y);
-            }
-            tmem_st32(tO + c * 32, r);
-          }
-          tmem_wait_st();
+          for (int e = 3; e < 15; e += 2) m = max3(m, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+          mx[i] = fmaxf(m, __uint_as_float(r[15]));
         }
-        if (need) {
-          l *= alpha;
+        return max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+      };
+      // P = exp2(scale*log2(e)*s - m) into the first 64 columns of S (bf16,
+      // two keys per column); returns the row's sum of P.
+      auto exps = [&](float m) -> float {
+        const float2 sl22 = make_float2(sl2, sl2), nb2 = make_float2(-m, -m);
+        float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          // keys [32c, 32c+32) -> P columns [16c, 16c+16) of this row
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float2 a =
+                fma2(make_float2(__uint_as_float(s[c][2 * e]), __uint_as_float(s[c][2 * e + 1])), sl22, nb2);
+            const float2 pe = make_float2(ex2(a.x), ex2(a.y));
+            rs[e & 1] = add2(rs[e & 1], pe);
+            w[e] = pack_bf16x2(pe.x, pe.y);
+          }
+          tmem_st16(tS + c * 16, w);
+        }
+        return (rs[0].x + rs[1].x) + (rs[0].y + rs[1].y);
+      };
+      // The reference m_used only guards against overflow (the exponentials'
+      // relative precision does not depend on it), so it is set from the row
+      // maximum on the first tile and afterwards moved only when a tile's row
+      // sum of P exceeds 2^16 (some score more than 9 above it): then that
+      // tile's P is formed again against the new maximum and O and l are
+      // rescaled.  P <= 2^16 keeps l and O at most 2^24 times |V|.
+      float tsum = 0.f;
+      bool set_ref = t == 0, need = true;
+#pragma unroll 1
+      for (int pass = 0; pass < 2; ++pass) {
+        if (set_ref) {
+          // t == 0: m_used = -inf.  Otherwise the S_X(t) commit we waited on
+          // also covers PV_X(t-1): O_X is final for tiles < t and no MMA
+          // touches it until P_X(t) is published.
+          const float ms = need ? fmaxf(row_max() * sl2, m_used) : m_used;
+          if (t > 0) {
+            const float alpha = ex2(m_used - ms);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld32(tO + c * 32, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; e += 2) {
+                const float2 v = mul2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
+                                      make_float2(alpha, alpha));
+                r[e] = __float_as_uint(v.x);
+                r[e + 1] = __float_as_uint(v.y);
+              }
+              tmem_st32(tO + c * 32, r);
+            }
+            tmem_wait_st();
+            l *= alpha;
+          }
           m_used = ms;
         }
+        tsum = exps(m_used);
+        if (set_ref) break;
+        need = !(tsum <= 65536.0f);  // also true for inf
+        if (!__any_sync(0xffffffffu, need)) break;
+        set_ref = true;
       }
-      const float2 sl22 = make_float2(sl2, sl2), nb2 = make_float2(-m_used, -m_used);
-      float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        // keys [32c, 32c+32) -> P columns [16c, 16c+16) of this row
-        uint32_t w[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float2 a =
-              fma2(make_float2(__uint_as_float(s[c][2 * e]), __uint_as_float(s[c][2 * e + 1])), sl22, nb2);
-          const float2 pe = make_float2(ex2(a.x), ex2(a.y));
-          rs[e & 1] = add2(rs[e & 1], pe);
-          w[e] = pack_bf16x2(pe.x, pe.y);
-        }
-        tmem_st16(tS + c * 16, w);
-      }
-      l += (rs[0].x + rs[1].x) + (rs[0].y + rs[1].y);
+      l += tsum;
       tmem_wait_st();
       tc_fence_before_sync();
       mbar_arrive(bar + kBarPFull + 8 * x);
