@@ -39,6 +39,12 @@ METRIC = "tokens/s + attn TFLOP/s (S=32K, 32 heads, P=8 virtual); seq↔head per
 
 # ------------------------------------------------------------------ helpers
 
+# DRAM bytes (read + write) per launch of a kernel on a workload, from one ncu
+# capture of this build (profiles/ names the command); a kernel changed since
+# its capture has no entry.
+TRAFFIC = {}
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -141,10 +147,13 @@ def run_ulysses(args, w, rank, world):
     U.ulysses_workspace_init(prob, buf.ws)
     torch.cuda.synchronize()
 
-    names = ["pack_qkv", "attn_fwd", "unpack_out"] + (["attn_bwd"] if backward else [])
+    names = ["pack_qkv", "attn_fwd", "unpack_out"] + (["bwd_prepare", "bwd_dkdv", "bwd_dq"] if backward else [])
     launches_per_step = 3 + (3 if backward else 0)
 
-    def step(evs=None):
+    def step(evs=None, split=True):
+        """One pass of the whole path.  With `split` the backward runs as its
+        three entry points (the same launches as ulysses_attn_bwd) so that each
+        kernel gets its own events."""
         def mark(i):
             if evs is not None:
                 evs[i].record(stream)
@@ -156,8 +165,15 @@ def run_ulysses(args, w, rank, world):
         U.ulysses_unpack_out(prob, buf.o_head, buf.o_seq)
         mark(3)
         if backward:
-            buf.backward()
-            mark(4)
+            if split:
+                U.ulysses_attn_bwd_prepare(prob, buf.o_head, buf.lse, buf.do_seq, buf.ws)
+                mark(4)
+                U.ulysses_attn_bwd_dkdv(prob, buf.q_head, buf.k_head, buf.v_head, buf.dk_seq, buf.dv_seq, buf.ws)
+                mark(5)
+                U.ulysses_attn_bwd_dq(prob, buf.q_head, buf.k_head, buf.v_head, buf.dq_seq, buf.ws)
+                mark(6)
+            else:
+                buf.backward()
 
     for _ in range(args.warmup):
         step()
@@ -198,7 +214,7 @@ def run_ulysses(args, w, rank, world):
         buf.v_seq.copy_(host["v"], non_blocking=True)
         if backward:
             buf.do_seq.copy_(host["do"], non_blocking=True)
-        step()
+        step(split=False)
         o_host.copy_(buf.o_seq, non_blocking=True)
         if backward:
             for h, d in zip(grads_host, (buf.dq_seq, buf.dk_seq, buf.dv_seq)):
@@ -428,11 +444,30 @@ def main():
     fl = attn_fwd_flops(w)
     es = 2 if w.dtype == "bf16" else 4
     attn_ms = per["attn_fwd"]
-    bwd_ms = per.get("attn_bwd")
+    bwd_parts = ("bwd_prepare", "bwd_dkdv", "bwd_dq")
+    bwd_ms = sum(per[k] for k in bwd_parts) if "bwd_dkdv" in per else None
     bwd_tflops = 2.0 * fl / (bwd_ms * 1e-3) / 1e12 if bwd_ms else None
     attn_tflops = fl / (attn_ms * 1e-3) / 1e12
     pack_gbs = permute_bytes(w, es) / (per["pack_qkv"] * 1e-3) / 1e9
     unpack_gbs = 2.0 * w.B * w.S * w.n_head * w.head_dim * es / (per["unpack_out"] * 1e-3) / 1e9
+    # Tensor-core kernels: algorithmic FLOPs per launch (the products the
+    # method defines: forward S and PV; backward dV, dP, dQ, dK, each half a
+    # forward) and the FLOPs each kernel executes (dK/dV and dQ both recompute
+    # S, dQ also dP).
+    tc = {"attn_fwd": ("attn_fwd_tc_kernel", fl, fl)}
+    if bwd_ms:
+        tc["bwd_dkdv"] = ("dkdv_kernel", 1.5 * fl, 2.0 * fl)
+        tc["bwd_dq"] = ("dq_kernel", 0.5 * fl, 1.5 * fl)
+    kernels = {}
+    for k, (kname, alg, exe) in tc.items():
+        a_tf = alg / (per[k] * 1e-3) / 1e12
+        kernels[k] = {"kernel": f"{kname}<{w.head_dim}>", "ms": per[k], "algorithmic_tflop": alg / 1e12,
+                      "achieved_tflops": a_tf, "frac": a_tf / tf_sust,
+                      "executed_tflops": exe / (per[k] * 1e-3) / 1e12,
+                      "executed_frac": exe / (per[k] * 1e-3) / 1e12 / tf_sust}
+    dominant = max(kernels, key=lambda k: kernels[k]["ms"])
+    dk = kernels[dominant]
+    fwd_tokens = job_throughput(tokens, (per["pack_qkv"] + attn_ms + per["unpack_out"]) * 1e-3, world)
     line = {
         "metric": METRIC, "value": job_throughput(tokens, ms * 1e-3, world), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -443,16 +478,21 @@ def main():
                    "passes": "fwd+bwd" if r["backward"] else "fwd",
                    "l2": "inputs larger than L2 (Q/K/V/O each >= 128 MiB); no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU, P virtual ranks"},
+        "fwd_tokens_per_s": fwd_tokens,
         "attn_fwd_tflops": attn_tflops, "attn_fwd_ms": attn_ms,
         "attn_bwd_tflops": bwd_tflops, "attn_bwd_ms": bwd_ms,
         "attn_bwd_flops_note": "backward algorithmic FLOPs = 2x forward (dV, dP, dQ, dK); the QK^T recompute is not counted",
         "pack_gbs": pack_gbs, "unpack_gbs": unpack_gbs,
         "kernel_ms": per,
-        "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": tf_sust, "unit": "TFLOP/s",
-                     "frac": attn_tflops / tf_sust, "traffic": None,
-                     "peak_source": f"{peak_src} bf16 sustained",
-                     "kernel": "attn_fwd_tc_kernel<128>"},
-        "secondary_rooflines": {"pack_qkv": {"bound": "hbm", "achieved": pack_gbs, "peak": hbm, "unit": "GB/s",
+        "tensor_kernels": kernels,
+        "roofline": {"bound": "tensor", "achieved": dk["achieved_tflops"], "peak": tf_sust, "unit": "TFLOP/s",
+                     "frac": dk["frac"], "traffic": TRAFFIC.get((dominant, w.name)),
+                     "peak_source": f"{peak_src} bf16 sustained", "kernel": dk["kernel"],
+                     "note": "dominant kernel by time; achieved counts its algorithmic products only"},
+        "secondary_rooflines": {**{k: {"bound": "tensor", "achieved": v["achieved_tflops"], "peak": tf_sust,
+                                       "unit": "TFLOP/s", "frac": v["frac"], "traffic": TRAFFIC.get((k, w.name))}
+                                   for k, v in kernels.items() if k != dominant},
+                                "pack_qkv": {"bound": "hbm", "achieved": pack_gbs, "peak": hbm, "unit": "GB/s",
                                              "frac": pack_gbs / hbm},
                                 "unpack_out": {"bound": "hbm", "achieved": unpack_gbs, "peak": hbm, "unit": "GB/s",
                                                "frac": unpack_gbs / hbm}},

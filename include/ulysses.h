@@ -190,6 +190,37 @@ int ulysses_attn_bwd(const ulysses_problem *prob, const void *q_head, const void
                      size_t ws_bytes, ulysses_stream_t stream);
 
 /*
+ * The backward in its three steps, for callers that schedule or time them
+ * separately; ulysses_attn_bwd is exactly these three calls in this order on
+ * one stream, and the results are identical.
+ *
+ * ulysses_attn_bwd_prepare: the seq -> head All-to-All of the output gradient
+ * ("Sequence Parallelism II", §6) together with delta_i = dO_i . O_i and the
+ * rescaled log-sum-exp, written into the workspace `ws` (phase 1, prepared by
+ * ulysses_workspace_init).  Reads o_head and lse from ulysses_attn_fwd and
+ * do_seq [P][B][Sl][H].
+ *
+ * ulysses_attn_bwd_dkdv: dK and dV per kv-head (summed over the q-heads that
+ * share it), then head -> seq into dk_seq / dv_seq [P][B][Sl][n_kv_head][D],
+ * with the RoPE rotation undone on dK.  Reads the head-layout q/k/v from
+ * ulysses_pack_qkv and what ulysses_attn_bwd_prepare left in `ws`.
+ *
+ * ulysses_attn_bwd_dq: dQ per q-head, then head -> seq into dq_seq
+ * [P][B][Sl][n_head][D] with the RoPE rotation undone.  Same inputs as the
+ * dK/dV step; the two may run in either order after the prepare step.
+ *
+ * bf16 and head_dim 64 or 128 (else ULYSSES_ERR_UNSUPPORTED); the errors and
+ * ownership rules of ulysses_attn_bwd apply to each.
+ */
+int ulysses_attn_bwd_prepare(const ulysses_problem *prob, const void *o_head, const float *lse,
+                             const void *do_seq, void *ws, size_t ws_bytes, ulysses_stream_t stream);
+int ulysses_attn_bwd_dkdv(const ulysses_problem *prob, const void *q_head, const void *k_head,
+                          const void *v_head, void *dk_seq, void *dv_seq, void *ws, size_t ws_bytes,
+                          ulysses_stream_t stream);
+int ulysses_attn_bwd_dq(const ulysses_problem *prob, const void *q_head, const void *k_head,
+                        const void *v_head, void *dq_seq, void *ws, size_t ws_bytes, ulysses_stream_t stream);
+
+/*
  * The backward for callers that cannot allocate device memory.
  *
  * The paper has no counterpart to this entry point (the pages describe no

@@ -8,6 +8,7 @@ import torch
 import oracle
 from pathcheck import GpuRun, assert_close, oracle_inputs, oracle_problem, to64
 from test_gpu_forward import sample_rows, wl
+from ulysses_sequence_attention_seq_gb300 import binding as U
 from ulysses_sequence_attention_seq_gb300.synthetic import WORKLOADS
 
 pytestmark = pytest.mark.gpu
@@ -78,3 +79,26 @@ def test_backward_workloads(name):
             sel_g = got[b][rows][:, heads]
             sel_r = ref[b][rows][:, heads]
             assert_close(sel_g, sel_r, w, f"{name} rank {r} kv-head {kl}")
+
+
+@pytest.mark.parametrize("order", ["dkdv_first", "dq_first"])
+def test_backward_steps_equal_composed_call(order):
+    """ulysses_attn_bwd_prepare + _dkdv + _dq (either order of the last two)
+    give exactly what ulysses_attn_bwd gives."""
+    w = WORKLOADS["C3"].with_(S=1024)
+    run = GpuRun(w, backward=True)
+    run.forward()
+    run.backward()
+    b = run.buf
+    ref = [t.clone() for t in (b.dq_seq, b.dk_seq, b.dv_seq)]
+    for t in (b.dq_seq, b.dk_seq, b.dv_seq):
+        t.zero_()
+    U.ulysses_attn_bwd_prepare(run.prob, b.o_head, b.lse, b.do_seq, b.ws)
+    steps = [lambda: U.ulysses_attn_bwd_dkdv(run.prob, b.q_head, b.k_head, b.v_head, b.dk_seq, b.dv_seq, b.ws),
+             lambda: U.ulysses_attn_bwd_dq(run.prob, b.q_head, b.k_head, b.v_head, b.dq_seq, b.ws)]
+    for f in (steps if order == "dkdv_first" else steps[::-1]):
+        f()
+    torch.cuda.synchronize()
+    assert U.ulysses_read_status(b.ws) == 0
+    for got, want in zip((b.dq_seq, b.dk_seq, b.dv_seq), ref):
+        assert torch.equal(got, want)

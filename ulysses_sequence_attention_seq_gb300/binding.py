@@ -109,6 +109,9 @@ def lib():
         L.ulysses_attn_fwd_folded.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_attn_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_attn_bwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.ulysses_attn_bwd_prepare.argtypes = [P, vp, vp, vp, vp, sz, vp]
+        L.ulysses_attn_bwd_dkdv.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.ulysses_attn_bwd_dq.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_status_string.argtypes = [ctypes.c_int]
         L.ulysses_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -182,6 +185,27 @@ def ulysses_attn_bwd(prob, q_head, k_head, v_head, o_head, lse, do_seq, dq_seq, 
         ctypes.byref(prob.c()), _ptr(q_head), _ptr(k_head), _ptr(v_head), _ptr(o_head), _ptr(lse),
         _ptr(do_seq), _ptr(dq_seq), _ptr(dk_seq), _ptr(dv_seq), _ptr(ws), ws.numel() * ws.element_size(),
         _stream(stream)))
+
+
+def ulysses_attn_bwd_prepare(prob, o_head, lse, do_seq, ws, stream=None):
+    """Step 1 of the backward: dO seq -> head, delta and the rescaled LSE into ws."""
+    _check("ulysses_attn_bwd_prepare", lib().ulysses_attn_bwd_prepare(
+        ctypes.byref(prob.c()), _ptr(o_head), _ptr(lse), _ptr(do_seq), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def ulysses_attn_bwd_dkdv(prob, q_head, k_head, v_head, dk_seq, dv_seq, ws, stream=None):
+    """Step 2 of the backward: dK, dV and their head -> seq All-to-All."""
+    _check("ulysses_attn_bwd_dkdv", lib().ulysses_attn_bwd_dkdv(
+        ctypes.byref(prob.c()), _ptr(q_head), _ptr(k_head), _ptr(v_head), _ptr(dk_seq), _ptr(dv_seq),
+        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def ulysses_attn_bwd_dq(prob, q_head, k_head, v_head, dq_seq, ws, stream=None):
+    """Step 3 of the backward: dQ and its head -> seq All-to-All."""
+    _check("ulysses_attn_bwd_dq", lib().ulysses_attn_bwd_dq(
+        ctypes.byref(prob.c()), _ptr(q_head), _ptr(k_head), _ptr(v_head), _ptr(dq_seq), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def ulysses_attn_bwd_noalloc(prob, q_head, k_head, v_head, o_head, lse, do_seq, dq_seq, dk_seq,

@@ -809,10 +809,13 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   if (threadIdx.x == 0 && *abort_flag) atomicOr(p.status, (uint32_t)ULYSSES_STATUS_BWD_TIMEOUT);
 }
 
+// Which of the two backward kernels a launch runs.
+enum BwdPart { kBwdDkDv = 1, kBwdDq = 2 };
+
 template <int D>
 cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void *q, const void *k,
                      const void *v, const void *do_head, const float *nlse, const float *delta,
-                     const void *ws, void *dq, void *dk, void *dv, uint32_t *status, cudaStream_t st) {
+                     const void *ws, void *dq, void *dk, void *dv, uint32_t *status, int parts, cudaStream_t st) {
   const int hp = p.n_head / p.P, kvp = p.n_kv_head / p.P, PB = p.P * p.B;
   CUtensorMap mK128, mV128, mL, mDl, mQ128, mdO128;
   bool ok = make_act_map(enc, &mK128, k, D, kvp, p.S, PB, 128) &&
@@ -855,17 +858,33 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   const long long kv_blocks = (long long)((p.S + 127) / 128) * PB * kvp;
   const long long q_blocks = (long long)((p.S + 127) / 128) * PB * hp;
   if (kv_blocks > 0x7fffffffll || q_blocks > 0x7fffffffll) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)KVLayout<D>::kAlloc);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QLayout<D>::kAlloc);
-  if (e != cudaSuccess) return e;
-  dkdv_kernel<D><<<(unsigned)kv_blocks, kThreadsKV, KVLayout<D>::kAlloc, st>>>(mK128, mV128, mQ128, mdO128,
-                                                                              mL, mDl, bp);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  dq_kernel<D><<<(unsigned)q_blocks, kThreadsQ, QLayout<D>::kAlloc, st>>>(mK128, mV128, bp);
-  return cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  if (parts & kBwdDkDv) {
+    e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)KVLayout<D>::kAlloc);
+    if (e != cudaSuccess) return e;
+    dkdv_kernel<D><<<(unsigned)kv_blocks, kThreadsKV, KVLayout<D>::kAlloc, st>>>(mK128, mV128, mQ128, mdO128,
+                                                                                mL, mDl, bp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (parts & kBwdDq) {
+    e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QLayout<D>::kAlloc);
+    if (e != cudaSuccess) return e;
+    dq_kernel<D><<<(unsigned)q_blocks, kThreadsQ, QLayout<D>::kAlloc, st>>>(mK128, mV128, bp);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+cudaError_t launch_parts(const ulysses_problem &p, const TmaEncoder &enc, const void *q, const void *k,
+                         const void *v, const void *do_head, const float *nlse, const float *delta,
+                         const void *ws, void *dq, void *dk, void *dv, uint32_t *status, int parts,
+                         cudaStream_t st) {
+  if (p.head_dim == 128)
+    return launch_d<128>(p, enc, q, k, v, do_head, nlse, delta, ws, dq, dk, dv, status, parts, st);
+  if (p.head_dim == 64)
+    return launch_d<64>(p, enc, q, k, v, do_head, nlse, delta, ws, dq, dk, dv, status, parts, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -874,11 +893,22 @@ cudaError_t launch_attn_bwd_tc(const ulysses_problem &p, const TmaEncoder &enc, 
                                const void *k, const void *v, const void *do_head, const float *nlse,
                                const float *delta, const void *ws, void *dq_seq, void *dk_seq,
                                void *dv_seq, uint32_t *status, cudaStream_t st) {
-  if (p.head_dim == 128)
-    return launch_d<128>(p, enc, q, k, v, do_head, nlse, delta, ws, dq_seq, dk_seq, dv_seq, status, st);
-  if (p.head_dim == 64)
-    return launch_d<64>(p, enc, q, k, v, do_head, nlse, delta, ws, dq_seq, dk_seq, dv_seq, status, st);
-  return cudaErrorInvalidValue;
+  return launch_parts(p, enc, q, k, v, do_head, nlse, delta, ws, dq_seq, dk_seq, dv_seq, status,
+                      kBwdDkDv | kBwdDq, st);
+}
+
+cudaError_t launch_attn_bwd_dkdv(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
+                                 const void *k, const void *v, const void *do_head, const float *nlse,
+                                 const float *delta, const void *ws, void *dk_seq, void *dv_seq,
+                                 uint32_t *status, cudaStream_t st) {
+  return launch_parts(p, enc, q, k, v, do_head, nlse, delta, ws, nullptr, dk_seq, dv_seq, status, kBwdDkDv, st);
+}
+
+cudaError_t launch_attn_bwd_dq(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
+                               const void *k, const void *v, const void *do_head, const float *nlse,
+                               const float *delta, const void *ws, void *dq_seq, uint32_t *status,
+                               cudaStream_t st) {
+  return launch_parts(p, enc, q, k, v, do_head, nlse, delta, ws, dq_seq, nullptr, nullptr, status, kBwdDq, st);
 }
 
 }  // namespace ulysses

@@ -62,5 +62,14 @@ cudaError_t launch_attn_bwd_tc(const ulysses_problem &p, const TmaEncoder &enc, 
                                const float *nlse, const float *delta, const void *ws,
                                void *dq_seq, void *dk_seq, void *dv_seq, uint32_t *status,
                                cudaStream_t st);
+// The two kernels of launch_attn_bwd_tc on their own (dK/dV, then dQ).
+cudaError_t launch_attn_bwd_dkdv(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
+                                 const void *k, const void *v, const void *do_head, const float *nlse,
+                                 const float *delta, const void *ws, void *dk_seq, void *dv_seq,
+                                 uint32_t *status, cudaStream_t st);
+cudaError_t launch_attn_bwd_dq(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
+                               const void *k, const void *v, const void *do_head, const float *nlse,
+                               const float *delta, const void *ws, void *dq_seq, uint32_t *status,
+                               cudaStream_t st);
 
 }  // namespace ulysses

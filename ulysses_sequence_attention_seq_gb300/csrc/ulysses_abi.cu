@@ -236,34 +236,86 @@ int ulysses_unpack_out(const ulysses_problem *prob, const void *o_head, void *o_
   return cuda_rc(launch_unpack(p, o_head, o_seq, (cudaStream_t)stream));
 }
 
-int ulysses_attn_bwd(const ulysses_problem *prob, const void *q_head, const void *k_head,
-                     const void *v_head, const void *o_head, const float *lse,
-                     const void *do_seq, void *dq_seq, void *dk_seq, void *dv_seq, void *ws,
-                     size_t ws_bytes, ulysses_stream_t stream) {
+// Shared checks of the backward entry points: a bf16 problem with a tensor-core
+// kernel, a phase-1 workspace.
+static int bwd_common(const ulysses_problem *prob, const void *ws, size_t ws_bytes) {
   int rc = ulysses_validate(prob);
   if (rc) return rc;
   const ulysses_problem &p = *prob;
-  if (p.dtype != ULYSSES_BF16 || (p.head_dim != 64 && p.head_dim != 128))
-    return ULYSSES_ERR_UNSUPPORTED;
-  const size_t nq = act_bytes(p, p.n_head), nk = act_bytes(p, p.n_kv_head);
+  if (p.dtype != ULYSSES_BF16 || (p.head_dim != 64 && p.head_dim != 128)) return ULYSSES_ERR_UNSUPPORTED;
+  return check_ws(p, ws, ws_bytes, 1);
+}
+
+int ulysses_attn_bwd_prepare(const ulysses_problem *prob, const void *o_head, const float *lse,
+                             const void *do_seq, void *ws, size_t ws_bytes, ulysses_stream_t stream) {
+  int rc = bwd_common(prob, ws, ws_bytes);
+  if (rc) return rc;
+  const ulysses_problem &p = *prob;
+  const size_t nq = act_bytes(p, p.n_head);
   const size_t nl = (size_t)p.B * p.n_head * p.S * sizeof(float);
-  const Span in[6] = {{q_head, nq}, {k_head, nk}, {v_head, nk}, {o_head, nq}, {lse, nl}, {do_seq, nq}};
-  const Span out[4] = {{dq_seq, nq}, {dk_seq, nk}, {dv_seq, nk}, {ws, ws_bytes}};
-  if ((rc = check_ws(p, ws, ws_bytes, 1))) return rc;
-  if ((rc = check_spans(in, 6, out, 4))) return rc;
+  const Span in[3] = {{o_head, nq}, {lse, nl}, {do_seq, nq}};
+  const Span out[1] = {{ws, ws_bytes}};
+  if ((rc = check_spans(in, 3, out, 1))) return rc;
+  const WorkspaceLayout L = workspace_layout(p);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  return cuda_rc(launch_pack_do_delta(p, do_seq, o_head, lse, w + L.dohead, reinterpret_cast<float *>(w + L.delta),
+                                      reinterpret_cast<float *>(w + L.nlse), (cudaStream_t)stream));
+}
+
+int ulysses_attn_bwd_dkdv(const ulysses_problem *prob, const void *q_head, const void *k_head,
+                          const void *v_head, void *dk_seq, void *dv_seq, void *ws, size_t ws_bytes,
+                          ulysses_stream_t stream) {
+  int rc = bwd_common(prob, ws, ws_bytes);
+  if (rc) return rc;
+  const ulysses_problem &p = *prob;
+  const size_t nq = act_bytes(p, p.n_head), nk = act_bytes(p, p.n_kv_head);
+  const Span in[3] = {{q_head, nq}, {k_head, nk}, {v_head, nk}};
+  const Span out[3] = {{dk_seq, nk}, {dv_seq, nk}, {ws, ws_bytes}};
+  if ((rc = check_spans(in, 3, out, 3))) return rc;
   TmaEncoder enc;
   if (!get_tma_encoder(&enc)) return ULYSSES_ERR_CUDA;
   const WorkspaceLayout L = workspace_layout(p);
   uint8_t *w = static_cast<uint8_t *>(ws);
-  float *delta = reinterpret_cast<float *>(w + L.delta);
-  float *nlse = reinterpret_cast<float *>(w + L.nlse);
-  void *do_head = w + L.dohead;
-  cudaStream_t st = (cudaStream_t)stream;
-  cudaError_t e = launch_pack_do_delta(p, do_seq, o_head, lse, do_head, delta, nlse, st);
-  if (e == cudaSuccess)
-    e = launch_attn_bwd_tc(p, enc, q_head, k_head, v_head, do_head, nlse, delta, ws, dq_seq, dk_seq,
-                           dv_seq, reinterpret_cast<uint32_t *>(w + L.status), st);
-  return cuda_rc(e);
+  return cuda_rc(launch_attn_bwd_dkdv(p, enc, q_head, k_head, v_head, w + L.dohead,
+                                      reinterpret_cast<const float *>(w + L.nlse),
+                                      reinterpret_cast<const float *>(w + L.delta), ws, dk_seq, dv_seq,
+                                      reinterpret_cast<uint32_t *>(w + L.status), (cudaStream_t)stream));
+}
+
+int ulysses_attn_bwd_dq(const ulysses_problem *prob, const void *q_head, const void *k_head,
+                        const void *v_head, void *dq_seq, void *ws, size_t ws_bytes, ulysses_stream_t stream) {
+  int rc = bwd_common(prob, ws, ws_bytes);
+  if (rc) return rc;
+  const ulysses_problem &p = *prob;
+  const size_t nq = act_bytes(p, p.n_head), nk = act_bytes(p, p.n_kv_head);
+  const Span in[3] = {{q_head, nq}, {k_head, nk}, {v_head, nk}};
+  const Span out[2] = {{dq_seq, nq}, {ws, ws_bytes}};
+  if ((rc = check_spans(in, 3, out, 2))) return rc;
+  TmaEncoder enc;
+  if (!get_tma_encoder(&enc)) return ULYSSES_ERR_CUDA;
+  const WorkspaceLayout L = workspace_layout(p);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  return cuda_rc(launch_attn_bwd_dq(p, enc, q_head, k_head, v_head, w + L.dohead,
+                                    reinterpret_cast<const float *>(w + L.nlse),
+                                    reinterpret_cast<const float *>(w + L.delta), ws, dq_seq,
+                                    reinterpret_cast<uint32_t *>(w + L.status), (cudaStream_t)stream));
+}
+
+int ulysses_attn_bwd(const ulysses_problem *prob, const void *q_head, const void *k_head,
+                     const void *v_head, const void *o_head, const float *lse,
+                     const void *do_seq, void *dq_seq, void *dk_seq, void *dv_seq, void *ws,
+                     size_t ws_bytes, ulysses_stream_t stream) {
+  int rc = bwd_common(prob, ws, ws_bytes);
+  if (rc) return rc;
+  const ulysses_problem &p = *prob;
+  const size_t nq = act_bytes(p, p.n_head), nk = act_bytes(p, p.n_kv_head);
+  const size_t nl = (size_t)p.B * p.n_head * p.S * sizeof(float);
+  const Span in[6] = {{q_head, nq}, {k_head, nk}, {v_head, nk}, {o_head, nq}, {lse, nl}, {do_seq, nq}};
+  const Span out[4] = {{dq_seq, nq}, {dk_seq, nk}, {dv_seq, nk}, {ws, ws_bytes}};
+  if ((rc = check_spans(in, 6, out, 4))) return rc;
+  if ((rc = ulysses_attn_bwd_prepare(prob, o_head, lse, do_seq, ws, ws_bytes, stream))) return rc;
+  if ((rc = ulysses_attn_bwd_dkdv(prob, q_head, k_head, v_head, dk_seq, dv_seq, ws, ws_bytes, stream))) return rc;
+  return ulysses_attn_bwd_dq(prob, q_head, k_head, v_head, dq_seq, ws, ws_bytes, stream);
 }
 
 const char *ulysses_status_string(int code) {
