@@ -49,6 +49,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct BwdParams {
   int B, S, P, Sl, hp, kvp, group, causal;
   int n_head, n_kv;                    // global head counts (row widths of the seq layout)
+  int group_kv, group_q;               // heads per CTA group (grouped_order) of the two kernels
   float scale, scale_log2;
   const float *nlse, *delta;           // [P][B][hp][S]; nlse = -lse * log2(e)
   const float *rope_cos, *rope_sin;    // [S][D/2], or null without RoPE
@@ -221,8 +222,10 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int heads_total = p.P * p.B * p.kvp;
-  const int n = (int)(blockIdx.x / heads_total);  // key tile; low tiles have the most work
-  const int hid = (int)(blockIdx.x % heads_total);
+  const int n_kt_all = (p.S + 127) / 128;
+  const dev::HeadTile ht = dev::grouped_order((int)blockIdx.x, heads_total, n_kt_all, p.group_kv);
+  const int n = ht.rank;  // key tile; low tiles have the most work
+  const int hid = ht.head;
   const int kl = hid % p.kvp, rb = hid / p.kvp;
   const int n_qt = (p.S + 127) / 128;
   const int m0 = p.causal ? n : 0;
@@ -489,7 +492,7 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
 // K tiles stream through a 3-slot ring (released after the dQ MMA), V tiles
 // through a 3-slot ring (released after the dP MMA).
 constexpr int kThreadsQ = 384;  // warpgroups 0-1 softmax, warpgroup 2: TMA, MMA, 2 idle warps
-constexpr uint32_t kRegsQProducer = 56, kRegsQSoftmax = 224;
+constexpr uint32_t kRegsQProducer = 72, kRegsQSoftmax = 216;
 static_assert(128 * kRegsQProducer + 256 * kRegsQSoftmax <= 384 * 168, "register split over budget");
 constexpr int kKSlots = 3, kVSlots = 3;
 
@@ -568,8 +571,9 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int heads_total = p.P * p.B * p.hp;
   const int n_qt = (p.S + 127) / 128;
-  const int m = n_qt - 1 - (int)(blockIdx.x / heads_total);  // longest tiles first
-  const int hid = (int)(blockIdx.x % heads_total);
+  const dev::HeadTile ht = dev::grouped_order((int)blockIdx.x, heads_total, n_qt, p.group_q);
+  const int m = n_qt - 1 - ht.rank;  // longest tiles first
+  const int hid = ht.head;
   const int j = hid % p.hp, rb = hid / p.hp;
   const int kl = j / p.group;
   const int n_kt = (p.S + 127) / 128;
@@ -836,6 +840,10 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   bp.causal = p.causal;
   bp.n_head = p.n_head;
   bp.n_kv = p.n_kv_head;
+  // dK/dV CTAs of a kv-head stream the Q and dO of its q-heads; dQ CTAs of a
+  // q-head stream its kv-head's K and V (shared by the group's q-heads).
+  bp.group_kv = l2_head_group((size_t)4 * p.S * D * bp.group, PB * kvp);
+  bp.group_q = l2_head_group((size_t)4 * p.S * D / bp.group, PB * hp);
   bp.scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)D);
   bp.scale_log2 = bp.scale * kLog2e;
   bp.nlse = nlse;

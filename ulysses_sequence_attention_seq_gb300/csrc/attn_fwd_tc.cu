@@ -101,6 +101,7 @@ struct FwdParams {
   // (the two All-to-Alls become addressing).  Needs Sl % 128 == 0 so a tile
   // never straddles two ranks' shards.
   int folded, Sl, n_head, n_kv_head;
+  int head_group;  // heads per CTA group (grouped_order)
   float scale_log2;
   __nv_bfloat16 *o;  // [P][B][S][hp][D], or [P][B][Sl][H] when folded
   float *lse;        // [P][B][hp][S]
@@ -145,8 +146,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int heads_total = p.P * p.B * p.hp;
-  const int qp = p.n_pairs - 1 - (int)(blockIdx.x / heads_total);  // longest pairs first
-  const int hid = (int)(blockIdx.x % heads_total);
+  const dev::HeadTile ht = dev::grouped_order((int)blockIdx.x, heads_total, p.n_pairs, p.head_group);
+  const int qp = p.n_pairs - 1 - ht.rank;  // longest pairs first
+  const int hid = ht.head;
   const int j = hid % p.hp;
   const int rb = hid / p.hp;  // r*B + b
   const int kl = j / p.group;
@@ -470,6 +472,8 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   fp.n_kv_head = p.n_kv_head;
   const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)D);
   fp.scale_log2 = scale * 1.4426950408889634f;
+  // a q-head's CTAs stream its kv-head's K and V; the group's q-heads share them
+  fp.head_group = l2_head_group((size_t)4 * p.S * D / fp.group, PB * hp);
   fp.o = static_cast<__nv_bfloat16 *>(o);
   fp.lse = lse;
   fp.status = status;

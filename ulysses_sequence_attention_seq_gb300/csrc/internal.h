@@ -72,4 +72,14 @@ cudaError_t launch_attn_bwd_dq(const ulysses_problem &p, const TmaEncoder &enc, 
                                const float *delta, const void *ws, void *dq_seq, uint32_t *status,
                                cudaStream_t st);
 
+// Heads per CTA group (see grouped_order): as many heads as keep the tiles
+// their CTAs stream (per_head_bytes each) within about 48 MiB of L2.
+inline int l2_head_group(size_t per_head_bytes, int n_heads) {
+  const size_t budget = (size_t)48 << 20;
+  size_t g = per_head_bytes ? budget / per_head_bytes : (size_t)n_heads;
+  if (g < 1) g = 1;
+  if (g > (size_t)n_heads) g = (size_t)n_heads;
+  return (int)g;
+}
+
 }  // namespace ulysses

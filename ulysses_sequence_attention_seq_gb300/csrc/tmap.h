@@ -50,6 +50,21 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, ok);
 }
 
+// CTA order over n_heads heads x n_tiles tiles: heads in consecutive groups of
+// `group_heads`, and within a group the tiles by rank (rank 0, the longest,
+// first), the group's heads interleaved.  A group's K/V (or Q/dO) tiles then
+// stay in L2 while its CTAs run, instead of every head's streaming through at
+// once; longest-first keeps the tail short.
+struct HeadTile {
+  int head, rank;
+};
+__device__ __forceinline__ HeadTile grouped_order(int b, int n_heads, int n_tiles, int group_heads) {
+  const int g = b / (group_heads * n_tiles);
+  const int hg = min(group_heads, n_heads - g * group_heads);
+  const int r = b - g * group_heads * n_tiles;
+  return {g * group_heads + r % hg, r / hg};
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, uint32_t bar, int c0,
                                             int c1) {
   asm volatile(
