@@ -842,8 +842,9 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   bp.n_kv = p.n_kv_head;
   // dK/dV CTAs of a kv-head stream the Q and dO of its q-heads; dQ CTAs of a
   // q-head stream its kv-head's K and V (shared by the group's q-heads).
-  bp.group_kv = l2_head_group((size_t)4 * p.S * D * bp.group, PB * kvp);
-  bp.group_q = l2_head_group((size_t)4 * p.S * D / bp.group, PB * hp);
+  const long long n_t = (p.S + 127) / 128;
+  bp.group_kv = l2_head_group((size_t)4 * p.S * D * bp.group, PB * kvp, n_t * PB * kvp);
+  bp.group_q = l2_head_group((size_t)4 * p.S * D / bp.group, PB * hp, n_t * PB * hp);
   bp.scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)D);
   bp.scale_log2 = bp.scale * kLog2e;
   bp.nlse = nlse;

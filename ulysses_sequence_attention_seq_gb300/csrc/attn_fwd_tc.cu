@@ -473,7 +473,7 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)D);
   fp.scale_log2 = scale * 1.4426950408889634f;
   // a q-head's CTAs stream its kv-head's K and V; the group's q-heads share them
-  fp.head_group = l2_head_group((size_t)4 * p.S * D / fp.group, PB * hp);
+  fp.head_group = l2_head_group((size_t)4 * p.S * D / fp.group, PB * hp, (long long)fp.n_pairs * PB * hp);
   fp.o = static_cast<__nv_bfloat16 *>(o);
   fp.lse = lse;
   fp.status = status;
