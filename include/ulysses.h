@@ -221,6 +221,20 @@ int ulysses_attn_bwd_dq(const ulysses_problem *prob, const void *q_head, const v
                         const void *v_head, void *dq_seq, void *ws, size_t ws_bytes, ulysses_stream_t stream);
 
 /*
+ * Self-test of failure detection (no counterpart in the pages): one CTA waits,
+ * with the bounded wait every pipeline wait of the attention kernels uses, on a
+ * barrier that nothing ever completes.  After `limit_ns` (1 ns .. 2 s) the wait
+ * gives up, the CTA sets ULYSSES_STATUS_FWD_TIMEOUT in the status word at the
+ * start of `ws` (any workspace prepared by ulysses_workspace_init, at least 256
+ * bytes) and exits normally; the context stays usable.  Asynchronous on
+ * `stream`; read the bit with ulysses_read_status, clear it with
+ * ulysses_workspace_init.  Errors: ULYSSES_ERR_ARG (NULL or too small `ws`,
+ * limit out of range), ULYSSES_ERR_ALIGN, ULYSSES_ERR_CUDA (launch failed).
+ */
+int ulysses_selftest_wait_timeout(void *ws, size_t ws_bytes, unsigned long long limit_ns,
+                                  ulysses_stream_t stream);
+
+/*
  * The backward for callers that cannot allocate device memory.
  *
  * The paper has no counterpart to this entry point (the pages describe no

@@ -106,3 +106,14 @@ def test_pointer_checks_fail_before_launch(lib):
     # the backward has no fp32 kernel
     pf = prob(dtype=U.FP32, S=1024)
     assert lib.ulysses_attn_bwd(ctypes.byref(pf.c()), *[vp(base + i * nq) for i in range(10)], nws, vp(0)) == -4
+
+
+def test_selftest_wait_timeout_argument_checks(lib):
+    """The timeout self-test refuses bad arguments on the host, before any launch."""
+    vp = ctypes.c_void_p
+    fn = lib.ulysses_selftest_wait_timeout
+    assert fn(vp(0), 4096, 1000000, vp(0)) == -1            # NULL workspace
+    assert fn(vp(0x10000), 128, 1000000, vp(0)) == -1       # smaller than the status block
+    assert fn(vp(0x10000), 4096, 0, vp(0)) == -1            # no limit
+    assert fn(vp(0x10000), 4096, 3000000000, vp(0)) == -1   # above 2 s
+    assert fn(vp(0x10008), 4096, 1000000, vp(0)) == -5      # misaligned

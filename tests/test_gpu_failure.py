@@ -1,0 +1,35 @@
+"""Failure detection on the GPU without a fault: a bounded pipeline wait is made
+to run out (a barrier nothing completes), the status word reports it, kernels
+launched on that workspace afterwards refuse to start, and once the workspace is
+prepared again the path computes the same result as before."""
+import pytest
+import torch
+
+from pathcheck import GpuRun
+from test_gpu_forward import wl
+from ulysses_sequence_attention_seq_gb300 import binding as U
+
+pytestmark = pytest.mark.gpu
+
+
+def test_bounded_wait_times_out_and_is_reported():
+    w = wl(2, 1, 256, 4, 4, 64)
+    run = GpuRun(w)
+    run.forward()
+    good = run.buf.o_seq.clone()
+
+    U.ulysses_selftest_wait_timeout(run.buf.ws, 20_000_000)   # 20 ms
+    torch.cuda.synchronize()
+    assert U.ulysses_read_status(run.buf.ws) & U.STATUS_FWD_TIMEOUT
+
+    # with a timeout bit set the attention kernel does not start: O is left alone
+    run.buf.o_head.fill_(0)
+    run.buf.forward()
+    torch.cuda.synchronize()
+    assert U.ulysses_read_status(run.buf.ws) & U.STATUS_FWD_TIMEOUT
+    assert not run.buf.o_head.any()
+
+    # the context is still usable: prepare the workspace again and the path runs
+    U.ulysses_workspace_init(run.prob, run.buf.ws)
+    run.forward()
+    assert torch.equal(run.buf.o_seq, good)

@@ -110,6 +110,7 @@ def lib():
         L.ulysses_attn_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_attn_bwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.ulysses_attn_bwd_prepare.argtypes = [P, vp, vp, vp, vp, sz, vp]
+        L.ulysses_selftest_wait_timeout.argtypes = [vp, sz, ctypes.c_ulonglong, vp]
         L.ulysses_attn_bwd_dkdv.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_attn_bwd_dq.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_status_string.argtypes = [ctypes.c_int]
@@ -206,6 +207,13 @@ def ulysses_attn_bwd_dq(prob, q_head, k_head, v_head, dq_seq, ws, stream=None):
     _check("ulysses_attn_bwd_dq", lib().ulysses_attn_bwd_dq(
         ctypes.byref(prob.c()), _ptr(q_head), _ptr(k_head), _ptr(v_head), _ptr(dq_seq), _ptr(ws),
         ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def ulysses_selftest_wait_timeout(ws, limit_ns, stream=None):
+    """A bounded wait that is made to run out: sets the forward-timeout bit of
+    the workspace status word after limit_ns, without any fault."""
+    _check("ulysses_selftest_wait_timeout", lib().ulysses_selftest_wait_timeout(
+        _ptr(ws), ws.numel() * ws.element_size(), int(limit_ns), _stream(stream)))
 
 
 def ulysses_attn_bwd_noalloc(prob, q_head, k_head, v_head, o_head, lse, do_seq, dq_seq, dk_seq,
