@@ -71,6 +71,9 @@ def load_library(path: str):
     ll = ctypes.POINTER(ctypes.c_longlong)
     L.oracle_a2a_seq_to_head.argtypes = [ctypes.c_int] * 6 + [pp, pp, ll, ll, ctypes.c_int, ctypes.c_int]
     L.oracle_a2a_head_to_seq.argtypes = [ctypes.c_int] * 6 + [pp, pp, ll, ll, ctypes.c_int, ctypes.c_int]
+    if hasattr(L, "oracle_a2a_seq_to_head_rep"):
+        L.oracle_a2a_seq_to_head_rep.argtypes = [ctypes.c_int] * 6 + [pp, pp, ll, ll]
+        L.oracle_reduce_head_to_seq_rep.argtypes = [ctypes.c_int] * 6 + [pp, pp, ll, ll]
     L.oracle_rope_seq.argtypes = [ctypes.c_int] * 5 + [ctypes.c_double, ctypes.c_int, pp]
     L.oracle_rope_seq.restype = None
     ip = ctypes.POINTER(ctypes.c_int)
@@ -102,6 +105,16 @@ class Problem:
     @property
     def Sl(self) -> int:
         return self.S // self.P
+
+    @property
+    def kv_replicas(self) -> int:
+        """R = P / n_kv_head ranks hold each kv-head when n_kv_head < P, else 1."""
+        return self.P // self.n_kv_head if self.n_kv_head < self.P else 1
+
+    @property
+    def kvp(self) -> int:
+        """kv-heads a rank holds in head layout."""
+        return self.n_kv_head // self.P if self.n_kv_head >= self.P else 1
 
     @property
     def softmax_scale(self) -> float:
@@ -151,6 +164,40 @@ def a2a_seq_to_head(x_ranks: Sequence[np.ndarray], heads: int, elem_bytes: int =
     if rc != 0:
         raise ValueError("heads must be a multiple of P")
     return y, list(sent), list(recv)
+
+
+def a2a_seq_to_head_replicated(x_ranks: Sequence[np.ndarray], heads: int, elem_bytes: int = 2):
+    """The kv All-to-All when heads < P (KV-head replication): rank d gets
+    kv-head d / (P/heads) over the full sequence, [B,S,1,D] per rank.
+    Returns (y_ranks, sent_bytes[P], recv_bytes[P])."""
+    P = len(x_ranks)
+    B, Sl, h, D = x_ranks[0].shape
+    assert h == heads
+    y = [np.zeros((B, Sl * P, 1, D), dtype=np.float64) for _ in range(P)]
+    sent = (ctypes.c_longlong * P)()
+    recv = (ctypes.c_longlong * P)()
+    rc = lib().oracle_a2a_seq_to_head_rep(P, B, Sl, heads, D, elem_bytes, _ptrs(x_ranks), _ptrs(y), sent, recv)
+    if rc != 0:
+        raise ValueError("heads must divide P")
+    return y, list(sent), list(recv)
+
+
+def reduce_head_to_seq_replicated(y_ranks: Sequence[np.ndarray], heads: int, elem_bytes: int = 2):
+    """Gradients of replicated kv-heads back to sequence layout: each kv-head's
+    gradient is the sum of its replicas' ([B,S,1,D] per rank ->
+    [B,Sl,heads,D])."""
+    P = len(y_ranks)
+    B, S, one, D = y_ranks[0].shape
+    assert one == 1 and S % P == 0
+    Sl = S // P
+    y_ranks = [np.ascontiguousarray(a, dtype=np.float64) for a in y_ranks]
+    x = [np.zeros((B, Sl, heads, D), dtype=np.float64) for _ in range(P)]
+    sent = (ctypes.c_longlong * P)()
+    recv = (ctypes.c_longlong * P)()
+    rc = lib().oracle_reduce_head_to_seq_rep(P, B, Sl, heads, D, elem_bytes, _ptrs(y_ranks), _ptrs(x), sent, recv)
+    if rc != 0:
+        raise ValueError("heads must divide P")
+    return x, list(sent), list(recv)
 
 
 def a2a_head_to_seq(y_ranks: Sequence[np.ndarray], heads: int, elem_bytes: int = 2,
@@ -223,7 +270,7 @@ def attention_bwd(prob: Problem, q_head, k_head, v_head, do_head, groups=None,
     kv-head) groups (default: all).  Returns (dq, dk, dv) head-layout ranks;
     entries not computed stay NaN."""
     P, B, S, D = prob.P, prob.B, prob.S, prob.D
-    hp, kvp = prob.n_head // P, prob.n_kv_head // P
+    hp, kvp = prob.n_head // P, prob.kvp
     dq = [np.full((B, S, hp, D), np.nan) for _ in range(P)]
     dk = [np.full((B, S, kvp, D), np.nan) for _ in range(P)]
     dv = [np.full((B, S, kvp, D), np.nan) for _ in range(P)]
@@ -262,8 +309,11 @@ def forward(prob: Problem, Q, K, V, rows=None, elem_bytes=2, nthreads=None):
         q_seq = rope_seq(q_seq, prob.rope_base, +1)
         k_seq = rope_seq(k_seq, prob.rope_base, +1)
     q_head, sq, _ = a2a_seq_to_head(q_seq, prob.n_head, elem_bytes)
-    k_head, sk, _ = a2a_seq_to_head(k_seq, prob.n_kv_head, elem_bytes)
-    v_head, sv, _ = a2a_seq_to_head(v_seq, prob.n_kv_head, elem_bytes)
+    # with fewer kv-heads than ranks each kv-head goes to the R ranks whose
+    # q-heads read it (KV-head replication)
+    kv_a2a = a2a_seq_to_head_replicated if prob.kv_replicas > 1 else a2a_seq_to_head
+    k_head, sk, _ = kv_a2a(k_seq, prob.n_kv_head, elem_bytes)
+    v_head, sv, _ = kv_a2a(v_seq, prob.n_kv_head, elem_bytes)
     o_head, lse = attention_fwd(prob, q_head, k_head, v_head, rows=rows, nthreads=nthreads)
     if rows is None:
         o_seq, so, _ = a2a_head_to_seq(o_head, prob.n_head, elem_bytes)
@@ -291,8 +341,13 @@ def backward(prob: Problem, Q, K, V, dO, groups=None, q_rows=None, kv_rows=None,
                                      groups=groups, q_rows=q_rows, kv_rows=kv_rows,
                                      nthreads=nthreads)
     dq_seq, sdq, _ = a2a_head_to_seq(dq_h, prob.n_head, elem_bytes, fill=np.nan)
-    dk_seq, sdk, _ = a2a_head_to_seq(dk_h, prob.n_kv_head, elem_bytes, fill=np.nan)
-    dv_seq, sdv, _ = a2a_head_to_seq(dv_h, prob.n_kv_head, elem_bytes, fill=np.nan)
+    if prob.kv_replicas > 1:
+        # each replica holds a partial dK, dV (its own q-heads' share): summed
+        dk_seq, sdk, _ = reduce_head_to_seq_replicated(dk_h, prob.n_kv_head, elem_bytes)
+        dv_seq, sdv, _ = reduce_head_to_seq_replicated(dv_h, prob.n_kv_head, elem_bytes)
+    else:
+        dk_seq, sdk, _ = a2a_head_to_seq(dk_h, prob.n_kv_head, elem_bytes, fill=np.nan)
+        dv_seq, sdv, _ = a2a_head_to_seq(dv_h, prob.n_kv_head, elem_bytes, fill=np.nan)
     if prob.use_rope:
         dq_seq = rope_seq(dq_seq, prob.rope_base, -1)
         dk_seq = rope_seq(dk_seq, prob.rope_base, -1)

@@ -241,6 +241,24 @@ typedef struct {
 /* Query-head g (global) -> kv-head (global), contiguous groups. */
 static int kv_head_of(const oracle_shape *sh, int g) { return g / (sh->n_head / sh->n_kv_head); }
 
+/* KV-head replication (n_kv_head < P, P a multiple of n_kv_head): the q-heads
+   of rank r all read kv-head r / R (R = P / n_kv_head), so the seq -> head
+   All-to-All hands that kv-head to each of its R ranks and every rank holds
+   one kv-head in head layout.  Otherwise a rank holds n_kv_head / P kv-heads
+   starting at r * n_kv_head / P. */
+static int kv_per_rank(const oracle_shape *sh) {
+  return sh->n_kv_head >= sh->P ? sh->n_kv_head / sh->P : 1;
+}
+static int rank_kv_base(const oracle_shape *sh, int r) {
+  return sh->n_kv_head >= sh->P ? r * (sh->n_kv_head / sh->P) : r / (sh->P / sh->n_kv_head);
+}
+/* The head counts the method defines: P divides n_head, n_kv_head divides
+   n_head, and P and n_kv_head divide one another. */
+static int heads_ok(const oracle_shape *sh) {
+  if (sh->P <= 0 || sh->n_kv_head <= 0 || sh->n_head % sh->P || sh->n_head % sh->n_kv_head) return 0;
+  return sh->n_kv_head % sh->P == 0 || sh->P % sh->n_kv_head == 0;
+}
+
 typedef struct {
   const oracle_shape *sh;
   const double *const *q, *const *k, *const *v;
@@ -255,7 +273,7 @@ typedef struct {
 static void fwd_item(void *vctx, long item, double *w) {
   fwd_ctx *c = (fwd_ctx *)vctx;
   const oracle_shape *sh = c->sh;
-  const int hp = sh->n_head / sh->P, kvp = sh->n_kv_head / sh->P, D = sh->D;
+  const int hp = sh->n_head / sh->P, kvp = kv_per_rank(sh), D = sh->D;
   const long S = sh->S;
   long n_chunks = (c->n_rows + c->chunk - 1) / c->chunk;
   long ch = item % n_chunks;
@@ -265,7 +283,7 @@ static void fwd_item(void *vctx, long item, double *w) {
   int b = (int)(rest % sh->B);
   int r = (int)(rest / sh->B);
   int g = r * hp + j;
-  int kl = kv_head_of(sh, g) - r * kvp; /* local kv index on rank r */
+  int kl = kv_head_of(sh, g) - rank_kv_base(sh, r); /* local kv index on rank r */
   const double *K = c->k[r] + ((long)b * S * kvp + kl) * D;
   const double *V = c->v[r] + ((long)b * S * kvp + kl) * D;
   for (long ii = ch * c->chunk; ii < c->n_rows && ii < (ch + 1) * c->chunk; ++ii) {
@@ -289,9 +307,7 @@ int oracle_attention_fwd(const oracle_shape *sh, const double *const *q_head,
                          const double *const *k_head, const double *const *v_head,
                          double *const *o_head, double *const *lse, const int *rows, long n_rows,
                          int nthreads) {
-  if (sh->P <= 0 || sh->n_head % sh->P || sh->n_kv_head % sh->P || sh->n_kv_head <= 0 ||
-      sh->n_head % sh->n_kv_head)
-    return -1;
+  if (!heads_ok(sh)) return -1;
   fwd_ctx c = {sh, q_head, k_head, v_head, o_head, lse, rows, rows ? n_rows : sh->S, 64};
   long n_chunks = (c.n_rows + c.chunk - 1) / c.chunk;
   long items = (long)sh->P * sh->B * (sh->n_head / sh->P) * n_chunks;
@@ -372,7 +388,7 @@ static const double *row_ptr(const double *base, long S, int width, int b, long 
 static void bwd_item(void *vctx, long item, double *w) {
   bwd_ctx *c = (bwd_ctx *)vctx;
   const oracle_shape *sh = c->sh;
-  const int hp = sh->n_head / sh->P, kvp = sh->n_kv_head / sh->P, D = sh->D;
+  const int hp = sh->n_head / sh->P, kvp = kv_per_rank(sh), D = sh->D;
   const long S = sh->S;
   const int r = c->r, b = c->b, kl = c->kl;
   const double *K = row_ptr(c->k[r], S, kvp, b, 0, kl, D);
@@ -445,9 +461,7 @@ int oracle_attention_bwd_group(const oracle_shape *sh, int r, int b, int kl,
                                double *const *dq_head, double *const *dk_head,
                                double *const *dv_head, const int *q_rows, long n_q_rows,
                                const int *kv_rows, long n_kv_rows, int nthreads) {
-  if (sh->P <= 0 || sh->n_head % sh->P || sh->n_kv_head % sh->P || sh->n_kv_head <= 0 ||
-      sh->n_head % sh->n_kv_head)
-    return -1;
+  if (!heads_ok(sh)) return -1;
   const long S = sh->S;
   bwd_ctx c;
   memset(&c, 0, sizeof c);
@@ -455,7 +469,10 @@ int oracle_attention_bwd_group(const oracle_shape *sh, int r, int b, int kl,
   c.r = r;
   c.b = b;
   c.kl = kl;
-  c.G = sh->n_head / sh->n_kv_head;
+  /* q-heads of rank r that read local kv-head kl: the whole group, or with
+     replicated kv-heads the rank's own hp (its share of the group; the other
+     replicas hold the rest and their dk, dv are summed afterwards). */
+  c.G = (sh->n_head / sh->P) / kv_per_rank(sh);
   c.q = q_head;
   c.k = k_head;
   c.v = v_head;
@@ -486,5 +503,78 @@ int oracle_attention_bwd_group(const oracle_shape *sh, int r, int b, int kl,
   }
   free(c.lse);
   free(c.delta);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* KV-head replication, seq -> head: the All-to-All for K and V when        */
+/* n_kv_head = heads < P.  Destination rank dst needs the kv-head its        */
+/* q-heads read, kv = dst / R (R = P / heads), over the full sequence; every */
+/* source rank sends it its Sl tokens of that head:                          */
+/*   y_dst[b][src*Sl + t][0][e] = x_src[b][t][dst/R][e]                       */
+/* Bytes of pieces with src != dst are counted as in oracle_a2a_seq_to_head. */
+/* Returns 0, or -1 unless heads divides P.                                  */
+/* ------------------------------------------------------------------------ */
+int oracle_a2a_seq_to_head_rep(int P, int B, int Sl, int heads, int D, int elem_bytes,
+                               const double *const *x_seq, double *const *y_head,
+                               long long *sent, long long *recv) {
+  if (P <= 0 || heads <= 0 || P % heads != 0) return -1;
+  const int R = P / heads;
+  const long S = (long)Sl * P;
+  for (int dst = 0; dst < P; ++dst) {
+    const int kv = dst / R;
+    for (int src = 0; src < P; ++src) {
+      const double *x = x_seq[src];
+      double *y = y_head[dst];
+      for (int b = 0; b < B; ++b)
+        for (int t = 0; t < Sl; ++t) {
+          const double *from = x + (((long)b * Sl + t) * heads + kv) * D;
+          double *to = y + ((long)b * S + ((long)src * Sl + t)) * D;
+          for (int e = 0; e < D; ++e) to[e] = from[e];
+        }
+      if (src != dst) {
+        const long long piece = (long long)B * Sl * D * elem_bytes;
+        if (sent) sent[src] += piece;
+        if (recv) recv[dst] += piece;
+      }
+    }
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* KV-head replication, head -> seq for the gradients of K and V.  The       */
+/* forward copied kv-head kv to the R ranks kv*R .. kv*R+R-1, so its         */
+/* gradient is the sum of what those ranks computed (the chain rule of a     */
+/* copy), added in rank order:                                               */
+/*   x_dst[b][t][kv][e] = sum_{j<R} y_{kv*R+j}[b][dst*Sl + t][0][e]           */
+/* Every replica sends its Sl rows for dst to dst; bytes of pieces with      */
+/* src != dst are counted.  Returns 0, or -1 unless heads divides P.         */
+/* ------------------------------------------------------------------------ */
+int oracle_reduce_head_to_seq_rep(int P, int B, int Sl, int heads, int D, int elem_bytes,
+                                  const double *const *y_head, double *const *x_seq,
+                                  long long *sent, long long *recv) {
+  if (P <= 0 || heads <= 0 || P % heads != 0) return -1;
+  const int R = P / heads;
+  const long S = (long)Sl * P;
+  for (int dst = 0; dst < P; ++dst) {
+    double *x = x_seq[dst];
+    for (int b = 0; b < B; ++b)
+      for (int t = 0; t < Sl; ++t)
+        for (int kv = 0; kv < heads; ++kv) {
+          double *to = x + (((long)b * Sl + t) * heads + kv) * D;
+          for (int e = 0; e < D; ++e) to[e] = 0.0;
+          for (int j = 0; j < R; ++j) {
+            const double *from = y_head[kv * R + j] + ((long)b * S + ((long)dst * Sl + t)) * D;
+            for (int e = 0; e < D; ++e) to[e] += from[e];
+          }
+        }
+    for (int src = 0; src < P; ++src)
+      if (src != dst) {
+        const long long piece = (long long)B * Sl * D * elem_bytes;
+        if (sent) sent[src] += piece;
+        if (recv) recv[dst] += piece;
+      }
+  }
   return 0;
 }

@@ -39,6 +39,9 @@ MUTANTS = [
     ("dk/dv causal range off by one", "for (long i = sh->causal ? kk : 0; i < S; ++i)",
      "for (long i = sh->causal ? kk + 1 : 0; i < S; ++i)"),
     ("dq transposed operand", "dqi[e] += sh->scale * ds * kr[e];", "dqi[e] += sh->scale * ds * vr[e];"),
+    ("replicated kv-heads dealt round-robin", "const int kv = dst / R;", "const int kv = dst % heads;"),
+    ("gradient reduce drops a replica", "for (int j = 0; j < R; ++j) {", "for (int j = 1; j < R; ++j) {"),
+    ("replica rank holds the wrong kv-head", "r / (sh->P / sh->n_kv_head);", "r % sh->n_kv_head;"),
 ]
 
 
@@ -57,6 +60,9 @@ def battery():
         ("torch", lambda: pins.test_single_rank_matches_torch_sdpa_and_autograd(True)),
         ("closed-forms", lambda: pins.test_closed_forms()),
         ("unsharded", lambda: pins.test_ulysses_equals_unsharded_attention_bit_exact(4, 2, 64, 8, 4, 8, True, True)),
+        ("unsharded-replicated", lambda: pins.test_ulysses_equals_unsharded_attention_bit_exact(8, 2, 64, 8, 1, 4, True, True)),
+        ("brute-replicated", lambda: pins.test_oracle_matches_brute_force(4, 1, 8, 4, 2, 4, True, True)),
+        ("replicated-adjoint", lambda: pins.test_replicated_reduce_is_the_adjoint_of_the_replicating_all_to_all(4, 1, 3, 2, 4)),
     ]
     failed = []
     for name, fn in cases:

@@ -190,7 +190,9 @@ def _global_lse(prob, lse_ranks):
 @pytest.mark.parametrize("P,B,S,h,kv,D,causal,rope", [
     (2, 1, 8, 2, 2, 4, True, True), (4, 1, 16, 4, 4, 4, True, True),
     (2, 2, 6, 4, 2, 6, False, True), (4, 1, 8, 8, 4, 2, True, False),
-    (1, 1, 5, 2, 1, 4, True, True), (2, 1, 4, 2, 2, 2, False, False)])
+    (1, 1, 5, 2, 1, 4, True, True), (2, 1, 4, 2, 2, 2, False, False),
+    # KV-head replication (n_kv_head < P): every kv-head held by P/n_kv ranks
+    (4, 1, 8, 4, 2, 4, True, True), (4, 2, 8, 4, 1, 2, False, True), (8, 1, 16, 8, 2, 2, True, False)])
 def test_oracle_matches_brute_force(P, B, S, h, kv, D, causal, rope):
     Q, K, V = rnd((B, S, h, D), 1), rnd((B, S, kv, D), 2), rnd((B, S, kv, D), 3)
     dO = rnd((B, S, h * D), 4)
@@ -234,7 +236,8 @@ def test_brute_force_gradients_match_finite_differences():
 
 @pytest.mark.parametrize("P,B,S,h,kv,D,causal,rope", [
     (4, 2, 64, 8, 4, 8, True, True), (2, 1, 96, 4, 2, 16, False, True),
-    (8, 1, 64, 8, 8, 4, True, False)])
+    (8, 1, 64, 8, 8, 4, True, False),
+    (4, 1, 64, 4, 2, 8, True, True), (8, 2, 64, 8, 1, 4, True, True), (8, 1, 96, 16, 4, 8, False, True)])
 def test_ulysses_equals_unsharded_attention_bit_exact(P, B, S, h, kv, D, causal, rope):
     """[SP2] §1/§3: the transposes are a permutation of ownership, so the
     sharded pipeline must reproduce unsharded attention exactly in fp64."""
@@ -335,3 +338,38 @@ def test_row_sampling_matches_full():
     bp = oracle.backward(prob, Q, K, V, dO, groups=[(1, 0, 0)], q_rows=rows, kv_rows=rows)
     for name in ("dq_head", "dk_head", "dv_head"):
         assert np.array_equal(bp[name][1][:, rows], bf[name][1][:, rows])
+
+
+@pytest.mark.parametrize("P,B,Sl,kv,D", [(4, 1, 3, 2, 4), (8, 2, 2, 1, 3), (8, 1, 4, 4, 2)])
+def test_replicated_reduce_is_the_adjoint_of_the_replicating_all_to_all(P, B, Sl, kv, D):
+    """The kv All-to-All with replication copies each kv-head to P/kv ranks; the
+    gradient step must be its exact transpose: <A(x), y> = <x, A^T(y)> for all
+    x, y (a dropped replica, a wrong replica index or a wrong source row breaks
+    the identity).  Also: identical replicas reduce to R times the value."""
+    rng = np.random.default_rng(41)
+    x = [rng.standard_normal((B, Sl, kv, D)) for _ in range(P)]
+    y = [rng.standard_normal((B, Sl * P, 1, D)) for _ in range(P)]
+    ax, _, _ = oracle.a2a_seq_to_head_replicated(x, kv, 8)
+    aty, _, _ = oracle.reduce_head_to_seq_replicated(y, kv, 8)
+    lhs = sum(float((a * b).sum()) for a, b in zip(ax, y))
+    rhs = sum(float((a * b).sum()) for a, b in zip(x, aty))
+    assert abs(lhs - rhs) <= 1e-12 * (abs(lhs) + 1.0)
+    R = P // kv
+    same, _, _ = oracle.reduce_head_to_seq_replicated(ax, kv, 8)
+    for r in range(P):  # R-fold repeated addition rounds at 3x, 5x, ...: not bit-equal to R*x
+        np.testing.assert_allclose(same[r], R * x[r], rtol=1e-15, atol=0)
+
+
+@pytest.mark.parametrize("P,B,Sl,kv,D,eb", [(4, 1, 3, 2, 4, 2), (8, 2, 5, 1, 8, 2), (8, 1, 2, 4, 6, 4)])
+def test_replicated_bytes_moved(P, B, Sl, kv, D, eb):
+    """With replication every rank needs one kv-head over the full sequence,
+    of which it holds 1/P itself: it receives (P-1)/P * B*S*D*eb bytes per
+    tensor, and (every rank holding exactly one kv-head) sends as much; the
+    gradient reduce moves the same amount the other way."""
+    x = [np.zeros((B, Sl, kv, D)) for _ in range(P)]
+    _, sent, recv = oracle.a2a_seq_to_head_replicated(x, kv, eb)
+    want = (P - 1) * B * Sl * D * eb
+    assert sent == [want] * P and recv == [want] * P
+    y = [np.zeros((B, Sl * P, 1, D)) for _ in range(P)]
+    _, sent, recv = oracle.reduce_head_to_seq_replicated(y, kv, eb)
+    assert sent == [want] * P and recv == [want] * P
