@@ -32,7 +32,7 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from ulysses_sequence_attention_seq_gb300.synthetic import WORKLOADS, make_inputs  # noqa: E402
+from ulysses_sequence_attention_seq_gb300.synthetic import EXTRA_WORKLOADS, WORKLOADS, make_inputs  # noqa: E402
 
 METRIC = "tokens/s + attn TFLOP/s (S=32K, 32 heads, P=8 virtual); seq↔head permute GB/s"
 
@@ -66,8 +66,11 @@ def attn_fwd_flops(w):
 
 
 def permute_bytes(w, es):
-    """Bytes read + written by the seq->head pack of Q, K, V (2 x tensor bytes)."""
-    return 2.0 * w.B * w.S * (w.n_head + 2 * w.n_kv_head) * w.head_dim * es
+    """Bytes read + written by the seq->head pack of Q, K, V: each tensor read
+    once and written once, K and V written once per replica when there are
+    fewer kv-heads than ranks (each kv-head then goes to P / n_kv_head ranks)."""
+    kv_written = w.n_kv_head if w.n_kv_head >= w.P else w.P
+    return float(w.B * w.S * w.head_dim * es) * (2 * w.n_head + 2 * w.n_kv_head + 2 * kv_written)
 
 
 class ClockSampler:
@@ -152,7 +155,9 @@ def run_ulysses(args, w, rank, world):
     torch.cuda.synchronize()
 
     names = ["pack_qkv", "attn_fwd", "unpack_out"] + (["bwd_prepare", "bwd_dkdv", "bwd_dq"] if backward else [])
-    launches_per_step = 3 + (3 if backward else 0)
+    # pack, forward, unpack; prepare, dK/dV (+ the replica sum when kv-heads are
+    # replicated), dQ
+    launches_per_step = 3 + ((4 if w.n_kv_head < w.P else 3) if backward else 0)
 
     def step(evs=None, split=True):
         """One pass of the whole path.  With `split` the backward runs as its
@@ -401,7 +406,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="C4", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="C4", choices=sorted(WORKLOADS) + sorted(EXTRA_WORKLOADS))
     ap.add_argument("--impl", default="ulysses", choices=["ulysses", "reference"])
     ap.add_argument("--fwd-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -415,7 +420,7 @@ def main():
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
-    w = WORKLOADS[args.workload]
+    w = WORKLOADS[args.workload] if args.workload in WORKLOADS else EXTRA_WORKLOADS[args.workload]
     hbm, tf_burst, tf_sust, peak_src = load_peaks()
     tokens = w.B * w.S
 

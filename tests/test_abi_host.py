@@ -47,7 +47,9 @@ def prob(**kw):
     (dict(rope_base=0.0, use_rope=False), 0), (dict(softmax_scale=-1.0), -1),
     (dict(S=4100), -2),                        # S % P
     (dict(n_head=36, hidden=36 * 128), -2),    # n_head % P
-    (dict(n_kv_head=4), -2),                   # n_kv_head % P: P > n_kv_head
+    (dict(n_kv_head=4), 0),                    # n_kv_head < P, P a multiple: kv-heads replicated (R = 2)
+    (dict(n_kv_head=1), 0),                    # one kv-head on every rank (R = 8)
+    (dict(n_head=48, hidden=48 * 128, n_kv_head=12), -2),  # neither of n_kv_head, P divides the other
     (dict(P=64, S=4096 * 64), -2),             # P > n_head: the head-count bound
     (dict(n_kv_head=24), -2),                  # n_head % n_kv_head
     (dict(hidden=1024), -3),
@@ -65,6 +67,9 @@ def test_workspace_sizes(lib):
     # backward adds delta [B][n_head][S] fp32 and dO in head layout
     assert b >= f + p.B * p.n_head * p.S * 4 + p.B * p.S * p.n_head * p.head_dim * 2
     assert U.ulysses_workspace_bytes(prob(use_rope=False), 0) == 256
+    # replicated kv-heads: the backward also holds every rank's float partial dK and dV
+    pr = prob(n_kv_head=2)
+    assert U.ulysses_workspace_bytes(pr, 1) >= b + 2 * pr.P * pr.B * pr.S * pr.head_dim * 4
     assert U.ulysses_workspace_bytes(prob(B=0), 0) == 0
 
 

@@ -102,3 +102,59 @@ def test_backward_steps_equal_composed_call(order):
     assert U.ulysses_read_status(b.ws) == 0
     for got, want in zip((b.dq_seq, b.dk_seq, b.dv_seq), ref):
         assert torch.equal(got, want)
+
+
+# KV-head replication: each replica computes dK, dV for its own q-heads; the
+# kv-head's gradient is their sum (deterministic, in rank order).
+REP_BWD_CASES = [wl(4, 1, 512, 8, 2, 128),                  # R = 2
+                 wl(8, 1, 1024, 8, 1, 64),                  # R = 8 (MQA)
+                 wl(8, 2, 392, 16, 4, 128, causal=False)]   # R = 2, B = 2, ragged tail
+
+
+@pytest.mark.parametrize("w", REP_BWD_CASES, ids=_ids)
+def test_replicated_kv_backward_matches_oracle(w):
+    w = w.with_(backward=True)
+    run = GpuRun(w, backward=True)
+    run.forward()
+    run.backward()
+    x = oracle_inputs(run.inputs)
+    want = oracle.backward(oracle_problem(w), x["q"], x["k"], x["v"], x["do"])
+    for name in ("dq_seq", "dk_seq", "dv_seq"):
+        assert_close(to64(getattr(run.buf, name)), np.stack(want[name]), w, name)
+
+
+def test_replicated_kv_backward_is_deterministic():
+    w = wl(8, 1, 512, 8, 2, 128).with_(backward=True)
+    run = GpuRun(w, backward=True)
+    run.forward()
+    outs = []
+    for _ in range(2):
+        run.backward()
+        outs.append([getattr(run.buf, n).clone() for n in ("dq_seq", "dk_seq", "dv_seq")])
+    for a, b in zip(outs[1], outs[0]):
+        assert torch.equal(a, b)
+
+
+def test_replicated_kv_backward_full_size_sampled():
+    """The replicated workload at full size (the bench's launch configuration),
+    sampled: kv-head 0 and the last kv-head with every replica rank of each
+    (their partials are what the sum needs), gradient rows at shard/tile
+    boundaries and seeded random rows, each exact over its full range."""
+    from ulysses_sequence_attention_seq_gb300.synthetic import EXTRA_WORKLOADS
+    w = EXTRA_WORKLOADS["C4-kv4"]
+    run = GpuRun(w, backward=True)
+    run.forward()
+    run.backward()
+    x = oracle_inputs(run.inputs)
+    rows = sample_rows(w, 12, seed=2)
+    R = w.P // w.n_kv_head
+    kvs = [0, w.n_kv_head - 1]
+    groups = [(kv * R + j, 0, 0) for kv in kvs for j in range(R)]
+    want = oracle.backward(oracle_problem(w), x["q"], x["k"], x["v"], x["do"], groups=groups,
+                           q_rows=rows, kv_rows=rows)
+    hp = w.n_head // w.P
+    for name, heads in (("dk_seq", kvs), ("dv_seq", kvs),
+                        ("dq_seq", [r * hp + j for (r, _, _) in groups for j in range(hp)])):
+        got = np.concatenate(list(to64(getattr(run.buf, name))), axis=1)   # [B][S][heads][D] global
+        ref = np.concatenate(list(want[name]), axis=1)
+        assert_close(got[0][rows][:, heads], ref[0][rows][:, heads], w, name)

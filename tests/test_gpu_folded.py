@@ -71,3 +71,18 @@ def test_folded_refuses_what_it_cannot_fold():
     with pytest.raises(U.UlyssesError) as e:
         U.ulysses_attn_fwd_folded(run.prob, b.q_seq, b.k_seq, b.v_seq, b.o_seq, b.lse, b.ws)
     assert e.value.code == -4
+
+
+def test_folded_with_replicated_kv_heads_equals_three_calls():
+    """KV-head replication in the folded forward: rank r's K/V tiles come from
+    kv-head r / R of the sequence-sharded buffers."""
+    w = wl(8, 1, 2048, 16, 2, 128, rope=False)
+    run = GpuRun(w)
+    run.forward()
+    o3, l3 = run.buf.o_seq.clone(), run.buf.lse.clone()
+    run.buf.o_seq.zero_()
+    b = run.buf
+    U.ulysses_attn_fwd_folded(run.prob, b.q_seq, b.k_seq, b.v_seq, b.o_seq, b.lse, b.ws)
+    torch.cuda.synchronize()
+    assert U.ulysses_read_status(b.ws) == 0
+    assert torch.equal(b.o_seq, o3) and torch.equal(b.lse, l3)

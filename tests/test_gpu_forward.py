@@ -209,3 +209,57 @@ def test_forward_moving_reference(slope, causal, D):
     want_o = np.stack([a.reshape(w.B, w.Sl, -1) for a in want["o_seq"]])
     assert_close(got_o, want_o, w, "o_seq")
     assert np.abs(to64(run.buf.lse) - np.stack(want["lse"])).max() <= LSE_BF16_MAX_ABS
+
+
+# KV-head replication: fewer kv-heads than ranks, each kv-head handed to the
+# P / n_kv_head ranks whose q-heads read it.
+REP_CASES = [wl(4, 1, 512, 8, 2, 128),                     # R = 2, GQA 4
+             wl(8, 2, 1024, 8, 1, 64),                     # R = 8 (one kv-head: MQA), B = 2
+             wl(8, 1, 648, 16, 4, 128, causal=False),      # R = 2, ragged tail
+             wl(4, 1, 256, 4, 2, 32, "fp32", causal=False, rope=False)]
+
+
+@pytest.mark.parametrize("w", REP_CASES, ids=lambda w: f"P{w.P}B{w.B}S{w.S}h{w.n_head}kv{w.n_kv_head}D{w.head_dim}{w.dtype}")
+def test_replicated_kv_pack_is_bit_exact(w):
+    """Without RoPE the kv part of the pack is the oracle's replicating
+    All-to-All bit for bit (and q's the plain one)."""
+    w = w.with_(use_rope=False)
+    run = GpuRun(w)
+    _pack(run)
+    x = oracle_inputs(run.inputs)
+    want_q, _, _ = oracle.a2a_seq_to_head(oracle.shard_sequence(x["q"], w.P), w.n_head)
+    g = to64(run.buf.q_head)
+    for r in range(w.P):
+        assert np.array_equal(g[r], want_q[r])
+    for name, got in (("k", run.buf.k_head), ("v", run.buf.v_head)):
+        want, _, _ = oracle.a2a_seq_to_head_replicated(oracle.shard_sequence(x[name], w.P), w.n_kv_head)
+        g = to64(got)
+        for r in range(w.P):
+            assert np.array_equal(g[r], want[r]), f"{name} rank {r}"
+
+
+@pytest.mark.parametrize("w", REP_CASES, ids=lambda w: f"P{w.P}B{w.B}S{w.S}h{w.n_head}kv{w.n_kv_head}D{w.head_dim}{w.dtype}{'c' if w.causal else 'n'}")
+def test_replicated_kv_forward_matches_oracle(w):
+    run = GpuRun(w)
+    run.forward()
+    x = oracle_inputs(run.inputs)
+    want = oracle.forward(oracle_problem(w), x["q"], x["k"], x["v"])
+    got_o = to64(run.buf.o_seq)
+    want_o = np.stack([a.reshape(w.B, w.Sl, -1) for a in want["o_seq"]])
+    assert_close(got_o, want_o, w, "o_seq")
+    tol = FP32_MAX_ABS if w.dtype == "fp32" else LSE_BF16_MAX_ABS
+    assert np.abs(to64(run.buf.lse) - np.stack(want["lse"])).max() <= tol
+
+
+def test_replicated_kv_forward_full_size_sampled():
+    """The replicated workload at full size (the bench's launch configuration),
+    on sampled query rows of every head."""
+    from ulysses_sequence_attention_seq_gb300.synthetic import EXTRA_WORKLOADS
+    w = EXTRA_WORKLOADS["C4-kv4"]
+    run = GpuRun(w, backward=False)
+    run.forward()
+    x = oracle_inputs(run.inputs)
+    rows = sample_rows(w, 24)
+    want = oracle.forward(oracle_problem(w), x["q"], x["k"], x["v"], rows=rows)
+    assert_close(to64(run.buf.o_head)[:, :, rows], np.stack(want["o_head"])[:, :, rows], w, "o_head")
+    assert np.abs(to64(run.buf.lse)[..., rows] - np.stack(want["lse"])[..., rows]).max() <= LSE_BF16_MAX_ABS

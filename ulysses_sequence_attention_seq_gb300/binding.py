@@ -84,7 +84,9 @@ class Problem:
 
     @property
     def kvp(self):
-        return self.n_kv_head // self.P
+        """kv-heads a rank holds in head layout: n_kv_head / P, or one when
+        n_kv_head < P (each kv-head then replicated to P / n_kv_head ranks)."""
+        return self.n_kv_head // self.P if self.n_kv_head >= self.P else 1
 
     def scale(self) -> float:
         return self.softmax_scale if self.softmax_scale > 0 else 1.0 / math.sqrt(self.head_dim)

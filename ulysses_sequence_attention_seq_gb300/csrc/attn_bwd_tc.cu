@@ -55,6 +55,8 @@ struct BwdParams {
   const float *rope_cos, *rope_sin;    // [S][D/2], or null without RoPE
   const __nv_bfloat16 *q, *dout;       // head layout [P][B][S][hp][D] (the dQ kernel's TMEM operands)
   __nv_bfloat16 *dq, *dk, *dv;         // sequence-sharded outputs
+  int kv_rep;                          // > 1: replicated kv-heads; dk/dv then point to float
+                                       // per-rank partials [P*B][S][D] (unscaled, not rotated)
   uint32_t *status;                    // status word; the RoPE table key follows it
   uint32_t rope_key;
 };
@@ -433,7 +435,32 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
     }
     // ------------------------------------------------------------ epilogue
     if (ok) ok = warp_wait(bar + kKBarAcc, 0, abort_flag, gst);
-    if (ok) {
+    if (ok && p.kv_rep > 1) {
+      // Replicated kv-head: this rank's q-heads give only part of dK, dV; the
+      // raw fp32 accumulators go to the per-rank partial buffers and the sum
+      // over the replicas (with scale and inverse rotation) follows.
+      tc_fence_after_sync();
+      const bool live = kvr < p.S;
+      float *pv = reinterpret_cast<float *>(p.dv) + ((size_t)rb * p.S + (live ? kvr : 0)) * D;
+      float *pk = reinterpret_cast<float *>(p.dk) + ((size_t)rb * p.S + (live ? kvr : 0)) * D;
+      // warpgroup g owns columns [g*D/2, (g+1)*D/2) of both accumulators; the
+      // TMEM loads are warp-wide, only the stores depend on the row
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = g * (D / 2) + c * 32;
+        uint32_t x[32], y[32];
+        tmem_ld32(tdV + lane_base + col, x);
+        tmem_ld32(tdK + lane_base + col, y);
+        tmem_wait_ld();
+        if (live) {
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            reinterpret_cast<uint4 *>(pv + col)[v] = make_uint4(x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]);
+            reinterpret_cast<uint4 *>(pk + col)[v] = make_uint4(y[4 * v], y[4 * v + 1], y[4 * v + 2], y[4 * v + 3]);
+          }
+        }
+      }
+    } else if (ok) {
       tc_fence_after_sync();
       const bool live = kvr < p.S;
       const int s_rank = kvr / p.Sl, t = kvr - s_rank * p.Sl;
@@ -820,7 +847,7 @@ template <int D>
 cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void *q, const void *k,
                      const void *v, const void *do_head, const float *nlse, const float *delta,
                      const void *ws, void *dq, void *dk, void *dv, uint32_t *status, int parts, cudaStream_t st) {
-  const int hp = p.n_head / p.P, kvp = p.n_kv_head / p.P, PB = p.P * p.B;
+  const int hp = p.n_head / p.P, kvp = kv_per_rank(p), PB = p.P * p.B;
   CUtensorMap mK128, mV128, mL, mDl, mQ128, mdO128;
   bool ok = make_act_map(enc, &mK128, k, D, kvp, p.S, PB, 128) &&
             make_act_map(enc, &mV128, v, D, kvp, p.S, PB, 128) &&
@@ -858,6 +885,7 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   } else {
     bp.rope_cos = bp.rope_sin = nullptr;
   }
+  bp.kv_rep = kv_replicas(p);
   bp.dq = static_cast<__nv_bfloat16 *>(dq);
   bp.dk = static_cast<__nv_bfloat16 *>(dk);
   bp.dv = static_cast<__nv_bfloat16 *>(dv);

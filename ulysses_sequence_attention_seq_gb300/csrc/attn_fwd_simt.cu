@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(kRows) attn_fwd_simt_kernel(
 
 cudaError_t launch_attn_fwd_simt(const ulysses_problem &p, const float *q, const float *k,
                                  const float *v, float *o, float *lse, cudaStream_t st) {
-  const int hp = p.n_head / p.P, kvp = p.n_kv_head / p.P, group = p.n_head / p.n_kv_head;
+  const int hp = p.n_head / p.P, kvp = kv_per_rank(p), group = hp / kvp;
   const int n_qt = (p.S + kRows - 1) / kRows;
   const long long blocks = (long long)n_qt * p.P * p.B * hp;
   const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)p.head_dim);

@@ -102,6 +102,7 @@ struct FwdParams {
   // never straddles two ranks' shards.
   int folded, Sl, n_head, n_kv_head;
   int head_group;  // heads per CTA group (grouped_order)
+  int kv_rep;      // > 1: replicated kv-heads, rank r reads kv-head r / kv_rep
   float scale_log2;
   __nv_bfloat16 *o;  // [P][B][S][hp][D], or [P][B][Sl][H] when folded
   float *lse;        // [P][B][hp][S]
@@ -113,11 +114,12 @@ struct FwdParams {
 struct TileCoord {
   int head, row, outer;
 };
+// `rep` > 1: a replicated kv-head (rank r reads global kv-head r / rep).
 __device__ __forceinline__ TileCoord tile_coord(const FwdParams &p, int rb, int lh, int heads_local,
-                                                int pos) {
+                                                int pos, int rep = 1) {
   if (!p.folded) return {lh, pos, rb};
   const int r = rb / p.B, b = rb - r * p.B, src = pos / p.Sl;
-  return {r * heads_local + lh, pos - src * p.Sl, src * p.B + b};
+  return {rep > 1 ? r / rep : r * heads_local + lh, pos - src * p.Sl, src * p.B + b};
 }
 
 // Position in the K/V ring of the n-th tile streamed (K_j is n = 2j, V_j is 2j+1).
@@ -203,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           mbar_arrive_expect_tx(bar + kBarKVFull + 8 * slot, L::kTile);
           const CUtensorMap *m = (n & 1) ? &tmV : &tmK;
-          const TileCoord tk = tile_coord(p, rb, kl, p.kvp, (n >> 1) * BN);
+          const TileCoord tk = tile_coord(p, rb, kl, p.kvp, (n >> 1) * BN, p.kv_rep);
           for (int c = 0; c < kChunks; ++c)
             tma_load_4d(sKV + slot * L::kTile + c * kChunkBytes, m, bar + kBarKVFull + 8 * slot,
                         c * 64, tk.head, tk.row, tk.outer);
@@ -449,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void *q, const void *k,
                      const void *v, void *o, float *lse, uint32_t *status, bool folded, cudaStream_t st) {
-  const int hp = p.n_head / p.P, kvp = p.n_kv_head / p.P, PB = p.P * p.B, Sl = p.S / p.P;
+  const int hp = p.n_head / p.P, kvp = kv_per_rank(p), PB = p.P * p.B, Sl = p.S / p.P;
   CUtensorMap mq, mk, mv;
   // head-sharded maps: [P*B][S][hp|kvp][D]; folded maps: [P*B][Sl][n_head|n_kv_head][D]
   const int rows = folded ? Sl : p.S;
@@ -470,6 +472,7 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   fp.Sl = Sl;
   fp.n_head = p.n_head;
   fp.n_kv_head = p.n_kv_head;
+  fp.kv_rep = kv_replicas(p);
   const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)D);
   fp.scale_log2 = scale * 1.4426950408889634f;
   // a q-head's CTAs stream its kv-head's K and V; the group's q-heads share them

@@ -18,6 +18,9 @@ struct WorkspaceLayout {
   size_t delta = 0, delta_bytes = 0;  // float [P][B][hp][S]          (backward)
   size_t nlse = 0, nlse_bytes = 0;    // float [P][B][hp][S], -lse*log2(e) (backward)
   size_t dohead = 0, dohead_bytes = 0;  // dO in head layout [P][B][S][hp][D] (backward)
+  // With replicated kv-heads (n_kv_head < P): each rank's partial dK and dV,
+  // float [P][B][S][D] each, summed over the replicas afterwards (backward).
+  size_t dkpart = 0, dvpart = 0, part_bytes = 0;
   size_t total_fwd = 0, total_bwd = 0;
 };
 WorkspaceLayout workspace_layout(const ulysses_problem &p);
@@ -27,6 +30,13 @@ WorkspaceLayout workspace_layout(const ulysses_problem &p);
 uint32_t rope_key(const ulysses_problem &p);
 
 inline size_t elem_size(const ulysses_problem &p) { return p.dtype == ULYSSES_BF16 ? 2 : 4; }
+
+// KV-head replication: with fewer kv-heads than ranks (P a multiple of
+// n_kv_head) the q-heads of rank r all read kv-head r / R, R = P / n_kv_head,
+// so the seq -> head All-to-All hands each kv-head to R ranks and every rank
+// holds one kv-head in head layout.
+inline int kv_replicas(const ulysses_problem &p) { return p.n_kv_head < p.P ? p.P / p.n_kv_head : 1; }
+inline int kv_per_rank(const ulysses_problem &p) { return p.n_kv_head >= p.P ? p.n_kv_head / p.P : 1; }
 
 // ---- permutation kernels (permute.cu) ----
 cudaError_t launch_rope_table(const ulysses_problem &p, void *ws, cudaStream_t st);
@@ -39,6 +49,11 @@ cudaError_t launch_unpack(const ulysses_problem &p, const void *o_head, void *o_
 cudaError_t launch_pack_do_delta(const ulysses_problem &p, const void *do_seq, const void *o_head,
                                  const float *lse, void *do_head, float *delta, float *nlse,
                                  cudaStream_t st);
+// Replicated kv-heads: dk_seq/dv_seq (bf16, sequence layout) = the sum over
+// each kv-head's replicas of their float partials, in rank order; dK also
+// scaled by `scale` and rotated back by the RoPE angle of its position.
+cudaError_t launch_kv_reduce(const ulysses_problem &p, const float *dk_part, const float *dv_part,
+                             void *dk_seq, void *dv_seq, float scale, const void *ws, cudaStream_t st);
 
 // ---- attention kernels ----
 struct TmaEncoder {

@@ -34,6 +34,7 @@ struct PermJob {
   void *dst;        // write side
   int heads;        // heads of this tensor
   int rope;         // 0: copy; +1: rotate by +angle; -1: rotate by -angle
+  int rep;          // > 1: heads < P and every head goes to `rep` ranks (rank d gets head d / rep)
 };
 
 struct PermParams {
@@ -125,12 +126,14 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const PermParams p) {
     for (int q = 0; q < 3; ++q) {
       if (q >= p.njobs) break;
       const PermJob J = p.job[q];
-      const int hp = J.heads / p.P;
+      const int hp = J.rep > 1 ? 1 : J.heads / p.P;
       // A unit is chunk c of both halves of a head (2 x 16 bytes), rotated or
-      // not: two loads in flight per thread either way.
+      // not: two loads in flight per thread either way.  With replicated heads
+      // the units run over the P destination ranks (one head each), so a head
+      // of the token row is read once per replica.
       const int cph = p.D / (2 * V);
       const int run = hp * cph;                           // units per destination piece
-      const int units = J.heads * cph;
+      const int units = p.P * run;
       const long long seq_row = row * (long long)J.heads * p.D;
       for (int u = threadIdx.x; u < units; u += kThreads) {
         const int d = u / run;  // the rank on the head side of this piece
@@ -138,7 +141,8 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const PermParams p) {
         const int j = w / cph, c = w - j * cph;
         const long long head_off =
             (((long long)(d * p.B + b) * S + pos) * hp + j) * p.D + (long long)c * V;
-        const long long seq_off = seq_row + (long long)(d * hp + j) * p.D + (long long)c * V;
+        const int seq_head = J.rep > 1 ? d / J.rep : d * hp + j;
+        const long long seq_off = seq_row + (long long)seq_head * p.D + (long long)c * V;
         const long long src_off = p.to_head ? seq_off : head_off;
         const long long dst_off = p.to_head ? head_off : seq_off;
         const T *src = static_cast<const T *>(J.src);
@@ -391,9 +395,10 @@ cudaError_t launch_pack_qkv(const ulysses_problem &p, const void *q, const void 
                             void *qh, void *kh, void *vh, void *ws, cudaStream_t st) {
   PermParams pp = base_params(p, ws, 1);
   const int r = p.use_rope ? 1 : 0;
-  pp.job[0] = {q, qh, p.n_head, r};
-  pp.job[1] = {k, kh, p.n_kv_head, r};
-  pp.job[2] = {v, vh, p.n_kv_head, 0};
+  const int R = kv_replicas(p);
+  pp.job[0] = {q, qh, p.n_head, r, 1};
+  pp.job[1] = {k, kh, p.n_kv_head, r, R};
+  pp.job[2] = {v, vh, p.n_kv_head, 0, R};
   pp.njobs = 3;
   return launch_perm(p, pp, st);
 }
@@ -401,7 +406,7 @@ cudaError_t launch_pack_qkv(const ulysses_problem &p, const void *q, const void 
 cudaError_t launch_unpack(const ulysses_problem &p, const void *o_head, void *o_seq,
                           cudaStream_t st) {
   PermParams pp = base_params(p, nullptr, 0);
-  pp.job[0] = {o_head, o_seq, p.n_head, 0};
+  pp.job[0] = {o_head, o_seq, p.n_head, 0, 1};
   pp.njobs = 1;
   return launch_perm(p, pp, st);
 }
@@ -417,6 +422,88 @@ cudaError_t launch_pack_do_delta(const ulysses_problem &p, const void *do_seq, c
       static_cast<const __nv_bfloat16 *>(do_seq), static_cast<const __nv_bfloat16 *>(o_head),
       lse, static_cast<__nv_bfloat16 *>(do_head), delta, nlse, p.P, p.B, p.S / p.P, p.n_head,
       p.head_dim);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Gradients of replicated kv-heads ("Sequence Parallelism II", §6: the
+// gradients go back head -> seq): kv-head kv was handed to the R ranks
+// kv*R .. kv*R+R-1, so its gradient is the sum of their partials, added in
+// rank order:
+//   dV_seq[d][b][t][kv][e] = sum_j dv_part[(kv*R+j)*B + b][d*Sl+t][e]
+// and dK the same, then scaled and rotated back by -angle(d*Sl+t) on the pairs
+// (i, i+D/2).  One thread per (row, kv-head, 4 rotation pairs): float4 loads of
+// both halves from each replica, two 8-byte bf16 stores per tensor.
+namespace {
+
+__global__ void __launch_bounds__(256) kv_reduce_kernel(const float *__restrict__ dkp, const float *__restrict__ dvp,
+                                                        __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv,
+                                                        int P, int B, int Sl, int n_kv, int D, float scale,
+                                                        const float *__restrict__ cs, const float *__restrict__ sn) {
+  const int R = P / n_kv, half = D / 2, q4 = half / 4;
+  const int S = P * Sl;
+  const long long n = (long long)P * B * Sl * n_kv * q4;
+  for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < n; u += (long long)gridDim.x * blockDim.x) {
+    const int c = (int)(u % q4);
+    long long rest = u / q4;
+    const int kv = (int)(rest % n_kv);
+    rest /= n_kv;
+    const int t = (int)(rest % Sl);
+    rest /= Sl;
+    const int b = (int)(rest % B);
+    const int d = (int)(rest / B);
+    const int pos = d * Sl + t;
+    float4 kx = make_float4(0.f, 0.f, 0.f, 0.f), ky = kx, vx = kx, vy = kx;
+    for (int j = 0; j < R; ++j) {
+      const size_t off = (((size_t)(kv * R + j) * B + b) * S + pos) * D + (size_t)c * 4;
+      const float4 a = *reinterpret_cast<const float4 *>(dkp + off);
+      const float4 a2 = *reinterpret_cast<const float4 *>(dkp + off + half);
+      const float4 v1 = *reinterpret_cast<const float4 *>(dvp + off);
+      const float4 v2 = *reinterpret_cast<const float4 *>(dvp + off + half);
+      kx.x += a.x; kx.y += a.y; kx.z += a.z; kx.w += a.w;
+      ky.x += a2.x; ky.y += a2.y; ky.z += a2.z; ky.w += a2.w;
+      vx.x += v1.x; vx.y += v1.y; vx.z += v1.z; vx.w += v1.w;
+      vy.x += v2.x; vy.y += v2.y; vy.z += v2.z; vy.w += v2.w;
+    }
+    float xs[4] = {kx.x * scale, kx.y * scale, kx.z * scale, kx.w * scale};
+    float ys[4] = {ky.x * scale, ky.y * scale, ky.z * scale, ky.w * scale};
+    if (cs) {
+      const float4 c4 = *reinterpret_cast<const float4 *>(cs + (size_t)pos * half + c * 4);
+      const float4 s4 = *reinterpret_cast<const float4 *>(sn + (size_t)pos * half + c * 4);
+      const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, ss[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {  // x' = x cos + y sin, y' = y cos - x sin
+        const float x = xs[q], y = ys[q];
+        xs[q] = x * cc[q] + y * ss[q];
+        ys[q] = y * cc[q] - x * ss[q];
+      }
+    }
+    const size_t o = (((size_t)(d * B + b) * Sl + t) * n_kv + kv) * D + (size_t)c * 4;
+    const __nv_bfloat162 k0 = __floats2bfloat162_rn(xs[0], xs[1]), k1 = __floats2bfloat162_rn(xs[2], xs[3]);
+    const __nv_bfloat162 k2 = __floats2bfloat162_rn(ys[0], ys[1]), k3 = __floats2bfloat162_rn(ys[2], ys[3]);
+    const __nv_bfloat162 w0 = __floats2bfloat162_rn(vx.x, vx.y), w1 = __floats2bfloat162_rn(vx.z, vx.w);
+    const __nv_bfloat162 w2 = __floats2bfloat162_rn(vy.x, vy.y), w3 = __floats2bfloat162_rn(vy.z, vy.w);
+    *reinterpret_cast<uint2 *>(dk + o) = make_uint2(*reinterpret_cast<const uint32_t *>(&k0), *reinterpret_cast<const uint32_t *>(&k1));
+    *reinterpret_cast<uint2 *>(dk + o + half) = make_uint2(*reinterpret_cast<const uint32_t *>(&k2), *reinterpret_cast<const uint32_t *>(&k3));
+    *reinterpret_cast<uint2 *>(dv + o) = make_uint2(*reinterpret_cast<const uint32_t *>(&w0), *reinterpret_cast<const uint32_t *>(&w1));
+    *reinterpret_cast<uint2 *>(dv + o + half) = make_uint2(*reinterpret_cast<const uint32_t *>(&w2), *reinterpret_cast<const uint32_t *>(&w3));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_kv_reduce(const ulysses_problem &p, const float *dk_part, const float *dv_part,
+                             void *dk_seq, void *dv_seq, float scale, const void *ws, cudaStream_t st) {
+  const float *cs = nullptr, *sn = nullptr;
+  if (p.use_rope) {
+    const WorkspaceLayout L = workspace_layout(p);
+    cs = reinterpret_cast<const float *>(static_cast<const uint8_t *>(ws) + L.rope);
+    sn = cs + (size_t)p.S * (p.head_dim / 2);
+  }
+  const long long n = (long long)p.B * p.S * p.n_kv_head * (p.head_dim / 8);
+  kv_reduce_kernel<<<grid_for(n / 256 + 1), 256, 0, st>>>(dk_part, dv_part, static_cast<__nv_bfloat16 *>(dk_seq),
+                                                          static_cast<__nv_bfloat16 *>(dv_seq), p.P, p.B,
+                                                          p.S / p.P, p.n_kv_head, p.head_dim, scale, cs, sn);
   return cudaGetLastError();
 }
 

@@ -30,7 +30,10 @@ WorkspaceLayout workspace_layout(const ulysses_problem &p) {
   L.nlse_bytes = L.delta_bytes;
   L.dohead = align256(L.nlse + L.nlse_bytes);
   L.dohead_bytes = (size_t)p.B * p.S * p.n_head * p.head_dim * es;
-  L.total_bwd = align256(L.dohead + L.dohead_bytes);
+  L.part_bytes = kv_replicas(p) > 1 ? (size_t)p.P * p.B * p.S * p.head_dim * 4 : 0;
+  L.dkpart = align256(L.dohead + L.dohead_bytes);
+  L.dvpart = align256(L.dkpart + L.part_bytes);
+  L.total_bwd = align256(L.dvpart + L.part_bytes);
   return L;
 }
 
@@ -115,6 +118,12 @@ size_t act_bytes(const ulysses_problem &p, int heads) {
   return (size_t)p.B * p.S * heads * p.head_dim * elem_size(p);
 }
 
+// K or V in head layout [P][B][S][kv-heads per rank][D]: with replicated
+// kv-heads P copies of one kv-head's rows, else the same size as the tensor.
+size_t kv_head_bytes(const ulysses_problem &p) {
+  return (size_t)p.P * p.B * p.S * kv_per_rank(p) * p.head_dim * elem_size(p);
+}
+
 }  // namespace
 
 extern "C" {
@@ -129,7 +138,8 @@ int ulysses_validate(const ulysses_problem *prob) {
     return ULYSSES_ERR_ARG;
   if (!(p.softmax_scale >= 0.f) || isinf(p.softmax_scale)) return ULYSSES_ERR_ARG;
   if (p.use_rope && (!(p.rope_base > 0.f) || isinf(p.rope_base))) return ULYSSES_ERR_ARG;
-  if (p.S % p.P || p.n_head % p.P || p.n_kv_head % p.P || p.n_head % p.n_kv_head)
+  if (p.S % p.P || p.n_head % p.P || p.n_head % p.n_kv_head ||
+      (p.n_kv_head % p.P != 0 && p.P % p.n_kv_head != 0))
     return ULYSSES_ERR_DIVISIBILITY;
   if ((long long)p.n_head * p.head_dim != p.hidden) return ULYSSES_ERR_HIDDEN;
   if (p.dtype != ULYSSES_BF16 && p.dtype != ULYSSES_FP32) return ULYSSES_ERR_UNSUPPORTED;
@@ -169,9 +179,9 @@ int ulysses_pack_qkv(const ulysses_problem *prob, const void *q_seq, const void 
   int rc = ulysses_validate(prob);
   if (rc) return rc;
   const ulysses_problem &p = *prob;
-  const size_t nq = act_bytes(p, p.n_head), nk = act_bytes(p, p.n_kv_head);
+  const size_t nq = act_bytes(p, p.n_head), nk = act_bytes(p, p.n_kv_head), nkh = kv_head_bytes(p);
   const Span in[4] = {{q_seq, nq}, {k_seq, nk}, {v_seq, nk}, {ws, ws_bytes}};
-  const Span out[3] = {{q_head, nq}, {k_head, nk}, {v_head, nk}};
+  const Span out[3] = {{q_head, nq}, {k_head, nkh}, {v_head, nkh}};
   if ((rc = check_ws(p, ws, ws_bytes, 0))) return rc;
   if ((rc = check_spans(in, 4, out, 3))) return rc;
   return cuda_rc(launch_pack_qkv(p, q_seq, k_seq, v_seq, q_head, k_head, v_head, ws,
@@ -185,9 +195,9 @@ int ulysses_attn_fwd(const ulysses_problem *prob, const void *q_head, const void
   if (rc) return rc;
   const ulysses_problem &p = *prob;
   if (p.dtype == ULYSSES_BF16 && p.head_dim != 64 && p.head_dim != 128) return ULYSSES_ERR_UNSUPPORTED;
-  const size_t nq = act_bytes(p, p.n_head), nk = act_bytes(p, p.n_kv_head);
+  const size_t nq = act_bytes(p, p.n_head), nkh = kv_head_bytes(p);
   const size_t nl = (size_t)p.B * p.n_head * p.S * sizeof(float);
-  const Span in[3] = {{q_head, nq}, {k_head, nk}, {v_head, nk}};
+  const Span in[3] = {{q_head, nq}, {k_head, nkh}, {v_head, nkh}};
   const Span out[3] = {{o_head, nq}, {lse, nl}, {ws, ws_bytes}};
   if ((rc = check_ws(p, ws, ws_bytes, 0))) return rc;
   if ((rc = check_spans(in, 3, out, 3))) return rc;
@@ -268,18 +278,33 @@ int ulysses_attn_bwd_dkdv(const ulysses_problem *prob, const void *q_head, const
   int rc = bwd_common(prob, ws, ws_bytes);
   if (rc) return rc;
   const ulysses_problem &p = *prob;
-  const size_t nq = act_bytes(p, p.n_head), nk = act_bytes(p, p.n_kv_head);
-  const Span in[3] = {{q_head, nq}, {k_head, nk}, {v_head, nk}};
+  const size_t nq = act_bytes(p, p.n_head), nk = act_bytes(p, p.n_kv_head), nkh = kv_head_bytes(p);
+  const Span in[3] = {{q_head, nq}, {k_head, nkh}, {v_head, nkh}};
   const Span out[3] = {{dk_seq, nk}, {dv_seq, nk}, {ws, ws_bytes}};
   if ((rc = check_spans(in, 3, out, 3))) return rc;
   TmaEncoder enc;
   if (!get_tma_encoder(&enc)) return ULYSSES_ERR_CUDA;
   const WorkspaceLayout L = workspace_layout(p);
   uint8_t *w = static_cast<uint8_t *>(ws);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (kv_replicas(p) > 1) {
+    // each rank's partial dK, dV (its own q-heads) into the workspace, then the
+    // sum over every kv-head's replicas into sequence layout
+    float *dkp = reinterpret_cast<float *>(w + L.dkpart), *dvp = reinterpret_cast<float *>(w + L.dvpart);
+    cudaError_t e = launch_attn_bwd_dkdv(p, enc, q_head, k_head, v_head, w + L.dohead,
+                                         reinterpret_cast<const float *>(w + L.nlse),
+                                         reinterpret_cast<const float *>(w + L.delta), ws, dkp, dvp,
+                                         reinterpret_cast<uint32_t *>(w + L.status), st);
+    if (e == cudaSuccess) {
+      const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)p.head_dim);
+      e = launch_kv_reduce(p, dkp, dvp, dk_seq, dv_seq, scale, ws, st);
+    }
+    return cuda_rc(e);
+  }
   return cuda_rc(launch_attn_bwd_dkdv(p, enc, q_head, k_head, v_head, w + L.dohead,
                                       reinterpret_cast<const float *>(w + L.nlse),
                                       reinterpret_cast<const float *>(w + L.delta), ws, dk_seq, dv_seq,
-                                      reinterpret_cast<uint32_t *>(w + L.status), (cudaStream_t)stream));
+                                      reinterpret_cast<uint32_t *>(w + L.status), st));
 }
 
 int ulysses_attn_bwd_dq(const ulysses_problem *prob, const void *q_head, const void *k_head,
@@ -287,8 +312,8 @@ int ulysses_attn_bwd_dq(const ulysses_problem *prob, const void *q_head, const v
   int rc = bwd_common(prob, ws, ws_bytes);
   if (rc) return rc;
   const ulysses_problem &p = *prob;
-  const size_t nq = act_bytes(p, p.n_head), nk = act_bytes(p, p.n_kv_head);
-  const Span in[3] = {{q_head, nq}, {k_head, nk}, {v_head, nk}};
+  const size_t nq = act_bytes(p, p.n_head), nkh = kv_head_bytes(p);
+  const Span in[3] = {{q_head, nq}, {k_head, nkh}, {v_head, nkh}};
   const Span out[2] = {{dq_seq, nq}, {ws, ws_bytes}};
   if ((rc = check_spans(in, 3, out, 2))) return rc;
   TmaEncoder enc;
@@ -308,9 +333,9 @@ int ulysses_attn_bwd(const ulysses_problem *prob, const void *q_head, const void
   int rc = bwd_common(prob, ws, ws_bytes);
   if (rc) return rc;
   const ulysses_problem &p = *prob;
-  const size_t nq = act_bytes(p, p.n_head), nk = act_bytes(p, p.n_kv_head);
+  const size_t nq = act_bytes(p, p.n_head), nk = act_bytes(p, p.n_kv_head), nkh = kv_head_bytes(p);
   const size_t nl = (size_t)p.B * p.n_head * p.S * sizeof(float);
-  const Span in[6] = {{q_head, nq}, {k_head, nk}, {v_head, nk}, {o_head, nq}, {lse, nl}, {do_seq, nq}};
+  const Span in[6] = {{q_head, nq}, {k_head, nkh}, {v_head, nkh}, {o_head, nq}, {lse, nl}, {do_seq, nq}};
   const Span out[4] = {{dq_seq, nq}, {dk_seq, nk}, {dv_seq, nk}, {ws, ws_bytes}};
   if ((rc = check_spans(in, 6, out, 4))) return rc;
   if ((rc = ulysses_attn_bwd_prepare(prob, o_head, lse, do_seq, ws, ws_bytes, stream))) return rc;
@@ -323,7 +348,8 @@ const char *ulysses_status_string(int code) {
     case ULYSSES_OK: return "ok";
     case ULYSSES_ERR_ARG: return "invalid argument (NULL pointer or non-positive size)";
     case ULYSSES_ERR_DIVISIBILITY:
-      return "divisibility: S, n_head and n_kv_head must be multiples of P and n_head a multiple of n_kv_head";
+      return "divisibility: S and n_head must be multiples of P, n_head a multiple of n_kv_head, and one of "
+             "n_kv_head, P a multiple of the other";
     case ULYSSES_ERR_HIDDEN: return "hidden must equal n_head * head_dim";
     case ULYSSES_ERR_UNSUPPORTED: return "unsupported head_dim / dtype / pass combination";
     case ULYSSES_ERR_ALIGN: return "a pointer is not 16-byte aligned";

@@ -64,6 +64,13 @@ WORKLOADS: Dict[str, Workload] = {
                    backward=False, seed=1005),
 }
 
+# Beyond the five: the pages' sizing with fewer kv-heads than ranks (4 kv-heads
+# over P=8, so each kv-head is replicated to 2 ranks), for the KV-head
+# replication path.
+EXTRA_WORKLOADS: Dict[str, Workload] = {
+    "C4-kv4": WORKLOADS["C4"].with_(name="C4-kv4", n_kv_head=4, seed=1006),
+}
+
 # The permute-only sweep at the head-count bound (P=32, one head per rank).
 SWEEP_S = (4096, 8192, 16384, 32768, 65536, 131072)
 
