@@ -356,6 +356,49 @@ def backward(prob: Problem, Q, K, V, dO, groups=None, q_rows=None, kv_rows=None,
                 v_head=fw["v_head"], sent=dict(do=sdo, dq=sdq, dk=sdk, dv=sdv))
 
 
+def qkv_projection(prob: Problem, x_ranks: Sequence[np.ndarray], W: np.ndarray, bias=None):
+    """[SP2] §2 second step ("run the QKV projections for the local sequence
+    chunk"; the rank has the full projection weights) and [CMP] "A simple
+    attention skeleton" (q/k/v projections of x, then view as heads): every
+    rank applies the complete, replicated projection to its own tokens.
+    x_r: [B, Sl, H] per rank; W: [(n_head + 2 n_kv_head) * D, H] -- the three
+    projection weights stacked (q rows, then k, then v) in the Linear layout
+    [out_features, in_features]; bias: [(n_head + 2 n_kv_head) * D] or None.
+    Returns per-rank q [B,Sl,n_head,D], k and v [B,Sl,n_kv_head,D]:
+    y = x W^T (+ b), the matrix product taken from numpy."""
+    D, h, kv = prob.D, prob.n_head, prob.n_kv_head
+    W = np.asarray(W, dtype=np.float64)
+    assert W.shape[0] == (h + 2 * kv) * D
+    q, k, v = [], [], []
+    for x in x_ranks:
+        x = np.asarray(x, dtype=np.float64)
+        B, Sl, H = x.shape
+        assert W.shape[1] == H
+        y = x.reshape(B * Sl, H) @ W.T
+        if bias is not None:
+            y = y + np.asarray(bias, dtype=np.float64)[None, :]
+        y = y.reshape(B, Sl, h + 2 * kv, D)
+        q.append(np.ascontiguousarray(y[:, :, :h]))
+        k.append(np.ascontiguousarray(y[:, :, h:h + kv]))
+        v.append(np.ascontiguousarray(y[:, :, h + kv:]))
+    return q, k, v
+
+
+def project_and_pack(prob: Problem, x_ranks, W, bias=None, elem_bytes=2):
+    """Projection, RoPE on q and k at global positions, and the seq -> head
+    All-to-All ([CMP] skeleton order: project, rope, then transpose), with
+    KV-head replication when n_kv_head < P.  Returns q_head, k_head, v_head."""
+    q, k, v = qkv_projection(prob, x_ranks, W, bias)
+    if prob.use_rope:
+        q = rope_seq(q, prob.rope_base, +1)
+        k = rope_seq(k, prob.rope_base, +1)
+    q_head, _, _ = a2a_seq_to_head(q, prob.n_head, elem_bytes)
+    kv_a2a = a2a_seq_to_head_replicated if prob.kv_replicas > 1 else a2a_seq_to_head
+    k_head, _, _ = kv_a2a(k, prob.n_kv_head, elem_bytes)
+    v_head, _, _ = kv_a2a(v, prob.n_kv_head, elem_bytes)
+    return q_head, k_head, v_head
+
+
 def unsharded(prob: Problem, Q, K, V, nthreads=None):
     """The same attention with no ranks: rope on global positions (one rank
     holding everything), then plain attention on [B,S,heads,D]."""

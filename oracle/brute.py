@@ -107,3 +107,23 @@ def loss(Q, K, V, dOut, causal, scale, use_rope, base):
     out, _ = forward(Q, K, V, causal, scale, use_rope, base)
     return sum(out[b][p][f] * dOut[b][p][f]
                for b in range(len(out)) for p in range(len(out[0])) for f in range(len(out[0][0])))
+
+
+def linear(x, W, bias=None):
+    """y[b][t][o] = sum_i x[b][t][i] * W[o][i] (+ bias[o]), in plain loops
+    (x: [B][S][H] nested lists, W: [out][H])."""
+    out = []
+    for xb in x:
+        rows = []
+        for xt in xb:
+            row = []
+            for o, wo in enumerate(W):
+                acc = 0.0
+                for xi, wi in zip(xt, wo):
+                    acc += xi * wi
+                if bias is not None:
+                    acc += bias[o]
+                row.append(acc)
+            rows.append(row)
+        out.append(rows)
+    return out

@@ -373,3 +373,40 @@ def test_replicated_bytes_moved(P, B, Sl, kv, D, eb):
     y = [np.zeros((B, Sl * P, 1, D)) for _ in range(P)]
     _, sent, recv = oracle.reduce_head_to_seq_replicated(y, kv, eb)
     assert sent == [want] * P and recv == [want] * P
+
+
+@pytest.mark.parametrize("P,B,S,h,kv,D,bias", [(2, 1, 6, 2, 1, 4, True), (4, 2, 8, 4, 2, 2, False), (4, 1, 8, 4, 1, 2, True)])
+def test_qkv_projection_matches_brute_force(P, B, S, h, kv, D, bias):
+    """The per-rank projection against plain loops over the unsharded tokens
+    (x W^T + b), then split into q, k, v heads."""
+    H = h * D
+    x = rnd((B, S, H), 51)
+    W = rnd(((h + 2 * kv) * D, H), 52)
+    b = rnd(((h + 2 * kv) * D,), 53) if bias else None
+    prob = _prob(P, B, S, h, kv, D, True, False)
+    q, k, v = oracle.qkv_projection(prob, oracle.shard_sequence(x, P), W, b)
+    y = np.array(brute.linear(x.tolist(), W.tolist(), None if b is None else b.tolist())).reshape(B, S, h + 2 * kv, D)
+    np.testing.assert_allclose(oracle.unshard_sequence(q), y[:, :, :h], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(oracle.unshard_sequence(k), y[:, :, h:h + kv], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(oracle.unshard_sequence(v), y[:, :, h + kv:], rtol=0, atol=1e-12)
+
+
+def test_qkv_projection_identity_weights_and_pack():
+    """Identity blocks as weights: q is x itself viewed as heads and k, v its
+    first n_kv_head heads; projecting and packing then equals packing x
+    (rotated) directly -- the fused path's definition reduces to the plain one."""
+    P, B, S, h, kv, D = 2, 2, 16, 4, 2, 8
+    H = h * D
+    x = rnd((B, S, H), 61)
+    I = np.eye(H)
+    W = np.concatenate([I, I[:kv * D], I[:kv * D]], axis=0)
+    prob = _prob(P, B, S, h, kv, D, True, True)
+    xs = oracle.shard_sequence(x, P)
+    qh, kh, vh = oracle.project_and_pack(prob, xs, W)
+    xq = [a.reshape(B, S // P, h, D) for a in xs]
+    xk = [np.ascontiguousarray(a[:, :, :kv * D]).reshape(B, S // P, kv, D) for a in xs]
+    want_q, _, _ = oracle.a2a_seq_to_head(oracle.rope_seq(xq, prob.rope_base, +1), h)
+    want_k, _, _ = oracle.a2a_seq_to_head(oracle.rope_seq(xk, prob.rope_base, +1), kv)
+    want_v, _, _ = oracle.a2a_seq_to_head(xk, kv)
+    for r in range(P):
+        assert np.array_equal(qh[r], want_q[r]) and np.array_equal(kh[r], want_k[r]) and np.array_equal(vh[r], want_v[r])
