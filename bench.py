@@ -401,6 +401,55 @@ def run_sweep(args):
     print(json.dumps({"sweep": "permute P=32 B=1 heads=32 D=128 bf16", "hbm_peak_GBs": hbm, "results": out}))
 
 
+def run_proj(args, w):
+    """The QKV projection with the pack and RoPE fused (ulysses_qkv_proj_pack) on
+    the workload's shapes with synthetic weights: X [P*B*Sl, hidden] times
+    W^T [hidden, (n_head + 2 n_kv_head) D], plus bias.  One JSON line."""
+    from ulysses_sequence_attention_seq_gb300 import binding as U
+    dev = torch.device("cuda", 0)
+    prob = U.Problem.from_workload(w)
+    buf = U.Buffers(prob, device=dev, backward=False)
+    H, N = w.hidden, (w.n_head + 2 * w.n_kv_head) * w.head_dim
+    g = torch.Generator().manual_seed(77)
+    x = U.seq_layout(torch.randn(w.B, w.S, H, generator=g).to(torch.bfloat16), w.P).to(dev)
+    W = (torch.randn(N, H, generator=g) / H ** 0.5).to(torch.bfloat16).to(dev)
+    b = (0.1 * torch.randn(N, generator=g)).to(torch.bfloat16).to(dev)
+    U.ulysses_workspace_init(prob, buf.ws)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        U.ulysses_qkv_proj_pack(prob, x, W, b, buf.q_head, buf.k_head, buf.v_head, buf.ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if U.ulysses_read_status(buf.ws) != 0:
+        raise RuntimeError("device status word set during warm-up")
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    hbm, tf_burst, tf_sust, peak_src = load_peaks()
+    flops = 2.0 * w.B * w.S * N * H
+    tf = flops / (ms * 1e-3) / 1e12
+    print(json.dumps({
+        "metric": "QKV projection + seq->head pack + RoPE (fused) TFLOP/s", "value": tf, "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic (seeded normal activations and weights)",
+        "config": {"workload": w.name, "M_tokens": w.B * w.S, "N_features": N, "K_hidden": H,
+                   "kv_replicas": w.P // w.n_kv_head if w.n_kv_head < w.P else 1},
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": tf_sust, "unit": "TFLOP/s", "frac": tf / tf_sust,
+                     "peak_source": f"{peak_src} bf16 sustained", "kernel": f"qkv_proj_kernel<{w.head_dim}>"},
+        "clocks": clk, "gpu_launches": args.steps, "device_status": U.ulysses_read_status(buf.ws)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -411,12 +460,17 @@ def main():
     ap.add_argument("--fwd-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="time the permutation alone over S = 4K..128K")
+    ap.add_argument("--proj", action="store_true",
+                    help="time the fused QKV projection + pack + RoPE on the workload's shapes")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
 
     if args.sweep:
         run_sweep(args)
+        return
+    if args.proj:
+        run_proj(args, WORKLOADS[args.workload] if args.workload in WORKLOADS else EXTRA_WORKLOADS[args.workload])
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

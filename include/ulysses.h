@@ -163,6 +163,28 @@ int ulysses_attn_fwd_folded(const ulysses_problem *prob, const void *q_seq, cons
                             ulysses_stream_t stream);
 
 /*
+ * The QKV projection with the seq -> head All-to-All and RoPE fused into it
+ * ("Sequence Parallelism II", §2 second and third steps: each rank projects
+ * its own tokens with the complete, replicated weights, then the All-to-All;
+ * "Comparing Ulysses and Megatron Sequence Parallelism", "A simple attention
+ * skeleton": q, k, v projections, viewed as heads, RoPE on q and k).
+ *   x_seq  [P][B][Sl][hidden] bf16 (the sequence-sharded activations);
+ *   w_qkv  [(n_head + 2 n_kv_head) * head_dim][hidden] bf16: the q, k and v
+ *          projection weights stacked in that order, each in the Linear
+ *          layout [out_features][in_features];
+ *   b_qkv  [(n_head + 2 n_kv_head) * head_dim] bf16, or NULL for no bias.
+ * Writes q_head/k_head/v_head exactly as ulysses_pack_qkv would from the
+ * projected q, k, v: q = x W_q^T + b_q etc. accumulated in fp32, RoPE applied
+ * in fp32, rounded once to bf16 (KV-head replication included).  `ws` (phase
+ * 0, prepared by ulysses_workspace_init) supplies the RoPE table and the
+ * status word.  bf16 and head_dim 64 or 128, else ULYSSES_ERR_UNSUPPORTED;
+ * other errors as ulysses_pack_qkv.
+ */
+int ulysses_qkv_proj_pack(const ulysses_problem *prob, const void *x_seq, const void *w_qkv,
+                          const void *b_qkv, void *q_head, void *k_head, void *v_head, void *ws,
+                          size_t ws_bytes, ulysses_stream_t stream);
+
+/*
  * Head -> seq All-to-All of the attention output ("Sequence Parallelism II",
  * §2 fifth step; "Comparing Ulysses and Megatron Sequence Parallelism",
  * "DeepSpeed Attention": [B,S,heads/P,D] back to [B,S/P,heads,D] = [B,S/P,H]):

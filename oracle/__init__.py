@@ -228,6 +228,19 @@ def rope_seq(x_ranks: Sequence[np.ndarray], base: float, direction: int = 1) -> 
     return out
 
 
+def rope_rows(x: np.ndarray, positions: Sequence[int], base: float) -> np.ndarray:
+    """The rotation of rope_seq for rows at arbitrary global positions:
+    x [n, heads, D], positions [n]; rotate-half, angle p * base^(-2i/D)."""
+    x = np.asarray(x, dtype=np.float64)
+    n, heads, D = x.shape
+    half = D // 2
+    i = np.arange(half, dtype=np.float64)
+    ang = np.asarray(positions, dtype=np.float64)[:, None] * np.power(float(base), -2.0 * i / D)[None, :]
+    c, s = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
 def attention_fwd(prob: Problem, q_head, k_head, v_head, rows=None, nthreads=None):
     """Per-rank attention over the full sequence for the rank's heads.
     Returns (o_head ranks [B,S,hp,D], lse ranks [B,hp,S]); rows not in `rows`

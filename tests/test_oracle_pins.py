@@ -410,3 +410,18 @@ def test_qkv_projection_identity_weights_and_pack():
     want_v, _, _ = oracle.a2a_seq_to_head(xk, kv)
     for r in range(P):
         assert np.array_equal(qh[r], want_q[r]) and np.array_equal(kh[r], want_k[r]) and np.array_equal(vh[r], want_v[r])
+
+
+def test_rope_rows_equals_rope_seq():
+    """rope_rows (arbitrary positions, used for sampled checks) is the same
+    rotation as the pinned rope_seq, row for row."""
+    P, B, Sl, h, D = 4, 2, 5, 3, 8
+    xs = [rnd((B, Sl, h, D), 70 + r) for r in range(P)]
+    want = oracle.rope_seq(xs, 10000.0, +1)
+    rows, pos, ref = [], [], []
+    for r in range(P):
+        for b in range(B):
+            for t in range(Sl):
+                rows.append(xs[r][b, t]); pos.append(r * Sl + t); ref.append(want[r][b, t])
+    got = oracle.rope_rows(np.stack(rows), pos, 10000.0)
+    np.testing.assert_allclose(got, np.stack(ref), rtol=0, atol=1e-12)

@@ -112,6 +112,7 @@ def lib():
         L.ulysses_attn_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_attn_bwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.ulysses_attn_bwd_prepare.argtypes = [P, vp, vp, vp, vp, sz, vp]
+        L.ulysses_qkv_proj_pack.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_selftest_wait_timeout.argtypes = [vp, sz, ctypes.c_ulonglong, vp]
         L.ulysses_attn_bwd_dkdv.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_attn_bwd_dq.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
@@ -209,6 +210,14 @@ def ulysses_attn_bwd_dq(prob, q_head, k_head, v_head, dq_seq, ws, stream=None):
     _check("ulysses_attn_bwd_dq", lib().ulysses_attn_bwd_dq(
         ctypes.byref(prob.c()), _ptr(q_head), _ptr(k_head), _ptr(v_head), _ptr(dq_seq), _ptr(ws),
         ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def ulysses_qkv_proj_pack(prob, x_seq, w_qkv, b_qkv, q_head, k_head, v_head, ws, stream=None):
+    """QKV projection of the sequence-sharded activations with the pack and
+    RoPE fused (b_qkv may be None)."""
+    _check("ulysses_qkv_proj_pack", lib().ulysses_qkv_proj_pack(
+        ctypes.byref(prob.c()), _ptr(x_seq), _ptr(w_qkv), None if b_qkv is None else _ptr(b_qkv),
+        _ptr(q_head), _ptr(k_head), _ptr(v_head), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def ulysses_selftest_wait_timeout(ws, limit_ns, stream=None):

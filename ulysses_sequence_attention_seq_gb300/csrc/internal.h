@@ -77,6 +77,10 @@ cudaError_t launch_attn_bwd_tc(const ulysses_problem &p, const TmaEncoder &enc, 
                                const float *nlse, const float *delta, const void *ws,
                                void *dq_seq, void *dk_seq, void *dv_seq, uint32_t *status,
                                cudaStream_t st);
+// QKV projection of the sequence-sharded activations with the pack and RoPE in
+// the epilogue (qkv_proj_tc.cu); bias may be null.
+cudaError_t launch_qkv_proj_pack(const ulysses_problem &p, const TmaEncoder &enc, const void *x, const void *w,
+                                 const void *bias, void *q, void *k, void *v, const void *ws, cudaStream_t st);
 // The two kernels of launch_attn_bwd_tc on their own (dK/dV, then dQ).
 cudaError_t launch_attn_bwd_dkdv(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
                                  const void *k, const void *v, const void *do_head, const float *nlse,

@@ -27,6 +27,20 @@ inline bool make_act_map(const TmaEncoder &enc, CUtensorMap *m, const void *base
          CUDA_SUCCESS;
 }
 
+// 2-D map over a row-major bf16 matrix [rows][cols] (cols contiguous): a box
+// is 64 columns (one 128-byte swizzle row) x `box_rows` rows; rows past the
+// end read as zero.
+inline bool make_mat_map(const TmaEncoder &enc, CUtensorMap *m, const void *base, long long cols, long long rows,
+                         int box_rows) {
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc.encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D map over a float array [rows][S] (LSE, delta): box of `box` positions of one row.
 inline bool make_row_map(const TmaEncoder &enc, CUtensorMap *m, const void *base, int S, int rows,
                          int box) {

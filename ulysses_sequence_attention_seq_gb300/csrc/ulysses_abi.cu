@@ -188,6 +188,27 @@ int ulysses_pack_qkv(const ulysses_problem *prob, const void *q_seq, const void 
                                  (cudaStream_t)stream));
 }
 
+int ulysses_qkv_proj_pack(const ulysses_problem *prob, const void *x_seq, const void *w_qkv, const void *b_qkv,
+                          void *q_head, void *k_head, void *v_head, void *ws, size_t ws_bytes,
+                          ulysses_stream_t stream) {
+  int rc = ulysses_validate(prob);
+  if (rc) return rc;
+  const ulysses_problem &p = *prob;
+  if (p.dtype != ULYSSES_BF16 || (p.head_dim != 64 && p.head_dim != 128)) return ULYSSES_ERR_UNSUPPORTED;
+  if (!x_seq || !w_qkv) return ULYSSES_ERR_ARG;
+  const size_t n_out = (size_t)(p.n_head + 2 * p.n_kv_head) * p.head_dim;
+  const size_t nx = (size_t)p.B * p.S * p.hidden * 2, nw = n_out * p.hidden * 2, nb = n_out * 2;
+  const size_t nq = act_bytes(p, p.n_head), nkh = kv_head_bytes(p);
+  const Span in[4] = {{x_seq, nx}, {w_qkv, nw}, {b_qkv ? b_qkv : x_seq, b_qkv ? nb : nx}, {ws, ws_bytes}};
+  const Span out[3] = {{q_head, nq}, {k_head, nkh}, {v_head, nkh}};
+  if ((rc = check_ws(p, ws, ws_bytes, 0))) return rc;
+  if ((rc = check_spans(in, 4, out, 3))) return rc;
+  TmaEncoder enc;
+  if (!get_tma_encoder(&enc)) return ULYSSES_ERR_CUDA;
+  return cuda_rc(launch_qkv_proj_pack(p, enc, x_seq, w_qkv, b_qkv, q_head, k_head, v_head, ws,
+                                      (cudaStream_t)stream));
+}
+
 int ulysses_attn_fwd(const ulysses_problem *prob, const void *q_head, const void *k_head,
                      const void *v_head, void *o_head, float *lse, void *ws, size_t ws_bytes,
                      ulysses_stream_t stream) {
