@@ -412,6 +412,25 @@ def project_and_pack(prob: Problem, x_ranks, W, bias=None, elem_bytes=2):
     return q_head, k_head, v_head
 
 
+def unpack_and_project(prob: Problem, o_head, W: np.ndarray, bias=None, elem_bytes=2):
+    """[SP2] §2 fifth step and [CMP] "DeepSpeed Attention": the head -> seq
+    All-to-All restores [B, S/P, H] on every rank, which then applies the
+    complete (replicated) output projection to its own tokens ([CMP]
+    skeleton: y = output_proj(y)).  o_head ranks [B,S,hp,D]; W [hidden,
+    n_head*D] in the Linear layout [out, in]; bias [hidden] or None.
+    Returns y ranks [B, Sl, hidden]: y = o W^T (+ b), numpy's matrix product."""
+    o_seq, _, _ = a2a_head_to_seq(o_head, prob.n_head, elem_bytes)
+    W = np.asarray(W, dtype=np.float64)
+    out = []
+    for o in o_seq:
+        B, Sl, h, D = o.shape
+        y = o.reshape(B * Sl, h * D) @ W.T
+        if bias is not None:
+            y = y + np.asarray(bias, dtype=np.float64)[None, :]
+        out.append(y.reshape(B, Sl, W.shape[0]))
+    return out
+
+
 def unsharded(prob: Problem, Q, K, V, nthreads=None):
     """The same attention with no ranks: rope on global positions (one rank
     holding everything), then plain attention on [B,S,heads,D]."""

@@ -425,3 +425,31 @@ def test_rope_rows_equals_rope_seq():
                 rows.append(xs[r][b, t]); pos.append(r * Sl + t); ref.append(want[r][b, t])
     got = oracle.rope_rows(np.stack(rows), pos, 10000.0)
     np.testing.assert_allclose(got, np.stack(ref), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("P,B,S,h,D,bias", [(2, 1, 6, 2, 4, True), (4, 2, 8, 4, 2, False)])
+def test_unpack_and_project_matches_brute_force(P, B, S, h, D, bias):
+    """Output projection after the inverse All-to-All, against plain loops
+    over the unsharded attention output (the unpack is a permutation, so
+    projecting per rank after it equals projecting the global tensor)."""
+    H = h * D
+    o = rnd((B, S, h, D), 81)
+    W = rnd((H, H), 82)
+    b = rnd((H,), 83) if bias else None
+    prob = _prob(P, B, S, h, h, D, True, False)
+    o_head, _, _ = oracle.a2a_seq_to_head(oracle.shard_sequence(o, P), h)
+    y = oracle.unpack_and_project(prob, o_head, W, b)
+    want = np.array(brute.linear(o.reshape(B, S, H).tolist(), W.tolist(), None if b is None else b.tolist()))
+    np.testing.assert_allclose(oracle.unshard_sequence(y), want, rtol=0, atol=1e-12)
+
+
+def test_unpack_and_project_identity_is_the_unpack():
+    """With W = I and no bias the fused definition is the plain unpack."""
+    P, B, S, h, D = 4, 2, 16, 4, 8
+    o = rnd((B, S, h, D), 91)
+    prob = _prob(P, B, S, h, h, D, True, False)
+    o_head, _, _ = oracle.a2a_seq_to_head(oracle.shard_sequence(o, P), h)
+    y = oracle.unpack_and_project(prob, o_head, np.eye(h * D))
+    back, _, _ = oracle.a2a_head_to_seq(o_head, h)
+    for r in range(P):
+        assert np.array_equal(y[r], back[r].reshape(B, S // P, h * D))
