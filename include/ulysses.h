@@ -195,6 +195,25 @@ int ulysses_unpack_out(const ulysses_problem *prob, const void *o_head, void *o_
                        ulysses_stream_t stream);
 
 /*
+ * The output projection with the head -> seq All-to-All folded into its
+ * operand loads ("Sequence Parallelism II", §2 fifth step: the inverse
+ * All-to-All gives every rank [B, S/P, H] back, and each rank applies the
+ * complete output projection to its own tokens; "Comparing Ulysses and
+ * Megatron Sequence Parallelism", skeleton: y = output_proj(y)).
+ *   o_head [P][B][S][hp][D] bf16 (as written by ulysses_attn_fwd);
+ *   w_o    [hidden][n_head * head_dim] bf16, the Linear layout [out][in];
+ *   b_o    [hidden] bf16, or NULL for no bias;
+ *   y_seq  [P][B][Sl][hidden] bf16: y = unpack(o) w_o^T + b_o, accumulated in
+ *          fp32 and rounded once.
+ * Requires bf16, head_dim 64 or 128 and S/P a multiple of 128 (a 128-token
+ * tile then lies in one rank's shard), else ULYSSES_ERR_UNSUPPORTED.  `ws`
+ * (phase 0) carries the status word.
+ */
+int ulysses_out_proj_unpack(const ulysses_problem *prob, const void *o_head, const void *w_o,
+                            const void *b_o, void *y_seq, void *ws, size_t ws_bytes,
+                            ulysses_stream_t stream);
+
+/*
  * Backward of the whole path ("Sequence Parallelism II", §6; "Comparing
  * Ulysses and Megatron Sequence Parallelism", "DeepSpeed Attention costs":
  * the inverse All-to-All for each tensor): dO_seq [P][B][Sl][H] goes seq ->

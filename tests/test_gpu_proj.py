@@ -78,3 +78,56 @@ def test_qkv_proj_pack_full_size_sampled():
     for hd in range(kv):
         assert_close(to64(buf.k_head[hd // kvp, 0, rows_t, hd % kvp]), k[:, hd], w, f"k head {hd}")
         assert_close(to64(buf.v_head[hd // kvp, 0, rows_t, hd % kvp]), v[:, hd], w, f"v head {hd}")
+
+
+OUT_CASES = [wl(2, 1, 512, 4, 4, 128),                      # 4 x 2 tiles
+             wl(4, 2, 1024, 8, 8, 64),                      # D = 64, B = 2
+             wl(1, 1, 256, 3, 1, 128, rope=False),          # hidden 384: a half feature tile
+             wl(8, 1, 2048, 32, 8, 128)]                    # the GQA workload's head layout
+
+
+@pytest.mark.parametrize("bias", [True, False])
+@pytest.mark.parametrize("w", OUT_CASES, ids=lambda w: f"P{w.P}B{w.B}S{w.S}h{w.n_head}D{w.head_dim}")
+def test_out_proj_unpack_matches_oracle(w, bias):
+    prob = U.Problem.from_workload(w)
+    buf = U.Buffers(prob)
+    dev = buf.q_head.device
+    g = torch.Generator().manual_seed(13)
+    H = w.hidden
+    o_head = torch.randn(w.P, w.B, w.S, w.n_head // w.P, w.head_dim, generator=g).to(torch.bfloat16)
+    W = (torch.randn(H, H, generator=g) / H ** 0.5).to(torch.bfloat16)
+    b = (0.1 * torch.randn(H, generator=g)).to(torch.bfloat16) if bias else None
+    y = torch.empty(w.P, w.B, w.Sl, H, dtype=torch.bfloat16, device=dev)
+    U.ulysses_workspace_init(prob, buf.ws)
+    U.ulysses_out_proj_unpack(prob, o_head.to(dev), W.to(dev), None if b is None else b.to(dev), y, buf.ws)
+    torch.cuda.synchronize()
+    assert U.ulysses_read_status(buf.ws) == 0
+    want = oracle.unpack_and_project(oracle_problem(w), list(to64(o_head)), to64(W), None if b is None else to64(b))
+    assert_close(to64(y), np.stack(want), w, "y_seq")
+
+
+def test_out_proj_unpack_full_size_sampled():
+    """The pages' sizing (P=8, S=32768, hidden 4096) in the launch
+    configuration the bench times, on sampled tokens of every rank."""
+    from ulysses_sequence_attention_seq_gb300.synthetic import WORKLOADS
+    w = WORKLOADS["C4"]
+    prob = U.Problem.from_workload(w)
+    buf = U.Buffers(prob)
+    dev = buf.q_head.device
+    g = torch.Generator().manual_seed(17)
+    H, hp, D = w.hidden, w.n_head // w.P, w.head_dim
+    o_head = torch.randn(w.P, w.B, w.S, hp, D, generator=g).to(torch.bfloat16)
+    W = (torch.randn(H, H, generator=g) / H ** 0.5).to(torch.bfloat16)
+    b = (0.1 * torch.randn(H, generator=g)).to(torch.bfloat16)
+    y = torch.empty(w.P, w.B, w.Sl, H, dtype=torch.bfloat16, device=dev)
+    U.ulysses_workspace_init(prob, buf.ws)
+    U.ulysses_out_proj_unpack(prob, o_head.to(dev), W.to(dev), b.to(dev), y, buf.ws)
+    torch.cuda.synchronize()
+    assert U.ulysses_read_status(buf.ws) == 0
+    rows = sample_rows(w, 48, seed=4)
+    o64 = to64(o_head)
+    # token p's feature vector: head hd comes from rank hd // hp, local head hd % hp
+    x = np.stack([np.concatenate([o64[hd // hp, 0, pos, hd % hp] for hd in range(w.n_head)]) for pos in rows])
+    want = x @ to64(W).T + to64(b)[None, :]
+    got = np.stack([to64(y[pos // w.Sl, 0, pos % w.Sl]) for pos in rows])
+    assert_close(got, want, w, "y rows")

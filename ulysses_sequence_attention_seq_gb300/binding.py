@@ -113,6 +113,7 @@ def lib():
         L.ulysses_attn_bwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.ulysses_attn_bwd_prepare.argtypes = [P, vp, vp, vp, vp, sz, vp]
         L.ulysses_qkv_proj_pack.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.ulysses_out_proj_unpack.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_selftest_wait_timeout.argtypes = [vp, sz, ctypes.c_ulonglong, vp]
         L.ulysses_attn_bwd_dkdv.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_attn_bwd_dq.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
@@ -218,6 +219,14 @@ def ulysses_qkv_proj_pack(prob, x_seq, w_qkv, b_qkv, q_head, k_head, v_head, ws,
     _check("ulysses_qkv_proj_pack", lib().ulysses_qkv_proj_pack(
         ctypes.byref(prob.c()), _ptr(x_seq), _ptr(w_qkv), None if b_qkv is None else _ptr(b_qkv),
         _ptr(q_head), _ptr(k_head), _ptr(v_head), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def ulysses_out_proj_unpack(prob, o_head, w_o, b_o, y_seq, ws, stream=None):
+    """Output projection of the head-layout attention output with the unpack
+    folded into its loads (b_o may be None)."""
+    _check("ulysses_out_proj_unpack", lib().ulysses_out_proj_unpack(
+        ctypes.byref(prob.c()), _ptr(o_head), _ptr(w_o), None if b_o is None else _ptr(b_o), _ptr(y_seq),
+        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def ulysses_selftest_wait_timeout(ws, limit_ns, stream=None):

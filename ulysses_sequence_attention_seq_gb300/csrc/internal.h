@@ -81,6 +81,10 @@ cudaError_t launch_attn_bwd_tc(const ulysses_problem &p, const TmaEncoder &enc, 
 // the epilogue (qkv_proj_tc.cu); bias may be null.
 cudaError_t launch_qkv_proj_pack(const ulysses_problem &p, const TmaEncoder &enc, const void *x, const void *w,
                                  const void *bias, void *q, void *k, void *v, const void *ws, cudaStream_t st);
+// Output projection with the head -> seq unpack folded into its operand loads
+// (qkv_proj_tc.cu); needs S/P % 128 == 0; bias may be null.
+cudaError_t launch_out_proj_unpack(const ulysses_problem &p, const TmaEncoder &enc, const void *o_head,
+                                   const void *w, const void *bias, void *y, const void *ws, cudaStream_t st);
 // The two kernels of launch_attn_bwd_tc on their own (dK/dV, then dQ).
 cudaError_t launch_attn_bwd_dkdv(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
                                  const void *k, const void *v, const void *do_head, const float *nlse,

@@ -29,6 +29,16 @@
 //               tile, thread = token row = TMEM lane; it drains accumulator
 //               t & 1 while the MMAs of the next tile fill the other.
 // All waits are bounded; a timeout sets the forward-timeout status bit.
+//
+// The same kernel in its second mode is the output projection fused with the
+// head -> seq All-to-All ([SP2] §2 fifth step: the inverse All-to-All restores
+// [B, S/P, H], then every rank applies the complete output projection to its
+// tokens; [CMP] skeleton: y = output_proj(y)).  The A operand is the attention
+// output in head layout: the 64 input features of a K-block lie in one head,
+// computed by rank head / hp, and a 128-token tile lies in one sequence shard
+// (S/P a multiple of 128), so each A tile is one TMA box of that rank's
+// head-sharded buffer at the tile's global positions -- the unpack becomes the
+// load addressing.  The epilogue adds the bias and writes sequence-layout rows.
 #include <cuda_bf16.h>
 #include <math.h>
 #include <stdint.h>
@@ -63,13 +73,16 @@ enum : uint32_t {
 };
 constexpr uint32_t kAlloc = kBarOff + 128 + 1024;  // room to align the base to 1024
 
+enum ProjMode { kQkvPack = 0, kOutUnpack = 1 };
+
 struct ProjParams {
-  int M, N, H;  // tokens (P*B*Sl), output features, hidden
+  int M, N, H;  // tokens (P*B*Sl), output features, input features
   int B, Sl, S, P, n_head, n_kv, hp, kvp, R;
   int n_mt, n_nt;
   const __nv_bfloat16 *bias;         // [N] or null
   const float *rope_cos, *rope_sin;  // [S][D/2] or null
-  __nv_bfloat16 *q, *k, *v;          // head layout
+  __nv_bfloat16 *q, *k, *v;          // head layout (QKV mode)
+  __nv_bfloat16 *y;                  // [P][B][Sl][N] sequence layout (output mode)
   uint32_t *status;
   uint32_t rope_key;
 };
@@ -83,7 +96,7 @@ __device__ __forceinline__ void tile_mn(const ProjParams &p, int t, int &m, int 
   n = r / gm;
 }
 
-template <int D>
+template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     qkv_proj_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                     const ProjParams p) {
@@ -141,7 +154,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           mbar_arrive_expect_tx(bar + kBFull + 8 * st, kStage);
           const uint32_t sA = sb + st * kStage;
-          dev::tma_load_2d(sA, &tmX, bar + kBFull + 8 * st, kb * BK, m * BM);
+          if (MODE == kQkvPack) {
+            dev::tma_load_2d(sA, &tmX, bar + kBFull + 8 * st, kb * BK, m * BM);
+          } else {
+            // features [64kb, 64kb+64) are elements e0.. of head hd (rank hd / hp,
+            // local head hd % hp); tokens m*128.. are positions pos0.. of (s, b)
+            const int f0 = kb * BK, hd = f0 / D, e0 = f0 - hd * D;
+            const int m0 = m * BM, sbk = m0 / p.Sl, pos0 = (sbk / p.B) * p.Sl + (m0 - sbk * p.Sl);
+            tma_load_4d(sA, &tmX, bar + kBFull + 8 * st, e0, hd % p.hp, pos0, (hd / p.hp) * p.B + sbk % p.B);
+          }
           dev::tma_load_2d(sA + kATile, &tmW, bar + kBFull + 8 * st, kb * BK, n * BN);
           issued = it;
         }
@@ -206,6 +227,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const int row = m * BM + w4 * 32 + lane;
       const bool live = row < p.M;
+      if (MODE == kOutUnpack) {
+        // plain sequence-layout rows: columns [128g, 128g+128) of the tile, + bias
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int col = n * BN + g * 128 + c * 32;
+          if (col >= p.N) break;  // ragged feature tail: the same for the whole warp
+          uint32_t xr[32];
+          tmem_ld32(tmem + lane_base + acc * BN + g * 128 + c * 32, xr);
+          tmem_wait_ld();
+          reg_fence(xr);
+          uint32_t wx[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float a = __uint_as_float(xr[2 * e]), b2 = __uint_as_float(xr[2 * e + 1]);
+            if (p.bias) {
+              a += __bfloat162float(p.bias[col + 2 * e]);
+              b2 += __bfloat162float(p.bias[col + 2 * e + 1]);
+            }
+            wx[e] = pack_bf16x2(a, b2);
+          }
+          if (live) {
+            uint4 *o = reinterpret_cast<uint4 *>(p.y + (size_t)row * p.N + col);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) o[v] = make_uint4(wx[4 * v], wx[4 * v + 1], wx[4 * v + 2], wx[4 * v + 3]);
+          }
+        }
+        tc_fence_before_sync();
+        mbar_arrive(bar + kBAccEmpty + 8 * acc);
+        continue;
+      }
       const int rr = live ? row : 0;
       const int tt = rr % p.Sl, sbk = rr / p.Sl;  // row = (s*B + b)*Sl + t
       const int b = sbk % p.B, s = sbk / p.B;
@@ -314,13 +365,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && *abort_flag) atomicOr(p.status, (uint32_t)ULYSSES_STATUS_FWD_TIMEOUT);
 }
 
-template <int D>
+template <int D, int MODE>
 cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void *x, const void *w,
-                     const void *bias, void *q, void *k, void *v, const void *ws, cudaStream_t st) {
+                     const void *bias, void *q, void *k, void *v, void *y, const void *ws, cudaStream_t st) {
   ProjParams pp;
-  pp.H = p.hidden;
+  pp.H = MODE == kQkvPack ? p.hidden : p.n_head * D;
   pp.M = p.B * p.S;
-  pp.N = (p.n_head + 2 * p.n_kv_head) * D;
+  pp.N = MODE == kQkvPack ? (p.n_head + 2 * p.n_kv_head) * D : p.hidden;
   pp.B = p.B;
   pp.Sl = p.S / p.P;
   pp.S = p.S;
@@ -344,19 +395,23 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   pp.q = static_cast<__nv_bfloat16 *>(q);
   pp.k = static_cast<__nv_bfloat16 *>(k);
   pp.v = static_cast<__nv_bfloat16 *>(v);
+  pp.y = static_cast<__nv_bfloat16 *>(y);
+  if (MODE == kOutUnpack) pp.rope_cos = pp.rope_sin = nullptr;  // no rotation on the output
   pp.status = reinterpret_cast<uint32_t *>(const_cast<uint8_t *>(wsb + L.status));
   pp.rope_key = rope_key(p);
   CUtensorMap mx, mw;
-  if (!make_mat_map(enc, &mx, x, pp.H, pp.M, BM) || !make_mat_map(enc, &mw, w, pp.H, pp.N, BN))
-    return cudaErrorInvalidValue;
+  const bool ok_x = MODE == kQkvPack ? make_mat_map(enc, &mx, x, pp.H, pp.M, BM)
+                                     : make_act_map(enc, &mx, x, D, pp.hp, p.S, p.P * p.B, BM);
+  if (!ok_x || !make_mat_map(enc, &mw, w, pp.H, pp.N, BN)) return cudaErrorInvalidValue;
   int dev = 0, sms = 152;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long tiles = (long long)pp.n_mt * pp.n_nt;
   if (tiles > 0x7fffffffll) return cudaErrorInvalidValue;
   const int grid = (int)(tiles < sms ? tiles : sms);
-  cudaError_t e = cudaFuncSetAttribute(qkv_proj_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAlloc);
+  cudaError_t e =
+      cudaFuncSetAttribute(qkv_proj_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAlloc);
   if (e != cudaSuccess) return e;
-  qkv_proj_kernel<D><<<grid, kThreads, kAlloc, st>>>(mx, mw, pp);
+  qkv_proj_kernel<D, MODE><<<grid, kThreads, kAlloc, st>>>(mx, mw, pp);
   return cudaGetLastError();
 }
 
@@ -364,8 +419,17 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
 
 cudaError_t launch_qkv_proj_pack(const ulysses_problem &p, const TmaEncoder &enc, const void *x, const void *w,
                                  const void *bias, void *q, void *k, void *v, const void *ws, cudaStream_t st) {
-  if (p.head_dim == 128) return launch_d<128>(p, enc, x, w, bias, q, k, v, ws, st);
-  if (p.head_dim == 64) return launch_d<64>(p, enc, x, w, bias, q, k, v, ws, st);
+  if (p.head_dim == 128) return launch_d<128, kQkvPack>(p, enc, x, w, bias, q, k, v, nullptr, ws, st);
+  if (p.head_dim == 64) return launch_d<64, kQkvPack>(p, enc, x, w, bias, q, k, v, nullptr, ws, st);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_out_proj_unpack(const ulysses_problem &p, const TmaEncoder &enc, const void *o_head,
+                                   const void *w, const void *bias, void *y, const void *ws, cudaStream_t st) {
+  if (p.head_dim == 128)
+    return launch_d<128, kOutUnpack>(p, enc, o_head, w, bias, nullptr, nullptr, nullptr, y, ws, st);
+  if (p.head_dim == 64)
+    return launch_d<64, kOutUnpack>(p, enc, o_head, w, bias, nullptr, nullptr, nullptr, y, ws, st);
   return cudaErrorInvalidValue;
 }
 

@@ -209,6 +209,25 @@ int ulysses_qkv_proj_pack(const ulysses_problem *prob, const void *x_seq, const 
                                       (cudaStream_t)stream));
 }
 
+int ulysses_out_proj_unpack(const ulysses_problem *prob, const void *o_head, const void *w_o, const void *b_o,
+                            void *y_seq, void *ws, size_t ws_bytes, ulysses_stream_t stream) {
+  int rc = ulysses_validate(prob);
+  if (rc) return rc;
+  const ulysses_problem &p = *prob;
+  if (p.dtype != ULYSSES_BF16 || (p.head_dim != 64 && p.head_dim != 128) || (p.S / p.P) % 128 != 0)
+    return ULYSSES_ERR_UNSUPPORTED;
+  if (!o_head || !w_o) return ULYSSES_ERR_ARG;
+  const size_t no = act_bytes(p, p.n_head), nw = (size_t)p.hidden * p.hidden * 2, nb = (size_t)p.hidden * 2;
+  const size_t ny = (size_t)p.B * p.S * p.hidden * 2;
+  const Span in[3] = {{o_head, no}, {w_o, nw}, {b_o ? b_o : o_head, b_o ? nb : no}};
+  const Span out[2] = {{y_seq, ny}, {ws, ws_bytes}};
+  if ((rc = check_ws(p, ws, ws_bytes, 0))) return rc;
+  if ((rc = check_spans(in, 3, out, 2))) return rc;
+  TmaEncoder enc;
+  if (!get_tma_encoder(&enc)) return ULYSSES_ERR_CUDA;
+  return cuda_rc(launch_out_proj_unpack(p, enc, o_head, w_o, b_o, y_seq, ws, (cudaStream_t)stream));
+}
+
 int ulysses_attn_fwd(const ulysses_problem *prob, const void *q_head, const void *k_head,
                      const void *v_head, void *o_head, float *lse, void *ws, size_t ws_bytes,
                      ulysses_stream_t stream) {
