@@ -461,6 +461,24 @@ def run_proj(args, w):
         otf = 2.0 * w.B * w.S * H * (w.n_head * w.head_dim) / (oms * 1e-3) / 1e12
         out = {"kernel": f"qkv_proj_kernel<{w.head_dim}, out>", "ms": oms, "achieved_tflops": otf,
                "frac": otf / tf_sust, "M_tokens": w.B * w.S, "N_features": H, "K_features": w.n_head * w.head_dim}
+
+        # the whole attention layer forward: projection + pack + RoPE, attention,
+        # output projection + unpack
+        def lstep():
+            step()
+            U.ulysses_attn_fwd(prob, buf.q_head, buf.k_head, buf.v_head, buf.o_head, buf.lse, buf.ws)
+            ostep()
+
+        for _ in range(args.warmup):
+            lstep()
+        a.record(stream)
+        for _ in range(args.steps):
+            lstep()
+        b2.record(stream)
+        torch.cuda.synchronize()
+        lms = a.elapsed_time(b2) / args.steps
+        out["layer_fwd"] = {"ms": lms, "tokens_per_s": w.B * w.S / (lms * 1e-3),
+                            "calls": "ulysses_qkv_proj_pack + ulysses_attn_fwd + ulysses_out_proj_unpack"}
     print(json.dumps({
         "metric": "QKV projection + seq->head pack + RoPE (fused) TFLOP/s", "value": tf, "unit": "TFLOP/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,

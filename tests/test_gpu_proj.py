@@ -131,3 +131,32 @@ def test_out_proj_unpack_full_size_sampled():
     want = x @ to64(W).T + to64(b)[None, :]
     got = np.stack([to64(y[pos // w.Sl, 0, pos % w.Sl]) for pos in rows])
     assert_close(got, want, w, "y rows")
+
+
+@pytest.mark.parametrize("w", [wl(2, 1, 512, 4, 2, 128), wl(4, 1, 1024, 8, 2, 64, causal=False)],
+                         ids=lambda w: f"P{w.P}S{w.S}h{w.n_head}kv{w.n_kv_head}D{w.head_dim}")
+def test_attention_layer_forward_matches_oracle(w):
+    """The whole Ulysses attention layer through the C ABI -- QKV projection
+    with the pack and RoPE, attention, output projection with the unpack --
+    against the oracle's steps in the pages' order."""
+    prob = U.Problem.from_workload(w)
+    buf = U.Buffers(prob)
+    dev = buf.q_head.device
+    x, W, b = _weights(w, True, 21)
+    g = torch.Generator().manual_seed(22)
+    H = w.hidden
+    Wo = (torch.randn(H, H, generator=g) / H ** 0.5).to(torch.bfloat16)
+    bo = (0.1 * torch.randn(H, generator=g)).to(torch.bfloat16)
+    y = torch.empty(w.P, w.B, w.Sl, H, dtype=torch.bfloat16, device=dev)
+    U.ulysses_workspace_init(prob, buf.ws)
+    U.ulysses_qkv_proj_pack(prob, U.seq_layout(x, w.P).to(dev), W.to(dev), b.to(dev), buf.q_head, buf.k_head,
+                            buf.v_head, buf.ws)
+    U.ulysses_attn_fwd(prob, buf.q_head, buf.k_head, buf.v_head, buf.o_head, buf.lse, buf.ws)
+    U.ulysses_out_proj_unpack(prob, buf.o_head, Wo.to(dev), bo.to(dev), y, buf.ws)
+    torch.cuda.synchronize()
+    assert U.ulysses_read_status(buf.ws) == 0
+    op = oracle_problem(w)
+    qh, kh, vh = oracle.project_and_pack(op, oracle.shard_sequence(to64(x), w.P), to64(W), to64(b))
+    o_head, _ = oracle.attention_fwd(op, qh, kh, vh)
+    want = oracle.unpack_and_project(op, o_head, to64(Wo), to64(bo))
+    assert_close(to64(y), np.stack(want), w, "layer y")
