@@ -43,7 +43,6 @@ METRIC = "tokens/s + attn TFLOP/s (S=32K, 32 heads, P=8 virtual); seq↔head per
 # capture of this build (profiles/launches_c4_fwd_bwd.md gives the command and
 # the table); a kernel changed since its capture has no entry.
 TRAFFIC = {
-    ("attn_fwd", "C4"): 1174501089,
     ("bwd_dkdv", "C4"): 1876801251,
     ("bwd_dq", "C4"): 1757049486,
 }

@@ -10,10 +10,13 @@
 // How: one CTA per pair of 128-query tiles (A = rows [256i, 256i+128),
 // B = the next 128) of one head, 12 warps (warps 10-11 only complete the
 // third warpgroup, which the per-warpgroup register split needs).
-//   warp 8      TMA producer: both Q tiles once, then K_0, V_0, K_1, V_1, ...
-//               through a 4-slot ring (128 rows x D, 128-byte swizzle, 4-D
-//               tensor maps over [P*B][S][heads][D] so a tile never crosses a
-//               sequence end).  Every K/V tile serves 256 query rows.
+//   warp 8      TMA producer: both Q tiles and K_0 once, then ring entries
+//               e = 0, 1, ... of a 2-entry ring, entry e holding V_e and
+//               K_{e+1}: exactly what key tile e's two bursts below read, so
+//               one barrier reports both (128 rows x D per tile, 128-byte
+//               swizzle, 4-D tensor maps over [P*B][S][heads][D] so a tile
+//               never crosses a sequence end).  Every K/V tile serves 256
+//               query rows.
 //   warp 9      MMA issuer (one thread), in the order
 //                 S_A(0) S_B(0) | PV_A(0) S_A(1) PV_B(0) S_B(1) | PV_A(1) ...
 //               so the tensor core alternates between the two tiles while the
@@ -26,8 +29,9 @@
 //               before issuing any of it: a thread with MMAs in flight stalls
 //               on its next shared-memory access (such as a barrier wait)
 //               until they have been taken by the tensor core, and each such
-//               stall leaves a gap in the pipe, so there are two per key tile
-//               rather than one per operand.
+//               stall leaves a gap in the pipe, so there are two waits per
+//               key tile (P_A(j) with entry j, then P_B(j)) rather than one
+//               per operand.
 //   warps 0-3   softmax of tile A, warps 4-7 of tile B: thread i of a
 //               warpgroup owns query row i = TMEM lane i.  It reads its score
 //               row from TMEM, takes the row maximum (base-2 domain) on the
@@ -68,31 +72,35 @@ constexpr int kTmaWarp = 8, kMmaWarp = 9;
 // softmax warpgroups rise to 216: 128*72 + 256*216 = 64512 = 384*168.
 constexpr uint32_t kRegsProducer = 72, kRegsSoftmax = 216;
 static_assert(128 * kRegsProducer + 256 * kRegsSoftmax <= 384 * 168, "register split over budget");
-constexpr int kSlots = 4;  // K/V ring
+constexpr int kSlots = 2;  // K/V ring entries: entry e holds V_e and K_{e+1}
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kChunkBytes = 128 * 128;    // 128 rows x 128 bytes (64 bf16)
 
 template <int D>
 struct Layout {
   static constexpr uint32_t kTile = 128u * D * 2;       // one 128-row tile of Q, K or V
+  static constexpr uint32_t kEntry = 2 * kTile;          // V_e, then K_{e+1}
   static constexpr uint32_t kQ = 0;                      // Q_A, Q_B
-  static constexpr uint32_t kKV = kQ + 2 * kTile;        // ring of kSlots tiles
-  static constexpr uint32_t kBar = kKV + kSlots * kTile;
+  static constexpr uint32_t kK0 = kQ + 2 * kTile;        // K_0
+  static constexpr uint32_t kKV = kK0 + kTile;           // ring of kSlots entries
+  static constexpr uint32_t kBar = kKV + kSlots * kEntry;
   static constexpr uint32_t kAlloc = kBar + 256 + 1024;  // room to align the base to 1024
 };
+static_assert(Layout<128>::kAlloc <= 232448, "shared memory");
 
 // Barrier slots (byte offsets inside the barrier block).
 enum : uint32_t {
   kBarQFull = 0,
-  kBarKVFull = 8,    // [4]
-  kBarKVEmpty = 40,  // [4]
-  kBarSFull = 72,    // [2] A, B
-  kBarPFull = 88,    // [2] A, B (128 arrivals)
-  kBarODone = 104,   // [2] A, B
-  kBarDrain = 120,
-  kTmemSlot = 128,
-  kAbortSlot = 132
+  kBarKVFull = 8,                         // [kSlots]
+  kBarKVEmpty = kBarKVFull + 8 * kSlots,  // [kSlots]
+  kBarSFull = kBarKVEmpty + 8 * kSlots,   // [2] A, B
+  kBarPFull = kBarSFull + 16,             // [2] A, B (128 arrivals)
+  kBarODone = kBarPFull + 16,             // [2] A, B
+  kBarDrain = kBarODone + 16,
+  kTmemSlot = kBarDrain + 8,
+  kAbortSlot = kTmemSlot + 4
 };
+static_assert(kAbortSlot + 4 <= 256, "barrier block");
 
 struct FwdParams {
   int B, S, P, hp, kvp, group, causal, n_pairs;
@@ -122,9 +130,9 @@ __device__ __forceinline__ TileCoord tile_coord(const FwdParams &p, int rb, int 
   return {rep > 1 ? r / rep : r * heads_local + lh, pos - src * p.Sl, src * p.B + b};
 }
 
-// Position in the K/V ring of the n-th tile streamed (K_j is n = 2j, V_j is 2j+1).
-__device__ __forceinline__ uint32_t ring_slot(int n) { return (uint32_t)(n % kSlots); }
-__device__ __forceinline__ uint32_t ring_parity(int n) { return (uint32_t)((n / kSlots) & 1); }
+// Slot and phase parity of ring entry e.
+__device__ __forceinline__ uint32_t ring_slot(int e) { return (uint32_t)(e % kSlots); }
+__device__ __forceinline__ uint32_t ring_parity(int e) { return (uint32_t)((e / kSlots) & 1); }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -138,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
   uint8_t *smem = smem_raw + pad;
   const uint32_t sb = raw + pad;
-  const uint32_t sQ = sb + L::kQ, sKV = sb + L::kKV;
+  const uint32_t sQ = sb + L::kQ, sK0 = sb + L::kK0, sKV = sb + L::kKV;
   const uint32_t bar = sb + L::kBar;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kBar + kAbortSlot);
   const volatile uint32_t *gst = p.status;
@@ -191,33 +199,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
-        mbar_arrive_expect_tx(bar + kBarQFull, 2 * L::kTile);
+        // Q_A, Q_B and K_0 on one barrier
+        mbar_arrive_expect_tx(bar + kBarQFull, 3 * L::kTile);
         for (int x = 0; x < 2; ++x) {
           const TileCoord tq = tile_coord(p, rb, j, p.hp, qp * 2 * BM + x * BM);
           for (int c = 0; c < kChunks; ++c)
             tma_load_4d(sQ + x * L::kTile + c * kChunkBytes, &tmQ, bar + kBarQFull, c * 64, tq.head,
                         tq.row, tq.outer);
         }
+        const TileCoord t0 = tile_coord(p, rb, kl, p.kvp, 0, p.kv_rep);
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_4d(sK0 + c * kChunkBytes, &tmK, bar + kBarQFull, c * 64, t0.head, t0.row, t0.outer);
+        // entry e = V_e and (when tile B goes on) K_{e+1}: what key tile e's two bursts read
         int issued = -1;
-        for (int n = 0; n < 2 * nB; ++n) {
-          const uint32_t slot = ring_slot(n);
-          if (!mbar_wait_bounded(bar + kBarKVEmpty + 8 * slot, ring_parity(n) ^ 1, abort_flag, gst))
-            break;
-          mbar_arrive_expect_tx(bar + kBarKVFull + 8 * slot, L::kTile);
-          const CUtensorMap *m = (n & 1) ? &tmV : &tmK;
-          const TileCoord tk = tile_coord(p, rb, kl, p.kvp, (n >> 1) * BN, p.kv_rep);
+        for (int e = 0; e < nB; ++e) {
+          const uint32_t slot = ring_slot(e), full = bar + kBarKVFull + 8 * slot;
+          if (!mbar_wait_bounded(bar + kBarKVEmpty + 8 * slot, ring_parity(e) ^ 1, abort_flag, gst)) break;
+          const bool has_k = e + 1 < nB;
+          mbar_arrive_expect_tx(full, (has_k ? 2u : 1u) * L::kTile);
+          const uint32_t dst = sKV + slot * L::kEntry;
+          const TileCoord tv = tile_coord(p, rb, kl, p.kvp, e * BN, p.kv_rep);
           for (int c = 0; c < kChunks; ++c)
-            tma_load_4d(sKV + slot * L::kTile + c * kChunkBytes, m, bar + kBarKVFull + 8 * slot,
-                        c * 64, tk.head, tk.row, tk.outer);
-          issued = n;
+            tma_load_4d(dst + c * kChunkBytes, &tmV, full, c * 64, tv.head, tv.row, tv.outer);
+          if (has_k) {
+            const TileCoord tk = tile_coord(p, rb, kl, p.kvp, (e + 1) * BN, p.kv_rep);
+            for (int c = 0; c < kChunks; ++c)
+              tma_load_4d(dst + L::kTile + c * kChunkBytes, &tmK, full, c * 64, tk.head, tk.row, tk.outer);
+          }
+          issued = e;
         }
         if (*abort_flag) {
           // Let the copies already in flight land before the CTA goes away.
           volatile int never = 0;
           mbar_wait_bounded(bar + kBarQFull, 0, &never, nullptr, 500000000ull);
-          for (int n = issued - (kSlots - 1); n <= issued; ++n)
-            if (n >= 0)
-              mbar_wait_bounded(bar + kBarKVFull + 8 * ring_slot(n), ring_parity(n), &never, nullptr,
+          for (int e = issued - (kSlots - 1); e <= issued; ++e)
+            if (e >= 0)
+              mbar_wait_bounded(bar + kBarKVFull + 8 * ring_slot(e), ring_parity(e), &never, nullptr,
                                 500000000ull);
         }
       }
@@ -228,8 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t idPV = idesc_bf16_f32(BM, D, 0, 1);  // P (TMEM), V MN-major
         // S_x(t) = Q_x K_t^T (K_t has landed: the caller waited for it).
         auto issue_s = [&](int x, int t) {
-          const int n = 2 * t;
-          const uint32_t kt = sKV + ring_slot(n) * L::kTile;
+          const uint32_t kt = t == 0 ? sK0 : sKV + ring_slot(t - 1) * L::kEntry + L::kTile;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t koff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
@@ -240,8 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         // O_x += P_x(t) V_t (P_x(t) published and V_t landed: the caller waited).
         auto issue_pv = [&](int x, int t) {
-          const int n = 2 * t + 1;
-          const uint32_t vt = sKV + ring_slot(n) * L::kTile;
+          const uint32_t vt = sKV + ring_slot(t) * L::kEntry;
           // keys 16kk..16kk+15 of P_X are TMEM columns x*BN + 8kk ..
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
@@ -249,19 +264,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_bf16_ts(tmem + 2 * BN + x * D, tmem + x * BN + kk * 8, b, idPV, (t > 0 || kk > 0) ? 1u : 0u);
           }
         };
-        auto kv_ready = [&](int n) -> bool {
-          return mbar_wait_bounded(bar + kBarKVFull + 8 * ring_slot(n), ring_parity(n), abort_flag, gst);
+        auto entry_ready = [&](int e) -> bool {
+          return mbar_wait_bounded(bar + kBarKVFull + 8 * ring_slot(e), ring_parity(e), abort_flag, gst);
         };
-        bool ok = mbar_wait_bounded(bar + kBarQFull, 0, abort_flag, gst) && kv_ready(0);
+        // Entry t is free once key tile t's two bursts have finished: its
+        // commit follows tile B's burst.  (A commit at the head of a burst,
+        // issued while the pipe is idle after the waits, was measured to delay
+        // the burst's MMAs by ~90 cycles; at the tail it costs nothing.)
+        auto release = [&](int e) { mma_commit(bar + kBarKVEmpty + 8 * ring_slot(e)); };
+        bool ok = mbar_wait_bounded(bar + kBarQFull, 0, abort_flag, gst);
         if (ok && nA > 0) issue_s(0, 0);
         if (ok) issue_s(1, 0);
-        if (ok) mma_commit(bar + kBarKVEmpty + 8 * ring_slot(0));
         for (int t = 0; ok && t < nB; ++t) {
-          // every wait of tile A's burst first: P_A(t), V_t and (when A goes on) K_{t+1}
+          // every wait of tile A's burst first: P_A(t) and entry t
           if (t < nA) {
-            if (!(ok = mbar_wait_bounded(bar + kBarPFull, t & 1, abort_flag, gst) && kv_ready(2 * t + 1) &&
-                       (t == nA - 1 || kv_ready(2 * t + 2))))
-              break;
+            if (!(ok = mbar_wait_bounded(bar + kBarPFull, t & 1, abort_flag, gst) && entry_ready(t))) break;
             tc_fence_after_sync();
             issue_pv(0, t);
             if (t == nA - 1)
@@ -269,19 +286,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
               issue_s(0, t + 1);
           }
-          // then tile B's: P_B(t), V_t and K_{t+1} (again only if A skipped them)
-          if (!(ok = mbar_wait_bounded(bar + kBarPFull + 8, t & 1, abort_flag, gst) &&
-                     (t < nA || kv_ready(2 * t + 1)) && (t == nB - 1 || kv_ready(2 * t + 2))))
+          // then tile B's: P_B(t) (and entry t if A skipped it)
+          if (!(ok = mbar_wait_bounded(bar + kBarPFull + 8, t & 1, abort_flag, gst) && (t < nA || entry_ready(t))))
             break;
           tc_fence_after_sync();
           issue_pv(1, t);
-          mma_commit(bar + kBarKVEmpty + 8 * ring_slot(2 * t + 1));
-          if (t == nB - 1) {
+          if (t == nB - 1)
             mma_commit(bar + kBarODone + 8);
-          } else {
+          else
             issue_s(1, t + 1);
-            mma_commit(bar + kBarKVEmpty + 8 * ring_slot(2 * t + 2));
-          }
+          release(t);
         }
         // All tensor-core work of this CTA is complete once this commit lands.
         mma_commit(bar + kBarDrain);
