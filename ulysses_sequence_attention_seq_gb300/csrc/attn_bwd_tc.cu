@@ -119,11 +119,15 @@ __device__ __forceinline__ void store_unrotated(__nv_bfloat16 *dx, __nv_bfloat16
 // computed while the softmax warps form dS^T(i); dP^T(i+1) likewise follows
 // dK(i) and runs while they form P^T(i+1).  So the tensor core never waits for
 // the softmax of its own step as long as each softmax phase is shorter than
-// two MMA groups.  The issuer takes every wait of a burst (dV(i) S^T(i+1), or
-// dK(i) dP^T(i+1)) before issuing any of it: a thread with MMAs in flight
-// stalls on its next shared-memory access until they have been taken by the
-// tensor core, which leaves a gap in the pipe, so there are two such points
-// per step rather than one per operand.
+// two MMA groups.  A thread with MMAs in flight stalls on its next
+// shared-memory access (such as a barrier wait, ~100 cycles each even on a
+// completed phase) until they have been taken by the tensor core, which leaves
+// a gap in the pipe, so the issuer waits once per burst: for PFull(i) before
+// dV(i) S^T(i+1) and for DSFull(i) before dK(i) dP^T(i+1).  The softmax warps
+// wait for the ring tiles in its place before arriving: at the end of step
+// i's dS phase for dO tile i+1 and Q tile i+2 (off the P phase, on which the
+// tensor core waits), so each arrival vouches for every tile the bursts after
+// it read.
 // Q tiles stream through a 3-slot ring released after dK (their last reader),
 // dO tiles through a 2-slot ring released after dV; each step's delta rides in
 // its Q slot (read in the dS phase, before dK) and its LSE in its dO slot (read
@@ -336,7 +340,10 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
           }
           mma_commit(bar + kKBarDPFull);
         };
-        bool ok = mbar_wait_bounded(bar + kKBarIn, 0, abort_flag, gst) && q_ready(0) && o_ready(0);
+        // Q tile 1 as well: the burst dV(0) S^T(1) follows the P phase of step 0,
+        // and later Q tiles are vouched for by the softmax's arrivals.
+        bool ok = mbar_wait_bounded(bar + kKBarIn, 0, abort_flag, gst) && q_ready(0) && o_ready(0) &&
+                  (n_iter < 2 || q_ready(1));
         if (ok && n_iter > 0) {
           tc_fence_after_sync();
           issue_s(0);
@@ -347,9 +354,7 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
           // burst 1: dV(i), S^T(i+1).  P^T / dS^T: queries 16kk..16kk+15 are
           // columns 8kk.. of warpgroup 0's half (kk < 4) or of warpgroup 1's
           // half at +64 (kk >= 4).
-          if (!(ok = mbar_wait_bounded(bar + kKBarPFull, i & 1, abort_flag, gst) &&
-                     (i + 1 == n_iter || q_ready(i + 1))))
-            break;
+          if (!(ok = mbar_wait_bounded(bar + kKBarPFull, i & 1, abort_flag, gst))) break;
           tc_fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
@@ -360,9 +365,7 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
           mma_commit(bar + kKBarOEmpty + 8 * os);
           if (i + 1 < n_iter) issue_s(i + 1);
           // burst 2: dK(i), dP^T(i+1)
-          if (!(ok = mbar_wait_bounded(bar + kKBarDSFull, i & 1, abort_flag, gst) &&
-                     (i + 1 == n_iter || o_ready(i + 1))))
-            break;
+          if (!(ok = mbar_wait_bounded(bar + kKBarDSFull, i & 1, abort_flag, gst))) break;
           tc_fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
@@ -393,8 +396,9 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
       uint32_t sr[2][32];
       tmem_ld32(tmem + lane_base + g * 64, sr[0]);
       tmem_ld32(tmem + lane_base + g * 64 + 32, sr[1]);
-      // This step's LSE rides in its dO slot (landed before dP^T(i) ran).
-      if (!warp_wait(bar + kKBarOFull + 8 * os, (i / kOSlots) & 1, abort_flag, gst)) { ok = false; break; }
+      // This step's LSE rides in its dO slot; after step 0 these threads
+      // waited for that slot at the end of the previous step.
+      if (i == 0 && !warp_wait(bar + kKBarOFull, 0, abort_flag, gst)) { ok = false; break; }
       tmem_wait_ld();
       reg_fence(sr[0]);
       reg_fence(sr[1]);
@@ -417,8 +421,9 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
       mbar_arrive(bar + kKBarPFull);
 
       if (!warp_wait(bar + kKBarDPFull, i & 1, abort_flag, gst)) { ok = false; break; }
-      // ... and its delta in its Q slot (landed before S^T(i) ran).
-      if (!warp_wait(bar + kKBarQFull + 8 * qs, (i / kQSlots) & 1, abort_flag, gst)) { ok = false; break; }
+      // ... and its delta in its Q slot, which these threads waited for at the
+      // end of step i-2 (steps 0 and 1: here).
+      if (i < 2 && !warp_wait(bar + kKBarQFull + 8 * qs, 0, abort_flag, gst)) { ok = false; break; }
       tc_fence_after_sync();
       uint32_t dr[2][32];
       tmem_ld32(tmem + lane_base + 128 + g * 64, dr[0]);
@@ -431,6 +436,21 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
       tmem_st16(tmem + lane_base + 128 + g * 64 + 16, w[1]);
       tmem_wait_st();
       tc_fence_before_sync();
+      // The issuer waits for this arrival alone before dK(i) dP^T(i+1) and
+      // (as the last wait before it) dV(i+1) S^T(i+2), so it also vouches for
+      // dO tile i+1 and Q tile i+2 having landed.  Waiting here, a step ahead
+      // of S^T(i+2), keeps these waits off the softmax's P phase, which the
+      // tensor core waits for.
+      if (i + 1 < n_iter &&
+          !warp_wait(bar + kKBarOFull + 8 * ((i + 1) % kOSlots), ((i + 1) / kOSlots) & 1, abort_flag, gst)) {
+        ok = false;
+        break;
+      }
+      if (i + 2 < n_iter &&
+          !warp_wait(bar + kKBarQFull + 8 * ((i + 2) % kQSlots), ((i + 2) / kQSlots) & 1, abort_flag, gst)) {
+        ok = false;
+        break;
+      }
       mbar_arrive(bar + kKBarDSFull);
     }
     // ------------------------------------------------------------ epilogue
@@ -702,8 +722,9 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
           mma_commit(bar + kQBarDPFull);
           mma_commit(bar + kQBarVEmpty + 8 * vs);
         };
-        // Every wait of a burst is taken before any of its MMAs is issued (a
-        // thread with MMAs in flight stalls on its next shared-memory access).
+        // One wait per burst (a thread with MMAs in flight stalls on its next
+        // shared-memory access): the softmax's SFree and DSFull arrivals also
+        // vouch for K tile i+1 and V tile i+1.
         bool ok = mbar_wait_bounded(bar + kQBarQReady, 0, abort_flag, gst) && (n_kv == 0 || (k_ready(0) && v_ready(0)));
         if (ok && n_kv > 0) {
           tc_fence_after_sync();
@@ -713,15 +734,13 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         for (int i = 0; ok && i < n_kv; ++i) {
           // burst 1: S_{i+1}, once the softmax has loaded S_i
           if (i + 1 < n_kv) {
-            if (!(ok = mbar_wait_bounded(bar + kQBarSFree, i & 1, abort_flag, gst) && k_ready(i + 1))) break;
+            if (!(ok = mbar_wait_bounded(bar + kQBarSFree, i & 1, abort_flag, gst))) break;
             tc_fence_after_sync();
             issue_s(i + 1);
           }
           // burst 2: dQ += dS_i K_i, dP_{i+1}.  Keys 16kk.. of dS_i are columns
           // 8kk.. of warpgroup 0's half (kk < 4) or of warpgroup 1's half at +64.
-          if (!(ok = mbar_wait_bounded(bar + kQBarDSFull, i & 1, abort_flag, gst) &&
-                     (i + 1 == n_kv || v_ready(i + 1))))
-            break;
+          if (!(ok = mbar_wait_bounded(bar + kQBarDSFull, i & 1, abort_flag, gst))) break;
           tc_fence_after_sync();
           const int ks = i % kKSlots;
 #pragma unroll
@@ -782,6 +801,13 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       tmem_ld32(tmem + lane_base + g * 64 + 32, sr[1]);
       tmem_wait_ld();
       tc_fence_before_sync();
+      // The issuer waits for this arrival alone before S_{i+1}, so it also
+      // vouches for K tile i+1 having landed.
+      if (i + 1 < n_kv &&
+          !warp_wait(bar + kQBarKFull + 8 * ((i + 1) % kKSlots), ((i + 1) / kKSlots) & 1, abort_flag, gst)) {
+        ok = false;
+        break;
+      }
       mbar_arrive(bar + kQBarSFree);
       reg_fence(sr[0]);
       reg_fence(sr[1]);
@@ -809,6 +835,12 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       tmem_st16(tmem + lane_base + kColDP + g * 64 + 16, wd[1]);
       tmem_wait_st();
       tc_fence_before_sync();
+      // ... and this one alone before dQ(i) and dP_{i+1}: V tile i+1 too.
+      if (i + 1 < n_kv &&
+          !warp_wait(bar + kQBarVFull + 8 * ((i + 1) % kVSlots), ((i + 1) / kVSlots) & 1, abort_flag, gst)) {
+        ok = false;
+        break;
+      }
       mbar_arrive(bar + kQBarDSFull);
     }
     if (ok) ok = warp_wait(bar + kQBarAcc, 0, abort_flag, gst);

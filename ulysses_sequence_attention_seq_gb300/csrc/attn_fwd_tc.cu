@@ -25,13 +25,13 @@
 //               PV_X(j) has finished: the softmax can then rescale O_X
 //               without any further barrier.  S_X(j+1) overwrites P_X(j) only
 //               after PV_X(j) has read it (one issuer's MMAs run in order).
-//               The issuer takes every wait a burst PV_X(j) S_X(j+1) needs
-//               before issuing any of it: a thread with MMAs in flight stalls
-//               on its next shared-memory access (such as a barrier wait)
-//               until they have been taken by the tensor core, and each such
-//               stall leaves a gap in the pipe, so there are two waits per
-//               key tile (P_A(j) with entry j, then P_B(j)) rather than one
-//               per operand.
+//               A thread with MMAs in flight stalls on its next shared-memory
+//               access (such as a barrier wait, ~100 cycles even on a
+//               completed phase) until they have been taken by the tensor
+//               core, and each such stall leaves a gap in the pipe, so the
+//               issuer waits once per burst, for P_X(j) alone: the softmax
+//               warps whose burst opens key tile j wait for ring entry j
+//               before publishing P, so that arrival vouches for the entry.
 //   warps 0-3   softmax of tile A, warps 4-7 of tile B: thread i of a
 //               warpgroup owns query row i = TMEM lane i.  It reads its score
 //               row from TMEM, takes the row maximum (base-2 domain) on the
@@ -264,9 +264,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_bf16_ts(tmem + 2 * BN + x * D, tmem + x * BN + kk * 8, b, idPV, (t > 0 || kk > 0) ? 1u : 0u);
           }
         };
-        auto entry_ready = [&](int e) -> bool {
-          return mbar_wait_bounded(bar + kBarKVFull + 8 * ring_slot(e), ring_parity(e), abort_flag, gst);
-        };
         // Entry t is free once key tile t's two bursts have finished: its
         // commit follows tile B's burst.  (A commit at the head of a burst,
         // issued while the pipe is idle after the waits, was measured to delay
@@ -276,9 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && nA > 0) issue_s(0, 0);
         if (ok) issue_s(1, 0);
         for (int t = 0; ok && t < nB; ++t) {
-          // every wait of tile A's burst first: P_A(t) and entry t
+          // tile A's burst: P_A(t) (whose arrival vouches for entry t)
           if (t < nA) {
-            if (!(ok = mbar_wait_bounded(bar + kBarPFull, t & 1, abort_flag, gst) && entry_ready(t))) break;
+            if (!(ok = mbar_wait_bounded(bar + kBarPFull, t & 1, abort_flag, gst))) break;
             tc_fence_after_sync();
             issue_pv(0, t);
             if (t == nA - 1)
@@ -286,9 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
               issue_s(0, t + 1);
           }
-          // then tile B's: P_B(t) (and entry t if A skipped it)
-          if (!(ok = mbar_wait_bounded(bar + kBarPFull + 8, t & 1, abort_flag, gst) && (t < nA || entry_ready(t))))
-            break;
+          // then tile B's: P_B(t) (vouching for entry t if A skipped it)
+          if (!(ok = mbar_wait_bounded(bar + kBarPFull + 8, t & 1, abort_flag, gst))) break;
           tc_fence_after_sync();
           issue_pv(1, t);
           if (t == nB - 1)
@@ -313,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_base + x * BN;
     const uint32_t tO = tmem + lane_base + 2 * BN + x * D;
     const int n_mine = x ? nB : nA;
+    const int own_entry_from = x ? nA : 0;  // key tiles whose first burst is this tile's
     const int diag = p.causal ? 2 * qp + x : -1;  // the key tile holding this tile's diagonal
     const float sl2 = p.scale_log2;
     float m_used = -INFINITY, l = 0.f;  // running max (scaled, base 2) and row sum
@@ -417,6 +414,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       l += tsum;
       tmem_wait_st();
       tc_fence_before_sync();
+      // The issuer waits for this arrival alone before the burst PV_X(t)
+      // S_X(t+1); when that burst is key tile t's first (tile A's, or B's once
+      // A is done) the arrival also vouches for ring entry t having landed.
+      if (t >= own_entry_from &&
+          !warp_wait(bar + kBarKVFull + 8 * ring_slot(t), ring_parity(t), abort_flag, gst)) {
+        ok = false;
+        break;
+      }
       mbar_arrive(bar + kBarPFull + 8 * x);
     }
     // --------------------------------------------------------------- epilogue
