@@ -101,6 +101,7 @@ class Problem:
     use_rope: bool = True
     rope_base: float = 10000.0
     scale: Optional[float] = None
+    ring: int = 1  # > 1: the Ulysses x ring hybrid of oracle/ring.py (P = (P/ring) * ring)
 
     @property
     def Sl(self) -> int:
