@@ -239,7 +239,7 @@ def run_ulysses(args, w, rank, world):
     # ---- folded forward (pack + attention + unpack in one kernel) vs the three
     # calls, same shapes with RoPE off (the folded path needs pre-rotated q, k)
     folded = None
-    if w.dtype == "bf16" and w.Sl % 128 == 0:
+    if w.dtype == "bf16" and w.Sl % 128 == 0 and w.ring == 1:  # the folded mode has no hybrid form
         import dataclasses
         pf = dataclasses.replace(prob, use_rope=False)
 
@@ -303,7 +303,9 @@ class OracleBench:
     def __init__(self, w, nthreads=None):
         sys.path.insert(0, os.path.join(ROOT, "tests"))
         import oracle
+        from oracle import ring as oracle_ring
         self.oracle = oracle
+        self.ring = oracle_ring
         self.w = w
         self.nthreads = nthreads or (os.cpu_count() or 1)
         ins = make_inputs(w, with_grad=False)
@@ -311,7 +313,7 @@ class OracleBench:
         del ins
         self.op = oracle.Problem(B=w.B, S=w.S, n_head=w.n_head, n_kv_head=w.n_kv_head, D=w.head_dim,
                                  P=w.P, causal=w.causal, use_rope=w.use_rope,
-                                 rope_base=float(np.float32(w.rope_base)))
+                                 rope_base=float(np.float32(w.rope_base)), ring=w.ring)
         self.rng = np.random.default_rng(0)
 
     def step(self, n_rows):
@@ -320,14 +322,23 @@ class OracleBench:
         q, k, v = (o.shard_sequence(x[n], w.P) for n in ("q", "k", "v"))
         if w.use_rope:
             q, k = o.rope_seq(q, self.op.rope_base), o.rope_seq(k, self.op.rope_base)
-        qh, _, _ = o.a2a_seq_to_head(q, w.n_head)
-        kh, _, _ = o.a2a_seq_to_head(k, w.n_kv_head)
-        vh, _, _ = o.a2a_seq_to_head(v, w.n_kv_head)
-        t1 = time.perf_counter()
         rows = sorted(set(int(r) for r in self.rng.integers(0, w.S, n_rows)))
-        oh, _ = o.attention_fwd(self.op, qh, kh, vh, rows=rows, nthreads=self.nthreads)
-        t2 = time.perf_counter()
-        o.a2a_head_to_seq(oh, w.n_head)
+        if w.ring > 1:  # the Ulysses x ring hybrid: All-to-All per ring position, ring attention
+            rg = self.ring
+            qh, kh, vh = (rg.a2a_seq_to_head(t, hh, w.ring)[0]
+                          for t, hh in ((q, w.n_head), (k, w.n_kv_head), (v, w.n_kv_head)))
+            t1 = time.perf_counter()
+            oh, _ = rg.ring_attention_fwd(self.op, qh, kh, vh, rows=rows)
+            t2 = time.perf_counter()
+            rg.a2a_head_to_seq(oh, w.n_head, w.ring)
+        else:
+            qh, _, _ = o.a2a_seq_to_head(q, w.n_head)
+            kh, _, _ = o.a2a_seq_to_head(k, w.n_kv_head)
+            vh, _, _ = o.a2a_seq_to_head(v, w.n_kv_head)
+            t1 = time.perf_counter()
+            oh, _ = o.attention_fwd(self.op, qh, kh, vh, rows=rows, nthreads=self.nthreads)
+            t2 = time.perf_counter()
+            o.a2a_head_to_seq(oh, w.n_head)
         t3 = time.perf_counter()
         pairs = sum((r + 1) if w.causal else w.S for r in rows)
         full = w.S * (w.S + 1) / 2 if w.causal else float(w.S) * w.S
@@ -345,7 +356,8 @@ class OracleBench:
 
     def describe(self, n_rows):
         w = self.w
-        return (f"{w.name} (P={w.P}, S={w.S}, {w.n_head} heads, D={w.head_dim}): split, RoPE and the 4 loop "
+        ring = f", {w.ring} ring positions" if w.ring > 1 else ""
+        return (f"{w.name} (P={w.P}{ring}, S={w.S}, {w.n_head} heads, D={w.head_dim}): split, RoPE and the 4 loop "
                 f"all-to-alls in full; attention for {n_rows} random query rows of all {w.n_head} heads, "
                 f"scaled to the full causal triangle by query-key pairs")
 
@@ -527,7 +539,7 @@ def main():
         line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": w.name, "P": w.P, "B": w.B, "S": w.S, "n_head": w.n_head,
+                "config": {"workload": w.name, "P": w.P, "ring": w.ring, "B": w.B, "S": w.S, "n_head": w.n_head,
                            "n_kv_head": w.n_kv_head, "head_dim": w.head_dim, "passes": "fwd"},
                 "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": ob.nthreads, "kind": "oracle",
                                  "sample": ob.describe(n_rows)},
@@ -573,7 +585,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic (seeded normal inputs of the workload's shape)",
-        "config": {"workload": w.name, "P": w.P, "B": w.B, "S": w.S, "n_head": w.n_head,
+        "config": {"workload": w.name, "P": w.P, "ring": w.ring, "B": w.B, "S": w.S, "n_head": w.n_head,
                    "n_kv_head": w.n_kv_head, "head_dim": w.head_dim, "causal": w.causal, "rope": w.use_rope,
                    "passes": "fwd+bwd" if r["backward"] else "fwd",
                    "l2": "inputs larger than L2 (Q/K/V/O each >= 128 MiB); no flush",

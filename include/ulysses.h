@@ -54,8 +54,9 @@ enum ulysses_dtype { ULYSSES_BF16 = 0, ULYSSES_FP32 = 1 };
 enum ulysses_status_code {
   ULYSSES_OK = 0,
   ULYSSES_ERR_ARG = -1,          /* NULL pointer, or a size <= 0 */
-  ULYSSES_ERR_DIVISIBILITY = -2, /* S%P, n_head%P, n_kv_head%P or n_head%n_kv_head != 0:
-                                    the head-count bound of plain Ulysses */
+  ULYSSES_ERR_DIVISIBILITY = -2, /* S%P, n_head%Pu, n_head%n_kv_head or P%ring != 0, or
+                                    neither of n_kv_head, Pu divides the other (Pu = P/ring):
+                                    the head-count bound of Ulysses */
   ULYSSES_ERR_HIDDEN = -3,       /* hidden != n_head * head_dim */
   ULYSSES_ERR_UNSUPPORTED = -4,  /* head_dim / dtype / pass with no kernel */
   ULYSSES_ERR_ALIGN = -5,        /* a pointer is not 16-byte aligned */
@@ -81,6 +82,22 @@ enum ulysses_device_status {
  * n_kv_head, head_dim and the sequence-parallel group size P; plus the causal
  * flag, the element type, RoPE on/off with its base, and the softmax scale
  * (0 selects 1/sqrt(head_dim)).
+ *
+ * `ring` (0 or 1: plain Ulysses) selects the Ulysses x ring hybrid that
+ * "Sequence Parallelism II: DeepSpeed Ulysses and All-to-All Attention" points
+ * to when P exceeds what the heads allow (§4: a head-sharded group cannot have
+ * more ranks than heads; §8: Ring Attention keeps query blocks and circulates
+ * key/value blocks).  The P ranks form `ring` ring positions of Pu = P/ring
+ * ranks: rank p = r*Pu + u still owns tokens [p*S/P, (p+1)*S/P) in sequence
+ * layout, and the All-to-All runs inside each ring position, so in head layout
+ * rank (r, u) holds chunk r (tokens [r*Cs, (r+1)*Cs), Cs = S/ring) of heads
+ * [u*hp, (u+1)*hp), hp = n_head/Pu (kv-heads likewise).  Attention for those
+ * query rows runs over the key/value chunks of every ring position (the
+ * ring's circulation), so O, dQ, dK, dV are those of plain attention.  Head
+ * layouts below then read [P][B][Cs][...] instead of [P][B][S][...], the LSE
+ * [P][B][hp][Cs].  ring > 1 needs bf16, head_dim 64 or 128, Cs a multiple of
+ * 128 and Pu dividing n_kv_head (ULYSSES_ERR_UNSUPPORTED otherwise); the
+ * folded forward and the two projections take ring <= 1 only.
  */
 typedef struct ulysses_problem {
   int B, S, hidden, n_head, n_kv_head, head_dim, P;
@@ -89,6 +106,7 @@ typedef struct ulysses_problem {
   int use_rope; /* 1: rotate q and k by their global position inside the pack */
   float rope_base;
   float softmax_scale;
+  int ring;     /* ring positions of the Ulysses x ring hybrid; 0 or 1: plain Ulysses */
 } ulysses_problem;
 
 /* Checks the problem statement alone.  Returns ULYSSES_OK or the first failing

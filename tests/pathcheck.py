@@ -29,7 +29,8 @@ LSE_BF16_MAX_ABS = 5e-2
 
 def oracle_problem(w: Workload) -> oracle.Problem:
     return oracle.Problem(B=w.B, S=w.S, n_head=w.n_head, n_kv_head=w.n_kv_head, D=w.head_dim, P=w.P,
-                          causal=w.causal, use_rope=w.use_rope, rope_base=float(np.float32(w.rope_base)))
+                          causal=w.causal, use_rope=w.use_rope, rope_base=float(np.float32(w.rope_base)),
+                          ring=w.ring)
 
 
 def to64(t: torch.Tensor) -> np.ndarray:

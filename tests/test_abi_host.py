@@ -55,6 +55,16 @@ def prob(**kw):
     (dict(hidden=1024), -3),
     (dict(head_dim=96, hidden=32 * 96), -4), (dict(dtype=7), -4),
     (dict(dtype=U.FP32, head_dim=32, hidden=1024), 0),
+    # Ulysses x ring hybrid: the head-count bound applies to the Pu = P/ring ranks of a ring position
+    (dict(P=64, S=4096 * 64, n_kv_head=32, ring=2), 0),  # P = 64 > 32 heads: 2 ring positions of 32
+    (dict(P=256, S=32768, n_kv_head=32, ring=8), 0),     # the pages' 32 heads over 256 ranks
+    (dict(ring=8), 0),                         # pure ring: one rank per position
+    (dict(P=64, S=4096 * 64, ring=3), -2),     # P % ring
+    (dict(ring=-1), -1),
+    (dict(ring=2, dtype=U.FP32), -4),          # the hybrid runs on the bf16 tensor-core kernels only
+    (dict(ring=2, head_dim=32, hidden=32 * 32), -4),
+    (dict(S=8 * 96, ring=4), -4),              # chunk S/ring = 192 is not a multiple of 128
+    (dict(ring=2, n_kv_head=2), -4),           # kv-head replication inside a ring position
 ])
 def test_validate_codes(lib, kw, code):
     assert U.ulysses_validate(prob(**kw)) == code
@@ -71,6 +81,21 @@ def test_workspace_sizes(lib):
     pr = prob(n_kv_head=2)
     assert U.ulysses_workspace_bytes(pr, 1) >= b + 2 * pr.P * pr.B * pr.S * pr.head_dim * 4
     assert U.ulysses_workspace_bytes(prob(B=0), 0) == 0
+    # the hybrid regroups the same rows: the same workspace
+    assert U.ulysses_workspace_bytes(prob(ring=2), 1) == b
+
+
+def test_ring_is_refused_where_no_kernel_takes_it(lib):
+    """The folded forward and the two projections have no hybrid mode; they
+    refuse ring > 1 on the host (fake pointers, never dereferenced)."""
+    vp = ctypes.c_void_p
+    p = prob(ring=2)
+    nws = U.ulysses_workspace_bytes(p, 0)
+    a = [vp((1 << 40) + i * (1 << 34)) for i in range(8)]
+    assert lib.ulysses_attn_fwd_folded(ctypes.byref(p.c()), a[0], a[1], a[2], a[3], a[4], a[5], nws, vp(0)) == -4
+    assert lib.ulysses_qkv_proj_pack(ctypes.byref(p.c()), a[0], a[1], None, a[2], a[3], a[4], a[5], nws,
+                                     vp(0)) == -4
+    assert lib.ulysses_out_proj_unpack(ctypes.byref(p.c()), a[0], a[1], None, a[2], a[5], nws, vp(0)) == -4
 
 
 def test_status_strings(lib):

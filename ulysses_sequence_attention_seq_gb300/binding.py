@@ -39,7 +39,7 @@ class CProblem(ctypes.Structure):
                 ("n_head", ctypes.c_int), ("n_kv_head", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("P", ctypes.c_int), ("causal", ctypes.c_int), ("dtype", ctypes.c_int),
                 ("use_rope", ctypes.c_int), ("rope_base", ctypes.c_float),
-                ("softmax_scale", ctypes.c_float)]
+                ("softmax_scale", ctypes.c_float), ("ring", ctypes.c_int)]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -57,18 +57,19 @@ class Problem:
     use_rope: bool = True
     rope_base: float = 10000.0
     softmax_scale: float = 0.0
+    ring: int = 1  # ring positions of the Ulysses x ring hybrid (1: plain Ulysses)
 
     @classmethod
     def from_workload(cls, w) -> "Problem":
         return cls(B=w.B, S=w.S, hidden=w.hidden, n_head=w.n_head, n_kv_head=w.n_kv_head,
                    head_dim=w.head_dim, P=w.P, causal=w.causal,
                    dtype=BF16 if w.dtype == "bf16" else FP32, use_rope=w.use_rope,
-                   rope_base=w.rope_base)
+                   rope_base=w.rope_base, ring=getattr(w, "ring", 1))
 
     def c(self) -> CProblem:
         return CProblem(self.B, self.S, self.hidden, self.n_head, self.n_kv_head, self.head_dim,
                         self.P, int(self.causal), self.dtype, int(self.use_rope),
-                        float(self.rope_base), float(self.softmax_scale))
+                        float(self.rope_base), float(self.softmax_scale), int(self.ring))
 
     @property
     def torch_dtype(self):
@@ -79,14 +80,24 @@ class Problem:
         return self.S // self.P
 
     @property
+    def Pu(self):
+        """Ranks of one ring position (the All-to-All group): P / ring."""
+        return self.P // max(self.ring, 1)
+
+    @property
+    def Cs(self):
+        """Tokens a head-layout buffer holds: S / ring (S for plain Ulysses)."""
+        return self.S // max(self.ring, 1)
+
+    @property
     def hp(self):
-        return self.n_head // self.P
+        return self.n_head // self.Pu
 
     @property
     def kvp(self):
-        """kv-heads a rank holds in head layout: n_kv_head / P, or one when
-        n_kv_head < P (each kv-head then replicated to P / n_kv_head ranks)."""
-        return self.n_kv_head // self.P if self.n_kv_head >= self.P else 1
+        """kv-heads a rank holds in head layout: n_kv_head / Pu, or one when
+        n_kv_head < Pu (each kv-head then replicated to Pu / n_kv_head ranks)."""
+        return self.n_kv_head // self.Pu if self.n_kv_head >= self.Pu else 1
 
     def scale(self) -> float:
         return self.softmax_scale if self.softmax_scale > 0 else 1.0 / math.sqrt(self.head_dim)
@@ -266,11 +277,11 @@ class Buffers:
         self.q_seq = e(p.P, p.B, p.Sl, p.n_head, D)
         self.k_seq = e(p.P, p.B, p.Sl, p.n_kv_head, D)
         self.v_seq = e(p.P, p.B, p.Sl, p.n_kv_head, D)
-        self.q_head = e(p.P, p.B, p.S, p.hp, D)
-        self.k_head = e(p.P, p.B, p.S, p.kvp, D)
-        self.v_head = e(p.P, p.B, p.S, p.kvp, D)
-        self.o_head = e(p.P, p.B, p.S, p.hp, D)
-        self.lse = e(p.P, p.B, p.hp, p.S, d=torch.float32)
+        self.q_head = e(p.P, p.B, p.Cs, p.hp, D)
+        self.k_head = e(p.P, p.B, p.Cs, p.kvp, D)
+        self.v_head = e(p.P, p.B, p.Cs, p.kvp, D)
+        self.o_head = e(p.P, p.B, p.Cs, p.hp, D)
+        self.lse = e(p.P, p.B, p.hp, p.Cs, d=torch.float32)
         self.o_seq = e(p.P, p.B, p.Sl, p.n_head * D)
         if backward:
             self.do_seq = e(p.P, p.B, p.Sl, p.n_head * D)

@@ -59,7 +59,18 @@ struct BwdParams {
                                        // per-rank partials [P*B][S][D] (unscaled, not rotated)
   uint32_t *status;                    // status word; the RoPE table key follows it
   uint32_t rope_key;
+  // Ulysses x ring hybrid: Pu ranks per ring position, Cs tokens per chunk
+  // (plain Ulysses: P, S).  A CTA works on one (group member, batch, head)
+  // over the full sequence; the rows at global position pos live in the
+  // head-layout buffer of rank (pos / Cs) * Pu + member, row pos % Cs.
+  int Pu, Cs;
 };
+
+// Head-layout (rank * B + batch) of the rows at global position `pos` for the
+// CTA of member*B + batch = `rb`.
+__device__ __forceinline__ int hl_outer(const BwdParams &p, int rb, int pos) {
+  return (pos / p.Cs) * p.Pu * p.B + rb;
+}
 
 // True (and the status bit set) when the workspace's RoPE table was built for
 // another problem: the kernel then writes nothing.
@@ -227,7 +238,7 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
   }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int heads_total = p.P * p.B * p.kvp;
+  const int heads_total = p.Pu * p.B * p.kvp;
   const int n_kt_all = (p.S + 127) / 128;
   const dev::HeadTile ht = dev::grouped_order((int)blockIdx.x, heads_total, n_kt_all, p.group_kv);
   const int n = ht.rank;  // key tile; low tiles have the most work
@@ -275,24 +286,25 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
         tma_prefetch_desc(&tmQ);
         mbar_arrive_expect_tx(bar + kKBarIn, 2 * L::kT);
         for (int c = 0; c < kCh; ++c) {
-          tma_load_4d(sK + c * 16384, &tmK, bar + kKBarIn, c * 64, kl, n * 128, rb);
-          tma_load_4d(sV + c * 16384, &tmV, bar + kKBarIn, c * 64, kl, n * 128, rb);
+          tma_load_4d(sK + c * 16384, &tmK, bar + kKBarIn, c * 64, kl, n * 128 % p.Cs, hl_outer(p, rb, n * 128));
+          tma_load_4d(sV + c * 16384, &tmV, bar + kKBarIn, c * 64, kl, n * 128 % p.Cs, hl_outer(p, rb, n * 128));
         }
         int issued_q = -1, issued_o = -1;
         for (int i = 0; i < n_iter; ++i) {
           const int qs = i % kQSlots, os = i % kOSlots;
           const int gi = i / n_m, m = m0 + i % n_m, j = kl * p.group + gi;
+          const int mrow = m * 128 % p.Cs, mo = hl_outer(p, rb, m * 128);
           if (!mbar_wait_bounded(bar + kKBarQEmpty + 8 * qs, ((i / kQSlots) & 1) ^ 1, abort_flag, gst)) break;
           mbar_arrive_expect_tx(bar + kKBarQFull + 8 * qs, L::kT + 512);
           for (int c = 0; c < kCh; ++c)
-            tma_load_4d(sQ + qs * L::kT + c * 16384, &tmQ, bar + kKBarQFull + 8 * qs, c * 64, j, m * 128, rb);
-          dev::tma_load_2d(sDl + qs * 512, &tmDl, bar + kKBarQFull + 8 * qs, m * 128, rb * p.hp + j);
+            tma_load_4d(sQ + qs * L::kT + c * 16384, &tmQ, bar + kKBarQFull + 8 * qs, c * 64, j, mrow, mo);
+          dev::tma_load_2d(sDl + qs * 512, &tmDl, bar + kKBarQFull + 8 * qs, mrow, mo * p.hp + j);
           issued_q = i;
           if (!mbar_wait_bounded(bar + kKBarOEmpty + 8 * os, ((i / kOSlots) & 1) ^ 1, abort_flag, gst)) break;
           mbar_arrive_expect_tx(bar + kKBarOFull + 8 * os, L::kT + 512);
           for (int c = 0; c < kCh; ++c)
-            tma_load_4d(sdO + os * L::kT + c * 16384, &tmdO, bar + kKBarOFull + 8 * os, c * 64, j, m * 128, rb);
-          dev::tma_load_2d(sL + os * 512, &tmL, bar + kKBarOFull + 8 * os, m * 128, rb * p.hp + j);
+            tma_load_4d(sdO + os * L::kT + c * 16384, &tmdO, bar + kKBarOFull + 8 * os, c * 64, j, mrow, mo);
+          dev::tma_load_2d(sL + os * 512, &tmL, bar + kKBarOFull + 8 * os, mrow, mo * p.hp + j);
           issued_o = i;
         }
         if (*abort_flag) {
@@ -616,7 +628,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   if ((*gst & 3u) || stale_rope_table(p)) return;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int heads_total = p.P * p.B * p.hp;
+  const int heads_total = p.Pu * p.B * p.hp;
   const int n_qt = (p.S + 127) / 128;
   const dev::HeadTile ht = dev::grouped_order((int)blockIdx.x, heads_total, n_qt, p.group_q);
   const int m = n_qt - 1 - ht.rank;  // longest tiles first
@@ -668,12 +680,14 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
           if (!mbar_wait_bounded(bar + kQBarKEmpty + 8 * ks, ((i / kKSlots) & 1) ^ 1, abort_flag, gst)) break;
           mbar_arrive_expect_tx(bar + kQBarKFull + 8 * ks, L::kT);
           for (int c = 0; c < kCh; ++c)
-            tma_load_4d(sK + ks * L::kT + c * 16384, &tmK, bar + kQBarKFull + 8 * ks, c * 64, kl, i * 128, rb);
+            tma_load_4d(sK + ks * L::kT + c * 16384, &tmK, bar + kQBarKFull + 8 * ks, c * 64, kl, i * 128 % p.Cs,
+                        hl_outer(p, rb, i * 128));
           issued_k = i;
           if (!mbar_wait_bounded(bar + kQBarVEmpty + 8 * vs, ((i / kVSlots) & 1) ^ 1, abort_flag, gst)) break;
           mbar_arrive_expect_tx(bar + kQBarVFull + 8 * vs, L::kT);
           for (int c = 0; c < kCh; ++c)
-            tma_load_4d(sV + vs * L::kT + c * 16384, &tmV, bar + kQBarVFull + 8 * vs, c * 64, kl, i * 128, rb);
+            tma_load_4d(sV + vs * L::kT + c * 16384, &tmV, bar + kQBarVFull + 8 * vs, c * 64, kl, i * 128 % p.Cs,
+                        hl_outer(p, rb, i * 128));
           issued_v = i;
         }
         if (*abort_flag) {
@@ -770,7 +784,9 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
     {
       // Warpgroup 0 copies this thread's Q row, warpgroup 1 its dO row, into
       // TMEM (rows past S are zero).
-      const __nv_bfloat16 *src = (g == 0 ? p.q : p.dout) + (((size_t)rb * p.S + (live ? qi : 0)) * p.hp + j) * D;
+      const int qr = live ? qi : 0;
+      const __nv_bfloat16 *src =
+          (g == 0 ? p.q : p.dout) + (((size_t)hl_outer(p, rb, qr) * p.Cs + qr % p.Cs) * p.hp + j) * D;
       const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
@@ -789,7 +805,8 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       tc_fence_before_sync();
       mbar_arrive(bar + kQBarQReady);
     }
-    const size_t lrow = ((size_t)rb * p.hp + j) * p.S + (live ? qi : 0);
+    const int qr = live ? qi : 0;
+    const size_t lrow = ((size_t)hl_outer(p, rb, qr) * p.hp + j) * p.Cs + qr % p.Cs;
     const float nl2 = live ? p.nlse[lrow] : 0.f;
     const float dlt = live ? p.delta[lrow] : 0.f;
     bool ok = true;
@@ -879,14 +896,16 @@ template <int D>
 cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void *q, const void *k,
                      const void *v, const void *do_head, const float *nlse, const float *delta,
                      const void *ws, void *dq, void *dk, void *dv, uint32_t *status, int parts, cudaStream_t st) {
-  const int hp = p.n_head / p.P, kvp = kv_per_rank(p), PB = p.P * p.B;
+  const int Pu = group_ranks(p), Cs = chunk_len(p);
+  const int hp = p.n_head / Pu, kvp = kv_per_rank(p), PB = p.P * p.B;
+  // head-layout maps: [P*B][Cs][heads][D] and rows [P*B*hp][Cs]
   CUtensorMap mK128, mV128, mL, mDl, mQ128, mdO128;
-  bool ok = make_act_map(enc, &mK128, k, D, kvp, p.S, PB, 128) &&
-            make_act_map(enc, &mV128, v, D, kvp, p.S, PB, 128) &&
-            make_row_map(enc, &mL, nlse, p.S, PB * hp, 128) &&
-            make_row_map(enc, &mDl, delta, p.S, PB * hp, 128) &&
-            make_act_map(enc, &mQ128, q, D, hp, p.S, PB, 128) &&
-            make_act_map(enc, &mdO128, do_head, D, hp, p.S, PB, 128);
+  bool ok = make_act_map(enc, &mK128, k, D, kvp, Cs, PB, 128) &&
+            make_act_map(enc, &mV128, v, D, kvp, Cs, PB, 128) &&
+            make_row_map(enc, &mL, nlse, Cs, PB * hp, 128) &&
+            make_row_map(enc, &mDl, delta, Cs, PB * hp, 128) &&
+            make_act_map(enc, &mQ128, q, D, hp, Cs, PB, 128) &&
+            make_act_map(enc, &mdO128, do_head, D, hp, Cs, PB, 128);
   if (!ok) return cudaErrorInvalidValue;
   BwdParams bp;
   bp.B = p.B;
@@ -899,11 +918,15 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   bp.causal = p.causal;
   bp.n_head = p.n_head;
   bp.n_kv = p.n_kv_head;
+  bp.Pu = Pu;
+  bp.Cs = Cs;
+  // CTA units: (group member, batch, head), each over the full sequence.
+  const int UB = Pu * p.B;
   // dK/dV CTAs of a kv-head stream the Q and dO of its q-heads; dQ CTAs of a
   // q-head stream its kv-head's K and V (shared by the group's q-heads).
   const long long n_t = (p.S + 127) / 128;
-  bp.group_kv = l2_head_group((size_t)4 * p.S * D * bp.group, PB * kvp, n_t * PB * kvp);
-  bp.group_q = l2_head_group((size_t)4 * p.S * D / bp.group, PB * hp, n_t * PB * hp);
+  bp.group_kv = l2_head_group((size_t)4 * p.S * D * bp.group, UB * kvp, n_t * UB * kvp);
+  bp.group_q = l2_head_group((size_t)4 * p.S * D / bp.group, UB * hp, n_t * UB * hp);
   bp.scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)D);
   bp.scale_log2 = bp.scale * kLog2e;
   bp.nlse = nlse;
@@ -924,8 +947,8 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   bp.status = status;
   bp.rope_key = rope_key(p);
 
-  const long long kv_blocks = (long long)((p.S + 127) / 128) * PB * kvp;
-  const long long q_blocks = (long long)((p.S + 127) / 128) * PB * hp;
+  const long long kv_blocks = n_t * UB * kvp;
+  const long long q_blocks = n_t * UB * hp;
   if (kv_blocks > 0x7fffffffll || q_blocks > 0x7fffffffll) return cudaErrorInvalidValue;
   cudaError_t e = cudaSuccess;
   if (parts & kBwdDkDv) {

@@ -111,6 +111,11 @@ struct FwdParams {
   int folded, Sl, n_head, n_kv_head;
   int head_group;  // heads per CTA group (grouped_order)
   int kv_rep;      // > 1: replicated kv-heads, rank r reads kv-head r / kv_rep
+  // Ulysses x ring hybrid: Pu ranks per ring position, Cs tokens per chunk;
+  // the 128-row tile at global position pos of group member u lives in the
+  // head-layout buffer of rank (pos / Cs) * Pu + u, row pos % Cs.  Plain
+  // Ulysses: Pu = P, Cs = S.
+  int Pu, Cs;
   float scale_log2;
   __nv_bfloat16 *o;  // [P][B][S][hp][D], or [P][B][Sl][H] when folded
   float *lse;        // [P][B][hp][S]
@@ -118,15 +123,21 @@ struct FwdParams {
 };
 
 // TMA coordinates (head, row, rank*B+batch) of the 128-row tile starting at
-// global position `pos` of local head `lh` on rank `r` (rb = r*B + b).
+// global position `pos` of local head `lh` of group member `r`, batch `b`
+// (with plain Ulysses the member is the rank).
 struct TileCoord {
   int head, row, outer;
 };
 // `rep` > 1: a replicated kv-head (rank r reads global kv-head r / rep).
-__device__ __forceinline__ TileCoord tile_coord(const FwdParams &p, int rb, int lh, int heads_local,
+__device__ __forceinline__ TileCoord tile_coord(const FwdParams &p, int r, int b, int lh, int heads_local,
                                                 int pos, int rep = 1) {
-  if (!p.folded) return {lh, pos, rb};
-  const int r = rb / p.B, b = rb - r * p.B, src = pos / p.Sl;
+  if (!p.folded) {
+    // ring position holding the tile (0 without a ring); a tile starting past
+    // the sequence end stays on the last one, its rows out of range (zeros)
+    const int c = (pos < p.S ? pos : p.S - 1) / p.Cs;
+    return {lh, pos - c * p.Cs, (c * p.Pu + r) * p.B + b};
+  }
+  const int src = pos / p.Sl;
   return {rep > 1 ? r / rep : r * heads_local + lh, pos - src * p.Sl, src * p.B + b};
 }
 
@@ -155,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (*gst & (ULYSSES_STATUS_FWD_TIMEOUT | ULYSSES_STATUS_BWD_TIMEOUT)) return;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int heads_total = p.P * p.B * p.hp;
+  const int heads_total = p.Pu * p.B * p.hp;
   const dev::HeadTile ht = dev::grouped_order((int)blockIdx.x, heads_total, p.n_pairs, p.head_group);
   const int qp = p.n_pairs - 1 - ht.rank;  // longest pairs first
   const int hid = ht.head;
@@ -199,32 +210,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        const int member = rb / p.B, bb = rb - member * p.B;
         // Q_A, Q_B and K_0 on one barrier
         mbar_arrive_expect_tx(bar + kBarQFull, 3 * L::kTile);
         for (int x = 0; x < 2; ++x) {
-          const TileCoord tq = tile_coord(p, rb, j, p.hp, qp * 2 * BM + x * BM);
+          const TileCoord tq = tile_coord(p, member, bb, j, p.hp, qp * 2 * BM + x * BM);
           for (int c = 0; c < kChunks; ++c)
             tma_load_4d(sQ + x * L::kTile + c * kChunkBytes, &tmQ, bar + kBarQFull, c * 64, tq.head,
                         tq.row, tq.outer);
         }
-        const TileCoord t0 = tile_coord(p, rb, kl, p.kvp, 0, p.kv_rep);
+        const TileCoord t0 = tile_coord(p, member, bb, kl, p.kvp, 0, p.kv_rep);
         for (int c = 0; c < kChunks; ++c)
           tma_load_4d(sK0 + c * kChunkBytes, &tmK, bar + kBarQFull, c * 64, t0.head, t0.row, t0.outer);
         // entry e = V_e and (when tile B goes on) K_{e+1}: what key tile e's two bursts read
         int issued = -1;
+        TileCoord tv = t0;  // key tile e's coordinates (K_e's and V_e's)
         for (int e = 0; e < nB; ++e) {
           const uint32_t slot = ring_slot(e), full = bar + kBarKVFull + 8 * slot;
           if (!mbar_wait_bounded(bar + kBarKVEmpty + 8 * slot, ring_parity(e) ^ 1, abort_flag, gst)) break;
           const bool has_k = e + 1 < nB;
           mbar_arrive_expect_tx(full, (has_k ? 2u : 1u) * L::kTile);
           const uint32_t dst = sKV + slot * L::kEntry;
-          const TileCoord tv = tile_coord(p, rb, kl, p.kvp, e * BN, p.kv_rep);
           for (int c = 0; c < kChunks; ++c)
             tma_load_4d(dst + c * kChunkBytes, &tmV, full, c * 64, tv.head, tv.row, tv.outer);
           if (has_k) {
-            const TileCoord tk = tile_coord(p, rb, kl, p.kvp, (e + 1) * BN, p.kv_rep);
+            tv = tile_coord(p, member, bb, kl, p.kvp, (e + 1) * BN, p.kv_rep);
             for (int c = 0; c < kChunks; ++c)
-              tma_load_4d(dst + L::kTile + c * kChunkBytes, &tmK, full, c * 64, tk.head, tk.row, tk.outer);
+              tma_load_4d(dst + L::kTile + c * kChunkBytes, &tmK, full, c * 64, tv.head, tv.row, tv.outer);
           }
           issued = e;
         }
@@ -430,8 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const float inv = 1.0f / l;
       __nv_bfloat16 *orow;
-      if (!p.folded) {
-        orow = p.o + (((size_t)rb * p.S + qpos) * p.hp + j) * D;
+      if (!p.folded) {  // rank (qpos / Cs) * Pu + member, row qpos % Cs
+        orow = p.o + ((((size_t)(qpos / p.Cs) * p.Pu * p.B + rb) * p.Cs + qpos % p.Cs) * p.hp + j) * D;
       } else {  // token qpos of rank qpos/Sl, global head r*hp + j
         const int r = rb / p.B, b = rb - r * p.B, dst = qpos / p.Sl;
         orow = p.o + (((size_t)(dst * p.B + b) * p.Sl + (qpos - dst * p.Sl)) * p.n_head + r * p.hp + j) * D;
@@ -452,8 +464,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
         }
       }
-      if (qpos < p.S)
-        p.lse[((size_t)rb * p.hp + j) * p.S + qpos] = (m_used + log2f(l)) * 0.69314718055994530942f;
+      if (qpos < p.S) {
+        const size_t hr = (size_t)(qpos / p.Cs) * p.Pu * p.B + rb;  // head-layout rank * B + b
+        p.lse[(hr * p.hp + j) * p.Cs + qpos % p.Cs] = (m_used + log2f(l)) * 0.69314718055994530942f;
+      }
     }
   }
 
@@ -470,10 +484,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void *q, const void *k,
                      const void *v, void *o, float *lse, uint32_t *status, bool folded, cudaStream_t st) {
-  const int hp = p.n_head / p.P, kvp = kv_per_rank(p), PB = p.P * p.B, Sl = p.S / p.P;
+  const int Pu = group_ranks(p), Cs = chunk_len(p);
+  const int hp = p.n_head / Pu, kvp = kv_per_rank(p), PB = p.P * p.B, Sl = p.S / p.P;
   CUtensorMap mq, mk, mv;
   // head-sharded maps: [P*B][S][hp|kvp][D]; folded maps: [P*B][Sl][n_head|n_kv_head][D]
-  const int rows = folded ? Sl : p.S;
+  const int rows = folded ? Sl : Cs;
   if (!make_act_map(enc, &mq, q, D, folded ? p.n_head : hp, rows, PB, 128) ||
       !make_act_map(enc, &mk, k, D, folded ? p.n_kv_head : kvp, rows, PB, 128) ||
       !make_act_map(enc, &mv, v, D, folded ? p.n_kv_head : kvp, rows, PB, 128))
@@ -492,14 +507,17 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   fp.n_head = p.n_head;
   fp.n_kv_head = p.n_kv_head;
   fp.kv_rep = kv_replicas(p);
+  fp.Pu = Pu;
+  fp.Cs = Cs;
   const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)D);
   fp.scale_log2 = scale * 1.4426950408889634f;
   // a q-head's CTAs stream its kv-head's K and V; the group's q-heads share them
-  fp.head_group = l2_head_group((size_t)4 * p.S * D / fp.group, PB * hp, (long long)fp.n_pairs * PB * hp);
+  const int units = Pu * p.B * hp;  // (group member, batch, local head): one full-sequence head each
+  fp.head_group = l2_head_group((size_t)4 * p.S * D / fp.group, units, (long long)fp.n_pairs * units);
   fp.o = static_cast<__nv_bfloat16 *>(o);
   fp.lse = lse;
   fp.status = status;
-  const long long blocks = (long long)fp.n_pairs * PB * hp;
+  const long long blocks = (long long)fp.n_pairs * units;
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)Layout<D>::kAlloc);

@@ -31,12 +31,24 @@ uint32_t rope_key(const ulysses_problem &p);
 
 inline size_t elem_size(const ulysses_problem &p) { return p.dtype == ULYSSES_BF16 ? 2 : 4; }
 
+// The Ulysses x ring hybrid: `ring` ring positions of Pu ranks each.  The
+// All-to-All runs inside a ring position (over Pu ranks) and a head-layout
+// buffer holds the Cs = S / ring tokens of its ring position; ring = 1 is
+// plain Ulysses (Pu = P, Cs = S).
+inline int ring_of(const ulysses_problem &p) { return p.ring > 1 ? p.ring : 1; }
+inline int group_ranks(const ulysses_problem &p) { return p.P / ring_of(p); }  // Pu
+inline int chunk_len(const ulysses_problem &p) { return p.S / ring_of(p); }    // Cs
+
 // KV-head replication: with fewer kv-heads than ranks (P a multiple of
 // n_kv_head) the q-heads of rank r all read kv-head r / R, R = P / n_kv_head,
 // so the seq -> head All-to-All hands each kv-head to R ranks and every rank
-// holds one kv-head in head layout.
-inline int kv_replicas(const ulysses_problem &p) { return p.n_kv_head < p.P ? p.P / p.n_kv_head : 1; }
-inline int kv_per_rank(const ulysses_problem &p) { return p.n_kv_head >= p.P ? p.n_kv_head / p.P : 1; }
+// holds one kv-head in head layout.  (Ranks here: the Pu of a ring position.)
+inline int kv_replicas(const ulysses_problem &p) {
+  return p.n_kv_head < group_ranks(p) ? group_ranks(p) / p.n_kv_head : 1;
+}
+inline int kv_per_rank(const ulysses_problem &p) {
+  return p.n_kv_head >= group_ranks(p) ? p.n_kv_head / group_ranks(p) : 1;
+}
 
 // ---- permutation kernels (permute.cu) ----
 cudaError_t launch_rope_table(const ulysses_problem &p, void *ws, cudaStream_t st);

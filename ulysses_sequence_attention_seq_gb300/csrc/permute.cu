@@ -17,6 +17,11 @@
 // Megatron Sequence Parallelism", skeleton: rope before the transpose) is
 // fused: a thread owning chunk c of the first half also owns chunk c of the
 // second half, so each rotation pair (i, i + D/2) is in one thread.
+// In the Ulysses x ring hybrid ("Sequence Parallelism II", §4 and §8) the
+// same All-to-All runs inside each ring position: source rank s sends to the
+// Pu ranks (s / Pu)*Pu + d of its own ring position, which store the piece at
+// row (s % Pu)*Sl + t of their Cs = Pu*Sl-token chunk.  Pu = P, Cs = S is
+// plain Ulysses.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -41,6 +46,7 @@ struct PermParams {
   PermJob job[3];
   int njobs;
   int P, B, Sl, D;
+  int Pu, Cs;   // ranks of a ring position and its tokens (plain Ulysses: P, S)
   int to_head;  // 1: src is sequence-sharded (pack); 0: src is head-sharded (unpack)
   const float *rope_cos, *rope_sin;  // [S][D/2] each
   const uint32_t *rope_key_ptr;
@@ -106,7 +112,6 @@ struct Chunk<float> {
 template <typename T>
 __global__ void __launch_bounds__(kThreads) permute_kernel(const PermParams p) {
   constexpr int V = Chunk<T>::kVec;
-  const int S = p.P * p.Sl;
   const long long rows = (long long)p.P * p.B * p.Sl;
   bool any_rope = false;
 #pragma unroll
@@ -122,25 +127,27 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const PermParams p) {
     const int b = (int)(sb % p.B);
     const int s = (int)(sb / p.B);
     const int pos = s * p.Sl + t;  // global token position
+    const int rp = s / p.Pu;       // ring position of the source rank
+    const int crow = pos - rp * p.Cs;  // row of the token in that position's chunk
 #pragma unroll
     for (int q = 0; q < 3; ++q) {
       if (q >= p.njobs) break;
       const PermJob J = p.job[q];
-      const int hp = J.rep > 1 ? 1 : J.heads / p.P;
+      const int hp = J.rep > 1 ? 1 : J.heads / p.Pu;
       // A unit is chunk c of both halves of a head (2 x 16 bytes), rotated or
       // not: two loads in flight per thread either way.  With replicated heads
       // the units run over the P destination ranks (one head each), so a head
       // of the token row is read once per replica.
       const int cph = p.D / (2 * V);
       const int run = hp * cph;                           // units per destination piece
-      const int units = p.P * run;
+      const int units = p.Pu * run;
       const long long seq_row = row * (long long)J.heads * p.D;
       for (int u = threadIdx.x; u < units; u += kThreads) {
         const int d = u / run;  // the rank on the head side of this piece
         const int w = u - d * run;
         const int j = w / cph, c = w - j * cph;
         const long long head_off =
-            (((long long)(d * p.B + b) * S + pos) * hp + j) * p.D + (long long)c * V;
+            (((long long)((rp * p.Pu + d) * p.B + b) * p.Cs + crow) * hp + j) * p.D + (long long)c * V;
         const int seq_head = J.rep > 1 ? d / J.rep : d * hp + j;
         const long long seq_off = seq_row + (long long)seq_head * p.D + (long long)c * V;
         const long long src_off = p.to_head ? seq_off : head_off;
@@ -178,11 +185,10 @@ __global__ void __launch_bounds__(32) unpack_bulk_kernel(const PermParams p, uin
   const uint32_t bar0 = sbase + kBulkStages * row_bytes;  // one mbarrier per stage
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kBulkStages * row_bytes + 8 * kBulkStages);
   const int lane = threadIdx.x;
-  const int S = p.P * p.Sl;
   const long long rows = (long long)p.P * p.B * p.Sl;
   const PermJob J = p.job[0];
-  const int hp = J.heads / p.P;
-  const uint32_t piece = row_bytes / p.P;  // hp * D elements
+  const int hp = J.heads / p.Pu;
+  const uint32_t piece = row_bytes / p.Pu;  // hp * D elements
   const T *src = static_cast<const T *>(J.src);
   T *dst = static_cast<T *>(J.dst);
   if (lane == 0) {
@@ -196,13 +202,16 @@ __global__ void __launch_bounds__(32) unpack_bulk_kernel(const PermParams p, uin
     const long long row = blockIdx.x + k * gridDim.x;  // (d*B + b)*Sl + t of the output
     const int t = (int)(row % p.Sl);
     const long long db = row / p.Sl;
-    const int b = (int)(db % p.B), pos = (int)(db / p.B) * p.Sl + t;
+    const int d = (int)(db / p.B), b = (int)(db % p.B);
+    const int rp = d / p.Pu, crow = (d - rp * p.Pu) * p.Sl + t;  // ring position, row in its chunk
     const uint32_t slot = (uint32_t)(k % kBulkStages);
     const uint32_t stage = sbase + slot * row_bytes, bar = bar0 + 8 * slot;
     if (lane == 0) mbar_arrive_expect_tx(bar, row_bytes);
     __syncwarp();
-    for (int r = lane; r < p.P; r += 32)  // rank r holds heads [r*hp, (r+1)*hp) at position pos
-      bulk_load(stage + r * piece, src + (((long long)(r * p.B + b) * S + pos) * hp) * p.D, piece, bar);
+    // member r of the ring position holds heads [r*hp, (r+1)*hp) of the token
+    for (int r = lane; r < p.Pu; r += 32)
+      bulk_load(stage + r * piece, src + (((long long)((rp * p.Pu + r) * p.B + b) * p.Cs + crow) * hp) * p.D,
+                piece, bar);
   };
   long long issued = -1, failed = n_mine;
   for (long long k = 0; k < kBulkStages - 1 && k < n_mine; ++k) load_row(issued = k);
@@ -262,8 +271,8 @@ __global__ void __launch_bounds__(kThreads)
     pack_do_delta_kernel(const __nv_bfloat16 *__restrict__ dout, const __nv_bfloat16 *__restrict__ o,
                          const float *__restrict__ lse, __nv_bfloat16 *__restrict__ do_head,
                          float *__restrict__ delta, float *__restrict__ nlse, int P, int B,
-                         int Sl, int H, int D) {
-  const int S = P * Sl, hp = H / P;
+                         int Sl, int H, int D, int Pu, int Cs) {
+  const int hp = H / Pu;
   const int lanes = D / 8;  // 8 or 16: divides 32
   const long long groups = (long long)P * B * Sl * H;
   const int lane = threadIdx.x & 31;
@@ -277,7 +286,7 @@ __global__ void __launch_bounds__(kThreads)
     const bool live = gid < groups;
     float acc = 0.f;
     long long head_row = 0;
-    int d = 0, b = 0, j = 0, pos = 0;
+    int d = 0, b = 0, j = 0, pos = 0, crow = 0;
     if (live) {
       const int g = (int)(gid % H);
       const long long row = gid / H;
@@ -286,9 +295,11 @@ __global__ void __launch_bounds__(kThreads)
       b = (int)(sb % B);
       const int s = (int)(sb / B);
       pos = s * Sl + t;
-      d = g / hp;
-      j = g - d * hp;
-      head_row = (((long long)(d * B + b) * S + pos) * hp + j) * D;
+      const int rp = s / Pu;  // ring position; the token's row in its chunk:
+      crow = pos - rp * Cs;
+      d = rp * Pu + g / hp;   // the head-layout rank holding head g of the token
+      j = g % hp;
+      head_row = (((long long)(d * B + b) * Cs + crow) * hp + j) * D;
       const uint4 x = __ldg(reinterpret_cast<const uint4 *>(dout + gid * D + c * 8));
       const uint4 y = __ldg(reinterpret_cast<const uint4 *>(o + head_row + c * 8));
       *reinterpret_cast<uint4 *>(do_head + head_row + c * 8) = x;
@@ -303,7 +314,7 @@ __global__ void __launch_bounds__(kThreads)
     }
     for (int off = lanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (live && c == 0) {
-      const long long idx = ((long long)(d * B + b) * hp + j) * S + pos;
+      const long long idx = ((long long)(d * B + b) * hp + j) * Cs + crow;
       delta[idx] = acc;
       nlse[idx] = -lse[idx] * 1.4426950408889634f;
     }
@@ -341,6 +352,8 @@ cudaError_t launch_rope_table(const ulysses_problem &p, void *ws, cudaStream_t s
 static PermParams base_params(const ulysses_problem &p, const void *ws, int to_head) {
   PermParams pp{};
   pp.P = p.P;
+  pp.Pu = group_ranks(p);
+  pp.Cs = chunk_len(p);
   pp.B = p.B;
   pp.Sl = p.S / p.P;
   pp.D = p.head_dim;
@@ -421,7 +434,7 @@ cudaError_t launch_pack_do_delta(const ulysses_problem &p, const void *do_seq, c
   pack_do_delta_kernel<<<grid, kThreads, 0, st>>>(
       static_cast<const __nv_bfloat16 *>(do_seq), static_cast<const __nv_bfloat16 *>(o_head),
       lse, static_cast<__nv_bfloat16 *>(do_head), delta, nlse, p.P, p.B, p.S / p.P, p.n_head,
-      p.head_dim);
+      p.head_dim, group_ranks(p), chunk_len(p));
   return cudaGetLastError();
 }
 

@@ -30,7 +30,7 @@ WorkspaceLayout workspace_layout(const ulysses_problem &p) {
   L.nlse_bytes = L.delta_bytes;
   L.dohead = align256(L.nlse + L.nlse_bytes);
   L.dohead_bytes = (size_t)p.B * p.S * p.n_head * p.head_dim * es;
-  L.part_bytes = kv_replicas(p) > 1 ? (size_t)p.P * p.B * p.S * p.head_dim * 4 : 0;
+  L.part_bytes = kv_replicas(p) > 1 ? (size_t)p.P * p.B * chunk_len(p) * p.head_dim * 4 : 0;
   L.dkpart = align256(L.dohead + L.dohead_bytes);
   L.dvpart = align256(L.dkpart + L.part_bytes);
   L.total_bwd = align256(L.dvpart + L.part_bytes);
@@ -118,10 +118,10 @@ size_t act_bytes(const ulysses_problem &p, int heads) {
   return (size_t)p.B * p.S * heads * p.head_dim * elem_size(p);
 }
 
-// K or V in head layout [P][B][S][kv-heads per rank][D]: with replicated
+// K or V in head layout [P][B][Cs][kv-heads per rank][D]: with replicated
 // kv-heads P copies of one kv-head's rows, else the same size as the tensor.
 size_t kv_head_bytes(const ulysses_problem &p) {
-  return (size_t)p.P * p.B * p.S * kv_per_rank(p) * p.head_dim * elem_size(p);
+  return (size_t)p.P * p.B * chunk_len(p) * kv_per_rank(p) * p.head_dim * elem_size(p);
 }
 
 }  // namespace
@@ -138,8 +138,10 @@ int ulysses_validate(const ulysses_problem *prob) {
     return ULYSSES_ERR_ARG;
   if (!(p.softmax_scale >= 0.f) || isinf(p.softmax_scale)) return ULYSSES_ERR_ARG;
   if (p.use_rope && (!(p.rope_base > 0.f) || isinf(p.rope_base))) return ULYSSES_ERR_ARG;
-  if (p.S % p.P || p.n_head % p.P || p.n_head % p.n_kv_head ||
-      (p.n_kv_head % p.P != 0 && p.P % p.n_kv_head != 0))
+  if (p.ring < 0) return ULYSSES_ERR_ARG;
+  const int Pu = p.P / ring_of(p);  // ranks of one ring position
+  if (p.P % ring_of(p) || p.S % p.P || p.n_head % Pu || p.n_head % p.n_kv_head ||
+      (p.n_kv_head % Pu != 0 && Pu % p.n_kv_head != 0))
     return ULYSSES_ERR_DIVISIBILITY;
   if ((long long)p.n_head * p.head_dim != p.hidden) return ULYSSES_ERR_HIDDEN;
   if (p.dtype != ULYSSES_BF16 && p.dtype != ULYSSES_FP32) return ULYSSES_ERR_UNSUPPORTED;
@@ -147,6 +149,11 @@ int ulysses_validate(const ulysses_problem *prob) {
   // Index arithmetic inside the kernels keeps per-tensor element counts in
   // 64 bits and per-row quantities in 32 bits.
   if ((long long)p.B * p.P > (1ll << 30) || (long long)p.S * p.n_head > (1ll << 31))
+    return ULYSSES_ERR_UNSUPPORTED;
+  // The hybrid runs on the tensor-core kernels, whose tiles must not straddle
+  // two ring positions' chunks, without kv-head replication.
+  if (ring_of(p) > 1 && (p.dtype != ULYSSES_BF16 || (p.head_dim != 64 && p.head_dim != 128) ||
+                         chunk_len(p) % 128 != 0 || p.n_kv_head % Pu != 0))
     return ULYSSES_ERR_UNSUPPORTED;
   return ULYSSES_OK;
 }
@@ -194,7 +201,8 @@ int ulysses_qkv_proj_pack(const ulysses_problem *prob, const void *x_seq, const 
   int rc = ulysses_validate(prob);
   if (rc) return rc;
   const ulysses_problem &p = *prob;
-  if (p.dtype != ULYSSES_BF16 || (p.head_dim != 64 && p.head_dim != 128)) return ULYSSES_ERR_UNSUPPORTED;
+  if (p.dtype != ULYSSES_BF16 || (p.head_dim != 64 && p.head_dim != 128) || ring_of(p) > 1)
+    return ULYSSES_ERR_UNSUPPORTED;
   if (!x_seq || !w_qkv) return ULYSSES_ERR_ARG;
   const size_t n_out = (size_t)(p.n_head + 2 * p.n_kv_head) * p.head_dim;
   const size_t nx = (size_t)p.B * p.S * p.hidden * 2, nw = n_out * p.hidden * 2, nb = n_out * 2;
@@ -214,7 +222,8 @@ int ulysses_out_proj_unpack(const ulysses_problem *prob, const void *o_head, con
   int rc = ulysses_validate(prob);
   if (rc) return rc;
   const ulysses_problem &p = *prob;
-  if (p.dtype != ULYSSES_BF16 || (p.head_dim != 64 && p.head_dim != 128) || (p.S / p.P) % 128 != 0)
+  if (p.dtype != ULYSSES_BF16 || (p.head_dim != 64 && p.head_dim != 128) || (p.S / p.P) % 128 != 0 ||
+      ring_of(p) > 1)
     return ULYSSES_ERR_UNSUPPORTED;
   if (!o_head || !w_o) return ULYSSES_ERR_ARG;
   const size_t no = act_bytes(p, p.n_head), nw = (size_t)p.hidden * p.hidden * 2, nb = (size_t)p.hidden * 2;
@@ -260,7 +269,7 @@ int ulysses_attn_fwd_folded(const ulysses_problem *prob, const void *q_seq, cons
   if (rc) return rc;
   const ulysses_problem &p = *prob;
   if (p.dtype != ULYSSES_BF16 || (p.head_dim != 64 && p.head_dim != 128) || p.use_rope ||
-      (p.S / p.P) % 128 != 0)
+      (p.S / p.P) % 128 != 0 || ring_of(p) > 1)
     return ULYSSES_ERR_UNSUPPORTED;
   const size_t nq = act_bytes(p, p.n_head), nk = act_bytes(p, p.n_kv_head);
   const size_t nl = (size_t)p.B * p.n_head * p.S * sizeof(float);

@@ -34,6 +34,7 @@ class Workload:
     sigma: float
     backward: bool
     seed: int
+    ring: int = 1         # ring positions of the Ulysses x ring hybrid (1: plain Ulysses)
 
     @property
     def Sl(self) -> int:
@@ -69,6 +70,10 @@ WORKLOADS: Dict[str, Workload] = {
 # replication path.
 EXTRA_WORKLOADS: Dict[str, Workload] = {
     "C4-kv4": WORKLOADS["C4"].with_(name="C4-kv4", n_kv_head=4, seed=1006),
+    # The pages' example of the head-count bound ("Sequence Parallelism II",
+    # §4: 32 heads cannot be spread over 256 ranks by heads alone), run as the
+    # Ulysses x ring hybrid: 8 ring positions of 32 ranks on C4's model.
+    "C4-ring8": WORKLOADS["C4"].with_(name="C4-ring8", P=256, ring=8, seed=1007),
 }
 
 # The permute-only sweep at the head-count bound (P=32, one head per rank).
