@@ -122,24 +122,34 @@ struct FwdParams {
   uint32_t *status;
 };
 
-// TMA coordinates (head, row, rank*B+batch) of the 128-row tile starting at
-// global position `pos` of local head `lh` of group member `r`, batch `b`
-// (with plain Ulysses the member is the rank).
-struct TileCoord {
-  int head, row, outer;
-};
-// `rep` > 1: a replicated kv-head (rank r reads global kv-head r / rep).
-__device__ __forceinline__ TileCoord tile_coord(const FwdParams &p, int r, int b, int lh, int heads_local,
-                                                int pos, int rep = 1) {
-  if (!p.folded) {
-    // ring position holding the tile (0 without a ring); a tile starting past
-    // the sequence end stays on the last one, its rows out of range (zeros)
-    const int c = (pos < p.S ? pos : p.S - 1) / p.Cs;
-    return {lh, pos - c * p.Cs, (c * p.Pu + r) * p.B + b};
+// TMA coordinates (head, row, rank*B+batch) of the 128-row tiles of one head,
+// walked in position order.  The tile at global position pos sits in block
+// c = pos / period at row pos % period: a block is a ring position's chunk
+// (period Cs; plain Ulysses has one block, the whole sequence) in head
+// layout, or, folded, a rank's sequence shard (period Sl).  Head `lh` of group
+// member `r` (the rank, without a ring), batch `b`; `rep` > 1: a replicated
+// kv-head (folded: rank r reads global kv-head r / rep).
+struct TileWalk {
+  int head, base, row, c, last, period, step;  // outer coordinate = c * step + base
+  __device__ __forceinline__ TileWalk(const FwdParams &p, int r, int b, int lh, int heads_local, int pos,
+                                      int rep = 1) {
+    if (!p.folded) {
+      head = lh, period = p.Cs, step = p.Pu * p.B, base = r * p.B + b;
+    } else {
+      head = rep > 1 ? r / rep : r * heads_local + lh, period = p.Sl, step = p.B, base = b;
+    }
+    // a tile starting past the sequence end stays in the last block, its rows
+    // out of range (read as zeros)
+    last = (p.S - 1) / period;
+    c = (pos < p.S ? pos : p.S - 1) / period;
+    row = pos - c * period;
   }
-  const int src = pos / p.Sl;
-  return {rep > 1 ? r / rep : r * heads_local + lh, pos - src * p.Sl, src * p.B + b};
-}
+  __device__ __forceinline__ int outer() const { return c * step + base; }
+  __device__ __forceinline__ void next() {  // the tile 128 positions on
+    row += 128;
+    if (row >= period && c < last) row -= period, ++c;
+  }
+};
 
 // Slot and phase parity of ring entry e.
 __device__ __forceinline__ uint32_t ring_slot(int e) { return (uint32_t)(e % kSlots); }
@@ -213,18 +223,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int member = rb / p.B, bb = rb - member * p.B;
         // Q_A, Q_B and K_0 on one barrier
         mbar_arrive_expect_tx(bar + kBarQFull, 3 * L::kTile);
-        for (int x = 0; x < 2; ++x) {
-          const TileCoord tq = tile_coord(p, member, bb, j, p.hp, qp * 2 * BM + x * BM);
+        TileWalk tq(p, member, bb, j, p.hp, qp * 2 * BM);
+        for (int x = 0; x < 2; ++x, tq.next())
           for (int c = 0; c < kChunks; ++c)
-            tma_load_4d(sQ + x * L::kTile + c * kChunkBytes, &tmQ, bar + kBarQFull, c * 64, tq.head,
-                        tq.row, tq.outer);
-        }
-        const TileCoord t0 = tile_coord(p, member, bb, kl, p.kvp, 0, p.kv_rep);
+            tma_load_4d(sQ + x * L::kTile + c * kChunkBytes, &tmQ, bar + kBarQFull, c * 64, tq.head, tq.row,
+                        tq.outer());
+        TileWalk tv(p, member, bb, kl, p.kvp, 0, p.kv_rep);  // key tile e (K_e, V_e)
         for (int c = 0; c < kChunks; ++c)
-          tma_load_4d(sK0 + c * kChunkBytes, &tmK, bar + kBarQFull, c * 64, t0.head, t0.row, t0.outer);
+          tma_load_4d(sK0 + c * kChunkBytes, &tmK, bar + kBarQFull, c * 64, tv.head, tv.row, tv.outer());
         // entry e = V_e and (when tile B goes on) K_{e+1}: what key tile e's two bursts read
         int issued = -1;
-        TileCoord tv = t0;  // key tile e's coordinates (K_e's and V_e's)
         for (int e = 0; e < nB; ++e) {
           const uint32_t slot = ring_slot(e), full = bar + kBarKVFull + 8 * slot;
           if (!mbar_wait_bounded(bar + kBarKVEmpty + 8 * slot, ring_parity(e) ^ 1, abort_flag, gst)) break;
@@ -232,12 +240,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(full, (has_k ? 2u : 1u) * L::kTile);
           const uint32_t dst = sKV + slot * L::kEntry;
           for (int c = 0; c < kChunks; ++c)
-            tma_load_4d(dst + c * kChunkBytes, &tmV, full, c * 64, tv.head, tv.row, tv.outer);
-          if (has_k) {
-            tv = tile_coord(p, member, bb, kl, p.kvp, (e + 1) * BN, p.kv_rep);
+            tma_load_4d(dst + c * kChunkBytes, &tmV, full, c * 64, tv.head, tv.row, tv.outer());
+          tv.next();
+          if (has_k)
             for (int c = 0; c < kChunks; ++c)
-              tma_load_4d(dst + L::kTile + c * kChunkBytes, &tmK, full, c * 64, tv.head, tv.row, tv.outer);
-          }
+              tma_load_4d(dst + L::kTile + c * kChunkBytes, &tmK, full, c * 64, tv.head, tv.row, tv.outer());
           issued = e;
         }
         if (*abort_flag) {
