@@ -42,7 +42,11 @@ METRIC = "tokens/s + attn TFLOP/s (S=32K, 32 heads, P=8 virtual); seq↔head per
 # DRAM bytes (read + write) per launch of a kernel on a workload, from one ncu
 # capture of this build (profiles/launches_c4_fwd_bwd.md gives the command and
 # the table); a kernel changed since its capture has no entry.
-TRAFFIC = {}
+TRAFFIC = {
+    ("attn_fwd", "C4"): 1178681479,
+    ("bwd_dkdv", "C4"): 1882669454,
+    ("bwd_dq", "C4"): 1769197710,
+}
 
 
 def load_peaks():
