@@ -20,7 +20,11 @@ taken (the plainest one the rest of the pages supports):
     own chunk r = tokens [r*Cs, (r+1)*Cs), Cs = S/R.
   * The Ulysses All-to-All runs inside each ring position over its Pu ranks:
     rank (r, u) receives heads [u*hp, (u+1)*hp), hp = n_head/Pu (kv-heads
-    likewise), of the whole chunk r, pieces in source order ([SP2] §1).
+    likewise), of the whole chunk r, pieces in source order ([SP2] §1).  With
+    fewer kv-heads than Pu (Pu a multiple of n_kv_head) each kv-head goes to
+    the rep = Pu/n_kv_head members whose q-heads read it, member u holding
+    kv-head u // rep, and a kv-head's gradient is the sum of its replicas'
+    (the KV-head replication of plain Ulysses, inside each ring position).
   * Ring attention over the R ranks (0, u) ... (R-1, u) that hold the same
     heads: rank (r, u) keeps its query block (chunk r); at ring step k it
     works on the key/value block of chunk c = (r - k) mod R, the blocks moving
@@ -48,12 +52,19 @@ from . import Problem, rope_seq, shard_sequence
 
 
 def dims(prob: Problem):
-    """(Pu, R, Cs, hp, kvp) of a hybrid problem."""
+    """(Pu, R, Cs, hp, kvp) of a hybrid problem; kvp = 1 with replicated kv-heads."""
     R = prob.ring
     assert R >= 1 and prob.P % R == 0 and prob.S % prob.P == 0
     Pu = prob.P // R
-    assert prob.n_head % Pu == 0 and prob.n_kv_head % Pu == 0 and prob.n_head % prob.n_kv_head == 0
-    return Pu, R, prob.S // R, prob.n_head // Pu, prob.n_kv_head // Pu
+    kv = prob.n_kv_head
+    assert prob.n_head % Pu == 0 and prob.n_head % kv == 0 and (kv % Pu == 0 or Pu % kv == 0)
+    return Pu, R, prob.S // R, prob.n_head // Pu, kv // Pu if kv >= Pu else 1
+
+
+def kv_replicas(prob: Problem) -> int:
+    """Members of a ring position holding each kv-head (1 unless n_kv_head < Pu)."""
+    Pu = prob.P // prob.ring
+    return Pu // prob.n_kv_head if prob.n_kv_head < Pu else 1
 
 
 def a2a_seq_to_head(x_ranks: Sequence[np.ndarray], heads: int, ring: int, elem_bytes: int = 2):
@@ -77,6 +88,52 @@ def a2a_seq_to_head(x_ranks: Sequence[np.ndarray], heads: int, ring: int, elem_b
                     sent[r * Pu + src] += piece
                     recv[r * Pu + dst] += piece
     return y, sent, recv
+
+
+def a2a_seq_to_head_replicated(x_ranks: Sequence[np.ndarray], heads: int, ring: int, elem_bytes: int = 2):
+    """The kv All-to-All of every ring position when heads < Pu: member u of
+    ring position r receives kv-head u // rep (rep = Pu/heads) of chunk r.
+    Per rank [B,Sl,heads,D] -> [B,Cs,1,D]."""
+    P = len(x_ranks)
+    Pu = P // ring
+    B, Sl, h, D = x_ranks[0].shape
+    assert h == heads and Pu % heads == 0
+    rep = Pu // heads
+    y = [np.zeros((B, Sl * Pu, 1, D)) for _ in range(P)]
+    sent, recv = [0] * P, [0] * P
+    piece = B * Sl * D * elem_bytes
+    for r in range(ring):
+        for dst in range(Pu):
+            for src in range(Pu):
+                y[r * Pu + dst][:, src * Sl:(src + 1) * Sl, 0] = x_ranks[r * Pu + src][:, :, dst // rep]
+                if src != dst:
+                    sent[r * Pu + src] += piece
+                    recv[r * Pu + dst] += piece
+    return y, sent, recv
+
+
+def reduce_head_to_seq_replicated(y_ranks: Sequence[np.ndarray], heads: int, ring: int, elem_bytes: int = 2):
+    """Adjoint of a2a_seq_to_head_replicated: kv-head kv of sequence rank
+    (r, dst) = the sum over its rep replicas (members kv*rep + j, j in order)
+    of their rows.  Per rank [B,Cs,1,D] -> [B,Sl,heads,D]."""
+    P = len(y_ranks)
+    Pu = P // ring
+    B, Cs, one, D = y_ranks[0].shape
+    assert one == 1 and Pu % heads == 0 and Cs % Pu == 0
+    rep, Sl = Pu // heads, Cs // Pu
+    x = [np.zeros((B, Sl, heads, D)) for _ in range(P)]
+    sent, recv = [0] * P, [0] * P
+    piece = B * Sl * D * elem_bytes
+    for r in range(ring):
+        for dst in range(Pu):
+            for kv in range(heads):
+                for j in range(rep):
+                    src = kv * rep + j
+                    x[r * Pu + dst][:, :, kv] += y_ranks[r * Pu + src][:, dst * Sl:(dst + 1) * Sl, 0]
+                    if src != dst:
+                        sent[r * Pu + src] += piece
+                        recv[r * Pu + dst] += piece
+    return x, sent, recv
 
 
 def a2a_head_to_seq(y_ranks: Sequence[np.ndarray], heads: int, ring: int, elem_bytes: int = 2):
@@ -213,8 +270,9 @@ def forward(prob: Problem, Q, K, V, rows=None, elem_bytes: int = 2):
         q_seq = rope_seq(q_seq, prob.rope_base, +1)
         k_seq = rope_seq(k_seq, prob.rope_base, +1)
     q_head, sq, _ = a2a_seq_to_head(q_seq, prob.n_head, prob.ring, elem_bytes)
-    k_head, sk, _ = a2a_seq_to_head(k_seq, prob.n_kv_head, prob.ring, elem_bytes)
-    v_head, sv, _ = a2a_seq_to_head(v_seq, prob.n_kv_head, prob.ring, elem_bytes)
+    kv_a2a = a2a_seq_to_head_replicated if kv_replicas(prob) > 1 else a2a_seq_to_head
+    k_head, sk, _ = kv_a2a(k_seq, prob.n_kv_head, prob.ring, elem_bytes)
+    v_head, sv, _ = kv_a2a(v_seq, prob.n_kv_head, prob.ring, elem_bytes)
     o_head, lse = ring_attention_fwd(prob, q_head, k_head, v_head, rows=rows)
     o_seq = a2a_head_to_seq(o_head, prob.n_head, prob.ring, elem_bytes)[0] if rows is None else None
     return dict(q_head=q_head, k_head=k_head, v_head=v_head, o_head=o_head, lse=lse, o_seq=o_seq,
@@ -232,8 +290,9 @@ def backward(prob: Problem, Q, K, V, dO, elem_bytes: int = 2):
     dq_h, dk_h, dv_h = ring_attention_bwd(prob, fw["q_head"], fw["k_head"], fw["v_head"], do_head,
                                           fw["o_head"], fw["lse"])
     dq_seq = a2a_head_to_seq(dq_h, prob.n_head, prob.ring, elem_bytes)[0]
-    dk_seq = a2a_head_to_seq(dk_h, prob.n_kv_head, prob.ring, elem_bytes)[0]
-    dv_seq = a2a_head_to_seq(dv_h, prob.n_kv_head, prob.ring, elem_bytes)[0]
+    kv_back = reduce_head_to_seq_replicated if kv_replicas(prob) > 1 else a2a_head_to_seq
+    dk_seq = kv_back(dk_h, prob.n_kv_head, prob.ring, elem_bytes)[0]
+    dv_seq = kv_back(dv_h, prob.n_kv_head, prob.ring, elem_bytes)[0]
     if prob.use_rope:
         dq_seq = rope_seq(dq_seq, prob.rope_base, -1)
         dk_seq = rope_seq(dk_seq, prob.rope_base, -1)
@@ -246,5 +305,6 @@ def unshard(xs: Sequence[np.ndarray]) -> np.ndarray:
     return np.concatenate(list(xs), axis=1)
 
 
-__all__: List[str] = ["dims", "a2a_seq_to_head", "a2a_head_to_seq", "block_attention", "merge",
+__all__: List[str] = ["dims", "kv_replicas", "a2a_seq_to_head", "a2a_seq_to_head_replicated",
+                      "reduce_head_to_seq_replicated", "a2a_head_to_seq", "block_attention", "merge",
                       "ring_attention_fwd", "ring_attention_bwd", "forward", "backward", "unshard"]

@@ -59,6 +59,8 @@ CASES = [  # P, R, B, S, h, kv, D, causal, rope
     (8, 8, 1, 64, 4, 4, 4, True, False),    # pure ring (Pu = 1)
     (4, 2, 2, 48, 4, 4, 8, False, True),
     (6, 3, 1, 72, 4, 2, 8, True, True),     # three ring positions
+    (8, 2, 1, 64, 8, 2, 4, True, True),     # kv-heads replicated inside a ring position (rep 2)
+    (16, 4, 2, 64, 4, 1, 4, False, True),   # one kv-head for the 4 members of every position
 ]
 
 
@@ -200,8 +202,12 @@ MUTANTS = [
      "= x_ranks[src * ring + r][:, :, dst * hp:(dst + 1) * hp]"),
     ("dK stays on the query rank", "dk[owner][b][:, kl] += scale * (ds.T @ q)", "dk[me][b][:, kl] += scale * (ds.T @ q)"),
     ("backward drops delta", "ds = p * (dp - delta[:, None])", "ds = p * dp"),
-    ("own piece counted as traffic", "                if src != dst:\n                    sent[r * Pu + src] += piece\n                    recv[r * Pu + dst] += piece\n    return y",
-     "                if True:\n                    sent[r * Pu + src] += piece\n                    recv[r * Pu + dst] += piece\n    return y"),
+    ("own piece counted as traffic", "dst * hp:(dst + 1) * hp]\n                if src != dst:",
+     "dst * hp:(dst + 1) * hp]\n                if True:"),
+    ("replica holds the wrong kv-head", "[:, src * Sl:(src + 1) * Sl, 0] = x_ranks[r * Pu + src][:, :, dst // rep]",
+     "[:, src * Sl:(src + 1) * Sl, 0] = x_ranks[r * Pu + src][:, :, dst % heads]"),
+    ("replica gradient dropped", "                for j in range(rep):\n                    src = kv * rep + j",
+     "                for j in range(1, rep):\n                    src = kv * rep + j"),
     ("block lse misses the max", "lse = np.where(live, ms + np.log(np.where(live, l, 1.0)), -np.inf)",
      "lse = np.where(live, np.log(np.where(live, l, 1.0)), -np.inf)"),
 ]
@@ -224,6 +230,7 @@ def battery(mod):
         ("fwd-P>h", lambda: check_forward_equals_unsharded(mod, *CASES[1])),
         ("bwd", lambda: check_backward_equals_plain(mod, *CASES[0])),
         ("bwd-three", lambda: check_backward_equals_plain(mod, *CASES[4])),
+        ("bwd-replicated", lambda: check_backward_equals_plain(mod, *CASES[5])),
         ("ulysses", lambda: check_ring_one_is_ulysses(mod)),
         ("ownership", lambda: check_ownership(mod)),
         ("bytes", lambda: check_identity_and_bytes(mod)),
