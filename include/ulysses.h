@@ -95,9 +95,11 @@ enum ulysses_device_status {
  * query rows runs over the key/value chunks of every ring position (the
  * ring's circulation), so O, dQ, dK, dV are those of plain attention.  Head
  * layouts below then read [P][B][Cs][...] instead of [P][B][S][...], the LSE
- * [P][B][hp][Cs].  ring > 1 needs bf16, head_dim 64 or 128, Cs a multiple of
- * 128 and Pu dividing n_kv_head (ULYSSES_ERR_UNSUPPORTED otherwise); the
- * folded forward and the two projections take ring <= 1 only.
+ * [P][B][hp][Cs].  With fewer kv-heads than Pu (Pu a multiple of n_kv_head)
+ * each kv-head goes to the Pu/n_kv_head members whose q-heads read it, as in
+ * plain Ulysses.  ring > 1 needs bf16, head_dim 64 or 128 and Cs a multiple of
+ * 128 (ULYSSES_ERR_UNSUPPORTED otherwise); the folded forward and the two
+ * projections take ring <= 1 only.
  */
 typedef struct ulysses_problem {
   int B, S, hidden, n_head, n_kv_head, head_dim, P;

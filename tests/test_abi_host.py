@@ -64,7 +64,8 @@ def prob(**kw):
     (dict(ring=2, dtype=U.FP32), -4),          # the hybrid runs on the bf16 tensor-core kernels only
     (dict(ring=2, head_dim=32, hidden=32 * 32), -4),
     (dict(S=8 * 96, ring=4), -4),              # chunk S/ring = 192 is not a multiple of 128
-    (dict(ring=2, n_kv_head=2), -4),           # kv-head replication inside a ring position
+    (dict(ring=2, n_kv_head=2), 0),            # kv-head replication inside a ring position (Pu = 4)
+    (dict(ring=2, n_kv_head=3, n_head=24, hidden=24 * 128), -2),  # neither of n_kv_head, Pu divides the other
 ])
 def test_validate_codes(lib, kw, code):
     assert U.ulysses_validate(prob(**kw)) == code

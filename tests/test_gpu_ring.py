@@ -28,7 +28,9 @@ RING_CASES = [rw(4, 2, 1, 512, 4, 2, 128),                  # 2 ring positions o
               rw(8, 4, 1, 1024, 4, 4, 64),                  # P = 8 > 4 heads
               rw(8, 8, 2, 1024, 2, 2, 128, causal=False),   # pure ring (one rank per position)
               rw(6, 3, 1, 768, 4, 2, 128),                  # three ring positions
-              rw(3, 3, 1, 384, 2, 2, 64)]                   # last query tile pair half past the end
+              rw(3, 3, 1, 384, 2, 2, 64),                   # last query tile pair half past the end
+              rw(8, 2, 1, 1024, 8, 2, 128),                 # kv-heads replicated inside a ring position
+              rw(16, 4, 2, 1024, 4, 1, 64, causal=False)]   # one kv-head for the 4 members of every position
 
 
 def _id(w):
@@ -55,12 +57,11 @@ def test_pack_is_the_ring_positions_all_to_all(w):
         for name, heads, got, rot in (("q", w.n_head, run.buf.q_head, rope), ("k", w.n_kv_head, run.buf.k_head, rope),
                                       ("v", w.n_kv_head, run.buf.v_head, False)):
             seq = oracle.shard_sequence(x[name], w.P)
-            want, _, _ = RG.a2a_seq_to_head(oracle.rope_seq(seq, float(np.float32(w.rope_base))) if rot else seq,
-                                            heads, w.ring)
+            a2a = RG.a2a_seq_to_head_replicated if heads < w.P // w.ring else RG.a2a_seq_to_head
+            want, _, _ = a2a(oracle.rope_seq(seq, float(np.float32(w.rope_base))) if rot else seq, heads, w.ring)
             # |x_i| + |x_{i+D/2}|: the size of what the fp32 rotation sums
-            mag, _, _ = RG.a2a_seq_to_head(
-                [np.concatenate([np.abs(a[..., :half]) + np.abs(a[..., half:])] * 2, axis=-1) for a in seq],
-                heads, w.ring)
+            mag, _, _ = a2a([np.concatenate([np.abs(a[..., :half]) + np.abs(a[..., half:])] * 2, axis=-1)
+                             for a in seq], heads, w.ring)
             g = to64(got)
             for r in range(w.P):
                 if not rot:
@@ -124,7 +125,7 @@ def _same_as_plain_ulysses(w, backward):
             torch.equal(a.transpose(0, 1).reshape(w.B, -1), b.transpose(0, 1).reshape(w.B, -1)), name
 
 
-@pytest.mark.parametrize("w", RING_CASES[:3], ids=_id)
+@pytest.mark.parametrize("w", RING_CASES[:3] + RING_CASES[5:], ids=_id)
 def test_bit_identical_to_plain_ulysses(w):
     _same_as_plain_ulysses(w.with_(backward=True), backward=True)
 

@@ -56,7 +56,7 @@ struct BwdParams {
   const __nv_bfloat16 *q, *dout;       // head layout [P][B][S][hp][D] (the dQ kernel's TMEM operands)
   __nv_bfloat16 *dq, *dk, *dv;         // sequence-sharded outputs
   int kv_rep;                          // > 1: replicated kv-heads; dk/dv then point to float
-                                       // per-rank partials [P*B][S][D] (unscaled, not rotated)
+                                       // per-rank partials [P*B][Cs][D] (unscaled, not rotated)
   uint32_t *status;                    // status word; the RoPE table key follows it
   uint32_t rope_key;
   // Ulysses x ring hybrid: Pu ranks per ring position, Cs tokens per chunk
@@ -473,8 +473,11 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
       // over the replicas (with scale and inverse rotation) follows.
       tc_fence_after_sync();
       const bool live = kvr < p.S;
-      float *pv = reinterpret_cast<float *>(p.dv) + ((size_t)rb * p.S + (live ? kvr : 0)) * D;
-      float *pk = reinterpret_cast<float *>(p.dk) + ((size_t)rb * p.S + (live ? kvr : 0)) * D;
+      // partials [P*B][Cs][D]: the row of key kvr in this member's head layout
+      const int kr = live ? kvr : 0;
+      const size_t prow = (size_t)hl_outer(p, rb, kr) * p.Cs + kr % p.Cs;
+      float *pv = reinterpret_cast<float *>(p.dv) + prow * D;
+      float *pk = reinterpret_cast<float *>(p.dk) + prow * D;
       // warpgroup g owns columns [g*D/2, (g+1)*D/2) of both accumulators; the
       // TMEM loads are warp-wide, only the stores depend on the row
 #pragma unroll

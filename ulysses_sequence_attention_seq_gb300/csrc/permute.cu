@@ -441,9 +441,11 @@ cudaError_t launch_pack_do_delta(const ulysses_problem &p, const void *do_seq, c
 // ---------------------------------------------------------------------------
 // Gradients of replicated kv-heads ("Sequence Parallelism II", §6: the
 // gradients go back head -> seq): kv-head kv was handed to the R ranks
-// kv*R .. kv*R+R-1, so its gradient is the sum of their partials, added in
-// rank order:
-//   dV_seq[d][b][t][kv][e] = sum_j dv_part[(kv*R+j)*B + b][d*Sl+t][e]
+// kv*R .. kv*R+R-1 (of the token's ring position rp: ranks rp*Pu + kv*R + j),
+// so its gradient is the sum of their partials, added in rank order:
+//   dV_seq[d][b][t][kv][e] = sum_j dv_part[(rp*Pu + kv*R+j)*B + b][crow][e],
+// crow = (d % Pu)*Sl + t the token's row in its ring position's chunk (plain
+// Ulysses: rp = 0, Pu = P, crow = d*Sl + t)
 // and dK the same, then scaled and rotated back by -angle(d*Sl+t) on the pairs
 // (i, i+D/2).  One thread per (row, kv-head, 4 rotation pairs): float4 loads of
 // both halves from each replica, two 8-byte bf16 stores per tensor.
@@ -451,10 +453,10 @@ namespace {
 
 __global__ void __launch_bounds__(256) kv_reduce_kernel(const float *__restrict__ dkp, const float *__restrict__ dvp,
                                                         __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv,
-                                                        int P, int B, int Sl, int n_kv, int D, float scale,
+                                                        int P, int B, int Sl, int n_kv, int D, int Pu, float scale,
                                                         const float *__restrict__ cs, const float *__restrict__ sn) {
-  const int R = P / n_kv, half = D / 2, q4 = half / 4;
-  const int S = P * Sl;
+  const int R = Pu / n_kv, half = D / 2, q4 = half / 4;
+  const int Cs = Pu * Sl;
   const long long n = (long long)P * B * Sl * n_kv * q4;
   for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < n; u += (long long)gridDim.x * blockDim.x) {
     const int c = (int)(u % q4);
@@ -466,9 +468,10 @@ __global__ void __launch_bounds__(256) kv_reduce_kernel(const float *__restrict_
     const int b = (int)(rest % B);
     const int d = (int)(rest / B);
     const int pos = d * Sl + t;
+    const int rp = d / Pu, crow = (d - rp * Pu) * Sl + t;  // ring position, row in its chunk
     float4 kx = make_float4(0.f, 0.f, 0.f, 0.f), ky = kx, vx = kx, vy = kx;
     for (int j = 0; j < R; ++j) {
-      const size_t off = (((size_t)(kv * R + j) * B + b) * S + pos) * D + (size_t)c * 4;
+      const size_t off = (((size_t)(rp * Pu + kv * R + j) * B + b) * Cs + crow) * D + (size_t)c * 4;
       const float4 a = *reinterpret_cast<const float4 *>(dkp + off);
       const float4 a2 = *reinterpret_cast<const float4 *>(dkp + off + half);
       const float4 v1 = *reinterpret_cast<const float4 *>(dvp + off);
@@ -516,7 +519,8 @@ cudaError_t launch_kv_reduce(const ulysses_problem &p, const float *dk_part, con
   const long long n = (long long)p.B * p.S * p.n_kv_head * (p.head_dim / 8);
   kv_reduce_kernel<<<grid_for(n / 256 + 1), 256, 0, st>>>(dk_part, dv_part, static_cast<__nv_bfloat16 *>(dk_seq),
                                                           static_cast<__nv_bfloat16 *>(dv_seq), p.P, p.B,
-                                                          p.S / p.P, p.n_kv_head, p.head_dim, scale, cs, sn);
+                                                          p.S / p.P, p.n_kv_head, p.head_dim, group_ranks(p), scale,
+                                                          cs, sn);
   return cudaGetLastError();
 }
 

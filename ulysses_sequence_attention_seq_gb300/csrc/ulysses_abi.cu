@@ -151,9 +151,9 @@ int ulysses_validate(const ulysses_problem *prob) {
   if ((long long)p.B * p.P > (1ll << 30) || (long long)p.S * p.n_head > (1ll << 31))
     return ULYSSES_ERR_UNSUPPORTED;
   // The hybrid runs on the tensor-core kernels, whose tiles must not straddle
-  // two ring positions' chunks, without kv-head replication.
+  // two ring positions' chunks.
   if (ring_of(p) > 1 && (p.dtype != ULYSSES_BF16 || (p.head_dim != 64 && p.head_dim != 128) ||
-                         chunk_len(p) % 128 != 0 || p.n_kv_head % Pu != 0))
+                         chunk_len(p) % 128 != 0))
     return ULYSSES_ERR_UNSUPPORTED;
   return ULYSSES_OK;
 }
