@@ -157,7 +157,7 @@ def run_ulysses(args, w, rank, world):
     names = ["pack_qkv", "attn_fwd", "unpack_out"] + (["bwd_prepare", "bwd_dkdv", "bwd_dq"] if backward else [])
     # pack, forward, unpack; prepare, dK/dV (+ the replica sum when kv-heads are
     # replicated), dQ
-    launches_per_step = 3 + ((4 if w.n_kv_head < w.P else 3) if backward else 0)
+    launches_per_step = 3 + ((4 if w.n_kv_head < w.P // w.ring else 3) if backward else 0)
 
     def step(evs=None, split=True):
         """One pass of the whole path.  With `split` the backward runs as its
@@ -209,37 +209,31 @@ def run_ulysses(args, w, rank, world):
     total_ms = t0.elapsed_time(t1)
     per = {n: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)] for i, n in enumerate(names)}
 
-    # ---- end to end through the public API with host buffers
-    o_host = torch.empty(buf.o_seq.shape, dtype=buf.o_seq.dtype, pin_memory=True)
-    grads_host = None
+    # ---- end to end through the public API with host buffers: every step
+    # uploads its inputs from pinned host memory and downloads its results
+    # (O, and dQ, dK, dV with a backward); the streamed path overlaps step k's
+    # compute with step k+1's upload and step k-1's download.
+    from ulysses_sequence_attention_seq_gb300.streamed import StreamedPath
+    sp = StreamedPath(prob, backward=backward, device=dev)
+    host_in = {"q_seq": host["q"], "k_seq": host["k"], "v_seq": host["v"]}
     if backward:
-        grads_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (buf.dq_seq, buf.dk_seq, buf.dv_seq)]
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = o_host.numel() * o_host.element_size() + (sum(t.numel() * t.element_size() for t in grads_host) if grads_host else 0)
-
-    def e2e_step():
-        buf.q_seq.copy_(host["q"], non_blocking=True)
-        buf.k_seq.copy_(host["k"], non_blocking=True)
-        buf.v_seq.copy_(host["v"], non_blocking=True)
-        if backward:
-            buf.do_seq.copy_(host["do"], non_blocking=True)
-        step(split=False)
-        o_host.copy_(buf.o_seq, non_blocking=True)
-        if backward:
-            for h, d in zip(grads_host, (buf.dq_seq, buf.dk_seq, buf.dv_seq)):
-                h.copy_(d, non_blocking=True)
-
-    for _ in range(2):
-        e2e_step()
+        host_in["do_seq"] = host["do"]
+    host_out = {n: torch.empty(getattr(sp.sets[0], n).shape, dtype=getattr(sp.sets[0], n).dtype, pin_memory=True)
+                for n in sp.out_names()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    sp.run(host_in, host_out, 2)
     torch.cuda.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    sp.run(host_in, host_out, args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
+    if sp.status() != 0:
+        raise RuntimeError("device status word set during the end-to-end steps")
+    del sp
     # ---- folded forward (pack + attention + unpack in one kernel) vs the three
     # calls, same shapes with RoPE off (the folded path needs pre-rotated q, k)
     folded = None
