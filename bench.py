@@ -262,9 +262,12 @@ def run_ulysses(args, w, rank, world):
             times[name] = a.elapsed_time(b2) / args.steps
         folded = dict(times, workload=f"{w.name} shapes, RoPE off (q and k rotated by their producer)")
     status = U.ulysses_read_status(buf.ws)
+    # the MUFU unit's exponential throughput on this GPU (the softmax's secondary bound)
+    ex2_rate = U.ulysses_selftest_ex2_rate()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     return dict(total_ms=total_ms, per=per, clocks=clk, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
                 launches=launches_per_step * args.steps, status=status, backward=backward,
-                folded=folded)
+                folded=folded, ex2_rate=ex2_rate, sms=sms)
 
 
 def barrier(world):
@@ -577,6 +580,17 @@ def main():
                       "executed_frac": exe / (per[k] * 1e-3) / 1e12 / tf_sust}
     dominant = max(kernels, key=lambda k: kernels[k]["ms"])
     dk = kernels[dominant]
+    # One exponential per (query, key) pair the forward computes, against the
+    # measured ex2 rate per SM per cycle at the median SM clock of the run.
+    exps = w.B * w.n_head * (w.S * (w.S + 1) / 2 if w.causal else float(w.S) * w.S)
+    clk_hz = (r["clocks"].get("sm_mhz") or 0) * 1e6
+    mufu = None
+    if clk_hz > 0 and r["ex2_rate"] > 0:
+        ach = exps / (attn_ms * 1e-3) / (r["sms"] * clk_hz)
+        mufu = {"bound": "mufu", "kernel": f"attn_fwd_tc_kernel<{w.head_dim}>", "achieved": ach,
+                "peak": r["ex2_rate"], "unit": "ex2/SM/cycle", "frac": ach / r["ex2_rate"], "exps_per_launch": exps,
+                "peak_source": "measured on this GPU by ulysses_selftest_ex2_rate",
+                "note": "exponentials per forward / kernel time / (SMs x median SM clock)"}
     fwd_tokens = job_throughput(tokens, (per["pack_qkv"] + attn_ms + per["unpack_out"]) * 1e-3, world)
     line = {
         "metric": METRIC, "value": job_throughput(tokens, ms * 1e-3, world), "unit": "tokens/s", "n_gpus": world,
@@ -605,7 +619,8 @@ def main():
                                 "pack_qkv": {"bound": "hbm", "achieved": pack_gbs, "peak": hbm, "unit": "GB/s",
                                              "frac": pack_gbs / hbm},
                                 "unpack_out": {"bound": "hbm", "achieved": unpack_gbs, "peak": hbm, "unit": "GB/s",
-                                               "frac": unpack_gbs / hbm}},
+                                               "frac": unpack_gbs / hbm},
+                                **({"attn_fwd_mufu": mufu} if mufu else {})},
         "clocks": r["clocks"],
         "e2e": {"value": job_throughput(tokens, e2e_ms * 1e-3, world), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},

@@ -296,6 +296,25 @@ int ulysses_selftest_wait_timeout(void *ws, size_t ws_bytes, unsigned long long 
                                   ulysses_stream_t stream);
 
 /*
+ * Throughput of the SM's base-2 exponential (the MUFU unit's ex2), the
+ * secondary bound of the softmax: the attention forward takes one exponential
+ * per (query, key) pair it computes ("Sequence Parallelism II: DeepSpeed
+ * Ulysses and All-to-All Attention", §8: causal attention keeps its triangular
+ * work), B*n_head*S(S+1)/2 for a causal pass.
+ *
+ * Launches, on `stream`, 2 blocks of 512 threads per SM, every thread running 8
+ * independent dependent chains of ex2 for 4096 steps, and writes the largest
+ * block's elapsed SM cycles (uint64) to the device pointer `cycles` (8 bytes,
+ * 8-byte aligned; the caller reads it after the stream completes).  Sets
+ * *ex2_per_launch to the exponentials the launch computes and *sms to the SM
+ * count, so ex2 per SM per cycle = *ex2_per_launch / (*sms * cycles).
+ * Errors: ULYSSES_ERR_ARG (NULL pointer, bytes < 8), ULYSSES_ERR_ALIGN,
+ * ULYSSES_ERR_CUDA.
+ */
+int ulysses_selftest_ex2_rate(void *cycles, size_t bytes, long long *ex2_per_launch, int *sms,
+                              ulysses_stream_t stream);
+
+/*
  * The backward for callers that cannot allocate device memory.
  *
  * The paper has no counterpart to this entry point (the pages describe no

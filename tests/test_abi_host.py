@@ -139,6 +139,16 @@ def test_pointer_checks_fail_before_launch(lib):
     assert lib.ulysses_attn_bwd(ctypes.byref(pf.c()), *[vp(base + i * nq) for i in range(10)], nws, vp(0)) == -4
 
 
+def test_selftest_ex2_rate_argument_checks(lib):
+    vp = ctypes.c_void_p
+    fn = lib.ulysses_selftest_ex2_rate
+    n, sms = ctypes.c_longlong(0), ctypes.c_int(0)
+    assert fn(vp(0), 8, ctypes.byref(n), ctypes.byref(sms), vp(0)) == -1          # NULL buffer
+    assert fn(vp(0x10000), 4, ctypes.byref(n), ctypes.byref(sms), vp(0)) == -1    # too small
+    assert fn(vp(0x10000), 8, None, ctypes.byref(sms), vp(0)) == -1               # NULL count
+    assert fn(vp(0x10004), 8, ctypes.byref(n), ctypes.byref(sms), vp(0)) == -5    # misaligned
+
+
 def test_selftest_wait_timeout_argument_checks(lib):
     """The timeout self-test refuses bad arguments on the host, before any launch."""
     vp = ctypes.c_void_p

@@ -126,6 +126,8 @@ def lib():
         L.ulysses_qkv_proj_pack.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_out_proj_unpack.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_selftest_wait_timeout.argtypes = [vp, sz, ctypes.c_ulonglong, vp]
+        L.ulysses_selftest_ex2_rate.argtypes = [vp, sz, ctypes.POINTER(ctypes.c_longlong),
+                                                ctypes.POINTER(ctypes.c_int), vp]
         L.ulysses_attn_bwd_dkdv.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_attn_bwd_dq.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_status_string.argtypes = [ctypes.c_int]
@@ -245,6 +247,16 @@ def ulysses_selftest_wait_timeout(ws, limit_ns, stream=None):
     the workspace status word after limit_ns, without any fault."""
     _check("ulysses_selftest_wait_timeout", lib().ulysses_selftest_wait_timeout(
         _ptr(ws), ws.numel() * ws.element_size(), int(limit_ns), _stream(stream)))
+
+
+def ulysses_selftest_ex2_rate(stream=None) -> float:
+    """Measured base-2 exponentials per SM per cycle (synchronizes)."""
+    cyc = torch.zeros(1, dtype=torch.int64, device="cuda")
+    n, sms = ctypes.c_longlong(0), ctypes.c_int(0)
+    _check("ulysses_selftest_ex2_rate", lib().ulysses_selftest_ex2_rate(
+        _ptr(cyc), 8, ctypes.byref(n), ctypes.byref(sms), _stream(stream)))
+    torch.cuda.synchronize()
+    return n.value / (sms.value * float(cyc.item()))
 
 
 def ulysses_attn_bwd_noalloc(prob, q_head, k_head, v_head, o_head, lse, do_seq, dq_seq, dk_seq,

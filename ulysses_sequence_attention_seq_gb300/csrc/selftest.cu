@@ -1,5 +1,7 @@
 // selftest.cu -- ulysses_selftest_wait_timeout: exercises the kernels' bounded
-// pipeline wait and its status reporting without a fault.
+// pipeline wait and its status reporting without a fault;
+// ulysses_selftest_ex2_rate: measures the SM's base-2 exponential (MUFU)
+// throughput, the secondary bound of the softmax.
 //
 // One CTA initialises an mbarrier that nothing ever arrives on and waits for it
 // with the same bounded wait the attention kernels use (sm100::mbar_wait_bounded),
@@ -32,7 +34,45 @@ __global__ void wait_timeout_kernel(uint32_t *status, unsigned long long limit_n
   }
 }
 
+// Every thread runs 8 independent chains x <- 2^(-x) (x stays in [1/2, 1]) for
+// `iters` steps; thread 0 of each block records the block's elapsed SM cycles.
+// All blocks are resident at once (2 per SM), so the largest is the launch's.
+__global__ void __launch_bounds__(512) ex2_rate_kernel(unsigned long long *cycles, int iters) {
+  float x[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) x[c] = 0.5f + 0.01f * c + 1e-6f * threadIdx.x;
+  __syncthreads();
+  const long long t0 = clock64();
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) x[c] = ulysses::sm100::ex2(-x[c]);
+  }
+  __syncthreads();
+  const long long t1 = clock64();
+  float acc = 0.f;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) acc += x[c];
+  if (threadIdx.x == 0) atomicMax(cycles, (unsigned long long)(t1 - t0) + (acc < 0.f ? 1ull : 0ull));
+}
+
 }  // namespace
+
+extern "C" int ulysses_selftest_ex2_rate(void *cycles, size_t bytes, long long *ex2_per_launch, int *sms,
+                                         ulysses_stream_t stream) {
+  if (!cycles || bytes < 8 || !ex2_per_launch || !sms) return ULYSSES_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(cycles) % 8 != 0) return ULYSSES_ERR_ALIGN;
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess || n <= 0)
+    return ULYSSES_ERR_CUDA;
+  constexpr int kIters = 4096, kThreads = 512, kPerSm = 2;
+  if (cudaMemsetAsync(cycles, 0, 8, (cudaStream_t)stream) != cudaSuccess) return ULYSSES_ERR_CUDA;
+  ex2_rate_kernel<<<n * kPerSm, kThreads, 0, (cudaStream_t)stream>>>(static_cast<unsigned long long *>(cycles),
+                                                                     kIters);
+  *ex2_per_launch = (long long)n * kPerSm * kThreads * kIters * 8;
+  *sms = n;
+  return cudaGetLastError() == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA;
+}
 
 extern "C" int ulysses_selftest_wait_timeout(void *ws, size_t ws_bytes, unsigned long long limit_ns,
                                              ulysses_stream_t stream) {
