@@ -1,0 +1,35 @@
+"""bench.py's CPU legs, no GPU: the reference arm prints the contract's JSON
+line (the fp64 oracle timed on the host), and the oracle leg runs the ring
+hybrid's steps for a hybrid workload."""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_prints_one_contract_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "C2",
+                          "--steps", "1", "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "tokens/s" and d["value"] > 0
+    assert d["higher_is_better"] is True and d["steps"] == 1 and d["warmup"] >= 3
+    assert d["config"]["workload"] == "C2"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_oracle_leg_runs_the_ring_hybrid():
+    sys.path.insert(0, ROOT)
+    import bench
+    from ulysses_sequence_attention_seq_gb300.synthetic import WORKLOADS
+    w = WORKLOADS["C2"].with_(name="C2-ring", P=8, ring=2, n_head=16, n_kv_head=16)
+    ob = bench.OracleBench(w, nthreads=2)
+    t_full, n_rows, pairs, wall = ob.step(8)
+    assert t_full > 0 and 0 < n_rows <= 8 and pairs > 0 and wall > 0
+    assert "2 ring positions" in ob.describe(n_rows)
