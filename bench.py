@@ -40,9 +40,8 @@ METRIC = "tokens/s + attn TFLOP/s (S=32K, 32 heads, P=8 virtual); seq↔head per
 # ------------------------------------------------------------------ helpers
 
 # DRAM bytes (read + write) per launch of a kernel on a workload, from one ncu
-# capture of this build (profiles/launches_c4_fwd_bwd.md and
-# profiles/launches_c4_ring8.md give the commands and the tables); a kernel
-# changed since its capture has no entry.
+# capture of this build (the launch-list summaries under profiles/ give the
+# commands and the tables); a kernel changed since its capture has no entry.
 TRAFFIC = {
     ("attn_fwd", "C4"): 1178681479,
     ("bwd_dkdv", "C4"): 1882669454,
