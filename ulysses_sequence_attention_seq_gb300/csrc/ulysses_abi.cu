@@ -11,9 +11,21 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "internal.h"
 
 namespace ulysses {
+
+// An NVTX range around an entry point's host work (validation and launches),
+// named after the entry point: a profiler's timeline shows which call enqueued
+// which kernels.  Header-only NVTX: without a tool attached it costs a branch.
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange &) = delete;
+  NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -183,6 +195,7 @@ int ulysses_read_status(const void *ws, uint32_t *status, ulysses_stream_t strea
 int ulysses_pack_qkv(const ulysses_problem *prob, const void *q_seq, const void *k_seq,
                      const void *v_seq, void *q_head, void *k_head, void *v_head, void *ws,
                      size_t ws_bytes, ulysses_stream_t stream) {
+  const NvtxRange range("ulysses_pack_qkv");
   int rc = ulysses_validate(prob);
   if (rc) return rc;
   const ulysses_problem &p = *prob;
@@ -198,6 +211,7 @@ int ulysses_pack_qkv(const ulysses_problem *prob, const void *q_seq, const void 
 int ulysses_qkv_proj_pack(const ulysses_problem *prob, const void *x_seq, const void *w_qkv, const void *b_qkv,
                           void *q_head, void *k_head, void *v_head, void *ws, size_t ws_bytes,
                           ulysses_stream_t stream) {
+  const NvtxRange range("ulysses_qkv_proj_pack");
   int rc = ulysses_validate(prob);
   if (rc) return rc;
   const ulysses_problem &p = *prob;
@@ -219,6 +233,7 @@ int ulysses_qkv_proj_pack(const ulysses_problem *prob, const void *x_seq, const 
 
 int ulysses_out_proj_unpack(const ulysses_problem *prob, const void *o_head, const void *w_o, const void *b_o,
                             void *y_seq, void *ws, size_t ws_bytes, ulysses_stream_t stream) {
+  const NvtxRange range("ulysses_out_proj_unpack");
   int rc = ulysses_validate(prob);
   if (rc) return rc;
   const ulysses_problem &p = *prob;
@@ -240,6 +255,7 @@ int ulysses_out_proj_unpack(const ulysses_problem *prob, const void *o_head, con
 int ulysses_attn_fwd(const ulysses_problem *prob, const void *q_head, const void *k_head,
                      const void *v_head, void *o_head, float *lse, void *ws, size_t ws_bytes,
                      ulysses_stream_t stream) {
+  const NvtxRange range("ulysses_attn_fwd");
   int rc = ulysses_validate(prob);
   if (rc) return rc;
   const ulysses_problem &p = *prob;
@@ -265,6 +281,7 @@ int ulysses_attn_fwd(const ulysses_problem *prob, const void *q_head, const void
 int ulysses_attn_fwd_folded(const ulysses_problem *prob, const void *q_seq, const void *k_seq,
                             const void *v_seq, void *o_seq, float *lse, void *ws, size_t ws_bytes,
                             ulysses_stream_t stream) {
+  const NvtxRange range("ulysses_attn_fwd_folded");
   int rc = ulysses_validate(prob);
   if (rc) return rc;
   const ulysses_problem &p = *prob;
@@ -285,6 +302,7 @@ int ulysses_attn_fwd_folded(const ulysses_problem *prob, const void *q_seq, cons
 
 int ulysses_unpack_out(const ulysses_problem *prob, const void *o_head, void *o_seq,
                        ulysses_stream_t stream) {
+  const NvtxRange range("ulysses_unpack_out");
   int rc = ulysses_validate(prob);
   if (rc) return rc;
   const ulysses_problem &p = *prob;
@@ -307,6 +325,7 @@ static int bwd_common(const ulysses_problem *prob, const void *ws, size_t ws_byt
 
 int ulysses_attn_bwd_prepare(const ulysses_problem *prob, const void *o_head, const float *lse,
                              const void *do_seq, void *ws, size_t ws_bytes, ulysses_stream_t stream) {
+  const NvtxRange range("ulysses_attn_bwd_prepare");
   int rc = bwd_common(prob, ws, ws_bytes);
   if (rc) return rc;
   const ulysses_problem &p = *prob;
@@ -324,6 +343,7 @@ int ulysses_attn_bwd_prepare(const ulysses_problem *prob, const void *o_head, co
 int ulysses_attn_bwd_dkdv(const ulysses_problem *prob, const void *q_head, const void *k_head,
                           const void *v_head, void *dk_seq, void *dv_seq, void *ws, size_t ws_bytes,
                           ulysses_stream_t stream) {
+  const NvtxRange range("ulysses_attn_bwd_dkdv");
   int rc = bwd_common(prob, ws, ws_bytes);
   if (rc) return rc;
   const ulysses_problem &p = *prob;
@@ -358,6 +378,7 @@ int ulysses_attn_bwd_dkdv(const ulysses_problem *prob, const void *q_head, const
 
 int ulysses_attn_bwd_dq(const ulysses_problem *prob, const void *q_head, const void *k_head,
                         const void *v_head, void *dq_seq, void *ws, size_t ws_bytes, ulysses_stream_t stream) {
+  const NvtxRange range("ulysses_attn_bwd_dq");
   int rc = bwd_common(prob, ws, ws_bytes);
   if (rc) return rc;
   const ulysses_problem &p = *prob;
@@ -379,6 +400,7 @@ int ulysses_attn_bwd(const ulysses_problem *prob, const void *q_head, const void
                      const void *v_head, const void *o_head, const float *lse,
                      const void *do_seq, void *dq_seq, void *dk_seq, void *dv_seq, void *ws,
                      size_t ws_bytes, ulysses_stream_t stream) {
+  const NvtxRange range("ulysses_attn_bwd");
   int rc = bwd_common(prob, ws, ws_bytes);
   if (rc) return rc;
   const ulysses_problem &p = *prob;
