@@ -266,57 +266,57 @@ __global__ void rope_table_kernel(float *cs, float *sn, int S, int D, double bas
 // dO: seq -> head, plus delta[d][b][j][pos] = sum_e dO * O (O read in head layout)
 // and nlse = -lse * log2(e) at the same index (the exponent offset the backward
 // kernels add to scale * s * log2(e)).
-// A group of D/8 lanes owns one (token, head); bf16 only.
+// One block per token row at a time (grid-stride over rows): the row's index
+// arithmetic is done once, and its H*D/8 (head, 16-byte chunk) tasks are
+// spread over the block's threads, D/8 consecutive lanes per head; bf16 only.
 __global__ void __launch_bounds__(kThreads)
     pack_do_delta_kernel(const __nv_bfloat16 *__restrict__ dout, const __nv_bfloat16 *__restrict__ o,
                          const float *__restrict__ lse, __nv_bfloat16 *__restrict__ do_head,
                          float *__restrict__ delta, float *__restrict__ nlse, int P, int B,
                          int Sl, int H, int D, int Pu, int Cs) {
   const int hp = H / Pu;
-  const int lanes = D / 8;  // 8 or 16: divides 32
-  const long long groups = (long long)P * B * Sl * H;
-  const int lane = threadIdx.x & 31;
-  const int c = lane % lanes;
-  // The loop bound is uniform across the warp so that the shuffles below see
-  // every lane: a warp always covers 32/lanes consecutive groups.
-  const long long warp_first = ((blockIdx.x * (long long)kThreads + threadIdx.x) & ~31ll) / lanes;
-  const long long gstride = (long long)gridDim.x * kThreads / lanes;
-  for (long long wg = warp_first; wg < groups; wg += gstride) {
-    const long long gid = wg + lane / lanes;
-    const bool live = gid < groups;
-    float acc = 0.f;
-    long long head_row = 0;
-    int d = 0, b = 0, j = 0, pos = 0, crow = 0;
-    if (live) {
-      const int g = (int)(gid % H);
-      const long long row = gid / H;
-      const int t = (int)(row % Sl);
-      const long long sb = row / Sl;
-      b = (int)(sb % B);
-      const int s = (int)(sb / B);
-      pos = s * Sl + t;
-      const int rp = s / Pu;  // ring position; the token's row in its chunk:
-      crow = pos - rp * Cs;
-      d = rp * Pu + g / hp;   // the head-layout rank holding head g of the token
-      j = g % hp;
-      head_row = (((long long)(d * B + b) * Cs + crow) * hp + j) * D;
-      const uint4 x = __ldg(reinterpret_cast<const uint4 *>(dout + gid * D + c * 8));
-      const uint4 y = __ldg(reinterpret_cast<const uint4 *>(o + head_row + c * 8));
-      *reinterpret_cast<uint4 *>(do_head + head_row + c * 8) = x;
-      const __nv_bfloat162 *px = reinterpret_cast<const __nv_bfloat162 *>(&x);
-      const __nv_bfloat162 *py = reinterpret_cast<const __nv_bfloat162 *>(&y);
+  const int lanes = D / 8;  // 8 or 16: divides 32 and kThreads
+  const int tasks = H * lanes;
+  const long long rows = (long long)P * B * Sl;
+  const int c = threadIdx.x % lanes;
+  for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
+    // row = (s*B + b)*Sl + t: token t of sequence shard s, batch b
+    const int t = (int)(row % Sl);
+    const long long sb = row / Sl;
+    const int b = (int)(sb % B);
+    const int s = (int)(sb / B);
+    const int pos = s * Sl + t;
+    const int rp = s / Pu;              // ring position; the token's row in its chunk:
+    const int crow = pos - rp * Cs;
+    // The trip count is uniform over the block, so the shuffles below see
+    // every lane of every warp.
+    for (int base = 0; base < tasks; base += kThreads) {
+      const int task = base + (int)threadIdx.x;
+      const bool live = task < tasks;
+      const int g = task / lanes;       // head (global)
+      const int d = rp * Pu + g / hp;   // the head-layout rank holding head g of the token
+      const int j = g % hp;
+      float acc = 0.f;
+      if (live) {
+        const long long head_row = (((long long)(d * B + b) * Cs + crow) * hp + j) * D;
+        const uint4 x = __ldg(reinterpret_cast<const uint4 *>(dout + (row * H + g) * D + c * 8));
+        const uint4 y = __ldg(reinterpret_cast<const uint4 *>(o + head_row + c * 8));
+        *reinterpret_cast<uint4 *>(do_head + head_row + c * 8) = x;
+        const __nv_bfloat162 *px = reinterpret_cast<const __nv_bfloat162 *>(&x);
+        const __nv_bfloat162 *py = reinterpret_cast<const __nv_bfloat162 *>(&y);
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        float2 a = __bfloat1622float2(px[w]), bb = __bfloat1622float2(py[w]);
-        acc = fmaf(a.x, bb.x, acc);
-        acc = fmaf(a.y, bb.y, acc);
+        for (int w = 0; w < 4; ++w) {
+          float2 a = __bfloat1622float2(px[w]), bb = __bfloat1622float2(py[w]);
+          acc = fmaf(a.x, bb.x, acc);
+          acc = fmaf(a.y, bb.y, acc);
+        }
       }
-    }
-    for (int off = lanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (live && c == 0) {
-      const long long idx = ((long long)(d * B + b) * hp + j) * Cs + crow;
-      delta[idx] = acc;
-      nlse[idx] = -lse[idx] * 1.4426950408889634f;
+      for (int off = lanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (live && c == 0) {
+        const long long idx = ((long long)(d * B + b) * hp + j) * Cs + crow;
+        delta[idx] = acc;
+        nlse[idx] = -lse[idx] * 1.4426950408889634f;
+      }
     }
   }
 }
@@ -427,10 +427,7 @@ cudaError_t launch_unpack(const ulysses_problem &p, const void *o_head, void *o_
 cudaError_t launch_pack_do_delta(const ulysses_problem &p, const void *do_seq, const void *o_head,
                                  const float *lse, void *do_head, float *delta, float *nlse,
                                  cudaStream_t st) {
-  const long long groups = (long long)p.B * p.S * p.n_head;
-  const int lanes = p.head_dim / 8;
-  long long blocks = (groups * lanes + kThreads - 1) / kThreads;
-  int grid = grid_for(blocks);
+  const int grid = grid_for((long long)p.B * p.S);  // one token row per block at a time
   pack_do_delta_kernel<<<grid, kThreads, 0, st>>>(
       static_cast<const __nv_bfloat16 *>(do_seq), static_cast<const __nv_bfloat16 *>(o_head),
       lse, static_cast<__nv_bfloat16 *>(do_head), delta, nlse, p.P, p.B, p.S / p.P, p.n_head,
