@@ -559,20 +559,21 @@ static_assert(128 * kRegsQProducer + 256 * kRegsQSoftmax <= 384 * 168, "register
 constexpr int kKSlots = 3, kVSlots = 3;
 
 enum : uint32_t {
-  kQBarQReady = 0,   // 256 arrivals: Q and dO are in TMEM
-  kQBarKFull = 8,    // [3]
-  kQBarKEmpty = 32,  // [3]
-  kQBarVFull = 56,   // [3]
-  kQBarVEmpty = 80,  // [3]
-  kQBarSFull = 104,
-  kQBarSFree = 112,  // 256 arrivals
-  kQBarDPFull = 120,
-  kQBarDSFull = 128, // 256 arrivals
-  kQBarAcc = 136,
-  kQBarDrain = 144,
-  kQTmemSlot = 152,
-  kQAbortSlot = 156
+  kQBarQReady = 0,                         // 256 arrivals: Q and dO are in TMEM
+  kQBarKFull = 8,                          // [kKSlots]
+  kQBarKEmpty = kQBarKFull + 8 * kKSlots,  // [kKSlots]
+  kQBarVFull = kQBarKEmpty + 8 * kKSlots,  // [kVSlots]
+  kQBarVEmpty = kQBarVFull + 8 * kVSlots,  // [kVSlots]
+  kQBarSFull = kQBarVEmpty + 8 * kVSlots,
+  kQBarSFree = kQBarSFull + 8,             // 256 arrivals
+  kQBarDPFull = kQBarSFree + 8,
+  kQBarDSFull = kQBarDPFull + 8,           // 256 arrivals
+  kQBarAcc = kQBarDSFull + 8,
+  kQBarDrain = kQBarAcc + 8,
+  kQTmemSlot = kQBarDrain + 8,
+  kQAbortSlot = kQTmemSlot + 4
 };
+static_assert(kQAbortSlot + 4 <= 256, "dQ barrier block");
 
 template <int D>
 struct QLayout {
