@@ -133,6 +133,13 @@ int ulysses_workspace_init(const ulysses_problem *prob, void *ws, size_t ws_byte
 /* Copies the workspace status word to *status (synchronises `stream`). */
 int ulysses_read_status(const void *ws, uint32_t *status, ulysses_stream_t stream);
 
+/* Enqueues the same copy on `stream` without synchronising: *status holds the
+ * word once the stream has reached this point (the caller waits on the stream
+ * or an event recorded after this call).  `status` should be pinned host
+ * memory (cudaHostAlloc / torch pin_memory) for the copy to stay asynchronous.
+ * Errors: ULYSSES_ERR_ARG (NULL pointer), ULYSSES_ERR_CUDA. */
+int ulysses_read_status_async(const void *ws, uint32_t *status, ulysses_stream_t stream);
+
 /*
  * Seq -> head All-to-All of Q, K and V, RoPE fused ("Sequence Parallelism II",
  * §1 ownership example and §3; "Comparing Ulysses and Megatron Sequence

@@ -139,6 +139,12 @@ def test_pointer_checks_fail_before_launch(lib):
     assert lib.ulysses_attn_bwd(ctypes.byref(pf.c()), *[vp(base + i * nq) for i in range(10)], nws, vp(0)) == -4
 
 
+def test_read_status_argument_checks(lib):
+    vp = ctypes.c_void_p
+    assert lib.ulysses_read_status_async(vp(0), vp(0x10000), vp(0)) == -1
+    assert lib.ulysses_read_status_async(vp(0x10000), vp(0), vp(0)) == -1
+
+
 def test_selftest_ex2_rate_argument_checks(lib):
     vp = ctypes.c_void_p
     fn = lib.ulysses_selftest_ex2_rate

@@ -19,7 +19,10 @@ def test_bounded_wait_times_out_and_is_reported():
     good = run.buf.o_seq.clone()
 
     U.ulysses_selftest_wait_timeout(run.buf.ws, 20_000_000)   # 20 ms
+    word = torch.zeros(1, dtype=torch.int32).pin_memory()
+    U.ulysses_read_status_async(run.buf.ws, word)             # enqueued behind the self-test
     torch.cuda.synchronize()
+    assert int(word.item()) & U.STATUS_FWD_TIMEOUT
     assert U.ulysses_read_status(run.buf.ws) & U.STATUS_FWD_TIMEOUT
 
     # with a timeout bit set the attention kernel does not start: O is left alone

@@ -116,6 +116,7 @@ def lib():
         L.ulysses_workspace_bytes.restype = sz
         L.ulysses_workspace_init.argtypes = [P, vp, sz, vp]
         L.ulysses_read_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
+        L.ulysses_read_status_async.argtypes = [vp, vp, vp]
         L.ulysses_pack_qkv.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_attn_fwd.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_unpack_out.argtypes = [P, vp, vp, vp]
@@ -172,6 +173,14 @@ def ulysses_read_status(ws: torch.Tensor, stream=None) -> int:
     out = ctypes.c_uint32(0)
     _check("ulysses_read_status", lib().ulysses_read_status(_ptr(ws), ctypes.byref(out), _stream(stream)))
     return out.value
+
+
+def ulysses_read_status_async(ws: torch.Tensor, out: torch.Tensor, stream=None):
+    """Enqueue a copy of the status word into `out` (a pinned uint32/int32
+    host tensor of at least one element) on the stream; no synchronisation."""
+    if out.device.type != "cpu" or out.element_size() != 4 or out.numel() < 1:
+        raise ValueError("out must be a 4-byte host tensor")
+    _check("ulysses_read_status_async", lib().ulysses_read_status_async(_ptr(ws), _ptr(out), _stream(stream)))
 
 
 def ulysses_pack_qkv(prob, q_seq, k_seq, v_seq, q_head, k_head, v_head, ws, stream=None):

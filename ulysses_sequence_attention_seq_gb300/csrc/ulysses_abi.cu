@@ -184,6 +184,11 @@ int ulysses_workspace_init(const ulysses_problem *prob, void *ws, size_t ws_byte
   return cuda_rc(launch_rope_table(*prob, ws, (cudaStream_t)stream));
 }
 
+int ulysses_read_status_async(const void *ws, uint32_t *status, ulysses_stream_t stream) {
+  if (!ws || !status) return ULYSSES_ERR_ARG;
+  return cuda_rc(cudaMemcpyAsync(status, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost, (cudaStream_t)stream));
+}
+
 int ulysses_read_status(const void *ws, uint32_t *status, ulysses_stream_t stream) {
   if (!ws || !status) return ULYSSES_ERR_ARG;
   cudaError_t e = cudaMemcpyAsync(status, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost,
