@@ -158,6 +158,28 @@ def test_forward_workloads(name):
             assert torch.equal(o_seq[d][:, :, s * hp * w.head_dim:(s + 1) * hp * w.head_dim], blk)
 
 
+def test_forward_at_the_longest_sequence():
+    """The pages' model at S = 131072 over P = 32 ranks (one head per rank; the
+    largest sequence of the permutation sweep): sampled query rows of every
+    head, each exact over its full key range, and the unpack inverting what the
+    kernel wrote.  Exercises the index arithmetic at 4M (position, head) rows
+    per tensor."""
+    w = WORKLOADS["C5"].with_(name="C5-128K", S=131072, seed=1008)
+    run = GpuRun(w, backward=False)
+    run.forward()
+    x = oracle_inputs(run.inputs)
+    rows = sample_rows(w, 12, seed=4)
+    want = oracle.forward(oracle_problem(w), x["q"], x["k"], x["v"], rows=rows)
+    got_h = to64(run.buf.o_head)
+    assert_close(got_h[:, :, rows], np.stack(want["o_head"])[:, :, rows], w, "C5-128K o_head")
+    assert np.abs(to64(run.buf.lse)[..., rows] - np.stack(want["lse"])[..., rows]).max() <= LSE_BF16_MAX_ABS
+    o_seq, o_head = run.buf.o_seq, run.buf.o_head
+    for d in (0, w.P - 1):
+        for s in (0, w.P - 1):
+            blk = o_head[s][:, d * w.Sl:(d + 1) * w.Sl].reshape(w.B, w.Sl, w.head_dim)
+            assert torch.equal(o_seq[d][:, :, s * w.head_dim:(s + 1) * w.head_dim], blk)
+
+
 def test_forward_is_deterministic():
     w = wl(4, 1, 1024, 8, 4, 128)
     run = GpuRun(w)
