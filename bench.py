@@ -611,6 +611,8 @@ def main():
         "attn_bwd_flops_note": "backward algorithmic FLOPs = 2x forward (dV, dP, dQ, dK); the QK^T recompute is not counted",
         "pack_gbs": pack_gbs, "unpack_gbs": unpack_gbs,
         "kernel_ms": per,
+        "kernel_ms_median": {k: statistics.median(v) for k, v in r["per"].items()},
+        "kernel_ms_min": {k: min(v) for k, v in r["per"].items()},
         "tensor_kernels": kernels,
         "roofline": {"bound": "tensor", "achieved": dk["achieved_tflops"], "peak": tf_sust, "unit": "TFLOP/s",
                      "frac": dk["frac"], "traffic": TRAFFIC.get((dominant, w.name)),
