@@ -70,9 +70,12 @@ enum ulysses_device_status {
   ULYSSES_STATUS_FWD_TIMEOUT = 1u << 0,  /* attention forward: a pipeline wait gave up */
   ULYSSES_STATUS_BWD_TIMEOUT = 1u << 1,  /* attention backward: a pipeline wait gave up */
   ULYSSES_STATUS_ROPE_TABLE = 1u << 2,   /* RoPE table missing or built for another problem */
-  ULYSSES_STATUS_SMEM_ALIGN = 1u << 3    /* a kernel's dynamic shared memory did not start on a
+  ULYSSES_STATUS_SMEM_ALIGN = 1u << 3,   /* a kernel's dynamic shared memory did not start on a
                                             1024-byte boundary and its tiles did not fit behind
                                             the padding: that kernel wrote nothing */
+  ULYSSES_STATUS_BOUNDS = 1u << 4        /* range-checked builds only (compiled with
+                                            ULYSSES_CHECK_BOUNDS): a global load or store fell
+                                            outside its buffer and was skipped */
 };
 
 /*

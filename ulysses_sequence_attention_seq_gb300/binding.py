@@ -16,12 +16,13 @@ from typing import Optional
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libulysses.so")
+# ULYSSES_LIB selects another build of the library (the range-checked one).
+LIB_PATH = os.environ.get("ULYSSES_LIB") or os.path.join(_HERE, "_build", "libulysses.so")
 _lib = None
 
 BF16, FP32 = 0, 1
 OK = 0
-STATUS_FWD_TIMEOUT, STATUS_BWD_TIMEOUT, STATUS_ROPE_TABLE, STATUS_SMEM_ALIGN = 1, 2, 4, 8
+STATUS_FWD_TIMEOUT, STATUS_BWD_TIMEOUT, STATUS_ROPE_TABLE, STATUS_SMEM_ALIGN, STATUS_BOUNDS = 1, 2, 4, 8, 16
 
 EXPORTS = ("ulysses_validate", "ulysses_workspace_bytes", "ulysses_workspace_init",
            "ulysses_read_status", "ulysses_pack_qkv", "ulysses_attn_fwd", "ulysses_unpack_out",

@@ -32,6 +32,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include "check.cuh"
 #include "internal.h"
 #include "sm100.cuh"
 #include "tmap.h"
@@ -64,6 +65,10 @@ struct BwdParams {
   // over the full sequence; the rows at global position pos live in the
   // head-layout buffer of rank (pos / Cs) * Pu + member, row pos % Cs.
   int Pu, Cs;
+  // Elements of the buffers the kernels read or write with plain loads and
+  // stores (range checks of a checked build): dQ, dK / dV (or their float
+  // partials), Q / dO in head layout, the nlse / delta rows, the RoPE table.
+  long long dq_n, dkv_n, qo_n, rows_n, rope_n;
 };
 
 // Head-layout (rank * B + batch) of the rows at global position `pos` for the
@@ -478,6 +483,7 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
       const size_t prow = (size_t)hl_outer(p, rb, kr) * p.Cs + kr % p.Cs;
       float *pv = reinterpret_cast<float *>(p.dv) + prow * D;
       float *pk = reinterpret_cast<float *>(p.dk) + prow * D;
+      const bool put = live && in_range(p.status, (long long)(prow * D), D, p.dkv_n);
       // warpgroup g owns columns [g*D/2, (g+1)*D/2) of both accumulators; the
       // TMEM loads are warp-wide, only the stores depend on the row
 #pragma unroll
@@ -487,7 +493,7 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
         tmem_ld32(tdV + lane_base + col, x);
         tmem_ld32(tdK + lane_base + col, y);
         tmem_wait_ld();
-        if (live) {
+        if (put) {
 #pragma unroll
           for (int v = 0; v < 8; ++v) {
             reinterpret_cast<uint4 *>(pv + col)[v] = make_uint4(x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]);
@@ -501,6 +507,8 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
       const int s_rank = kvr / p.Sl, t = kvr - s_rank * p.Sl;
       const int rr = rb / p.B, bb = rb - rr * p.B;
       const size_t row = (((size_t)(s_rank * p.B + bb) * p.Sl + t) * p.n_kv + (rr * p.kvp + kl)) * D;
+      const bool put = live && in_range(p.status, (long long)row, D, p.dkv_n) &&
+                       (!p.rope_cos || in_range(p.status, (long long)kvr * (D / 2), D / 2, p.rope_n));
       // dV: warpgroup g owns columns [g*D/2, (g+1)*D/2)
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
@@ -508,7 +516,7 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
         const int col = g * (D / 2) + c * 32;
         tmem_ld32(tdV + lane_base + col, x);
         tmem_wait_ld();
-        if (live) store_plain(p.dv + row + col, x, 1.0f);
+        if (put) store_plain(p.dv + row + col, x, 1.0f);
       }
       // dK: rotation pairs (i, i + D/2); warpgroup g owns i in [g*32, g*32+32)
       // for D = 128, warpgroup 0 owns all 32 pairs for D = 64.
@@ -518,7 +526,7 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
         tmem_ld32(tdK + lane_base + i0, x);
         tmem_ld32(tdK + lane_base + D / 2 + i0, y);
         tmem_wait_ld();
-        if (live) {
+        if (put) {
           const float *cs = p.rope_cos ? p.rope_cos + (size_t)kvr * (D / 2) + i0 : nullptr;
           const float *sn = p.rope_sin ? p.rope_sin + (size_t)kvr * (D / 2) + i0 : nullptr;
           store_unrotated(p.dk + row + i0, p.dk + row + D / 2 + i0, x, y, p.scale, cs, sn);
@@ -789,15 +797,16 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       // Warpgroup 0 copies this thread's Q row, warpgroup 1 its dO row, into
       // TMEM (rows past S are zero).
       const int qr = live ? qi : 0;
-      const __nv_bfloat16 *src =
-          (g == 0 ? p.q : p.dout) + (((size_t)hl_outer(p, rb, qr) * p.Cs + qr % p.Cs) * p.hp + j) * D;
+      const size_t qoff = (((size_t)hl_outer(p, rb, qr) * p.Cs + qr % p.Cs) * p.hp + j) * D;
+      const __nv_bfloat16 *src = (g == 0 ? p.q : p.dout) + qoff;
       const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+      const bool get = live && in_range(p.status, (long long)qoff, D, p.qo_n);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         uint32_t x[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
-          const uint4 u = live ? __ldg(s4 + c * 8 + v) : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 u = get ? __ldg(s4 + c * 8 + v) : make_uint4(0u, 0u, 0u, 0u);
           x[4 * v] = u.x;
           x[4 * v + 1] = u.y;
           x[4 * v + 2] = u.z;
@@ -811,8 +820,9 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
     }
     const int qr = live ? qi : 0;
     const size_t lrow = ((size_t)hl_outer(p, rb, qr) * p.hp + j) * p.Cs + qr % p.Cs;
-    const float nl2 = live ? p.nlse[lrow] : 0.f;
-    const float dlt = live ? p.delta[lrow] : 0.f;
+    const bool get_row = live && in_range(p.status, (long long)lrow, 1, p.rows_n);
+    const float nl2 = get_row ? p.nlse[lrow] : 0.f;
+    const float dlt = get_row ? p.delta[lrow] : 0.f;
     bool ok = true;
     for (int i = 0; i < n_kv; ++i) {
       if (!warp_wait(bar + kQBarSFull, i & 1, abort_flag, gst)) { ok = false; break; }
@@ -875,7 +885,8 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       tmem_ld32(tdQ + lane_base + i0, x);
       tmem_ld32(tdQ + lane_base + D / 2 + i0, y);
       tmem_wait_ld();
-      if (live) {
+      if (live && in_range(p.status, (long long)row, D, p.dq_n) &&
+          (!p.rope_cos || in_range(p.status, (long long)qi * (D / 2), D / 2, p.rope_n))) {
         const float *cs = p.rope_cos ? p.rope_cos + (size_t)qi * (D / 2) + i0 : nullptr;
         const float *sn = p.rope_sin ? p.rope_sin + (size_t)qi * (D / 2) + i0 : nullptr;
         store_unrotated(p.dq + row + i0, p.dq + row + D / 2 + i0, x, y, p.scale, cs, sn);
@@ -924,6 +935,11 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   bp.n_kv = p.n_kv_head;
   bp.Pu = Pu;
   bp.Cs = Cs;
+  bp.dq_n = (long long)p.B * p.S * p.n_head * D;
+  bp.dkv_n = kv_replicas(p) > 1 ? (long long)p.P * p.B * Cs * D : (long long)p.B * p.S * p.n_kv_head * D;
+  bp.qo_n = (long long)p.B * p.S * p.n_head * D;
+  bp.rows_n = (long long)p.B * p.n_head * p.S;
+  bp.rope_n = (long long)p.S * (D / 2);
   // CTA units: (group member, batch, head), each over the full sequence.
   const int UB = Pu * p.B;
   // dK/dV CTAs of a kv-head stream the Q and dO of its q-heads; dQ CTAs of a

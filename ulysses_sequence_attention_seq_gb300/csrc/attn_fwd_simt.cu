@@ -9,6 +9,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include "check.cuh"
 #include "internal.h"
 
 namespace ulysses {
@@ -21,7 +22,7 @@ template <int D>
 __global__ void __launch_bounds__(kRows) attn_fwd_simt_kernel(
     const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
     float *__restrict__ o, float *__restrict__ lse, int S, int hp, int kvp, int group, int causal,
-    float scale_log2) {
+    float scale_log2, uint32_t *status, long long qo_n, long long kv_n, long long lse_n) {
   __shared__ float Ks[kKeys][D];
   __shared__ float Vs[kKeys][D];
   const int n_qt = (S + kRows - 1) / kRows;
@@ -34,10 +35,12 @@ __global__ void __launch_bounds__(kRows) attn_fwd_simt_kernel(
   const bool live = i < S;
 
   float qr[D], acc[D];
-  const float *qrow = q + ((rb * S + (live ? i : 0)) * hp + j) * D;
+  const long long qoff = ((rb * S + (live ? i : 0)) * hp + j) * D;
+  const float *qrow = q + qoff;
+  const bool get = live && in_range(status, qoff, D, qo_n);
 #pragma unroll
   for (int e = 0; e < D; ++e) {
-    qr[e] = live ? qrow[e] : 0.f;
+    qr[e] = get ? qrow[e] : 0.f;
     acc[e] = 0.f;
   }
   float m = -INFINITY, l = 0.f;
@@ -49,7 +52,7 @@ __global__ void __launch_bounds__(kRows) attn_fwd_simt_kernel(
     for (int idx = threadIdx.x; idx < kKeys * D; idx += kRows) {
       const int rr = idx / D, e = idx % D;
       const int kk = k0 + rr;
-      const bool in = kk < S;
+      const bool in = kk < S && in_range(status, (rb * S * kvp + kl) * D + (long long)kk * kvp * D + e, 1, kv_n);
       Ks[rr][e] = in ? kbase[(long long)kk * kvp * D + e] : 0.f;
       Vs[rr][e] = in ? vbase[(long long)kk * kvp * D + e] : 0.f;
     }
@@ -77,16 +80,22 @@ __global__ void __launch_bounds__(kRows) attn_fwd_simt_kernel(
   }
   if (!live) return;
   const float inv = 1.f / l;
-  float *orow = o + ((rb * S + i) * hp + j) * D;
+  const long long ooff = ((rb * S + i) * hp + j) * D;
+  float *orow = o + ooff;
+  if (in_range(status, ooff, D, qo_n)) {
 #pragma unroll
-  for (int e = 0; e < D; ++e) orow[e] = acc[e] * inv;
-  lse[hid * S + i] = (m + log2f(l)) * 0.69314718055994530942f;
+    for (int e = 0; e < D; ++e) orow[e] = acc[e] * inv;
+  }
+  if (in_range(status, hid * S + i, 1, lse_n)) lse[hid * S + i] = (m + log2f(l)) * 0.69314718055994530942f;
 }
 
 }  // namespace
 
 cudaError_t launch_attn_fwd_simt(const ulysses_problem &p, const float *q, const float *k,
-                                 const float *v, float *o, float *lse, cudaStream_t st) {
+                                 const float *v, float *o, float *lse, uint32_t *status, cudaStream_t st) {
+  const long long qo_n = (long long)p.B * p.S * p.n_head * p.head_dim;
+  const long long kv_n = (long long)p.P * p.B * p.S * kv_per_rank(p) * p.head_dim;
+  const long long lse_n = (long long)p.B * p.n_head * p.S;
   const int hp = p.n_head / p.P, kvp = kv_per_rank(p), group = hp / kvp;
   const int n_qt = (p.S + kRows - 1) / kRows;
   const long long blocks = (long long)n_qt * p.P * p.B * hp;
@@ -95,13 +104,16 @@ cudaError_t launch_attn_fwd_simt(const ulysses_problem &p, const float *q, const
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
   switch (p.head_dim) {
     case 32:
-      attn_fwd_simt_kernel<32><<<(unsigned)blocks, kRows, 0, st>>>(q, k, v, o, lse, p.S, hp, kvp, group, p.causal, scale_log2);
+      attn_fwd_simt_kernel<32><<<(unsigned)blocks, kRows, 0, st>>>(q, k, v, o, lse, p.S, hp, kvp, group, p.causal, scale_log2,
+                                                                  status, qo_n, kv_n, lse_n);
       break;
     case 64:
-      attn_fwd_simt_kernel<64><<<(unsigned)blocks, kRows, 0, st>>>(q, k, v, o, lse, p.S, hp, kvp, group, p.causal, scale_log2);
+      attn_fwd_simt_kernel<64><<<(unsigned)blocks, kRows, 0, st>>>(q, k, v, o, lse, p.S, hp, kvp, group, p.causal, scale_log2,
+                                                                  status, qo_n, kv_n, lse_n);
       break;
     case 128:
-      attn_fwd_simt_kernel<128><<<(unsigned)blocks, kRows, 0, st>>>(q, k, v, o, lse, p.S, hp, kvp, group, p.causal, scale_log2);
+      attn_fwd_simt_kernel<128><<<(unsigned)blocks, kRows, 0, st>>>(q, k, v, o, lse, p.S, hp, kvp, group, p.causal, scale_log2,
+                                                                  status, qo_n, kv_n, lse_n);
       break;
     default:
       return cudaErrorInvalidValue;

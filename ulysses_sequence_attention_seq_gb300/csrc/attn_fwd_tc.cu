@@ -54,6 +54,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include "check.cuh"
 #include "internal.h"
 #include "sm100.cuh"
 #include "tmap.h"
@@ -119,6 +120,7 @@ struct FwdParams {
   float scale_log2;
   __nv_bfloat16 *o;  // [P][B][S][hp][D], or [P][B][Sl][H] when folded
   float *lse;        // [P][B][hp][S]
+  long long o_n, lse_n;  // their elements (range checks of a checked build)
   uint32_t *status;
 };
 
@@ -449,18 +451,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const float inv = 1.0f / l;
       __nv_bfloat16 *orow;
+      size_t ooff;
       if (!p.folded) {  // rank (qpos / Cs) * Pu + member, row qpos % Cs
-        orow = p.o + ((((size_t)(qpos / p.Cs) * p.Pu * p.B + rb) * p.Cs + qpos % p.Cs) * p.hp + j) * D;
+        ooff = ((((size_t)(qpos / p.Cs) * p.Pu * p.B + rb) * p.Cs + qpos % p.Cs) * p.hp + j) * D;
       } else {  // token qpos of rank qpos/Sl, global head r*hp + j
         const int r = rb / p.B, b = rb - r * p.B, dst = qpos / p.Sl;
-        orow = p.o + (((size_t)(dst * p.B + b) * p.Sl + (qpos - dst * p.Sl)) * p.n_head + r * p.hp + j) * D;
+        ooff = (((size_t)(dst * p.B + b) * p.Sl + (qpos - dst * p.Sl)) * p.n_head + r * p.hp + j) * D;
       }
+      orow = p.o + ooff;
+      const bool store = qpos < p.S && in_range(p.status, (long long)ooff, D, p.o_n);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(tO + c * 32, r);
         tmem_wait_ld();
-        if (qpos < p.S) {
+        if (store) {
           uint32_t w[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
@@ -473,7 +478,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (qpos < p.S) {
         const size_t hr = (size_t)(qpos / p.Cs) * p.Pu * p.B + rb;  // head-layout rank * B + b
-        p.lse[(hr * p.hp + j) * p.Cs + qpos % p.Cs] = (m_used + log2f(l)) * 0.69314718055994530942f;
+        const size_t li = (hr * p.hp + j) * p.Cs + qpos % p.Cs;
+        if (in_range(p.status, (long long)li, 1, p.lse_n))
+          p.lse[li] = (m_used + log2f(l)) * 0.69314718055994530942f;
       }
     }
   }
@@ -523,6 +530,8 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   fp.head_group = l2_head_group((size_t)4 * p.S * D / fp.group, units, (long long)fp.n_pairs * units);
   fp.o = static_cast<__nv_bfloat16 *>(o);
   fp.lse = lse;
+  fp.o_n = (long long)p.B * p.S * p.n_head * D;  // O in head or sequence layout: the same elements
+  fp.lse_n = (long long)p.B * p.n_head * p.S;
   fp.status = status;
   const long long blocks = (long long)fp.n_pairs * units;
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;

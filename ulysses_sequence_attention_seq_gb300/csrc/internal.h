@@ -60,7 +60,7 @@ cudaError_t launch_unpack(const ulysses_problem &p, const void *o_head, void *o_
 // per (rank, b, head, row).
 cudaError_t launch_pack_do_delta(const ulysses_problem &p, const void *do_seq, const void *o_head,
                                  const float *lse, void *do_head, float *delta, float *nlse,
-                                 cudaStream_t st);
+                                 uint32_t *status, cudaStream_t st);
 // Replicated kv-heads: dk_seq/dv_seq (bf16, sequence layout) = the sum over
 // each kv-head's replicas of their float partials, in rank order; dK also
 // scaled by `scale` and rotated back by the RoPE angle of its position.
@@ -78,7 +78,7 @@ struct TmaEncoder {
 bool get_tma_encoder(TmaEncoder *enc);
 
 cudaError_t launch_attn_fwd_simt(const ulysses_problem &p, const float *q, const float *k,
-                                 const float *v, float *o, float *lse, cudaStream_t st);
+                                 const float *v, float *o, float *lse, uint32_t *status, cudaStream_t st);
 // folded: q/k/v are the sequence-sharded buffers and o is written in sequence
 // layout (requires S/P % 128 == 0).
 cudaError_t launch_attn_fwd_tc(const ulysses_problem &p, const TmaEncoder &enc, const void *q,

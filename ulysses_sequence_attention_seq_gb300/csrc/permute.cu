@@ -25,6 +25,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "check.cuh"
 #include "internal.h"
 #include "sm100.cuh"
 
@@ -40,6 +41,7 @@ struct PermJob {
   int heads;        // heads of this tensor
   int rope;         // 0: copy; +1: rotate by +angle; -1: rotate by -angle
   int rep;          // > 1: heads < P and every head goes to `rep` ranks (rank d gets head d / rep)
+  long long src_n, dst_n;  // elements of each side (range checks of a checked build)
 };
 
 struct PermParams {
@@ -52,6 +54,7 @@ struct PermParams {
   const uint32_t *rope_key_ptr;
   uint32_t rope_key;
   uint32_t *status;
+  long long rope_n;  // floats in each of cos, sin
 };
 
 __device__ __forceinline__ void rotate(float &x, float &y, float c, float s, int dir) {
@@ -155,12 +158,14 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const PermParams p) {
         const T *src = static_cast<const T *>(J.src);
         T *dst = static_cast<T *>(J.dst);
         const int half = p.D / 2;
+        const long long toff = (long long)pos * half + (long long)c * V;
+        // a unit spans [off, off + D/2 + V) of each side
+        if (!in_range(p.status, src_off, half + V, J.src_n) || !in_range(p.status, dst_off, half + V, J.dst_n) ||
+            (J.rope && !in_range(p.status, toff, V, p.rope_n)))
+          continue;
         uint4 x = __ldg(reinterpret_cast<const uint4 *>(src + src_off));
         uint4 y = __ldg(reinterpret_cast<const uint4 *>(src + src_off + half));
-        if (J.rope) {
-          const long long toff = (long long)pos * half + (long long)c * V;
-          Chunk<T>::rope(x, y, p.rope_cos + toff, p.rope_sin + toff, J.rope);
-        }
+        if (J.rope) Chunk<T>::rope(x, y, p.rope_cos + toff, p.rope_sin + toff, J.rope);
         *reinterpret_cast<uint4 *>(dst + dst_off) = x;
         *reinterpret_cast<uint4 *>(dst + dst_off + half) = y;
       }
@@ -209,9 +214,12 @@ __global__ void __launch_bounds__(32) unpack_bulk_kernel(const PermParams p, uin
     if (lane == 0) mbar_arrive_expect_tx(bar, row_bytes);
     __syncwarp();
     // member r of the ring position holds heads [r*hp, (r+1)*hp) of the token
-    for (int r = lane; r < p.Pu; r += 32)
-      bulk_load(stage + r * piece, src + (((long long)((rp * p.Pu + r) * p.B + b) * p.Cs + crow) * hp) * p.D,
-                piece, bar);
+    for (int r = lane; r < p.Pu; r += 32) {
+      const long long off = (((long long)((rp * p.Pu + r) * p.B + b) * p.Cs + crow) * hp) * p.D;
+      // a skipped piece leaves the stage's transaction count short: that
+      // stage's wait then times out and reports, as the check already has
+      if (in_range(p.status, off, (long long)hp * p.D, J.src_n)) bulk_load(stage + r * piece, src + off, piece, bar);
+    }
   };
   long long issued = -1, failed = n_mine;
   for (long long k = 0; k < kBulkStages - 1 && k < n_mine; ++k) load_row(issued = k);
@@ -229,7 +237,8 @@ __global__ void __launch_bounds__(32) unpack_bulk_kernel(const PermParams p, uin
     failed = n_mine;
     if (lane == 0) {
       const long long row = blockIdx.x + k * gridDim.x;
-      bulk_store(dst + row * (long long)J.heads * p.D, sbase + (uint32_t)(k % kBulkStages) * row_bytes, row_bytes);
+      if (in_range(p.status, row * J.heads * p.D, (long long)J.heads * p.D, J.dst_n))
+        bulk_store(dst + row * (long long)J.heads * p.D, sbase + (uint32_t)(k % kBulkStages) * row_bytes, row_bytes);
       bulk_commit();
     }
   }
@@ -273,7 +282,9 @@ __global__ void __launch_bounds__(kThreads)
     pack_do_delta_kernel(const __nv_bfloat16 *__restrict__ dout, const __nv_bfloat16 *__restrict__ o,
                          const float *__restrict__ lse, __nv_bfloat16 *__restrict__ do_head,
                          float *__restrict__ delta, float *__restrict__ nlse, int P, int B,
-                         int Sl, int H, int D, int Pu, int Cs) {
+                         int Sl, int H, int D, int Pu, int Cs, uint32_t *status) {
+  // elements of dO / O / dO in head layout, and of the lse / delta / nlse rows
+  const long long act_n = (long long)P * B * Sl * H * D, rows_n = (long long)P * B * Sl * H;
   const int hp = H / Pu;
   const int lanes = D / 8;  // 8 or 16: divides 32 and kThreads
   const int tasks = H * lanes;
@@ -297,9 +308,10 @@ __global__ void __launch_bounds__(kThreads)
       const int d = rp * Pu + g / hp;   // the head-layout rank holding head g of the token
       const int j = g % hp;
       float acc = 0.f;
-      if (live) {
-        const long long head_row = (((long long)(d * B + b) * Cs + crow) * hp + j) * D;
-        const uint4 x = __ldg(reinterpret_cast<const uint4 *>(dout + (row * H + g) * D + c * 8));
+      const long long head_row = (((long long)(d * B + b) * Cs + crow) * hp + j) * D;
+      const long long seq_off = (row * H + g) * D + c * 8;
+      if (live && in_range(status, seq_off, 8, act_n) && in_range(status, head_row + c * 8, 8, act_n)) {
+        const uint4 x = __ldg(reinterpret_cast<const uint4 *>(dout + seq_off));
         const uint4 y = __ldg(reinterpret_cast<const uint4 *>(o + head_row + c * 8));
         *reinterpret_cast<uint4 *>(do_head + head_row + c * 8) = x;
         const __nv_bfloat162 *px = reinterpret_cast<const __nv_bfloat162 *>(&x);
@@ -314,6 +326,7 @@ __global__ void __launch_bounds__(kThreads)
       for (int off = lanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
       if (live && c == 0) {
         const long long idx = ((long long)(d * B + b) * hp + j) * Cs + crow;
+        if (!in_range(status, idx, 1, rows_n)) continue;
         delta[idx] = acc;
         nlse[idx] = -lse[idx] * 1.4426950408889634f;
       }
@@ -366,6 +379,7 @@ static PermParams base_params(const ulysses_problem &p, const void *ws, int to_h
     pp.rope_key = rope_key(p);
     pp.rope_cos = reinterpret_cast<const float *>(base + L.rope);
     pp.rope_sin = pp.rope_cos + (size_t)p.S * (p.head_dim / 2);
+    pp.rope_n = (long long)p.S * (p.head_dim / 2);
   }
   return pp;
 }
@@ -409,9 +423,14 @@ cudaError_t launch_pack_qkv(const ulysses_problem &p, const void *q, const void 
   PermParams pp = base_params(p, ws, 1);
   const int r = p.use_rope ? 1 : 0;
   const int R = kv_replicas(p);
-  pp.job[0] = {q, qh, p.n_head, r, 1};
-  pp.job[1] = {k, kh, p.n_kv_head, r, R};
-  pp.job[2] = {v, vh, p.n_kv_head, 0, R};
+  // elements: the sequence-sharded tensor, and its head layout (P copies of
+  // one kv-head's rows per rank with replicated kv-heads)
+  const long long nq = (long long)p.B * p.S * p.n_head * p.head_dim;
+  const long long nk = (long long)p.B * p.S * p.n_kv_head * p.head_dim;
+  const long long nkh = (long long)p.P * p.B * chunk_len(p) * kv_per_rank(p) * p.head_dim;
+  pp.job[0] = {q, qh, p.n_head, r, 1, nq, nq};
+  pp.job[1] = {k, kh, p.n_kv_head, r, R, nk, nkh};
+  pp.job[2] = {v, vh, p.n_kv_head, 0, R, nk, nkh};
   pp.njobs = 3;
   return launch_perm(p, pp, st);
 }
@@ -419,19 +438,20 @@ cudaError_t launch_pack_qkv(const ulysses_problem &p, const void *q, const void 
 cudaError_t launch_unpack(const ulysses_problem &p, const void *o_head, void *o_seq,
                           cudaStream_t st) {
   PermParams pp = base_params(p, nullptr, 0);
-  pp.job[0] = {o_head, o_seq, p.n_head, 0, 1};
+  const long long no = (long long)p.B * p.S * p.n_head * p.head_dim;
+  pp.job[0] = {o_head, o_seq, p.n_head, 0, 1, no, no};
   pp.njobs = 1;
   return launch_perm(p, pp, st);
 }
 
 cudaError_t launch_pack_do_delta(const ulysses_problem &p, const void *do_seq, const void *o_head,
                                  const float *lse, void *do_head, float *delta, float *nlse,
-                                 cudaStream_t st) {
+                                 uint32_t *status, cudaStream_t st) {
   const int grid = grid_for((long long)p.B * p.S);  // one token row per block at a time
   pack_do_delta_kernel<<<grid, kThreads, 0, st>>>(
       static_cast<const __nv_bfloat16 *>(do_seq), static_cast<const __nv_bfloat16 *>(o_head),
       lse, static_cast<__nv_bfloat16 *>(do_head), delta, nlse, p.P, p.B, p.S / p.P, p.n_head,
-      p.head_dim, group_ranks(p), chunk_len(p));
+      p.head_dim, group_ranks(p), chunk_len(p), status);
   return cudaGetLastError();
 }
 
@@ -451,9 +471,13 @@ namespace {
 __global__ void __launch_bounds__(256) kv_reduce_kernel(const float *__restrict__ dkp, const float *__restrict__ dvp,
                                                         __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv,
                                                         int P, int B, int Sl, int n_kv, int D, int Pu, float scale,
-                                                        const float *__restrict__ cs, const float *__restrict__ sn) {
+                                                        const float *__restrict__ cs, const float *__restrict__ sn,
+                                                        uint32_t *status) {
   const int R = Pu / n_kv, half = D / 2, q4 = half / 4;
   const int Cs = Pu * Sl;
+  // elements of the float partials, of dK / dV in sequence layout, of cos / sin
+  const long long part_n = (long long)P * B * Cs * D, seq_n = (long long)P * B * Sl * n_kv * D;
+  const long long rope_n = (long long)P * Sl * half;
   const long long n = (long long)P * B * Sl * n_kv * q4;
   for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < n; u += (long long)gridDim.x * blockDim.x) {
     const int c = (int)(u % q4);
@@ -467,6 +491,15 @@ __global__ void __launch_bounds__(256) kv_reduce_kernel(const float *__restrict_
     const int pos = d * Sl + t;
     const int rp = d / Pu, crow = (d - rp * Pu) * Sl + t;  // ring position, row in its chunk
     float4 kx = make_float4(0.f, 0.f, 0.f, 0.f), ky = kx, vx = kx, vy = kx;
+    const size_t o = (((size_t)(d * B + b) * Sl + t) * n_kv + kv) * D + (size_t)c * 4;
+    if (!in_range(status, (long long)o, half + 4, seq_n) ||
+        (cs && !in_range(status, (long long)pos * half + c * 4, 4, rope_n)))
+      continue;
+    bool whole = true;
+    for (int j = 0; j < R; ++j)
+      whole = whole && in_range(status, (((long long)(rp * Pu + kv * R + j) * B + b) * Cs + crow) * D + c * 4,
+                                half + 4, part_n);
+    if (!whole) continue;
     for (int j = 0; j < R; ++j) {
       const size_t off = (((size_t)(rp * Pu + kv * R + j) * B + b) * Cs + crow) * D + (size_t)c * 4;
       const float4 a = *reinterpret_cast<const float4 *>(dkp + off);
@@ -491,7 +524,6 @@ __global__ void __launch_bounds__(256) kv_reduce_kernel(const float *__restrict_
         ys[q] = y * cc[q] - x * ss[q];
       }
     }
-    const size_t o = (((size_t)(d * B + b) * Sl + t) * n_kv + kv) * D + (size_t)c * 4;
     const __nv_bfloat162 k0 = __floats2bfloat162_rn(xs[0], xs[1]), k1 = __floats2bfloat162_rn(xs[2], xs[3]);
     const __nv_bfloat162 k2 = __floats2bfloat162_rn(ys[0], ys[1]), k3 = __floats2bfloat162_rn(ys[2], ys[3]);
     const __nv_bfloat162 w0 = __floats2bfloat162_rn(vx.x, vx.y), w1 = __floats2bfloat162_rn(vx.z, vx.w);
@@ -517,7 +549,8 @@ cudaError_t launch_kv_reduce(const ulysses_problem &p, const float *dk_part, con
   kv_reduce_kernel<<<grid_for(n / 256 + 1), 256, 0, st>>>(dk_part, dv_part, static_cast<__nv_bfloat16 *>(dk_seq),
                                                           static_cast<__nv_bfloat16 *>(dv_seq), p.P, p.B,
                                                           p.S / p.P, p.n_kv_head, p.head_dim, group_ranks(p), scale,
-                                                          cs, sn);
+                                                          cs, sn,
+                                                          const_cast<uint32_t *>(static_cast<const uint32_t *>(ws)));
   return cudaGetLastError();
 }
 

@@ -43,6 +43,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include "check.cuh"
 #include "internal.h"
 #include "sm100.cuh"
 #include "tmap.h"
@@ -85,6 +86,9 @@ struct ProjParams {
   __nv_bfloat16 *y;                  // [P][B][Sl][N] sequence layout (output mode)
   uint32_t *status;
   uint32_t rope_key;
+  // elements of q / k / v (head layout) or y, and of each RoPE table (range
+  // checks of a checked build; the bias has N)
+  long long q_n, kv_n, y_n, rope_n;
 };
 
 __device__ __forceinline__ void tile_mn(const ProjParams &p, int t, int &m, int &n) {
@@ -247,7 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             wx[e] = pack_bf16x2(a, b2);
           }
-          if (live) {
+          if (live && in_range(p.status, (long long)row * p.N + col, 32, p.y_n) &&
+              (!p.bias || in_range(p.status, col, 32, p.N))) {
             uint4 *o = reinterpret_cast<uint4 *>(p.y + (size_t)row * p.N + col);
 #pragma unroll
             for (int v = 0; v < 4; ++v) o[v] = make_uint4(wx[4 * v], wx[4 * v + 1], wx[4 * v + 2], wx[4 * v + 3]);
@@ -294,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             fx[e] = __uint_as_float(xr[e]);
             fy[e] = __uint_as_float(yr[e]);
           }
-          if (p.bias) {
+          if (p.bias && in_range(p.status, col0 + c * 32, D / 2 + 32, p.N)) {
             const __nv_bfloat16 *bx = p.bias + col0 + c * 32, *by = bx + D / 2;
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
@@ -302,7 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               fy[e] += __bfloat162float(by[e]);
             }
           }
-          if (rope) {  // x' = x cos a - y sin a, y' = y cos a + x sin a, a = pos * theta_i
+          if (rope && in_range(p.status, (long long)pos * (D / 2) + c * 32, 32, p.rope_n)) {
+            // x' = x cos a - y sin a, y' = y cos a + x sin a, a = pos * theta_i
             const float *cs = p.rope_cos + (size_t)pos * (D / 2) + c * 32;
             const float *sn = p.rope_sin + (size_t)pos * (D / 2) + c * 32;
 #pragma unroll
@@ -338,8 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 d0 = head / p.kvp, nd = 1, j = head % p.kvp, width = p.kvp;
             }
             for (int dd = 0; dd < nd; ++dd) {
-              __nv_bfloat16 *dst =
-                  base + ((((size_t)(d0 + dd) * p.B + b) * p.S + pos) * width + j) * D + c * 32;
+              const long long off = ((((long long)(d0 + dd) * p.B + b) * p.S + pos) * width + j) * D + c * 32;
+              if (!in_range(p.status, off, D / 2 + 32, kind == 0 ? p.q_n : p.kv_n)) continue;
+              __nv_bfloat16 *dst = base + off;
               uint4 *ox = reinterpret_cast<uint4 *>(dst), *oy = reinterpret_cast<uint4 *>(dst + D / 2);
 #pragma unroll
               for (int v = 0; v < 4; ++v) {
@@ -399,6 +406,10 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   if (MODE == kOutUnpack) pp.rope_cos = pp.rope_sin = nullptr;  // no rotation on the output
   pp.status = reinterpret_cast<uint32_t *>(const_cast<uint8_t *>(wsb + L.status));
   pp.rope_key = rope_key(p);
+  pp.q_n = (long long)p.B * p.S * p.n_head * D;
+  pp.kv_n = (long long)p.P * p.B * p.S * pp.kvp * D;
+  pp.y_n = (long long)pp.M * p.hidden;
+  pp.rope_n = (long long)p.S * (D / 2);
   CUtensorMap mx, mw;
   const bool ok_x = MODE == kQkvPack ? make_mat_map(enc, &mx, x, pp.H, pp.M, BM)
                                      : make_act_map(enc, &mx, x, D, pp.hp, p.S, p.P * p.B, BM);

@@ -276,7 +276,7 @@ int ulysses_attn_fwd(const ulysses_problem *prob, const void *q_head, const void
     return cuda_rc(launch_attn_fwd_simt(p, static_cast<const float *>(q_head),
                                         static_cast<const float *>(k_head),
                                         static_cast<const float *>(v_head),
-                                        static_cast<float *>(o_head), lse, (cudaStream_t)stream));
+                                        static_cast<float *>(o_head), lse, status, (cudaStream_t)stream));
   TmaEncoder enc;
   if (!get_tma_encoder(&enc)) return ULYSSES_ERR_CUDA;
   return cuda_rc(launch_attn_fwd_tc(p, enc, q_head, k_head, v_head, o_head, lse, status, false,
@@ -342,7 +342,8 @@ int ulysses_attn_bwd_prepare(const ulysses_problem *prob, const void *o_head, co
   const WorkspaceLayout L = workspace_layout(p);
   uint8_t *w = static_cast<uint8_t *>(ws);
   return cuda_rc(launch_pack_do_delta(p, do_seq, o_head, lse, w + L.dohead, reinterpret_cast<float *>(w + L.delta),
-                                      reinterpret_cast<float *>(w + L.nlse), (cudaStream_t)stream));
+                                      reinterpret_cast<float *>(w + L.nlse), reinterpret_cast<uint32_t *>(w + L.status),
+                                      (cudaStream_t)stream));
 }
 
 int ulysses_attn_bwd_dkdv(const ulysses_problem *prob, const void *q_head, const void *k_head,
