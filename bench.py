@@ -71,8 +71,10 @@ def attn_fwd_flops(w):
 def permute_bytes(w, es):
     """Bytes read + written by the seq->head pack of Q, K, V: each tensor read
     once and written once, K and V written once per replica when there are
-    fewer kv-heads than ranks (each kv-head then goes to P / n_kv_head ranks)."""
-    kv_written = w.n_kv_head if w.n_kv_head >= w.P else w.P
+    fewer kv-heads than ranks in an All-to-All group (each kv-head then goes to
+    Pu / n_kv_head ranks; Pu = P / ring is the group's size)."""
+    pu = w.P // getattr(w, "ring", 1)
+    kv_written = w.n_kv_head if w.n_kv_head >= pu else pu
     return float(w.B * w.S * w.head_dim * es) * (2 * w.n_head + 2 * w.n_kv_head + 2 * kv_written)
 
 

@@ -33,3 +33,19 @@ def test_oracle_leg_runs_the_ring_hybrid():
     t_full, n_rows, pairs, wall = ob.step(8)
     assert t_full > 0 and 0 < n_rows <= 8 and pairs > 0 and wall > 0
     assert "2 ring positions" in ob.describe(n_rows)
+
+
+def test_pack_bytes_count_replicas_within_an_all_to_all_group():
+    """K and V are written once per replica only when there are fewer
+    kv-heads than ranks in one All-to-All group (P / ring ranks): the ring
+    hybrid at P = 256 with 32 kv-heads replicates nothing, C4 with 4 kv-heads
+    writes each kv-head to 2 ranks."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from ulysses_sequence_attention_seq_gb300.synthetic import EXTRA_WORKLOADS, WORKLOADS
+    c4 = WORKLOADS["C4"]
+    per_head = c4.B * c4.S * c4.head_dim * 2            # one bf16 head over the sequence
+    assert bench.permute_bytes(c4, 2) == 6 * 32 * per_head
+    assert bench.permute_bytes(EXTRA_WORKLOADS["C4-ring8"], 2) == 6 * 32 * per_head
+    kv4 = EXTRA_WORKLOADS["C4-kv4"]
+    assert bench.permute_bytes(kv4, 2) == per_head * (2 * 32 + 2 * 4 + 2 * 8)
