@@ -84,6 +84,11 @@ def test_workspace_sizes(lib):
     assert U.ulysses_workspace_bytes(prob(B=0), 0) == 0
     # the hybrid regroups the same rows: the same workspace
     assert U.ulysses_workspace_bytes(prob(ring=2), 1) == b
+    # S = 4098 over P = 2: the delta and base-2 LSE rows (one per batch and
+    # head, 4098 floats) are padded to 4100 floats so each starts on 16 bytes
+    po = prob(P=2, S=4098)
+    fo, bo = U.ulysses_workspace_bytes(po, 0), U.ulysses_workspace_bytes(po, 1)
+    assert bo - fo >= 2 * po.B * po.n_head * 4100 * 4 + po.B * po.S * po.n_head * po.head_dim * 2
 
 
 def test_ring_is_refused_where_no_kernel_takes_it(lib):

@@ -52,7 +52,7 @@ struct BwdParams {
   int n_head, n_kv;                    // global head counts (row widths of the seq layout)
   int group_kv, group_q;               // heads per CTA group (grouped_order) of the two kernels
   float scale, scale_log2;
-  const float *nlse, *delta;           // [P][B][hp][S]; nlse = -lse * log2(e)
+  const float *nlse, *delta;           // [P][B][hp] rows of Cs values, Ld apart; nlse = -lse * log2(e)
   const float *rope_cos, *rope_sin;    // [S][D/2], or null without RoPE
   const __nv_bfloat16 *q, *dout;       // head layout [P][B][S][hp][D] (the dQ kernel's TMEM operands)
   __nv_bfloat16 *dq, *dk, *dv;         // sequence-sharded outputs
@@ -65,6 +65,7 @@ struct BwdParams {
   // over the full sequence; the rows at global position pos live in the
   // head-layout buffer of rank (pos / Cs) * Pu + member, row pos % Cs.
   int Pu, Cs;
+  int Ld;                              // row stride of nlse / delta (Cs rounded up to 4)
   // Elements of the buffers the kernels read or write with plain loads and
   // stores (range checks of a checked build): dQ, dK / dV (or their float
   // partials), Q / dO in head layout, the nlse / delta rows, the RoPE table.
@@ -819,7 +820,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       mbar_arrive(bar + kQBarQReady);
     }
     const int qr = live ? qi : 0;
-    const size_t lrow = ((size_t)hl_outer(p, rb, qr) * p.hp + j) * p.Cs + qr % p.Cs;
+    const size_t lrow = ((size_t)hl_outer(p, rb, qr) * p.hp + j) * p.Ld + qr % p.Cs;
     const bool get_row = live && in_range(p.status, (long long)lrow, 1, p.rows_n);
     const float nl2 = get_row ? p.nlse[lrow] : 0.f;
     const float dlt = get_row ? p.delta[lrow] : 0.f;
@@ -917,8 +918,8 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   CUtensorMap mK128, mV128, mL, mDl, mQ128, mdO128;
   bool ok = make_act_map(enc, &mK128, k, D, kvp, Cs, PB, 128) &&
             make_act_map(enc, &mV128, v, D, kvp, Cs, PB, 128) &&
-            make_row_map(enc, &mL, nlse, Cs, PB * hp, 128) &&
-            make_row_map(enc, &mDl, delta, Cs, PB * hp, 128) &&
+            make_row_map(enc, &mL, nlse, Cs, delta_ld(p), PB * hp, 128) &&
+            make_row_map(enc, &mDl, delta, Cs, delta_ld(p), PB * hp, 128) &&
             make_act_map(enc, &mQ128, q, D, hp, Cs, PB, 128) &&
             make_act_map(enc, &mdO128, do_head, D, hp, Cs, PB, 128);
   if (!ok) return cudaErrorInvalidValue;
@@ -938,7 +939,8 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   bp.dq_n = (long long)p.B * p.S * p.n_head * D;
   bp.dkv_n = kv_replicas(p) > 1 ? (long long)p.P * p.B * Cs * D : (long long)p.B * p.S * p.n_kv_head * D;
   bp.qo_n = (long long)p.B * p.S * p.n_head * D;
-  bp.rows_n = (long long)p.B * p.n_head * p.S;
+  bp.Ld = delta_ld(p);
+  bp.rows_n = (long long)PB * hp * bp.Ld;
   bp.rope_n = (long long)p.S * (D / 2);
   // CTA units: (group member, batch, head), each over the full sequence.
   const int UB = Pu * p.B;

@@ -15,8 +15,8 @@ namespace ulysses {
 struct WorkspaceLayout {
   size_t status = 0;
   size_t rope = 0, rope_bytes = 0;    // float cos[S][D/2], then float sin[S][D/2]
-  size_t delta = 0, delta_bytes = 0;  // float [P][B][hp][S]          (backward)
-  size_t nlse = 0, nlse_bytes = 0;    // float [P][B][hp][S], -lse*log2(e) (backward)
+  size_t delta = 0, delta_bytes = 0;  // float [P][B][hp][delta_ld]    (backward)
+  size_t nlse = 0, nlse_bytes = 0;    // float [P][B][hp][delta_ld], -lse*log2(e) (backward)
   size_t dohead = 0, dohead_bytes = 0;  // dO in head layout [P][B][S][hp][D] (backward)
   // With replicated kv-heads (n_kv_head < P): each rank's partial dK and dV,
   // float [P][B][S][D] each, summed over the replicas afterwards (backward).
@@ -38,6 +38,11 @@ inline size_t elem_size(const ulysses_problem &p) { return p.dtype == ULYSSES_BF
 inline int ring_of(const ulysses_problem &p) { return p.ring > 1 ? p.ring : 1; }
 inline int group_ranks(const ulysses_problem &p) { return p.P / ring_of(p); }  // Pu
 inline int chunk_len(const ulysses_problem &p) { return p.S / ring_of(p); }    // Cs
+// Row stride, in floats, of the backward's delta and rescaled-LSE rows in the
+// workspace: Cs rounded up to 4 so that every row starts on 16 bytes (a TMA
+// tensor map's row stride must be a multiple of 16 bytes).  The pad is never
+// read or written.
+inline int delta_ld(const ulysses_problem &p) { return (chunk_len(p) + 3) & ~3; }
 
 // KV-head replication: with fewer kv-heads than ranks (P a multiple of
 // n_kv_head) the q-heads of rank r all read kv-head r / R, R = P / n_kv_head,

@@ -282,10 +282,12 @@ __global__ void __launch_bounds__(kThreads)
     pack_do_delta_kernel(const __nv_bfloat16 *__restrict__ dout, const __nv_bfloat16 *__restrict__ o,
                          const float *__restrict__ lse, __nv_bfloat16 *__restrict__ do_head,
                          float *__restrict__ delta, float *__restrict__ nlse, int P, int B,
-                         int Sl, int H, int D, int Pu, int Cs, uint32_t *status) {
-  // elements of dO / O / dO in head layout, and of the lse / delta / nlse rows
-  const long long act_n = (long long)P * B * Sl * H * D, rows_n = (long long)P * B * Sl * H;
+                         int Sl, int H, int D, int Pu, int Cs, int Ld, uint32_t *status) {
+  // elements of dO / O / dO in head layout, of the lse rows (Cs per row) and of
+  // the delta / nlse rows (Ld >= Cs per row)
   const int hp = H / Pu;
+  const long long act_n = (long long)P * B * Sl * H * D, rows_n = (long long)P * B * Sl * H,
+                  ws_rows_n = (long long)P * B * hp * Ld;
   const int lanes = D / 8;  // 8 or 16: divides 32 and kThreads
   const int tasks = H * lanes;
   const long long rows = (long long)P * B * Sl;
@@ -325,10 +327,11 @@ __global__ void __launch_bounds__(kThreads)
       }
       for (int off = lanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
       if (live && c == 0) {
-        const long long idx = ((long long)(d * B + b) * hp + j) * Cs + crow;
-        if (!in_range(status, idx, 1, rows_n)) continue;
-        delta[idx] = acc;
-        nlse[idx] = -lse[idx] * 1.4426950408889634f;
+        const long long hrow = (long long)(d * B + b) * hp + j;
+        const long long idx = hrow * Cs + crow, widx = hrow * Ld + crow;
+        if (!in_range(status, idx, 1, rows_n) || !in_range(status, widx, 1, ws_rows_n)) continue;
+        delta[widx] = acc;
+        nlse[widx] = -lse[idx] * 1.4426950408889634f;
       }
     }
   }
@@ -451,7 +454,7 @@ cudaError_t launch_pack_do_delta(const ulysses_problem &p, const void *do_seq, c
   pack_do_delta_kernel<<<grid, kThreads, 0, st>>>(
       static_cast<const __nv_bfloat16 *>(do_seq), static_cast<const __nv_bfloat16 *>(o_head),
       lse, static_cast<__nv_bfloat16 *>(do_head), delta, nlse, p.P, p.B, p.S / p.P, p.n_head,
-      p.head_dim, group_ranks(p), chunk_len(p), status);
+      p.head_dim, group_ranks(p), chunk_len(p), delta_ld(p), status);
   return cudaGetLastError();
 }
 

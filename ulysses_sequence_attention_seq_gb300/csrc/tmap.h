@@ -41,11 +41,13 @@ inline bool make_mat_map(const TmaEncoder &enc, CUtensorMap *m, const void *base
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D map over a float array [rows][S] (LSE, delta): box of `box` positions of one row.
-inline bool make_row_map(const TmaEncoder &enc, CUtensorMap *m, const void *base, int S, int rows,
+// 2-D map over a float array of `rows` rows of S values, `ld` floats apart
+// (ld >= S, a multiple of 4): box of `box` positions of one row; positions
+// past S read as zero.
+inline bool make_row_map(const TmaEncoder &enc, CUtensorMap *m, const void *base, int S, int ld, int rows,
                          int box) {
   const cuuint64_t dims[2] = {(cuuint64_t)S, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)S * 4};
+  const cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
   const cuuint32_t boxd[2] = {(cuuint32_t)box, 1};
   const cuuint32_t estr[2] = {1, 1};
   return enc.encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides,

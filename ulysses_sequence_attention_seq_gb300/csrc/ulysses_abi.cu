@@ -37,7 +37,8 @@ WorkspaceLayout workspace_layout(const ulysses_problem &p) {
   L.rope_bytes = p.use_rope ? (size_t)p.S * p.head_dim * 4 : 0;
   L.total_fwd = align256(L.rope + L.rope_bytes);
   L.delta = L.total_fwd;
-  L.delta_bytes = (size_t)p.B * p.n_head * p.S * 4;
+  // rows of P*B*hp = B*n_head*ring, each delta_ld floats
+  L.delta_bytes = (size_t)p.B * p.n_head * ring_of(p) * delta_ld(p) * 4;
   L.nlse = align256(L.delta + L.delta_bytes);
   L.nlse_bytes = L.delta_bytes;
   L.dohead = align256(L.nlse + L.nlse_bytes);
