@@ -46,6 +46,9 @@ TRAFFIC = {
     ("attn_fwd", "C4"): 1180097837,
     ("bwd_dkdv", "C4"): 1882788892,
     ("bwd_dq", "C4"): 1769575339,
+    ("attn_fwd", "C4-ring8"): 1202139961,
+    ("bwd_dkdv", "C4-ring8"): 1899695417,
+    ("bwd_dq", "C4-ring8"): 1811152697,
 }
 
 

@@ -1,5 +1,7 @@
 """The streamed host-to-host path (two device buffer sets, upload / compute /
-download streams) gives exactly what the plain device path gives."""
+download streams handing over per C-ABI call) gives exactly what the plain
+device path gives, for every step, with different inputs at every step so
+that a result read or written out of order cannot go unnoticed."""
 import pytest
 import torch
 
@@ -11,20 +13,41 @@ from ulysses_sequence_attention_seq_gb300.streamed import StreamedPath
 pytestmark = pytest.mark.gpu
 
 
+def _outs(sp):
+    return {n: torch.empty(getattr(sp.sets[0], n).shape, dtype=getattr(sp.sets[0], n).dtype, pin_memory=True)
+            for n in sp.out_names()}
+
+
 @pytest.mark.parametrize("backward", [False, True])
 def test_streamed_steps_match_the_device_path(backward):
     w = wl(4, 1, 1024, 8, 4, 128).with_(backward=backward)
     sp = StreamedPath(U.Problem.from_workload(w), backward=backward)
-    outs = {n: torch.empty(getattr(sp.sets[0], n).shape, dtype=getattr(sp.sets[0], n).dtype, pin_memory=True)
-            for n in sp.out_names()}
-    for seed, steps in ((7, 1), (8, 3), (9, 2)):
+    refs, hosts = [], []
+    for seed in (7, 8, 9):
         ref = GpuRun(w.with_(seed=seed), backward=backward)
         ref.forward()
         if backward:
             ref.backward()
-        host = {n: getattr(ref.buf, n).cpu().pin_memory() for n in sp.in_names()}
-        sp.run(host, outs, steps)
+        refs.append({n: getattr(ref.buf, n).cpu() for n in sp.out_names()})
+        hosts.append({n: getattr(ref.buf, n).cpu().pin_memory() for n in sp.in_names()})
+    # one input set for every step
+    outs = _outs(sp)
+    for i, steps in ((0, 1), (1, 3), (2, 2)):
+        sp.run(hosts[i], outs, steps)
         torch.cuda.synchronize()
         assert sp.status() == 0
         for n in sp.out_names():
-            assert torch.equal(outs[n], getattr(ref.buf, n).cpu()), (seed, n)
+            assert torch.equal(outs[n], refs[i][n]), (i, n)
+    # a different input set at every step (step k uses set k % 3), each
+    # step's results into their own host buffers
+    outs = [_outs(sp) for _ in range(3)]
+    for steps in (3, 5, 4):
+        for o in outs:
+            for t in o.values():
+                t.zero_()
+        sp.run(hosts, outs, steps)
+        torch.cuda.synchronize()
+        assert sp.status() == 0
+        for i in range(min(steps, 3)):
+            for n in sp.out_names():
+                assert torch.equal(outs[i][n], refs[i][n]), (steps, i, n)
