@@ -254,8 +254,18 @@ def run_ulysses(args, w, rank, world):
         def fold():
             U.ulysses_attn_fwd_folded(pf, buf.q_seq, buf.k_seq, buf.v_seq, buf.o_seq, buf.lse, buf.ws)
 
-        times = {}
-        for name, fn in (("unfolded_ms", three), ("ms", fold)):
+        # the backward on the packed buffers (dO pack + delta, dK/dV, dQ) vs the
+        # folded backward (delta from O and dO in place, the same two kernels
+        # reading the sequence-sharded buffers)
+        def bwd_packed():
+            U.ulysses_attn_bwd(pf, buf.q_head, buf.k_head, buf.v_head, buf.o_head, buf.lse, buf.do_seq,
+                               buf.dq_seq, buf.dk_seq, buf.dv_seq, buf.ws)
+
+        def bwd_fold():
+            U.ulysses_attn_bwd_folded(pf, buf.q_seq, buf.k_seq, buf.v_seq, buf.o_seq, buf.lse, buf.do_seq,
+                                      buf.dq_seq, buf.dk_seq, buf.dv_seq, buf.ws)
+
+        def timed(fn):
             for _ in range(2):
                 fn()
             a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -264,8 +274,12 @@ def run_ulysses(args, w, rank, world):
                 fn()
             b2.record(stream)
             torch.cuda.synchronize()
-            times[name] = a.elapsed_time(b2) / args.steps
-        folded = dict(times, workload=f"{w.name} shapes, RoPE off (q and k rotated by their producer)")
+            return a.elapsed_time(b2) / args.steps
+
+        label = f"{w.name} shapes, RoPE off (q and k rotated by their producer)"
+        folded = {"fwd": dict(unfolded_ms=timed(three), ms=timed(fold), workload=label)}
+        if backward:
+            folded["bwd"] = dict(unfolded_ms=timed(bwd_packed), ms=timed(bwd_fold), workload=label)
     status = U.ulysses_read_status(buf.ws)
     # the MUFU unit's exponential throughput on this GPU (the softmax's secondary bound)
     ex2_rate = U.ulysses_selftest_ex2_rate()
@@ -632,7 +646,8 @@ def main():
         "e2e": {"value": job_throughput(tokens, e2e_ms * 1e-3, world), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": r["launches"],
-        "folded_fwd": r["folded"],
+        "folded_fwd": r["folded"]["fwd"] if r["folded"] else None,
+        "folded_bwd": r["folded"].get("bwd") if r["folded"] else None,
         "device_status": r["status"],
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

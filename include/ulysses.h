@@ -292,6 +292,31 @@ int ulysses_attn_bwd_dq(const ulysses_problem *prob, const void *q_head, const v
                         const void *v_head, void *dq_seq, void *ws, size_t ws_bytes, ulysses_stream_t stream);
 
 /*
+ * Folded backward: the backward of ulysses_attn_fwd_folded with every
+ * All-to-All turned into addressing ("Sequence Parallelism II", §6: the
+ * backward makes the forward's layout changes in reverse).  The dK/dV and dQ
+ * kernels read the 128-row tiles of q, k, v and dO straight out of the
+ * sequence-sharded buffers (the tile at global position p of head g comes from
+ * rank p/Sl, row p%Sl, head g) and write dQ, dK, dV straight into sequence
+ * layout; a first kernel forms delta_i = dO_i . O_i from o_seq and do_seq in
+ * place (no dO pack).  Results are identical to ulysses_attn_bwd on the packed
+ * buffers of the same problem.
+ * Inputs: q_seq [P][B][Sl][n_head][D], k_seq/v_seq [P][B][Sl][n_kv_head][D]
+ * (the already-rotated q, k the folded forward read), o_seq [P][B][Sl][H] and
+ * lse [P][B][hp][S] from the folded forward, do_seq [P][B][Sl][H].  Outputs
+ * dq_seq [P][B][Sl][n_head][D], dk_seq/dv_seq [P][B][Sl][n_kv_head][D] (the
+ * gradients with respect to the rotated q, k: no rotation is undone).
+ * Requires bf16, head_dim 64 or 128, use_rope == 0, ring <= 1 and S/P a
+ * multiple of 128, else ULYSSES_ERR_UNSUPPORTED.  `ws` must be sized for
+ * phase 1 and prepared by ulysses_workspace_init; other errors and the
+ * ownership rules as for ulysses_attn_bwd.
+ */
+int ulysses_attn_bwd_folded(const ulysses_problem *prob, const void *q_seq, const void *k_seq,
+                            const void *v_seq, const void *o_seq, const float *lse, const void *do_seq,
+                            void *dq_seq, void *dk_seq, void *dv_seq, void *ws, size_t ws_bytes,
+                            ulysses_stream_t stream);
+
+/*
  * Self-test of failure detection (no counterpart in the pages): one CTA waits,
  * with the bounded wait every pipeline wait of the attention kernels uses, on a
  * barrier that nothing ever completes.  After `limit_ns` (1 ns .. 2 s) the wait

@@ -104,6 +104,19 @@ def test_ring_is_refused_where_no_kernel_takes_it(lib):
     assert lib.ulysses_out_proj_unpack(ctypes.byref(p.c()), a[0], a[1], None, a[2], a[5], nws, vp(0)) == -4
 
 
+@pytest.mark.parametrize("kw", [dict(use_rope=True), dict(use_rope=False, S=800, P=8),   # RoPE; Sl = 100
+                                dict(use_rope=False, ring=2), dict(use_rope=False, dtype=U.FP32)])
+def test_folded_backward_refusals(lib, kw):
+    """The folded backward needs RoPE off, S/P a multiple of 128, plain
+    Ulysses and bf16; anything else is ERR_UNSUPPORTED before a launch (fake
+    pointers, never dereferenced)."""
+    vp = ctypes.c_void_p
+    p = prob(**kw)
+    nws = U.ulysses_workspace_bytes(p, 1)
+    a = [vp((1 << 40) + i * (1 << 34)) for i in range(11)]
+    assert lib.ulysses_attn_bwd_folded(ctypes.byref(p.c()), *a[:10], nws, vp(0)) == -4
+
+
 def test_status_strings(lib):
     for code in range(0, -9, -1):
         s = lib.ulysses_status_string(code)

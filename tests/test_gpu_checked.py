@@ -1,8 +1,9 @@
 """The range-checked build (-DULYSSES_CHECK_BOUNDS: every plain global load
 and store checked against its buffer) runs the whole path without a single
 failed check and gives bit for bit what the normal build gives: forward,
-backward, the fp32 forward, replicated kv-heads, the ring hybrid and the two
-projections.  The checked library runs in a child process (ULYSSES_LIB)."""
+backward, the fp32 forward, replicated kv-heads, the ring hybrid, the folded
+forward and backward and the two projections.  The checked library runs in a
+child process (ULYSSES_LIB)."""
 import os
 import subprocess
 import sys
@@ -41,6 +42,17 @@ for n, w in enumerate(cases):
     for name in names:
         out[f"{n}/{name}"] = getattr(run.buf, name).cpu()
     out[f"{n}/status"] = torch.tensor(U.ulysses_read_status(run.buf.ws))
+# the folded forward and backward (RoPE off, S/P = 256, kv-heads replicated)
+w = wl(8, 1, 2048, 16, 2, 128, rope=False).with_(backward=True)
+run = GpuRun(w, backward=True)
+b = run.buf
+U.ulysses_attn_fwd_folded(run.prob, b.q_seq, b.k_seq, b.v_seq, b.o_seq, b.lse, b.ws)
+U.ulysses_attn_bwd_folded(run.prob, b.q_seq, b.k_seq, b.v_seq, b.o_seq, b.lse, b.do_seq,
+                          b.dq_seq, b.dk_seq, b.dv_seq, b.ws)
+torch.cuda.synchronize()
+for name in ("o_seq", "lse", "dq_seq", "dk_seq", "dv_seq"):
+    out[f"fold/{name}"] = getattr(b, name).cpu()
+out["fold/status"] = torch.tensor(U.ulysses_read_status(b.ws))
 # the projections (QKV with pack and RoPE; output with unpack)
 w = wl(2, 1, 512, 4, 2, 128)
 prob = U.Problem.from_workload(w)

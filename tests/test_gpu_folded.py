@@ -1,7 +1,8 @@
-"""Folded forward (ulysses_attn_fwd_folded): the attention kernel reads the
-sequence-sharded Q/K/V directly and writes O in sequence layout, so both
-All-to-Alls become addressing.  It must reproduce pack -> attention -> unpack
-bit for bit, and the fp64 oracle within the bf16 tolerance."""
+"""Folded forward and backward (ulysses_attn_fwd_folded, ulysses_attn_bwd_folded):
+the attention kernels read the sequence-sharded Q/K/V (and dO) directly and
+write O (and dQ, dK, dV) in sequence layout, so every All-to-All becomes
+addressing.  They must reproduce the packed path bit for bit, and the fp64
+oracle within the bf16 tolerance."""
 import numpy as np
 import pytest
 import torch
@@ -86,3 +87,67 @@ def test_folded_with_replicated_kv_heads_equals_three_calls():
     torch.cuda.synchronize()
     assert U.ulysses_read_status(b.ws) == 0
     assert torch.equal(b.o_seq, o3) and torch.equal(b.lse, l3)
+
+
+# ------------------------------------------------------------ folded backward
+
+BWD_CASES = CASES + [wl(8, 1, 2048, 16, 2, 128, rope=False)]   # kv-heads replicated (R = 4)
+
+
+def _folded_bwd(run):
+    b = run.buf
+    outs = {n: torch.full_like(getattr(b, n), float("nan")) for n in ("dq_seq", "dk_seq", "dv_seq")}
+    U.ulysses_attn_bwd_folded(run.prob, b.q_seq, b.k_seq, b.v_seq, b.o_seq, b.lse, b.do_seq,
+                              outs["dq_seq"], outs["dk_seq"], outs["dv_seq"], b.ws)
+    torch.cuda.synchronize()
+    assert U.ulysses_read_status(b.ws) == 0
+    return outs
+
+
+@pytest.mark.parametrize("w", BWD_CASES, ids=lambda w: f"P{w.P}B{w.B}S{w.S}h{w.n_head}kv{w.n_kv_head}D{w.head_dim}{'c' if w.causal else 'n'}")
+def test_folded_backward_equals_the_packed_backward_bit_exact(w):
+    """The dK/dV and dQ kernels read the same tiles through the sequence-layout
+    maps as through the packed buffers, and delta is formed from the same O and
+    dO values in the same order: every gradient bit for bit."""
+    w = w.with_(backward=True)
+    run = GpuRun(w, backward=True)
+    run.forward()
+    run.backward()
+    outs = _folded_bwd(run)
+    for n, t in outs.items():
+        assert torch.equal(t, getattr(run.buf, n)), n
+
+
+def test_folded_backward_matches_oracle():
+    w = CASES[0].with_(backward=True)
+    run = GpuRun(w, backward=True)
+    o, lse = _folded(run)
+    run.buf.o_seq.copy_(o)
+    run.buf.lse.copy_(lse)
+    outs = _folded_bwd(run)
+    x = oracle_inputs(run.inputs)
+    want = oracle.backward(oracle_problem(w), x["q"], x["k"], x["v"], x["do"])
+    for n in ("dq_seq", "dk_seq", "dv_seq"):
+        assert_close(to64(outs[n]), np.stack(want[n]), w, "folded " + n)
+
+
+def test_folded_backward_full_size_pages_sizing_without_rope():
+    w = WORKLOADS["C4"].with_(use_rope=False, backward=True)
+    run = GpuRun(w, backward=True)
+    run.forward()
+    run.backward()
+    outs = _folded_bwd(run)
+    for n, t in outs.items():
+        assert torch.equal(t, getattr(run.buf, n)), n
+
+
+@pytest.mark.parametrize("w", [wl(2, 1, 512, 4, 2, 128, rope=True),          # RoPE must be applied by the producer
+                               wl(2, 1, 200, 4, 2, 128, rope=False),         # Sl = 100: tiles would straddle ranks
+                               wl(8, 1, 1024, 4, 4, 128, rope=False).with_(ring=4)])   # no hybrid form
+def test_folded_backward_refuses_what_it_cannot_fold(w):
+    run = GpuRun(w.with_(backward=True), backward=True)
+    b = run.buf
+    with pytest.raises(U.UlyssesError) as e:
+        U.ulysses_attn_bwd_folded(run.prob, b.q_seq, b.k_seq, b.v_seq, b.o_seq, b.lse, b.do_seq,
+                                  b.dq_seq, b.dk_seq, b.dv_seq, b.ws)
+    assert e.value.code == -4

@@ -26,7 +26,7 @@ STATUS_FWD_TIMEOUT, STATUS_BWD_TIMEOUT, STATUS_ROPE_TABLE, STATUS_SMEM_ALIGN, ST
 
 EXPORTS = ("ulysses_validate", "ulysses_workspace_bytes", "ulysses_workspace_init",
            "ulysses_read_status", "ulysses_pack_qkv", "ulysses_attn_fwd", "ulysses_unpack_out",
-           "ulysses_attn_bwd", "ulysses_attn_fwd_folded", "ulysses_status_string")
+           "ulysses_attn_bwd", "ulysses_attn_fwd_folded", "ulysses_attn_bwd_folded", "ulysses_status_string")
 
 
 class UlyssesError(RuntimeError):
@@ -123,6 +123,7 @@ def lib():
         L.ulysses_unpack_out.argtypes = [P, vp, vp, vp]
         L.ulysses_attn_fwd_folded.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_attn_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.ulysses_attn_bwd_folded.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_attn_bwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.ulysses_attn_bwd_prepare.argtypes = [P, vp, vp, vp, vp, sz, vp]
         L.ulysses_qkv_proj_pack.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -200,6 +201,15 @@ def ulysses_attn_fwd_folded(prob, q_seq, k_seq, v_seq, o_seq, lse, ws, stream=No
     _check("ulysses_attn_fwd_folded", lib().ulysses_attn_fwd_folded(
         ctypes.byref(prob.c()), _ptr(q_seq), _ptr(k_seq), _ptr(v_seq), _ptr(o_seq), _ptr(lse),
         _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def ulysses_attn_bwd_folded(prob, q_seq, k_seq, v_seq, o_seq, lse, do_seq, dq_seq, dk_seq, dv_seq, ws,
+                            stream=None):
+    """The folded backward: q, k, v, O and dO read in sequence layout, the
+    gradients written in sequence layout (RoPE off, S/P % 128 == 0)."""
+    _check("ulysses_attn_bwd_folded", lib().ulysses_attn_bwd_folded(
+        ctypes.byref(prob.c()), _ptr(q_seq), _ptr(k_seq), _ptr(v_seq), _ptr(o_seq), _ptr(lse), _ptr(do_seq),
+        _ptr(dq_seq), _ptr(dk_seq), _ptr(dv_seq), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def ulysses_unpack_out(prob, o_head, o_seq, stream=None):

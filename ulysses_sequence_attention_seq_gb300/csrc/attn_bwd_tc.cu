@@ -66,6 +66,10 @@ struct BwdParams {
   // head-layout buffer of rank (pos / Cs) * Pu + member, row pos % Cs.
   int Pu, Cs;
   int Ld;                              // row stride of nlse / delta (Cs rounded up to 4)
+  // Folded addressing: q, dout and the K / V maps cover the sequence-sharded
+  // buffers [P*B][Sl][heads][D] instead of the head-layout ones (plain Ulysses,
+  // Sl a multiple of 128); nlse / delta keep their head-layout rows.
+  int folded;
   // Elements of the buffers the kernels read or write with plain loads and
   // stores (range checks of a checked build): dQ, dK / dV (or their float
   // partials), Q / dO in head layout, the nlse / delta rows, the RoPE table.
@@ -76,6 +80,29 @@ struct BwdParams {
 // CTA of member*B + batch = `rb`.
 __device__ __forceinline__ int hl_outer(const BwdParams &p, int rb, int pos) {
   return (pos / p.Cs) * p.Pu * p.B + rb;
+}
+
+// TMA coordinates (head, row, outer) of the 128 rows at position `pos` (a
+// multiple of 128) of local head `h` of the CTA's (member, batch) `rb`: in the
+// head-layout buffers, or, folded, in the sequence shard that holds them (rank
+// pos / Sl, row pos % Sl, the global head: member * heads_local + h, or
+// member / rep for a kv-head replicated over rep ranks).
+struct ActCoord {
+  int head, row, outer;
+};
+__device__ __forceinline__ ActCoord act_coord(const BwdParams &p, int rb, int h, int heads_local, int pos,
+                                              int rep) {
+  if (!p.folded) return {h, pos % p.Cs, hl_outer(p, rb, pos)};
+  const int u = rb / p.B, b = rb - u * p.B;
+  return {rep > 1 ? u / rep : u * heads_local + h, pos % p.Sl, (pos / p.Sl) * p.B + b};
+}
+
+// Element offset of row `pos` of local q-head j of the CTA's (member, batch)
+// `rb` in q / dout (head layout, or folded the sequence-sharded buffer).
+__device__ __forceinline__ size_t q_row_offset(const BwdParams &p, int rb, int j, int pos, int D) {
+  if (!p.folded) return (((size_t)hl_outer(p, rb, pos) * p.Cs + pos % p.Cs) * p.hp + j) * D;
+  const int u = rb / p.B, b = rb - u * p.B, s = pos / p.Sl;
+  return ((((size_t)s * p.B + b) * p.Sl + (pos - s * p.Sl)) * p.n_head + u * p.hp + j) * D;
 }
 
 // True (and the status bit set) when the workspace's RoPE table was built for
@@ -291,25 +318,30 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmQ);
         mbar_arrive_expect_tx(bar + kKBarIn, 2 * L::kT);
+        const ActCoord kc = act_coord(p, rb, kl, p.kvp, n * 128, p.kv_rep);
         for (int c = 0; c < kCh; ++c) {
-          tma_load_4d(sK + c * 16384, &tmK, bar + kKBarIn, c * 64, kl, n * 128 % p.Cs, hl_outer(p, rb, n * 128));
-          tma_load_4d(sV + c * 16384, &tmV, bar + kKBarIn, c * 64, kl, n * 128 % p.Cs, hl_outer(p, rb, n * 128));
+          tma_load_4d(sK + c * 16384, &tmK, bar + kKBarIn, c * 64, kc.head, kc.row, kc.outer);
+          tma_load_4d(sV + c * 16384, &tmV, bar + kKBarIn, c * 64, kc.head, kc.row, kc.outer);
         }
         int issued_q = -1, issued_o = -1;
         for (int i = 0; i < n_iter; ++i) {
           const int qs = i % kQSlots, os = i % kOSlots;
           const int gi = i / n_m, m = m0 + i % n_m, j = kl * p.group + gi;
+          // the delta / nlse rows are in head layout in either mode
           const int mrow = m * 128 % p.Cs, mo = hl_outer(p, rb, m * 128);
+          const ActCoord qc = act_coord(p, rb, j, p.hp, m * 128, 1);
           if (!mbar_wait_bounded(bar + kKBarQEmpty + 8 * qs, ((i / kQSlots) & 1) ^ 1, abort_flag, gst)) break;
           mbar_arrive_expect_tx(bar + kKBarQFull + 8 * qs, L::kT + 512);
           for (int c = 0; c < kCh; ++c)
-            tma_load_4d(sQ + qs * L::kT + c * 16384, &tmQ, bar + kKBarQFull + 8 * qs, c * 64, j, mrow, mo);
+            tma_load_4d(sQ + qs * L::kT + c * 16384, &tmQ, bar + kKBarQFull + 8 * qs, c * 64, qc.head, qc.row,
+                        qc.outer);
           dev::tma_load_2d(sDl + qs * 512, &tmDl, bar + kKBarQFull + 8 * qs, mrow, mo * p.hp + j);
           issued_q = i;
           if (!mbar_wait_bounded(bar + kKBarOEmpty + 8 * os, ((i / kOSlots) & 1) ^ 1, abort_flag, gst)) break;
           mbar_arrive_expect_tx(bar + kKBarOFull + 8 * os, L::kT + 512);
           for (int c = 0; c < kCh; ++c)
-            tma_load_4d(sdO + os * L::kT + c * 16384, &tmdO, bar + kKBarOFull + 8 * os, c * 64, j, mrow, mo);
+            tma_load_4d(sdO + os * L::kT + c * 16384, &tmdO, bar + kKBarOFull + 8 * os, c * 64, qc.head, qc.row,
+                        qc.outer);
           dev::tma_load_2d(sL + os * 512, &tmL, bar + kKBarOFull + 8 * os, mrow, mo * p.hp + j);
           issued_o = i;
         }
@@ -692,15 +724,16 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
           const int ks = i % kKSlots, vs = i % kVSlots;
           if (!mbar_wait_bounded(bar + kQBarKEmpty + 8 * ks, ((i / kKSlots) & 1) ^ 1, abort_flag, gst)) break;
           mbar_arrive_expect_tx(bar + kQBarKFull + 8 * ks, L::kT);
+          const ActCoord kc = act_coord(p, rb, kl, p.kvp, i * 128, p.kv_rep);
           for (int c = 0; c < kCh; ++c)
-            tma_load_4d(sK + ks * L::kT + c * 16384, &tmK, bar + kQBarKFull + 8 * ks, c * 64, kl, i * 128 % p.Cs,
-                        hl_outer(p, rb, i * 128));
+            tma_load_4d(sK + ks * L::kT + c * 16384, &tmK, bar + kQBarKFull + 8 * ks, c * 64, kc.head, kc.row,
+                        kc.outer);
           issued_k = i;
           if (!mbar_wait_bounded(bar + kQBarVEmpty + 8 * vs, ((i / kVSlots) & 1) ^ 1, abort_flag, gst)) break;
           mbar_arrive_expect_tx(bar + kQBarVFull + 8 * vs, L::kT);
           for (int c = 0; c < kCh; ++c)
-            tma_load_4d(sV + vs * L::kT + c * 16384, &tmV, bar + kQBarVFull + 8 * vs, c * 64, kl, i * 128 % p.Cs,
-                        hl_outer(p, rb, i * 128));
+            tma_load_4d(sV + vs * L::kT + c * 16384, &tmV, bar + kQBarVFull + 8 * vs, c * 64, kc.head, kc.row,
+                        kc.outer);
           issued_v = i;
         }
         if (*abort_flag) {
@@ -798,7 +831,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       // Warpgroup 0 copies this thread's Q row, warpgroup 1 its dO row, into
       // TMEM (rows past S are zero).
       const int qr = live ? qi : 0;
-      const size_t qoff = (((size_t)hl_outer(p, rb, qr) * p.Cs + qr % p.Cs) * p.hp + j) * D;
+      const size_t qoff = q_row_offset(p, rb, j, qr, D);
       const __nv_bfloat16 *src = (g == 0 ? p.q : p.dout) + qoff;
       const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
       const bool get = live && in_range(p.status, (long long)qoff, D, p.qo_n);
@@ -911,17 +944,21 @@ enum BwdPart { kBwdDkDv = 1, kBwdDq = 2 };
 template <int D>
 cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void *q, const void *k,
                      const void *v, const void *do_head, const float *nlse, const float *delta,
-                     const void *ws, void *dq, void *dk, void *dv, uint32_t *status, int parts, cudaStream_t st) {
-  const int Pu = group_ranks(p), Cs = chunk_len(p);
+                     const void *ws, void *dq, void *dk, void *dv, uint32_t *status, int parts, bool folded,
+                     cudaStream_t st) {
+  const int Pu = group_ranks(p), Cs = chunk_len(p), Sl = p.S / p.P;
   const int hp = p.n_head / Pu, kvp = kv_per_rank(p), PB = p.P * p.B;
-  // head-layout maps: [P*B][Cs][heads][D] and rows [P*B*hp][Cs]
+  // head-layout maps [P*B][Cs][hp|kvp][D], or folded the sequence-sharded
+  // [P*B][Sl][n_head|n_kv_head][D]; the delta / nlse rows [P*B*hp][Cs] (Ld apart)
+  const int rows = folded ? Sl : Cs, qh = folded ? p.n_head : hp, kh = folded ? p.n_kv_head : kvp;
+  if (folded && (ring_of(p) > 1 || Sl % 128 != 0)) return cudaErrorInvalidValue;
   CUtensorMap mK128, mV128, mL, mDl, mQ128, mdO128;
-  bool ok = make_act_map(enc, &mK128, k, D, kvp, Cs, PB, 128) &&
-            make_act_map(enc, &mV128, v, D, kvp, Cs, PB, 128) &&
+  bool ok = make_act_map(enc, &mK128, k, D, kh, rows, PB, 128) &&
+            make_act_map(enc, &mV128, v, D, kh, rows, PB, 128) &&
             make_row_map(enc, &mL, nlse, Cs, delta_ld(p), PB * hp, 128) &&
             make_row_map(enc, &mDl, delta, Cs, delta_ld(p), PB * hp, 128) &&
-            make_act_map(enc, &mQ128, q, D, hp, Cs, PB, 128) &&
-            make_act_map(enc, &mdO128, do_head, D, hp, Cs, PB, 128);
+            make_act_map(enc, &mQ128, q, D, qh, rows, PB, 128) &&
+            make_act_map(enc, &mdO128, do_head, D, qh, rows, PB, 128);
   if (!ok) return cudaErrorInvalidValue;
   BwdParams bp;
   bp.B = p.B;
@@ -936,6 +973,7 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   bp.n_kv = p.n_kv_head;
   bp.Pu = Pu;
   bp.Cs = Cs;
+  bp.folded = folded ? 1 : 0;
   bp.dq_n = (long long)p.B * p.S * p.n_head * D;
   bp.dkv_n = kv_replicas(p) > 1 ? (long long)p.P * p.B * Cs * D : (long long)p.B * p.S * p.n_kv_head * D;
   bp.qo_n = (long long)p.B * p.S * p.n_head * D;
@@ -992,12 +1030,12 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
 
 cudaError_t launch_parts(const ulysses_problem &p, const TmaEncoder &enc, const void *q, const void *k,
                          const void *v, const void *do_head, const float *nlse, const float *delta,
-                         const void *ws, void *dq, void *dk, void *dv, uint32_t *status, int parts,
+                         const void *ws, void *dq, void *dk, void *dv, uint32_t *status, int parts, bool folded,
                          cudaStream_t st) {
   if (p.head_dim == 128)
-    return launch_d<128>(p, enc, q, k, v, do_head, nlse, delta, ws, dq, dk, dv, status, parts, st);
+    return launch_d<128>(p, enc, q, k, v, do_head, nlse, delta, ws, dq, dk, dv, status, parts, folded, st);
   if (p.head_dim == 64)
-    return launch_d<64>(p, enc, q, k, v, do_head, nlse, delta, ws, dq, dk, dv, status, parts, st);
+    return launch_d<64>(p, enc, q, k, v, do_head, nlse, delta, ws, dq, dk, dv, status, parts, folded, st);
   return cudaErrorInvalidValue;
 }
 
@@ -1008,21 +1046,23 @@ cudaError_t launch_attn_bwd_tc(const ulysses_problem &p, const TmaEncoder &enc, 
                                const float *delta, const void *ws, void *dq_seq, void *dk_seq,
                                void *dv_seq, uint32_t *status, cudaStream_t st) {
   return launch_parts(p, enc, q, k, v, do_head, nlse, delta, ws, dq_seq, dk_seq, dv_seq, status,
-                      kBwdDkDv | kBwdDq, st);
+                      kBwdDkDv | kBwdDq, false, st);
 }
 
 cudaError_t launch_attn_bwd_dkdv(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
                                  const void *k, const void *v, const void *do_head, const float *nlse,
                                  const float *delta, const void *ws, void *dk_seq, void *dv_seq,
-                                 uint32_t *status, cudaStream_t st) {
-  return launch_parts(p, enc, q, k, v, do_head, nlse, delta, ws, nullptr, dk_seq, dv_seq, status, kBwdDkDv, st);
+                                 uint32_t *status, cudaStream_t st, bool folded) {
+  return launch_parts(p, enc, q, k, v, do_head, nlse, delta, ws, nullptr, dk_seq, dv_seq, status, kBwdDkDv,
+                      folded, st);
 }
 
 cudaError_t launch_attn_bwd_dq(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
                                const void *k, const void *v, const void *do_head, const float *nlse,
                                const float *delta, const void *ws, void *dq_seq, uint32_t *status,
-                               cudaStream_t st) {
-  return launch_parts(p, enc, q, k, v, do_head, nlse, delta, ws, dq_seq, nullptr, nullptr, status, kBwdDq, st);
+                               cudaStream_t st, bool folded) {
+  return launch_parts(p, enc, q, k, v, do_head, nlse, delta, ws, dq_seq, nullptr, nullptr, status, kBwdDq, folded,
+                      st);
 }
 
 }  // namespace ulysses

@@ -62,10 +62,11 @@ cudaError_t launch_pack_qkv(const ulysses_problem &p, const void *q, const void 
 cudaError_t launch_unpack(const ulysses_problem &p, const void *o_head, void *o_seq,
                           cudaStream_t st);
 // dO seq -> head, delta[i] = sum_e dO[i][e] * O[i][e] and nlse[i] = -lse[i] * log2(e)
-// per (rank, b, head, row).
-cudaError_t launch_pack_do_delta(const ulysses_problem &p, const void *do_seq, const void *o_head,
+// per (rank, b, head, row).  Folded: `o` is O in sequence layout and dO is not
+// packed (do_head unused); delta and nlse are the same.
+cudaError_t launch_pack_do_delta(const ulysses_problem &p, const void *do_seq, const void *o,
                                  const float *lse, void *do_head, float *delta, float *nlse,
-                                 uint32_t *status, cudaStream_t st);
+                                 uint32_t *status, cudaStream_t st, bool folded = false);
 // Replicated kv-heads: dk_seq/dv_seq (bf16, sequence layout) = the sum over
 // each kv-head's replicas of their float partials, in rank order; dK also
 // scaled by `scale` and rotated back by the RoPE angle of its position.
@@ -103,14 +104,16 @@ cudaError_t launch_qkv_proj_pack(const ulysses_problem &p, const TmaEncoder &enc
 cudaError_t launch_out_proj_unpack(const ulysses_problem &p, const TmaEncoder &enc, const void *o_head,
                                    const void *w, const void *bias, void *y, const void *ws, cudaStream_t st);
 // The two kernels of launch_attn_bwd_tc on their own (dK/dV, then dQ).
+// folded: q/k/v/do are the sequence-sharded buffers (plain Ulysses, S/P % 128
+// == 0); the gradients are written in sequence layout either way.
 cudaError_t launch_attn_bwd_dkdv(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
                                  const void *k, const void *v, const void *do_head, const float *nlse,
                                  const float *delta, const void *ws, void *dk_seq, void *dv_seq,
-                                 uint32_t *status, cudaStream_t st);
+                                 uint32_t *status, cudaStream_t st, bool folded = false);
 cudaError_t launch_attn_bwd_dq(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
                                const void *k, const void *v, const void *do_head, const float *nlse,
                                const float *delta, const void *ws, void *dq_seq, uint32_t *status,
-                               cudaStream_t st);
+                               cudaStream_t st, bool folded = false);
 
 // Heads per CTA group (see grouped_order): as many heads as keep the tiles
 // their CTAs stream (per_head_bytes each) within about 48 MiB of L2.  A grid

@@ -274,10 +274,13 @@ __global__ void rope_table_kernel(float *cs, float *sn, int S, int D, double bas
 
 // dO: seq -> head, plus delta[d][b][j][pos] = sum_e dO * O (O read in head layout)
 // and nlse = -lse * log2(e) at the same index (the exponent offset the backward
-// kernels add to scale * s * log2(e)).
+// kernels add to scale * s * log2(e)).  kFolded: O is read in sequence layout,
+// at dO's own offset, and dO is not packed (the folded backward reads it in
+// place); delta and nlse as above.
 // One block per token row at a time (grid-stride over rows): the row's index
 // arithmetic is done once, and its H*D/8 (head, 16-byte chunk) tasks are
 // spread over the block's threads, D/8 consecutive lanes per head; bf16 only.
+template <bool kFolded>
 __global__ void __launch_bounds__(kThreads)
     pack_do_delta_kernel(const __nv_bfloat16 *__restrict__ dout, const __nv_bfloat16 *__restrict__ o,
                          const float *__restrict__ lse, __nv_bfloat16 *__restrict__ do_head,
@@ -314,8 +317,8 @@ __global__ void __launch_bounds__(kThreads)
       const long long seq_off = (row * H + g) * D + c * 8;
       if (live && in_range(status, seq_off, 8, act_n) && in_range(status, head_row + c * 8, 8, act_n)) {
         const uint4 x = __ldg(reinterpret_cast<const uint4 *>(dout + seq_off));
-        const uint4 y = __ldg(reinterpret_cast<const uint4 *>(o + head_row + c * 8));
-        *reinterpret_cast<uint4 *>(do_head + head_row + c * 8) = x;
+        const uint4 y = __ldg(reinterpret_cast<const uint4 *>(o + (kFolded ? seq_off : head_row + c * 8)));
+        if (!kFolded) *reinterpret_cast<uint4 *>(do_head + head_row + c * 8) = x;
         const __nv_bfloat162 *px = reinterpret_cast<const __nv_bfloat162 *>(&x);
         const __nv_bfloat162 *py = reinterpret_cast<const __nv_bfloat162 *>(&y);
 #pragma unroll
@@ -447,12 +450,13 @@ cudaError_t launch_unpack(const ulysses_problem &p, const void *o_head, void *o_
   return launch_perm(p, pp, st);
 }
 
-cudaError_t launch_pack_do_delta(const ulysses_problem &p, const void *do_seq, const void *o_head,
+cudaError_t launch_pack_do_delta(const ulysses_problem &p, const void *do_seq, const void *o,
                                  const float *lse, void *do_head, float *delta, float *nlse,
-                                 uint32_t *status, cudaStream_t st) {
+                                 uint32_t *status, cudaStream_t st, bool folded) {
   const int grid = grid_for((long long)p.B * p.S);  // one token row per block at a time
-  pack_do_delta_kernel<<<grid, kThreads, 0, st>>>(
-      static_cast<const __nv_bfloat16 *>(do_seq), static_cast<const __nv_bfloat16 *>(o_head),
+  auto kernel = folded ? pack_do_delta_kernel<true> : pack_do_delta_kernel<false>;
+  kernel<<<grid, kThreads, 0, st>>>(
+      static_cast<const __nv_bfloat16 *>(do_seq), static_cast<const __nv_bfloat16 *>(o),
       lse, static_cast<__nv_bfloat16 *>(do_head), delta, nlse, p.P, p.B, p.S / p.P, p.n_head,
       p.head_dim, group_ranks(p), chunk_len(p), delta_ld(p), status);
   return cudaGetLastError();

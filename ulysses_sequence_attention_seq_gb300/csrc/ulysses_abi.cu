@@ -421,6 +421,47 @@ int ulysses_attn_bwd(const ulysses_problem *prob, const void *q_head, const void
   return ulysses_attn_bwd_dq(prob, q_head, k_head, v_head, dq_seq, ws, ws_bytes, stream);
 }
 
+int ulysses_attn_bwd_folded(const ulysses_problem *prob, const void *q_seq, const void *k_seq,
+                            const void *v_seq, const void *o_seq, const float *lse, const void *do_seq,
+                            void *dq_seq, void *dk_seq, void *dv_seq, void *ws, size_t ws_bytes,
+                            ulysses_stream_t stream) {
+  const NvtxRange range("ulysses_attn_bwd_folded");
+  int rc = bwd_common(prob, ws, ws_bytes);
+  if (rc) return rc;
+  const ulysses_problem &p = *prob;
+  if (p.use_rope || (p.S / p.P) % 128 != 0 || ring_of(p) > 1) return ULYSSES_ERR_UNSUPPORTED;
+  const size_t nq = act_bytes(p, p.n_head), nk = act_bytes(p, p.n_kv_head);
+  const size_t nl = (size_t)p.B * p.n_head * p.S * sizeof(float);
+  const Span in[6] = {{q_seq, nq}, {k_seq, nk}, {v_seq, nk}, {o_seq, nq}, {lse, nl}, {do_seq, nq}};
+  const Span out[4] = {{dq_seq, nq}, {dk_seq, nk}, {dv_seq, nk}, {ws, ws_bytes}};
+  if ((rc = check_spans(in, 6, out, 4))) return rc;
+  TmaEncoder enc;
+  if (!get_tma_encoder(&enc)) return ULYSSES_ERR_CUDA;
+  const WorkspaceLayout L = workspace_layout(p);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t *status = reinterpret_cast<uint32_t *>(w + L.status);
+  const float *nlse = reinterpret_cast<const float *>(w + L.nlse);
+  const float *delta = reinterpret_cast<const float *>(w + L.delta);
+  // delta and the base-2 LSE from O and dO in sequence layout (no dO pack)
+  cudaError_t e = launch_pack_do_delta(p, do_seq, o_seq, lse, nullptr, reinterpret_cast<float *>(w + L.delta),
+                                       reinterpret_cast<float *>(w + L.nlse), status, st, true);
+  if (e != cudaSuccess) return cuda_rc(e);
+  if (kv_replicas(p) > 1) {
+    float *dkp = reinterpret_cast<float *>(w + L.dkpart), *dvp = reinterpret_cast<float *>(w + L.dvpart);
+    e = launch_attn_bwd_dkdv(p, enc, q_seq, k_seq, v_seq, do_seq, nlse, delta, ws, dkp, dvp, status, st, true);
+    if (e == cudaSuccess) {
+      const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)p.head_dim);
+      e = launch_kv_reduce(p, dkp, dvp, dk_seq, dv_seq, scale, ws, st);
+    }
+  } else {
+    e = launch_attn_bwd_dkdv(p, enc, q_seq, k_seq, v_seq, do_seq, nlse, delta, ws, dk_seq, dv_seq, status, st,
+                             true);
+  }
+  if (e != cudaSuccess) return cuda_rc(e);
+  return cuda_rc(launch_attn_bwd_dq(p, enc, q_seq, k_seq, v_seq, do_seq, nlse, delta, ws, dq_seq, status, st, true));
+}
+
 const char *ulysses_status_string(int code) {
   switch (code) {
     case ULYSSES_OK: return "ok";
