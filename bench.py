@@ -40,15 +40,16 @@ METRIC = "tokens/s + attn TFLOP/s (S=32K, 32 heads, P=8 virtual); seq↔head per
 # ------------------------------------------------------------------ helpers
 
 # DRAM bytes (read + write) per launch of a kernel on a workload, from one ncu
-# capture of this build (the launch-list summaries under profiles/ give the
+# capture of this build: the mean over the launches of the bench's own steps
+# (3 warm-up + 2 timed; the launch-list summaries under profiles/ give the
 # commands and the tables); a kernel changed since its capture has no entry.
 TRAFFIC = {
-    ("attn_fwd", "C4"): 1180097837,
-    ("bwd_dkdv", "C4"): 1882788892,
-    ("bwd_dq", "C4"): 1769575339,
-    ("attn_fwd", "C4-ring8"): 1202139961,
-    ("bwd_dkdv", "C4-ring8"): 1899695417,
-    ("bwd_dq", "C4-ring8"): 1811152697,
+    ("attn_fwd", "C4"): 1179509350,
+    ("bwd_dkdv", "C4"): 1792275866,
+    ("bwd_dq", "C4"): 1727045376,
+    ("attn_fwd", "C4-ring8"): 1205396685,
+    ("bwd_dkdv", "C4-ring8"): 1825418240,
+    ("bwd_dq", "C4-ring8"): 1798017178,
 }
 
 

@@ -126,17 +126,36 @@ __device__ __forceinline__ void store_plain(__nv_bfloat16 *dst, const uint32_t (
   for (int v = 0; v < 4; ++v) d[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
 }
 
+// The cos / sin of rotation pairs [i0, i0+32) at one position, read ahead of
+// the epilogue that undoes the rotation: `rope_prefetch` asks L2 for the two
+// 128-byte rows (kept with evict-last priority: every head's CTAs over the
+// same rows read them) when a CTA starts, `rope_load` brings them into
+// registers while the last products are still running.
+struct RopeRow {
+  float4 c[8], s[8];
+};
+__device__ __forceinline__ void rope_prefetch(const float *cs, const float *sn) {
+  asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(cs));
+  asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(sn));
+}
+__device__ __forceinline__ void rope_load(RopeRow &a, const float *cs, const float *sn) {
+#pragma unroll
+  for (int v = 0; v < 8; ++v) {
+    a.c[v] = __ldg(reinterpret_cast<const float4 *>(cs) + v);
+    a.s[v] = __ldg(reinterpret_cast<const float4 *>(sn) + v);
+  }
+}
+
 // Columns [i0, i0+32) (x) and [i0+D/2, i0+D/2+32) (y) of a gradient row:
 // scale, undo the rotation by the position's angle (x' = x cos + y sin,
-// y' = y cos - x sin), round to bf16 and store.
+// y' = y cos - x sin) when `rot`, round to bf16 and store.
 __device__ __forceinline__ void store_unrotated(__nv_bfloat16 *dx, __nv_bfloat16 *dy, uint32_t (&x)[32],
-                                                uint32_t (&y)[32], float scale, const float *cs,
-                                                const float *sn) {
-  if (cs) {
+                                                uint32_t (&y)[32], float scale, bool rot, const RopeRow &a) {
+  if (rot) {
 #pragma unroll
     for (int e = 0; e < 32; e += 4) {
-      const float4 c4 = *reinterpret_cast<const float4 *>(cs + e);
-      const float4 s4 = *reinterpret_cast<const float4 *>(sn + e);
+      const float4 c4 = a.c[e / 4];
+      const float4 s4 = a.s[e / 4];
       const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, ss[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -438,6 +457,13 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
     const int r = w4 * 32 + lane;  // key row within the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)(w4 * 32) << 16;
     const int kvr = n * 128 + r;
+    // dK's epilogue undoes the rotation of key row kvr: pairs [g*32, g*32+32)
+    // (warpgroup 0 alone for D = 64)
+    const bool rot = p.rope_cos && p.kv_rep == 1 && (D == 128 || g == 0) && kvr < p.S &&
+                     in_range(p.status, (long long)kvr * (D / 2), D / 2, p.rope_n);
+    const float *rcs = rot ? p.rope_cos + (size_t)kvr * (D / 2) + g * 32 : nullptr;
+    const float *rsn = rot ? p.rope_sin + (size_t)kvr * (D / 2) + g * 32 : nullptr;
+    if (rot) rope_prefetch(rcs, rsn);
     bool ok = true;
     for (int i = 0; i < n_iter; ++i) {
       const int qs = i % kQSlots, os = i % kOSlots;
@@ -504,6 +530,8 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
       mbar_arrive(bar + kKBarDSFull);
     }
     // ------------------------------------------------------------ epilogue
+    RopeRow angles;
+    if (ok && rot) rope_load(angles, rcs, rsn);
     if (ok) ok = warp_wait(bar + kKBarAcc, 0, abort_flag, gst);
     if (ok && p.kv_rep > 1) {
       // Replicated kv-head: this rank's q-heads give only part of dK, dV; the
@@ -559,11 +587,7 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
         tmem_ld32(tdK + lane_base + i0, x);
         tmem_ld32(tdK + lane_base + D / 2 + i0, y);
         tmem_wait_ld();
-        if (put) {
-          const float *cs = p.rope_cos ? p.rope_cos + (size_t)kvr * (D / 2) + i0 : nullptr;
-          const float *sn = p.rope_sin ? p.rope_sin + (size_t)kvr * (D / 2) + i0 : nullptr;
-          store_unrotated(p.dk + row + i0, p.dk + row + D / 2 + i0, x, y, p.scale, cs, sn);
-        }
+        if (put) store_unrotated(p.dk + row + i0, p.dk + row + D / 2 + i0, x, y, p.scale, rot, angles);
       }
     }
   }
@@ -827,6 +851,13 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
     const uint32_t lane_base = (uint32_t)(w4 * 32) << 16;
     const int qi = m * 128 + r;
     const bool live = qi < p.S;
+    // dQ's epilogue undoes the rotation of query row qi: pairs [g*32, g*32+32)
+    // (warpgroup 0 alone for D = 64)
+    const bool rot = p.rope_cos && (D == 128 || g == 0) && live &&
+                     in_range(p.status, (long long)qi * (D / 2), D / 2, p.rope_n);
+    const float *rcs = rot ? p.rope_cos + (size_t)qi * (D / 2) + g * 32 : nullptr;
+    const float *rsn = rot ? p.rope_sin + (size_t)qi * (D / 2) + g * 32 : nullptr;
+    if (rot) rope_prefetch(rcs, rsn);
     {
       // Warpgroup 0 copies this thread's Q row, warpgroup 1 its dO row, into
       // TMEM (rows past S are zero).
@@ -908,6 +939,8 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       }
       mbar_arrive(bar + kQBarDSFull);
     }
+    RopeRow angles;
+    if (ok && rot) rope_load(angles, rcs, rsn);
     if (ok) ok = warp_wait(bar + kQBarAcc, 0, abort_flag, gst);
     if (ok && (D == 128 || g == 0)) {
       tc_fence_after_sync();
@@ -920,11 +953,8 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       tmem_ld32(tdQ + lane_base + D / 2 + i0, y);
       tmem_wait_ld();
       if (live && in_range(p.status, (long long)row, D, p.dq_n) &&
-          (!p.rope_cos || in_range(p.status, (long long)qi * (D / 2), D / 2, p.rope_n))) {
-        const float *cs = p.rope_cos ? p.rope_cos + (size_t)qi * (D / 2) + i0 : nullptr;
-        const float *sn = p.rope_sin ? p.rope_sin + (size_t)qi * (D / 2) + i0 : nullptr;
-        store_unrotated(p.dq + row + i0, p.dq + row + D / 2 + i0, x, y, p.scale, cs, sn);
-      }
+          (!p.rope_cos || in_range(p.status, (long long)qi * (D / 2), D / 2, p.rope_n)))
+        store_unrotated(p.dq + row + i0, p.dq + row + D / 2 + i0, x, y, p.scale, rot, angles);
     }
   }
 
