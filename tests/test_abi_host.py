@@ -117,6 +117,31 @@ def test_folded_backward_refusals(lib, kw):
     assert lib.ulysses_attn_bwd_folded(ctypes.byref(p.c()), *a[:10], nws, vp(0)) == -4
 
 
+def test_folded_backward_pointer_checks(lib):
+    """A foldable problem with a NULL, a misaligned or an overlapping buffer is
+    refused before anything is enqueued (fake addresses, never dereferenced)."""
+    vp = ctypes.c_void_p
+    p = prob(S=1024, use_rope=False)
+    nws = U.ulysses_workspace_bytes(p, 1)
+    nq = p.B * p.S * p.n_head * p.head_dim * 2
+    base = 1 << 40
+    bufs = [base + i * 4 * nq for i in range(10)]          # q k v o lse do dq dk dv ws, far apart
+
+    def call(b, n=nws):
+        return lib.ulysses_attn_bwd_folded(ctypes.byref(p.c()), *[vp(x) for x in b], n, vp(0))
+    for i in range(10):
+        b = list(bufs)
+        b[i] = 0
+        assert call(b) == (-7 if i == 9 else -1), i       # NULL (the workspace: ERR_WORKSPACE)
+    b = list(bufs)
+    b[0] += 8
+    assert call(b) == -5                                      # misaligned q
+    b = list(bufs)
+    b[6] = bufs[0]
+    assert call(b) == -6                                      # dQ written over q
+    assert call(bufs, nws - 256) == -7                        # workspace too small
+
+
 def test_status_strings(lib):
     for code in range(0, -9, -1):
         s = lib.ulysses_status_string(code)
