@@ -625,7 +625,9 @@ def main():
         "fwd_tokens_per_s": fwd_tokens,
         "attn_fwd_tflops": attn_tflops, "attn_fwd_ms": attn_ms,
         "attn_bwd_tflops": bwd_tflops, "attn_bwd_ms": bwd_ms,
-        "attn_bwd_flops_note": "backward algorithmic FLOPs = 2x forward (dV, dP, dQ, dK); the QK^T recompute is not counted",
+        "attn_bwd_tflops_2p5x": bwd_tflops * 1.25 if bwd_tflops else None,
+        "attn_bwd_flops_note": "backward algorithmic FLOPs = 2x forward (dV, dP, dQ, dK); the QK^T recompute is not "
+                               "counted (attn_bwd_tflops_2p5x counts it: 2.5x forward)",
         "pack_gbs": pack_gbs, "unpack_gbs": unpack_gbs,
         "kernel_ms": per,
         "kernel_ms_median": {k: statistics.median(v) for k, v in r["per"].items()},

@@ -1,10 +1,13 @@
 """bench.py's CPU legs, no GPU: the reference arm prints the contract's JSON
-line (the fp64 oracle timed on the host), and the oracle leg runs the ring
-hybrid's steps for a hybrid workload."""
+line (the fp64 oracle timed on the host), the oracle leg runs the ring
+hybrid's steps for a hybrid workload, the permutation byte counts, and the
+JSON line the GPU arm assembles from its measurements (fed fixed numbers)."""
 import json
 import os
 import subprocess
 import sys
+
+import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -49,3 +52,44 @@ def test_pack_bytes_count_replicas_within_an_all_to_all_group():
     assert bench.permute_bytes(EXTRA_WORKLOADS["C4-ring8"], 2) == 6 * 32 * per_head
     kv4 = EXTRA_WORKLOADS["C4-kv4"]
     assert bench.permute_bytes(kv4, 2) == per_head * (2 * 32 + 2 * 4 + 2 * 8)
+
+
+def _fake_measurements(backward, steps):
+    """What run_ulysses returns, with plausible timings (no GPU involved)."""
+    per = {"pack_qkv": [0.29] * steps, "attn_fwd": [5.4] * steps, "unpack_out": [0.08] * steps}
+    if backward:
+        per.update(bwd_prepare=[0.17] * steps, bwd_dkdv=[10.9] * steps, bwd_dq=[8.4] * steps)
+    total = sum(v[0] for v in per.values()) * steps
+    return dict(total_ms=total, per=per, clocks={"sm_mhz": 2040.0, "sm_max_mhz": 2070.0, "reasons": []},
+                e2e_ms=total * 1.03, h2d=1 << 30, d2h=1 << 30, launches=6 * steps, status=0, backward=backward,
+                folded={"fwd": {"unfolded_ms": 5.8, "ms": 5.6}, "bwd": {"unfolded_ms": 19.8, "ms": 19.9}},
+                ex2_rate=32.0, sms=152)
+
+
+def test_bench_line_carries_the_contract_keys(monkeypatch, capsys):
+    """The JSON line bench.py assembles from its measurements (run_ulysses
+    replaced by fixed numbers): every key the contract asks for, with the
+    roofline of the dominant kernel and its traffic."""
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setattr(bench, "run_ulysses", lambda args, w, rank, world: _fake_measurements(True, args.steps))
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--steps", "4", "--no-cpu-baseline"])
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.delenv("RANK", raising=False)
+    bench.main()
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "clocks", "gpu_launches"):
+        assert key in line, key
+    assert line["steps"] == 4 and line["warmup"] == 3 and line["n_gpus"] == 1
+    assert line["config"]["workload"] == "C4"
+    r = line["roofline"]
+    assert r["kernel"] == "dkdv_kernel<128>" and r["bound"] == "tensor"
+    assert r["traffic"] == bench.TRAFFIC[("bwd_dkdv", "C4")]
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-12
+    # dK/dV: dV, dP, dK = 1.5 forwards of algorithmic FLOPs over 10.9 ms
+    assert abs(r["achieved"] - 1.5 * bench.attn_fwd_flops(bench.WORKLOADS["C4"]) / 10.9e-3 / 1e12) < 1e-6
+    assert abs(line["attn_bwd_tflops_2p5x"] - 1.25 * line["attn_bwd_tflops"]) < 1e-9
+    assert line["value"] == pytest.approx(32768 / (line["ms_per_step"] * 1e-3))
+    assert set(line["e2e"]) == {"value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"}
+    assert line["folded_bwd"] == {"unfolded_ms": 19.8, "ms": 19.9}
