@@ -441,9 +441,3 @@ def unsharded(prob: Problem, Q, K, V, nthreads=None):
         q = rope_seq([q], prob.rope_base, +1)[0]
         k = rope_seq([k], prob.rope_base, +1)[0]
     return attention_unsharded(prob, q, k, np.asarray(V, dtype=np.float64), nthreads=nthreads)
-
-
-def a2a_bytes_formula(N_bytes: int, P: int) -> float:
-    """[CMP] "DeepSpeed Attention costs": an All-to-All of an N-byte global
-    tensor over P ranks sends and receives N*(P-1)/P^2 bytes per rank."""
-    return N_bytes * (P - 1) / (P * P)
