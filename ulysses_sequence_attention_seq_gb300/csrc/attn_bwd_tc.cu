@@ -1071,14 +1071,6 @@ cudaError_t launch_parts(const ulysses_problem &p, const TmaEncoder &enc, const 
 
 }  // namespace
 
-cudaError_t launch_attn_bwd_tc(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
-                               const void *k, const void *v, const void *do_head, const float *nlse,
-                               const float *delta, const void *ws, void *dq_seq, void *dk_seq,
-                               void *dv_seq, uint32_t *status, cudaStream_t st) {
-  return launch_parts(p, enc, q, k, v, do_head, nlse, delta, ws, dq_seq, dk_seq, dv_seq, status,
-                      kBwdDkDv | kBwdDq, false, st);
-}
-
 cudaError_t launch_attn_bwd_dkdv(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
                                  const void *k, const void *v, const void *do_head, const float *nlse,
                                  const float *delta, const void *ws, void *dk_seq, void *dv_seq,

@@ -90,11 +90,6 @@ cudaError_t launch_attn_fwd_simt(const ulysses_problem &p, const float *q, const
 cudaError_t launch_attn_fwd_tc(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
                                const void *k, const void *v, void *o, float *lse,
                                uint32_t *status, bool folded, cudaStream_t st);
-cudaError_t launch_attn_bwd_tc(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
-                               const void *k, const void *v, const void *do_head,
-                               const float *nlse, const float *delta, const void *ws,
-                               void *dq_seq, void *dk_seq, void *dv_seq, uint32_t *status,
-                               cudaStream_t st);
 // QKV projection of the sequence-sharded activations with the pack and RoPE in
 // the epilogue (qkv_proj_tc.cu); bias may be null.
 cudaError_t launch_qkv_proj_pack(const ulysses_problem &p, const TmaEncoder &enc, const void *x, const void *w,
@@ -103,7 +98,8 @@ cudaError_t launch_qkv_proj_pack(const ulysses_problem &p, const TmaEncoder &enc
 // (qkv_proj_tc.cu); needs S/P % 128 == 0; bias may be null.
 cudaError_t launch_out_proj_unpack(const ulysses_problem &p, const TmaEncoder &enc, const void *o_head,
                                    const void *w, const void *bias, void *y, const void *ws, cudaStream_t st);
-// The two kernels of launch_attn_bwd_tc on their own (dK/dV, then dQ).
+// The two tensor-core kernels of the backward (attn_bwd_tc.cu): dK/dV, then dQ,
+// reading the delta / nlse rows the dO step wrote into the workspace.
 // folded: q/k/v/do are the sequence-sharded buffers (plain Ulysses, S/P % 128
 // == 0); the gradients are written in sequence layout either way.
 cudaError_t launch_attn_bwd_dkdv(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
