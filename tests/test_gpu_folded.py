@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import oracle
-from pathcheck import GpuRun, LSE_BF16_MAX_ABS, assert_close, oracle_inputs, oracle_problem, to64
+from pathcheck import GpuRun, assert_close, assert_lse_close, oracle_inputs, oracle_problem, to64
 from test_gpu_forward import wl
 from ulysses_sequence_attention_seq_gb300 import binding as U
 from ulysses_sequence_attention_seq_gb300.synthetic import WORKLOADS
@@ -48,7 +48,7 @@ def test_folded_matches_oracle():
     x = oracle_inputs(run.inputs)
     want = oracle.forward(oracle_problem(w), x["q"], x["k"], x["v"])
     assert_close(to64(o), np.stack([a.reshape(w.B, w.Sl, -1) for a in want["o_seq"]]), w, "folded o_seq")
-    assert np.abs(to64(lse) - np.stack(want["lse"])).max() <= LSE_BF16_MAX_ABS
+    assert_lse_close(to64(lse), np.stack(want["lse"]), w, "folded lse")
 
 
 def test_folded_full_size_pages_sizing_without_rope():

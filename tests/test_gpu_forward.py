@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from pathcheck import (GpuRun, LSE_BF16_MAX_ABS, FP32_MAX_ABS, assert_close, oracle_inputs,
+from pathcheck import (GpuRun, assert_close, assert_lse_close, oracle_inputs,
                        oracle_problem, to64, ulp_bf16)
 from ulysses_sequence_attention_seq_gb300 import binding as U
 from ulysses_sequence_attention_seq_gb300.synthetic import WORKLOADS, Workload
@@ -109,8 +109,7 @@ def test_forward_matches_oracle(w):
     want_o = np.stack([a.reshape(w.B, w.Sl, -1) for a in want["o_seq"]])
     assert_close(got_o, want_o, w, "o_seq")
     want_lse = np.stack(want["lse"])
-    tol = FP32_MAX_ABS if w.dtype == "fp32" else LSE_BF16_MAX_ABS
-    assert np.abs(got_lse - want_lse).max() <= tol
+    assert_lse_close(got_lse, want_lse, w)
     # bit-exact consistency of the unpack with the kernel's own head-layout output
     o_head = to64(run.buf.o_head)
     hp = w.n_head // w.P
@@ -146,8 +145,7 @@ def test_forward_workloads(name):
     want_h = np.stack(want["o_head"])[:, :, sel]
     assert_close(got_h[:, :, sel], want_h, w, f"{name} o_head")
     want_lse = np.stack(want["lse"])[..., sel]
-    tol = FP32_MAX_ABS if w.dtype == "fp32" else LSE_BF16_MAX_ABS
-    assert np.abs(got_lse[..., sel] - want_lse).max() <= tol
+    assert_lse_close(got_lse[..., sel], want_lse, w, f"{name} lse")
     # the unpack is the exact inverse permutation of what the kernel wrote
     o_seq = run.buf.o_seq
     o_head = run.buf.o_head
@@ -172,7 +170,7 @@ def test_forward_at_the_longest_sequence():
     want = oracle.forward(oracle_problem(w), x["q"], x["k"], x["v"], rows=rows)
     got_h = to64(run.buf.o_head)
     assert_close(got_h[:, :, rows], np.stack(want["o_head"])[:, :, rows], w, "C5-128K o_head")
-    assert np.abs(to64(run.buf.lse)[..., rows] - np.stack(want["lse"])[..., rows]).max() <= LSE_BF16_MAX_ABS
+    assert_lse_close(to64(run.buf.lse)[..., rows], np.stack(want["lse"])[..., rows], w)
     o_seq, o_head = run.buf.o_seq, run.buf.o_head
     for d in (0, w.P - 1):
         for s in (0, w.P - 1):
@@ -230,7 +228,7 @@ def test_forward_moving_reference(slope, causal, D):
     got_o = to64(run.buf.o_seq)
     want_o = np.stack([a.reshape(w.B, w.Sl, -1) for a in want["o_seq"]])
     assert_close(got_o, want_o, w, "o_seq")
-    assert np.abs(to64(run.buf.lse) - np.stack(want["lse"])).max() <= LSE_BF16_MAX_ABS
+    assert_lse_close(to64(run.buf.lse), np.stack(want["lse"]), w)
 
 
 # KV-head replication: fewer kv-heads than ranks, each kv-head handed to the
@@ -269,8 +267,7 @@ def test_replicated_kv_forward_matches_oracle(w):
     got_o = to64(run.buf.o_seq)
     want_o = np.stack([a.reshape(w.B, w.Sl, -1) for a in want["o_seq"]])
     assert_close(got_o, want_o, w, "o_seq")
-    tol = FP32_MAX_ABS if w.dtype == "fp32" else LSE_BF16_MAX_ABS
-    assert np.abs(to64(run.buf.lse) - np.stack(want["lse"])).max() <= tol
+    assert_lse_close(to64(run.buf.lse), np.stack(want["lse"]), w)
 
 
 def test_replicated_kv_forward_full_size_sampled():
@@ -284,4 +281,4 @@ def test_replicated_kv_forward_full_size_sampled():
     rows = sample_rows(w, 24)
     want = oracle.forward(oracle_problem(w), x["q"], x["k"], x["v"], rows=rows)
     assert_close(to64(run.buf.o_head)[:, :, rows], np.stack(want["o_head"])[:, :, rows], w, "o_head")
-    assert np.abs(to64(run.buf.lse)[..., rows] - np.stack(want["lse"])[..., rows]).max() <= LSE_BF16_MAX_ABS
+    assert_lse_close(to64(run.buf.lse)[..., rows], np.stack(want["lse"])[..., rows], w)

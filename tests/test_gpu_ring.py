@@ -12,7 +12,7 @@ import torch
 
 import oracle
 from oracle import ring as RG
-from pathcheck import GpuRun, LSE_BF16_MAX_ABS, assert_close, oracle_inputs, oracle_problem, to64, ulp_bf16
+from pathcheck import GpuRun, assert_close, assert_lse_close, oracle_inputs, oracle_problem, to64, ulp_bf16
 from test_gpu_forward import sample_rows, wl
 from ulysses_sequence_attention_seq_gb300 import binding as U
 from ulysses_sequence_attention_seq_gb300.synthetic import EXTRA_WORKLOADS
@@ -93,7 +93,7 @@ def test_forward_matches_ring_oracle(w):
     want = RG.forward(oracle_problem(w), x["q"], x["k"], x["v"])
     got_o = to64(run.buf.o_seq)
     assert_close(got_o, np.stack([a.reshape(w.B, w.Sl, -1) for a in want["o_seq"]]), w, "o_seq")
-    assert np.abs(to64(run.buf.lse) - np.stack(want["lse"])).max() <= LSE_BF16_MAX_ABS
+    assert_lse_close(to64(run.buf.lse), np.stack(want["lse"]), w)
 
 
 @pytest.mark.parametrize("w", RING_CASES, ids=_id)
@@ -150,7 +150,7 @@ def test_full_size_pages_example():
         for u in (0, prob.Pu // 2, prob.Pu - 1):
             me = r * prob.Pu + u
             assert_close(got_h[me][:, mine], want["o_head"][me][:, mine], w, f"o_head rank {me}")
-            assert np.abs(got_lse[me][..., mine] - want["lse"][me][..., mine]).max() <= LSE_BF16_MAX_ABS
+            assert_lse_close(got_lse[me][..., mine], want["lse"][me][..., mine], w, f"lse rank {me}")
     del run, x, want
     torch.cuda.empty_cache()
     _same_as_plain_ulysses(w, backward=True)
