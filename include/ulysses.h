@@ -364,8 +364,11 @@ int ulysses_selftest_ex2_rate(void *cycles, size_t bytes, long long *ex2_per_lau
  * 32 MiB array in the library's own device memory, which every GPU that loads
  * the library holds until the process exits.  A problem whose phase-1
  * workspace (ulysses_workspace_bytes(prob, 1)) exceeds 32 MiB is rejected with
- * ULYSSES_ERR_WORKSPACE before anything is enqueued.  No device memory is
- * allocated by this call.
+ * ULYSSES_ERR_WORKSPACE before anything is enqueued; so are problems and
+ * pointers ulysses_attn_bwd would refuse (same codes, checked before the array
+ * is touched).  No device memory is allocated by this call.  Faults the
+ * kernels find are flagged in the array's status word: read it with
+ * ulysses_noalloc_read_status.
  * The first call on each device looks up the array's device address (with that
  * device current); make that first call before any stream capture.  Every call
  * rebuilds the RoPE table and clears the status word in the array before the
@@ -377,6 +380,14 @@ int ulysses_attn_bwd_noalloc(const ulysses_problem *prob, const void *q_head, co
                              const void *v_head, const void *o_head, const float *lse,
                              const void *do_seq, void *dq_seq, void *dk_seq, void *dv_seq,
                              ulysses_stream_t stream);
+
+/* The status word of the scratch array ulysses_attn_bwd_noalloc uses on the
+ * current device (the bits of enum ulysses_device_status, as
+ * ulysses_read_status returns them for a workspace): waits for `stream`, then
+ * copies the word written by the noalloc calls enqueued before this point.
+ * Like that entry point, it has no counterpart in the pages.
+ * Errors: ULYSSES_ERR_ARG (NULL status), ULYSSES_ERR_CUDA. */
+int ulysses_noalloc_read_status(uint32_t *status, ulysses_stream_t stream);
 
 /* A static English description of a return code. */
 const char *ulysses_status_string(int code);

@@ -207,3 +207,17 @@ def test_selftest_wait_timeout_argument_checks(lib):
     assert fn(vp(0x10000), 4096, 0, vp(0)) == -1            # no limit
     assert fn(vp(0x10000), 4096, 3000000000, vp(0)) == -1   # above 2 s
     assert fn(vp(0x10008), 4096, 1000000, vp(0)) == -5      # misaligned
+
+
+def test_noalloc_refusals_before_any_device_call(lib):
+    """The workspace-free backward refuses an fp32 problem, and a problem whose
+    backward scratch exceeds its fixed 32 MiB array, before it touches the GPU;
+    its status reader refuses a NULL destination."""
+    vp = ctypes.c_void_p
+    ptrs = [vp((1 << 40) + i * (1 << 30)) for i in range(9)]
+    pf = prob(dtype=U.FP32, S=1024)
+    assert lib.ulysses_attn_bwd_noalloc(ctypes.byref(pf.c()), *ptrs, vp(0)) == -4
+    big = prob(S=32768, n_kv_head=32)
+    assert U.ulysses_workspace_bytes(big, 1) > 32 << 20
+    assert lib.ulysses_attn_bwd_noalloc(ctypes.byref(big.c()), *ptrs, vp(0)) == -7
+    assert lib.ulysses_noalloc_read_status(None, vp(0)) == -1

@@ -1,8 +1,8 @@
 """The range-checked build (-DULYSSES_CHECK_BOUNDS: every plain global load
 and store checked against its buffer) runs the whole path without a single
 failed check and gives bit for bit what the normal build gives: forward,
-backward, the fp32 forward, replicated kv-heads, the ring hybrid, the folded
-forward and backward and the two projections.  The checked library runs in a
+backward, the workspace-free backward, the fp32 forward, replicated kv-heads,
+the ring hybrid, the folded forward and backward and the two projections.  The checked library runs in a
 child process (ULYSSES_LIB)."""
 import os
 import subprocess
@@ -42,6 +42,13 @@ for n, w in enumerate(cases):
     for name in names:
         out[f"{n}/{name}"] = getattr(run.buf, name).cpu()
     out[f"{n}/status"] = torch.tensor(U.ulysses_read_status(run.buf.ws))
+    if n == 0:  # the workspace-free backward on the same buffers
+        b = run.buf
+        grads = [torch.empty_like(getattr(b, g)) for g in ("dq_seq", "dk_seq", "dv_seq")]
+        U.ulysses_attn_bwd_noalloc(run.prob, b.q_head, b.k_head, b.v_head, b.o_head, b.lse, b.do_seq, *grads)
+        for g, t in zip(("dq_seq", "dk_seq", "dv_seq"), grads):
+            out[f"noalloc/{g}"] = t.cpu()
+        out["noalloc/status"] = torch.tensor(U.ulysses_noalloc_read_status())
 # the folded forward and backward (RoPE off, S/P = 256, kv-heads replicated)
 w = wl(8, 1, 2048, 16, 2, 128, rope=False).with_(backward=True)
 run = GpuRun(w, backward=True)

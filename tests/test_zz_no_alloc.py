@@ -2,20 +2,25 @@
 
 It serves callers that cannot allocate device memory (their allocator is owned
 by someone else, or they must not call cudaMalloc on this path): its scratch
-is the library's fixed 32 MiB device array.  Its results must match the
-ordinary backward (which takes a caller workspace) on two calls in a row, and
-a problem too large for the fixed array must be refused up front.  This file
-sorts last so that a run stopping at the first failure has run everything else.
+is the library's fixed 32 MiB device array.  It runs the very kernels of the
+ordinary backward (which takes a caller workspace) on the same inputs, so its
+gradients must equal that backward's bit for bit, on two calls in a row, with
+the array's status word clear after each.  Problems the backward would refuse,
+or too large for the fixed array, must be refused up front.  This file sorts
+last so that a run stopping at the first failure has run everything else.
 """
-import numpy as np
+import dataclasses
+
 import pytest
 import torch
 
-from pathcheck import GpuRun, assert_close, to64
+from pathcheck import GpuRun
 from test_gpu_forward import wl
 from ulysses_sequence_attention_seq_gb300 import binding as U
 
 pytestmark = pytest.mark.gpu
+
+GRADS = ("dq_seq", "dk_seq", "dv_seq")
 
 
 def _noalloc(run, outs):
@@ -23,20 +28,21 @@ def _noalloc(run, outs):
     U.ulysses_attn_bwd_noalloc(run.prob, b.q_head, b.k_head, b.v_head, b.o_head, b.lse, b.do_seq, *outs)
 
 
-@pytest.mark.parametrize("w", [wl(2, 1, 424, 4, 2, 128), wl(4, 1, 512, 8, 8, 64, causal=False)],
-                         ids=["P2S424gqaD128", "P4S512D64nc"])
-def test_noalloc_backward_matches_workspace_backward_twice(w):
+@pytest.mark.parametrize("w", [wl(2, 1, 424, 4, 2, 128), wl(4, 1, 512, 8, 8, 64, causal=False),
+                               wl(4, 1, 512, 8, 8, 64, causal=False, rope=False)],
+                         ids=["P2S424gqaD128", "P4S512D64nc", "P4S512D64nc-norope"])
+def test_noalloc_backward_equals_workspace_backward_twice(w):
     w = w.with_(backward=True)
     run = GpuRun(w, backward=True)
     run.forward()
     run.backward()                       # the ordinary entry point, caller workspace
-    ref = [to64(getattr(run.buf, n)) for n in ("dq_seq", "dk_seq", "dv_seq")]
+    ref = [getattr(run.buf, n).clone() for n in GRADS]
     for _ in range(2):                   # two calls in a row share the fixed array
-        outs = [torch.full_like(getattr(run.buf, n), float("nan")) for n in ("dq_seq", "dk_seq", "dv_seq")]
+        outs = [torch.full_like(getattr(run.buf, n), float("nan")) for n in GRADS]
         _noalloc(run, outs)
-        torch.cuda.synchronize()
-        for got, want, name in zip(outs, ref, ("dq", "dk", "dv")):
-            assert_close(to64(got), want, w, f"noalloc {name}")
+        assert U.ulysses_noalloc_read_status() == 0   # waits for the stream
+        for got, want, name in zip(outs, ref, GRADS):
+            assert torch.equal(got, want), f"noalloc {name} differs from the workspace backward"
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch():
@@ -47,3 +53,23 @@ def test_noalloc_refuses_problems_beyond_its_scratch():
     with pytest.raises(U.UlyssesError) as e:
         U.ulysses_attn_bwd_noalloc(p, dummy, dummy, dummy, dummy, lse, dummy, dummy, dummy, dummy)
     assert e.value.code == -7
+
+
+def test_noalloc_refuses_what_the_backward_refuses():
+    """An fp32 problem (no backward kernel) and aliased outputs are refused with
+    the ordinary backward's codes, and the array is left as the last call left it."""
+    w = wl(2, 1, 256, 4, 4, 64).with_(backward=True)
+    run = GpuRun(w, backward=True)
+    run.forward()
+    b = run.buf
+    outs = [torch.empty_like(getattr(b, n)) for n in GRADS]
+    pf = dataclasses.replace(run.prob, dtype=U.FP32)
+    with pytest.raises(U.UlyssesError) as e:
+        U.ulysses_attn_bwd_noalloc(pf, b.q_head, b.k_head, b.v_head, b.o_head, b.lse, b.do_seq, *outs)
+    assert e.value.code == -4
+    with pytest.raises(U.UlyssesError) as e:   # dK written over dQ
+        U.ulysses_attn_bwd_noalloc(run.prob, b.q_head, b.k_head, b.v_head, b.o_head, b.lse, b.do_seq,
+                                   outs[0], outs[0], outs[2])
+    assert e.value.code == -6
+    _noalloc(run, outs)
+    assert U.ulysses_noalloc_read_status() == 0

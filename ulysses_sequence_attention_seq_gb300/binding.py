@@ -125,6 +125,7 @@ def lib():
         L.ulysses_attn_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_attn_bwd_folded.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_attn_bwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.ulysses_noalloc_read_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
         L.ulysses_attn_bwd_prepare.argtypes = [P, vp, vp, vp, vp, sz, vp]
         L.ulysses_qkv_proj_pack.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_out_proj_unpack.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
@@ -286,6 +287,13 @@ def ulysses_attn_bwd_noalloc(prob, q_head, k_head, v_head, o_head, lse, do_seq, 
     _check("ulysses_attn_bwd_noalloc", lib().ulysses_attn_bwd_noalloc(
         ctypes.byref(prob.c()), _ptr(q_head), _ptr(k_head), _ptr(v_head), _ptr(o_head), _ptr(lse),
         _ptr(do_seq), _ptr(dq_seq), _ptr(dk_seq), _ptr(dv_seq), _stream(stream)))
+
+
+def ulysses_noalloc_read_status(stream=None) -> int:
+    """Status word of the noalloc backward's scratch array (waits for the stream)."""
+    out = ctypes.c_uint32(0)
+    _check("ulysses_noalloc_read_status", lib().ulysses_noalloc_read_status(ctypes.byref(out), _stream(stream)))
+    return out.value
 
 
 # ---------------------------------------------------------------- buffers

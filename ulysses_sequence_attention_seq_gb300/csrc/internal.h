@@ -55,6 +55,13 @@ inline int kv_per_rank(const ulysses_problem &p) {
   return p.n_kv_head >= group_ranks(p) ? p.n_kv_head / group_ranks(p) : 1;
 }
 
+// Every host check of ulysses_attn_bwd (problem, bf16 / head_dim, phase-1
+// workspace size and alignment, pointers, alignment, overlaps) without
+// enqueueing anything; ULYSSES_OK or the code ulysses_attn_bwd would return.
+int check_bwd_call(const ulysses_problem *prob, const void *q_head, const void *k_head, const void *v_head,
+                   const void *o_head, const float *lse, const void *do_seq, const void *dq_seq,
+                   const void *dk_seq, const void *dv_seq, const void *ws, size_t ws_bytes);
+
 // ---- permutation kernels (permute.cu) ----
 cudaError_t launch_rope_table(const ulysses_problem &p, void *ws, cudaStream_t st);
 cudaError_t launch_pack_qkv(const ulysses_problem &p, const void *q, const void *k, const void *v,

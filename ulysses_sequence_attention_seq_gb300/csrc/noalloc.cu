@@ -24,6 +24,8 @@
 
 #include "internal.h"
 
+using ulysses::check_bwd_call;
+
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = 32ull << 20;  // 32 MiB
@@ -60,14 +62,29 @@ extern "C" int ulysses_attn_bwd_noalloc(const ulysses_problem *prob, const void 
                                         ulysses_stream_t stream) {
   int rc = ulysses_validate(prob);
   if (rc) return rc;
+  if (prob->dtype != ULYSSES_BF16 || (prob->head_dim != 64 && prob->head_dim != 128))
+    return ULYSSES_ERR_UNSUPPORTED;  // the backward's kernels are bf16, head_dim 64 or 128
   const size_t need = ulysses_workspace_bytes(prob, 1);
   if (need == 0 || need > kNoAllocScratchBytes) return ULYSSES_ERR_WORKSPACE;
   void *scratch = scratch_on_current_device();
   if (!scratch) return ULYSSES_ERR_CUDA;
+  // Every check the backward makes, with the scratch array in the place of the
+  // workspace, before anything is enqueued: a refused call leaves the array
+  // (and any earlier call still running on it) untouched.
+  rc = check_bwd_call(prob, q_head, k_head, v_head, o_head, lse, do_seq, dq_seq, dk_seq, dv_seq, scratch,
+                      kNoAllocScratchBytes);
+  if (rc) return rc;
   // Rebuild the RoPE table and clear the status word for this problem, then
   // run the ordinary backward on the fixed scratch.
   rc = ulysses_workspace_init(prob, scratch, kNoAllocScratchBytes, stream);
   if (rc) return rc;
   return ulysses_attn_bwd(prob, q_head, k_head, v_head, o_head, lse, do_seq, dq_seq, dk_seq, dv_seq,
                           scratch, kNoAllocScratchBytes, stream);
+}
+
+extern "C" int ulysses_noalloc_read_status(uint32_t *status, ulysses_stream_t stream) {
+  if (!status) return ULYSSES_ERR_ARG;
+  void *scratch = scratch_on_current_device();
+  if (!scratch) return ULYSSES_ERR_CUDA;
+  return ulysses_read_status(scratch, status, stream);
 }

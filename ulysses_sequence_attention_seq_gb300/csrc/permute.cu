@@ -355,9 +355,11 @@ cudaError_t launch_rope_table(const ulysses_problem &p, void *ws, cudaStream_t s
   uint8_t *base = static_cast<uint8_t *>(ws);
   uint32_t *hdr = reinterpret_cast<uint32_t *>(base + L.status);
   if (!p.use_rope) {
-    // clear the status word and write the key anyway
-    const uint32_t h[2] = {0u, rope_key(p)};
-    return cudaMemcpyAsync(hdr, h, sizeof h, cudaMemcpyHostToDevice, st);
+    // no table: one thread clears the status word and writes the key (a kernel,
+    // not a host copy, so nothing waits on the host and a captured graph holds
+    // no pointer to host memory)
+    rope_table_kernel<<<1, 32, 0, st>>>(nullptr, nullptr, 0, p.head_dim, 1.0, hdr, rope_key(p));
+    return cudaGetLastError();
   }
   float *cs = reinterpret_cast<float *>(base + L.rope);
   float *sn = cs + (size_t)p.S * (p.head_dim / 2);

@@ -403,11 +403,12 @@ int ulysses_attn_bwd_dq(const ulysses_problem *prob, const void *q_head, const v
                                     reinterpret_cast<uint32_t *>(w + L.status), (cudaStream_t)stream));
 }
 
-int ulysses_attn_bwd(const ulysses_problem *prob, const void *q_head, const void *k_head,
-                     const void *v_head, const void *o_head, const float *lse,
-                     const void *do_seq, void *dq_seq, void *dk_seq, void *dv_seq, void *ws,
-                     size_t ws_bytes, ulysses_stream_t stream) {
-  const NvtxRange range("ulysses_attn_bwd");
+}  // extern "C"
+
+int ulysses::check_bwd_call(const ulysses_problem *prob, const void *q_head, const void *k_head,
+                            const void *v_head, const void *o_head, const float *lse, const void *do_seq,
+                            const void *dq_seq, const void *dk_seq, const void *dv_seq, const void *ws,
+                            size_t ws_bytes) {
   int rc = bwd_common(prob, ws, ws_bytes);
   if (rc) return rc;
   const ulysses_problem &p = *prob;
@@ -415,7 +416,19 @@ int ulysses_attn_bwd(const ulysses_problem *prob, const void *q_head, const void
   const size_t nl = (size_t)p.B * p.n_head * p.S * sizeof(float);
   const Span in[6] = {{q_head, nq}, {k_head, nkh}, {v_head, nkh}, {o_head, nq}, {lse, nl}, {do_seq, nq}};
   const Span out[4] = {{dq_seq, nq}, {dk_seq, nk}, {dv_seq, nk}, {ws, ws_bytes}};
-  if ((rc = check_spans(in, 6, out, 4))) return rc;
+  return check_spans(in, 6, out, 4);
+}
+
+extern "C" {
+
+int ulysses_attn_bwd(const ulysses_problem *prob, const void *q_head, const void *k_head,
+                     const void *v_head, const void *o_head, const float *lse,
+                     const void *do_seq, void *dq_seq, void *dk_seq, void *dv_seq, void *ws,
+                     size_t ws_bytes, ulysses_stream_t stream) {
+  const NvtxRange range("ulysses_attn_bwd");
+  int rc = check_bwd_call(prob, q_head, k_head, v_head, o_head, lse, do_seq, dq_seq, dk_seq, dv_seq, ws,
+                          ws_bytes);
+  if (rc) return rc;
   if ((rc = ulysses_attn_bwd_prepare(prob, o_head, lse, do_seq, ws, ws_bytes, stream))) return rc;
   if ((rc = ulysses_attn_bwd_dkdv(prob, q_head, k_head, v_head, dk_seq, dv_seq, ws, ws_bytes, stream))) return rc;
   return ulysses_attn_bwd_dq(prob, q_head, k_head, v_head, dq_seq, ws, ws_bytes, stream);
