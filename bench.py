@@ -290,6 +290,13 @@ def run_ulysses(args, w, rank, world):
                 folded=folded, ex2_rate=ex2_rate, sms=sms)
 
 
+def line_config(w, passes, l2, parallelism):
+    """The `config` of a JSON line: the same keys on the GPU arm and the reference arm."""
+    return {"workload": w.name, "P": w.P, "ring": w.ring, "B": w.B, "S": w.S, "n_head": w.n_head,
+            "n_kv_head": w.n_kv_head, "head_dim": w.head_dim, "causal": w.causal, "rope": w.use_rope,
+            "passes": passes, "l2": l2, "parallelism": parallelism}
+
+
 def barrier(world):
     if world > 1:
         torch.distributed.barrier()
@@ -315,13 +322,19 @@ def job_throughput(units_per_rank, seconds_max, world):
 class OracleBench:
     """Times the fp64 oracle, as it stands, on a bounded sample of a workload.
 
-    One sampled step runs the oracle's steps in the path's order: split by
-    sequence, RoPE and the three loop All-to-Alls of Q, K, V in full;
-    attention for `n_rows` query rows of every head; the inverse All-to-All in
-    full.  The full step's time is estimated as layout time + attention time x
-    (query-key pairs of the full workload / pairs sampled)."""
+    One sampled step runs the oracle's steps in the path's order.  Forward:
+    split by sequence, RoPE and the three loop All-to-Alls of Q, K, V in full;
+    attention for `n_rows` random query rows of every head; the inverse
+    All-to-All in full.  Backward (workloads with one, plain Ulysses): the
+    All-to-All of dO in full; the attention backward of one (rank, batch,
+    kv-head) group, whose statistics phase (lse and delta of every row of the
+    group) runs in full and whose dQ and dK/dV phases run for `n_bwd_rows`
+    random query rows and key rows; the inverse All-to-Alls of dQ, dK, dV and
+    the inverse RoPE in full.  The full step's time is estimated as the layout
+    time + each attention phase's time x (query-key pairs of the full workload
+    / pairs sampled), the backward's groups being alike."""
 
-    def __init__(self, w, nthreads=None):
+    def __init__(self, w, nthreads=None, backward=None):
         sys.path.insert(0, os.path.join(ROOT, "tests"))
         import oracle
         from oracle import ring as oracle_ring
@@ -329,7 +342,9 @@ class OracleBench:
         self.ring = oracle_ring
         self.w = w
         self.nthreads = nthreads or (os.cpu_count() or 1)
-        ins = make_inputs(w, with_grad=False)
+        # the ring hybrid's oracle backward has no row sampling: forward only there
+        self.backward = (w.backward if backward is None else backward) and w.ring == 1
+        ins = make_inputs(w, with_grad=self.backward)
         self.x = {k: v.to(torch.float64).numpy() for k, v in ins.items()}
         del ins
         self.op = oracle.Problem(B=w.B, S=w.S, n_head=w.n_head, n_kv_head=w.n_kv_head, D=w.head_dim,
@@ -337,7 +352,17 @@ class OracleBench:
                                  rope_base=float(np.float32(w.rope_base)), ring=w.ring)
         self.rng = np.random.default_rng(0)
 
-    def step(self, n_rows):
+    @property
+    def passes(self):
+        return "fwd+bwd" if self.backward else "fwd"
+
+    def _full_pairs(self):
+        w = self.w
+        return w.S * (w.S + 1) / 2 if w.causal else float(w.S) * w.S
+
+    def step(self, n_rows, n_bwd_rows=None):
+        """One sampled step.  Returns (estimated full-step seconds, query rows
+        sampled in the forward, forward pairs sampled, wall seconds)."""
         o, w, x = self.oracle, self.w, self.x
         t0 = time.perf_counter()
         q, k, v = (o.shard_sequence(x[n], w.P) for n in ("q", "k", "v"))
@@ -354,33 +379,97 @@ class OracleBench:
             rg.a2a_head_to_seq(oh, w.n_head, w.ring)
         else:
             qh, _, _ = o.a2a_seq_to_head(q, w.n_head)
-            kh, _, _ = o.a2a_seq_to_head(k, w.n_kv_head)
-            vh, _, _ = o.a2a_seq_to_head(v, w.n_kv_head)
+            kv_a2a = o.a2a_seq_to_head_replicated if self.op.kv_replicas > 1 else o.a2a_seq_to_head
+            kh, _, _ = kv_a2a(k, w.n_kv_head)
+            vh, _, _ = kv_a2a(v, w.n_kv_head)
             t1 = time.perf_counter()
             oh, _ = o.attention_fwd(self.op, qh, kh, vh, rows=rows, nthreads=self.nthreads)
             t2 = time.perf_counter()
             o.a2a_head_to_seq(oh, w.n_head)
         t3 = time.perf_counter()
         pairs = sum((r + 1) if w.causal else w.S for r in rows)
-        full = w.S * (w.S + 1) / 2 if w.causal else float(w.S) * w.S
+        full = self._full_pairs()
         t_full = (t1 - t0) + (t3 - t2) + (t2 - t1) * full / pairs
-        return t_full, len(rows), pairs, t3 - t0
+        self.last = {"fwd_s": t_full}
+        if self.backward:
+            t_bwd = self._backward(qh, kh, vh, n_bwd_rows or self.bwd_rows_for(n_rows))
+            t_full += t_bwd
+            self.last["bwd_s"] = t_bwd
+        return t_full, len(rows), pairs, time.perf_counter() - t0
+
+    def bwd_rows_for(self, n_rows):
+        """Backward rows giving the dQ and dK/dV phases about as much work as the
+        forward's sampled attention: that covers all n_head heads, the backward
+        sample one group of G heads at about 3.5 forward products per pair."""
+        w = self.w
+        G = (w.n_head // w.P) // self.op.kvp
+        return int(min(w.S, max(16, n_rows * (w.n_head // G) // 4)))
+
+    def _backward(self, qh, kh, vh, n_bwd_rows):
+        o, w, x, op = self.oracle, self.w, self.x, self.op
+        D, hp, kvp = w.head_dim, w.n_head // w.P, op.kvp
+        G = hp // kvp
+        tb0 = time.perf_counter()
+        do_seq = o.shard_sequence(x["do"].reshape(w.B, w.S, w.n_head, D), w.P)
+        doh, _, _ = o.a2a_seq_to_head(do_seq, w.n_head)
+        tb1 = time.perf_counter()
+        q_rows = sorted(set(int(r) for r in self.rng.integers(0, w.S, n_bwd_rows)))
+        kv_rows = sorted(set(int(r) for r in self.rng.integers(0, w.S, n_bwd_rows)))
+        ph = []
+        dqh, dkh, dvh = o.attention_bwd(op, qh, kh, vh, doh, groups=[(0, 0, 0)], q_rows=q_rows, kv_rows=kv_rows,
+                                        nthreads=self.nthreads, phase_seconds=ph)
+        tb2 = time.perf_counter()
+        dq_seq, _, _ = o.a2a_head_to_seq(dqh, w.n_head, fill=np.nan)
+        if op.kv_replicas > 1:
+            dk_seq, _, _ = o.reduce_head_to_seq_replicated(dkh, w.n_kv_head)
+            o.reduce_head_to_seq_replicated(dvh, w.n_kv_head)
+        else:
+            dk_seq, _, _ = o.a2a_head_to_seq(dkh, w.n_kv_head, fill=np.nan)
+            o.a2a_head_to_seq(dvh, w.n_kv_head, fill=np.nan)
+        if w.use_rope:
+            o.rope_seq(dq_seq, op.rope_base, -1)
+            o.rope_seq(dk_seq, op.rope_base, -1)
+        tb3 = time.perf_counter()
+        t_stat, t_dq, t_dkdv = ph[0]
+        full = G * self._full_pairs()
+        pairs_dq = G * sum((i + 1) if w.causal else w.S for i in q_rows)
+        pairs_dkdv = G * sum((w.S - kk) if w.causal else w.S for kk in kv_rows)
+        t_group = t_stat + t_dq * full / pairs_dq + t_dkdv * full / pairs_dkdv
+        n_groups = w.P * w.B * kvp
+        self.last.update(bwd_rows=n_bwd_rows, bwd_groups=n_groups,
+                         bwd_sampled_s=tb3 - tb0)
+        return (tb1 - tb0) + (tb3 - tb2) + n_groups * t_group
 
     def calibrate(self, attn_budget_s):
-        """Row count whose attention takes about `attn_budget_s` seconds."""
+        """Row count whose forward attention takes about `attn_budget_s` seconds
+        (forward only: the backward sample is sized from it)."""
         n = 16
-        while True:
-            _, nr, pairs, wall = self.step(n)
-            if wall > attn_budget_s or n >= self.w.S:
-                return n
-            n = min(self.w.S, n * 4)
+        bwd, self.backward = self.backward, False
+        try:
+            while True:
+                _, nr, pairs, wall = self.step(n)
+                if wall > attn_budget_s or n >= self.w.S:
+                    return n
+                n = min(self.w.S, n * 4)
+        finally:
+            self.backward = bwd
 
     def describe(self, n_rows):
         w = self.w
         ring = f", {w.ring} ring positions" if w.ring > 1 else ""
-        return (f"{w.name} (P={w.P}{ring}, S={w.S}, {w.n_head} heads, D={w.head_dim}): split, RoPE and the 4 loop "
+        text = (f"{w.name} (P={w.P}{ring}, S={w.S}, {w.n_head} heads, D={w.head_dim}): split, RoPE and the 4 loop "
                 f"all-to-alls in full; attention for {n_rows} random query rows of all {w.n_head} heads, "
                 f"scaled to the full causal triangle by query-key pairs")
+        if self.backward:
+            G = (w.n_head // w.P) // self.op.kvp
+            text += (f"; backward: dO all-to-all, the inverse all-to-alls of dQ, dK, dV and the inverse RoPE in "
+                     f"full; the attention backward of 1 of {w.P * w.B * self.op.kvp} (rank, batch, kv-head) "
+                     f"groups ({G} q-head(s)) with its statistics phase in full and its dQ and dK/dV phases for "
+                     f"{self.bwd_rows_for(n_rows)} random query and key rows, scaled by query-key pairs and "
+                     f"by the number of groups")
+        else:
+            text += "; forward only"
+        return text
 
 
 def run_sweep(args):
@@ -551,17 +640,23 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        ob = OracleBench(w)
+        ob = OracleBench(w, backward=w.backward and not args.fwd_only)
         per_step_budget = max(2.0, 150.0 / max(args.steps + args.warmup, 1))
-        n_rows = ob.calibrate(per_step_budget / 2)
-        times = [ob.step(n_rows)[0] for _ in range(args.steps)]
+        n_rows = ob.calibrate(per_step_budget / 4)
+        times, walls = [], []
+        for _ in range(args.steps):
+            t_full, _, _, wall = ob.step(n_rows)
+            times.append(t_full)
+            walls.append(wall)
         t = statistics.median(times)
         value = tokens / t
         line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+                "ms_per_step_kind": "extrapolated_from_sample",
+                "sample_wall_ms_per_step": statistics.median(walls) * 1e3,
+                "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": w.name, "P": w.P, "ring": w.ring, "B": w.B, "S": w.S, "n_head": w.n_head,
-                           "n_kv_head": w.n_kv_head, "head_dim": w.head_dim, "passes": "fwd"},
+                "config": line_config(w, ob.passes, "n/a (host cores)", "host cores, P virtual ranks (oracle)"),
                 "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": ob.nthreads, "kind": "oracle",
                                  "sample": ob.describe(n_rows)},
                 "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -617,11 +712,9 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic (seeded normal inputs of the workload's shape)",
-        "config": {"workload": w.name, "P": w.P, "ring": w.ring, "B": w.B, "S": w.S, "n_head": w.n_head,
-                   "n_kv_head": w.n_kv_head, "head_dim": w.head_dim, "causal": w.causal, "rope": w.use_rope,
-                   "passes": "fwd+bwd" if r["backward"] else "fwd",
-                   "l2": "inputs larger than L2 (Q/K/V/O each >= 128 MiB); no flush",
-                   "parallelism": "replicas" if world > 1 else "single GPU, P virtual ranks"},
+        "config": line_config(w, "fwd+bwd" if r["backward"] else "fwd",
+                              "inputs larger than L2 (Q/K/V/O each >= 128 MiB); no flush",
+                              "replicas" if world > 1 else "single GPU, P virtual ranks"),
         "fwd_tokens_per_s": fwd_tokens,
         "attn_fwd_tflops": attn_tflops, "attn_fwd_ms": attn_ms,
         "attn_bwd_tflops": bwd_tflops, "attn_bwd_ms": bwd_ms,
@@ -636,7 +729,11 @@ def main():
         "roofline": {"bound": "tensor", "achieved": dk["achieved_tflops"], "peak": tf_sust, "unit": "TFLOP/s",
                      "frac": dk["frac"], "traffic": TRAFFIC.get((dominant, w.name)),
                      "peak_source": f"{peak_src} bf16 sustained", "kernel": dk["kernel"],
-                     "note": "dominant kernel by time; achieved counts its algorithmic products only"},
+                     "peak_burst": tf_burst, "frac_burst": dk["achieved_tflops"] / tf_burst,
+                     "sm_mhz": r["clocks"].get("sm_mhz"),
+                     "note": "dominant kernel by time; achieved counts its algorithmic products only; frac is "
+                             "against the sustained (power-capped) cuBLAS figure, frac_burst against the burst "
+                             "one; sm_mhz is the median SM clock sampled while the timed steps ran"},
         "secondary_rooflines": {**{k: {"bound": "tensor", "achieved": v["achieved_tflops"], "peak": tf_sust,
                                        "unit": "TFLOP/s", "frac": v["frac"], "traffic": TRAFFIC.get((k, w.name))}
                                    for k, v in kernels.items() if k != dominant},
@@ -654,11 +751,12 @@ def main():
         "device_status": r["status"],
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        ob = OracleBench(w)
-        n_rows = ob.calibrate(8.0)
-        t_full = ob.step(n_rows)[0]
+        ob = OracleBench(w, backward=r["backward"])
+        n_rows = ob.calibrate(4.0)
+        t_full, _, _, wall = ob.step(n_rows)
         line["cpu_baseline"] = {"value": tokens / t_full, "unit": "tokens/s", "cores": ob.nthreads,
-                                "kind": "oracle", "sample": ob.describe(n_rows)}
+                                "kind": "oracle", "passes": ob.passes, "sample": ob.describe(n_rows),
+                                "value_kind": "extrapolated_from_sample", "sample_wall_s": wall}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

@@ -82,7 +82,8 @@ def load_library(path: str):
     L.oracle_attention_unsharded.argtypes = [ctypes.POINTER(_Shape)] + [ctypes.c_void_p] * 5 + [ctypes.c_int]
     L.oracle_attention_bwd_group.argtypes = [ctypes.POINTER(_Shape), ctypes.c_int, ctypes.c_int,
                                              ctypes.c_int, pp, pp, pp, pp, pp, pp, pp, ip,
-                                             ctypes.c_long, ip, ctypes.c_long, ctypes.c_int]
+                                             ctypes.c_long, ip, ctypes.c_long, ctypes.c_int,
+                                             ctypes.POINTER(ctypes.c_double)]
     return L
 
 
@@ -279,10 +280,11 @@ def attention_unsharded(prob: Problem, q, k, v, nthreads=None):
 
 
 def attention_bwd(prob: Problem, q_head, k_head, v_head, do_head, groups=None,
-                  q_rows=None, kv_rows=None, nthreads=None):
+                  q_rows=None, kv_rows=None, nthreads=None, phase_seconds=None):
     """Backward on head-sharded buffers for the listed (rank, batch, local
     kv-head) groups (default: all).  Returns (dq, dk, dv) head-layout ranks;
-    entries not computed stay NaN."""
+    entries not computed stay NaN.  `phase_seconds` (a list, optional) gets
+    the wall time of each group's three phases appended (timing only)."""
     P, B, S, D = prob.P, prob.B, prob.S, prob.D
     hp, kvp = prob.n_head // P, prob.kvp
     dq = [np.full((B, S, hp, D), np.nan) for _ in range(P)]
@@ -296,13 +298,16 @@ def attention_bwd(prob: Problem, q_head, k_head, v_head, do_head, groups=None,
     sh = prob.shape()
     ptrs = [_ptrs(x) for x in (q_head, k_head, v_head, do_head, dq, dk, dv)]
     for (r, b, kl) in groups:
+        secs = (ctypes.c_double * 3)()
         rc = lib().oracle_attention_bwd_group(
             ctypes.byref(sh), r, b, kl, *ptrs,
             qa.ctypes.data_as(ip) if qa is not None else None, len(qa) if qa is not None else 0,
             ka.ctypes.data_as(ip) if ka is not None else None, len(ka) if ka is not None else 0,
-            _nthreads(nthreads))
+            _nthreads(nthreads), secs)
         if rc != 0:
             raise ValueError(f"oracle backward failed ({rc})")
+        if phase_seconds is not None:
+            phase_seconds.append(tuple(secs))
     return dq, dk, dv
 
 

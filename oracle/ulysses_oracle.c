@@ -42,6 +42,7 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#include <time.h>
 
 /* ------------------------------------------------------------------------ */
 /* A tiny thread pool: items [0, n) are handed out by an atomic counter.     */
@@ -66,6 +67,12 @@ static void *pool_worker(void *arg) {
   }
   free(scratch);
   return NULL;
+}
+
+static double wall_seconds(void) {
+  struct timespec ts;
+  clock_gettime(CLOCK_MONOTONIC, &ts);
+  return (double)ts.tv_sec + 1e-9 * (double)ts.tv_nsec;
 }
 
 static void run_items(item_fn fn, void *ctx, long n_items, long scratch_len, int nthreads) {
@@ -367,7 +374,9 @@ int oracle_attention_unsharded(const oracle_shape *sh, const double *q, const do
 /* One call handles one (rank, batch, local kv-head) group.  It recomputes   */
 /* o_i and lse_i for all rows of the group's q-heads first.  dq is written   */
 /* for the rows in q_rows (NULL = all), dk/dv for the key rows in kv_rows    */
-/* (NULL = all); other rows are left untouched.                              */
+/* (NULL = all); other rows are left untouched.  phase_seconds (NULL: not    */
+/* wanted) receives the wall time of the three phases (statistics, dq,       */
+/* dk/dv): instrumentation for the benchmark's CPU baseline, no arithmetic.  */
 /* ------------------------------------------------------------------------ */
 typedef struct {
   const oracle_shape *sh;
@@ -460,7 +469,8 @@ int oracle_attention_bwd_group(const oracle_shape *sh, int r, int b, int kl,
                                const double *const *v_head, const double *const *do_head,
                                double *const *dq_head, double *const *dk_head,
                                double *const *dv_head, const int *q_rows, long n_q_rows,
-                               const int *kv_rows, long n_kv_rows, int nthreads) {
+                               const int *kv_rows, long n_kv_rows, int nthreads,
+                               double *phase_seconds) {
   if (!heads_ok(sh)) return -1;
   const long S = sh->S;
   bwd_ctx c;
@@ -491,16 +501,23 @@ int oracle_attention_bwd_group(const oracle_shape *sh, int r, int b, int kl,
     free(c.delta);
     return -2;
   }
+  double t[4] = {0.0, 0.0, 0.0, 0.0};
+  t[0] = wall_seconds();
   c.phase = 0;
   run_items(bwd_item, &c, (long)c.G * S, S + sh->D, nthreads);
+  t[1] = wall_seconds();
   if (dq_head) {
     c.phase = 1;
     run_items(bwd_item, &c, (long)c.G * c.n_q_rows, 1, nthreads);
   }
+  t[2] = wall_seconds();
   if (dk_head && dv_head) {
     c.phase = 2;
     run_items(bwd_item, &c, c.n_kv_rows, 1, nthreads);
   }
+  t[3] = wall_seconds();
+  if (phase_seconds)
+    for (int i = 0; i < 3; ++i) phase_seconds[i] = t[i + 1] - t[i];
   free(c.lse);
   free(c.delta);
   return 0;

@@ -93,3 +93,29 @@ def test_bench_line_carries_the_contract_keys(monkeypatch, capsys):
     assert line["value"] == pytest.approx(32768 / (line["ms_per_step"] * 1e-3))
     assert set(line["e2e"]) == {"value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"}
     assert line["folded_bwd"] == {"unfolded_ms": 19.8, "ms": 19.9}
+
+
+def test_reference_arm_times_both_passes_with_the_gpu_arms_config(monkeypatch, capsys):
+    """For a workload with a backward the reference arm times the oracle's
+    forward and backward (passes fwd+bwd, like the GPU arm's headline), labels
+    its per-step time as extrapolated from a sample, and its config has the
+    GPU arm's keys."""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "C3",
+                          "--steps", "1", "--warmup", "3"], capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    ref = json.loads([ln for ln in out.stdout.splitlines() if ln.startswith("{")][0])
+    assert ref["config"]["passes"] == "fwd+bwd"
+    assert ref["ms_per_step_kind"] == "extrapolated_from_sample" and ref["sample_wall_ms_per_step"] > 0
+    assert "backward" in ref["cpu_baseline"]["sample"]
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setattr(bench, "run_ulysses", lambda args, w, rank, world: _fake_measurements(True, args.steps))
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--steps", "2", "--workload", "C3", "--no-cpu-baseline"])
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.delenv("RANK", raising=False)
+    bench.main()
+    gpu = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert set(gpu["config"]) == set(ref["config"])
+    assert all(gpu["config"][k] == ref["config"][k] for k in gpu["config"] if k not in ("l2", "parallelism"))
+    r = gpu["roofline"]
+    assert abs(r["frac_burst"] - r["achieved"] / r["peak_burst"]) < 1e-12 and r["sm_mhz"] == 2040.0
