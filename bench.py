@@ -146,7 +146,8 @@ def run_ulysses(args, w, rank, world):
     prob = U.Problem.from_workload(w)
     backward = w.backward and not args.fwd_only
     ins = make_inputs(w, with_grad=backward)
-    buf = U.Buffers(prob, device=dev, backward=backward)
+    # phase-2 workspace: the fused backward (timed beside the two-kernel one) needs its dQ accumulator
+    buf = U.Buffers(prob, device=dev, backward=backward, fused=backward)
     host = {"q": U.seq_layout(ins["q"], w.P).pin_memory(), "k": U.seq_layout(ins["k"], w.P).pin_memory(),
             "v": U.seq_layout(ins["v"], w.P).pin_memory()}
     if backward:
@@ -214,6 +215,36 @@ def run_ulysses(args, w, rank, world):
     barrier(world)
     total_ms = t0.elapsed_time(t1)
     per = {n: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)] for i, n in enumerate(names)}
+
+    # ---- the fused backward (dQ accumulated in the dK/dV loop): the same
+    # K steps' backward through its three entry points, each kernel timed
+    fused_per = None
+    if backward:
+        fnames = ["bwd_prepare", "bwd_dkdvq", "bwd_dq_finish"]
+
+        def fused_bwd(ev=None):
+            def fmark(i):
+                if ev is not None:
+                    ev[i].record(stream)
+            fmark(0)
+            U.ulysses_attn_bwd_prepare(prob, buf.o_head, buf.lse, buf.do_seq, buf.ws)
+            fmark(1)
+            U.ulysses_attn_bwd_dkdvq(prob, buf.q_head, buf.k_head, buf.v_head, buf.dk_seq, buf.dv_seq, buf.ws)
+            fmark(2)
+            U.ulysses_attn_bwd_dq_finish(prob, buf.dq_seq, buf.ws)
+            fmark(3)
+
+        for _ in range(2):
+            fused_bwd()
+        fev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for k in range(args.steps):
+            fused_bwd(fev[k])
+        torch.cuda.synchronize()
+        fused_per = {n: [fev[k][i].elapsed_time(fev[k][i + 1]) for k in range(args.steps)]
+                     for i, n in enumerate(fnames)}
+        if U.ulysses_read_status(buf.ws) != 0:
+            raise RuntimeError("device status word set during the fused backward steps")
 
     # ---- end to end through the public API with host buffers: every step
     # uploads its inputs from pinned host memory and downloads its results
@@ -285,7 +316,7 @@ def run_ulysses(args, w, rank, world):
     # the MUFU unit's exponential throughput on this GPU (the softmax's secondary bound)
     ex2_rate = U.ulysses_selftest_ex2_rate()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    return dict(total_ms=total_ms, per=per, clocks=clk, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
+    return dict(total_ms=total_ms, per=per, fused_per=fused_per, clocks=clk, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
                 launches=launches_per_step * args.steps, status=status, backward=backward,
                 folded=folded, ex2_rate=ex2_rate, sms=sms)
 
@@ -693,6 +724,22 @@ def main():
                       "achieved_tflops": a_tf, "frac": a_tf / tf_sust,
                       "executed_tflops": exe / (per[k] * 1e-3) / 1e12,
                       "executed_frac": exe / (per[k] * 1e-3) / 1e12 / tf_sust}
+    bwd_modes = None
+    if bwd_ms and r.get("fused_per"):
+        fp = {k: statistics.mean(v) for k, v in r["fused_per"].items()}
+        f_ms = sum(fp.values())
+        a_tf = 2.0 * fl / (fp["bwd_dkdvq"] * 1e-3) / 1e12
+        bwd_modes = {
+            "two_kernel": {"ms": bwd_ms, "kernel_ms": {k: per[k] for k in bwd_parts},
+                           "note": "ulysses_attn_bwd: dK/dV kernel, then the dQ kernel recomputing S and dP; "
+                                   "7 products per tile pair; bit-reproducible"},
+            "fused": {"ms": f_ms, "kernel_ms": fp,
+                      "kernel": f"dkdvq_kernel<{w.head_dim}>", "algorithmic_tflop": 2.0 * fl / 1e12,
+                      "achieved_tflops": a_tf, "frac": a_tf / tf_sust,
+                      "executed_tflops": 2.5 * fl / (fp["bwd_dkdvq"] * 1e-3) / 1e12,
+                      "note": "ulysses_attn_bwd_fused: dQ shares reduce-added into a float accumulator inside the "
+                              "dK/dV loop; 5 products per tile pair; dQ reproducible to float rounding"},
+            "headline_uses": "two_kernel"}
     dominant = max(kernels, key=lambda k: kernels[k]["ms"])
     dk = kernels[dominant]
     # One exponential per (query, key) pair the forward computes, against the
@@ -726,6 +773,7 @@ def main():
         "kernel_ms_median": {k: statistics.median(v) for k, v in r["per"].items()},
         "kernel_ms_min": {k: min(v) for k, v in r["per"].items()},
         "tensor_kernels": kernels,
+        "bwd_modes": bwd_modes,
         "roofline": {"bound": "tensor", "achieved": dk["achieved_tflops"], "peak": tf_sust, "unit": "TFLOP/s",
                      "frac": dk["frac"], "traffic": TRAFFIC.get((dominant, w.name)),
                      "peak_source": f"{peak_src} bf16 sustained", "kernel": dk["kernel"],

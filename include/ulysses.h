@@ -120,14 +120,16 @@ typedef struct ulysses_problem {
 int ulysses_validate(const ulysses_problem *prob);
 
 /* Workspace bytes for a phase: 0 = forward (pack + attention + unpack),
- * 1 = backward (also valid for the forward).  Returns 0 for an invalid
- * problem.  Host only; needs no GPU. */
+ * 1 = backward (also valid for the forward), 2 = the fused backward
+ * (ulysses_attn_bwd_fused; the phase-1 workspace followed by a float dQ
+ * accumulator of B*n_head*ceil(S/128)*128*head_dim*4 bytes; valid for every
+ * call).  Returns 0 for an invalid problem.  Host only; needs no GPU. */
 size_t ulysses_workspace_bytes(const ulysses_problem *prob, int phase);
 
 /* Prepares a workspace for `prob`: clears the status word and, when use_rope
  * is set, fills the RoPE table (cos and sin of p*base^(-2i/D), p < S,
- * i < D/2, computed in double precision and rounded to float).  Call once per
- * (workspace, problem) before any call that takes `ws`; calls with a
+ * i < D/2, computed in double precision and rounded to float).  Call once
+ * per (workspace, problem) before any call that takes `ws`; calls with a
  * workspace prepared for another problem flag ULYSSES_STATUS_ROPE_TABLE and
  * leave their outputs unwritten. */
 int ulysses_workspace_init(const ulysses_problem *prob, void *ws, size_t ws_bytes,
@@ -290,6 +292,41 @@ int ulysses_attn_bwd_dkdv(const ulysses_problem *prob, const void *q_head, const
                           ulysses_stream_t stream);
 int ulysses_attn_bwd_dq(const ulysses_problem *prob, const void *q_head, const void *k_head,
                         const void *v_head, void *dq_seq, void *ws, size_t ws_bytes, ulysses_stream_t stream);
+
+/*
+ * The backward with dQ accumulated inside the dK/dV loop ("Sequence
+ * Parallelism II", §6, the same gradients as ulysses_attn_bwd; "Comparing
+ * Ulysses and Megatron Sequence Parallelism", "DeepSpeed Attention costs":
+ * the backward does about twice the forward's products).  ulysses_attn_bwd
+ * runs two tensor-core kernels, the second recomputing the scores and dP for
+ * dQ: seven matrix products per (128-key, 128-query) tile pair.  Here one
+ * kernel forms dV, dK and each tile pair's dQ share from the same scores:
+ * five products per pair.  The dQ shares of one query tile come from the
+ * CTAs of different key tiles and are added into a float accumulator in the
+ * workspace by the copy engine's reduce-add, in an order that varies from run
+ * to run: dQ is reproducible to float rounding, not bit for bit (dK and dV
+ * are bit-identical to ulysses_attn_bwd's).  Same arguments, layouts and
+ * results (within the stated tolerance) as ulysses_attn_bwd; `ws` must be
+ * sized for phase 2 and prepared by ulysses_workspace_init.  bf16, head_dim
+ * 64 or 128; the errors of ulysses_attn_bwd, and ULYSSES_ERR_WORKSPACE for a
+ * workspace smaller than phase 2.
+ *
+ * Its steps, for callers that time or schedule them: ulysses_attn_bwd_prepare
+ * (above), then ulysses_attn_bwd_dkdvq (zeroes the accumulator, then dK, dV
+ * into dk_seq / dv_seq as ulysses_attn_bwd_dkdv writes them and every dQ
+ * share added into the accumulator), then ulysses_attn_bwd_dq_finish (dQ
+ * from the accumulator: scaled, RoPE rotation undone, rounded to bf16 into
+ * dq_seq [P][B][Sl][n_head][D]).
+ */
+int ulysses_attn_bwd_fused(const ulysses_problem *prob, const void *q_head, const void *k_head,
+                           const void *v_head, const void *o_head, const float *lse, const void *do_seq,
+                           void *dq_seq, void *dk_seq, void *dv_seq, void *ws, size_t ws_bytes,
+                           ulysses_stream_t stream);
+int ulysses_attn_bwd_dkdvq(const ulysses_problem *prob, const void *q_head, const void *k_head,
+                           const void *v_head, void *dk_seq, void *dv_seq, void *ws, size_t ws_bytes,
+                           ulysses_stream_t stream);
+int ulysses_attn_bwd_dq_finish(const ulysses_problem *prob, void *dq_seq, void *ws, size_t ws_bytes,
+                               ulysses_stream_t stream);
 
 /*
  * Folded backward: the backward of ulysses_attn_fwd_folded with every

@@ -107,11 +107,11 @@ class GpuRun:
     """Inputs on the device in the sequence-sharded layout, workspace prepared,
     forward (and optionally backward) run through the C ABI."""
 
-    def __init__(self, w: Workload, backward: bool = False, inputs=None):
+    def __init__(self, w: Workload, backward: bool = False, inputs=None, fused: bool = False):
         self.w = w
         self.prob = U.Problem.from_workload(w)
         self.inputs = inputs if inputs is not None else make_inputs(w, with_grad=backward)
-        self.buf = U.Buffers(self.prob, backward=backward)
+        self.buf = U.Buffers(self.prob, backward=backward, fused=fused)
         P = w.P
         self.buf.q_seq.copy_(U.seq_layout(self.inputs["q"], P))
         self.buf.k_seq.copy_(U.seq_layout(self.inputs["k"], P))
@@ -127,6 +127,11 @@ class GpuRun:
 
     def backward(self):
         self.buf.backward()
+        torch.cuda.synchronize()
+        assert U.ulysses_read_status(self.buf.ws) == 0
+
+    def backward_fused(self):
+        self.buf.backward_fused()
         torch.cuda.synchronize()
         assert U.ulysses_read_status(self.buf.ws) == 0
 

@@ -60,7 +60,10 @@ def _fake_measurements(backward, steps):
     if backward:
         per.update(bwd_prepare=[0.17] * steps, bwd_dkdv=[10.9] * steps, bwd_dq=[8.4] * steps)
     total = sum(v[0] for v in per.values()) * steps
-    return dict(total_ms=total, per=per, clocks={"sm_mhz": 2040.0, "sm_max_mhz": 2070.0, "reasons": []},
+    fused_per = ({"bwd_prepare": [0.17] * steps, "bwd_dkdvq": [20.0] * steps, "bwd_dq_finish": [1.0] * steps}
+                 if backward else None)
+    return dict(total_ms=total, per=per, fused_per=fused_per,
+                clocks={"sm_mhz": 2040.0, "sm_max_mhz": 2070.0, "reasons": []},
                 e2e_ms=total * 1.03, h2d=1 << 30, d2h=1 << 30, launches=6 * steps, status=0, backward=backward,
                 folded={"fwd": {"unfolded_ms": 5.8, "ms": 5.6}, "bwd": {"unfolded_ms": 19.8, "ms": 19.9}},
                 ex2_rate=32.0, sms=152)
@@ -93,6 +96,9 @@ def test_bench_line_carries_the_contract_keys(monkeypatch, capsys):
     assert line["value"] == pytest.approx(32768 / (line["ms_per_step"] * 1e-3))
     assert set(line["e2e"]) == {"value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"}
     assert line["folded_bwd"] == {"unfolded_ms": 19.8, "ms": 19.9}
+    m = line["bwd_modes"]
+    assert m["two_kernel"]["ms"] == pytest.approx(0.17 + 10.9 + 8.4)
+    assert m["fused"]["ms"] == pytest.approx(0.17 + 20.0 + 1.0) and m["fused"]["kernel"] == "dkdvq_kernel<128>"
 
 
 def test_reference_arm_times_both_passes_with_the_gpu_arms_config(monkeypatch, capsys):

@@ -134,6 +134,9 @@ def lib():
                                                 ctypes.POINTER(ctypes.c_int), vp]
         L.ulysses_attn_bwd_dkdv.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_attn_bwd_dq.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
+        L.ulysses_attn_bwd_fused.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.ulysses_attn_bwd_dkdvq.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.ulysses_attn_bwd_dq_finish.argtypes = [P, vp, vp, sz, vp]
         L.ulysses_status_string.argtypes = [ctypes.c_int]
         L.ulysses_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -247,6 +250,28 @@ def ulysses_attn_bwd_dq(prob, q_head, k_head, v_head, dq_seq, ws, stream=None):
         ws.numel() * ws.element_size(), _stream(stream)))
 
 
+def ulysses_attn_bwd_fused(prob, q_head, k_head, v_head, o_head, lse, do_seq, dq_seq, dk_seq, dv_seq, ws,
+                           stream=None):
+    """The backward with dQ accumulated in the dK/dV loop (phase-2 workspace)."""
+    _check("ulysses_attn_bwd_fused", lib().ulysses_attn_bwd_fused(
+        ctypes.byref(prob.c()), _ptr(q_head), _ptr(k_head), _ptr(v_head), _ptr(o_head), _ptr(lse),
+        _ptr(do_seq), _ptr(dq_seq), _ptr(dk_seq), _ptr(dv_seq), _ptr(ws), ws.numel() * ws.element_size(),
+        _stream(stream)))
+
+
+def ulysses_attn_bwd_dkdvq(prob, q_head, k_head, v_head, dk_seq, dv_seq, ws, stream=None):
+    """Fused step 2: dK, dV and the dQ shares added into the workspace accumulator."""
+    _check("ulysses_attn_bwd_dkdvq", lib().ulysses_attn_bwd_dkdvq(
+        ctypes.byref(prob.c()), _ptr(q_head), _ptr(k_head), _ptr(v_head), _ptr(dk_seq), _ptr(dv_seq),
+        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def ulysses_attn_bwd_dq_finish(prob, dq_seq, ws, stream=None):
+    """Fused step 3: dQ from the accumulator into sequence layout (accumulator re-zeroed)."""
+    _check("ulysses_attn_bwd_dq_finish", lib().ulysses_attn_bwd_dq_finish(
+        ctypes.byref(prob.c()), _ptr(dq_seq), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
 def ulysses_qkv_proj_pack(prob, x_seq, w_qkv, b_qkv, q_head, k_head, v_head, ws, stream=None):
     """QKV projection of the sequence-sharded activations with the pack and
     RoPE fused (b_qkv may be None)."""
@@ -310,7 +335,7 @@ class Buffers:
     intermediates, outputs and the workspace (allocated by torch, owned by
     the caller, as the C ABI requires)."""
 
-    def __init__(self, prob: Problem, device="cuda", backward: bool = False):
+    def __init__(self, prob: Problem, device="cuda", backward: bool = False, fused: bool = False):
         dt, p = prob.torch_dtype, prob
         D = p.head_dim
         e = lambda *s, d=dt: torch.empty(*s, dtype=d, device=device)
@@ -328,7 +353,8 @@ class Buffers:
             self.dq_seq = e(p.P, p.B, p.Sl, p.n_head, D)
             self.dk_seq = e(p.P, p.B, p.Sl, p.n_kv_head, D)
             self.dv_seq = e(p.P, p.B, p.Sl, p.n_kv_head, D)
-        nbytes = ulysses_workspace_bytes(prob, 1 if backward else 0)
+        # phase 2 (the fused backward's dQ accumulator too) when asked for
+        nbytes = ulysses_workspace_bytes(prob, (2 if fused else 1) if backward else 0)
         if nbytes == 0:
             raise UlyssesError("ulysses_workspace_bytes", ulysses_validate(prob))
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
@@ -345,3 +371,7 @@ class Buffers:
     def backward(self, stream=None):
         ulysses_attn_bwd(self.prob, self.q_head, self.k_head, self.v_head, self.o_head, self.lse,
                          self.do_seq, self.dq_seq, self.dk_seq, self.dv_seq, self.ws, stream)
+
+    def backward_fused(self, stream=None):
+        ulysses_attn_bwd_fused(self.prob, self.q_head, self.k_head, self.v_head, self.o_head, self.lse,
+                               self.do_seq, self.dq_seq, self.dk_seq, self.dv_seq, self.ws, stream)

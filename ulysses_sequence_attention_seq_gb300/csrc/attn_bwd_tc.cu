@@ -66,6 +66,8 @@ struct BwdParams {
   // head-layout buffer of rank (pos / Cs) * Pu + member, row pos % Cs.
   int Pu, Cs;
   int Ld;                              // row stride of nlse / delta (Cs rounded up to 4)
+  int Sp;                              // S rounded up to 128: rows per head of the fused kernel's
+                                       // float dQ accumulator [Pu*B][hp][Sp][D]
   // Folded addressing: q, dout and the K / V maps cover the sequence-sharded
   // buffers [P*B][Sl][heads][D] instead of the head-layout ones (plain Ulysses,
   // Sl a multiple of 128); nlse / delta keep their head-layout rows.
@@ -968,14 +970,602 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   if (threadIdx.x == 0 && *abort_flag) atomicOr(p.status, (uint32_t)ULYSSES_STATUS_BWD_TIMEOUT);
 }
 
-// Which of the two backward kernels a launch runs.
-enum BwdPart { kBwdDkDv = 1, kBwdDq = 2 };
+// ======================================================= fused dK / dV / dQ kernel
+// The dK/dV kernel's loop with dQ added to it: besides dV += P^T dO and
+// dK += dS^T Q, every step also forms its query tile's dQ share dS K (the
+// step's 128 keys' part of dQ) and adds it into a float accumulator in the
+// workspace with the copy engine's reduce-add (cp.reduce.async.bulk.tensor
+// .add): five products per (key tile, query tile) pair instead of the seven
+// the two-kernel backward executes (which recomputes S and dP for dQ).  The
+// float additions of one dQ row arrive from several CTAs in an order that
+// varies from run to run, so dQ is reproducible only to float rounding; dK
+// and dV are accumulated exactly as the dK/dV kernel does (bit-identical).
+//
+// TMEM: S^T [0,128) with P^T (bf16) over the first half of each softmax
+// warpgroup's columns; dP^T [128,256) with dS^T (bf16) likewise, and after
+// the dK MMA has read it the step's dQ share [128, 128+D) (query rows as
+// lanes); dV [256, 256+D), dK [256+D, 256+2D).
+// Shared memory: K, V resident; Q in a 2-slot ring (its delta and -LSE*log2e
+// rows ride in the slot), dO in one slot; dS (bf16, [key][query] in two
+// 128-byte-swizzled 64-query chunks: the MN-major A operand of dQ = dS K); a
+// float staging area X for half of a dQ share's columns.  A warpgroup of its
+// own drains each dQ share: TMEM into registers (which frees the TMEM for the
+// next dP), then columns [D/2, D) through the dS area (free once the dQ MMA
+// has read it, until the next dS) and [0, D/2) through X, one reduce-add per
+// [128 x 32] box.  The copy engine's reduce-adds run at the L2's pace (about
+// 6 TB/s over the whole chip).
+// Warps: 0-7 softmax (two warpgroups, each half of a step's 128 queries),
+// 8-11 dQ drain, 12 TMA producer, 13 MMA issuer, 14-15 idle; registers split
+// 160 / 144 / 48 per thread by warpgroup.
+// Tensor-core order, one wait per burst:
+//   prologue   S(0) dP(0) | PFull(0): dV(0)
+//   step i     DSFull(i): S(i+1) dK(i) dQ(i)  | XGo(i): dP(i+1) dV(i+1)
+// XGo(i) is arrived by the softmax warps after P(i+1) and by the drain warps
+// once dQ(i) is out of TMEM and dO tile i+1 has landed, so it vouches for
+// everything dP(i+1) and dV(i+1) use; DSFull(i) after Q tile i+1 has landed.
+// What bounds it (measured at the pages' sizing, clock64 traces of one CTA): a
+// step takes ~5,500 cycles against 2,560 of tensor-core work.  Its chain is
+// DSFull -> S dK dQ (24 MMAs, ~1,970) -> dQ out of TMEM -> dP -> dS phase ->
+// DSFull, with every other phase hidden behind it; the dS phase waits for the
+// reduce-adds to read the dS area back, because each step's dQ share (64 KB of
+// floats) leaves at the L2's reduce rate, ~20 bytes per SM-cycle, ~3,200
+// cycles per step.  Shared memory carries ~480 KB per step (the SS products
+// read 64 KB each, the staging writes and reads 128 KB), close to its 128
+// bytes per cycle over a step.  The five products per pair then take about as
+// long as the two-kernel backward's seven.
+constexpr int kFQSlots = 2;
+constexpr int kThreadsF = 512;
+constexpr int kFTmaWarp = 12, kFMmaWarp = 13;
+constexpr uint32_t kRegsFSoftmax = 160, kRegsFDrain = 144, kRegsFProducer = 48;
+static_assert(128 * (2 * kRegsFSoftmax + kRegsFDrain + kRegsFProducer) <= 65536, "register split over budget");
+
+enum : uint32_t {
+  kFBarIn = 0,
+  kFBarQFull = 8,     // [2]
+  kFBarQEmpty = 24,   // [2]
+  kFBarOFull = 40,
+  kFBarOEmpty = 48,
+  kFBarSFull = 56,
+  kFBarDPFull = 64,
+  kFBarPFull = 72,    // 256 arrivals (step 0 only)
+  kFBarDSFull = 80,   // 256 arrivals
+  kFBarDQFull = 88,
+  kFBarXGo = 96,      // 384 arrivals: softmax after P(i+1), drain after dQ(i) left TMEM
+  kFBarStage = 104,   // 128 arrivals: the drain warps have staged a half of dQ(i)
+  kFBarBufFree = 112, // 1 arrival: the reduce-adds of dQ(i) have read the dS area
+  kFBarXFree = 120,   // 1 arrival: ... and X
+  kFBarAcc = 128,
+  kFBarDrain = 136,
+  kFTmemSlot = 144,
+  kFAbortSlot = 148,
+  kFBarBytes = 152
+};
+
+template <int D>
+struct FLayout {
+  static constexpr uint32_t kT = 128u * D * 2;        // one 128-row tile of K, V, Q or dO
+  static constexpr uint32_t kDS = 128u * 128u * 2;    // dS: 128 keys x 128 queries, bf16
+  static constexpr uint32_t kStage = 128u * (D / 2) * 4;  // half of a dQ share's columns, float
+  static constexpr uint32_t oK = 0, oV = kT, oQ = 2 * kT, odO = oQ + kFQSlots * kT, oDS = odO + kT,
+                            oX = oDS + kDS,
+                            oRows = oX + kStage,  // per Q slot: delta row, then -LSE*log2(e) row
+                            oBar = oRows + kFQSlots * 1024;
+  static constexpr uint32_t kUsed = oBar + kFBarBytes;
+  static constexpr uint32_t kAlloc = kUsed + 1024 <= kMaxDynSmem ? kUsed + 1024 : kMaxDynSmem;
+  static_assert(kUsed <= kMaxDynSmem, "fused backward tiles exceed shared memory");
+};
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Reduce-add of a float box in shared memory into the global tensor of `m`
+// at (c0, c1), tracked by this thread's bulk async-groups.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *m, uint32_t src, int c0, int c1) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// D/2 floats of a thread's row (`x`) into a staging area: D/64 boxes of
+// [128 rows][32 floats], 128-byte swizzled (the 16-byte unit c of row r at
+// unit c ^ (r % 8)), so the 8 rows a quarter-warp writes land in distinct
+// banks; the reduce-add's tensor map has the same swizzle.
+template <int D>
+__device__ __forceinline__ void stage_half(uint8_t *area, int r, const uint32_t *x) {
+#pragma unroll
+  for (int b = 0; b < D / 64; ++b) {
+    uint8_t *row = area + b * 16384 + r * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) * 16)) =
+          make_uint4(x[32 * b + 4 * c], x[32 * b + 4 * c + 1], x[32 * b + 4 * c + 2], x[32 * b + 4 * c + 3]);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsF, 1)
+    dkdvq_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                 const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                 const __grid_constant__ CUtensorMap tmL, const __grid_constant__ CUtensorMap tmDl,
+                 const __grid_constant__ CUtensorMap tmAcc, const BwdParams p) {
+  using L = FLayout<D>;
+  constexpr int kCh = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  uint8_t *smem = smem_raw + pad;
+  const uint32_t sb = raw + pad;
+  const uint32_t sK = sb + L::oK, sV = sb + L::oV, sQ = sb + L::oQ, sdO = sb + L::odO, sDS = sb + L::oDS,
+                 sX = sb + L::oX, sRows = sb + L::oRows, bar = sb + L::oBar;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::oBar + kFAbortSlot);
+  const volatile uint32_t *gst = p.status;
+  if ((*gst & 3u) || stale_rope_table(p)) return;
+  if (pad + L::kUsed > L::kAlloc) {  // uniform over the block: nobody has touched a barrier yet
+    if (threadIdx.x == 0) atomicOr(p.status, (uint32_t)ULYSSES_STATUS_SMEM_ALIGN);
+    return;
+  }
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int heads_total = p.Pu * p.B * p.kvp;
+  const int n_kt_all = (p.S + 127) / 128;
+  const dev::HeadTile ht = dev::grouped_order((int)blockIdx.x, heads_total, n_kt_all, p.group_kv);
+  const int n = ht.rank;  // key tile; low tiles have the most work
+  const int hid = ht.head;
+  const int kl = hid % p.kvp, rb = hid / p.kvp;
+  const int n_qt = (p.S + 127) / 128;
+  const int m0 = p.causal ? n : 0;
+  const int n_m = n_qt - m0;
+  const int n_iter = p.group * n_m;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar + kFBarIn, 1);
+    for (int i = 0; i < kFQSlots; ++i) {
+      mbar_init(bar + kFBarQFull + 8 * i, 1);
+      mbar_init(bar + kFBarQEmpty + 8 * i, 1);
+    }
+    mbar_init(bar + kFBarOFull, 1);
+    mbar_init(bar + kFBarOEmpty, 1);
+    mbar_init(bar + kFBarSFull, 1);
+    mbar_init(bar + kFBarDPFull, 1);
+    mbar_init(bar + kFBarPFull, 256);
+    mbar_init(bar + kFBarDSFull, 256);
+    mbar_init(bar + kFBarDQFull, 1);
+    mbar_init(bar + kFBarXGo, 384);
+    mbar_init(bar + kFBarStage, 128);
+    mbar_init(bar + kFBarBufFree, 1);
+    mbar_init(bar + kFBarXFree, 1);
+    mbar_init(bar + kFBarAcc, 1);
+    mbar_init(bar + kFBarDrain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kFMmaWarp) {
+    __syncwarp();
+    tmem_alloc(bar + kFTmemSlot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::oBar + kFTmemSlot);
+  const uint32_t tdQ = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
+
+  if (warp >= 12) {
+    regs_dec<kRegsFProducer>();
+    if (warp == kFTmaWarp) {
+      if (lane == 0) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmQ);
+        mbar_arrive_expect_tx(bar + kFBarIn, 2 * L::kT);
+        const ActCoord kc = act_coord(p, rb, kl, p.kvp, n * 128, p.kv_rep);
+        for (int c = 0; c < kCh; ++c) {
+          tma_load_4d(sK + c * 16384, &tmK, bar + kFBarIn, c * 64, kc.head, kc.row, kc.outer);
+          tma_load_4d(sV + c * 16384, &tmV, bar + kFBarIn, c * 64, kc.head, kc.row, kc.outer);
+        }
+        // Loads in the order the slots free up: dO(i) after dV(i-1), Q(i) after dK(i-2).
+        int issued_q = -1, issued_o = -1;
+        for (int i = 0; i < n_iter; ++i) {
+          const int qs = i % kFQSlots;
+          const int gi = i / n_m, m = m0 + i % n_m, j = kl * p.group + gi;
+          // the delta / nlse rows are in head layout in either mode
+          const int mrow = m * 128 % p.Cs, mo = hl_outer(p, rb, m * 128);
+          const ActCoord qc = act_coord(p, rb, j, p.hp, m * 128, 1);
+          if (!mbar_wait_bounded(bar + kFBarQEmpty + 8 * qs, ((i / kFQSlots) & 1) ^ 1, abort_flag, gst)) break;
+          mbar_arrive_expect_tx(bar + kFBarQFull + 8 * qs, L::kT + 1024);
+          for (int c = 0; c < kCh; ++c)
+            tma_load_4d(sQ + qs * L::kT + c * 16384, &tmQ, bar + kFBarQFull + 8 * qs, c * 64, qc.head, qc.row,
+                        qc.outer);
+          dev::tma_load_2d(sRows + qs * 1024, &tmDl, bar + kFBarQFull + 8 * qs, mrow, mo * p.hp + j);
+          dev::tma_load_2d(sRows + qs * 1024 + 512, &tmL, bar + kFBarQFull + 8 * qs, mrow, mo * p.hp + j);
+          issued_q = i;
+          if (!mbar_wait_bounded(bar + kFBarOEmpty, (i & 1) ^ 1, abort_flag, gst)) break;
+          mbar_arrive_expect_tx(bar + kFBarOFull, L::kT);
+          for (int c = 0; c < kCh; ++c)
+            tma_load_4d(sdO + c * 16384, &tmdO, bar + kFBarOFull, c * 64, qc.head, qc.row, qc.outer);
+          issued_o = i;
+        }
+        if (*abort_flag) {
+          volatile int never = 0;
+          mbar_wait_bounded(bar + kFBarIn, 0, &never, nullptr, 500000000ull);
+          for (int i = issued_q - (kFQSlots - 1); i <= issued_q; ++i)
+            if (i >= 0)
+              mbar_wait_bounded(bar + kFBarQFull + 8 * (i % kFQSlots), (i / kFQSlots) & 1, &never, nullptr,
+                                500000000ull);
+          if (issued_o >= 0) mbar_wait_bounded(bar + kFBarOFull, issued_o & 1, &never, nullptr, 500000000ull);
+        }
+      }
+    } else if (warp == kFMmaWarp) {
+      if (lane == 0) {
+        constexpr uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);  // S^T, dP^T: both operands K-major
+        constexpr uint32_t idA = idesc_bf16_f32(128, D, 0, 1);    // dV, dK: B (dO, Q) MN-major
+        constexpr uint32_t idQ = idesc_bf16_f32(128, D, 1, 1);    // dQ: A (dS) and B (K) MN-major
+        const uint32_t sK_ = sK, sV_ = sV, sQ_ = sQ, sdO_ = sdO, sDS_ = sDS;
+        // The shared-memory bases pass through an empty asm in each helper, so
+        // the descriptors are formed when a burst is issued instead of all
+        // being held in registers across the loop (this warpgroup runs on 48).
+        auto opaque = [](uint32_t v) {
+          asm volatile("" : "+r"(v));
+          return v;
+        };
+        // S^T(i) = K Q_i^T.
+        auto issue_s = [&](int i) {
+          const int qs = i % kFQSlots;
+          const uint32_t sK = opaque(sK_), sQ = opaque(sQ_);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_bf16_ss(tmem, smem_desc_sw128(sK + o, 16, 1024), smem_desc_sw128(sQ + qs * L::kT + o, 16, 1024),
+                        idS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar + kFBarSFull);
+        };
+        // dP^T(i) = V dO_i^T.
+        auto issue_dp = [&]() {
+          const uint32_t sV = opaque(sV_), sdO = opaque(sdO_);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t o = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_bf16_ss(tmem + 128, smem_desc_sw128(sV + o, 16, 1024), smem_desc_sw128(sdO + o, 16, 1024), idS,
+                        kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar + kFBarDPFull);
+        };
+        // dV += P^T(i) dO_i (P^T from TMEM: queries 16kk.. are columns 8kk.. of
+        // warpgroup 0's half (kk < 4) or of warpgroup 1's half at +64); releases dO.
+        auto issue_dv = [&](int i) {
+          const uint32_t sdO = opaque(sdO_);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t ac = (kk < 4 ? 0u : 64u) + (uint32_t)(kk & 3) * 8;
+            mma_bf16_ts(tdV, tmem + ac, smem_desc_sw128(sdO + kk * 2048, 16384, 1024), idA,
+                        (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bar + kFBarOEmpty);
+        };
+        // The two waits of each step are on the critical path and usually not
+        // yet complete when reached, so the issuer polls them (a suspended
+        // try_wait resumed ~500 cycles after the phase completed); the softmax
+        // warps keep sleeping waits (polling there cost more issue slots than
+        // it saved).
+        bool ok = mbar_wait_bounded(bar + kFBarIn, 0, abort_flag, gst) &&
+                  mbar_wait_bounded(bar + kFBarQFull, 0, abort_flag, gst) &&
+                  mbar_wait_bounded(bar + kFBarOFull, 0, abort_flag, gst);
+        if (ok) {
+          tc_fence_after_sync();
+          issue_s(0);
+          issue_dp();
+          if ((ok = mbar_wait_bounded(bar + kFBarPFull, 0, abort_flag, gst))) {
+            tc_fence_after_sync();
+            issue_dv(0);
+          }
+        }
+        for (int i = 0; ok && i < n_iter; ++i) {
+          const int qs = i % kFQSlots;
+          // burst 1: S^T(i+1), dK(i), dQ(i)
+          if (!(ok = mbar_wait_spin_bounded(bar + kFBarDSFull, i & 1, abort_flag, gst))) break;
+          tc_fence_after_sync();
+          if (i + 1 < n_iter) issue_s(i + 1);
+          const uint32_t sQ = opaque(sQ_), sDS = opaque(sDS_), sK = opaque(sK_);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t ac = (kk < 4 ? 0u : 64u) + (uint32_t)(kk & 3) * 8;
+            mma_bf16_ts(tdK, tmem + 128 + ac, smem_desc_sw128(sQ + qs * L::kT + kk * 2048, 16384, 1024), idA,
+                        (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bar + kFBarQEmpty + 8 * qs);
+          // dQ share = dS K over this tile's keys (16kk.. per MMA): A = dS [key][query]
+          // (MN-major, two 64-query chunks), B = K [key][d] (MN-major, D/64 chunks)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tdQ, smem_desc_sw128(sDS + kk * 2048, 16384, 1024),
+                        smem_desc_sw128(sK + kk * 2048, 16384, 1024), idQ, kk > 0 ? 1u : 0u);
+          mma_commit(bar + kFBarDQFull);
+          if (i + 1 >= n_iter) break;
+          // burst 2: dP^T(i+1), dV(i+1), once dQ(i) is out of TMEM and P^T(i+1) is in
+          if (!(ok = mbar_wait_spin_bounded(bar + kFBarXGo, i & 1, abort_flag, gst))) break;
+          tc_fence_after_sync();
+          issue_dp();
+          issue_dv(i + 1);
+        }
+        mma_commit(bar + kFBarAcc);
+        mma_commit(bar + kFBarDrain);
+        volatile int never = 0;
+        mbar_wait_bounded(bar + kFBarDrain, 0, &never, nullptr);
+      }
+    }
+  } else if (warp >= 8) {
+    regs_inc<kRegsFDrain>();
+    // ------------------------------------------------------- dQ drain warpgroup
+    const int w4 = warp & 3;
+    const int r = w4 * 32 + lane;  // query row of the dQ share == TMEM lane
+    const uint32_t lane_base = (uint32_t)(w4 * 32) << 16;
+    const bool elected = w4 == 0 && lane == 0;  // issues the reduce-adds
+    for (int i = 0; i < n_iter; ++i) {
+      if (!dev::warp_wait(bar + kFBarDQFull, i & 1, abort_flag, gst)) break;
+      tc_fence_after_sync();
+      uint32_t x[D];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(tdQ + lane_base + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(x + 32 * c));
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) reg_fence(*reinterpret_cast<uint32_t(*)[32]>(x + 32 * c));
+      if (i + 1 < n_iter) {
+        // dP(i+1) and dV(i+1) read dO tile i+1
+        if (!dev::warp_wait(bar + kFBarOFull, (i + 1) & 1, abort_flag, gst)) break;
+        tc_fence_before_sync();
+        mbar_arrive(bar + kFBarXGo);
+      }
+      // Columns [D/2, D) go through the dS area (the dQ MMA is done with it;
+      // the softmax writes the next dS there only after BufFree), their
+      // reduce-adds first, so that area is read back soonest; columns
+      // [0, D/2) through X (free once the last step's X reduce-adds have read it).
+      bool ok = true;
+      const int gi = i / n_m, m = m0 + i % n_m, j = kl * p.group + gi;
+      const int row0 = (rb * p.hp + j) * p.Sp + m * 128;
+#pragma unroll
+      for (int h = 1; h >= 0; --h) {
+        if (h == 0 && i > 0 && !dev::warp_wait(bar + kFBarXFree, (i - 1) & 1, abort_flag, gst)) {
+          ok = false;
+          break;
+        }
+        stage_half<D>(smem + (h ? L::oDS : L::oX), r, x + h * (D / 2));
+        fence_proxy_async_smem();
+        mbar_arrive(bar + kFBarStage);
+        if (elected) {
+          if (!mbar_wait_bounded(bar + kFBarStage, (2 * i + (1 - h)) & 1, abort_flag, gst)) {
+            ok = false;
+          } else {
+#pragma unroll
+            for (int bx = 0; bx < D / 64; ++bx)
+              tma_reduce_add_2d(&tmAcc, (h ? sDS : sX) + bx * 16384, h * (D / 2) + 32 * bx, row0);
+            bulk_commit();
+          }
+        }
+        __syncwarp();
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
+      if (elected && ok) {
+        bulk_wait_read_1();  // the dS area's group (the older one) has been read
+        mbar_arrive(bar + kFBarBufFree);
+        bulk_wait_read_all();
+        mbar_arrive(bar + kFBarXFree);
+      }
+      if (!__all_sync(0xffffffffu, ok)) break;
+    }
+    // every reduce-add this warpgroup issued is complete before the CTA ends
+    if (elected) bulk_wait_all();
+  } else {
+    regs_inc<kRegsFSoftmax>();
+    // ------------------------------------------------- softmax warpgroups
+    const int g = warp >> 2, w4 = warp & 3;
+    const int r = w4 * 32 + lane;  // key row of S^T, dP^T == TMEM lane
+    const uint32_t lane_base = (uint32_t)(w4 * 32) << 16;
+    const int kvr = n * 128 + r;
+    const bool rot = p.rope_cos && p.kv_rep == 1 && (D == 128 || g == 0) && kvr < p.S &&
+                     in_range(p.status, (long long)kvr * (D / 2), D / 2, p.rope_n);
+    const float *rcs = rot ? p.rope_cos + (size_t)kvr * (D / 2) + g * 32 : nullptr;
+    const float *rsn = rot ? p.rope_sin + (size_t)kvr * (D / 2) + g * 32 : nullptr;
+    if (rot) rope_prefetch(rcs, rsn);
+    float2 pf[32];  // P of this thread's 64 columns, kept for dS
+    uint32_t w[2][16];
+    // P phase of step s: S^T(s) -> P^T (bf16) over the first half of this
+    // warpgroup's S^T columns; P kept in pf.
+    auto p_phase = [&](int s) -> bool {
+      if (!dev::warp_wait(bar + kFBarSFull, s & 1, abort_flag, gst)) return false;
+      tc_fence_after_sync();
+      uint32_t sr[2][32];
+      tmem_ld32(tmem + lane_base + g * 64, sr[0]);
+      tmem_ld32(tmem + lane_base + g * 64 + 32, sr[1]);
+      // this step's -LSE*log2(e) rides in its Q slot (step 0: waited here;
+      // later steps: waited in the dS phase before)
+      if (s == 0 && !dev::warp_wait(bar + kFBarQFull, 0, abort_flag, gst)) return false;
+      tmem_wait_ld();
+      reg_fence(sr[0]);
+      reg_fence(sr[1]);
+      const int q0 = (m0 + s % n_m) * 128 + g * 64;
+      const int lo = p.causal ? kvr - q0 : 0, hi = p.S - q0;
+      const float2 *nl2 = reinterpret_cast<const float2 *>(smem + L::oRows + (s % kFQSlots) * 1024 + 512) + g * 32;
+      if (__all_sync(0xffffffffu, lo <= 0 && hi >= 64))
+        p_columns<false>(sr, nl2, p.scale_log2, lo, hi, pf, w);
+      else
+        p_columns<true>(sr, nl2, p.scale_log2, lo, hi, pf, w);
+      tmem_st16(tmem + lane_base + g * 64, w[0]);
+      tmem_st16(tmem + lane_base + g * 64 + 16, w[1]);
+      tmem_wait_st();
+      tc_fence_before_sync();
+      return true;
+    };
+    bool ok = p_phase(0);
+    if (ok) mbar_arrive(bar + kFBarPFull);
+    for (int i = 0; ok && i < n_iter; ++i) {
+      const int qs = i % kFQSlots;
+      // ---------------- dS phase of step i
+      if (!dev::warp_wait(bar + kFBarDPFull, i & 1, abort_flag, gst)) { ok = false; break; }
+      tc_fence_after_sync();
+      uint32_t dr[2][32];
+      tmem_ld32(tmem + lane_base + 128 + g * 64, dr[0]);
+      tmem_ld32(tmem + lane_base + 128 + g * 64 + 32, dr[1]);
+      tmem_wait_ld();
+      reg_fence(dr[0]);
+      reg_fence(dr[1]);
+      const float2 *dl2 = reinterpret_cast<const float2 *>(smem + L::oRows + qs * 1024) + g * 32;
+      ds_columns(dr, dl2, pf, w);
+      tmem_st16(tmem + lane_base + 128 + g * 64, w[0]);
+      tmem_st16(tmem + lane_base + 128 + g * 64 + 16, w[1]);
+      // the dS area held columns [D/2, D) of dQ(i-1) for their reduce-adds
+      if (i > 0 && !dev::warp_wait(bar + kFBarBufFree, (i - 1) & 1, abort_flag, gst)) { ok = false; break; }
+      {
+        // dS [key r][queries 64g..64g+63] into chunk g of the dS area, 128-byte swizzle
+        uint8_t *row = smem + L::oDS + g * 16384 + r * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4 *>(row + ((u ^ (r & 7)) * 16)) =
+              make_uint4(w[u >> 2][(u & 3) * 4], w[u >> 2][(u & 3) * 4 + 1], w[u >> 2][(u & 3) * 4 + 2],
+                         w[u >> 2][(u & 3) * 4 + 3]);
+      }
+      fence_proxy_async_smem();
+      tmem_wait_st();
+      tc_fence_before_sync();
+      // The issuer waits for this arrival alone before S^T(i+1) dK(i) dQ(i):
+      // Q tile i+1 (and the rows riding with it) must have landed.
+      if (i + 1 < n_iter &&
+          !dev::warp_wait(bar + kFBarQFull + 8 * ((i + 1) % kFQSlots), ((i + 1) / kFQSlots) & 1, abort_flag, gst)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive(bar + kFBarDSFull);
+      // ---------------- P phase of step i+1 (overlaps dK(i), dQ(i))
+      if (i + 1 < n_iter) {
+        if (!(ok = p_phase(i + 1))) break;
+        mbar_arrive(bar + kFBarXGo);
+      }
+    }
+    // ------------------------------------------------------------ epilogue
+    RopeRow angles;
+    if (ok && rot) rope_load(angles, rcs, rsn);
+    if (ok) ok = dev::warp_wait(bar + kFBarAcc, 0, abort_flag, gst);
+    if (ok && p.kv_rep > 1) {
+      tc_fence_after_sync();
+      const bool live = kvr < p.S;
+      const int kr = live ? kvr : 0;
+      const size_t prow = (size_t)hl_outer(p, rb, kr) * p.Cs + kr % p.Cs;
+      float *pv = reinterpret_cast<float *>(p.dv) + prow * D;
+      float *pk = reinterpret_cast<float *>(p.dk) + prow * D;
+      const bool put = live && in_range(p.status, (long long)(prow * D), D, p.dkv_n);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = g * (D / 2) + c * 32;
+        uint32_t xv[32], yk[32];
+        tmem_ld32(tdV + lane_base + col, xv);
+        tmem_ld32(tdK + lane_base + col, yk);
+        tmem_wait_ld();
+        if (put) {
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            reinterpret_cast<uint4 *>(pv + col)[v] =
+                make_uint4(xv[4 * v], xv[4 * v + 1], xv[4 * v + 2], xv[4 * v + 3]);
+            reinterpret_cast<uint4 *>(pk + col)[v] =
+                make_uint4(yk[4 * v], yk[4 * v + 1], yk[4 * v + 2], yk[4 * v + 3]);
+          }
+        }
+      }
+    } else if (ok) {
+      tc_fence_after_sync();
+      const bool live = kvr < p.S;
+      const int s_rank = kvr / p.Sl, t = kvr - s_rank * p.Sl;
+      const int rr = rb / p.B, bb = rb - rr * p.B;
+      const size_t row = (((size_t)(s_rank * p.B + bb) * p.Sl + t) * p.n_kv + (rr * p.kvp + kl)) * D;
+      const bool put = live && in_range(p.status, (long long)row, D, p.dkv_n) &&
+                       (!p.rope_cos || in_range(p.status, (long long)kvr * (D / 2), D / 2, p.rope_n));
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t xv[32];
+        const int col = g * (D / 2) + c * 32;
+        tmem_ld32(tdV + lane_base + col, xv);
+        tmem_wait_ld();
+        if (put) store_plain(p.dv + row + col, xv, 1.0f);
+      }
+      if (D == 128 || g == 0) {
+        const int i0 = g * 32;
+        uint32_t xk[32], yk[32];
+        tmem_ld32(tdK + lane_base + i0, xk);
+        tmem_ld32(tdK + lane_base + D / 2 + i0, yk);
+        tmem_wait_ld();
+        if (put) store_unrotated(p.dk + row + i0, p.dk + row + D / 2 + i0, xk, yk, p.scale, rot, angles);
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kFMmaWarp) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(p.status, (uint32_t)ULYSSES_STATUS_BWD_TIMEOUT);
+}
+
+// dQ from the fused kernel's float accumulator: scale, undo the rotation,
+// round to bf16 and write to its sequence-layout row (nothing is written when
+// the status word reports a fault).  Accumulator rows [Pu*B][hp][Sp][D]
+// (Sp = S rounded up to 128).  One thread per (token, head, 4 rotation pairs:
+// x at c*4.., y at D/2 + c*4..), consecutive threads along the token's heads,
+// so a token's dQ row in sequence layout (n_head*D values) is written
+// contiguously.  (Zeroing each accumulator row right behind its load here ran
+// at a seventh of the memory rate; the fused step zeroes the accumulator with
+// a plain fill before its kernel instead.)
+template <int D>
+__global__ void __launch_bounds__(256) dq_finish_kernel(const float *__restrict__ acc, const BwdParams p) {
+  constexpr int half = D / 2, q4 = half / 4;
+  const long long task = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int per_tok = p.n_head * q4;
+  if (task >= (long long)p.B * p.S * per_tok) return;
+  const int tok = (int)(task / per_tok), rest = (int)(task - (long long)tok * per_tok);
+  const int g = rest / q4, c = rest - g * q4;
+  const int bb = tok / p.S, pos = tok - bb * p.S;
+  const int rr = g / p.hp, j = g - rr * p.hp;  // group member holding global head g, its local head
+  const long long arow = ((long long)(rr * p.B + bb) * p.hp + j) * p.Sp + pos;
+  const long long acc_n = (long long)p.Pu * p.B * p.hp * p.Sp * D;
+  if (!in_range(p.status, arow * D + c * 4, half + 4, acc_n)) return;
+  if ((*p.status & 3u) != 0u || (p.rope_cos && p.status[1] != p.rope_key)) return;
+  const float *a = acc + arow * D + c * 4;
+  const float4 x4 = *reinterpret_cast<const float4 *>(a);
+  const float4 y4 = *reinterpret_cast<const float4 *>(a + half);
+  float xs[4] = {x4.x, x4.y, x4.z, x4.w}, ys[4] = {y4.x, y4.y, y4.z, y4.w};
+  if (p.rope_cos) {
+    if (!in_range(p.status, (long long)pos * half + c * 4, 4, p.rope_n)) return;
+    const float4 c4 = *reinterpret_cast<const float4 *>(p.rope_cos + (size_t)pos * half + c * 4);
+    const float4 s4 = *reinterpret_cast<const float4 *>(p.rope_sin + (size_t)pos * half + c * 4);
+    const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, ss[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // x' = x cos + y sin, y' = y cos - x sin
+      const float xq = xs[q], yq = ys[q];
+      xs[q] = xq * cc[q] + yq * ss[q];
+      ys[q] = yq * cc[q] - xq * ss[q];
+    }
+  }
+  const int s_rank = pos / p.Sl, t = pos - s_rank * p.Sl;
+  const size_t o = ((((size_t)s_rank * p.B + bb) * p.Sl + t) * p.n_head + g) * D + c * 4;
+  if (!in_range(p.status, (long long)o, half + 4, p.dq_n)) return;
+  const uint32_t w0 = pack_bf16x2(xs[0] * p.scale, xs[1] * p.scale);
+  const uint32_t w1 = pack_bf16x2(xs[2] * p.scale, xs[3] * p.scale);
+  const uint32_t w2 = pack_bf16x2(ys[0] * p.scale, ys[1] * p.scale);
+  const uint32_t w3 = pack_bf16x2(ys[2] * p.scale, ys[3] * p.scale);
+  *reinterpret_cast<uint2 *>(p.dq + o) = make_uint2(w0, w1);
+  *reinterpret_cast<uint2 *>(p.dq + o + half) = make_uint2(w2, w3);
+}
+
+// Which of the backward kernels a launch runs.
+enum BwdPart { kBwdDkDv = 1, kBwdDq = 2, kBwdFused = 4, kBwdFinish = 8 };
 
 template <int D>
 cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void *q, const void *k,
                      const void *v, const void *do_head, const float *nlse, const float *delta,
-                     const void *ws, void *dq, void *dk, void *dv, uint32_t *status, int parts, bool folded,
-                     cudaStream_t st) {
+                     const void *ws, void *dq, void *dk, void *dv, float *dqacc, uint32_t *status, int parts,
+                     bool folded, cudaStream_t st) {
   const int Pu = group_ranks(p), Cs = chunk_len(p), Sl = p.S / p.P;
   const int hp = p.n_head / Pu, kvp = kv_per_rank(p), PB = p.P * p.B;
   // head-layout maps [P*B][Cs][hp|kvp][D], or folded the sequence-sharded
@@ -983,13 +1573,15 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   const int rows = folded ? Sl : Cs, qh = folded ? p.n_head : hp, kh = folded ? p.n_kv_head : kvp;
   if (folded && (ring_of(p) > 1 || Sl % 128 != 0)) return cudaErrorInvalidValue;
   CUtensorMap mK128, mV128, mL, mDl, mQ128, mdO128;
-  bool ok = make_act_map(enc, &mK128, k, D, kh, rows, PB, 128) &&
-            make_act_map(enc, &mV128, v, D, kh, rows, PB, 128) &&
-            make_row_map(enc, &mL, nlse, Cs, delta_ld(p), PB * hp, 128) &&
-            make_row_map(enc, &mDl, delta, Cs, delta_ld(p), PB * hp, 128) &&
-            make_act_map(enc, &mQ128, q, D, qh, rows, PB, 128) &&
-            make_act_map(enc, &mdO128, do_head, D, qh, rows, PB, 128);
-  if (!ok) return cudaErrorInvalidValue;
+  if (parts & (kBwdDkDv | kBwdDq | kBwdFused)) {  // the dQ finish step reads no tile
+    const bool ok = make_act_map(enc, &mK128, k, D, kh, rows, PB, 128) &&
+                    make_act_map(enc, &mV128, v, D, kh, rows, PB, 128) &&
+                    make_row_map(enc, &mL, nlse, Cs, delta_ld(p), PB * hp, 128) &&
+                    make_row_map(enc, &mDl, delta, Cs, delta_ld(p), PB * hp, 128) &&
+                    make_act_map(enc, &mQ128, q, D, qh, rows, PB, 128) &&
+                    make_act_map(enc, &mdO128, do_head, D, qh, rows, PB, 128);
+    if (!ok) return cudaErrorInvalidValue;
+  }
   BwdParams bp;
   bp.B = p.B;
   bp.S = p.S;
@@ -1009,6 +1601,7 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   bp.qo_n = (long long)p.B * p.S * p.n_head * D;
   bp.Ld = delta_ld(p);
   bp.rows_n = (long long)PB * hp * bp.Ld;
+  bp.Sp = (p.S + 127) / 128 * 128;
   bp.rope_n = (long long)p.S * (D / 2);
   // CTA units: (group member, batch, head), each over the full sequence.
   const int UB = Pu * p.B;
@@ -1054,18 +1647,49 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
     if (e != cudaSuccess) return e;
     dq_kernel<D><<<(unsigned)q_blocks, kThreadsQ, QLayout<D>::kAlloc, st>>>(mK128, mV128, bp);
     e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  // the float dQ accumulator [Pu*B*hp*Sp][D]: the fused kernel adds [128 x 32] boxes into it
+  const long long acc_rows = (long long)UB * hp * bp.Sp;
+  if ((parts & (kBwdFused | kBwdFinish)) && acc_rows > 0x7fffffffll) return cudaErrorInvalidValue;  // int coords
+  if (parts & kBwdFused) {
+    CUtensorMap mAcc;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)acc_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 4};
+    const cuuint32_t box[2] = {32, 128};  // 128-byte rows, swizzled like the staging areas
+    const cuuint32_t estr[2] = {1, 1};
+    if (!dqacc || enc.encode(&mAcc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, dqacc, dims, strides, box, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    // the fused kernel's CTAs also keep their heads' dQ accumulator rows in L2
+    bp.group_kv = l2_head_group((size_t)4 * p.S * D * bp.group * 2, UB * kvp, n_t * UB * kvp);
+    e = cudaFuncSetAttribute(dkdvq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)FLayout<D>::kAlloc);
+    if (e != cudaSuccess) return e;
+    dkdvq_kernel<D><<<(unsigned)kv_blocks, kThreadsF, FLayout<D>::kAlloc, st>>>(mK128, mV128, mQ128, mdO128, mL,
+                                                                                  mDl, mAcc, bp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (parts & kBwdFinish) {
+    if (!dqacc) return cudaErrorInvalidValue;
+    const long long tasks = (long long)p.B * p.S * p.n_head * (D / 8);  // (token, head, 4 rotation pairs)
+    const long long grid = (tasks + 255) / 256;
+    if (grid > 0x7fffffffll) return cudaErrorInvalidValue;
+    dq_finish_kernel<D><<<(unsigned)grid, 256, 0, st>>>(dqacc, bp);
+    e = cudaGetLastError();
   }
   return e;
 }
 
 cudaError_t launch_parts(const ulysses_problem &p, const TmaEncoder &enc, const void *q, const void *k,
                          const void *v, const void *do_head, const float *nlse, const float *delta,
-                         const void *ws, void *dq, void *dk, void *dv, uint32_t *status, int parts, bool folded,
-                         cudaStream_t st) {
+                         const void *ws, void *dq, void *dk, void *dv, float *dqacc, uint32_t *status, int parts,
+                         bool folded, cudaStream_t st) {
   if (p.head_dim == 128)
-    return launch_d<128>(p, enc, q, k, v, do_head, nlse, delta, ws, dq, dk, dv, status, parts, folded, st);
+    return launch_d<128>(p, enc, q, k, v, do_head, nlse, delta, ws, dq, dk, dv, dqacc, status, parts, folded, st);
   if (p.head_dim == 64)
-    return launch_d<64>(p, enc, q, k, v, do_head, nlse, delta, ws, dq, dk, dv, status, parts, folded, st);
+    return launch_d<64>(p, enc, q, k, v, do_head, nlse, delta, ws, dq, dk, dv, dqacc, status, parts, folded, st);
   return cudaErrorInvalidValue;
 }
 
@@ -1075,16 +1699,30 @@ cudaError_t launch_attn_bwd_dkdv(const ulysses_problem &p, const TmaEncoder &enc
                                  const void *k, const void *v, const void *do_head, const float *nlse,
                                  const float *delta, const void *ws, void *dk_seq, void *dv_seq,
                                  uint32_t *status, cudaStream_t st, bool folded) {
-  return launch_parts(p, enc, q, k, v, do_head, nlse, delta, ws, nullptr, dk_seq, dv_seq, status, kBwdDkDv,
+  return launch_parts(p, enc, q, k, v, do_head, nlse, delta, ws, nullptr, dk_seq, dv_seq, nullptr, status, kBwdDkDv,
                       folded, st);
+}
+
+cudaError_t launch_attn_bwd_fused(const ulysses_problem &p, const TmaEncoder &enc, const void *q, const void *k,
+                                  const void *v, const void *do_head, const float *nlse, const float *delta,
+                                  const void *ws, float *dq_acc, void *dk_seq, void *dv_seq, uint32_t *status,
+                                  cudaStream_t st, bool folded) {
+  return launch_parts(p, enc, q, k, v, do_head, nlse, delta, ws, nullptr, dk_seq, dv_seq, dq_acc, status, kBwdFused,
+                      folded, st);
+}
+
+cudaError_t launch_dq_finish(const ulysses_problem &p, const TmaEncoder &enc, const void *ws, float *dq_acc,
+                             void *dq_seq, uint32_t *status, cudaStream_t st) {
+  return launch_parts(p, enc, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, ws, dq_seq, nullptr, nullptr,
+                      dq_acc, status, kBwdFinish, false, st);
 }
 
 cudaError_t launch_attn_bwd_dq(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
                                const void *k, const void *v, const void *do_head, const float *nlse,
                                const float *delta, const void *ws, void *dq_seq, uint32_t *status,
                                cudaStream_t st, bool folded) {
-  return launch_parts(p, enc, q, k, v, do_head, nlse, delta, ws, dq_seq, nullptr, nullptr, status, kBwdDq, folded,
-                      st);
+  return launch_parts(p, enc, q, k, v, do_head, nlse, delta, ws, dq_seq, nullptr, nullptr, nullptr, status, kBwdDq,
+                      folded, st);
 }
 
 }  // namespace ulysses

@@ -22,6 +22,9 @@ struct WorkspaceLayout {
   // float [P][B][S][D] each, summed over the replicas afterwards (backward).
   size_t dkpart = 0, dvpart = 0, part_bytes = 0;
   size_t total_fwd = 0, total_bwd = 0;
+  // The fused backward's float dQ accumulator [B*n_head][Sp][D] (Sp = S rounded
+  // up to 128), behind the phase-1 workspace (phase 2 only).
+  size_t dqacc = 0, dqacc_bytes = 0, total_fused = 0;
 };
 WorkspaceLayout workspace_layout(const ulysses_problem &p);
 
@@ -117,6 +120,18 @@ cudaError_t launch_attn_bwd_dq(const ulysses_problem &p, const TmaEncoder &enc, 
                                const void *k, const void *v, const void *do_head, const float *nlse,
                                const float *delta, const void *ws, void *dq_seq, uint32_t *status,
                                cudaStream_t st, bool folded = false);
+// The fused backward (attn_bwd_tc.cu): dK / dV as the dK/dV kernel writes
+// them, and every step's dQ share added into the float accumulator dq_acc
+// (which must hold zeros); then dq_finish scales, unrotates and writes dQ in
+// sequence layout.
+cudaError_t launch_attn_bwd_fused(const ulysses_problem &p, const TmaEncoder &enc, const void *q, const void *k,
+                                  const void *v, const void *do_head, const float *nlse, const float *delta,
+                                  const void *ws, float *dq_acc, void *dk_seq, void *dv_seq, uint32_t *status,
+                                  cudaStream_t st, bool folded = false);
+cudaError_t launch_dq_finish(const ulysses_problem &p, const TmaEncoder &enc, const void *ws, float *dq_acc,
+                             void *dq_seq, uint32_t *status, cudaStream_t st);
+// n floats from `p` (16-byte aligned) set to zero.
+cudaError_t launch_zero(float *p, size_t n, cudaStream_t st);
 
 // Heads per CTA group (see grouped_order): as many heads as keep the tiles
 // their CTAs stream (per_head_bytes each) within about 48 MiB of L2.  A grid

@@ -370,6 +370,20 @@ cudaError_t launch_rope_table(const ulysses_problem &p, void *ws, cudaStream_t s
   return cudaGetLastError();
 }
 
+__global__ void zero_kernel(float4 *p, long long n4) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x)
+    p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+cudaError_t launch_zero(float *p, size_t n, cudaStream_t st) {
+  const long long n4 = (long long)(n / 4);
+  if (n % 4 || n4 == 0) return n4 == 0 && n == 0 ? cudaSuccess : cudaErrorInvalidValue;
+  long long grid = (n4 + 255) / 256;
+  if (grid > 4096) grid = 4096;
+  zero_kernel<<<(unsigned)grid, 256, 0, st>>>(reinterpret_cast<float4 *>(p), n4);
+  return cudaGetLastError();
+}
+
 static PermParams base_params(const ulysses_problem &p, const void *ws, int to_head) {
   PermParams pp{};
   pp.P = p.P;

@@ -47,6 +47,9 @@ WorkspaceLayout workspace_layout(const ulysses_problem &p) {
   L.dkpart = align256(L.dohead + L.dohead_bytes);
   L.dvpart = align256(L.dkpart + L.part_bytes);
   L.total_bwd = align256(L.dvpart + L.part_bytes);
+  L.dqacc = L.total_bwd;
+  L.dqacc_bytes = (size_t)p.B * p.n_head * ((p.S + 127) / 128 * 128) * p.head_dim * 4;
+  L.total_fused = align256(L.dqacc + L.dqacc_bytes);
   return L;
 }
 
@@ -121,7 +124,7 @@ int check_ws(const ulysses_problem &p, const void *ws, size_t ws_bytes, int phas
   if (!ws) return ULYSSES_ERR_WORKSPACE;
   if (!aligned16(ws)) return ULYSSES_ERR_ALIGN;
   const WorkspaceLayout L = workspace_layout(p);
-  if (ws_bytes < (phase ? L.total_bwd : L.total_fwd)) return ULYSSES_ERR_WORKSPACE;
+  if (ws_bytes < (phase == 2 ? L.total_fused : phase ? L.total_bwd : L.total_fwd)) return ULYSSES_ERR_WORKSPACE;
   return ULYSSES_OK;
 }
 
@@ -174,7 +177,7 @@ int ulysses_validate(const ulysses_problem *prob) {
 size_t ulysses_workspace_bytes(const ulysses_problem *prob, int phase) {
   if (ulysses_validate(prob) != ULYSSES_OK) return 0;
   const WorkspaceLayout L = workspace_layout(*prob);
-  return phase ? L.total_bwd : L.total_fwd;
+  return phase == 2 ? L.total_fused : phase ? L.total_bwd : L.total_fwd;
 }
 
 int ulysses_workspace_init(const ulysses_problem *prob, void *ws, size_t ws_bytes,
@@ -420,6 +423,72 @@ int ulysses::check_bwd_call(const ulysses_problem *prob, const void *q_head, con
 }
 
 extern "C" {
+
+int ulysses_attn_bwd_dkdvq(const ulysses_problem *prob, const void *q_head, const void *k_head,
+                           const void *v_head, void *dk_seq, void *dv_seq, void *ws, size_t ws_bytes,
+                           ulysses_stream_t stream) {
+  const NvtxRange range("ulysses_attn_bwd_dkdvq");
+  int rc = bwd_common(prob, ws, ws_bytes);
+  if (rc) return rc;
+  const ulysses_problem &p = *prob;
+  if ((rc = check_ws(p, ws, ws_bytes, 2))) return rc;
+  const size_t nq = act_bytes(p, p.n_head), nk = act_bytes(p, p.n_kv_head), nkh = kv_head_bytes(p);
+  const Span in[3] = {{q_head, nq}, {k_head, nkh}, {v_head, nkh}};
+  const Span out[3] = {{dk_seq, nk}, {dv_seq, nk}, {ws, ws_bytes}};
+  if ((rc = check_spans(in, 3, out, 3))) return rc;
+  TmaEncoder enc;
+  if (!get_tma_encoder(&enc)) return ULYSSES_ERR_CUDA;
+  const WorkspaceLayout L = workspace_layout(p);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  cudaStream_t st = (cudaStream_t)stream;
+  float *acc = reinterpret_cast<float *>(w + L.dqacc);
+  uint32_t *status = reinterpret_cast<uint32_t *>(w + L.status);
+  const float *nlse = reinterpret_cast<const float *>(w + L.nlse), *delta = reinterpret_cast<const float *>(w + L.delta);
+  // the dQ shares are added into a zeroed accumulator
+  if (launch_zero(acc, L.dqacc_bytes / 4, st) != cudaSuccess) return ULYSSES_ERR_CUDA;
+  if (kv_replicas(p) > 1) {
+    float *dkp = reinterpret_cast<float *>(w + L.dkpart), *dvp = reinterpret_cast<float *>(w + L.dvpart);
+    cudaError_t e = launch_attn_bwd_fused(p, enc, q_head, k_head, v_head, w + L.dohead, nlse, delta, ws, acc, dkp,
+                                          dvp, status, st);
+    if (e == cudaSuccess) {
+      const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)p.head_dim);
+      e = launch_kv_reduce(p, dkp, dvp, dk_seq, dv_seq, scale, ws, st);
+    }
+    return cuda_rc(e);
+  }
+  return cuda_rc(launch_attn_bwd_fused(p, enc, q_head, k_head, v_head, w + L.dohead, nlse, delta, ws, acc, dk_seq,
+                                       dv_seq, status, st));
+}
+
+int ulysses_attn_bwd_dq_finish(const ulysses_problem *prob, void *dq_seq, void *ws, size_t ws_bytes,
+                               ulysses_stream_t stream) {
+  const NvtxRange range("ulysses_attn_bwd_dq_finish");
+  int rc = bwd_common(prob, ws, ws_bytes);
+  if (rc) return rc;
+  const ulysses_problem &p = *prob;
+  if ((rc = check_ws(p, ws, ws_bytes, 2))) return rc;
+  const Span out[2] = {{dq_seq, act_bytes(p, p.n_head)}, {ws, ws_bytes}};
+  if ((rc = check_spans(nullptr, 0, out, 2))) return rc;
+  TmaEncoder enc;
+  const WorkspaceLayout L = workspace_layout(p);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  return cuda_rc(launch_dq_finish(p, enc, ws, reinterpret_cast<float *>(w + L.dqacc), dq_seq,
+                                  reinterpret_cast<uint32_t *>(w + L.status), (cudaStream_t)stream));
+}
+
+int ulysses_attn_bwd_fused(const ulysses_problem *prob, const void *q_head, const void *k_head,
+                           const void *v_head, const void *o_head, const float *lse, const void *do_seq,
+                           void *dq_seq, void *dk_seq, void *dv_seq, void *ws, size_t ws_bytes,
+                           ulysses_stream_t stream) {
+  const NvtxRange range("ulysses_attn_bwd_fused");
+  int rc = check_bwd_call(prob, q_head, k_head, v_head, o_head, lse, do_seq, dq_seq, dk_seq, dv_seq, ws,
+                          ws_bytes);
+  if (rc) return rc;
+  if ((rc = check_ws(*prob, ws, ws_bytes, 2))) return rc;
+  if ((rc = ulysses_attn_bwd_prepare(prob, o_head, lse, do_seq, ws, ws_bytes, stream))) return rc;
+  if ((rc = ulysses_attn_bwd_dkdvq(prob, q_head, k_head, v_head, dk_seq, dv_seq, ws, ws_bytes, stream))) return rc;
+  return ulysses_attn_bwd_dq_finish(prob, dq_seq, ws, ws_bytes, stream);
+}
 
 int ulysses_attn_bwd(const ulysses_problem *prob, const void *q_head, const void *k_head,
                      const void *v_head, const void *o_head, const float *lse,
