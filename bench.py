@@ -794,8 +794,13 @@ def main():
         "e2e": {"value": job_throughput(tokens, e2e_ms * 1e-3, world), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": r["launches"],
-        "folded_fwd": r["folded"]["fwd"] if r["folded"] else None,
-        "folded_bwd": r["folded"].get("bwd") if r["folded"] else None,
+        # the folded mode (both All-to-Alls as addressing) is timed beside the
+        # headline path, not on it: it needs q and k rotated by their producer
+        # (RoPE off), and its backward reads dO and Q in sequence layout with
+        # strided tile rows, which costs more than the dO pack it saves
+        "folded_mode": ({**r["folded"], "on_headline_path": False,
+                         "note": "RoPE off (q, k rotated by their producer); timed beside the headline path"}
+                        if r["folded"] else None),
         "device_status": r["status"],
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -95,7 +95,8 @@ def test_bench_line_carries_the_contract_keys(monkeypatch, capsys):
     assert abs(line["attn_bwd_tflops_2p5x"] - 1.25 * line["attn_bwd_tflops"]) < 1e-9
     assert line["value"] == pytest.approx(32768 / (line["ms_per_step"] * 1e-3))
     assert set(line["e2e"]) == {"value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"}
-    assert line["folded_bwd"] == {"unfolded_ms": 19.8, "ms": 19.9}
+    assert line["folded_mode"]["bwd"] == {"unfolded_ms": 19.8, "ms": 19.9}
+    assert line["folded_mode"]["on_headline_path"] is False
     m = line["bwd_modes"]
     assert m["two_kernel"]["ms"] == pytest.approx(0.17 + 10.9 + 8.4)
     assert m["fused"]["ms"] == pytest.approx(0.17 + 20.0 + 1.0) and m["fused"]["kernel"] == "dkdvq_kernel<128>"
