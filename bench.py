@@ -39,17 +39,18 @@ METRIC = "tokens/s + attn TFLOP/s (S=32K, 32 heads, P=8 virtual); seq↔head per
 
 # ------------------------------------------------------------------ helpers
 
-# DRAM bytes (read + write) per launch of a kernel on a workload, from one ncu
-# capture of this build: the mean over the launches of the bench's own steps
-# (3 warm-up + 2 timed; the launch-list summaries under profiles/ give the
-# commands and the tables); a kernel changed since its capture has no entry.
+# DRAM bytes (read + write) per launch of a kernel on a workload, from ncu
+# captures of this build: one kernel per capture, the mean of its two launches
+# in the bench's timed steps (`-k regex:<kernel> -s 3 -c 2` on `bench.py
+# --workload <w> --steps 2 --warmup 3 --no-cpu-baseline`; profiles/ gives the
+# commands and tables); a kernel changed since its capture has no entry.
 TRAFFIC = {
-    ("attn_fwd", "C4"): 1179509350,
-    ("bwd_dkdv", "C4"): 1792275866,
-    ("bwd_dq", "C4"): 1727045376,
-    ("attn_fwd", "C4-ring8"): 1205396685,
-    ("bwd_dkdv", "C4-ring8"): 1825418240,
-    ("bwd_dq", "C4-ring8"): 1798017178,
+    ("attn_fwd", "C4"): 1062845312,
+    ("bwd_dkdv", "C4"): 1627353472,
+    ("bwd_dq", "C4"): 1359185920,
+    ("attn_fwd", "C4-ring8"): 1077393792,
+    ("bwd_dkdv", "C4-ring8"): 1636954368,
+    ("bwd_dq", "C4-ring8"): 1360104576,
 }
 
 

@@ -1608,8 +1608,14 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   // dK/dV CTAs of a kv-head stream the Q and dO of its q-heads; dQ CTAs of a
   // q-head stream its kv-head's K and V (shared by the group's q-heads).
   const long long n_t = (p.S + 127) / 128;
-  bp.group_kv = l2_head_group((size_t)4 * p.S * D * bp.group, UB * kvp, n_t * UB * kvp);
-  bp.group_q = l2_head_group((size_t)4 * p.S * D / bp.group, UB * hp, n_t * UB * hp);
+  // Budgets measured at the pages' sizing (16 MiB of K and V, or of Q and dO,
+  // per head; DRAM bytes per launch, same kernel times): dK/dV 1.80 GB with
+  // 48 MiB (3-head groups), 1.63 GB with 32 MiB (the algorithmic 1.61 GB); dQ
+  // 1.72 GB with 48 MiB, 1.43 GB with 32 MiB, 1.36 GB with 16 MiB (algorithmic
+  // 1.34 GB).  Half of the 129 MB L2 sits on each die, and the tiles of the
+  // running groups share it with the outputs and the other operands.
+  bp.group_kv = l2_head_group((size_t)4 * p.S * D * bp.group, UB * kvp, n_t * UB * kvp, (size_t)32 << 20);
+  bp.group_q = l2_head_group((size_t)4 * p.S * D / bp.group, UB * hp, n_t * UB * hp, (size_t)16 << 20);
   bp.scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)D);
   bp.scale_log2 = bp.scale * kLog2e;
   bp.nlse = nlse;

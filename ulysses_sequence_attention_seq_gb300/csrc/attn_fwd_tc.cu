@@ -69,9 +69,11 @@ constexpr int BM = 128;        // query rows per tile (two tiles per CTA)
 constexpr int BN = 128;        // keys per tile
 constexpr int kThreads = 384;  // warpgroups 0-1 softmax, warpgroup 2: TMA, MMA, 2 idle warps
 constexpr int kTmaWarp = 8, kMmaWarp = 9;
-// Register split (launch: 384 threads x 168): warpgroup 2 drops to 72, the
-// softmax warpgroups rise to 216: 128*72 + 256*216 = 64512 = 384*168.
-constexpr uint32_t kRegsProducer = 72, kRegsSoftmax = 216;
+// Register split (launch: 384 threads x 168): warpgroup 2 drops to 64, the
+// softmax warpgroups rise to 216: 128*64 + 256*216 = 63488 <= 384*168.  (With
+// 72 for warpgroup 2, ptxas allocated the kernel with a 4-byte spill; with 64
+// it has none.)
+constexpr uint32_t kRegsProducer = 64, kRegsSoftmax = 216;
 static_assert(128 * kRegsProducer + 256 * kRegsSoftmax <= 384 * 168, "register split over budget");
 constexpr int kSlots = 2;  // K/V ring entries: entry e holds V_e and K_{e+1}
 constexpr uint32_t kTmemCols = 512;
@@ -527,7 +529,11 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   fp.scale_log2 = scale * 1.4426950408889634f;
   // a q-head's CTAs stream its kv-head's K and V; the group's q-heads share them
   const int units = Pu * p.B * hp;  // (group member, batch, local head): one full-sequence head each
-  fp.head_group = l2_head_group((size_t)4 * p.S * D / fp.group, units, (long long)fp.n_pairs * units);
+  // 32 MiB: at the pages' sizing 3-head groups (48 MiB) moved 1.18 GB of DRAM
+  // per launch, 2-head groups 1.06 GB (the algorithmic 1.08 GB), in the same
+  // time (16 MiB, 1-head groups: 2 % slower).
+  fp.head_group = l2_head_group((size_t)4 * p.S * D / fp.group, units, (long long)fp.n_pairs * units,
+                                (size_t)32 << 20);
   fp.o = static_cast<__nv_bfloat16 *>(o);
   fp.lse = lse;
   fp.o_n = (long long)p.B * p.S * p.n_head * D;  // O in head or sequence layout: the same elements

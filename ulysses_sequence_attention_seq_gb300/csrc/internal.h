@@ -134,17 +134,18 @@ cudaError_t launch_dq_finish(const ulysses_problem &p, const TmaEncoder &enc, co
 cudaError_t launch_zero(float *p, size_t n, cudaStream_t st);
 
 // Heads per CTA group (see grouped_order): as many heads as keep the tiles
-// their CTAs stream (per_head_bytes each) within about 48 MiB of L2.  A grid
+// their CTAs stream (per_head_bytes each) within `budget` bytes of L2 (48 MiB
+// unless the kernel asks for less).  A grid
 // with fewer than 16 CTAs per SM keeps one group (plain longest-first order):
 // there a late group's longest CTAs would start near the end and lengthen the
 // tail by more than the L2 misses cost.
-inline int l2_head_group(size_t per_head_bytes, int n_heads, long long n_ctas) {
+inline int l2_head_group(size_t per_head_bytes, int n_heads, long long n_ctas,
+                         size_t budget = (size_t)48 << 20) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
                                                 cudaSuccess || sms <= 0)
     sms = 152;
   if (n_ctas < 16LL * sms) return n_heads;
-  const size_t budget = (size_t)48 << 20;
   size_t g = per_head_bytes ? budget / per_head_bytes : (size_t)n_heads;
   if (g < 1) g = 1;
   if (g > (size_t)n_heads) g = (size_t)n_heads;
