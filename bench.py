@@ -63,6 +63,42 @@ def load_peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+# The backward's tensor-core kernels: (kernel, algorithmic FLOPs, executed
+# FLOPs) as functions of the forward's algorithmic FLOPs.  The method's
+# products are the forward's S and PV and the backward's dV, dP, dQ, dK, each
+# half a forward; the two-kernel backward's kernels both recompute S and the
+# dQ kernel dP as well; the dS-store dK/dV kernel is the dK/dV kernel that
+# also writes dS (its dQ step is a plain sum of products over stored tiles,
+# bound by HBM); the fused kernel adds each pair's dQ share.
+BWD_TC = {
+    "bwd_dkdv": lambda fl: ("dkdv_kernel", 1.5 * fl, 2.0 * fl),
+    "bwd_dq": lambda fl: ("dq_kernel", 0.5 * fl, 1.5 * fl),
+    "bwd_dkdv_ds": lambda fl: ("dkdv_kernel", 1.5 * fl, 2.0 * fl),
+    "bwd_dkdvq": lambda fl: ("dkdvq_kernel", 2.0 * fl, 2.5 * fl),
+}
+BWD_NOTES = {
+    "two_kernel": "ulysses_attn_bwd: dK/dV kernel, then the dQ kernel recomputing S and dP; 7 products per tile "
+                  "pair; bit-reproducible",
+    "ds_store": "ulysses_attn_bwd_ds: the dK/dV kernel also stores every tile pair's bf16 dS (32 KB a pair), dQ "
+                "is summed from the stored tiles; 5 products per tile pair; bit-reproducible",
+    "fused": "ulysses_attn_bwd_fused: dQ shares reduce-added into a float accumulator inside the dK/dV loop; 5 "
+             "products per tile pair; dQ reproducible to float rounding",
+}
+
+
+def ds_tiles(w):
+    """(key tile, query tile) pairs of one head the dS store holds."""
+    n = (w.S + 127) // 128
+    return n * (n + 1) // 2 if w.causal else n * n
+
+
+def dq_ds_bytes(w, es):
+    """Bytes the dQ-from-dS step moves at the least: every stored 128 x 128
+    bf16 dS tile, K (the kv-heads over the sequence) and dQ, once each."""
+    return (w.B * w.n_head * ds_tiles(w) * 128 * 128 * 2 + w.B * w.S * w.n_kv_head * w.head_dim * es
+            + w.B * w.S * w.n_head * w.head_dim * es)
+
+
 def attn_fwd_flops(w):
     """Algorithmic FLOPs of the attention forward: two matmuls (QK^T and PV),
     2*D flops per (query, key) pair each; causal counts S(S+1)/2 pairs."""
@@ -147,8 +183,10 @@ def run_ulysses(args, w, rank, world):
     prob = U.Problem.from_workload(w)
     backward = w.backward and not args.fwd_only
     ins = make_inputs(w, with_grad=backward)
-    # phase-2 workspace: the fused backward (timed beside the two-kernel one) needs its dQ accumulator
-    buf = U.Buffers(prob, device=dev, backward=backward, fused=backward)
+    # a workspace for every backward mode: the fused one's dQ accumulator
+    # (phase 2) and the dS-store one's tiles (phase 3); the modes not on the
+    # headline are timed beside it
+    buf = U.Buffers(prob, device=dev, backward=backward, fused=backward, ds=backward)
     host = {"q": U.seq_layout(ins["q"], w.P).pin_memory(), "k": U.seq_layout(ins["k"], w.P).pin_memory(),
             "v": U.seq_layout(ins["v"], w.P).pin_memory()}
     if backward:
@@ -162,15 +200,36 @@ def run_ulysses(args, w, rank, world):
     U.ulysses_workspace_init(prob, buf.ws)
     torch.cuda.synchronize()
 
-    names = ["pack_qkv", "attn_fwd", "unpack_out"] + (["bwd_prepare", "bwd_dkdv", "bwd_dq"] if backward else [])
+    # Each backward mode as the entry points that make up its composed call
+    # (ulysses_attn_bwd, ulysses_attn_bwd_ds, ulysses_attn_bwd_fused), so
+    # that each kernel gets its own events.
+    b = buf
+    bwd_steps = {
+        "two_kernel": (
+            ("bwd_prepare", lambda: U.ulysses_attn_bwd_prepare(prob, b.o_head, b.lse, b.do_seq, b.ws)),
+            ("bwd_dkdv", lambda: U.ulysses_attn_bwd_dkdv(prob, b.q_head, b.k_head, b.v_head, b.dk_seq, b.dv_seq,
+                                                         b.ws)),
+            ("bwd_dq", lambda: U.ulysses_attn_bwd_dq(prob, b.q_head, b.k_head, b.v_head, b.dq_seq, b.ws))),
+        "ds_store": (
+            ("bwd_prepare", lambda: U.ulysses_attn_bwd_prepare(prob, b.o_head, b.lse, b.do_seq, b.ws)),
+            ("bwd_dkdv_ds", lambda: U.ulysses_attn_bwd_dkdv_ds(prob, b.q_head, b.k_head, b.v_head, b.dk_seq,
+                                                               b.dv_seq, b.ws)),
+            ("bwd_dq_ds", lambda: U.ulysses_attn_bwd_dq_ds(prob, b.k_head, b.dq_seq, b.ws))),
+        "fused": (
+            ("bwd_prepare", lambda: U.ulysses_attn_bwd_prepare(prob, b.o_head, b.lse, b.do_seq, b.ws)),
+            ("bwd_dkdvq", lambda: U.ulysses_attn_bwd_dkdvq(prob, b.q_head, b.k_head, b.v_head, b.dk_seq, b.dv_seq,
+                                                           b.ws)),
+            ("bwd_dq_finish", lambda: U.ulysses_attn_bwd_dq_finish(prob, b.dq_seq, b.ws))),
+    }
+    mode = args.bwd_mode if backward else None
+    names = ["pack_qkv", "attn_fwd", "unpack_out"] + ([n for n, _ in bwd_steps[mode]] if backward else [])
     # pack, forward, unpack; prepare, dK/dV (+ the replica sum when kv-heads are
     # replicated), dQ
     launches_per_step = 3 + ((4 if w.n_kv_head < w.P // w.ring else 3) if backward else 0)
 
-    def step(evs=None, split=True):
-        """One pass of the whole path.  With `split` the backward runs as its
-        three entry points (the same launches as ulysses_attn_bwd) so that each
-        kernel gets its own events."""
+    def step(evs=None):
+        """One pass of the whole path: pack, attention, unpack, and the
+        backward of the headline mode."""
         def mark(i):
             if evs is not None:
                 evs[i].record(stream)
@@ -182,15 +241,9 @@ def run_ulysses(args, w, rank, world):
         U.ulysses_unpack_out(prob, buf.o_head, buf.o_seq)
         mark(3)
         if backward:
-            if split:
-                U.ulysses_attn_bwd_prepare(prob, buf.o_head, buf.lse, buf.do_seq, buf.ws)
-                mark(4)
-                U.ulysses_attn_bwd_dkdv(prob, buf.q_head, buf.k_head, buf.v_head, buf.dk_seq, buf.dv_seq, buf.ws)
-                mark(5)
-                U.ulysses_attn_bwd_dq(prob, buf.q_head, buf.k_head, buf.v_head, buf.dq_seq, buf.ws)
-                mark(6)
-            else:
-                buf.backward()
+            for i, (_, fn) in enumerate(bwd_steps[mode]):
+                fn()
+                mark(4 + i)
 
     for _ in range(args.warmup):
         step()
@@ -217,42 +270,39 @@ def run_ulysses(args, w, rank, world):
     total_ms = t0.elapsed_time(t1)
     per = {n: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)] for i, n in enumerate(names)}
 
-    # ---- the fused backward (dQ accumulated in the dK/dV loop): the same
-    # K steps' backward through its three entry points, each kernel timed
-    fused_per = None
-    if backward:
-        fnames = ["bwd_prepare", "bwd_dkdvq", "bwd_dq_finish"]
+    # ---- the other backward modes: the same K steps' backward through each
+    # one's entry points, each kernel timed
+    alt_per = {}
+    for m in (sorted(bwd_steps) if backward else []):
+        if m == mode:
+            continue
 
-        def fused_bwd(ev=None):
-            def fmark(i):
+        def alt_bwd(ev=None, m=m):
+            if ev is not None:
+                ev[0].record(stream)
+            for i, (_, fn) in enumerate(bwd_steps[m]):
+                fn()
                 if ev is not None:
-                    ev[i].record(stream)
-            fmark(0)
-            U.ulysses_attn_bwd_prepare(prob, buf.o_head, buf.lse, buf.do_seq, buf.ws)
-            fmark(1)
-            U.ulysses_attn_bwd_dkdvq(prob, buf.q_head, buf.k_head, buf.v_head, buf.dk_seq, buf.dv_seq, buf.ws)
-            fmark(2)
-            U.ulysses_attn_bwd_dq_finish(prob, buf.dq_seq, buf.ws)
-            fmark(3)
+                    ev[i + 1].record(stream)
 
         for _ in range(2):
-            fused_bwd()
+            alt_bwd()
         fev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
         torch.cuda.synchronize()
         for k in range(args.steps):
-            fused_bwd(fev[k])
+            alt_bwd(fev[k])
         torch.cuda.synchronize()
-        fused_per = {n: [fev[k][i].elapsed_time(fev[k][i + 1]) for k in range(args.steps)]
-                     for i, n in enumerate(fnames)}
+        alt_per[m] = {n: [fev[k][i].elapsed_time(fev[k][i + 1]) for k in range(args.steps)]
+                      for i, (n, _) in enumerate(bwd_steps[m])}
         if U.ulysses_read_status(buf.ws) != 0:
-            raise RuntimeError("device status word set during the fused backward steps")
+            raise RuntimeError(f"device status word set during the {m} backward steps")
 
     # ---- end to end through the public API with host buffers: every step
     # uploads its inputs from pinned host memory and downloads its results
     # (O, and dQ, dK, dV with a backward); the streamed path overlaps step k's
     # compute with step k+1's upload and step k-1's download.
     from ulysses_sequence_attention_seq_gb300.streamed import StreamedPath
-    sp = StreamedPath(prob, backward=backward, device=dev)
+    sp = StreamedPath(prob, backward=backward, device=dev, bwd_mode=mode or "two_kernel")
     host_in = {"q_seq": host["q"], "k_seq": host["k"], "v_seq": host["v"]}
     if backward:
         host_in["do_seq"] = host["do"]
@@ -317,8 +367,8 @@ def run_ulysses(args, w, rank, world):
     # the MUFU unit's exponential throughput on this GPU (the softmax's secondary bound)
     ex2_rate = U.ulysses_selftest_ex2_rate()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    return dict(total_ms=total_ms, per=per, fused_per=fused_per, clocks=clk, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
-                launches=launches_per_step * args.steps, status=status, backward=backward,
+    return dict(total_ms=total_ms, per=per, alt_per=alt_per, bwd_mode=mode, clocks=clk, e2e_ms=e2e_ms, h2d=h2d,
+                d2h=d2h, launches=launches_per_step * args.steps, status=status, backward=backward,
                 folded=folded, ex2_rate=ex2_rate, sms=sms)
 
 
@@ -649,6 +699,8 @@ def main():
     ap.add_argument("--workload", default="C4", choices=sorted(WORKLOADS) + sorted(EXTRA_WORKLOADS))
     ap.add_argument("--impl", default="ulysses", choices=["ulysses", "reference"])
     ap.add_argument("--fwd-only", action="store_true")
+    ap.add_argument("--bwd-mode", default="ds_store", choices=["ds_store", "two_kernel", "fused"],
+                    help="the backward on the headline step (the other modes are timed beside it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="time the permutation alone over S = 4K..128K")
     ap.add_argument("--proj", action="store_true",
@@ -704,8 +756,8 @@ def main():
     fl = attn_fwd_flops(w)
     es = 2 if w.dtype == "bf16" else 4
     attn_ms = per["attn_fwd"]
-    bwd_parts = ("bwd_prepare", "bwd_dkdv", "bwd_dq")
-    bwd_ms = sum(per[k] for k in bwd_parts) if "bwd_dkdv" in per else None
+    bwd_parts = tuple(k for k in per if k.startswith("bwd_"))
+    bwd_ms = sum(per[k] for k in bwd_parts) if bwd_parts else None
     bwd_tflops = 2.0 * fl / (bwd_ms * 1e-3) / 1e12 if bwd_ms else None
     attn_tflops = fl / (attn_ms * 1e-3) / 1e12
     pack_gbs = permute_bytes(w, es) / (per["pack_qkv"] * 1e-3) / 1e9
@@ -715,9 +767,7 @@ def main():
     # forward) and the FLOPs each kernel executes (dK/dV and dQ both recompute
     # S, dQ also dP).
     tc = {"attn_fwd": ("attn_fwd_tc_kernel", fl, fl)}
-    if bwd_ms:
-        tc["bwd_dkdv"] = ("dkdv_kernel", 1.5 * fl, 2.0 * fl)
-        tc["bwd_dq"] = ("dq_kernel", 0.5 * fl, 1.5 * fl)
+    tc.update({k: BWD_TC[k](fl) for k in bwd_parts if k in BWD_TC})
     kernels = {}
     for k, (kname, alg, exe) in tc.items():
         a_tf = alg / (per[k] * 1e-3) / 1e12
@@ -725,22 +775,28 @@ def main():
                       "achieved_tflops": a_tf, "frac": a_tf / tf_sust,
                       "executed_tflops": exe / (per[k] * 1e-3) / 1e12,
                       "executed_frac": exe / (per[k] * 1e-3) / 1e12 / tf_sust}
+    # dQ from the stored dS tiles reads them once: bound by HBM
+    hbm_kernels = {}
+    if "bwd_dq_ds" in per:
+        nb = dq_ds_bytes(w, es)
+        gbs = nb / (per["bwd_dq_ds"] * 1e-3) / 1e9
+        hbm_kernels["bwd_dq_ds"] = {"bound": "hbm", "kernel": f"dq_ds_kernel<{w.head_dim}>", "achieved": gbs,
+                                    "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "bytes_per_launch": nb,
+                                    "traffic": TRAFFIC.get(("bwd_dq_ds", w.name)),
+                                    "note": "bytes: every stored dS tile, K and dQ once each"}
     bwd_modes = None
-    if bwd_ms and r.get("fused_per"):
-        fp = {k: statistics.mean(v) for k, v in r["fused_per"].items()}
-        f_ms = sum(fp.values())
-        a_tf = 2.0 * fl / (fp["bwd_dkdvq"] * 1e-3) / 1e12
-        bwd_modes = {
-            "two_kernel": {"ms": bwd_ms, "kernel_ms": {k: per[k] for k in bwd_parts},
-                           "note": "ulysses_attn_bwd: dK/dV kernel, then the dQ kernel recomputing S and dP; "
-                                   "7 products per tile pair; bit-reproducible"},
-            "fused": {"ms": f_ms, "kernel_ms": fp,
-                      "kernel": f"dkdvq_kernel<{w.head_dim}>", "algorithmic_tflop": 2.0 * fl / 1e12,
-                      "achieved_tflops": a_tf, "frac": a_tf / tf_sust,
-                      "executed_tflops": 2.5 * fl / (fp["bwd_dkdvq"] * 1e-3) / 1e12,
-                      "note": "ulysses_attn_bwd_fused: dQ shares reduce-added into a float accumulator inside the "
-                              "dK/dV loop; 5 products per tile pair; dQ reproducible to float rounding"},
-            "headline_uses": "two_kernel"}
+    if bwd_ms:
+        by_mode = {r["bwd_mode"]: {k: per[k] for k in bwd_parts}}
+        by_mode.update({m: {k: statistics.mean(v) for k, v in kp.items()} for m, kp in r["alt_per"].items()})
+        bwd_modes = {}
+        for m, kms in by_mode.items():
+            main_k = max((k for k in kms if k in BWD_TC), key=lambda k: kms[k])
+            kname, alg, exe = BWD_TC[main_k](fl)
+            a_tf = alg / (kms[main_k] * 1e-3) / 1e12
+            bwd_modes[m] = {"ms": sum(kms.values()), "kernel_ms": kms, "kernel": f"{kname}<{w.head_dim}>",
+                            "kernel_achieved_tflops": a_tf, "kernel_frac": a_tf / tf_sust,
+                            "kernel_executed_tflops": exe / (kms[main_k] * 1e-3) / 1e12, "note": BWD_NOTES[m]}
+        bwd_modes["headline_uses"] = r["bwd_mode"]
     dominant = max(kernels, key=lambda k: kernels[k]["ms"])
     dk = kernels[dominant]
     # One exponential per (query, key) pair the forward computes, against the
@@ -779,13 +835,16 @@ def main():
                      "frac": dk["frac"], "traffic": TRAFFIC.get((dominant, w.name)),
                      "peak_source": f"{peak_src} bf16 sustained", "kernel": dk["kernel"],
                      "peak_burst": tf_burst, "frac_burst": dk["achieved_tflops"] / tf_burst,
-                     "sm_mhz": r["clocks"].get("sm_mhz"),
+                     "sm_mhz": r["clocks"].get("sm_mhz"), "bwd_mode": r["bwd_mode"],
                      "note": "dominant kernel by time; achieved counts its algorithmic products only; frac is "
                              "against the sustained (power-capped) cuBLAS figure, frac_burst against the burst "
-                             "one; sm_mhz is the median SM clock sampled while the timed steps ran"},
+                             "one; sm_mhz is the median SM clock sampled while the timed steps ran"
+                             + ("; in the dS-store backward the dK/dV kernel also writes every tile pair's dS"
+                                if dominant == "bwd_dkdv_ds" else "")},
         "secondary_rooflines": {**{k: {"bound": "tensor", "achieved": v["achieved_tflops"], "peak": tf_sust,
                                        "unit": "TFLOP/s", "frac": v["frac"], "traffic": TRAFFIC.get((k, w.name))}
                                    for k, v in kernels.items() if k != dominant},
+                                **hbm_kernels,
                                 "pack_qkv": {"bound": "hbm", "achieved": pack_gbs, "peak": hbm, "unit": "GB/s",
                                              "frac": pack_gbs / hbm},
                                 "unpack_out": {"bound": "hbm", "achieved": unpack_gbs, "peak": hbm, "unit": "GB/s",

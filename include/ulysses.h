@@ -123,7 +123,11 @@ int ulysses_validate(const ulysses_problem *prob);
  * 1 = backward (also valid for the forward), 2 = the fused backward
  * (ulysses_attn_bwd_fused; the phase-1 workspace followed by a float dQ
  * accumulator of B*n_head*ceil(S/128)*128*head_dim*4 bytes; valid for every
- * call).  Returns 0 for an invalid problem.  Host only; needs no GPU. */
+ * call), 3 = the dS-store backward (ulysses_attn_bwd_ds; the phase-1
+ * workspace followed by B*n_head*T tiles of 128*128 bf16, T = n(n+1)/2 causal
+ * or n*n unmasked, n = ceil(S/128); valid for every call but the fused
+ * backward's when smaller than phase 2).  Returns 0 for an invalid problem.
+ * Host only; needs no GPU. */
 size_t ulysses_workspace_bytes(const ulysses_problem *prob, int phase);
 
 /* Prepares a workspace for `prob`: clears the status word and, when use_rope
@@ -327,6 +331,39 @@ int ulysses_attn_bwd_dkdvq(const ulysses_problem *prob, const void *q_head, cons
                            ulysses_stream_t stream);
 int ulysses_attn_bwd_dq_finish(const ulysses_problem *prob, void *dq_seq, void *ws, size_t ws_bytes,
                                ulysses_stream_t stream);
+
+/*
+ * The backward with dS stored ("Sequence Parallelism II", §6, the same
+ * gradients as ulysses_attn_bwd).  The dK/dV kernel, which forms every
+ * (128-key, 128-query) tile pair's dS as the operand of its dK product, also
+ * writes that bf16 tile to the workspace; a second tensor-core kernel then
+ * sums dQ = scale * dS K over the stored tiles instead of recomputing the
+ * scores and dP: five matrix products per tile pair, deterministic (every
+ * call gives the same bits), at the price of writing and reading 32 KB per
+ * tile pair (B*n_head*T*32 KB in all, T as under ulysses_workspace_bytes).
+ * dK and dV are bit-identical to ulysses_attn_bwd's; dQ is the sum of the
+ * same bf16 dS values the dK product uses (within the stated tolerance of
+ * ulysses_attn_bwd's).  Same arguments, layouts and results as
+ * ulysses_attn_bwd; `ws` must be sized for phase 3 and prepared by
+ * ulysses_workspace_init.  bf16, head_dim 64 or 128; the errors of
+ * ulysses_attn_bwd, and ULYSSES_ERR_WORKSPACE for a workspace smaller than
+ * phase 3.
+ *
+ * Its steps: ulysses_attn_bwd_prepare (above), then ulysses_attn_bwd_dkdv_ds
+ * (dK, dV into dk_seq / dv_seq as ulysses_attn_bwd_dkdv writes them, and the
+ * dS tiles into the workspace), then ulysses_attn_bwd_dq_ds (dQ from the
+ * tiles and k_head: scaled, RoPE rotation undone, rounded to bf16 into dq_seq
+ * [P][B][Sl][n_head][D]; reads no q, v or dO).
+ */
+int ulysses_attn_bwd_ds(const ulysses_problem *prob, const void *q_head, const void *k_head,
+                        const void *v_head, const void *o_head, const float *lse, const void *do_seq,
+                        void *dq_seq, void *dk_seq, void *dv_seq, void *ws, size_t ws_bytes,
+                        ulysses_stream_t stream);
+int ulysses_attn_bwd_dkdv_ds(const ulysses_problem *prob, const void *q_head, const void *k_head,
+                             const void *v_head, void *dk_seq, void *dv_seq, void *ws, size_t ws_bytes,
+                             ulysses_stream_t stream);
+int ulysses_attn_bwd_dq_ds(const ulysses_problem *prob, const void *k_head, void *dq_seq, void *ws,
+                           size_t ws_bytes, ulysses_stream_t stream);
 
 /*
  * Folded backward: the backward of ulysses_attn_fwd_folded with every

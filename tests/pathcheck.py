@@ -107,11 +107,11 @@ class GpuRun:
     """Inputs on the device in the sequence-sharded layout, workspace prepared,
     forward (and optionally backward) run through the C ABI."""
 
-    def __init__(self, w: Workload, backward: bool = False, inputs=None, fused: bool = False):
+    def __init__(self, w: Workload, backward: bool = False, inputs=None, fused: bool = False, ds: bool = False):
         self.w = w
         self.prob = U.Problem.from_workload(w)
         self.inputs = inputs if inputs is not None else make_inputs(w, with_grad=backward)
-        self.buf = U.Buffers(self.prob, backward=backward, fused=fused)
+        self.buf = U.Buffers(self.prob, backward=backward, fused=fused, ds=ds)
         P = w.P
         self.buf.q_seq.copy_(U.seq_layout(self.inputs["q"], P))
         self.buf.k_seq.copy_(U.seq_layout(self.inputs["k"], P))
@@ -132,6 +132,11 @@ class GpuRun:
 
     def backward_fused(self):
         self.buf.backward_fused()
+        torch.cuda.synchronize()
+        assert U.ulysses_read_status(self.buf.ws) == 0
+
+    def backward_ds(self):
+        self.buf.backward_ds()
         torch.cuda.synchronize()
         assert U.ulysses_read_status(self.buf.ws) == 0
 

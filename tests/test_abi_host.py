@@ -91,6 +91,30 @@ def test_workspace_sizes(lib):
     assert bo - fo >= 2 * po.B * po.n_head * 4100 * 4 + po.B * po.S * po.n_head * po.head_dim * 2
 
 
+def test_ds_store_workspace(lib):
+    """Phase 3 is phase 1 followed by one bf16 128 x 128 dS tile per causal
+    (key tile, query tile) pair of every (batch, q-head), or every pair
+    without the mask; S = 4098 has 33 tiles, the last one ragged."""
+    for kw, n, pairs in ((dict(), 32, 32 * 33 // 2), (dict(causal=False), 32, 32 * 32),
+                         (dict(P=2, S=4098), 33, 33 * 34 // 2)):
+        p = prob(**kw)
+        assert p.S == n * 128 or (p.S + 127) // 128 == n
+        b, d = U.ulysses_workspace_bytes(p, 1), U.ulysses_workspace_bytes(p, 3)
+        assert d == b + ((p.B * p.n_head * pairs * 128 * 128 * 2 + 255) // 256) * 256
+
+
+def test_ds_store_refusals(lib):
+    """The dS-store backward and its dQ step refuse a workspace smaller than
+    phase 3 before any launch."""
+    vp = ctypes.c_void_p
+    ptrs = [vp((1 << 40) + i * (1 << 30)) for i in range(10)]
+    p = prob()
+    n3 = U.ulysses_workspace_bytes(p, 3)
+    assert lib.ulysses_attn_bwd_ds(ctypes.byref(p.c()), *ptrs[:9], vp(1 << 46), n3 - 256, vp(0)) == -7
+    assert lib.ulysses_attn_bwd_dq_ds(ctypes.byref(p.c()), ptrs[1], ptrs[6], vp(1 << 46), n3 - 256, vp(0)) == -7
+    assert lib.ulysses_attn_bwd_dkdv_ds(ctypes.byref(p.c()), *ptrs[:5], vp(1 << 46), n3 - 256, vp(0)) == -7
+
+
 def test_ring_is_refused_where_no_kernel_takes_it(lib):
     """The folded forward and the two projections have no hybrid mode; they
     refuse ring > 1 on the host (fake pointers, never dereferenced)."""

@@ -55,14 +55,17 @@ def test_pack_bytes_count_replicas_within_an_all_to_all_group():
 
 
 def _fake_measurements(backward, steps):
-    """What run_ulysses returns, with plausible timings (no GPU involved)."""
+    """What run_ulysses returns, with plausible timings (no GPU involved): the
+    dS-store backward on the headline, the other two modes beside it."""
     per = {"pack_qkv": [0.29] * steps, "attn_fwd": [5.4] * steps, "unpack_out": [0.08] * steps}
+    alt_per = {}
     if backward:
-        per.update(bwd_prepare=[0.17] * steps, bwd_dkdv=[10.9] * steps, bwd_dq=[8.4] * steps)
+        per.update(bwd_prepare=[0.17] * steps, bwd_dkdv_ds=[13.0] * steps, bwd_dq_ds=[5.0] * steps)
+        alt_per = {"two_kernel": {"bwd_prepare": [0.17] * steps, "bwd_dkdv": [10.9] * steps, "bwd_dq": [8.4] * steps},
+                   "fused": {"bwd_prepare": [0.17] * steps, "bwd_dkdvq": [20.0] * steps,
+                             "bwd_dq_finish": [1.0] * steps}}
     total = sum(v[0] for v in per.values()) * steps
-    fused_per = ({"bwd_prepare": [0.17] * steps, "bwd_dkdvq": [20.0] * steps, "bwd_dq_finish": [1.0] * steps}
-                 if backward else None)
-    return dict(total_ms=total, per=per, fused_per=fused_per,
+    return dict(total_ms=total, per=per, alt_per=alt_per, bwd_mode="ds_store" if backward else None,
                 clocks={"sm_mhz": 2040.0, "sm_max_mhz": 2070.0, "reasons": []},
                 e2e_ms=total * 1.03, h2d=1 << 30, d2h=1 << 30, launches=6 * steps, status=0, backward=backward,
                 folded={"fwd": {"unfolded_ms": 5.8, "ms": 5.6}, "bwd": {"unfolded_ms": 19.8, "ms": 19.9}},
@@ -87,18 +90,26 @@ def test_bench_line_carries_the_contract_keys(monkeypatch, capsys):
     assert line["steps"] == 4 and line["warmup"] == 3 and line["n_gpus"] == 1
     assert line["config"]["workload"] == "C4"
     r = line["roofline"]
-    assert r["kernel"] == "dkdv_kernel<128>" and r["bound"] == "tensor"
-    assert r["traffic"] == bench.TRAFFIC[("bwd_dkdv", "C4")]
+    assert r["kernel"] == "dkdv_kernel<128>" and r["bound"] == "tensor" and r["bwd_mode"] == "ds_store"
+    assert r["traffic"] == bench.TRAFFIC.get(("bwd_dkdv_ds", "C4"))
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-12
-    # dK/dV: dV, dP, dK = 1.5 forwards of algorithmic FLOPs over 10.9 ms
-    assert abs(r["achieved"] - 1.5 * bench.attn_fwd_flops(bench.WORKLOADS["C4"]) / 10.9e-3 / 1e12) < 1e-6
+    # dK/dV (storing dS): dV, dP, dK = 1.5 forwards of algorithmic FLOPs over 13.0 ms
+    c4 = bench.WORKLOADS["C4"]
+    assert abs(r["achieved"] - 1.5 * bench.attn_fwd_flops(c4) / 13.0e-3 / 1e12) < 1e-6
+    # dQ from the stored tiles: HBM-bound, every causal tile pair's 32 KB once, K and dQ once
+    h = line["secondary_rooflines"]["bwd_dq_ds"]
+    tiles = c4.B * c4.n_head * (256 * 257 // 2)
+    assert h["bound"] == "hbm" and h["bytes_per_launch"] == tiles * 32768 + c4.B * c4.S * (32 + 32) * 128 * 2
+    assert abs(h["achieved"] - h["bytes_per_launch"] / 5.0e-3 / 1e9) < 1e-6
     assert abs(line["attn_bwd_tflops_2p5x"] - 1.25 * line["attn_bwd_tflops"]) < 1e-9
     assert line["value"] == pytest.approx(32768 / (line["ms_per_step"] * 1e-3))
     assert set(line["e2e"]) == {"value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"}
     assert line["folded_mode"]["bwd"] == {"unfolded_ms": 19.8, "ms": 19.9}
     assert line["folded_mode"]["on_headline_path"] is False
     m = line["bwd_modes"]
-    assert m["two_kernel"]["ms"] == pytest.approx(0.17 + 10.9 + 8.4)
+    assert m["headline_uses"] == "ds_store"
+    assert m["ds_store"]["ms"] == pytest.approx(0.17 + 13.0 + 5.0) == line["attn_bwd_ms"]
+    assert m["two_kernel"]["ms"] == pytest.approx(0.17 + 10.9 + 8.4) and m["two_kernel"]["kernel"] == "dkdv_kernel<128>"
     assert m["fused"]["ms"] == pytest.approx(0.17 + 20.0 + 1.0) and m["fused"]["kernel"] == "dkdvq_kernel<128>"
 
 

@@ -1,7 +1,8 @@
 """The streamed host-to-host path (two device buffer sets, upload / compute /
 download streams handing over per C-ABI call) gives exactly what the plain
 device path gives, for every step, with different inputs at every step so
-that a result read or written out of order cannot go unnoticed."""
+that a result read or written out of order cannot go unnoticed; with either
+backward (two-kernel, or dS-store)."""
 import pytest
 import torch
 
@@ -18,15 +19,17 @@ def _outs(sp):
             for n in sp.out_names()}
 
 
-@pytest.mark.parametrize("backward", [False, True])
-def test_streamed_steps_match_the_device_path(backward):
+@pytest.mark.parametrize("backward,mode", [(False, "two_kernel"), (True, "two_kernel"), (True, "ds_store")])
+def test_streamed_steps_match_the_device_path(backward, mode):
     w = wl(4, 1, 1024, 8, 4, 128).with_(backward=backward)
-    sp = StreamedPath(U.Problem.from_workload(w), backward=backward)
+    sp = StreamedPath(U.Problem.from_workload(w), backward=backward, bwd_mode=mode)
     refs, hosts = [], []
     for seed in (7, 8, 9):
-        ref = GpuRun(w.with_(seed=seed), backward=backward)
+        ref = GpuRun(w.with_(seed=seed), backward=backward, ds=mode == "ds_store")
         ref.forward()
-        if backward:
+        if backward and mode == "ds_store":
+            ref.backward_ds()
+        elif backward:
             ref.backward()
         refs.append({n: getattr(ref.buf, n).cpu() for n in sp.out_names()})
         hosts.append({n: getattr(ref.buf, n).cpu().pin_memory() for n in sp.in_names()})

@@ -137,6 +137,9 @@ def lib():
         L.ulysses_attn_bwd_fused.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_attn_bwd_dkdvq.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]
         L.ulysses_attn_bwd_dq_finish.argtypes = [P, vp, vp, sz, vp]
+        L.ulysses_attn_bwd_ds.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.ulysses_attn_bwd_dkdv_ds.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.ulysses_attn_bwd_dq_ds.argtypes = [P, vp, vp, vp, sz, vp]
         L.ulysses_status_string.argtypes = [ctypes.c_int]
         L.ulysses_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -272,6 +275,30 @@ def ulysses_attn_bwd_dq_finish(prob, dq_seq, ws, stream=None):
         ctypes.byref(prob.c()), _ptr(dq_seq), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
+def ulysses_attn_bwd_ds(prob, q_head, k_head, v_head, o_head, lse, do_seq, dq_seq, dk_seq, dv_seq, ws,
+                        stream=None):
+    """The backward with every tile pair's dS stored and dQ read back from it
+    (phase-3 workspace)."""
+    _check("ulysses_attn_bwd_ds", lib().ulysses_attn_bwd_ds(
+        ctypes.byref(prob.c()), _ptr(q_head), _ptr(k_head), _ptr(v_head), _ptr(o_head), _ptr(lse),
+        _ptr(do_seq), _ptr(dq_seq), _ptr(dk_seq), _ptr(dv_seq), _ptr(ws), ws.numel() * ws.element_size(),
+        _stream(stream)))
+
+
+def ulysses_attn_bwd_dkdv_ds(prob, q_head, k_head, v_head, dk_seq, dv_seq, ws, stream=None):
+    """dS-store step 2: dK, dV, and every tile pair's dS into the workspace."""
+    _check("ulysses_attn_bwd_dkdv_ds", lib().ulysses_attn_bwd_dkdv_ds(
+        ctypes.byref(prob.c()), _ptr(q_head), _ptr(k_head), _ptr(v_head), _ptr(dk_seq), _ptr(dv_seq),
+        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def ulysses_attn_bwd_dq_ds(prob, k_head, dq_seq, ws, stream=None):
+    """dS-store step 3: dQ from the stored dS tiles and K, in sequence layout."""
+    _check("ulysses_attn_bwd_dq_ds", lib().ulysses_attn_bwd_dq_ds(
+        ctypes.byref(prob.c()), _ptr(k_head), _ptr(dq_seq), _ptr(ws), ws.numel() * ws.element_size(),
+        _stream(stream)))
+
+
 def ulysses_qkv_proj_pack(prob, x_seq, w_qkv, b_qkv, q_head, k_head, v_head, ws, stream=None):
     """QKV projection of the sequence-sharded activations with the pack and
     RoPE fused (b_qkv may be None)."""
@@ -335,7 +362,8 @@ class Buffers:
     intermediates, outputs and the workspace (allocated by torch, owned by
     the caller, as the C ABI requires)."""
 
-    def __init__(self, prob: Problem, device="cuda", backward: bool = False, fused: bool = False):
+    def __init__(self, prob: Problem, device="cuda", backward: bool = False, fused: bool = False,
+                 ds: bool = False):
         dt, p = prob.torch_dtype, prob
         D = p.head_dim
         e = lambda *s, d=dt: torch.empty(*s, dtype=d, device=device)
@@ -353,8 +381,10 @@ class Buffers:
             self.dq_seq = e(p.P, p.B, p.Sl, p.n_head, D)
             self.dk_seq = e(p.P, p.B, p.Sl, p.n_kv_head, D)
             self.dv_seq = e(p.P, p.B, p.Sl, p.n_kv_head, D)
-        # phase 2 (the fused backward's dQ accumulator too) when asked for
-        nbytes = ulysses_workspace_bytes(prob, (2 if fused else 1) if backward else 0)
+        # phase 2 (the fused backward's dQ accumulator) and phase 3 (the dS
+        # store) when asked for
+        phases = [1] + [2] * fused + [3] * ds if backward else [0]
+        nbytes = max(ulysses_workspace_bytes(prob, ph) for ph in phases)
         if nbytes == 0:
             raise UlyssesError("ulysses_workspace_bytes", ulysses_validate(prob))
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
@@ -375,3 +405,7 @@ class Buffers:
     def backward_fused(self, stream=None):
         ulysses_attn_bwd_fused(self.prob, self.q_head, self.k_head, self.v_head, self.o_head, self.lse,
                                self.do_seq, self.dq_seq, self.dk_seq, self.dv_seq, self.ws, stream)
+
+    def backward_ds(self, stream=None):
+        ulysses_attn_bwd_ds(self.prob, self.q_head, self.k_head, self.v_head, self.o_head, self.lse,
+                            self.do_seq, self.dq_seq, self.dk_seq, self.dv_seq, self.ws, stream)

@@ -76,6 +76,11 @@ struct BwdParams {
   // stores (range checks of a checked build): dQ, dK / dV (or their float
   // partials), Q / dO in head layout, the nlse / delta rows, the RoPE table.
   long long dq_n, dkv_n, qo_n, rows_n, rope_n;
+  // dS-store mode: the dK/dV kernel also writes every step's dS tile (bf16,
+  // [128 keys][128 queries]) to `ds` (null: not stored); `ds_pairs` tiles per
+  // q-head (see ds_tile).
+  __nv_bfloat16 *ds;
+  long long ds_pairs;
 };
 
 // Head-layout (rank * B + batch) of the rows at global position `pos` for the
@@ -97,6 +102,21 @@ __device__ __forceinline__ ActCoord act_coord(const BwdParams &p, int rb, int h,
   if (!p.folded) return {h, pos % p.Cs, hl_outer(p, rb, pos)};
   const int u = rb / p.B, b = rb - u * p.B;
   return {rep > 1 ? u / rep : u * heads_local + h, pos % p.Sl, (pos / p.Sl) * p.B + b};
+}
+
+// Tile index of (q-head hq, query tile m, key tile n) in the dS store: the
+// causal pairs n <= m of a head in query-tile order (m(m+1)/2 + n), or all
+// n_kt * n_kt pairs without the mask; a head's pairs are contiguous.  A tile
+// is 8 chunks of 16 queries, each chunk the 128 keys' 32-byte rows, the two
+// 8-query halves of a row swapped in every other group of 4 keys: element
+// (key k, query q) at (q / 16 * 128 + k) * 16 + ((q / 8 % 2) ^ (k / 4 % 2)) * 8
+// + q % 8.  Read back whole, that is the 32-byte-swizzled MN-major operand
+// layout, and the dK/dV kernel's lanes (one key each) write it with 32-byte
+// stores, 1 KB contiguous per warp.
+__device__ __forceinline__ long long ds_tile(const BwdParams &p, int hq, int m, int n) {
+  const int n_kt = (p.S + 127) / 128;
+  const long long t = p.causal ? (long long)m * (m + 1) / 2 + n : (long long)m * n_kt + n;
+  return (long long)hq * p.ds_pairs + t;
 }
 
 // Element offset of row `pos` of local q-head j of the CTA's (member, batch)
@@ -467,6 +487,12 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
     const float *rsn = rot ? p.rope_sin + (size_t)kvr * (D / 2) + g * 32 : nullptr;
     if (rot) rope_prefetch(rcs, rsn);
     bool ok = true;
+    // dS-store mode: the stored row is a copy that stays live until the next
+    // step's copy, so the next step's P and dS values go to other registers
+    // and never wait for a store that has not yet read its data.
+    uint32_t wc[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) wc[k] = 0u;
     for (int i = 0; i < n_iter; ++i) {
       const int qs = i % kQSlots, os = i % kOSlots;
       if (!warp_wait(bar + kKBarSFull, i & 1, abort_flag, gst)) { ok = false; break; }
@@ -530,6 +556,25 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
         break;
       }
       mbar_arrive(bar + kKBarDSFull);
+      if (p.ds) {
+        // dS-store mode: this row's 64 dS values (queries 64g..) into the tile of
+        // (q-head, query tile, key tile n), as four 16-query chunks (see ds_tile);
+        // streamed past L2
+        const int gi = i / n_m, j = kl * p.group + gi;
+        const long long e = ds_tile(p, rb * p.hp + j, m0 + i % n_m, n) * 16384 + (g * 4 * 128 + r) * 16;
+        if (in_range(p.status, e, 3 * 2048 + 16, p.ds_pairs * 16384LL * p.Pu * p.B * p.hp)) {
+          __nv_bfloat16 *dst = p.ds + e;
+          const bool sw = (r >> 2) & 1;  // the halves' swap: words 4..7 first
+#pragma unroll
+          for (int k = 0; k < 32; ++k) asm volatile("" ::"r"(wc[k]));  // the previous row lives until here
+#pragma unroll
+          for (int k = 0; k < 32; ++k) wc[k] = sw ? w[k >> 4][(k & 15) ^ 4] : w[k >> 4][k & 15];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            st_global_cs_v8(dst + u * 2048, wc[8 * u], wc[8 * u + 1], wc[8 * u + 2], wc[8 * u + 3], wc[8 * u + 4],
+                            wc[8 * u + 5], wc[8 * u + 6], wc[8 * u + 7]);
+        }
+      }
     }
     // ------------------------------------------------------------ epilogue
     RopeRow angles;
@@ -1558,14 +1603,182 @@ __global__ void __launch_bounds__(256) dq_finish_kernel(const float *__restrict_
   *reinterpret_cast<uint2 *>(p.dq + o + half) = make_uint2(w2, w3);
 }
 
+// ============================================== dQ from stored dS (dS-store mode)
+// The dK/dV kernel can also write every step's dS tile (bf16, [128 keys][128
+// queries], the values it feeds its dK MMA) to the workspace.  dQ is then a
+// plain sum of products over the stored tiles, dQ_m = sum_n dS_{m,n} K_n, and
+// the scores and dP need not be recomputed: five products per tile pair in all
+// (S^T, dP^T, dV, dK; dQ) instead of seven, deterministic, at the price of
+// writing and reading the dS tiles once (32 KB per pair).
+// One CTA per (q-head, 128-query tile m), longest first; a 3-stage ring of
+// (dS tile, K tile) pairs, the dS tile by one bulk copy (it is stored in the
+// 32-byte-swizzled MN-major operand layout) and K by TMA; dQ += dS K with A = dS
+// MN-major and B = K MN-major, accumulated in TMEM in key-tile order; the epilogue (one warpgroup, thread = query row) scales, undoes the
+// RoPE rotation and writes sequence layout, as the dQ kernel does.
+constexpr int kDSStages = 3;
+constexpr int kThreadsDS = 192;  // warps 0-3 epilogue, 4 TMA, 5 MMA
+constexpr int kDSTmaWarp = 4, kDSMmaWarp = 5;
+enum : uint32_t {
+  kDBarFull = 0,                          // [kDSStages]
+  kDBarEmpty = 8 * kDSStages,             // [kDSStages]
+  kDBarAcc = 16 * kDSStages,
+  kDBarDrain = kDBarAcc + 8,
+  kDTmemSlot = kDBarDrain + 8,
+  kDAbortSlot = kDTmemSlot + 4,
+  kDBarBytes = kDAbortSlot + 4
+};
+
+template <int D>
+struct DSLayout {
+  static constexpr uint32_t kDS = 128u * 128u * 2;  // one dS tile
+  static constexpr uint32_t kT = 128u * D * 2;      // one K tile
+  static constexpr uint32_t kStage = kDS + kT;
+  static constexpr uint32_t oBar = kDSStages * kStage;
+  static constexpr uint32_t kAlloc = oBar + 256 + 1024;
+  static_assert(kAlloc <= kMaxDynSmem, "dS-store dQ tiles exceed shared memory");
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsDS, 1)
+    dq_ds_kernel(const __grid_constant__ CUtensorMap tmK, const BwdParams p) {
+  using L = DSLayout<D>;
+  constexpr int kCh = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  uint8_t *smem = smem_raw + pad;
+  const uint32_t sb = raw + pad;
+  const uint32_t bar = sb + L::oBar;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::oBar + kDAbortSlot);
+  const volatile uint32_t *gst = p.status;
+  if ((*gst & 3u) || stale_rope_table(p)) return;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int heads_total = p.Pu * p.B * p.hp;
+  const int n_qt = (p.S + 127) / 128;
+  const dev::HeadTile ht = dev::grouped_order((int)blockIdx.x, heads_total, n_qt, p.group_q);
+  const int m = n_qt - 1 - ht.rank;  // longest tiles first
+  const int hq = ht.head;            // (member * B + batch) * hp + local q-head
+  const int j = hq % p.hp, rb = hq / p.hp;
+  const int kl = j / p.group;
+  const int n_kv = p.causal ? m + 1 : n_qt;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kDSStages; ++s) {
+      mbar_init(bar + kDBarFull + 8 * s, 1);
+      mbar_init(bar + kDBarEmpty + 8 * s, 1);
+    }
+    mbar_init(bar + kDBarAcc, 1);
+    mbar_init(bar + kDBarDrain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kDSMmaWarp) {
+    __syncwarp();
+    tmem_alloc(bar + kDTmemSlot, D < 32 ? 32 : D);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::oBar + kDTmemSlot);
+
+  if (warp == kDSTmaWarp) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      int issued = -1;
+      for (int n = 0; n < n_kv; ++n) {
+        const int s = n % kDSStages;
+        if (!mbar_wait_bounded(bar + kDBarEmpty + 8 * s, ((n / kDSStages) & 1) ^ 1, abort_flag, gst)) break;
+        const uint32_t full = bar + kDBarFull + 8 * s, st = sb + s * L::kStage;
+        mbar_arrive_expect_tx(full, L::kStage);
+        bulk_load(st, p.ds + ds_tile(p, hq, m, n) * 16384, L::kDS, full);
+        const ActCoord kc = act_coord(p, rb, kl, p.kvp, n * 128, p.kv_rep);
+        for (int c = 0; c < kCh; ++c)
+          tma_load_4d(st + L::kDS + c * 16384, &tmK, full, c * 64, kc.head, kc.row, kc.outer);
+        issued = n;
+      }
+      if (*abort_flag) {
+        volatile int never = 0;
+        for (int n = issued - (kDSStages - 1); n <= issued; ++n)
+          if (n >= 0)
+            mbar_wait_bounded(bar + kDBarFull + 8 * (n % kDSStages), (n / kDSStages) & 1, &never, nullptr,
+                              500000000ull);
+      }
+    }
+  } else if (warp == kDSMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idQ = idesc_bf16_f32(128, D, 1, 1);  // A (dS) and B (K) MN-major
+      bool ok = true;
+      for (int n = 0; ok && n < n_kv; ++n) {
+        const int s = n % kDSStages;
+        if (!(ok = mbar_wait_bounded(bar + kDBarFull + 8 * s, (n / kDSStages) & 1, abort_flag, gst))) break;
+        tc_fence_after_sync();
+        const uint32_t st = sb + s * L::kStage;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // keys 16kk..: two 8-row groups of 32-byte rows
+          mma_bf16_ss(tmem, smem_desc_sw32(st + kk * 512, 4096, 256),
+                      smem_desc_sw128(st + L::kDS + kk * 2048, 16384, 1024), idQ, (n > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar + kDBarEmpty + 8 * s);
+      }
+      mma_commit(bar + kDBarAcc);
+      mma_commit(bar + kDBarDrain);
+      volatile int never = 0;
+      mbar_wait_bounded(bar + kDBarDrain, 0, &never, nullptr);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------ epilogue: thread = query row
+    const int r = warp * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int qi = m * 128 + r;
+    const bool live = qi < p.S;
+    const bool rot = p.rope_cos && live && in_range(p.status, (long long)qi * (D / 2), D / 2, p.rope_n);
+    if (rot) rope_prefetch(p.rope_cos + (size_t)qi * (D / 2), p.rope_sin + (size_t)qi * (D / 2));
+    if (dev::warp_wait(bar + kDBarAcc, 0, abort_flag, gst)) {
+      tc_fence_after_sync();
+      const int s_rank = qi / p.Sl, t = qi - s_rank * p.Sl;
+      const int rr = rb / p.B, bb = rb - rr * p.B;
+      const size_t row = (((size_t)(s_rank * p.B + bb) * p.Sl + t) * p.n_head + (rr * p.hp + j)) * D;
+      const bool put = live && in_range(p.status, (long long)row, D, p.dq_n) &&
+                       (!p.rope_cos || in_range(p.status, (long long)qi * (D / 2), D / 2, p.rope_n));
+      // rotation pairs (i, i + D/2), 32 at a time
+#pragma unroll
+      for (int i0 = 0; i0 < D / 2; i0 += 32) {
+        RopeRow angles;
+        if (rot) rope_load(angles, p.rope_cos + (size_t)qi * (D / 2) + i0, p.rope_sin + (size_t)qi * (D / 2) + i0);
+        uint32_t x[32], y[32];
+        tmem_ld32(tmem + lane_base + i0, x);
+        tmem_ld32(tmem + lane_base + D / 2 + i0, y);
+        tmem_wait_ld();
+        if (put) store_unrotated(p.dq + row + i0, p.dq + row + D / 2 + i0, x, y, p.scale, rot, angles);
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kDSMmaWarp) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, D < 32 ? 32 : D);
+  }
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(p.status, (uint32_t)ULYSSES_STATUS_BWD_TIMEOUT);
+}
+
 // Which of the backward kernels a launch runs.
-enum BwdPart { kBwdDkDv = 1, kBwdDq = 2, kBwdFused = 4, kBwdFinish = 8 };
+enum BwdPart { kBwdDkDv = 1, kBwdDq = 2, kBwdFused = 4, kBwdFinish = 8, kBwdDqDS = 16 };
+
+// Causal (key tile, query tile) pairs of one head: n_kt (n_kt + 1) / 2.
+inline long long n_tiles_pairs(const ulysses_problem &p) {
+  const long long n = (p.S + 127) / 128;
+  return n * (n + 1) / 2;
+}
 
 template <int D>
 cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void *q, const void *k,
                      const void *v, const void *do_head, const float *nlse, const float *delta,
-                     const void *ws, void *dq, void *dk, void *dv, float *dqacc, uint32_t *status, int parts,
-                     bool folded, cudaStream_t st) {
+                     const void *ws, void *dq, void *dk, void *dv, float *dqacc, void *ds, uint32_t *status,
+                     int parts, bool folded, cudaStream_t st) {
   const int Pu = group_ranks(p), Cs = chunk_len(p), Sl = p.S / p.P;
   const int hp = p.n_head / Pu, kvp = kv_per_rank(p), PB = p.P * p.B;
   // head-layout maps [P*B][Cs][hp|kvp][D], or folded the sequence-sharded
@@ -1573,7 +1786,9 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   const int rows = folded ? Sl : Cs, qh = folded ? p.n_head : hp, kh = folded ? p.n_kv_head : kvp;
   if (folded && (ring_of(p) > 1 || Sl % 128 != 0)) return cudaErrorInvalidValue;
   CUtensorMap mK128, mV128, mL, mDl, mQ128, mdO128;
-  if (parts & (kBwdDkDv | kBwdDq | kBwdFused)) {  // the dQ finish step reads no tile
+  if ((parts & kBwdDqDS) && !(parts & (kBwdDkDv | kBwdDq | kBwdFused))) {  // dQ from the dS store reads K only
+    if (!make_act_map(enc, &mK128, k, D, kh, rows, PB, 128)) return cudaErrorInvalidValue;
+  } else if (parts & (kBwdDkDv | kBwdDq | kBwdFused)) {  // the dQ finish step reads no tile
     const bool ok = make_act_map(enc, &mK128, k, D, kh, rows, PB, 128) &&
                     make_act_map(enc, &mV128, v, D, kh, rows, PB, 128) &&
                     make_row_map(enc, &mL, nlse, Cs, delta_ld(p), PB * hp, 128) &&
@@ -1635,6 +1850,8 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   bp.dv = static_cast<__nv_bfloat16 *>(dv);
   bp.status = status;
   bp.rope_key = rope_key(p);
+  bp.ds = static_cast<__nv_bfloat16 *>(ds);
+  bp.ds_pairs = p.causal ? n_tiles_pairs(p) : (long long)((p.S + 127) / 128) * ((p.S + 127) / 128);
 
   const long long kv_blocks = n_t * UB * kvp;
   const long long q_blocks = n_t * UB * hp;
@@ -1652,6 +1869,14 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
     e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QLayout<D>::kAlloc);
     if (e != cudaSuccess) return e;
     dq_kernel<D><<<(unsigned)q_blocks, kThreadsQ, QLayout<D>::kAlloc, st>>>(mK128, mV128, bp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (parts & kBwdDqDS) {
+    if (!ds || (reinterpret_cast<uintptr_t>(ds) & 15)) return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(dq_ds_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DSLayout<D>::kAlloc);
+    if (e != cudaSuccess) return e;
+    dq_ds_kernel<D><<<(unsigned)q_blocks, kThreadsDS, DSLayout<D>::kAlloc, st>>>(mK128, bp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1690,12 +1915,12 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
 
 cudaError_t launch_parts(const ulysses_problem &p, const TmaEncoder &enc, const void *q, const void *k,
                          const void *v, const void *do_head, const float *nlse, const float *delta,
-                         const void *ws, void *dq, void *dk, void *dv, float *dqacc, uint32_t *status, int parts,
-                         bool folded, cudaStream_t st) {
+                         const void *ws, void *dq, void *dk, void *dv, float *dqacc, void *ds, uint32_t *status,
+                         int parts, bool folded, cudaStream_t st) {
   if (p.head_dim == 128)
-    return launch_d<128>(p, enc, q, k, v, do_head, nlse, delta, ws, dq, dk, dv, dqacc, status, parts, folded, st);
+    return launch_d<128>(p, enc, q, k, v, do_head, nlse, delta, ws, dq, dk, dv, dqacc, ds, status, parts, folded, st);
   if (p.head_dim == 64)
-    return launch_d<64>(p, enc, q, k, v, do_head, nlse, delta, ws, dq, dk, dv, dqacc, status, parts, folded, st);
+    return launch_d<64>(p, enc, q, k, v, do_head, nlse, delta, ws, dq, dk, dv, dqacc, ds, status, parts, folded, st);
   return cudaErrorInvalidValue;
 }
 
@@ -1704,31 +1929,38 @@ cudaError_t launch_parts(const ulysses_problem &p, const TmaEncoder &enc, const 
 cudaError_t launch_attn_bwd_dkdv(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
                                  const void *k, const void *v, const void *do_head, const float *nlse,
                                  const float *delta, const void *ws, void *dk_seq, void *dv_seq,
-                                 uint32_t *status, cudaStream_t st, bool folded) {
-  return launch_parts(p, enc, q, k, v, do_head, nlse, delta, ws, nullptr, dk_seq, dv_seq, nullptr, status, kBwdDkDv,
-                      folded, st);
+                                 uint32_t *status, cudaStream_t st, bool folded, void *ds) {
+  return launch_parts(p, enc, q, k, v, do_head, nlse, delta, ws, nullptr, dk_seq, dv_seq, nullptr, ds, status,
+                      kBwdDkDv, folded, st);
 }
 
 cudaError_t launch_attn_bwd_fused(const ulysses_problem &p, const TmaEncoder &enc, const void *q, const void *k,
                                   const void *v, const void *do_head, const float *nlse, const float *delta,
                                   const void *ws, float *dq_acc, void *dk_seq, void *dv_seq, uint32_t *status,
                                   cudaStream_t st, bool folded) {
-  return launch_parts(p, enc, q, k, v, do_head, nlse, delta, ws, nullptr, dk_seq, dv_seq, dq_acc, status, kBwdFused,
-                      folded, st);
+  return launch_parts(p, enc, q, k, v, do_head, nlse, delta, ws, nullptr, dk_seq, dv_seq, dq_acc, nullptr, status,
+                      kBwdFused, folded, st);
+}
+
+cudaError_t launch_dq_from_ds(const ulysses_problem &p, const TmaEncoder &enc, const void *k, const void *ws,
+                              const void *ds, void *dq_seq, uint32_t *status, cudaStream_t st) {
+  // the K map and the parameters are those of the packed (head-layout) backward
+  return launch_parts(p, enc, nullptr, k, nullptr, nullptr, nullptr, nullptr, ws, dq_seq, nullptr, nullptr, nullptr,
+                      const_cast<void *>(ds), status, kBwdDqDS, false, st);
 }
 
 cudaError_t launch_dq_finish(const ulysses_problem &p, const TmaEncoder &enc, const void *ws, float *dq_acc,
                              void *dq_seq, uint32_t *status, cudaStream_t st) {
   return launch_parts(p, enc, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, ws, dq_seq, nullptr, nullptr,
-                      dq_acc, status, kBwdFinish, false, st);
+                      dq_acc, nullptr, status, kBwdFinish, false, st);
 }
 
 cudaError_t launch_attn_bwd_dq(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
                                const void *k, const void *v, const void *do_head, const float *nlse,
                                const float *delta, const void *ws, void *dq_seq, uint32_t *status,
                                cudaStream_t st, bool folded) {
-  return launch_parts(p, enc, q, k, v, do_head, nlse, delta, ws, dq_seq, nullptr, nullptr, nullptr, status, kBwdDq,
-                      folded, st);
+  return launch_parts(p, enc, q, k, v, do_head, nlse, delta, ws, dq_seq, nullptr, nullptr, nullptr, nullptr, status,
+                      kBwdDq, folded, st);
 }
 
 }  // namespace ulysses

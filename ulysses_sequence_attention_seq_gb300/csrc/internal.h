@@ -25,6 +25,9 @@ struct WorkspaceLayout {
   // The fused backward's float dQ accumulator [B*n_head][Sp][D] (Sp = S rounded
   // up to 128), behind the phase-1 workspace (phase 2 only).
   size_t dqacc = 0, dqacc_bytes = 0, total_fused = 0;
+  // phase 3 (dS-store backward): every causal (or, unmasked, every) 128 x 128
+  // tile pair's bf16 dS, at the same offset as the fused mode's accumulator
+  size_t ds = 0, ds_bytes = 0, total_ds = 0;
 };
 WorkspaceLayout workspace_layout(const ulysses_problem &p);
 
@@ -115,11 +118,17 @@ cudaError_t launch_out_proj_unpack(const ulysses_problem &p, const TmaEncoder &e
 cudaError_t launch_attn_bwd_dkdv(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
                                  const void *k, const void *v, const void *do_head, const float *nlse,
                                  const float *delta, const void *ws, void *dk_seq, void *dv_seq,
-                                 uint32_t *status, cudaStream_t st, bool folded = false);
+                                 uint32_t *status, cudaStream_t st, bool folded = false, void *ds = nullptr);
 cudaError_t launch_attn_bwd_dq(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
                                const void *k, const void *v, const void *do_head, const float *nlse,
                                const float *delta, const void *ws, void *dq_seq, uint32_t *status,
                                cudaStream_t st, bool folded = false);
+// dS-store backward (attn_bwd_tc.cu): the dK/dV kernel above with `ds` set
+// also writes every step's bf16 dS tile there; this computes dQ = scale *
+// sum dS K from those tiles (no recomputation) and writes it in sequence
+// layout.  Head layout only (not folded).
+cudaError_t launch_dq_from_ds(const ulysses_problem &p, const TmaEncoder &enc, const void *k, const void *ws,
+                              const void *ds, void *dq_seq, uint32_t *status, cudaStream_t st);
 // The fused backward (attn_bwd_tc.cu): dK / dV as the dK/dV kernel writes
 // them, and every step's dQ share added into the float accumulator dq_acc
 // (which must hold zeros); then dq_finish scales, unrotates and writes dQ in

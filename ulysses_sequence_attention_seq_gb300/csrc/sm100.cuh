@@ -74,18 +74,23 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   uint64_t limit_ns = 2000000000ull) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (;;) {
+  for (uint32_t it = 1;; ++it) {
     // Sleeps until the phase completes (or ~1 us), so waiting warps do not
     // take issue slots from the warps doing the work.
     if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
     if (*abort_flag) return false;
-    if (gstatus && (*gstatus & 3u) != 0u) {  // a timeout bit of the status word
-      *abort_flag = 1;
-      return false;
-    }
-    if (globaltimer_ns() - t0 > limit_ns) {
-      *abort_flag = 1;
-      return false;
+    // The global status word every 8th round only: under heavy store
+    // traffic a global load takes microseconds, and a phase that completes
+    // meanwhile is seen only after it.
+    if ((it & 7u) == 0u) {
+      if (gstatus && (*gstatus & 3u) != 0u) {  // a timeout bit of the status word
+        *abort_flag = 1;
+        return false;
+      }
+      if (globaltimer_ns() - t0 > limit_ns) {
+        *abort_flag = 1;
+        return false;
+      }
     }
   }
 }
@@ -209,6 +214,29 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
   d |= (uint64_t)1 << 46;
   d |= (uint64_t)2 << 61;
   return d;
+}
+
+// Shared-memory matrix descriptor for a 32-byte-swizzled operand (layout
+// field 6): rows of 32 bytes whose two 16-byte halves trade places in every
+// other group of 4 rows (address bit 4 ^= bit 7).  MN-major: 16 MN-contiguous
+// elements per K row; `lbo` = distance between 16-element MN chunks, `sbo` =
+// distance between 8-row K groups.
+__device__ __forceinline__ uint64_t smem_desc_sw32(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)6 << 61;
+  return d;
+}
+
+// 32-byte streaming store (evict-first) of eight words.
+__device__ __forceinline__ void st_global_cs_v8(void *dst, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                uint32_t a4, uint32_t a5, uint32_t a6, uint32_t a7) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a0), "r"(a1),
+               "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+               : "memory");
 }
 
 // Instruction descriptor, kind::f16 with bf16 inputs and fp32 accumulator.

@@ -50,6 +50,10 @@ WorkspaceLayout workspace_layout(const ulysses_problem &p) {
   L.dqacc = L.total_bwd;
   L.dqacc_bytes = (size_t)p.B * p.n_head * ((p.S + 127) / 128 * 128) * p.head_dim * 4;
   L.total_fused = align256(L.dqacc + L.dqacc_bytes);
+  const size_t n_kt = (size_t)(p.S + 127) / 128;
+  L.ds = L.total_bwd;
+  L.ds_bytes = (size_t)p.B * p.n_head * (p.causal ? n_kt * (n_kt + 1) / 2 : n_kt * n_kt) * 128 * 128 * 2;
+  L.total_ds = align256(L.ds + L.ds_bytes);
   return L;
 }
 
@@ -124,7 +128,8 @@ int check_ws(const ulysses_problem &p, const void *ws, size_t ws_bytes, int phas
   if (!ws) return ULYSSES_ERR_WORKSPACE;
   if (!aligned16(ws)) return ULYSSES_ERR_ALIGN;
   const WorkspaceLayout L = workspace_layout(p);
-  if (ws_bytes < (phase == 2 ? L.total_fused : phase ? L.total_bwd : L.total_fwd)) return ULYSSES_ERR_WORKSPACE;
+  if (ws_bytes < (phase == 3 ? L.total_ds : phase == 2 ? L.total_fused : phase ? L.total_bwd : L.total_fwd))
+    return ULYSSES_ERR_WORKSPACE;
   return ULYSSES_OK;
 }
 
@@ -177,7 +182,7 @@ int ulysses_validate(const ulysses_problem *prob) {
 size_t ulysses_workspace_bytes(const ulysses_problem *prob, int phase) {
   if (ulysses_validate(prob) != ULYSSES_OK) return 0;
   const WorkspaceLayout L = workspace_layout(*prob);
-  return phase == 2 ? L.total_fused : phase ? L.total_bwd : L.total_fwd;
+  return phase == 3 ? L.total_ds : phase == 2 ? L.total_fused : phase ? L.total_bwd : L.total_fwd;
 }
 
 int ulysses_workspace_init(const ulysses_problem *prob, void *ws, size_t ws_bytes,
@@ -488,6 +493,71 @@ int ulysses_attn_bwd_fused(const ulysses_problem *prob, const void *q_head, cons
   if ((rc = ulysses_attn_bwd_prepare(prob, o_head, lse, do_seq, ws, ws_bytes, stream))) return rc;
   if ((rc = ulysses_attn_bwd_dkdvq(prob, q_head, k_head, v_head, dk_seq, dv_seq, ws, ws_bytes, stream))) return rc;
   return ulysses_attn_bwd_dq_finish(prob, dq_seq, ws, ws_bytes, stream);
+}
+
+int ulysses_attn_bwd_dkdv_ds(const ulysses_problem *prob, const void *q_head, const void *k_head,
+                             const void *v_head, void *dk_seq, void *dv_seq, void *ws, size_t ws_bytes,
+                             ulysses_stream_t stream) {
+  const NvtxRange range("ulysses_attn_bwd_dkdv_ds");
+  int rc = bwd_common(prob, ws, ws_bytes);
+  if (rc) return rc;
+  const ulysses_problem &p = *prob;
+  if ((rc = check_ws(p, ws, ws_bytes, 3))) return rc;
+  const size_t nq = act_bytes(p, p.n_head), nk = act_bytes(p, p.n_kv_head), nkh = kv_head_bytes(p);
+  const Span in[3] = {{q_head, nq}, {k_head, nkh}, {v_head, nkh}};
+  const Span out[3] = {{dk_seq, nk}, {dv_seq, nk}, {ws, ws_bytes}};
+  if ((rc = check_spans(in, 3, out, 3))) return rc;
+  TmaEncoder enc;
+  if (!get_tma_encoder(&enc)) return ULYSSES_ERR_CUDA;
+  const WorkspaceLayout L = workspace_layout(p);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t *status = reinterpret_cast<uint32_t *>(w + L.status);
+  const float *nlse = reinterpret_cast<const float *>(w + L.nlse), *delta = reinterpret_cast<const float *>(w + L.delta);
+  if (kv_replicas(p) > 1) {
+    float *dkp = reinterpret_cast<float *>(w + L.dkpart), *dvp = reinterpret_cast<float *>(w + L.dvpart);
+    cudaError_t e = launch_attn_bwd_dkdv(p, enc, q_head, k_head, v_head, w + L.dohead, nlse, delta, ws, dkp, dvp,
+                                         status, st, false, w + L.ds);
+    if (e == cudaSuccess) {
+      const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)p.head_dim);
+      e = launch_kv_reduce(p, dkp, dvp, dk_seq, dv_seq, scale, ws, st);
+    }
+    return cuda_rc(e);
+  }
+  return cuda_rc(launch_attn_bwd_dkdv(p, enc, q_head, k_head, v_head, w + L.dohead, nlse, delta, ws, dk_seq,
+                                      dv_seq, status, st, false, w + L.ds));
+}
+
+int ulysses_attn_bwd_dq_ds(const ulysses_problem *prob, const void *k_head, void *dq_seq, void *ws,
+                           size_t ws_bytes, ulysses_stream_t stream) {
+  const NvtxRange range("ulysses_attn_bwd_dq_ds");
+  int rc = bwd_common(prob, ws, ws_bytes);
+  if (rc) return rc;
+  const ulysses_problem &p = *prob;
+  if ((rc = check_ws(p, ws, ws_bytes, 3))) return rc;
+  const Span in[1] = {{k_head, kv_head_bytes(p)}};
+  const Span out[2] = {{dq_seq, act_bytes(p, p.n_head)}, {ws, ws_bytes}};
+  if ((rc = check_spans(in, 1, out, 2))) return rc;
+  TmaEncoder enc;
+  if (!get_tma_encoder(&enc)) return ULYSSES_ERR_CUDA;
+  const WorkspaceLayout L = workspace_layout(p);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  return cuda_rc(launch_dq_from_ds(p, enc, k_head, ws, w + L.ds, dq_seq, reinterpret_cast<uint32_t *>(w + L.status),
+                                   (cudaStream_t)stream));
+}
+
+int ulysses_attn_bwd_ds(const ulysses_problem *prob, const void *q_head, const void *k_head,
+                        const void *v_head, const void *o_head, const float *lse, const void *do_seq,
+                        void *dq_seq, void *dk_seq, void *dv_seq, void *ws, size_t ws_bytes,
+                        ulysses_stream_t stream) {
+  const NvtxRange range("ulysses_attn_bwd_ds");
+  int rc = check_bwd_call(prob, q_head, k_head, v_head, o_head, lse, do_seq, dq_seq, dk_seq, dv_seq, ws,
+                          ws_bytes);
+  if (rc) return rc;
+  if ((rc = check_ws(*prob, ws, ws_bytes, 3))) return rc;
+  if ((rc = ulysses_attn_bwd_prepare(prob, o_head, lse, do_seq, ws, ws_bytes, stream))) return rc;
+  if ((rc = ulysses_attn_bwd_dkdv_ds(prob, q_head, k_head, v_head, dk_seq, dv_seq, ws, ws_bytes, stream))) return rc;
+  return ulysses_attn_bwd_dq_ds(prob, k_head, dq_seq, ws, ws_bytes, stream);
 }
 
 int ulysses_attn_bwd(const ulysses_problem *prob, const void *q_head, const void *k_head,

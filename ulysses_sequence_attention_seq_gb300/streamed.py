@@ -22,7 +22,10 @@ its outputs, the download of that output from two steps back has finished.
 
 Orchestration only: every step is the same sequence of C-ABI calls as
 `binding.Buffers.forward` followed by the three calls that make up
-`ulysses_attn_bwd`; nothing here computes.
+`ulysses_attn_bwd` (bwd_mode "two_kernel"), `ulysses_attn_bwd_ds` (bwd_mode
+"ds_store": dK/dV storing dS, then dQ from the stored tiles, each set's
+workspace holding its tiles) or `ulysses_attn_bwd_fused` (bwd_mode "fused");
+nothing here computes.
 """
 from __future__ import annotations
 
@@ -45,10 +48,15 @@ class StreamedPath:
     IN_BWD = ("do_seq",)
     OUT_BWD = ("dq_seq", "dk_seq", "dv_seq")
 
-    def __init__(self, prob: U.Problem, backward: bool = False, device="cuda"):
-        self.prob, self.backward = prob, backward
+    BWD_MODES = ("two_kernel", "ds_store", "fused")
+
+    def __init__(self, prob: U.Problem, backward: bool = False, device="cuda", bwd_mode: str = "two_kernel"):
+        if bwd_mode not in self.BWD_MODES:
+            raise ValueError(f"bwd_mode must be one of {self.BWD_MODES}")
+        self.prob, self.backward, self.bwd_mode = prob, backward, bwd_mode
         self.dev = torch.device(device)
-        self.sets = [U.Buffers(prob, device=self.dev, backward=backward) for _ in range(2)]
+        self.sets = [U.Buffers(prob, device=self.dev, backward=backward, fused=backward and bwd_mode == "fused",
+                               ds=backward and bwd_mode == "ds_store") for _ in range(2)]
         for b in self.sets:
             U.ulysses_workspace_init(prob, b.ws)
         self.compute = torch.cuda.current_stream(self.dev)
@@ -118,10 +126,20 @@ class StreamedPath:
             U.ulysses_attn_bwd_prepare(p, b.o_head, b.lse, b.do_seq, b.ws, self.compute)
             ev["do_read"] = self._record(self.compute)
             self._wait(self.compute, ev["dkv_down"])
-            U.ulysses_attn_bwd_dkdv(p, b.q_head, b.k_head, b.v_head, b.dk_seq, b.dv_seq, b.ws, self.compute)
+            if self.bwd_mode == "ds_store":
+                U.ulysses_attn_bwd_dkdv_ds(p, b.q_head, b.k_head, b.v_head, b.dk_seq, b.dv_seq, b.ws, self.compute)
+            elif self.bwd_mode == "fused":
+                U.ulysses_attn_bwd_dkdvq(p, b.q_head, b.k_head, b.v_head, b.dk_seq, b.dv_seq, b.ws, self.compute)
+            else:
+                U.ulysses_attn_bwd_dkdv(p, b.q_head, b.k_head, b.v_head, b.dk_seq, b.dv_seq, b.ws, self.compute)
             dkv_ready = self._record(self.compute)
             self._wait(self.compute, ev["dq_down"])
-            U.ulysses_attn_bwd_dq(p, b.q_head, b.k_head, b.v_head, b.dq_seq, b.ws, self.compute)
+            if self.bwd_mode == "ds_store":
+                U.ulysses_attn_bwd_dq_ds(p, b.k_head, b.dq_seq, b.ws, self.compute)
+            elif self.bwd_mode == "fused":
+                U.ulysses_attn_bwd_dq_finish(p, b.dq_seq, b.ws, self.compute)
+            else:
+                U.ulysses_attn_bwd_dq(p, b.q_head, b.k_head, b.v_head, b.dq_seq, b.ws, self.compute)
             dq_ready = self._record(self.compute)
             self.down.wait_event(dkv_ready)
             with torch.cuda.stream(self.down):
