@@ -1,7 +1,7 @@
 """The range-checked build (-DULYSSES_CHECK_BOUNDS: every plain global load
 and store checked against its buffer) runs the whole path without a single
 failed check and gives bit for bit what the normal build gives: forward,
-backward, the workspace-free backward, the fp32 forward, replicated kv-heads,
+backward (two-kernel and dS-store), the workspace-free backward, the fp32 forward, replicated kv-heads,
 the ring hybrid, the folded forward and backward and the two projections.  The checked library runs in a
 child process (ULYSSES_LIB)."""
 import os
@@ -33,7 +33,7 @@ cases = [wl(2, 1, 424, 4, 2, 128).with_(backward=True),
          wl(2, 1, 256, 4, 4, 32, "fp32", causal=False, rope=False)]
 out = {}
 for n, w in enumerate(cases):
-    run = GpuRun(w, backward=w.backward)
+    run = GpuRun(w, backward=w.backward, ds=w.backward)
     run.forward()
     names = ["o_seq", "lse"]
     if w.backward:
@@ -42,6 +42,11 @@ for n, w in enumerate(cases):
     for name in names:
         out[f"{n}/{name}"] = getattr(run.buf, name).cpu()
     out[f"{n}/status"] = torch.tensor(U.ulysses_read_status(run.buf.ws))
+    if w.backward:  # the dS-store backward on the same buffers (its tile store written and read back)
+        run.buf.backward_ds()
+        for name in ("dq_seq", "dk_seq", "dv_seq"):
+            out[f"{n}/ds/{name}"] = getattr(run.buf, name).cpu()
+        out[f"{n}/ds/status"] = torch.tensor(U.ulysses_read_status(run.buf.ws))
     if n == 0:  # the workspace-free backward on the same buffers
         b = run.buf
         grads = [torch.empty_like(getattr(b, g)) for g in ("dq_seq", "dk_seq", "dv_seq")]

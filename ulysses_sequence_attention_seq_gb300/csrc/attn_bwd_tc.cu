@@ -104,6 +104,15 @@ __device__ __forceinline__ ActCoord act_coord(const BwdParams &p, int rb, int h,
   return {rep > 1 ? u / rep : u * heads_local + h, pos % p.Sl, (pos / p.Sl) * p.B + b};
 }
 
+// One key row's 64 dS values of a warpgroup's half tile (see ds_tile): four
+// 32-byte streaming stores, 2048 elements apart; read by another kernel.
+__device__ __forceinline__ void store_ds_row(__nv_bfloat16 *dst, const uint32_t (&x)[32]) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    st_global_cs_v8(dst + u * 2048, x[8 * u], x[8 * u + 1], x[8 * u + 2], x[8 * u + 3], x[8 * u + 4], x[8 * u + 5],
+                    x[8 * u + 6], x[8 * u + 7]);
+}
+
 // Tile index of (q-head hq, query tile m, key tile n) in the dS store: the
 // causal pairs n <= m of a head in query-tile order (m(m+1)/2 + n), or all
 // n_kt * n_kt pairs without the mask; a head's pairs are contiguous.  A tile
@@ -487,12 +496,6 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
     const float *rsn = rot ? p.rope_sin + (size_t)kvr * (D / 2) + g * 32 : nullptr;
     if (rot) rope_prefetch(rcs, rsn);
     bool ok = true;
-    // dS-store mode: the stored row is a copy that stays live until the next
-    // step's copy, so the next step's P and dS values go to other registers
-    // and never wait for a store that has not yet read its data.
-    uint32_t wc[32];
-#pragma unroll
-    for (int k = 0; k < 32; ++k) wc[k] = 0u;
     for (int i = 0; i < n_iter; ++i) {
       const int qs = i % kQSlots, os = i % kOSlots;
       if (!warp_wait(bar + kKBarSFull, i & 1, abort_flag, gst)) { ok = false; break; }
@@ -559,20 +562,16 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
       if (p.ds) {
         // dS-store mode: this row's 64 dS values (queries 64g..) into the tile of
         // (q-head, query tile, key tile n), as four 16-query chunks (see ds_tile);
-        // streamed past L2
+        // issued after the arrival that releases dK(i), they drain while these
+        // threads wait for the next scores
         const int gi = i / n_m, j = kl * p.group + gi;
         const long long e = ds_tile(p, rb * p.hp + j, m0 + i % n_m, n) * 16384 + (g * 4 * 128 + r) * 16;
         if (in_range(p.status, e, 3 * 2048 + 16, p.ds_pairs * 16384LL * p.Pu * p.B * p.hp)) {
-          __nv_bfloat16 *dst = p.ds + e;
           const bool sw = (r >> 2) & 1;  // the halves' swap: words 4..7 first
+          uint32_t x[32];
 #pragma unroll
-          for (int k = 0; k < 32; ++k) asm volatile("" ::"r"(wc[k]));  // the previous row lives until here
-#pragma unroll
-          for (int k = 0; k < 32; ++k) wc[k] = sw ? w[k >> 4][(k & 15) ^ 4] : w[k >> 4][k & 15];
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            st_global_cs_v8(dst + u * 2048, wc[8 * u], wc[8 * u + 1], wc[8 * u + 2], wc[8 * u + 3], wc[8 * u + 4],
-                            wc[8 * u + 5], wc[8 * u + 6], wc[8 * u + 7]);
+          for (int k = 0; k < 32; ++k) x[k] = sw ? w[k >> 4][(k & 15) ^ 4] : w[k >> 4][k & 15];
+          store_ds_row(p.ds + e, x);
         }
       }
     }
@@ -1691,8 +1690,13 @@ __global__ void __launch_bounds__(kThreadsDS, 1)
         const int s = n % kDSStages;
         if (!mbar_wait_bounded(bar + kDBarEmpty + 8 * s, ((n / kDSStages) & 1) ^ 1, abort_flag, gst)) break;
         const uint32_t full = bar + kDBarFull + 8 * s, st = sb + s * L::kStage;
+        const long long e = ds_tile(p, hq, m, n) * 16384;
+        if (!in_range(p.status, e, 16384, p.ds_pairs * 16384LL * p.Pu * p.B * p.hp)) {  // checked build only
+          *abort_flag = 1;
+          break;
+        }
         mbar_arrive_expect_tx(full, L::kStage);
-        bulk_load(st, p.ds + ds_tile(p, hq, m, n) * 16384, L::kDS, full);
+        bulk_load(st, p.ds + e, L::kDS, full);
         const ActCoord kc = act_coord(p, rb, kl, p.kvp, n * 128, p.kv_rep);
         for (int c = 0; c < kCh; ++c)
           tma_load_4d(st + L::kDS + c * 16384, &tmK, full, c * 64, kc.head, kc.row, kc.outer);
