@@ -106,3 +106,32 @@ def test_ds_backward_workloads(name):
     want_dq = np.concatenate(list(want["dq_seq"]), axis=1)
     for b in sorted({g[1] for g in groups}):
         assert_close(got[b][rows][:, heads], want_dq[b][rows][:, heads], w, f"dS-store dq_seq batch {b}")
+
+
+TINY = [wl(2, 1, 96, 2, 2, 64),                    # one ragged 128-row tile
+        wl(2, 1, 2, 4, 2, 128),                    # one token per rank
+        wl(4, 1, 40, 4, 1, 64, causal=False),      # unmasked, replicated kv-head
+        wl(1, 1, 129, 2, 1, 128)]                  # a full tile and one row
+
+
+@pytest.mark.parametrize("w", TINY, ids=_ids)
+def test_tiny_sequences_every_backward_mode(w):
+    """Degenerate lengths (fewer rows than a tile, one token per rank, a tile
+    and one row): the two-kernel, dS-store and fused backwards against the
+    oracle, dK and dV identical across the three."""
+    w = w.with_(backward=True)
+    run = GpuRun(w, backward=True, ds=True, fused=True)
+    run.forward()
+    x = oracle_inputs(run.inputs)
+    want = oracle.backward(oracle_problem(w), x["q"], x["k"], x["v"], x["do"])
+    ref = None
+    for name, call in (("two-kernel", run.backward), ("dS-store", run.backward_ds), ("fused", run.backward_fused)):
+        for n in GRADS:
+            getattr(run.buf, n).fill_(float("nan"))
+        call()
+        for n in GRADS:
+            assert_close(to64(getattr(run.buf, n)), np.stack(want[n]), w, f"{name} {n}")
+        if ref is None:
+            ref = {n: getattr(run.buf, n).clone() for n in ("dk_seq", "dv_seq")}
+        else:
+            assert all(torch.equal(getattr(run.buf, n), ref[n]) for n in ref), f"{name} dK/dV differ"
