@@ -1603,17 +1603,19 @@ __global__ void __launch_bounds__(256) dq_finish_kernel(const float *__restrict_
 }
 
 // ============================================== dQ from stored dS (dS-store mode)
-// The dK/dV kernel can also write every step's dS tile (bf16, [128 keys][128
-// queries], the values it feeds its dK MMA) to the workspace.  dQ is then a
-// plain sum of products over the stored tiles, dQ_m = sum_n dS_{m,n} K_n, and
-// the scores and dP need not be recomputed: five products per tile pair in all
-// (S^T, dP^T, dV, dK; dQ) instead of seven, deterministic, at the price of
-// writing and reading the dS tiles once (32 KB per pair).
+// The dK/dV kernel can also write every step's dS tile (bf16, 128 keys x 128
+// queries, the values it feeds its dK MMA, in the layout described at
+// ds_tile) to the workspace.  dQ is then a plain sum of products over the
+// stored tiles, dQ_m = sum_n dS_{m,n} K_n, and the scores and dP need not be
+// recomputed: five products per tile pair in all (S^T, dP^T, dV, dK; dQ)
+// instead of seven, deterministic, at the price of writing and reading the dS
+// tiles once (32 KB per pair).
 // One CTA per (q-head, 128-query tile m), longest first; a 3-stage ring of
-// (dS tile, K tile) pairs, the dS tile by one bulk copy (it is stored in the
-// 32-byte-swizzled MN-major operand layout) and K by TMA; dQ += dS K with A = dS
-// MN-major and B = K MN-major, accumulated in TMEM in key-tile order; the epilogue (one warpgroup, thread = query row) scales, undoes the
-// RoPE rotation and writes sequence layout, as the dQ kernel does.
+// (dS tile, K tile) pairs, the dS tile by one bulk copy (stored as the
+// 32-byte-swizzled MN-major operand) and K by TMA; dQ += dS K with A = dS and
+// B = K both MN-major, accumulated in TMEM in key-tile order; the epilogue
+// (one warpgroup, thread = query row) scales, undoes the RoPE rotation and
+// writes sequence layout, as the dQ kernel does.
 constexpr int kDSStages = 3;
 constexpr int kThreadsDS = 192;  // warps 0-3 epilogue, 4 TMA, 5 MMA
 constexpr int kDSTmaWarp = 4, kDSMmaWarp = 5;
