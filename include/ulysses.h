@@ -126,7 +126,8 @@ int ulysses_validate(const ulysses_problem *prob);
  * call), 3 = the dS-store backward (ulysses_attn_bwd_ds; the phase-1
  * workspace followed by B*n_head*T tiles of 128*128 bf16, T = n(n+1)/2 causal
  * or n*n unmasked, n = ceil(S/128); valid for every call but the fused
- * backward's when smaller than phase 2).  Returns 0 for an invalid problem.
+ * backward's when smaller than phase 2).  Returns 0 for an invalid problem or
+ * a phase outside 0..3.
  * Host only; needs no GPU. */
 size_t ulysses_workspace_bytes(const ulysses_problem *prob, int phase);
 

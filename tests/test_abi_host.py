@@ -82,6 +82,7 @@ def test_workspace_sizes(lib):
     pr = prob(n_kv_head=2)
     assert U.ulysses_workspace_bytes(pr, 1) >= b + 2 * pr.P * pr.B * pr.S * pr.head_dim * 4
     assert U.ulysses_workspace_bytes(prob(B=0), 0) == 0
+    assert U.ulysses_workspace_bytes(p, 4) == 0 and U.ulysses_workspace_bytes(p, -1) == 0
     # the hybrid regroups the same rows: the same workspace
     assert U.ulysses_workspace_bytes(prob(ring=2), 1) == b
     # S = 4098 over P = 2: the delta and base-2 LSE rows (one per batch and

@@ -180,7 +180,7 @@ int ulysses_validate(const ulysses_problem *prob) {
 }
 
 size_t ulysses_workspace_bytes(const ulysses_problem *prob, int phase) {
-  if (ulysses_validate(prob) != ULYSSES_OK) return 0;
+  if (phase < 0 || phase > 3 || ulysses_validate(prob) != ULYSSES_OK) return 0;
   const WorkspaceLayout L = workspace_layout(*prob);
   return phase == 3 ? L.total_ds : phase == 2 ? L.total_fused : phase ? L.total_bwd : L.total_fwd;
 }
