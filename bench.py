@@ -838,11 +838,14 @@ def main():
                      "peak_source": f"{peak_src} bf16 sustained", "kernel": dk["kernel"],
                      "peak_burst": tf_burst, "frac_burst": dk["achieved_tflops"] / tf_burst,
                      "sm_mhz": r["clocks"].get("sm_mhz"), "bwd_mode": r["bwd_mode"],
+                     # DRAM rate of the same launch (traffic from the ncu capture over this run's time)
+                     "dram_gbs": (TRAFFIC[(dominant, w.name)] / (dk["ms"] * 1e-3) / 1e9
+                                  if (dominant, w.name) in TRAFFIC else None),
                      "note": "dominant kernel by time; achieved counts its algorithmic products only; frac is "
                              "against the sustained (power-capped) cuBLAS figure, frac_burst against the burst "
                              "one; sm_mhz is the median SM clock sampled while the timed steps ran"
-                             + ("; in the dS-store backward the dK/dV kernel also writes every tile pair's dS"
-                                if dominant == "bwd_dkdv_ds" else "")},
+                             + ("; in the dS-store backward the dK/dV kernel also writes every tile pair's dS "
+                                "(dram_gbs: its DRAM traffic over its time)" if dominant == "bwd_dkdv_ds" else "")},
         "secondary_rooflines": {**{k: {"bound": "tensor", "achieved": v["achieved_tflops"], "peak": tf_sust,
                                        "unit": "TFLOP/s", "frac": v["frac"], "traffic": TRAFFIC.get((k, w.name))}
                                    for k, v in kernels.items() if k != dominant},
