@@ -99,8 +99,9 @@ def test_fused_backward_workloads(name):
     want = oracle.backward(op, x["q"], x["k"], x["v"], x["do"], groups=groups, q_rows=rows, kv_rows=[rows[0]])
     hp = w.n_head // w.P
     G = hp // op.kvp
-    heads = [r * hp + kl * G + gi for (r, _, kl) in groups for gi in range(G)]
     got = np.concatenate(list(to64(run.buf.dq_seq)), axis=1)      # [B][S][n_head][D] global
     want_dq = np.concatenate(list(want["dq_seq"]), axis=1)
     for b in sorted({g[1] for g in groups}):
+        # the q-heads of the groups of batch b (the oracle computed no others)
+        heads = [r * hp + kl * G + gi for (r, bb, kl) in groups if bb == b for gi in range(G)]
         assert_close(got[b][rows][:, heads], want_dq[b][rows][:, heads], w, f"fused dq_seq batch {b}")
