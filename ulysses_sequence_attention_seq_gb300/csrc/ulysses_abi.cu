@@ -145,6 +145,54 @@ size_t kv_head_bytes(const ulysses_problem &p) {
   return (size_t)p.P * p.B * chunk_len(p) * kv_per_rank(p) * p.head_dim * elem_size(p);
 }
 
+
+// Shared checks of the backward entry points: a bf16 problem with a tensor-core
+// kernel, a phase-1 workspace.
+int bwd_common(const ulysses_problem *prob, const void *ws, size_t ws_bytes) {
+  int rc = ulysses_validate(prob);
+  if (rc) return rc;
+  const ulysses_problem &p = *prob;
+  if (p.dtype != ULYSSES_BF16 || (p.head_dim != 64 && p.head_dim != 128)) return ULYSSES_ERR_UNSUPPORTED;
+  return check_ws(p, ws, ws_bytes, 1);
+}
+
+// Step 2 of the backward, with or without the dS store (phase-3 workspace):
+// dK, dV (with replicated kv-heads, each rank's float partials and then
+// their sum) in sequence layout.
+int dkdv_call(const ulysses_problem *prob, const void *q_head, const void *k_head, const void *v_head,
+              void *dk_seq, void *dv_seq, void *ws, size_t ws_bytes, ulysses_stream_t stream, bool store_ds) {
+  int rc = bwd_common(prob, ws, ws_bytes);
+  if (rc) return rc;
+  const ulysses_problem &p = *prob;
+  if (store_ds && (rc = check_ws(p, ws, ws_bytes, 3))) return rc;
+  const size_t nk = act_bytes(p, p.n_kv_head), nkh = kv_head_bytes(p);
+  const Span in[3] = {{q_head, act_bytes(p, p.n_head)}, {k_head, nkh}, {v_head, nkh}};
+  const Span out[3] = {{dk_seq, nk}, {dv_seq, nk}, {ws, ws_bytes}};
+  if ((rc = check_spans(in, 3, out, 3))) return rc;
+  TmaEncoder enc;
+  if (!get_tma_encoder(&enc)) return ULYSSES_ERR_CUDA;
+  const WorkspaceLayout L = workspace_layout(p);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t *status = reinterpret_cast<uint32_t *>(w + L.status);
+  const float *nlse = reinterpret_cast<const float *>(w + L.nlse), *delta = reinterpret_cast<const float *>(w + L.delta);
+  void *ds = store_ds ? static_cast<void *>(w + L.ds) : nullptr;
+  if (kv_replicas(p) > 1) {
+    // each rank's partial dK, dV (its own q-heads) into the workspace, then the
+    // sum over every kv-head's replicas into sequence layout
+    float *dkp = reinterpret_cast<float *>(w + L.dkpart), *dvp = reinterpret_cast<float *>(w + L.dvpart);
+    cudaError_t e = launch_attn_bwd_dkdv(p, enc, q_head, k_head, v_head, w + L.dohead, nlse, delta, ws, dkp, dvp,
+                                         status, st, false, ds);
+    if (e == cudaSuccess) {
+      const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)p.head_dim);
+      e = launch_kv_reduce(p, dkp, dvp, dk_seq, dv_seq, scale, ws, st);
+    }
+    return cuda_rc(e);
+  }
+  return cuda_rc(launch_attn_bwd_dkdv(p, enc, q_head, k_head, v_head, w + L.dohead, nlse, delta, ws, dk_seq, dv_seq,
+                                      status, st, false, ds));
+}
+
 }  // namespace
 
 extern "C" {
@@ -327,16 +375,6 @@ int ulysses_unpack_out(const ulysses_problem *prob, const void *o_head, void *o_
   return cuda_rc(launch_unpack(p, o_head, o_seq, (cudaStream_t)stream));
 }
 
-// Shared checks of the backward entry points: a bf16 problem with a tensor-core
-// kernel, a phase-1 workspace.
-static int bwd_common(const ulysses_problem *prob, const void *ws, size_t ws_bytes) {
-  int rc = ulysses_validate(prob);
-  if (rc) return rc;
-  const ulysses_problem &p = *prob;
-  if (p.dtype != ULYSSES_BF16 || (p.head_dim != 64 && p.head_dim != 128)) return ULYSSES_ERR_UNSUPPORTED;
-  return check_ws(p, ws, ws_bytes, 1);
-}
-
 int ulysses_attn_bwd_prepare(const ulysses_problem *prob, const void *o_head, const float *lse,
                              const void *do_seq, void *ws, size_t ws_bytes, ulysses_stream_t stream) {
   const NvtxRange range("ulysses_attn_bwd_prepare");
@@ -359,36 +397,7 @@ int ulysses_attn_bwd_dkdv(const ulysses_problem *prob, const void *q_head, const
                           const void *v_head, void *dk_seq, void *dv_seq, void *ws, size_t ws_bytes,
                           ulysses_stream_t stream) {
   const NvtxRange range("ulysses_attn_bwd_dkdv");
-  int rc = bwd_common(prob, ws, ws_bytes);
-  if (rc) return rc;
-  const ulysses_problem &p = *prob;
-  const size_t nq = act_bytes(p, p.n_head), nk = act_bytes(p, p.n_kv_head), nkh = kv_head_bytes(p);
-  const Span in[3] = {{q_head, nq}, {k_head, nkh}, {v_head, nkh}};
-  const Span out[3] = {{dk_seq, nk}, {dv_seq, nk}, {ws, ws_bytes}};
-  if ((rc = check_spans(in, 3, out, 3))) return rc;
-  TmaEncoder enc;
-  if (!get_tma_encoder(&enc)) return ULYSSES_ERR_CUDA;
-  const WorkspaceLayout L = workspace_layout(p);
-  uint8_t *w = static_cast<uint8_t *>(ws);
-  cudaStream_t st = (cudaStream_t)stream;
-  if (kv_replicas(p) > 1) {
-    // each rank's partial dK, dV (its own q-heads) into the workspace, then the
-    // sum over every kv-head's replicas into sequence layout
-    float *dkp = reinterpret_cast<float *>(w + L.dkpart), *dvp = reinterpret_cast<float *>(w + L.dvpart);
-    cudaError_t e = launch_attn_bwd_dkdv(p, enc, q_head, k_head, v_head, w + L.dohead,
-                                         reinterpret_cast<const float *>(w + L.nlse),
-                                         reinterpret_cast<const float *>(w + L.delta), ws, dkp, dvp,
-                                         reinterpret_cast<uint32_t *>(w + L.status), st);
-    if (e == cudaSuccess) {
-      const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)p.head_dim);
-      e = launch_kv_reduce(p, dkp, dvp, dk_seq, dv_seq, scale, ws, st);
-    }
-    return cuda_rc(e);
-  }
-  return cuda_rc(launch_attn_bwd_dkdv(p, enc, q_head, k_head, v_head, w + L.dohead,
-                                      reinterpret_cast<const float *>(w + L.nlse),
-                                      reinterpret_cast<const float *>(w + L.delta), ws, dk_seq, dv_seq,
-                                      reinterpret_cast<uint32_t *>(w + L.status), st));
+  return dkdv_call(prob, q_head, k_head, v_head, dk_seq, dv_seq, ws, ws_bytes, stream, false);
 }
 
 int ulysses_attn_bwd_dq(const ulysses_problem *prob, const void *q_head, const void *k_head,
@@ -499,33 +508,7 @@ int ulysses_attn_bwd_dkdv_ds(const ulysses_problem *prob, const void *q_head, co
                              const void *v_head, void *dk_seq, void *dv_seq, void *ws, size_t ws_bytes,
                              ulysses_stream_t stream) {
   const NvtxRange range("ulysses_attn_bwd_dkdv_ds");
-  int rc = bwd_common(prob, ws, ws_bytes);
-  if (rc) return rc;
-  const ulysses_problem &p = *prob;
-  if ((rc = check_ws(p, ws, ws_bytes, 3))) return rc;
-  const size_t nq = act_bytes(p, p.n_head), nk = act_bytes(p, p.n_kv_head), nkh = kv_head_bytes(p);
-  const Span in[3] = {{q_head, nq}, {k_head, nkh}, {v_head, nkh}};
-  const Span out[3] = {{dk_seq, nk}, {dv_seq, nk}, {ws, ws_bytes}};
-  if ((rc = check_spans(in, 3, out, 3))) return rc;
-  TmaEncoder enc;
-  if (!get_tma_encoder(&enc)) return ULYSSES_ERR_CUDA;
-  const WorkspaceLayout L = workspace_layout(p);
-  uint8_t *w = static_cast<uint8_t *>(ws);
-  cudaStream_t st = (cudaStream_t)stream;
-  uint32_t *status = reinterpret_cast<uint32_t *>(w + L.status);
-  const float *nlse = reinterpret_cast<const float *>(w + L.nlse), *delta = reinterpret_cast<const float *>(w + L.delta);
-  if (kv_replicas(p) > 1) {
-    float *dkp = reinterpret_cast<float *>(w + L.dkpart), *dvp = reinterpret_cast<float *>(w + L.dvpart);
-    cudaError_t e = launch_attn_bwd_dkdv(p, enc, q_head, k_head, v_head, w + L.dohead, nlse, delta, ws, dkp, dvp,
-                                         status, st, false, w + L.ds);
-    if (e == cudaSuccess) {
-      const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)p.head_dim);
-      e = launch_kv_reduce(p, dkp, dvp, dk_seq, dv_seq, scale, ws, st);
-    }
-    return cuda_rc(e);
-  }
-  return cuda_rc(launch_attn_bwd_dkdv(p, enc, q_head, k_head, v_head, w + L.dohead, nlse, delta, ws, dk_seq,
-                                      dv_seq, status, st, false, w + L.ds));
+  return dkdv_call(prob, q_head, k_head, v_head, dk_seq, dv_seq, ws, ws_bytes, stream, true);
 }
 
 int ulysses_attn_bwd_dq_ds(const ulysses_problem *prob, const void *k_head, void *dq_seq, void *ws,
