@@ -137,3 +137,18 @@ def test_reference_arm_times_both_passes_with_the_gpu_arms_config(monkeypatch, c
     assert all(gpu["config"][k] == ref["config"][k] for k in gpu["config"] if k not in ("l2", "parallelism"))
     r = gpu["roofline"]
     assert abs(r["frac_burst"] - r["achieved"] / r["peak_burst"]) < 1e-12 and r["sm_mhz"] == 2040.0
+
+
+def test_ds_store_byte_counts():
+    """The dS store holds one tile per causal (key tile, query tile) pair of
+    every (batch, q-head), or every pair without the mask; the dQ step's
+    algorithmic bytes are those tiles, K and dQ once each."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from ulysses_sequence_attention_seq_gb300.synthetic import WORKLOADS
+    c3 = WORKLOADS["C3"]                                   # S = 8192: 64 tiles
+    assert bench.ds_tiles(c3) == 64 * 65 // 2
+    assert bench.ds_tiles(c3.with_(causal=False)) == 64 * 64
+    assert bench.ds_tiles(c3.with_(S=8193)) == 65 * 66 // 2
+    nb = bench.dq_ds_bytes(c3, 2)
+    assert nb == c3.B * c3.n_head * (64 * 65 // 2) * 32768 + c3.B * c3.S * (c3.n_kv_head + c3.n_head) * 128 * 2
