@@ -126,8 +126,11 @@ int ulysses_validate(const ulysses_problem *prob);
  * call), 3 = the dS-store backward (ulysses_attn_bwd_ds; the phase-1
  * workspace followed by B*n_head*T tiles of 128*128 bf16, T = n(n+1)/2 causal
  * or n*n unmasked, n = ceil(S/128); valid for every call but the fused
- * backward's when smaller than phase 2).  Returns 0 for an invalid problem or
- * a phase outside 0..3.
+ * backward's when smaller than phase 2), 4 = the least workspace the
+ * dS-store backward takes (the phase-1 workspace followed by the tiles of one
+ * kv-head's q-heads on one rank; ulysses_attn_bwd_ds then runs the kv-heads in
+ * chunks, as many at a time as the workspace holds).  Returns 0 for an invalid
+ * problem or a phase outside 0..4.
  * Host only; needs no GPU. */
 size_t ulysses_workspace_bytes(const ulysses_problem *prob, int phase);
 
@@ -345,12 +348,16 @@ int ulysses_attn_bwd_dq_finish(const ulysses_problem *prob, void *dq_seq, void *
  * dK and dV are bit-identical to ulysses_attn_bwd's; dQ is the sum of the
  * same bf16 dS values the dK product uses (within the stated tolerance of
  * ulysses_attn_bwd's).  Same arguments, layouts and results as
- * ulysses_attn_bwd; `ws` must be sized for phase 3 and prepared by
- * ulysses_workspace_init.  bf16, head_dim 64 or 128; the errors of
+ * ulysses_attn_bwd; `ws` must be sized for at least phase 4 and prepared by
+ * ulysses_workspace_init.  With less than phase 3 the kv-heads are processed
+ * in chunks (each: the dK/dV step storing its q-heads' tiles, then their dQ),
+ * as many kv-heads at a time as the workspace holds tiles for; the results
+ * are the same bits either way.  bf16, head_dim 64 or 128; the errors of
  * ulysses_attn_bwd, and ULYSSES_ERR_WORKSPACE for a workspace smaller than
- * phase 3.
+ * phase 4.
  *
- * Its steps: ulysses_attn_bwd_prepare (above), then ulysses_attn_bwd_dkdv_ds
+ * Its steps, with a phase-3 workspace (all the tiles at once):
+ * ulysses_attn_bwd_prepare (above), then ulysses_attn_bwd_dkdv_ds
  * (dK, dV into dk_seq / dv_seq as ulysses_attn_bwd_dkdv writes them, and the
  * dS tiles into the workspace), then ulysses_attn_bwd_dq_ds (dQ from the
  * tiles and k_head: scaled, RoPE rotation undone, rounded to bf16 into dq_seq

@@ -82,7 +82,7 @@ def test_workspace_sizes(lib):
     pr = prob(n_kv_head=2)
     assert U.ulysses_workspace_bytes(pr, 1) >= b + 2 * pr.P * pr.B * pr.S * pr.head_dim * 4
     assert U.ulysses_workspace_bytes(prob(B=0), 0) == 0
-    assert U.ulysses_workspace_bytes(p, 4) == 0 and U.ulysses_workspace_bytes(p, -1) == 0
+    assert U.ulysses_workspace_bytes(p, 5) == 0 and U.ulysses_workspace_bytes(p, -1) == 0
     # the hybrid regroups the same rows: the same workspace
     assert U.ulysses_workspace_bytes(prob(ring=2), 1) == b
     # S = 4098 over P = 2: the delta and base-2 LSE rows (one per batch and
@@ -104,14 +104,26 @@ def test_ds_store_workspace(lib):
         assert d == b + ((p.B * p.n_head * pairs * 128 * 128 * 2 + 255) // 256) * 256
 
 
+def test_ds_store_least_workspace(lib):
+    """Phase 4 is phase 1 followed by the tiles of one kv-head's q-heads on
+    one rank (n_head / n_kv_head of them; with replicated kv-heads, all of a
+    rank's n_head / P)."""
+    for kw, per_kv in ((dict(), 32 // 8), (dict(n_kv_head=2), 32 // 8), (dict(n_kv_head=32), 1)):
+        p = prob(**kw)
+        tiles = 32 * 33 // 2
+        b, m = U.ulysses_workspace_bytes(p, 1), U.ulysses_workspace_bytes(p, 4)
+        assert m == b + ((per_kv * tiles * 128 * 128 * 2 + 255) // 256) * 256
+        assert m < U.ulysses_workspace_bytes(p, 3)
+
+
 def test_ds_store_refusals(lib):
-    """The dS-store backward and its dQ step refuse a workspace smaller than
-    phase 3 before any launch."""
+    """The dS-store backward refuses a workspace smaller than phase 4, and its
+    steps one smaller than phase 3, before any launch."""
     vp = ctypes.c_void_p
     ptrs = [vp((1 << 40) + i * (1 << 30)) for i in range(10)]
     p = prob()
-    n3 = U.ulysses_workspace_bytes(p, 3)
-    assert lib.ulysses_attn_bwd_ds(ctypes.byref(p.c()), *ptrs[:9], vp(1 << 46), n3 - 256, vp(0)) == -7
+    n3, n4 = U.ulysses_workspace_bytes(p, 3), U.ulysses_workspace_bytes(p, 4)
+    assert lib.ulysses_attn_bwd_ds(ctypes.byref(p.c()), *ptrs[:9], vp(1 << 46), n4 - 256, vp(0)) == -7
     assert lib.ulysses_attn_bwd_dq_ds(ctypes.byref(p.c()), ptrs[1], ptrs[6], vp(1 << 46), n3 - 256, vp(0)) == -7
     assert lib.ulysses_attn_bwd_dkdv_ds(ctypes.byref(p.c()), *ptrs[:5], vp(1 << 46), n3 - 256, vp(0)) == -7
 

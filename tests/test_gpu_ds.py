@@ -138,3 +138,31 @@ def test_tiny_sequences_every_backward_mode(w):
             ref = {n: getattr(run.buf, n).clone() for n in ("dk_seq", "dv_seq")}
         else:
             assert all(torch.equal(getattr(run.buf, n), ref[n]) for n in ref), f"{name} dK/dV differ"
+
+
+@pytest.mark.parametrize("w", [wl(8, 1, 1024, 32, 8, 128),            # GQA: 4 q-heads a kv-head, 8 kv-heads
+                               wl(8, 1, 1024, 8, 2, 128),             # kv-heads replicated over 4 ranks
+                               wl(4, 2, 512, 8, 8, 64, causal=False)], ids=_ids)
+def test_ds_backward_in_chunks_of_kv_heads(w):
+    """A workspace smaller than phase 3 (down to phase 4: one kv-head's tiles)
+    makes the dS-store backward run the kv-heads in chunks; every chunking
+    gives the same bits as the whole-workspace call."""
+    w = w.with_(backward=True)
+    run = GpuRun(w, backward=True, ds=True)
+    run.forward()
+    run.backward_ds()
+    b, p = run.buf, run.prob
+    ref = {n: getattr(b, n).clone() for n in GRADS}
+    n1, n3, n4 = (U.ulysses_workspace_bytes(p, k) for k in (1, 3, 4))
+    per_kv = n4 - n1
+    for nbytes in (n4, n1 + 3 * per_kv, n3 - 256):
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        U.ulysses_workspace_init(p, ws)
+        for n in GRADS:
+            getattr(b, n).fill_(float("nan"))
+        U.ulysses_attn_bwd_ds(p, b.q_head, b.k_head, b.v_head, b.o_head, b.lse, b.do_seq, b.dq_seq, b.dk_seq,
+                              b.dv_seq, ws)
+        torch.cuda.synchronize()
+        assert U.ulysses_read_status(ws) == 0
+        for n in GRADS:
+            assert torch.equal(getattr(b, n), ref[n]), (nbytes, n)

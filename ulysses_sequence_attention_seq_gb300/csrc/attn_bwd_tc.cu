@@ -81,6 +81,11 @@ struct BwdParams {
   // q-head (see ds_tile).
   __nv_bfloat16 *ds;
   long long ds_pairs;
+  // The kv-heads ((member * B + batch) * kvp + local kv-head) a dK/dV or
+  // dQ-from-dS launch covers, [head0, head0 + head_n), with their q-heads; the
+  // dS store then holds the tiles of those q-heads only, the first q-head's at
+  // its start.
+  int head0, head_n;
 };
 
 // Head-layout (rank * B + batch) of the rows at global position `pos` for the
@@ -125,7 +130,7 @@ __device__ __forceinline__ void store_ds_row(__nv_bfloat16 *dst, const uint32_t 
 __device__ __forceinline__ long long ds_tile(const BwdParams &p, int hq, int m, int n) {
   const int n_kt = (p.S + 127) / 128;
   const long long t = p.causal ? (long long)m * (m + 1) / 2 + n : (long long)m * n_kt + n;
-  return (long long)hq * p.ds_pairs + t;
+  return (long long)(hq - p.head0 * p.group) * p.ds_pairs + t;
 }
 
 // Element offset of row `pos` of local q-head j of the CTA's (member, batch)
@@ -321,11 +326,10 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
   }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int heads_total = p.Pu * p.B * p.kvp;
   const int n_kt_all = (p.S + 127) / 128;
-  const dev::HeadTile ht = dev::grouped_order((int)blockIdx.x, heads_total, n_kt_all, p.group_kv);
+  const dev::HeadTile ht = dev::grouped_order((int)blockIdx.x, p.head_n, n_kt_all, p.group_kv);
   const int n = ht.rank;  // key tile; low tiles have the most work
-  const int hid = ht.head;
+  const int hid = p.head0 + ht.head;
   const int kl = hid % p.kvp, rb = hid / p.kvp;
   const int n_qt = (p.S + 127) / 128;
   const int m0 = p.causal ? n : 0;
@@ -566,7 +570,7 @@ __global__ void __launch_bounds__(kThreadsKV, 1)
         // threads wait for the next scores
         const int gi = i / n_m, j = kl * p.group + gi;
         const long long e = ds_tile(p, rb * p.hp + j, m0 + i % n_m, n) * 16384 + (g * 4 * 128 + r) * 16;
-        if (in_range(p.status, e, 3 * 2048 + 16, p.ds_pairs * 16384LL * p.Pu * p.B * p.hp)) {
+        if (in_range(p.status, e, 3 * 2048 + 16, p.ds_pairs * 16384LL * p.head_n * p.group)) {
           const bool sw = (r >> 2) & 1;  // the halves' swap: words 4..7 first
           uint32_t x[32];
 #pragma unroll
@@ -1655,11 +1659,10 @@ __global__ void __launch_bounds__(kThreadsDS, 1)
   if ((*gst & 3u) || stale_rope_table(p)) return;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int heads_total = p.Pu * p.B * p.hp;
   const int n_qt = (p.S + 127) / 128;
-  const dev::HeadTile ht = dev::grouped_order((int)blockIdx.x, heads_total, n_qt, p.group_q);
-  const int m = n_qt - 1 - ht.rank;  // longest tiles first
-  const int hq = ht.head;            // (member * B + batch) * hp + local q-head
+  const dev::HeadTile ht = dev::grouped_order((int)blockIdx.x, p.head_n * p.group, n_qt, p.group_q);
+  const int m = n_qt - 1 - ht.rank;            // longest tiles first
+  const int hq = p.head0 * p.group + ht.head;  // (member * B + batch) * hp + local q-head
   const int j = hq % p.hp, rb = hq / p.hp;
   const int kl = j / p.group;
   const int n_kv = p.causal ? m + 1 : n_qt;
@@ -1693,7 +1696,7 @@ __global__ void __launch_bounds__(kThreadsDS, 1)
         if (!mbar_wait_bounded(bar + kDBarEmpty + 8 * s, ((n / kDSStages) & 1) ^ 1, abort_flag, gst)) break;
         const uint32_t full = bar + kDBarFull + 8 * s, st = sb + s * L::kStage;
         const long long e = ds_tile(p, hq, m, n) * 16384;
-        if (!in_range(p.status, e, 16384, p.ds_pairs * 16384LL * p.Pu * p.B * p.hp)) {  // checked build only
+        if (!in_range(p.status, e, 16384, p.ds_pairs * 16384LL * p.head_n * p.group)) {  // checked build only
           *abort_flag = 1;
           break;
         }
@@ -1784,7 +1787,7 @@ template <int D>
 cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void *q, const void *k,
                      const void *v, const void *do_head, const float *nlse, const float *delta,
                      const void *ws, void *dq, void *dk, void *dv, float *dqacc, void *ds, uint32_t *status,
-                     int parts, bool folded, cudaStream_t st) {
+                     int parts, bool folded, cudaStream_t st, int head0, int head_n) {
   const int Pu = group_ranks(p), Cs = chunk_len(p), Sl = p.S / p.P;
   const int hp = p.n_head / Pu, kvp = kv_per_rank(p), PB = p.P * p.B;
   // head-layout maps [P*B][Cs][hp|kvp][D], or folded the sequence-sharded
@@ -1835,8 +1838,18 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   // 1.72 GB with 48 MiB, 1.43 GB with 32 MiB, 1.36 GB with 16 MiB (algorithmic
   // 1.34 GB).  Half of the 129 MB L2 sits on each die, and the tiles of the
   // running groups share it with the outputs and the other operands.
-  bp.group_kv = l2_head_group((size_t)4 * p.S * D * bp.group, UB * kvp, n_t * UB * kvp, (size_t)32 << 20);
-  bp.group_q = l2_head_group((size_t)4 * p.S * D / bp.group, UB * hp, n_t * UB * hp, (size_t)16 << 20);
+  // A launch of the dK/dV or the dQ-from-dS kernel may cover a range of the
+  // kv-heads (and their q-heads); the other kernels cover all of them.
+  const int all_kv = UB * kvp;
+  if (head_n < 0) head_n = all_kv;
+  if (head0 < 0 || head_n <= 0 || head0 + head_n > all_kv ||
+      ((parts & (kBwdDq | kBwdFused | kBwdFinish)) && (head0 != 0 || head_n != all_kv)))
+    return cudaErrorInvalidValue;
+  bp.head0 = head0;
+  bp.head_n = head_n;
+  bp.group_kv = l2_head_group((size_t)4 * p.S * D * bp.group, head_n, n_t * head_n, (size_t)32 << 20);
+  bp.group_q = l2_head_group((size_t)4 * p.S * D / bp.group, head_n * bp.group, n_t * head_n * bp.group,
+                             (size_t)16 << 20);
   bp.scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)D);
   bp.scale_log2 = bp.scale * kLog2e;
   bp.nlse = nlse;
@@ -1859,8 +1872,8 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
   bp.ds = static_cast<__nv_bfloat16 *>(ds);
   bp.ds_pairs = p.causal ? n_tiles_pairs(p) : (long long)((p.S + 127) / 128) * ((p.S + 127) / 128);
 
-  const long long kv_blocks = n_t * UB * kvp;
-  const long long q_blocks = n_t * UB * hp;
+  const long long kv_blocks = n_t * head_n;             // the dK/dV kernels' CTAs
+  const long long q_blocks = n_t * head_n * bp.group;   // the dQ kernels' CTAs
   if (kv_blocks > 0x7fffffffll || q_blocks > 0x7fffffffll) return cudaErrorInvalidValue;
   cudaError_t e = cudaSuccess;
   if (parts & kBwdDkDv) {
@@ -1922,11 +1935,13 @@ cudaError_t launch_d(const ulysses_problem &p, const TmaEncoder &enc, const void
 cudaError_t launch_parts(const ulysses_problem &p, const TmaEncoder &enc, const void *q, const void *k,
                          const void *v, const void *do_head, const float *nlse, const float *delta,
                          const void *ws, void *dq, void *dk, void *dv, float *dqacc, void *ds, uint32_t *status,
-                         int parts, bool folded, cudaStream_t st) {
+                         int parts, bool folded, cudaStream_t st, int head0 = 0, int head_n = -1) {
   if (p.head_dim == 128)
-    return launch_d<128>(p, enc, q, k, v, do_head, nlse, delta, ws, dq, dk, dv, dqacc, ds, status, parts, folded, st);
+    return launch_d<128>(p, enc, q, k, v, do_head, nlse, delta, ws, dq, dk, dv, dqacc, ds, status, parts, folded, st,
+                         head0, head_n);
   if (p.head_dim == 64)
-    return launch_d<64>(p, enc, q, k, v, do_head, nlse, delta, ws, dq, dk, dv, dqacc, ds, status, parts, folded, st);
+    return launch_d<64>(p, enc, q, k, v, do_head, nlse, delta, ws, dq, dk, dv, dqacc, ds, status, parts, folded, st,
+                        head0, head_n);
   return cudaErrorInvalidValue;
 }
 
@@ -1935,9 +1950,10 @@ cudaError_t launch_parts(const ulysses_problem &p, const TmaEncoder &enc, const 
 cudaError_t launch_attn_bwd_dkdv(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
                                  const void *k, const void *v, const void *do_head, const float *nlse,
                                  const float *delta, const void *ws, void *dk_seq, void *dv_seq,
-                                 uint32_t *status, cudaStream_t st, bool folded, void *ds) {
+                                 uint32_t *status, cudaStream_t st, bool folded, void *ds, int head0,
+                                 int head_n) {
   return launch_parts(p, enc, q, k, v, do_head, nlse, delta, ws, nullptr, dk_seq, dv_seq, nullptr, ds, status,
-                      kBwdDkDv, folded, st);
+                      kBwdDkDv, folded, st, head0, head_n);
 }
 
 cudaError_t launch_attn_bwd_fused(const ulysses_problem &p, const TmaEncoder &enc, const void *q, const void *k,
@@ -1949,10 +1965,11 @@ cudaError_t launch_attn_bwd_fused(const ulysses_problem &p, const TmaEncoder &en
 }
 
 cudaError_t launch_dq_from_ds(const ulysses_problem &p, const TmaEncoder &enc, const void *k, const void *ws,
-                              const void *ds, void *dq_seq, uint32_t *status, cudaStream_t st) {
+                              const void *ds, void *dq_seq, uint32_t *status, cudaStream_t st, int head0,
+                              int head_n) {
   // the K map and the parameters are those of the packed (head-layout) backward
   return launch_parts(p, enc, nullptr, k, nullptr, nullptr, nullptr, nullptr, ws, dq_seq, nullptr, nullptr, nullptr,
-                      const_cast<void *>(ds), status, kBwdDqDS, false, st);
+                      const_cast<void *>(ds), status, kBwdDqDS, false, st, head0, head_n);
 }
 
 cudaError_t launch_dq_finish(const ulysses_problem &p, const TmaEncoder &enc, const void *ws, float *dq_acc,

@@ -28,6 +28,9 @@ struct WorkspaceLayout {
   // phase 3 (dS-store backward): every causal (or, unmasked, every) 128 x 128
   // tile pair's bf16 dS, at the same offset as the fused mode's accumulator
   size_t ds = 0, ds_bytes = 0, total_ds = 0;
+  // phase 4: room for the tiles of one kv-head's q-heads at a time (the
+  // dS-store backward then runs the kv-heads in chunks)
+  size_t ds_kv_bytes = 0, total_ds_min = 0;
 };
 WorkspaceLayout workspace_layout(const ulysses_problem &p);
 
@@ -118,7 +121,8 @@ cudaError_t launch_out_proj_unpack(const ulysses_problem &p, const TmaEncoder &e
 cudaError_t launch_attn_bwd_dkdv(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
                                  const void *k, const void *v, const void *do_head, const float *nlse,
                                  const float *delta, const void *ws, void *dk_seq, void *dv_seq,
-                                 uint32_t *status, cudaStream_t st, bool folded = false, void *ds = nullptr);
+                                 uint32_t *status, cudaStream_t st, bool folded = false, void *ds = nullptr,
+                                 int head0 = 0, int head_n = -1);
 cudaError_t launch_attn_bwd_dq(const ulysses_problem &p, const TmaEncoder &enc, const void *q,
                                const void *k, const void *v, const void *do_head, const float *nlse,
                                const float *delta, const void *ws, void *dq_seq, uint32_t *status,
@@ -126,9 +130,13 @@ cudaError_t launch_attn_bwd_dq(const ulysses_problem &p, const TmaEncoder &enc, 
 // dS-store backward (attn_bwd_tc.cu): the dK/dV kernel above with `ds` set
 // also writes every step's bf16 dS tile there; this computes dQ = scale *
 // sum dS K from those tiles (no recomputation) and writes it in sequence
-// layout.  Head layout only (not folded).
+// layout.  Head layout only (not folded).  Both can be limited to the
+// kv-heads [head0, head0 + head_n) of (member * B + batch) * kvp + local
+// kv-head and their q-heads (head_n < 0: all of them); `ds` then holds the
+// tiles of those q-heads only.
 cudaError_t launch_dq_from_ds(const ulysses_problem &p, const TmaEncoder &enc, const void *k, const void *ws,
-                              const void *ds, void *dq_seq, uint32_t *status, cudaStream_t st);
+                              const void *ds, void *dq_seq, uint32_t *status, cudaStream_t st, int head0 = 0,
+                              int head_n = -1);
 // The fused backward (attn_bwd_tc.cu): dK / dV as the dK/dV kernel writes
 // them, and every step's dQ share added into the float accumulator dq_acc
 // (which must hold zeros); then dq_finish scales, unrotates and writes dQ in

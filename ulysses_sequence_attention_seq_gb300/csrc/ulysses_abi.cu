@@ -52,8 +52,13 @@ WorkspaceLayout workspace_layout(const ulysses_problem &p) {
   L.total_fused = align256(L.dqacc + L.dqacc_bytes);
   const size_t n_kt = (size_t)(p.S + 127) / 128;
   L.ds = L.total_bwd;
-  L.ds_bytes = (size_t)p.B * p.n_head * (p.causal ? n_kt * (n_kt + 1) / 2 : n_kt * n_kt) * 128 * 128 * 2;
+  const size_t tiles = p.causal ? n_kt * (n_kt + 1) / 2 : n_kt * n_kt;  // per q-head
+  L.ds_bytes = (size_t)p.B * p.n_head * tiles * 128 * 128 * 2;
   L.total_ds = align256(L.ds + L.ds_bytes);
+  // a kv-head's q-heads on one rank: n_head / n_kv_head, or with replicated
+  // kv-heads (fewer than the ranks of a group) all n_head / Pu of the rank's
+  L.ds_kv_bytes = (size_t)(p.n_head / group_ranks(p) / kv_per_rank(p)) * tiles * 128 * 128 * 2;
+  L.total_ds_min = align256(L.ds + L.ds_kv_bytes);
   return L;
 }
 
@@ -128,7 +133,11 @@ int check_ws(const ulysses_problem &p, const void *ws, size_t ws_bytes, int phas
   if (!ws) return ULYSSES_ERR_WORKSPACE;
   if (!aligned16(ws)) return ULYSSES_ERR_ALIGN;
   const WorkspaceLayout L = workspace_layout(p);
-  if (ws_bytes < (phase == 3 ? L.total_ds : phase == 2 ? L.total_fused : phase ? L.total_bwd : L.total_fwd))
+  if (ws_bytes < (phase == 4   ? L.total_ds_min
+                  : phase == 3 ? L.total_ds
+                  : phase == 2 ? L.total_fused
+                  : phase      ? L.total_bwd
+                               : L.total_fwd))
     return ULYSSES_ERR_WORKSPACE;
   return ULYSSES_OK;
 }
@@ -228,9 +237,13 @@ int ulysses_validate(const ulysses_problem *prob) {
 }
 
 size_t ulysses_workspace_bytes(const ulysses_problem *prob, int phase) {
-  if (phase < 0 || phase > 3 || ulysses_validate(prob) != ULYSSES_OK) return 0;
+  if (phase < 0 || phase > 4 || ulysses_validate(prob) != ULYSSES_OK) return 0;
   const WorkspaceLayout L = workspace_layout(*prob);
-  return phase == 3 ? L.total_ds : phase == 2 ? L.total_fused : phase ? L.total_bwd : L.total_fwd;
+  return phase == 4 ? L.total_ds_min
+         : phase == 3 ? L.total_ds
+         : phase == 2 ? L.total_fused
+         : phase      ? L.total_bwd
+                      : L.total_fwd;
 }
 
 int ulysses_workspace_init(const ulysses_problem *prob, void *ws, size_t ws_bytes,
@@ -537,10 +550,37 @@ int ulysses_attn_bwd_ds(const ulysses_problem *prob, const void *q_head, const v
   int rc = check_bwd_call(prob, q_head, k_head, v_head, o_head, lse, do_seq, dq_seq, dk_seq, dv_seq, ws,
                           ws_bytes);
   if (rc) return rc;
-  if ((rc = check_ws(*prob, ws, ws_bytes, 3))) return rc;
+  const ulysses_problem &p = *prob;
+  if ((rc = check_ws(p, ws, ws_bytes, 4))) return rc;
   if ((rc = ulysses_attn_bwd_prepare(prob, o_head, lse, do_seq, ws, ws_bytes, stream))) return rc;
-  if ((rc = ulysses_attn_bwd_dkdv_ds(prob, q_head, k_head, v_head, dk_seq, dv_seq, ws, ws_bytes, stream))) return rc;
-  return ulysses_attn_bwd_dq_ds(prob, k_head, dq_seq, ws, ws_bytes, stream);
+  TmaEncoder enc;
+  if (!get_tma_encoder(&enc)) return ULYSSES_ERR_CUDA;
+  const WorkspaceLayout L = workspace_layout(p);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t *status = reinterpret_cast<uint32_t *>(w + L.status);
+  const float *nlse = reinterpret_cast<const float *>(w + L.nlse), *delta = reinterpret_cast<const float *>(w + L.delta);
+  const bool rep = kv_replicas(p) > 1;
+  void *dkk = rep ? static_cast<void *>(w + L.dkpart) : dk_seq, *dvv = rep ? static_cast<void *>(w + L.dvpart) : dv_seq;
+  // As many kv-heads' tiles as the workspace holds at a time (all of them with
+  // a phase-3 workspace): dK/dV storing that chunk's dS, then its dQ.
+  const int all_kv = group_ranks(p) * p.B * kv_per_rank(p);
+  const size_t fit = (ws_bytes - L.ds) / L.ds_kv_bytes;
+  const int chunk = fit >= (size_t)all_kv ? all_kv : (int)fit;
+  cudaError_t e = cudaSuccess;
+  for (int h0 = 0; h0 < all_kv && e == cudaSuccess; h0 += chunk) {
+    const int hn = all_kv - h0 < chunk ? all_kv - h0 : chunk;
+    e = launch_attn_bwd_dkdv(p, enc, q_head, k_head, v_head, w + L.dohead, nlse, delta, ws, dkk, dvv, status, st,
+                             false, w + L.ds, h0, hn);
+    if (e == cudaSuccess) e = launch_dq_from_ds(p, enc, k_head, ws, w + L.ds, dq_seq, status, st, h0, hn);
+  }
+  if (e == cudaSuccess && rep) {
+    // the sum over every kv-head's replicas of the ranks' partials
+    const float scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)p.head_dim);
+    e = launch_kv_reduce(p, reinterpret_cast<float *>(dkk), reinterpret_cast<float *>(dvv), dk_seq, dv_seq, scale, ws,
+                         st);
+  }
+  return cuda_rc(e);
 }
 
 int ulysses_attn_bwd(const ulysses_problem *prob, const void *q_head, const void *k_head,
