@@ -324,6 +324,24 @@ def run_ulysses(args, w, rank, world):
     if sp.status() != 0:
         raise RuntimeError("device status word set during the end-to-end steps")
     del sp
+    # the host link's copy rate on this machine (the q input, up and then down,
+    # each copy alone): what bounds the end-to-end leg's first upload and last
+    # download, the copies the compute cannot hide
+    link = {}
+    up = torch.empty_like(host["q"], device=dev)
+    down = torch.empty(host["q"].shape, dtype=host["q"].dtype, pin_memory=True)
+    for name, fn in (("h2d_gbs", lambda: up.copy_(host["q"], non_blocking=True)),
+                     ("d2h_gbs", lambda: down.copy_(up, non_blocking=True))):
+        fn()
+        torch.cuda.synchronize()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(3):
+            fn()
+        z.record(stream)
+        torch.cuda.synchronize()
+        link[name] = 3 * up.numel() * up.element_size() / (a.elapsed_time(z) * 1e-3) / 1e9
+    del up, down
     # ---- folded forward (pack + attention + unpack in one kernel) vs the three
     # calls, same shapes with RoPE off (the folded path needs pre-rotated q, k)
     folded = None
@@ -370,7 +388,7 @@ def run_ulysses(args, w, rank, world):
     ex2_rate = U.ulysses_selftest_ex2_rate()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     return dict(total_ms=total_ms, per=per, alt_per=alt_per, bwd_mode=mode, clocks=clk, e2e_ms=e2e_ms, h2d=h2d,
-                d2h=d2h, launches=launches_per_step * args.steps, status=status, backward=backward,
+                d2h=d2h, link=link, launches=launches_per_step * args.steps, status=status, backward=backward,
                 folded=folded, ex2_rate=ex2_rate, sms=sms)
 
 
@@ -858,6 +876,10 @@ def main():
         "clocks": r["clocks"],
         "e2e": {"value": job_throughput(tokens, e2e_ms * 1e-3, world), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "host_link": {**r.get("link", {}),
+                      "note": "pinned host <-> device copy rate on this machine, one copy at a time; the end-to-end "
+                              "leg hides every step's copies behind the compute but the first upload and the "
+                              "last download"},
         "gpu_launches": r["launches"],
         # the folded mode (both All-to-Alls as addressing) is timed beside the
         # headline path, not on it: it needs q and k rotated by their producer
