@@ -53,6 +53,8 @@ TRAFFIC = {
     ("attn_fwd", "C4-ring8"): 1077393792,
     ("bwd_dkdv", "C4-ring8"): 1636954368,
     ("bwd_dq", "C4-ring8"): 1360104576,
+    ("bwd_dkdv_ds", "C4-ring8"): 36822935168,
+    ("bwd_dq_ds", "C4-ring8"): 35417668224,
 }
 
 
