@@ -55,6 +55,9 @@ TRAFFIC = {
     ("bwd_dq", "C4-ring8"): 1360104576,
     ("bwd_dkdv_ds", "C4-ring8"): 36822935168,
     ("bwd_dq_ds", "C4-ring8"): 35417668224,
+    ("attn_fwd", "C4-kv4"): 640970624,
+    ("bwd_dkdv_ds", "C4-kv4"): 40575356032,
+    ("bwd_dq_ds", "C4-kv4"): 35152657664,
 }
 
 
