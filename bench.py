@@ -48,8 +48,8 @@ TRAFFIC = {
     ("attn_fwd", "C4"): 1062845312,
     ("bwd_dkdv", "C4"): 1627353472,
     ("bwd_dq", "C4"): 1359185920,
-    ("bwd_dkdv_ds", "C4"): 36852312576,
-    ("bwd_dq_ds", "C4"): 35417489536,
+    ("bwd_dkdv_ds", "C4"): 36864050432,
+    ("bwd_dq_ds", "C4"): 35416766208,
     ("attn_fwd", "C4-ring8"): 1077393792,
     ("bwd_dkdv", "C4-ring8"): 1636954368,
     ("bwd_dq", "C4-ring8"): 1360104576,
