@@ -2,12 +2,14 @@
 C ABI: one token per rank (S = P), shards of an odd length (S not a multiple
 of 4, so the backward's per-row delta / LSE rows are padded to 16 bytes in the
 workspace), a shard length just past one tile, and a single token, where
-attention has a closed form (O = V, LSE = the one score, dV = dO)."""
+attention has a closed form (O = V, LSE = the one score, dV = dO); the
+backward in each of its three modes."""
 import numpy as np
 import pytest
 import torch
 
 import test_gpu_backward as BWD
+import test_gpu_ds as DS
 import test_gpu_forward as FWD
 from pathcheck import GpuRun, to64
 from test_gpu_forward import wl
@@ -31,6 +33,13 @@ def test_backward_at_degenerate_sizes(w):
     BWD.test_backward_matches_oracle(w)
 
 
+@pytest.mark.parametrize("w", CASES, ids=BWD._ids)
+def test_every_backward_mode_at_degenerate_sizes(w):
+    """The two-kernel, dS-store and fused backwards against the oracle, dK and
+    dV identical across the three."""
+    DS.test_tiny_sequences_every_backward_mode(w)
+
+
 def test_fp32_forward_one_token_per_rank():
     FWD.test_forward_matches_oracle(wl(2, 1, 2, 2, 2, 32, "fp32"))
 
@@ -41,13 +50,16 @@ def test_single_token_has_the_closed_form():
     is the scaled score q.k / sqrt(D) (RoPE at position 0 is the identity),
     and dS = P (dP - delta) vanishes up to rounding, and with it dQ and dK."""
     w = wl(1, 1, 1, 1, 1, 64).with_(backward=True)
-    run = GpuRun(w, backward=True)
+    run = GpuRun(w, backward=True, ds=True, fused=True)
     run.forward()
-    run.backward()
     b = run.buf
     assert torch.equal(b.o_seq.flatten(), b.v_seq.flatten())
     q, k = to64(b.q_seq).reshape(-1), to64(b.k_seq).reshape(-1)
     want = float(q @ k) / np.sqrt(w.head_dim)
     assert abs(float(to64(b.lse).reshape(-1)[0]) - want) <= 1e-3 * (1 + abs(want))
-    assert torch.equal(b.dv_seq.flatten(), b.do_seq.flatten())
-    assert b.dq_seq.float().abs().max() <= 1e-2 and b.dk_seq.float().abs().max() <= 1e-2
+    for call in (run.backward, run.backward_ds, run.backward_fused):
+        for t in (b.dq_seq, b.dk_seq, b.dv_seq):
+            t.fill_(float("nan"))
+        call()
+        assert torch.equal(b.dv_seq.flatten(), b.do_seq.flatten())
+        assert b.dq_seq.float().abs().max() <= 1e-2 and b.dk_seq.float().abs().max() <= 1e-2

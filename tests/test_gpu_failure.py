@@ -36,3 +36,36 @@ def test_bounded_wait_times_out_and_is_reported():
     U.ulysses_workspace_init(run.prob, run.buf.ws)
     run.forward()
     assert torch.equal(run.buf.o_seq, good)
+
+
+def test_every_backward_mode_refuses_to_start_after_a_timeout():
+    """With a timeout bit in the status word the two-kernel, dS-store and fused
+    backwards write no gradient; prepared again, each gives its earlier bits."""
+    w = wl(2, 1, 256, 4, 4, 64).with_(backward=True)
+    run = GpuRun(w, backward=True, ds=True, fused=True)
+    run.forward()
+    b = run.buf
+    grads = ("dq_seq", "dk_seq", "dv_seq")
+    modes = {"two-kernel": b.backward, "dS-store": b.backward_ds, "fused": b.backward_fused}
+    good = {}
+    for name, call in modes.items():
+        call()
+        torch.cuda.synchronize()
+        assert U.ulysses_read_status(b.ws) == 0
+        good[name] = [getattr(b, n).clone() for n in grads]
+
+    U.ulysses_selftest_wait_timeout(b.ws, 20_000_000)        # 20 ms
+    for name, call in modes.items():
+        for n in grads:
+            getattr(b, n).zero_()
+        call()
+        torch.cuda.synchronize()
+        assert U.ulysses_read_status(b.ws) & U.STATUS_FWD_TIMEOUT
+        assert not any(getattr(b, n).any() for n in grads), f"{name} backward wrote after a timeout"
+
+    U.ulysses_workspace_init(run.prob, b.ws)
+    for name, call in modes.items():
+        call()
+        torch.cuda.synchronize()
+        assert U.ulysses_read_status(b.ws) == 0
+        assert all(torch.equal(getattr(b, n), g) for n, g in zip(grads, good[name])), name

@@ -98,44 +98,66 @@ def test_forward_matches_ring_oracle(w):
 
 @pytest.mark.parametrize("w", RING_CASES, ids=_id)
 def test_backward_matches_ring_oracle(w):
+    """The two-kernel and the dS-store backward against the ring oracle; the
+    dS-store one's dK and dV bit-identical to the two-kernel one's (the same
+    kernel, which only also stores dS)."""
     w = w.with_(backward=True)
-    run = GpuRun(w, backward=True)
+    run = GpuRun(w, backward=True, ds=True)
     run.forward()
     run.backward()
     x = oracle_inputs(run.inputs)
     want = RG.backward(oracle_problem(w), x["q"], x["k"], x["v"], x["do"])
     for name in ("dq_seq", "dk_seq", "dv_seq"):
         assert_close(to64(getattr(run.buf, name)), np.stack(want[name]), w, name)
+    ref = {n: getattr(run.buf, n).clone() for n in ("dk_seq", "dv_seq")}
+    for n in ("dq_seq", "dk_seq", "dv_seq"):
+        getattr(run.buf, n).fill_(float("nan"))
+    run.backward_ds()
+    assert_close(to64(run.buf.dq_seq), np.stack(want["dq_seq"]), w, "dS-store dq_seq")
+    for n, t in ref.items():
+        assert torch.equal(getattr(run.buf, n), t), f"dS-store {n} differs from the two-kernel backward"
 
 
-def _same_as_plain_ulysses(w, backward):
+def _same_as_plain_ulysses(w, backward, ds=False):
     """The hybrid and plain Ulysses over Pu ranks compute every head with the
-    same tiles in the same order: outputs equal bit for bit (sequence layout)."""
-    hyb = GpuRun(w, backward=backward)
-    plain = GpuRun(w.with_(P=w.P // w.ring, ring=1), backward=backward, inputs=hyb.inputs)
+    same tiles in the same order: outputs equal bit for bit (sequence layout).
+    With `ds`, the dS-store backward is compared too."""
+    hyb = GpuRun(w, backward=backward, ds=ds)
+    plain = GpuRun(w.with_(P=w.P // w.ring, ring=1), backward=backward, inputs=hyb.inputs, ds=ds)
+    names = ("o_seq",) + (("dq_seq", "dk_seq", "dv_seq") if backward else ())
+
+    def same(what):
+        for name in names:
+            a, b = getattr(hyb.buf, name), getattr(plain.buf, name)
+            # both are [P][B][Sl][...] of the same global sequence, sharded P or P/ring ways
+            assert torch.equal(a.reshape(-1), b.reshape(-1)) if w.B == 1 else \
+                torch.equal(a.transpose(0, 1).reshape(w.B, -1), b.transpose(0, 1).reshape(w.B, -1)), (what, name)
+
     for run in (hyb, plain):
         run.forward()
         if backward:
             run.backward()
-    names = ("o_seq",) + (("dq_seq", "dk_seq", "dv_seq") if backward else ())
-    for name in names:
-        a, b = getattr(hyb.buf, name), getattr(plain.buf, name)
-        # both are [P][B][Sl][...] of the same global sequence, sharded P or P/ring ways
-        assert torch.equal(a.reshape(-1), b.reshape(-1)) if w.B == 1 else \
-            torch.equal(a.transpose(0, 1).reshape(w.B, -1), b.transpose(0, 1).reshape(w.B, -1)), name
+    same("two-kernel backward")
+    if backward and ds:
+        for run in (hyb, plain):
+            for n in ("dq_seq", "dk_seq", "dv_seq"):
+                getattr(run.buf, n).fill_(float("nan"))
+            run.backward_ds()
+        same("dS-store backward")
 
 
 @pytest.mark.parametrize("w", RING_CASES[:3] + RING_CASES[5:], ids=_id)
 def test_bit_identical_to_plain_ulysses(w):
-    _same_as_plain_ulysses(w.with_(backward=True), backward=True)
+    _same_as_plain_ulysses(w.with_(backward=True), backward=True, ds=True)
 
 
 def test_full_size_pages_example():
     """The pages' head-count example at full size, in the bench's launch
     configuration: C4's model (32 heads, S = 32768) over P = 256 ranks as 8
     ring positions of 32.  Forward sampled against the ring oracle (every
-    query row exact over its full key range), then forward and backward
-    bit-identical to plain Ulysses over 32 ranks."""
+    query row exact over its full key range), then forward and both the
+    two-kernel and the dS-store backward bit-identical to plain Ulysses over
+    32 ranks."""
     w = EXTRA_WORKLOADS["C4-ring8"]
     run = GpuRun(w, backward=False)
     run.forward()
@@ -153,4 +175,4 @@ def test_full_size_pages_example():
             assert_lse_close(got_lse[me][..., mine], want["lse"][me][..., mine], w, f"lse rank {me}")
     del run, x, want
     torch.cuda.empty_cache()
-    _same_as_plain_ulysses(w, backward=True)
+    _same_as_plain_ulysses(w, backward=True, ds=True)
