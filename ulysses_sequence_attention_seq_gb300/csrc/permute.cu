@@ -340,10 +340,16 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-int grid_for(long long rows) {
-  int dev = 0, sms = 148;
+// A grid-stride kernel's grid: as many blocks as are resident at once on all
+// SMs (the kernel's own occupancy at `threads` threads a block), so that none
+// waits for a second wave, and no more blocks than work items.
+template <typename Kernel>
+int grid_for(Kernel kernel, int threads, long long rows) {
+  int dev = 0, sms = 148, per_sm = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  long long g = (long long)sms * 8;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  long long g = (long long)sms * per_sm;
   if (rows < g) g = rows;
   return (int)(g > 0 ? g : 1);
 }
@@ -432,11 +438,11 @@ static cudaError_t launch_perm(const ulysses_problem &p, const PermParams &pp, c
     if (p.dtype == ULYSSES_BF16) return launch_unpack_bulk<__nv_bfloat16>(p, pp, (uint32_t)row_bytes, st);
     return launch_unpack_bulk<float>(p, pp, (uint32_t)row_bytes, st);
   }
-  const int grid = grid_for((long long)p.B * p.S);
+  const long long rows = (long long)p.B * p.S;
   if (p.dtype == ULYSSES_BF16)
-    permute_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(pp);
+    permute_kernel<__nv_bfloat16><<<grid_for(permute_kernel<__nv_bfloat16>, kThreads, rows), kThreads, 0, st>>>(pp);
   else
-    permute_kernel<float><<<grid, kThreads, 0, st>>>(pp);
+    permute_kernel<float><<<grid_for(permute_kernel<float>, kThreads, rows), kThreads, 0, st>>>(pp);
   return cudaGetLastError();
 }
 
@@ -469,8 +475,8 @@ cudaError_t launch_unpack(const ulysses_problem &p, const void *o_head, void *o_
 cudaError_t launch_pack_do_delta(const ulysses_problem &p, const void *do_seq, const void *o,
                                  const float *lse, void *do_head, float *delta, float *nlse,
                                  uint32_t *status, cudaStream_t st, bool folded) {
-  const int grid = grid_for((long long)p.B * p.S);  // one token row per block at a time
   auto kernel = folded ? pack_do_delta_kernel<true> : pack_do_delta_kernel<false>;
+  const int grid = grid_for(kernel, kThreads, (long long)p.B * p.S);  // one token row per block at a time
   kernel<<<grid, kThreads, 0, st>>>(
       static_cast<const __nv_bfloat16 *>(do_seq), static_cast<const __nv_bfloat16 *>(o),
       lse, static_cast<__nv_bfloat16 *>(do_head), delta, nlse, p.P, p.B, p.S / p.P, p.n_head,
@@ -569,7 +575,7 @@ cudaError_t launch_kv_reduce(const ulysses_problem &p, const float *dk_part, con
     sn = cs + (size_t)p.S * (p.head_dim / 2);
   }
   const long long n = (long long)p.B * p.S * p.n_kv_head * (p.head_dim / 8);
-  kv_reduce_kernel<<<grid_for(n / 256 + 1), 256, 0, st>>>(dk_part, dv_part, static_cast<__nv_bfloat16 *>(dk_seq),
+  kv_reduce_kernel<<<grid_for(kv_reduce_kernel, 256, n / 256 + 1), 256, 0, st>>>(dk_part, dv_part, static_cast<__nv_bfloat16 *>(dk_seq),
                                                           static_cast<__nv_bfloat16 *>(dv_seq), p.P, p.B,
                                                           p.S / p.P, p.n_kv_head, p.head_dim, group_ranks(p), scale,
                                                           cs, sn,
