@@ -384,9 +384,7 @@ __global__ void zero_kernel(float4 *p, long long n4) {
 cudaError_t launch_zero(float *p, size_t n, cudaStream_t st) {
   const long long n4 = (long long)(n / 4);
   if (n % 4 || n4 == 0) return n4 == 0 && n == 0 ? cudaSuccess : cudaErrorInvalidValue;
-  long long grid = (n4 + 255) / 256;
-  if (grid > 4096) grid = 4096;
-  zero_kernel<<<(unsigned)grid, 256, 0, st>>>(reinterpret_cast<float4 *>(p), n4);
+  zero_kernel<<<grid_for(zero_kernel, 256, (n4 + 255) / 256), 256, 0, st>>>(reinterpret_cast<float4 *>(p), n4);
   return cudaGetLastError();
 }
 
