@@ -1,7 +1,7 @@
 """The range-checked build (-DULYSSES_CHECK_BOUNDS: every plain global load
 and store checked against its buffer) runs the whole path without a single
 failed check and gives bit for bit what the normal build gives: forward,
-backward (two-kernel and dS-store), the workspace-free backward, the fp32 forward, replicated kv-heads,
+backward (two-kernel, dS-store, and dS-store in kv-head chunks), the workspace-free backward, the fp32 forward, replicated kv-heads,
 the ring hybrid, the folded forward and backward and the two projections.  The checked library runs in a
 child process (ULYSSES_LIB)."""
 import os
@@ -47,6 +47,16 @@ for n, w in enumerate(cases):
         for name in ("dq_seq", "dk_seq", "dv_seq"):
             out[f"{n}/ds/{name}"] = getattr(run.buf, name).cpu()
         out[f"{n}/ds/status"] = torch.tensor(U.ulysses_read_status(run.buf.ws))
+        # and in kv-head chunks, one kv-head's tiles at a time (a phase-4 workspace)
+        b = run.buf
+        ws4 = torch.empty(U.ulysses_workspace_bytes(run.prob, 4), dtype=torch.uint8, device="cuda")
+        U.ulysses_workspace_init(run.prob, ws4)
+        U.ulysses_attn_bwd_ds(run.prob, b.q_head, b.k_head, b.v_head, b.o_head, b.lse, b.do_seq, b.dq_seq,
+                              b.dk_seq, b.dv_seq, ws4)
+        torch.cuda.synchronize()
+        for name in ("dq_seq", "dk_seq", "dv_seq"):
+            out[f"{n}/ds4/{name}"] = getattr(b, name).cpu()
+        out[f"{n}/ds4/status"] = torch.tensor(U.ulysses_read_status(ws4))
     if n == 0:  # the workspace-free backward on the same buffers
         b = run.buf
         grads = [torch.empty_like(getattr(b, g)) for g in ("dq_seq", "dk_seq", "dv_seq")]
