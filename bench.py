@@ -61,6 +61,9 @@ TRAFFIC = {
 }
 
 
+SM_MAX_MHZ_FALLBACK = 2070.0  # GB300's maximum SM clock, when nvidia-smi gave none
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -791,15 +794,21 @@ def main():
     # method defines: forward S and PV; backward dV, dP, dQ, dK, each half a
     # forward) and the FLOPs each kernel executes (dK/dV and dQ both recompute
     # S, dQ also dP).
-    tc = {"attn_fwd": ("attn_fwd_tc_kernel", fl, fl)}
+    # The fp32 workload's forward runs on the CUDA cores (fp32 FMA): its peak
+    # is derived, SMs x 128 fp32 lanes x 2 FLOP per FMA x the maximum SM clock.
+    fp32 = w.dtype != "bf16"
+    sm_max = r["clocks"].get("sm_max_mhz") or SM_MAX_MHZ_FALLBACK
+    alu_peak = r["sms"] * 128 * 2 * sm_max * 1e6 / 1e12
+    peak_k = alu_peak if fp32 else tf_sust
+    tc = {"attn_fwd": ("attn_fwd_simt_kernel" if fp32 else "attn_fwd_tc_kernel", fl, fl)}
     tc.update({k: BWD_TC[k](fl) for k in bwd_parts if k in BWD_TC})
     kernels = {}
     for k, (kname, alg, exe) in tc.items():
         a_tf = alg / (per[k] * 1e-3) / 1e12
         kernels[k] = {"kernel": f"{kname}<{w.head_dim}>", "ms": per[k], "algorithmic_tflop": alg / 1e12,
-                      "achieved_tflops": a_tf, "frac": a_tf / tf_sust,
+                      "achieved_tflops": a_tf, "frac": a_tf / peak_k,
                       "executed_tflops": exe / (per[k] * 1e-3) / 1e12,
-                      "executed_frac": exe / (per[k] * 1e-3) / 1e12 / tf_sust}
+                      "executed_frac": exe / (per[k] * 1e-3) / 1e12 / peak_k}
     # dQ from the stored dS tiles reads them once: bound by HBM
     hbm_kernels = {}
     if "bwd_dq_ds" in per:
@@ -829,7 +838,7 @@ def main():
     exps = w.B * w.n_head * (w.S * (w.S + 1) / 2 if w.causal else float(w.S) * w.S)
     clk_hz = (r["clocks"].get("sm_mhz") or 0) * 1e6
     mufu = None
-    if clk_hz > 0 and r["ex2_rate"] > 0:
+    if clk_hz > 0 and r["ex2_rate"] > 0 and not fp32:
         ach = exps / (attn_ms * 1e-3) / (r["sms"] * clk_hz)
         mufu = {"bound": "mufu", "kernel": f"attn_fwd_tc_kernel<{w.head_dim}>", "achieved": ach,
                 "peak": r["ex2_rate"], "unit": "ex2/SM/cycle", "frac": ach / r["ex2_rate"], "exps_per_launch": exps,
@@ -856,10 +865,12 @@ def main():
         "kernel_ms_min": {k: min(v) for k, v in r["per"].items()},
         "tensor_kernels": kernels,
         "bwd_modes": bwd_modes,
-        "roofline": {"bound": "tensor", "achieved": dk["achieved_tflops"], "peak": tf_sust, "unit": "TFLOP/s",
-                     "frac": dk["frac"], "traffic": TRAFFIC.get((dominant, w.name)),
-                     "peak_source": f"{peak_src} bf16 sustained", "kernel": dk["kernel"],
-                     "peak_burst": tf_burst, "frac_burst": dk["achieved_tflops"] / tf_burst,
+        "roofline": {"bound": "alu" if fp32 else "tensor", "achieved": dk["achieved_tflops"], "peak": peak_k,
+                     "unit": "TFLOP/s", "frac": dk["frac"], "traffic": TRAFFIC.get((dominant, w.name)),
+                     "peak_source": (f"derived fp32 FMA: {r['sms']} SMs x 128 lanes x 2 FLOP x {sm_max:.0f} MHz"
+                                     if fp32 else f"{peak_src} bf16 sustained"), "kernel": dk["kernel"],
+                     "peak_burst": None if fp32 else tf_burst,
+                     "frac_burst": None if fp32 else dk["achieved_tflops"] / tf_burst,
                      "sm_mhz": r["clocks"].get("sm_mhz"), "bwd_mode": r["bwd_mode"],
                      # DRAM rate of the same launch (traffic from the ncu capture over this run's time)
                      "dram_gbs": (TRAFFIC[(dominant, w.name)] / (dk["ms"] * 1e-3) / 1e9
@@ -869,7 +880,8 @@ def main():
                              "one; sm_mhz is the median SM clock sampled while the timed steps ran"
                              + ("; in the dS-store backward the dK/dV kernel also writes every tile pair's dS "
                                 "(dram_gbs: its DRAM traffic over its time)" if dominant == "bwd_dkdv_ds" else "")},
-        "secondary_rooflines": {**{k: {"bound": "tensor", "achieved": v["achieved_tflops"], "peak": tf_sust,
+        "secondary_rooflines": {**{k: {"bound": "alu" if fp32 else "tensor", "achieved": v["achieved_tflops"],
+                                       "peak": peak_k,
                                        "unit": "TFLOP/s", "frac": v["frac"], "traffic": TRAFFIC.get((k, w.name))}
                                    for k, v in kernels.items() if k != dominant},
                                 **hbm_kernels,

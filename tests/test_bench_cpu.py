@@ -113,6 +113,27 @@ def test_bench_line_carries_the_contract_keys(monkeypatch, capsys):
     assert m["fused"]["ms"] == pytest.approx(0.17 + 20.0 + 1.0) and m["fused"]["kernel"] == "dkdvq_kernel<128>"
 
 
+def test_fp32_workload_reports_the_cuda_core_kernel_against_its_fma_peak(monkeypatch, capsys):
+    """The fp32 workload (C1) runs its forward on the CUDA cores: the roofline
+    names that kernel, bound "alu", against SMs x 128 fp32 lanes x 2 FLOP x
+    the maximum SM clock, and carries no tensor-core figures."""
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setattr(bench, "run_ulysses", lambda args, w, rank, world: _fake_measurements(False, args.steps))
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--workload", "C1", "--steps", "4", "--no-cpu-baseline"])
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.delenv("RANK", raising=False)
+    bench.main()
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    r = line["roofline"]
+    assert line["dtype"] == "f32" and line["config"]["workload"] == "C1"
+    assert r["kernel"] == "attn_fwd_simt_kernel<32>" and r["bound"] == "alu"
+    assert r["peak"] == pytest.approx(152 * 128 * 2 * 2070e6 / 1e12)
+    assert r["achieved"] == pytest.approx(bench.attn_fwd_flops(bench.WORKLOADS["C1"]) / 5.4e-3 / 1e12)
+    assert r["peak_burst"] is None and r["frac_burst"] is None
+    assert "attn_fwd_mufu" not in line["secondary_rooflines"]
+
+
 def test_reference_arm_times_both_passes_with_the_gpu_arms_config(monkeypatch, capsys):
     """For a workload with a backward the reference arm times the oracle's
     forward and backward (passes fwd+bwd, like the GPU arm's headline), labels
