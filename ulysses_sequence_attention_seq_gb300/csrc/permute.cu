@@ -34,6 +34,10 @@ namespace ulysses {
 namespace {
 
 constexpr int kThreads = 256;
+// A block of the permute kernel takes up to this many token rows per pass, so
+// that jobs with few (head, chunk) units a row (few kv-heads, D = 64) still
+// occupy its threads.
+constexpr int kMaxRowsPerPass = 8;
 
 struct PermJob {
   const void *src;  // read side
@@ -50,6 +54,7 @@ struct PermParams {
   int P, B, Sl, D;
   int Pu, Cs;   // ranks of a ring position and its tokens (plain Ulysses: P, S)
   int to_head;  // 1: src is sequence-sharded (pack); 0: src is head-sharded (unpack)
+  int nrow;     // token rows a block takes per pass (1 .. kMaxRowsPerPass)
   const float *rope_cos, *rope_sin;  // [S][D/2] each
   const uint32_t *rope_key_ptr;
   uint32_t rope_key;
@@ -123,15 +128,25 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const PermParams p) {
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.status, (uint32_t)ULYSSES_STATUS_ROPE_TABLE);
     return;
   }
-  for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
-    // row = (s*B + b)*Sl + t : token t of sequence shard s, batch b
-    const int t = (int)(row % p.Sl);
-    const long long sb = row / p.Sl;
-    const int b = (int)(sb % p.B);
-    const int s = (int)(sb / p.B);
-    const int pos = s * p.Sl + t;  // global token position
-    const int rp = s / p.Pu;       // ring position of the source rank
-    const int crow = pos - rp * p.Cs;  // row of the token in that position's chunk
+  // per pass: each row's batch, global position, ring position and row in
+  // that position's chunk, computed once by one thread each
+  __shared__ int row_b[kMaxRowsPerPass], row_pos[kMaxRowsPerPass], row_rp[kMaxRowsPerPass],
+      row_crow[kMaxRowsPerPass];
+  const int nrow = p.nrow;
+  for (long long row0 = (long long)blockIdx.x * nrow; row0 < rows; row0 += (long long)gridDim.x * nrow) {
+    __syncthreads();  // the previous pass is done with the row table
+    if ((int)threadIdx.x < nrow) {
+      // row = (s*B + b)*Sl + t : token t of sequence shard s, batch b
+      const long long row = row0 + threadIdx.x;
+      const int t = (int)(row % p.Sl);
+      const long long sb = row / p.Sl;
+      const int s = (int)(sb / p.B);
+      row_b[threadIdx.x] = (int)(sb % p.B);
+      row_pos[threadIdx.x] = s * p.Sl + t;                         // global token position
+      row_rp[threadIdx.x] = s / p.Pu;                              // ring position of the source rank
+      row_crow[threadIdx.x] = s * p.Sl + t - (s / p.Pu) * p.Cs;    // row of the token in that position's chunk
+    }
+    __syncthreads();
 #pragma unroll
     for (int q = 0; q < 3; ++q) {
       if (q >= p.njobs) break;
@@ -140,12 +155,18 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const PermParams p) {
       // A unit is chunk c of both halves of a head (2 x 16 bytes), rotated or
       // not: two loads in flight per thread either way.  With replicated heads
       // the units run over the P destination ranks (one head each), so a head
-      // of the token row is read once per replica.
+      // of the token row is read once per replica.  A pass's nrow rows are
+      // laid end to end: task i is unit i % units of row i / units.
       const int cph = p.D / (2 * V);
       const int run = hp * cph;                           // units per destination piece
       const int units = p.Pu * run;
-      const long long seq_row = row * (long long)J.heads * p.D;
-      for (int u = threadIdx.x; u < units; u += kThreads) {
+      for (int task = threadIdx.x; task < nrow * units; task += kThreads) {
+        const int rl = nrow == 1 ? 0 : task / units;
+        const int u = task - rl * units;
+        const long long row = row0 + rl;
+        if (row >= rows) break;  // rows of a pass run in order: the rest are past the end too
+        const int b = row_b[rl], pos = row_pos[rl], rp = row_rp[rl], crow = row_crow[rl];
+        const long long seq_row = row * (long long)J.heads * p.D;
         const int d = u / run;  // the rank on the head side of this piece
         const int w = u - d * run;
         const int j = w / cph, c = w - j * cph;
@@ -437,10 +458,21 @@ static cudaError_t launch_perm(const ulysses_problem &p, const PermParams &pp, c
     return launch_unpack_bulk<float>(p, pp, (uint32_t)row_bytes, st);
   }
   const long long rows = (long long)p.B * p.S;
+  // rows per pass: enough for the job with the fewest units a row to fill the block
+  const int vec = p.dtype == ULYSSES_BF16 ? 8 : 4;
+  int min_units = kThreads;
+  for (int q = 0; q < pp.njobs; ++q) {
+    const PermJob &J = pp.job[q];
+    const int u = pp.Pu * (J.rep > 1 ? 1 : J.heads / pp.Pu) * (p.head_dim / (2 * vec));
+    if (u < min_units) min_units = u;
+  }
+  PermParams pr = pp;
+  pr.nrow = min_units >= kThreads ? 1 : (kThreads / min_units < kMaxRowsPerPass ? kThreads / min_units : kMaxRowsPerPass);
+  const long long passes = (rows + pr.nrow - 1) / pr.nrow;
   if (p.dtype == ULYSSES_BF16)
-    permute_kernel<__nv_bfloat16><<<grid_for(permute_kernel<__nv_bfloat16>, kThreads, rows), kThreads, 0, st>>>(pp);
+    permute_kernel<__nv_bfloat16><<<grid_for(permute_kernel<__nv_bfloat16>, kThreads, passes), kThreads, 0, st>>>(pr);
   else
-    permute_kernel<float><<<grid_for(permute_kernel<float>, kThreads, rows), kThreads, 0, st>>>(pp);
+    permute_kernel<float><<<grid_for(permute_kernel<float>, kThreads, passes), kThreads, 0, st>>>(pr);
   return cudaGetLastError();
 }
 
