@@ -336,6 +336,11 @@ __global__ void __launch_bounds__(kThreads)
       float acc = 0.f;
       const long long head_row = (((long long)(d * B + b) * Cs + crow) * hp + j) * D;
       const long long seq_off = (row * H + g) * D + c * 8;
+      // the row's LSE is read before the products, so its load overlaps theirs
+      const long long hrow = (long long)(d * B + b) * hp + j;
+      const long long idx = hrow * Cs + crow, widx = hrow * Ld + crow;
+      const bool writer = live && c == 0 && in_range(status, idx, 1, rows_n) && in_range(status, widx, 1, ws_rows_n);
+      const float row_lse = writer ? __ldg(lse + idx) : 0.f;
       if (live && in_range(status, seq_off, 8, act_n) && in_range(status, head_row + c * 8, 8, act_n)) {
         const uint4 x = __ldg(reinterpret_cast<const uint4 *>(dout + seq_off));
         const uint4 y = __ldg(reinterpret_cast<const uint4 *>(o + (kFolded ? seq_off : head_row + c * 8)));
@@ -350,12 +355,9 @@ __global__ void __launch_bounds__(kThreads)
         }
       }
       for (int off = lanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      if (live && c == 0) {
-        const long long hrow = (long long)(d * B + b) * hp + j;
-        const long long idx = hrow * Cs + crow, widx = hrow * Ld + crow;
-        if (!in_range(status, idx, 1, rows_n) || !in_range(status, widx, 1, ws_rows_n)) continue;
+      if (writer) {
         delta[widx] = acc;
-        nlse[widx] = -lse[idx] * 1.4426950408889634f;
+        nlse[widx] = -row_lse * 1.4426950408889634f;
       }
     }
   }
