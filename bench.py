@@ -349,7 +349,27 @@ def run_ulysses(args, w, rank, world):
         z.record(stream)
         torch.cuda.synchronize()
         link[name] = 3 * up.numel() * up.element_size() / (a.elapsed_time(z) * 1e-3) / 1e9
-    del up, down
+    # and both directions at once, as the end-to-end leg runs them (an upload
+    # and a download on two streams): each direction's rate while the other runs
+    src_dev = up.clone()
+    s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    torch.cuda.synchronize()
+    ev = {n: torch.cuda.Event(enable_timing=True) for n in ("u0", "u1", "d0", "d1")}
+    with torch.cuda.stream(s_up):
+        ev["u0"].record(s_up)
+        for _ in range(3):
+            up.copy_(host["q"], non_blocking=True)
+        ev["u1"].record(s_up)
+    with torch.cuda.stream(s_down):
+        ev["d0"].record(s_down)
+        for _ in range(3):
+            down.copy_(src_dev, non_blocking=True)
+        ev["d1"].record(s_down)
+    torch.cuda.synchronize()
+    nb = 3 * up.numel() * up.element_size()
+    link["h2d_gbs_both_ways"] = nb / (ev["u0"].elapsed_time(ev["u1"]) * 1e-3) / 1e9
+    link["d2h_gbs_both_ways"] = nb / (ev["d0"].elapsed_time(ev["d1"]) * 1e-3) / 1e9
+    del up, down, src_dev
     # ---- folded forward (pack + attention + unpack in one kernel) vs the three
     # calls, same shapes with RoPE off (the folded path needs pre-rotated q, k)
     folded = None
@@ -894,9 +914,10 @@ def main():
         "e2e": {"value": job_throughput(tokens, e2e_ms * 1e-3, world), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "host_link": {**r.get("link", {}),
-                      "note": "pinned host <-> device copy rate on this machine, one copy at a time; the end-to-end "
-                              "leg hides every step's copies behind the compute but the first upload and the "
-                              "last download"},
+                      "note": "pinned host <-> device copy rate on this machine, one copy at a time (h2d_gbs, "
+                              "d2h_gbs) and with an upload and a download running at once (*_both_ways, as the "
+                              "end-to-end leg runs them); the end-to-end leg hides every step's copies behind the "
+                              "compute but the first upload and the last download"},
         "gpu_launches": r["launches"],
         # the folded mode (both All-to-Alls as addressing) is timed beside the
         # headline path, not on it: it needs q and k rotated by their producer
