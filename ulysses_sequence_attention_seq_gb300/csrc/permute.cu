@@ -339,7 +339,8 @@ __global__ void __launch_bounds__(kThreads)
       // the row's LSE is read before the products, so its load overlaps theirs
       const long long hrow = (long long)(d * B + b) * hp + j;
       const long long idx = hrow * Cs + crow, widx = hrow * Ld + crow;
-      const bool writer = live && c == 0 && in_range(status, idx, 1, rows_n) && in_range(status, widx, 1, ws_rows_n);
+      const bool writer =
+          live && c == 0 && in_range(status, idx, 1, rows_n) && in_range(status, widx, 1, ws_rows_n);
       const float row_lse = writer ? __ldg(lse + idx) : 0.f;
       if (live && in_range(status, seq_off, 8, act_n) && in_range(status, head_row + c * 8, 8, act_n)) {
         const uint4 x = __ldg(reinterpret_cast<const uint4 *>(dout + seq_off));
@@ -469,12 +470,16 @@ static cudaError_t launch_perm(const ulysses_problem &p, const PermParams &pp, c
     if (u < min_units) min_units = u;
   }
   PermParams pr = pp;
-  pr.nrow = min_units >= kThreads ? 1 : (kThreads / min_units < kMaxRowsPerPass ? kThreads / min_units : kMaxRowsPerPass);
+  const int fill = kThreads / min_units;
+  pr.nrow = fill < 1 ? 1 : (fill > kMaxRowsPerPass ? kMaxRowsPerPass : fill);
   const long long passes = (rows + pr.nrow - 1) / pr.nrow;
-  if (p.dtype == ULYSSES_BF16)
-    permute_kernel<__nv_bfloat16><<<grid_for(permute_kernel<__nv_bfloat16>, kThreads, passes), kThreads, 0, st>>>(pr);
-  else
-    permute_kernel<float><<<grid_for(permute_kernel<float>, kThreads, passes), kThreads, 0, st>>>(pr);
+  if (p.dtype == ULYSSES_BF16) {
+    const int grid = grid_for(permute_kernel<__nv_bfloat16>, kThreads, passes);
+    permute_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(pr);
+  } else {
+    const int grid = grid_for(permute_kernel<float>, kThreads, passes);
+    permute_kernel<float><<<grid, kThreads, 0, st>>>(pr);
+  }
   return cudaGetLastError();
 }
 
@@ -607,11 +612,11 @@ cudaError_t launch_kv_reduce(const ulysses_problem &p, const float *dk_part, con
     sn = cs + (size_t)p.S * (p.head_dim / 2);
   }
   const long long n = (long long)p.B * p.S * p.n_kv_head * (p.head_dim / 8);
-  kv_reduce_kernel<<<grid_for(kv_reduce_kernel, 256, n / 256 + 1), 256, 0, st>>>(dk_part, dv_part, static_cast<__nv_bfloat16 *>(dk_seq),
-                                                          static_cast<__nv_bfloat16 *>(dv_seq), p.P, p.B,
-                                                          p.S / p.P, p.n_kv_head, p.head_dim, group_ranks(p), scale,
-                                                          cs, sn,
-                                                          const_cast<uint32_t *>(static_cast<const uint32_t *>(ws)));
+  const int grid = grid_for(kv_reduce_kernel, 256, n / 256 + 1);
+  kv_reduce_kernel<<<grid, 256, 0, st>>>(dk_part, dv_part, static_cast<__nv_bfloat16 *>(dk_seq),
+                                         static_cast<__nv_bfloat16 *>(dv_seq), p.P, p.B, p.S / p.P, p.n_kv_head,
+                                         p.head_dim, group_ranks(p), scale, cs, sn,
+                                         const_cast<uint32_t *>(static_cast<const uint32_t *>(ws)));
   return cudaGetLastError();
 }
 
